@@ -1,0 +1,245 @@
+/*
+ * nvfp4moe -- NVFP4 W4A4 mixture-of-experts expert block for GB300 (sm_103a).
+ *
+ * C ABI.  Every entry point takes plain pointers and sizes; no PyTorch type appears.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device pointers; the caller owns all memory.
+ *     The library never allocates or frees memory: scratch space comes from the
+ *     caller's `workspace` (size from the matching *_workspace_size call).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, passed as void*; NULL is the
+ *     legacy default stream) and return after the kernels are enqueued.
+ *   - Arguments that can be checked on the host (sizes, alignment, workspace size) are
+ *     checked before anything is enqueued; a failed check returns an error code and
+ *     enqueues nothing.
+ *   - Errors found on the device (an expert id out of range, a device-side wait that
+ *     ran out of time) are recorded in a per-device status word; nvfp4_status_check()
+ *     synchronises the stream, returns and clears it.  No kernel traps.
+ *   - Inputs are finite; NaN or Inf inputs give unspecified (but memory-safe) results.
+ *   - Results are deterministic, and a token's output bits do not depend on the other
+ *     tokens of the batch (per-token activation scales, a fixed accumulation order,
+ *     no split-K, no atomics on data).
+ *
+ * Format (pages: "The 4-bitter Lesson: Balancing Stability and Performance in NVFP4
+ * RL", §Baseline): NVFP4 = 4-bit E2M1 values, one E4M3 scale per 16 consecutive
+ * values along the contraction (last) dimension, one FP32 global scale per scope.
+ * Storage used by this library:
+ *   codes:  uint8 [rows, cols/2], two codes per byte, element 2i in the low nibble.
+ *   scales: E4M3 bytes in the 128x4 tiled layout consumed by Blackwell block-scaled
+ *           MMAs: tile (r/128, c/4) at byte ((r/128)*ceil(C/4) + c/4)*512, and inside a
+ *           tile (r%32)*16 + ((r%128)/32)*4 + c%4, where C = cols/16 and rows are
+ *           padded to a multiple of 128 (size nvfp4_sf_bytes(rows, cols)).
+ *   global scale g (decode direction): DQ(x) = value(code) * decode(sf) * g.
+ * Scale arithmetic, every step one float32 operation rounded to nearest even:
+ *   g = amax/2688; sf = E4M3_rn_satfinite(amax_block / (6*g)); s = decode(sf)*g;
+ *   code = E2M1(x * (1/s)), zero magnitudes encoded as +0.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,   /* null pointer, bad size or misaligned pointer */
+  NVFP4_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement */
+  NVFP4_ERR_WORKSPACE = 3,     /* workspace too small */
+  NVFP4_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  NVFP4_ERR_DEVICE_STATUS = 5, /* a kernel recorded bad input (e.g. expert id out of range) */
+  NVFP4_ERR_TIMEOUT = 6        /* a device-side wait ran out of time */
+} nvfp4_status;
+
+typedef enum {
+  NVFP4_SCALE_PER_TENSOR = 0,  /* one g for the whole tensor (weights, standalone tensors) */
+  NVFP4_SCALE_PER_ROW = 1,     /* one g per row (per token: activations) */
+  NVFP4_SCALE_PER_GROUP = 2    /* one g per `group_rows` consecutive rows (stacked experts) */
+} nvfp4_scale_mode;
+
+typedef enum {
+  NVFP4_ROUND_RNE = 0,         /* round to nearest, ties to even */
+  NVFP4_ROUND_STOCHASTIC = 1   /* Philox4x32-10 driven stochastic rounding of the codes */
+} nvfp4_rounding;
+
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 } nvfp4_out_dtype;
+
+/* Prepared (quantised) expert weights.  Caller-allocated device buffers, sizes from
+ * moe_weights_sizes().  W13 rows are stored with gate and up interleaved in chunks of
+ * 64 rows ([gate 0..63, up 0..63, gate 64..127, up 64..127, ...]) so that one 128-column
+ * output tile holds matching gate and up columns; W2's contraction dimension is
+ * zero-padded to Ip = round_up(I, 256). */
+typedef struct {
+  int32_t E;          /* experts */
+  int64_t H;          /* hidden size (gate/up contraction, down output) */
+  int64_t I;          /* intermediate size */
+  uint8_t* w13_codes; /* device [E, 2I, H/2] */
+  uint8_t* w13_sf;    /* device, tiled layout over E*2I rows, H/16 scale columns */
+  float* w13_g;       /* device [E] */
+  uint8_t* w2_codes;  /* device [E, H, Ip/2] */
+  uint8_t* w2_sf;     /* device, tiled layout over E*H rows, Ip/16 scale columns */
+  float* w2_g;        /* device [E] */
+} nvfp4_moe_weights;
+
+/* ---------------------------------------------------------------- sizes / status */
+
+/* Bytes of the tiled scale-factor buffer for a rows x cols NVFP4 tensor. */
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
+
+/* Byte sizes of the six nvfp4_moe_weights buffers, in struct order
+ * (w13_codes, w13_sf, w13_g, w2_codes, w2_sf, w2_g). */
+nvfp4_status moe_weights_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[6]);
+
+/* Workspace bytes for each entry point (0 when none is needed).  `op` is one of: */
+enum {
+  NVFP4_OP_QUANTIZE = 0,        /* args: rows, cols (others 0) */
+  NVFP4_OP_PREPARE_WEIGHTS = 1, /* args: E, H, I */
+  NVFP4_OP_MOE_FORWARD = 2,     /* args: T, k, E, H, I */
+  NVFP4_OP_MOE_PERMUTE = 3      /* args: T, k, E */
+};
+size_t nvfp4_workspace_size(int op, int64_t T_or_rows, int64_t k_or_cols, int64_t E,
+                            int64_t H, int64_t I);
+
+/* Synchronises `stream`, then returns and clears the device status word of the
+ * current device: NVFP4_OK, NVFP4_ERR_DEVICE_STATUS or NVFP4_ERR_TIMEOUT. */
+nvfp4_status nvfp4_status_check(void* stream);
+
+const char* nvfp4_status_string(nvfp4_status s);
+
+/* ---------------------------------------------------------------- quantiser */
+
+/* NVFP4 quantisation of a BF16 matrix ("The 4-bitter Lesson...", §Baseline for the
+ * format; §"Why is the NVFP4 pretraining recipe not sufficient for RL?" for the
+ * per-tensor weight scale, the per-token activation scale and stochastic rounding).
+ *   x:            device BF16 [rows, ld_elems], the first `cols` of each row are used.
+ *   rows, cols:   cols % 16 == 0, 16 <= cols <= 8192; ld_elems >= cols, ld_elems % 8 == 0.
+ *   mode:         per tensor / per row / per group of `group_rows` rows.
+ *   rounding:     RNE, or stochastic with (seed, rng_offset): element with row-major
+ *                 index i uses 16 bits of Philox4x32-10 block rng_offset + i/8, key=seed.
+ *   global_scale_in:  device, nullable.  When given, g is read from it (1, rows or
+ *                 rows/group_rows floats) instead of being computed from amax.
+ *   global_scale_out: device float [1 | rows | rows/group_rows], receives g.
+ *   codes_out:    device uint8 [rows, cols/2] (16-byte aligned).
+ *   sf_out:       device uint8 [nvfp4_sf_bytes(rows, cols)], tiled layout; padding
+ *                 rows/columns of the tile grid are written as 0.
+ *   workspace:    device, nvfp4_workspace_size(NVFP4_OP_QUANTIZE, rows, cols, ...) bytes
+ *                 (holds the amax of each scope for the per-tensor / per-group modes).
+ */
+nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_elems,
+                            nvfp4_scale_mode mode, int64_t group_rows, nvfp4_rounding rounding,
+                            uint64_t seed, uint64_t rng_offset, const float* global_scale_in,
+                            float* global_scale_out, uint8_t* codes_out, uint8_t* sf_out,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- grouped GEMM */
+
+/* W4A4 grouped GEMM over ragged expert groups ("Low-Bit Precision Training Is Ready
+ * for Production...", §"What W4A4 GEMM Actually Changes": both operands in 4 bits so
+ * the GEMM runs on FP4 tensor cores; "miniTE identifies and closes the execution gap
+ * ...", §Development: grouped GEMMs).  For every expert e and every row r of its group
+ * (rows group_offsets[e] .. group_offsets[e] + group_rows[e] - 1):
+ *     D[r, n] = (gA[r] * gB[e]) * sum_k DQ'(A)[r, k] * DQ'(B_e)[n, k]
+ * where DQ' = value(code) * decode(sf), accumulated in FP32 on the tensor cores in a
+ * fixed order (no split-K), then rounded once to the output type.
+ *   A, SFA, gA:   device, codes [M_total, K/2], tiled scales for M_total rows, [M_total].
+ *   B, SFB, gB:   device, codes [E, N, K/2], tiled scales for E*N rows, [E].
+ *   group_offsets: device int32 [E+1], multiples of 128, non-decreasing,
+ *                 group_offsets[E] <= M_total.  group_rows: device int32 [E],
+ *                 group_rows[e] <= group_offsets[e+1] - group_offsets[e].
+ *   M_total:      rows allocated for A (a multiple of 128).
+ *   N % 128 == 0, K % 256 == 0, E <= 1024.
+ *   D:            device, [M_total, ldd] of out_dtype; rows outside every group are not
+ *                 written.  ldd % 8 == 0.
+ * A, SFA, B, SFB and D must be 16-byte aligned; gA, gB and the group arrays 4-byte
+ * aligned.  No workspace.
+ */
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const float* gA,
+                                const uint8_t* B, const uint8_t* SFB, const float* gB,
+                                const int32_t* group_offsets, const int32_t* group_rows,
+                                int64_t M_total, int64_t N, int64_t K, int32_t E, void* D,
+                                nvfp4_out_dtype out_dtype, int64_t ldd, void* stream);
+
+/* ---------------------------------------------------------------- MoE helpers */
+
+/* Top-k routing of router logits.  ids[t, :] = the k experts with the largest logits,
+ * in descending order, ties to the lower expert id; weights = softmax over the chosen k
+ * (renormalize != 0) or the full-softmax probabilities of the chosen experts.
+ *   logits: device float [T, E]; ids: device int32 [T, k]; weights: device float [T, k].
+ *   1 <= k <= 32, k <= E <= 1024. */
+nvfp4_status moe_route_topk(const float* logits, int64_t T, int32_t E, int32_t k,
+                            int renormalize, int32_t* ids, float* weights, void* stream);
+
+/* Expert grouping of the T*k (token, j) entries: counts [E], offsets [E+1] (exclusive
+ * scan of counts), padded_offsets [E+1] (each group starts at a multiple of 128),
+ * inv [T, k] = slot of (t, j), perm [M_cap] = token of each slot, -1 for padding slots
+ * below padded_offsets[E] (entries beyond it are not written).  Slots are ordered by
+ * expert, then by token.  M_cap = round_up(T*k + E*127, 128) bounds padded_offsets[E].
+ * Ids outside [0, E) set NVFP4_ERR_DEVICE_STATUS and are counted nowhere. */
+nvfp4_status moe_permute(const int32_t* ids, int64_t T, int32_t k, int32_t E,
+                         int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                         int32_t* inv, int32_t* perm, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Router-weighted un-permute: out[t] = BF16( sum_{j=0..k-1} w[t, j] * y[inv[t, j]] ),
+ * each product and each partial sum a float32 operation, in the order j = 0..k-1.
+ *   y: device BF16 [*, H]; inv: device int32 [T, k]; w: device float [T, k];
+ *   out: device BF16 [T, H].  H % 8 == 0. */
+nvfp4_status moe_combine(const void* y, const int32_t* inv, const float* w, int64_t T,
+                         int32_t k, int64_t H, void* out, void* stream);
+
+/* SwiGLU of the interleaved gate/up output followed by per-row NVFP4 requantisation.
+ * For each row r with perm[r] >= 0 and each c < I:
+ *     h[r, c] = BF16( silu(gate) * up )   (the nearest BF16 to the exact value)
+ * where gate/up are D's columns in the 64-chunk interleave of nvfp4_moe_weights; then
+ * h's row is quantised with a per-row scale into hq [rows, Ip/2] (zero-padded to
+ * Ip = round_up(I, 256)), tiled scales (Ip/16 columns) and gh [rows].
+ *   d: device BF16 [rows, 2I]; h_out: device BF16 [rows, I] or NULL. */
+nvfp4_status moe_swiglu_quantize(const void* d, const int32_t* perm, int64_t rows, int64_t I,
+                                 void* h_out, uint8_t* hq, uint8_t* hsf, float* gh,
+                                 void* stream);
+
+/* Quantise the expert weights once per weight update ("The 4-bitter Lesson...",
+ * §"Why is the NVFP4 pretraining recipe not sufficient for RL?": weights use per-block
+ * E4M3 scales and one FP32 global scale; each expert matrix is its own tensor).
+ *   w13: device BF16 [E, 2I, H] (gate rows 0..I-1, up rows I..2I-1);
+ *   w2:  device BF16 [E, H, I].  H % 256 == 0, I % 64 == 0.
+ *   out: struct of caller-allocated buffers (moe_weights_sizes). */
+nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int64_t H,
+                                 int64_t I, const nvfp4_moe_weights* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* The expert block forward ("Low-Bit Precision Training Is Ready for Production...",
+ * §"What W4A4 GEMM Actually Changes": W4A4 on the expert layers; "The 4-bitter
+ * Lesson...", per-token activation scales, fused per-token quantiser):
+ *   permute -> per-token NVFP4 of x written to every routed slot -> gate/up grouped GEMM
+ *   (BF16) -> SwiGLU + per-row requantisation -> down grouped GEMM (BF16) -> weighted
+ *   combine (BF16).
+ *   x: device BF16 [T, H] and out: device BF16 [T, H], 16-byte aligned;
+ *   ids: device int32 [T, k] and w: device float [T, k], 4-byte aligned;
+ *   weights: prepared weights (16-byte aligned buffers).
+ *   workspace: nvfp4_workspace_size(NVFP4_OP_MOE_FORWARD, T, k, E, H, I) bytes; its
+ *   layout (for inspection) is given by moe_forward_workspace_layout().
+ *   1 <= k <= 32, T*k < 2^31. */
+nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* w, int64_t T,
+                                int32_t k, const nvfp4_moe_weights* weights, void* out,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Byte offsets of the forward's intermediates inside its workspace, in this order:
+ * [0] counts int32[E], [1] offsets int32[E+1], [2] padded_offsets int32[E+1],
+ * [3] inv int32[T*k], [4] perm int32[M_cap], [5] Aq codes [M_cap, H/2],
+ * [6] Aq scales (tiled, M_cap rows, H/16 cols), [7] gA float[M_cap],
+ * [8] D BF16 [M_cap, 2I] (interleaved gate/up), [9] hq codes [M_cap, Ip/2],
+ * [10] hq scales (tiled, M_cap rows, Ip/16 cols), [11] gh float[M_cap],
+ * [12] y BF16 [M_cap, H], [13] M_cap (a row count, not an offset),
+ * [14] total bytes.  Only rows below padded_offsets[E] are meaningful. */
+nvfp4_status moe_forward_workspace_layout(int64_t T, int32_t k, int32_t E, int64_t H,
+                                          int64_t I, int64_t layout_out[15]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,296 @@
+"""NVFP4 W4A4 mixture-of-experts expert block for GB300 (sm_103a).
+
+Python binding of the C ABI in ``include/nvfp4moe.h``: every function here marshals
+torch tensors into raw device pointers, sizes and the current CUDA stream, and calls the
+CUDA library ``_build/libnvfp4moe.so`` (built in-tree by ``build.py``).  PyTorch supplies
+device memory and streams only; every step of the path runs in the library's kernels.
+There is no fallback: if the library cannot be loaded, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "load", "library_path", "Status", "NVFP4Error",
+    "nvfp4_quantize", "nvfp4_grouped_gemm", "moe_route_topk", "moe_permute", "moe_combine",
+    "moe_swiglu_quantize", "moe_prepare_weights", "moe_expert_forward", "moe_forward_workspace",
+    "moe_forward_workspace_layout", "nvfp4_status_check", "nvfp4_sf_bytes", "NVFP4MoEWeights",
+    "SCALE_PER_TENSOR", "SCALE_PER_ROW", "SCALE_PER_GROUP", "ROUND_RNE", "ROUND_STOCHASTIC",
+]
+
+SCALE_PER_TENSOR, SCALE_PER_ROW, SCALE_PER_GROUP = 0, 1, 2
+ROUND_RNE, ROUND_STOCHASTIC = 0, 1
+OUT_BF16, OUT_F32 = 0, 1
+OP_QUANTIZE, OP_PREPARE_WEIGHTS, OP_MOE_FORWARD, OP_MOE_PERMUTE = 0, 1, 2, 3
+
+_lib = None
+_vp, _i64, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t
+
+
+class Status:
+    OK, INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA, DEVICE_STATUS, TIMEOUT = range(7)
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [("E", _i32), ("H", _i64), ("I", _i64), ("w13_codes", _vp), ("w13_sf", _vp),
+                ("w13_g", _vp), ("w2_codes", _vp), ("w2_sf", _vp), ("w2_g", _vp)]
+
+
+_SIGS = {
+    "nvfp4_sf_bytes": (_sz, [_i64, _i64]),
+    "moe_weights_sizes": (ctypes.c_int, [_i32, _i64, _i64, ctypes.POINTER(_sz)]),
+    "nvfp4_workspace_size": (_sz, [ctypes.c_int, _i64, _i64, _i64, _i64, _i64]),
+    "nvfp4_status_check": (ctypes.c_int, [_vp]),
+    "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "nvfp4_quantize": (ctypes.c_int, [_vp, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int, _u64, _u64,
+                                      _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
+                                          _vp, ctypes.c_int, _i64, _vp]),
+    "moe_route_topk": (ctypes.c_int, [_vp, _i64, _i32, _i32, ctypes.c_int, _vp, _vp, _vp]),
+    "moe_permute": (ctypes.c_int, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _i64, _vp, _vp]),
+    "moe_swiglu_quantize": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "moe_prepare_weights": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i64, ctypes.POINTER(_Weights), _vp, _sz,
+                                           _vp]),
+    "moe_expert_forward": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, ctypes.POINTER(_Weights), _vp, _vp,
+                                          _sz, _vp]),
+    "moe_forward_workspace_layout": (ctypes.c_int, [_i64, _i32, _i32, _i64, _i64, ctypes.POINTER(_i64)]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def header_functions() -> list:
+    """Names of the functions declared in include/nvfp4moe.h."""
+    src = open(os.path.join(_build.INCLUDE, "nvfp4moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z][a-z0-9_]*)\s*\(", src)) - {"if", "sizeof"})
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().nvfp4_status_string(code).decode()
+    except Exception:  # noqa: BLE001 - only used for messages
+        return "unknown"
+
+
+def _check(code: int, what: str):
+    if code != Status.OK:
+        raise NVFP4Error(code, what)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t):
+    if not t.is_cuda:
+        raise ValueError("tensors must be on a CUDA device")
+    return t.device
+
+
+def nvfp4_sf_bytes(rows: int, cols: int) -> int:
+    return int(load().nvfp4_sf_bytes(rows, cols))
+
+
+def nvfp4_status_check(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status word."""
+    return int(load().nvfp4_status_check(_stream(stream)))
+
+
+# --------------------------------------------------------------------------- quantiser
+
+def nvfp4_quantize(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, rounding: int = ROUND_RNE, seed: int = 0,
+                   rng_offset: int = 0, group_rows: int = 0, global_scale: torch.Tensor | None = None,
+                   out=None, workspace: torch.Tensor | None = None, stream=None):
+    """NVFP4 of a BF16 matrix [rows, cols].  Returns (codes [rows, cols/2] uint8,
+    tiled scales uint8 [nvfp4_sf_bytes], g float32 [1 | rows | rows/group_rows])."""
+    lib = load()
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    dev = _dev(x)
+    n_g = 1 if mode == SCALE_PER_TENSOR else (rows if mode == SCALE_PER_ROW else rows // max(group_rows, 1))
+    if out is None:
+        codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
+        sf = torch.empty(max(nvfp4_sf_bytes(rows, cols), 16), dtype=torch.uint8, device=dev)
+        g = torch.empty(max(n_g, 1), dtype=torch.float32, device=dev)
+    else:
+        codes, sf, g = out
+    ws_bytes = int(lib.nvfp4_workspace_size(OP_QUANTIZE, rows, cols, 0, 0, 0))
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _check(lib.nvfp4_quantize(_p(x), rows, cols, x.stride(0), mode, group_rows, rounding, seed, rng_offset,
+                              _p(global_scale), _p(g), _p(codes), _p(sf), _p(workspace), workspace.numel(),
+                              _stream(stream)), "nvfp4_quantize")
+    return codes, sf, g
+
+
+# --------------------------------------------------------------------------- GEMM
+
+def nvfp4_grouped_gemm(A, SFA, gA, B, SFB, gB, group_offsets, group_rows, N: int, K: int, E: int,
+                       out_dtype=torch.bfloat16, out: torch.Tensor | None = None, stream=None):
+    """D[M_total, N] = grouped W4A4 GEMM (rows outside the groups are left unwritten)."""
+    lib = load()
+    M_total = A.shape[0]
+    if out is None:
+        out = torch.empty(M_total, N, dtype=out_dtype, device=_dev(A))
+    code = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.nvfp4_grouped_gemm(_p(A), _p(SFA), _p(gA), _p(B), _p(SFB), _p(gB), _p(group_offsets),
+                                  _p(group_rows), M_total, N, K, E, _p(out), code, out.stride(0),
+                                  _stream(stream)), "nvfp4_grouped_gemm")
+    return out
+
+
+# --------------------------------------------------------------------------- MoE helpers
+
+def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool = True, stream=None):
+    lib = load()
+    T, E = logits.shape
+    ids = torch.empty(T, k, dtype=torch.int32, device=_dev(logits))
+    w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _check(lib.moe_route_topk(_p(logits.contiguous()), T, E, k, int(renormalize), _p(ids), _p(w),
+                              _stream(stream)), "moe_route_topk")
+    return ids, w
+
+
+def moe_mcap(T: int, k: int, E: int) -> int:
+    return (T * k + E * 127 + 127) // 128 * 128
+
+
+def moe_permute(ids: torch.Tensor, E: int, stream=None):
+    lib = load()
+    T, k = ids.shape
+    dev = _dev(ids)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    padded = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    inv = torch.empty(T, k, dtype=torch.int32, device=dev)
+    perm = torch.full((moe_mcap(T, k, E),), -2, dtype=torch.int32, device=dev)
+    ws = torch.empty(int(lib.nvfp4_workspace_size(OP_MOE_PERMUTE, T, k, E, 0, 0)), dtype=torch.uint8, device=dev)
+    _check(lib.moe_permute(_p(ids.contiguous()), T, k, E, _p(counts), _p(offsets), _p(padded), _p(inv), _p(perm),
+                           _p(ws), ws.numel(), _stream(stream)), "moe_permute")
+    return dict(counts=counts, offsets=offsets, padded_offsets=padded, inv=inv, perm=perm)
+
+
+def moe_combine(y: torch.Tensor, inv: torch.Tensor, w: torch.Tensor, stream=None):
+    lib = load()
+    T, k = inv.shape
+    H = y.shape[1]
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=_dev(y))
+    _check(lib.moe_combine(_p(y), _p(inv.contiguous()), _p(w.contiguous()), T, k, H, _p(out), _stream(stream)),
+           "moe_combine")
+    return out
+
+
+def moe_swiglu_quantize(d: torch.Tensor, perm: torch.Tensor, I: int, want_h: bool = True, stream=None):
+    """h = BF16(silu(gate) * up) over the interleaved gate/up output, then per-row NVFP4."""
+    lib = load()
+    rows = d.shape[0]
+    dev = _dev(d)
+    Ip = (I + 255) // 256 * 256
+    h = torch.empty(rows, I, dtype=torch.bfloat16, device=dev) if want_h else None
+    hq = torch.empty(rows, Ip // 2, dtype=torch.uint8, device=dev)
+    hsf = torch.empty(nvfp4_sf_bytes(rows, Ip), dtype=torch.uint8, device=dev)
+    gh = torch.empty(rows, dtype=torch.float32, device=dev)
+    _check(lib.moe_swiglu_quantize(_p(d), _p(perm), rows, I, _p(h), _p(hq), _p(hsf), _p(gh), _stream(stream)),
+           "moe_swiglu_quantize")
+    return h, hq, hsf, gh
+
+
+class NVFP4MoEWeights:
+    """Quantised expert weights (device tensors) plus the C struct that points at them."""
+
+    def __init__(self, E: int, H: int, I: int, device):
+        lib = load()
+        sizes = (_sz * 6)()
+        _check(lib.moe_weights_sizes(E, H, I, sizes), "moe_weights_sizes")
+        Ip = (I + 255) // 256 * 256
+        self.E, self.H, self.I, self.Ip = E, H, I, Ip
+        self.w13_codes = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
+        self.w13_sf = torch.empty(sizes[1], dtype=torch.uint8, device=device)
+        self.w13_g = torch.empty(E, dtype=torch.float32, device=device)
+        self.w2_codes = torch.empty(E, H, Ip // 2, dtype=torch.uint8, device=device)
+        self.w2_sf = torch.empty(sizes[4], dtype=torch.uint8, device=device)
+        self.w2_g = torch.empty(E, dtype=torch.float32, device=device)
+        assert self.w13_codes.numel() == sizes[0] and self.w2_codes.numel() == sizes[3]
+        self.struct = _Weights(E, H, I, self.w13_codes.data_ptr(), self.w13_sf.data_ptr(), self.w13_g.data_ptr(),
+                               self.w2_codes.data_ptr(), self.w2_sf.data_ptr(), self.w2_g.data_ptr())
+
+
+def moe_prepare_weights(w13: torch.Tensor, w2: torch.Tensor, stream=None) -> NVFP4MoEWeights:
+    """Quantise W13 [E, 2I, H] (gate rows then up rows) and W2 [E, H, I], BF16."""
+    lib = load()
+    E, N13, H = w13.shape
+    I = N13 // 2
+    assert w2.shape == (E, H, I)
+    pw = NVFP4MoEWeights(E, H, I, _dev(w13))
+    ws = torch.empty(int(lib.nvfp4_workspace_size(OP_PREPARE_WEIGHTS, E, 0, 0, 0, 0)), dtype=torch.uint8,
+                     device=w13.device)
+    _check(lib.moe_prepare_weights(_p(w13.contiguous()), _p(w2.contiguous()), E, H, I, ctypes.byref(pw.struct),
+                                   _p(ws), ws.numel(), _stream(stream)), "moe_prepare_weights")
+    pw._ws = ws
+    return pw
+
+
+def moe_forward_workspace_layout(T: int, k: int, E: int, H: int, I: int) -> list:
+    lib = load()
+    out = (_i64 * 15)()
+    _check(lib.moe_forward_workspace_layout(T, k, E, H, I, out), "moe_forward_workspace_layout")
+    return list(out)
+
+
+def moe_forward_workspace(T: int, k: int, weights: NVFP4MoEWeights, device) -> torch.Tensor:
+    lib = load()
+    n = int(lib.nvfp4_workspace_size(OP_MOE_FORWARD, T, k, weights.E, weights.H, weights.I))
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_expert_forward(x: torch.Tensor, ids: torch.Tensor, w: torch.Tensor, weights: NVFP4MoEWeights,
+                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """out[T, H] BF16 = the NVFP4 W4A4 expert block over routed tokens."""
+    lib = load()
+    T, H = x.shape
+    k = ids.shape[1]
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=_dev(x))
+    if workspace is None:
+        workspace = moe_forward_workspace(T, k, weights, x.device)
+    _check(lib.moe_expert_forward(_p(x), _p(ids), _p(w), T, k, ctypes.byref(weights.struct), _p(out),
+                                  _p(workspace), workspace.numel(), _stream(stream)), "moe_expert_forward")
+    return out

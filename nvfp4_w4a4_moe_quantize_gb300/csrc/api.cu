@@ -1,0 +1,457 @@
+// C ABI of the NVFP4 W4A4 MoE library: argument checks, workspace layouts, TMA tensor
+// maps and the order of the kernels.  Every entry point only enqueues work on the
+// caller's stream; nothing here allocates device memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "nvfp4moe.h"
+#include "launch.h"
+#include "status.cuh"
+
+namespace nvfp4 {
+
+__device__ int g_device_status;   // first error recorded by any kernel of this library
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+int* g_status_ptr[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d < 0 || d >= kMaxDevices ? 0 : d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+inline size_t align256(size_t a) { return (a + 255) & ~size_t(255); }
+
+nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+// 2-D map over a [rows, row_bytes] byte matrix, box = 128 bytes x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, uint32_t box_rows) {
+  auto enc = encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct ForwardLayout {
+  int64_t off[15];
+};
+
+// hist | counts | offsets | padded | inv | perm | Aq | SFA | gA | D | hq | SFH | gH | y
+ForwardLayout forward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t I, size_t* hist_off,
+                             size_t* hist_bytes) {
+  ForwardLayout L;
+  const int64_t Ip = round_up(I, 256);
+  const int64_t mcap = round_up(T * k + E * 127, 128);
+  const int64_t nchunks = permute_chunks(T * k);
+  size_t p = 0;
+  *hist_off = p;
+  *hist_bytes = align256(sizeof(int32_t) * (size_t)(E * (nchunks > 0 ? nchunks : 1)));
+  p += *hist_bytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = p;
+    p += align256(bytes);
+    return (int64_t)o;
+  };
+  L.off[0] = take(4 * E);
+  L.off[1] = take(4 * (E + 1));
+  L.off[2] = take(4 * (E + 1));
+  L.off[3] = take(4 * T * k);
+  L.off[4] = take(4 * mcap);
+  L.off[5] = take((size_t)mcap * (H / 2));
+  L.off[6] = take(nvfp4_sf_bytes(mcap, H));
+  L.off[7] = take(4 * mcap);
+  L.off[8] = take((size_t)mcap * 2 * I * 2);
+  L.off[9] = take((size_t)mcap * (Ip / 2));
+  L.off[10] = take(nvfp4_sf_bytes(mcap, Ip));
+  L.off[11] = take(4 * mcap);
+  L.off[12] = take((size_t)mcap * H * 2);
+  L.off[13] = mcap;
+  L.off[14] = (int64_t)p;
+  return L;
+}
+
+nvfp4_status gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const uint8_t* B, const uint8_t* SFB,
+                  const float* gB, const int32_t* offsets, const int32_t* rows, int64_t M_total, int64_t N, int64_t K,
+                  int32_t E, void* D, int out_f32, int64_t ldd, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M_total, K / 2, 128) || !make_map(&mb, B, (int64_t)E * N, K / 2, 128))
+    return NVFP4_ERR_CUDA;
+  GemmArgs g;
+  g.sfa = SFA;
+  g.sfb = SFB;
+  g.ga = gA;
+  g.gb = gB;
+  g.offsets = offsets;
+  g.rows = rows;
+  g.E = E;
+  g.N = (int32_t)N;
+  g.K = (int32_t)K;
+  g.d = D;
+  g.ldd = ldd;
+  g.out_f32 = out_f32;
+  g.status = device_status_ptr();
+  return from_cuda(launch_grouped_gemm(ma, mb, g, M_total / 128, s));
+}
+
+}  // namespace
+
+int num_sms() {
+  const int d = current_device();
+  if (g_sms[d] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = v > 0 ? v : 1;
+  }
+  return g_sms[d];
+}
+
+int* device_status_ptr() {
+  const int d = current_device();
+  if (g_status_ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) g_status_ptr[d] = static_cast<int*>(p);
+  }
+  return g_status_ptr[d];
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return (size_t)((rows + 127) / 128) * (size_t)((cols + 63) / 64) * 512u;
+}
+
+nvfp4_status moe_weights_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[6]) {
+  if (E <= 0 || H <= 0 || I <= 0 || sizes_out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  const int64_t Ip = round_up(I, 256);
+  sizes_out[0] = (size_t)E * 2 * I * (H / 2);
+  sizes_out[1] = nvfp4_sf_bytes((int64_t)E * 2 * I, H);
+  sizes_out[2] = 4u * (size_t)E;
+  sizes_out[3] = (size_t)E * H * (Ip / 2);
+  sizes_out[4] = nvfp4_sf_bytes((int64_t)E * H, Ip);
+  sizes_out[5] = 4u * (size_t)E;
+  return NVFP4_OK;
+}
+
+size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t E, int64_t H, int64_t I) {
+  switch (op) {
+    case NVFP4_OP_QUANTIZE:
+      return align256(4u * (size_t)(a > 1 ? a : 1));
+    case NVFP4_OP_PREPARE_WEIGHTS:
+      return align256(8u * (size_t)(a > 1 ? a : 1));
+    case NVFP4_OP_MOE_FORWARD: {
+      size_t ho, hb;
+      return (size_t)forward_layout(a, b, E, H, I, &ho, &hb).off[14];
+    }
+    case NVFP4_OP_MOE_PERMUTE: {
+      const int64_t n = permute_chunks(a * b);
+      return align256(4u * (size_t)(E * (n > 0 ? n : 1)));
+    }
+    default:
+      return 0;
+  }
+}
+
+nvfp4_status moe_forward_workspace_layout(int64_t T, int32_t k, int32_t E, int64_t H, int64_t I,
+                                          int64_t layout_out[15]) {
+  if (T < 0 || k <= 0 || E <= 0 || H <= 0 || I <= 0 || layout_out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  size_t ho, hb;
+  const ForwardLayout L = forward_layout(T, k, E, H, I, &ho, &hb);
+  std::memcpy(layout_out, L.off, sizeof(L.off));
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_status_check(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
+  if (v == kStatusTimeout) return NVFP4_ERR_TIMEOUT;
+  if (v != 0) return NVFP4_ERR_DEVICE_STATUS;
+  return NVFP4_OK;
+}
+
+const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_UNSUPPORTED: return "unsupported shape";
+    case NVFP4_ERR_WORKSPACE: return "workspace too small";
+    case NVFP4_ERR_CUDA: return "CUDA error";
+    case NVFP4_ERR_DEVICE_STATUS: return "device reported invalid input";
+    case NVFP4_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, nvfp4_scale_mode mode,
+                            int64_t group_rows, nvfp4_rounding rounding, uint64_t seed, uint64_t rng_offset,
+                            const float* g_in, float* g_out, uint8_t* codes, uint8_t* sf, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0 || ld < cols || ld % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (cols > 8192) return NVFP4_ERR_UNSUPPORTED;
+  if (mode < NVFP4_SCALE_PER_TENSOR || mode > NVFP4_SCALE_PER_GROUP) return NVFP4_ERR_INVALID_ARG;
+  if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_STOCHASTIC) return NVFP4_ERR_INVALID_ARG;
+  if (mode == NVFP4_SCALE_PER_GROUP && (group_rows <= 0 || rows % group_rows != 0)) return NVFP4_ERR_INVALID_ARG;
+  if (rows == 0) return NVFP4_OK;
+  if (!x || !codes || !sf || !aligned16(x) || !aligned16(codes) || !aligned16(sf)) return NVFP4_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t n_scopes = mode == NVFP4_SCALE_PER_TENSOR ? 1 : (mode == NVFP4_SCALE_PER_GROUP ? rows / group_rows : rows);
+  uint32_t* amax = nullptr;
+  if (mode != NVFP4_SCALE_PER_ROW && g_in == nullptr) {
+    if (ws == nullptr || ws_bytes < 4u * (size_t)n_scopes || !aligned16(ws)) return NVFP4_ERR_WORKSPACE;
+    amax = static_cast<uint32_t*>(ws);
+    cudaError_t e = launch_amax(x, rows, cols, ld, mode == NVFP4_SCALE_PER_GROUP ? group_rows : 0, amax, n_scopes, s);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
+  QuantArgs a{};
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.rows = rows;
+  a.cols = cols;
+  a.ld = ld;
+  a.mode = mode;
+  a.group_rows = group_rows;
+  a.g_in = g_in;
+  a.amax_bits = amax;
+  a.g_out = g_out;
+  a.codes = codes;
+  a.codes_ld = cols / 2;
+  a.sf = sf;
+  a.sf_words = (cols + 63) / 64;
+  a.cols_pad = cols;
+  a.rows_total = round_up(rows, 128);
+  a.map = kMapIdentity;
+  a.seed = seed;
+  a.rng_offset = rng_offset;
+  a.status = device_status_ptr();
+  return from_cuda(launch_quantize_rows(a, rounding, s));
+}
+
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const uint8_t* B,
+                                const uint8_t* SFB, const float* gB, const int32_t* group_offsets,
+                                const int32_t* group_rows, int64_t M_total, int64_t N, int64_t K, int32_t E,
+                                void* D, nvfp4_out_dtype out_dtype, int64_t ldd, void* stream) {
+  if (E <= 0 || E > 1024 || N <= 0 || K <= 0 || M_total < 0 || M_total % 128 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((int64_t)E * N >= (int64_t)1 << 31 || M_total >= (int64_t)1 << 31 || K >= (int64_t)1 << 20)
+    return NVFP4_ERR_UNSUPPORTED;
+  if (ldd < N || ldd % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_INVALID_ARG;
+  if (M_total == 0) return NVFP4_OK;
+  const void* ptrs[] = {A, SFA, B, SFB, D};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned4(gA) || !aligned4(gB) || !aligned4(group_offsets) || !aligned4(group_rows))
+    return NVFP4_ERR_INVALID_ARG;
+  return gemm(A, SFA, gA, B, SFB, gB, group_offsets, group_rows, M_total, N, K, E, D,
+              out_dtype == NVFP4_OUT_F32, ldd, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status moe_route_topk(const float* logits, int64_t T, int32_t E, int32_t k, int renormalize, int32_t* ids,
+                            float* weights, void* stream) {
+  if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > 32 || k > E) return NVFP4_ERR_INVALID_ARG;
+  if (T == 0) return NVFP4_OK;
+  if (!logits || !ids || !weights) return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_route_topk(logits, T, E, k, renormalize, ids, weights, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_permute(const int32_t* ids, int64_t T, int32_t k, int32_t E, int32_t* counts, int32_t* offsets,
+                         int32_t* padded_offsets, int32_t* inv, int32_t* perm, void* ws, size_t ws_bytes,
+                         void* stream) {
+  if (T < 0 || k <= 0 || k > 32 || E <= 0 || E > 1024 || T * k >= ((int64_t)1 << 31) - (int64_t)E * 128)
+    return NVFP4_ERR_INVALID_ARG;
+  if (!counts || !offsets || !padded_offsets || (T > 0 && (!ids || !inv))) return NVFP4_ERR_INVALID_ARG;
+  const size_t need = nvfp4_workspace_size(NVFP4_OP_MOE_PERMUTE, T, k, E, 0, 0);
+  if (ws == nullptr || ws_bytes < need) return NVFP4_ERR_WORKSPACE;
+  return from_cuda(launch_permute(ids, T, k, E, counts, offsets, padded_offsets, inv, perm,
+                                  static_cast<int32_t*>(ws), permute_chunks(T * k), device_status_ptr(),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_combine(const void* y, const int32_t* inv, const float* w, int64_t T, int32_t k, int64_t H,
+                         void* out, void* stream) {
+  if (T < 0 || k <= 0 || k > 32 || H <= 0 || H % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (T == 0) return NVFP4_OK;
+  if (!y || !inv || !w || !out || !aligned16(y) || !aligned16(out)) return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_combine(y, inv, w, T, k, H, out, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_swiglu_quantize(const void* d, const int32_t* perm, int64_t rows, int64_t I, void* h_out,
+                                 uint8_t* hq, uint8_t* hsf, float* gh, void* stream) {
+  if (rows < 0 || I <= 0 || I % 64 != 0 || I > 4096) return NVFP4_ERR_INVALID_ARG;
+  if (rows == 0) return NVFP4_OK;
+  if (!d || !perm || !hq || !hsf || !gh || !aligned16(d) || !aligned16(hq) || !aligned16(hsf))
+    return NVFP4_ERR_INVALID_ARG;
+  if (h_out != nullptr && !aligned16(h_out)) return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_swiglu_quant(d, perm, rows, nullptr, I, round_up(I, 256), h_out, hq, hsf, gh,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int64_t H, int64_t I,
+                                 const nvfp4_moe_weights* out, void* ws, size_t ws_bytes, void* stream) {
+  if (E <= 0 || E > 1024 || H <= 0 || I <= 0 || out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 64 != 0 || H > 8192 || I > 4096) return NVFP4_ERR_UNSUPPORTED;
+  if (out->E != E || out->H != H || out->I != I) return NVFP4_ERR_INVALID_ARG;
+  const void* ptrs[] = {w13, w2, out->w13_codes, out->w13_sf, out->w13_g, out->w2_codes, out->w2_sf, out->w2_g};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < nvfp4_workspace_size(NVFP4_OP_PREPARE_WEIGHTS, E, 0, 0, 0, 0) || !aligned16(ws))
+    return NVFP4_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t Ip = round_up(I, 256);
+  uint32_t* amax = static_cast<uint32_t*>(ws);
+  cudaError_t e = launch_amax(w13, (int64_t)E * 2 * I, H, H, 2 * I, amax, E, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  QuantArgs a{};
+  a.x = static_cast<const __nv_bfloat16*>(w13);
+  a.rows = (int64_t)E * 2 * I;
+  a.cols = H;
+  a.ld = H;
+  a.mode = kScopeGroup;
+  a.group_rows = 2 * I;
+  a.amax_bits = amax;
+  a.g_out = out->w13_g;
+  a.codes = out->w13_codes;
+  a.codes_ld = H / 2;
+  a.sf = out->w13_sf;
+  a.sf_words = H / 64;
+  a.cols_pad = H;
+  a.rows_total = a.rows;
+  a.map = kMapInterleave;
+  a.map_I = I;
+  a.status = device_status_ptr();
+  e = launch_quantize_rows(a, kRoundRNE, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  uint32_t* amax2 = amax + E;
+  e = launch_amax(w2, (int64_t)E * H, I, I, H, amax2, E, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  QuantArgs b{};
+  b.x = static_cast<const __nv_bfloat16*>(w2);
+  b.rows = (int64_t)E * H;
+  b.cols = I;
+  b.ld = I;
+  b.mode = kScopeGroup;
+  b.group_rows = H;
+  b.amax_bits = amax2;
+  b.g_out = out->w2_g;
+  b.codes = out->w2_codes;
+  b.codes_ld = Ip / 2;
+  b.sf = out->w2_sf;
+  b.sf_words = Ip / 64;
+  b.cols_pad = Ip;
+  b.rows_total = b.rows;
+  b.map = kMapIdentity;
+  b.status = device_status_ptr();
+  return from_cuda(launch_quantize_rows(b, kRoundRNE, s));
+}
+
+nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* w, int64_t T, int32_t k,
+                                const nvfp4_moe_weights* wt, void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (wt == nullptr || T < 0 || k <= 0 || k > 32) return NVFP4_ERR_INVALID_ARG;
+  const int32_t E = wt->E;
+  const int64_t H = wt->H, I = wt->I;
+  if (E <= 0 || E > 1024 || k > E) return NVFP4_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 64 != 0 || H > 8192 || I > 4096) return NVFP4_ERR_UNSUPPORTED;
+  if (T * k >= ((int64_t)1 << 31) - (int64_t)E * 128) return NVFP4_ERR_UNSUPPORTED;
+  if (T == 0) return NVFP4_OK;
+  const void* ptrs[] = {x, out, ws, wt->w13_codes, wt->w13_sf, wt->w13_g, wt->w2_codes, wt->w2_sf, wt->w2_g};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned4(ids) || !aligned4(w)) return NVFP4_ERR_INVALID_ARG;   // read element by element
+  size_t hist_off, hist_bytes;
+  const ForwardLayout L = forward_layout(T, k, E, H, I, &hist_off, &hist_bytes);
+  if (ws_bytes < (size_t)L.off[14]) return NVFP4_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  auto at = [&](int i) { return base + L.off[i]; };
+  int32_t* counts = reinterpret_cast<int32_t*>(at(0));
+  int32_t* offsets = reinterpret_cast<int32_t*>(at(1));
+  int32_t* padded = reinterpret_cast<int32_t*>(at(2));
+  int32_t* inv = reinterpret_cast<int32_t*>(at(3));
+  int32_t* perm = reinterpret_cast<int32_t*>(at(4));
+  uint8_t* aq = at(5);
+  uint8_t* sfa = at(6);
+  float* ga = reinterpret_cast<float*>(at(7));
+  void* dbuf = at(8);
+  uint8_t* hq = at(9);
+  uint8_t* sfh = at(10);
+  float* gh = reinterpret_cast<float*>(at(11));
+  void* ybuf = at(12);
+  const int64_t mcap = L.off[13];
+  const int64_t Ip = round_up(I, 256);
+  int* status = device_status_ptr();
+
+  cudaError_t e = launch_permute(ids, T, k, E, counts, offsets, padded, inv, perm,
+                                 reinterpret_cast<int32_t*>(base + hist_off), permute_chunks(T * k), status, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+
+  QuantArgs a{};
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.rows = T;
+  a.cols = H;
+  a.ld = H;
+  a.mode = kScopeRow;
+  a.g_out = ga;
+  a.codes = aq;
+  a.codes_ld = H / 2;
+  a.sf = sfa;
+  a.sf_words = H / 64;
+  a.cols_pad = H;
+  a.rows_total = T;
+  a.map = kMapScatter;
+  a.inv = inv;
+  a.k = k;
+  a.status = status;
+  e = launch_quantize_rows(a, kRoundRNE, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+
+  nvfp4_status st = gemm(aq, sfa, ga, wt->w13_codes, wt->w13_sf, wt->w13_g, padded, counts, mcap, 2 * I, H, E,
+                         dbuf, 0, 2 * I, s);
+  if (st != NVFP4_OK) return st;
+  e = launch_swiglu_quant(dbuf, perm, mcap, padded + E, I, Ip, nullptr, hq, sfh, gh, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  st = gemm(hq, sfh, gh, wt->w2_codes, wt->w2_sf, wt->w2_g, padded, counts, mcap, H, Ip, E, ybuf, 0, H, s);
+  if (st != NVFP4_OK) return st;
+  return from_cuda(launch_combine(ybuf, inv, w, T, k, H, out, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,267 @@
+// W4A4 grouped GEMM over ragged expert groups on the 5th-generation tensor cores.
+//
+// "Low-Bit Precision Training Is Ready for Production...", §"What W4A4 GEMM Actually
+// Changes": with both operands in 4 bits the GEMM itself runs at FP4 tensor-core rate;
+// "miniTE identifies and closes the execution gap...", §Development: grouped GEMMs
+// over the experts.  For every row r of expert e's group:
+//     D[r, n] = (gA[r] * gB[e]) * sum_k value(A)[r,k] sf_A[r,k/16] value(B_e)[n,k] sf_B[n,k/16]
+//
+// Design (one CTA per SM, persistent, 6 warps):
+//   warp 0  TMA producer: A tile 128 x 256 codes and B tile 128 x 256 codes per stage
+//           (128-byte swizzled boxes), plus the matching 2 KB scale-factor blocks of A and
+//           B by bulk copy -- the tiled scale layout keeps them contiguous.
+//   warp 1  MMA issuer: copies the stage's scales into TMEM (tcgen05.cp 32x128b.warpx4),
+//           then four tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=128,
+//           K=64) into a TMEM accumulator; tcgen05.commit frees the stage.  Two
+//           accumulators let the epilogue of one tile overlap the main loop of the next.
+//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns, scale by gA[r] * gB[e] in
+//           float32, round to BF16 (or keep float32), store rows of the group only.
+// Tiles are (128-row block of the padded group layout) x (128 output columns); tile t
+// is row block t / (N/128), column block t % (N/128), so CTAs running at the same time
+// share A tiles and one expert's weights in L2.  The K loop has a fixed order and no
+// split, so every output element has one accumulation order whatever the batch.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+namespace gg {
+constexpr int kBM = 128;          // rows per tile (one per TMEM lane)
+constexpr int kBN = 128;          // output columns per tile
+constexpr int kBKBytes = 128;     // K bytes per stage = 256 FP4 values (one 128-byte swizzle row)
+constexpr int kStages = 6;
+constexpr int kABytes = kBM * kBKBytes;
+constexpr int kBBytes = kBN * kBKBytes;
+constexpr int kSFABytes = 4 * 512;           // 4 k-groups of 64 x 128 rows
+constexpr int kSFBBytes = (kBN / 128) * 4 * 512;
+constexpr uint32_t kStageTx = kABytes + kBBytes + kSFABytes + kSFBBytes;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = kBN;                // one accumulator: 128 lanes x kBN float32
+constexpr int kSFCol0 = 2 * kAccCols;        // scale factors after the two accumulators
+constexpr int kSFStageCols = 16 + 4 * 4 * (kBN / 128);
+constexpr int kThreads = 192;
+constexpr int kMaxE = 1024;
+
+struct Smem {
+  uint8_t a[kStages][kABytes];
+  uint8_t b[kStages][kBBytes];
+  uint8_t sfa[kStages][kSFABytes];
+  uint8_t sfb[kStages][kSFBBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t accf[2];
+  uint64_t acce[2];
+  uint32_t tmem_base;
+  int abort;
+  int32_t offsets[kMaxE + 1];
+};
+static_assert(kSFCol0 + kStages * kSFStageCols <= kTmemCols, "TMEM budget");
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+}  // namespace gg
+
+__device__ __forceinline__ int find_group(const int32_t* off, int E, int32_t row0) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= row0) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(gg::kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                        const GemmArgs g) {
+  using namespace gg;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sm.accf[a], 1);
+      mbar_init(&sm.acce[a], 4 * 32);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tma);
+    prefetch_tensormap(&tmb);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort = &sm.abort;
+
+  const int n_tiles = g.N / kBN;
+  const int m_tiles = sm.offsets[g.E] / kBM;
+  const int total = m_tiles * n_tiles;
+  const int kblocks = g.K / (2 * kBKBytes);
+  const int64_t sf_kgroups = g.K / 64;   // 512-byte scale blocks per 128-row block
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
+        const int32_t row0 = m_tile * kBM;
+        const int e = find_group(sm.offsets, g.E, row0);
+        const int32_t brow = e * g.N + n_tile * kBN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, g.status, abort)) goto producer_done;
+          mbar_arrive_expect_tx(&sm.full[stage], kStageTx);
+          tma_load_2d(sm.a[stage], &tma, kb * kBKBytes, row0, &sm.full[stage]);
+          tma_load_2d(sm.b[stage], &tmb, kb * kBKBytes, brow, &sm.full[stage]);
+          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)m_tile * sf_kgroups + kb * 4) * 512, kSFABytes,
+                    &sm.full[stage]);
+#pragma unroll
+          for (int h = 0; h < kBN / 128; ++h)
+            bulk_load(sm.sfb[stage] + h * 2048, g.sfb + ((int64_t)(brow / 128 + h) * sf_kgroups + kb * 4) * 512,
+                      2048, &sm.full[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        const uint32_t acc = it & 1, acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&sm.acce[acc], acc_phase ^ 1u, g.status, abort)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * kAccCols;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&sm.full[stage], phase, g.status, abort)) goto mma_done;
+          tc_fence_after();
+          const uint32_t sfa_t = tmem + kSFCol0 + stage * kSFStageCols;
+          const uint32_t sfb_t = sfa_t + 16;
+          const uint32_t sa = smem_u32(sm.a[stage]), sb = smem_u32(sm.b[stage]);
+          const uint32_t ssfa = smem_u32(sm.sfa[stage]), ssfb = smem_u32(sm.sfb[stage]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
+#pragma unroll
+            for (int h = 0; h < kBN / 128; ++h)
+              tc_cp_32x128b_warpx4(sfb_t + 4 * (kBN / 128) * j + 4 * h, smem_desc(ssfb + 2048 * h + 512 * j, 0, 128, 0));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
+            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * (kBN / 128) * j,
+                        (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit(&sm.empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        tc_commit(&sm.accf[acc]);
+      }
+    mma_done:;
+    }
+  } else {
+    // epilogue: warps 2..5; TMEM lane quadrant = warp % 4
+    const int q = warp & 3;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const uint32_t acc = it & 1, acc_phase = (it >> 1) & 1;
+      if (!mbar_wait(&sm.accf[acc], acc_phase, g.status, abort)) break;
+      tc_fence_after();
+      const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
+      const int32_t row0 = m_tile * kBM;
+      const int e = find_group(sm.offsets, g.E, row0);
+      const int32_t r_in_group = row0 - sm.offsets[e] + q * 32 + lane;
+      const bool valid = r_in_group < g.rows[e];
+      const int64_t row = (int64_t)row0 + q * 32 + lane;
+      const float scale = valid ? __fmul_rn(g.ga[row], g.gb[e]) : 0.0f;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c0, v);
+        tmem_ld_wait();
+        if (valid) {
+          const int64_t n0 = (int64_t)n_tile * kBN + c0;
+          if (g.out_f32) {
+            float* dp = static_cast<float*>(g.d) + row * g.ldd + n0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float4 o;
+              o.x = __fmul_rn(__uint_as_float(v[4 * u + 0]), scale);
+              o.y = __fmul_rn(__uint_as_float(v[4 * u + 1]), scale);
+              o.z = __fmul_rn(__uint_as_float(v[4 * u + 2]), scale);
+              o.w = __fmul_rn(__uint_as_float(v[4 * u + 3]), scale);
+              *reinterpret_cast<float4*>(dp + 4 * u) = o;
+            }
+          } else {
+            __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(g.d) + row * g.ldd + n0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t w[4];
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const __nv_bfloat162 b2 =
+                    __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[8 * u + 2 * p]), scale),
+                                          __fmul_rn(__uint_as_float(v[8 * u + 2 * p + 1]), scale));
+                w[p] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              *reinterpret_cast<uint4*>(dp + 8 * u) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.acce[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
+                                int64_t max_m_tiles, cudaStream_t s) {
+  static bool attr_set[64] = {};   // the attribute is set once per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)gg::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int64_t tiles = max_m_tiles * (g.N / gg::kBN);
+  if (tiles == 0) return cudaSuccess;
+  int grid = num_sms();
+  if (tiles < grid) grid = (int)tiles;
+  grouped_gemm_kernel<<<grid, gg::kThreads, gg::kSmemBytes, s>>>(tma, tmb, g);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,77 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+enum : int { kScopeTensor = 0, kScopeRow = 1, kScopeGroup = 2 };
+enum : int { kRoundRNE = 0, kRoundSR = 1 };
+enum : int { kMapIdentity = 0, kMapInterleave = 1, kMapScatter = 2 };
+
+struct QuantArgs {
+  const __nv_bfloat16* x;  // input rows [rows, ld]
+  int64_t rows, cols, ld;
+  int mode;                // kScope*
+  int64_t group_rows;
+  const float* g_in;       // nullable: given global scales
+  const uint32_t* amax_bits;  // tensor / group modes without g_in
+  float* g_out;            // nullable
+  uint8_t* codes;          // output codes, codes_ld bytes per output row
+  int64_t codes_ld;
+  uint8_t* sf;             // tiled scales
+  int64_t sf_words;        // 4-scale words per row of the tile grid = ceil(cols_pad / 64)
+  int64_t cols_pad;        // stored columns (>= cols): codes / scales beyond cols are zero
+  int64_t rows_total;      // rows visited; rows..rows_total-1 only get zero scales
+  int map;                 // kMap*
+  int64_t map_I;           // interleave: intermediate size I
+  const int32_t* inv;      // scatter: output rows inv[row * k + j]
+  int k;
+  uint64_t seed, rng_offset;
+  int* status;
+};
+
+struct GemmArgs {
+  const uint8_t* sfa;      // tiled scales of A (M_total rows)
+  const uint8_t* sfb;      // tiled scales of B (E*N rows)
+  const float* ga;         // [M_total]
+  const float* gb;         // [E]
+  const int32_t* offsets;  // [E+1] padded group starts
+  const int32_t* rows;     // [E] valid rows per group
+  int32_t E;
+  int32_t N, K;
+  void* d;
+  int64_t ldd;
+  int out_f32;
+  int* status;
+};
+
+int num_sms();
+int* device_status_ptr();
+
+cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t group_rows,
+                        uint32_t* amax_bits, int64_t n_scopes, cudaStream_t s);
+cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s);
+
+// Grouped GEMM: tensor maps are built by the caller (api.cu).
+cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
+                                int64_t max_m_tiles, cudaStream_t s);
+
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renorm, int32_t* ids,
+                              float* w, cudaStream_t s);
+cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* padded, int32_t* inv, int32_t* perm, int32_t* hist, int64_t nchunks,
+                           int* status, cudaStream_t s);
+cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int64_t T, int k, int64_t H,
+                           void* out, cudaStream_t s);
+// rows: rows of d to visit; nrows_dev (nullable): device count that caps rows.
+cudaError_t launch_swiglu_quant(const void* d, const int32_t* perm, int64_t rows, const int32_t* nrows_dev,
+                                int64_t I, int64_t Ip, void* h_out, uint8_t* hq, uint8_t* hsf, float* gh,
+                                cudaStream_t s);
+
+constexpr int64_t kPermuteChunk = 1024;   // (token, j) entries per warp in the permute
+inline int64_t permute_chunks(int64_t entries) { return (entries + kPermuteChunk - 1) / kPermuteChunk; }
+
+}  // namespace nvfp4

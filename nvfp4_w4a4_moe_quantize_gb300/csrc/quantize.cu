@@ -1,0 +1,231 @@
+// NVFP4 quantiser kernels: the scope amax pass and the row quantiser.
+//
+// "The 4-bitter Lesson: Balancing Stability and Performance in NVFP4 RL":
+//   §Baseline -- E2M1 values, one E4M3 scale per 16 values, one FP32 global scale;
+//   §"Why is the NVFP4 pretraining recipe not sufficient for RL?" -- one global scale
+//   per weight tensor, one per token for activations, computed inside the fused
+//   quantisation kernel, and stochastic rounding as the pretraining recipe's option.
+//
+// Layout of the work: one warp per input row.  Lane l owns the 16-byte chunks at
+// columns 8l + 256i, so every load instruction of the warp reads 512 contiguous bytes
+// and every code store writes 128 contiguous bytes.  The two lanes l, l^1 hold the two
+// halves of one 16-value block; their shuffle gives the block max.  Lanes 8q gather the
+// four scale bytes of a 64-column group into the one 32-bit word the tiled scale layout
+// keeps contiguous.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "encode.cuh"
+#include "launch.h"
+#include "status.cuh"
+
+namespace nvfp4 {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ int64_t sf_word_offset(int64_t r, int64_t w, int64_t sf_words) {
+  return ((r >> 7) * sf_words + w) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------ amax of each scope
+
+// Max |x| over the tensor (group_rows == 0) or over each group of group_rows rows.
+// Results are float bit patterns combined with atomicMax, which for non-negative floats
+// is the float maximum whatever the order: deterministic.
+__global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols,
+                                                   int64_t ld, int64_t group_rows, uint32_t* amax_bits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  const int64_t per = (rows + nwarp - 1) / nwarp;
+  const int64_t r0 = warp * per, r1 = min(rows, r0 + per);
+  float m = 0.0f;
+  int64_t grp = group_rows ? (r0 / group_rows) : 0;
+  for (int64_t r = r0; r < r1; ++r) {
+    if (group_rows && r / group_rows != grp) {
+      m = warp_max(m);
+      if (lane == 0 && m > 0.0f) atomicMax(&amax_bits[grp], __float_as_uint(m));
+      m = 0.0f;
+      grp = r / group_rows;
+    }
+    const __nv_bfloat16* xr = x + r * ld;
+    for (int64_t c = 8 * lane; c < cols; c += 256) {
+      float f[8];
+      bf16x8_to_f32(ld_nc_v4(xr + c), f);
+      m = fmaxf(m, absmax8(f));
+    }
+  }
+  m = warp_max(m);
+  if (group_rows) {
+    if (lane == 0 && r0 < r1 && m > 0.0f) atomicMax(&amax_bits[grp], __float_as_uint(m));
+    return;
+  }
+  __shared__ float sm[8];
+  if (lane == 0) sm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = sm[0];
+    for (int i = 1; i < 8; ++i) b = fmaxf(b, sm[i]);
+    if (b > 0.0f) atomicMax(&amax_bits[0], __float_as_uint(b));
+  }
+}
+
+// ------------------------------------------------------------------ row quantiser
+
+__device__ __forceinline__ int64_t interleave_row(int64_t r, int64_t I) {
+  const int64_t n2 = 2 * I, e = r / n2, rl = r - e * n2;
+  int64_t o;
+  if (rl < I) {
+    o = (rl >> 6) * 128 + (rl & 63);
+  } else {
+    const int64_t u = rl - I;
+    o = (u >> 6) * 128 + 64 + (u & 63);
+  }
+  return e * n2 + o;
+}
+
+template <int RND, int MAXC>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(QuantArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  const int64_t data_words = (a.cols + 63) / 64;
+
+  for (int64_t row = warp; row < a.rows_total; row += nwarp) {
+    if (row >= a.rows) {  // padding row of the tile grid: its scales are zero
+      for (int64_t w = lane; w < a.sf_words; w += 32)
+        *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(row, w, a.sf_words)) = 0u;
+      continue;
+    }
+    uint4 q[MAXC];
+    float bm[MAXC];
+    const __nv_bfloat16* xr = a.x + row * a.ld;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int64_t col = 8 * lane + 256 * i;
+      q[i] = col < a.cols ? ld_nc_v4(xr + col) : make_uint4(0, 0, 0, 0);
+    }
+    float rmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      float f[8];
+      bf16x8_to_f32(q[i], f);
+      const float cm = absmax8(f);
+      bm[i] = fmaxf(cm, __shfl_xor_sync(kFull, cm, 1));
+      rmax = fmaxf(rmax, bm[i]);
+    }
+    float g;
+    if (a.mode == kScopeRow) {
+      rmax = warp_max(rmax);
+      g = a.g_in ? a.g_in[row] : __fdiv_rn(rmax, kGlobalDivisor);
+    } else if (a.mode == kScopeTensor) {
+      g = a.g_in ? a.g_in[0] : __fdiv_rn(__uint_as_float(a.amax_bits[0]), kGlobalDivisor);
+    } else {
+      const int64_t gi = row / a.group_rows;
+      g = a.g_in ? a.g_in[gi] : __fdiv_rn(__uint_as_float(a.amax_bits[gi]), kGlobalDivisor);
+    }
+    const float six_g = __fmul_rn(6.0f, g);
+
+    const int nout = a.map == kMapScatter ? a.k : 1;
+    const int64_t orow0 = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
+    int32_t my_slot = 0;
+    if (a.map == kMapScatter && lane < a.k) my_slot = a.inv[row * a.k + lane];
+
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int64_t col = 8 * lane + 256 * i;
+      const bool active = col < a.cols;
+      const BlockScale bs = block_scale(bm[i], g, six_g);
+      float f[8], v[8];
+      bf16x8_to_f32(q[i], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(f[e], bs.r);
+      uint32_t word;
+      if (RND == kRoundSR) {
+        const uint64_t j = a.rng_offset + (uint64_t)(row * a.cols + col) / 8u;
+        const uint4 rnd = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u),
+                                        (uint32_t)a.seed, (uint32_t)(a.seed >> 32));
+        word = e2m1x8_sr(v, rnd);
+      } else {
+        word = e2m1x8_rn(v);
+      }
+      const uint32_t sfb = active ? bs.sf : 0u;
+      const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
+      const uint32_t s4 = __shfl_down_sync(kFull, sfb, 4);
+      const uint32_t s6 = __shfl_down_sync(kFull, sfb, 6);
+      const uint32_t sfw = sfb | (s2 << 8) | (s4 << 16) | (s6 << 24);
+      for (int j = 0; j < nout; ++j) {
+        const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
+        if (orow < 0) continue;   // entry whose expert id was rejected: no slot
+        if (active) *reinterpret_cast<uint32_t*>(a.codes + orow * a.codes_ld + col / 2) = word;
+        if ((lane & 7) == 0 && active)
+          *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, 4 * i + lane / 8, a.sf_words)) = sfw;
+      }
+    }
+    for (int j = 0; j < nout; ++j) {
+      const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
+      if (orow < 0) continue;
+      for (int64_t w = data_words + lane; w < a.sf_words; w += 32)
+        *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, w, a.sf_words)) = 0u;
+      for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
+        *reinterpret_cast<uint2*>(a.codes + orow * a.codes_ld + b) = make_uint2(0u, 0u);
+      if (lane == 0 && a.g_out != nullptr) {
+        if (a.mode == kScopeRow) a.g_out[a.map == kMapScatter ? orow : row] = g;
+        else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
+        else if (a.mode == kScopeGroup && row % a.group_rows == 0) a.g_out[row / a.group_rows] = g;
+      }
+    }
+  }
+}
+
+template <int RND>
+static cudaError_t launch_quant_rnd(const QuantArgs& a, int maxc, int grid, cudaStream_t s) {
+  switch (maxc) {
+    case 1: quantize_rows_kernel<RND, 1><<<grid, 256, 0, s>>>(a); break;
+    case 2: quantize_rows_kernel<RND, 2><<<grid, 256, 0, s>>>(a); break;
+    case 4: quantize_rows_kernel<RND, 4><<<grid, 256, 0, s>>>(a); break;
+    case 8: quantize_rows_kernel<RND, 8><<<grid, 256, 0, s>>>(a); break;
+    case 16: quantize_rows_kernel<RND, 16><<<grid, 256, 0, s>>>(a); break;
+    default: quantize_rows_kernel<RND, 32><<<grid, 256, 0, s>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t group_rows,
+                        uint32_t* amax_bits, int64_t n_scopes, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t) * n_scopes, s);
+  if (err != cudaSuccess) return err;
+  if (rows == 0) return cudaSuccess;
+  const int sms = num_sms();
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > 4 * sms) blocks = 4 * sms;
+  amax_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, group_rows,
+                                          amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s) {
+  if (a.rows_total == 0) return cudaSuccess;
+  int maxc = 1;
+  while (maxc * 256 < a.cols) maxc *= 2;
+  const int sms = num_sms();
+  int64_t blocks = (a.rows_total + 7) / 8;
+  const int64_t cap = (int64_t)(maxc <= 8 ? 8 : 4) * sms;
+  if (blocks > cap) blocks = cap;
+  return rounding == kRoundSR ? launch_quant_rnd<kRoundSR>(a, maxc, (int)blocks, s)
+                              : launch_quant_rnd<kRoundRNE>(a, maxc, (int)blocks, s);
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,351 @@
+// Routing, expert grouping and the weighted un-permute of the MoE expert block.
+//
+// Top-k routing and the grouping of (token, slot) pairs by expert are the "token permute
+// by router top-k" around the expert GEMMs; the weighted un-permute returns every
+// token's k expert outputs to its row.  Slot order: experts ascending, tokens ascending
+// inside an expert (a stable counting sort), each expert's group starting at a multiple
+// of 128 rows -- deterministic and independent of thread timing, so that a token's
+// output bits never depend on the batch ("Low-Bit Precision Training Is Ready for
+// Production...", §"The Cross-Engine Alignment Problem").
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "status.cuh"
+
+namespace nvfp4 {
+
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+// ------------------------------------------------------------------ top-k routing
+
+// One warp per token.  Lane l holds experts l, l+32, ...; k rounds of a warp arg-max
+// with (larger logit, then lower id) as the order.  Weights: expf relative to the top
+// logit, then divided by the sum over the chosen k (or over all experts).
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
+                                                         int renorm, int32_t* __restrict__ ids,
+                                                         float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  for (int64_t t = warp; t < T; t += nwarp) {
+    float v[EPL];
+    const float* lr = logits + t * E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? lr[e] : -INFINITY;
+    }
+    uint32_t taken = 0;
+    int my_id = 0;
+    float my_v = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7FFFFFFF;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(kFullMask, bv, o);
+        const int oi = __shfl_xor_sync(kFullMask, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_id = bi;
+        my_v = bv;
+      }
+    }
+    const float top = __shfl_sync(kFullMask, my_v, 0);
+    const float ex = lane < k ? expf(my_v - top) : 0.0f;
+    float den;
+    if (renorm) {
+      den = ex;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFullMask, den, o);
+    } else {
+      den = 0.0f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i < E) den += expf(v[i] - top);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFullMask, den, o);
+    }
+    if (lane < k) {
+      ids[t * k + lane] = my_id;
+      w[t * k + lane] = __fdiv_rn(ex, den);
+    }
+  }
+}
+
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renorm, int32_t* ids, float* w,
+                              cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  int64_t blocks = (T + 7) / 8;
+  if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
+  const int epl = (E + 31) / 32;
+#define NVFP4_ROUTE(N) route_topk_kernel<N><<<(int)blocks, 256, 0, s>>>(logits, T, E, k, renorm, ids, w)
+  if (epl <= 1) NVFP4_ROUTE(1);
+  else if (epl <= 2) NVFP4_ROUTE(2);
+  else if (epl <= 4) NVFP4_ROUTE(4);
+  else if (epl <= 8) NVFP4_ROUTE(8);
+  else if (epl <= 16) NVFP4_ROUTE(16);
+  else NVFP4_ROUTE(32);
+#undef NVFP4_ROUTE
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ expert grouping
+
+// Pass 1: per chunk of kPermuteChunk flattened entries (one warp each), the count of
+// entries per expert.  hist is [E][nchunks].  Matching lanes are found with
+// __match_any_sync; the lowest lane of each match group adds the group's size.
+__global__ void __launch_bounds__(256) permute_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int E,
+                                                           int64_t nchunks, int32_t* __restrict__ hist,
+                                                           int* status) {
+  extern __shared__ int32_t sh[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 8 + wib;
+  if (c >= nchunks) return;
+  int32_t* cnt = sh + wib * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const int64_t end = min(n, (c + 1) * kPermuteChunk);
+  for (int64_t base = c * kPermuteChunk; base < end; base += 32) {
+    const int64_t i = base + lane;
+    int e = -1;
+    if (i < end) {
+      e = ids[i];
+      if (e < 0 || e >= E) {
+        set_status(status, kStatusBadInput);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(kFullMask, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
+    __syncwarp();
+  }
+  for (int e = lane; e < E; e += 32) hist[(int64_t)e * nchunks + c] = cnt[e];
+}
+
+// Pass 2 (one block): exclusive scan of every expert's chunk counts (in place), the
+// per-expert totals, the unpadded and 128-padded exclusive scans over experts, and -1
+// in the padding slots of perm.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ hist, int64_t nchunks, int E,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ padded,
+                                                            int32_t* __restrict__ perm) {
+  __shared__ int32_t s_cnt[1024];
+  __shared__ int32_t s_pad[1025];
+  __shared__ int32_t s_wsum[2][32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  constexpr int kVec = 8;
+  for (int e = wid; e < E; e += 32) {
+    int32_t* h = hist + (int64_t)e * nchunks;
+    int32_t carry = 0;
+    for (int64_t c0 = 0; c0 < nchunks; c0 += 32 * kVec) {
+      int32_t v[kVec];
+#pragma unroll
+      for (int u = 0; u < kVec; ++u) {
+        const int64_t c = c0 + 32 * u + lane;
+        v[u] = c < nchunks ? h[c] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kVec; ++u) {
+        int32_t x = v[u];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t y = __shfl_up_sync(kFullMask, x, o);
+          if (lane >= o) x += y;
+        }
+        const int64_t c = c0 + 32 * u + lane;
+        if (c < nchunks) h[c] = carry + x - v[u];
+        carry += __shfl_sync(kFullMask, x, 31);
+      }
+    }
+    if (lane == 0) s_cnt[e] = carry;
+  }
+  __syncthreads();
+  // block scans over experts (E <= 1024): one thread per expert
+  const int e = threadIdx.x;
+  const int32_t cnt = e < E ? s_cnt[e] : 0;
+  const int32_t pc = (cnt + 127) / 128 * 128;
+  int32_t x0 = cnt, x1 = pc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y0 = __shfl_up_sync(kFullMask, x0, o);
+    const int32_t y1 = __shfl_up_sync(kFullMask, x1, o);
+    if (lane >= o) {
+      x0 += y0;
+      x1 += y1;
+    }
+  }
+  if (lane == 31) {
+    s_wsum[0][wid] = x0;
+    s_wsum[1][wid] = x1;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    int32_t a0 = s_wsum[0][lane], a1 = s_wsum[1][lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y0 = __shfl_up_sync(kFullMask, a0, o);
+      const int32_t y1 = __shfl_up_sync(kFullMask, a1, o);
+      if (lane >= o) {
+        a0 += y0;
+        a1 += y1;
+      }
+    }
+    s_wsum[0][lane] = a0 - s_wsum[0][lane];
+    s_wsum[1][lane] = a1 - s_wsum[1][lane];
+  }
+  __syncthreads();
+  const int32_t excl0 = x0 - cnt + s_wsum[0][wid];
+  const int32_t excl1 = x1 - pc + s_wsum[1][wid];
+  if (e < E) {
+    counts[e] = cnt;
+    offsets[e] = excl0;
+    padded[e] = excl1;
+    s_pad[e] = excl1;
+    if (e == E - 1) {
+      offsets[E] = excl0 + cnt;
+      padded[E] = excl1 + pc;
+      s_pad[E] = excl1 + pc;
+    }
+  }
+  __syncthreads();
+  if (perm != nullptr) {
+    for (int ee = wid; ee < E; ee += 32) {
+      const int32_t lo = s_pad[ee] + s_cnt[ee], hi = s_pad[ee + 1];
+      for (int32_t r = lo + lane; r < hi; r += 32) perm[r] = -1;
+    }
+  }
+}
+
+// Pass 3: the slot of every entry.  Inside a chunk the warp walks 32 entries at a time
+// in order; an entry's rank among equal experts is the count of matching lower lanes
+// plus the running count of that expert, which starts at the chunk's exclusive prefix.
+__global__ void __launch_bounds__(256) permute_rank_kernel(const int32_t* __restrict__ ids, int64_t n, int k,
+                                                           int E, int64_t nchunks,
+                                                           const int32_t* __restrict__ hist,
+                                                           const int32_t* __restrict__ padded,
+                                                           int32_t* __restrict__ inv, int32_t* __restrict__ perm) {
+  extern __shared__ int32_t sh[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  int32_t* s_pad = sh;                 // E
+  int32_t* run = sh + E + wib * E;     // E per warp
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_pad[e] = padded[e];
+  __syncthreads();
+  const int64_t c = (int64_t)blockIdx.x * 8 + wib;
+  if (c >= nchunks) return;
+  for (int e = lane; e < E; e += 32) run[e] = hist[(int64_t)e * nchunks + c];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  const int64_t end = min(n, (c + 1) * kPermuteChunk);
+  for (int64_t base = c * kPermuteChunk; base < end; base += 32) {
+    const int64_t i = base + lane;
+    int e = -1;
+    if (i < end) {
+      e = ids[i];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(kFullMask, e);
+    if (e >= 0) {
+      const int32_t slot = s_pad[e] + run[e] + __popc(peers & lt);
+      inv[i] = slot;
+      if (perm != nullptr) perm[slot] = (int32_t)(i / k);
+    } else if (i < end) {
+      inv[i] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) run[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* padded, int32_t* inv, int32_t* perm, int32_t* hist, int64_t nchunks,
+                           int* status, cudaStream_t s) {
+  const int64_t n = T * k;
+  const int blocks = (int)((nchunks + 7) / 8);
+  if (nchunks > 0) {
+    permute_hist_kernel<<<blocks, 256, 8 * E * sizeof(int32_t), s>>>(ids, n, E, nchunks, hist, status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  permute_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, E, counts, offsets, padded, perm);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || nchunks == 0) return err;
+  permute_rank_kernel<<<blocks, 256, 9 * E * sizeof(int32_t), s>>>(ids, n, k, E, nchunks, hist, padded, inv, perm);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ weighted un-permute
+
+// One warp per token; lane l owns columns 8l + 256i.  out = BF16 of the float32 sum, in
+// order j = 0..k-1, of float32 products w[t, j] * y[slot]; a slot of -1 (an entry whose
+// expert id was rejected) contributes nothing.
+__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ y,
+                                                      const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ w, int64_t T, int k, int64_t H,
+                                                      __nv_bfloat16* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  for (int64_t t = warp; t < T; t += nwarp) {
+    int32_t my_slot = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+      my_slot = inv[t * k + lane];
+      my_w = w[t * k + lane];
+    }
+    for (int64_t c = 8 * lane; c < H; c += 256) {
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int32_t sl = __shfl_sync(kFullMask, my_slot, j);
+        const float wj = __shfl_sync(kFullMask, my_w, j);
+        if (sl < 0) continue;
+        const uint4 q = *reinterpret_cast<const uint4*>(y + (int64_t)sl * H + c);
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wj, __uint_as_float(wd[e] << 16)));
+          acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wj, __uint_as_float(wd[e] & 0xFFFF0000u)));
+        }
+      }
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+        ow[e] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      *reinterpret_cast<uint4*>(out + t * H + c) = o;
+    }
+  }
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int64_t T, int k, int64_t H, void* out,
+                           cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  int64_t blocks = (T + 7) / 8;
+  if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
+  combine_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(y), inv, w, T, k, H,
+                                             static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,154 @@
+// SwiGLU over the gate/up GEMM output, followed by per-row NVFP4 requantisation of h.
+//
+// The down projection's input is quantised the same way as the block's input: one FP32
+// scale per routed row, E4M3 scales per 16 values, E2M1 codes ("The 4-bitter Lesson:
+// Balancing Stability and Performance in NVFP4 RL", §"Why is the NVFP4 pretraining
+// recipe not sufficient for RL?": per-token activation scales).
+//
+// h = BF16(silu(gate) * up) is the BF16 value nearest to the exact real number.  The
+// float32 evaluation (expf <= 2 ulp, three correctly rounded operations) is within
+// 7 ulps of it; when that float32 value lies within 64 ulps of a BF16 rounding midpoint,
+// or outside the range where the bound holds, h is recomputed in float64 and rounded
+// once to BF16 through a round-to-odd float32 step.  The result equals the rounding of
+// the exact value except when the exact value sits within ~1e-15 (relative) of a
+// midpoint, which silu(g)*u with g != 0 never reaches exactly.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "encode.cuh"
+#include "launch.h"
+
+namespace nvfp4 {
+
+constexpr unsigned kAll = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t f32_to_bf16_rne_bits(uint32_t b) {
+  return (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;
+}
+
+// float64 -> BF16 with a single rounding: round-to-odd into float32 (which keeps 16 more
+// bits than BF16), then round-to-nearest-even into BF16.
+__device__ __forceinline__ uint32_t f64_to_bf16_bits(double v) {
+  float f = __double2float_rz(v);
+  uint32_t b = __float_as_uint(f);
+  if ((double)f != v) b |= 1u;
+  return f32_to_bf16_rne_bits(b);
+}
+
+__device__ __noinline__ uint32_t swiglu_f64(float g, float u) {
+  const double gd = g, ud = u;
+  const double sd = gd / (1.0 + exp(-gd));
+  return f64_to_bf16_bits(sd * ud);
+}
+
+__device__ __forceinline__ uint32_t swiglu_bf16(float g, float u) {
+  const float e = expf(-g);
+  const float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), u);
+  const uint32_t b = __float_as_uint(h);
+  const uint32_t low = b & 0xFFFFu;
+  const float ah = fabsf(h);
+  const bool exact_zero = (g == 0.0f) || (u == 0.0f);
+  const bool in_range = ah >= 1e-30f && ah <= 1e30f && e <= 3.0e38f;
+  const bool near_mid = low >= 0x8000u - 64u && low <= 0x8000u + 64u;
+  if (exact_zero || (in_range && !near_mid)) return f32_to_bf16_rne_bits(b);
+  return swiglu_f64(g, u);
+}
+
+// One warp per routed row.  Lane l owns h columns 8l + 256i; gate of h column c sits at
+// D column (c/64)*128 + c%64 and up at the same plus 64 (64-row interleave of W13).
+template <int MAXC>
+__global__ void __launch_bounds__(256) swiglu_quant_kernel(const __nv_bfloat16* __restrict__ d,
+                                                           const int32_t* __restrict__ perm, int64_t rows,
+                                                           const int32_t* __restrict__ nrows_dev, int64_t I,
+                                                           int64_t Ip,
+                                                           __nv_bfloat16* __restrict__ h_out,
+                                                           uint8_t* __restrict__ hq, uint8_t* __restrict__ hsf,
+                                                           float* __restrict__ gh) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  const int64_t sf_words = Ip / 64, data_words = (I + 63) / 64;
+  if (nrows_dev != nullptr && (int64_t)*nrows_dev < rows) rows = *nrows_dev;
+  for (int64_t r = warp; r < rows; r += nwarp) {
+    if (perm[r] < 0) continue;
+    const __nv_bfloat16* dr = d + r * (2 * I);
+    uint4 hv[MAXC];
+    float bm[MAXC];
+    float rmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int64_t c = 8 * lane + 256 * i;
+      hv[i] = make_uint4(0, 0, 0, 0);
+      float cm = 0.0f;
+      if (c < I) {
+        const int64_t gc = (c >> 6) * 128 + (c & 63);
+        const uint4 gq = *reinterpret_cast<const uint4*>(dr + gc);
+        const uint4 uq = *reinterpret_cast<const uint4*>(dr + gc + 64);
+        float gf[8], uf[8];
+        bf16x8_to_f32(gq, gf);
+        bf16x8_to_f32(uq, uf);
+        uint32_t hb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          hb[e] = swiglu_bf16(gf[e], uf[e]);
+          cm = fmaxf(cm, fabsf(__uint_as_float(hb[e] << 16)));
+        }
+        hv[i] = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
+                           hb[6] | (hb[7] << 16));
+        if (h_out != nullptr) *reinterpret_cast<uint4*>(h_out + r * I + c) = hv[i];
+      }
+      bm[i] = fmaxf(cm, __shfl_xor_sync(kAll, cm, 1));
+      rmax = fmaxf(rmax, bm[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rmax = fmaxf(rmax, __shfl_xor_sync(kAll, rmax, o));
+    const float g = __fdiv_rn(rmax, kGlobalDivisor);
+    const float six_g = __fmul_rn(6.0f, g);
+    uint8_t* qr = hq + r * (Ip / 2);
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int64_t c = 8 * lane + 256 * i;
+      const bool active = c < I;
+      const BlockScale bs = block_scale(bm[i], g, six_g);
+      float f[8], v[8];
+      bf16x8_to_f32(hv[i], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(f[e], bs.r);
+      const uint32_t word = e2m1x8_rn(v);
+      const uint32_t sfb = active ? bs.sf : 0u;
+      const uint32_t s2 = __shfl_down_sync(kAll, sfb, 2);
+      const uint32_t s4 = __shfl_down_sync(kAll, sfb, 4);
+      const uint32_t s6 = __shfl_down_sync(kAll, sfb, 6);
+      if (active) {
+        *reinterpret_cast<uint32_t*>(qr + c / 2) = word;
+        if ((lane & 7) == 0) {
+          const int64_t w = 4 * i + lane / 8;
+          *reinterpret_cast<uint32_t*>(hsf + ((r >> 7) * sf_words + w) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) =
+              sfb | (s2 << 8) | (s4 << 16) | (s6 << 24);
+        }
+      }
+    }
+    for (int64_t w = data_words + lane; w < sf_words; w += 32)
+      *reinterpret_cast<uint32_t*>(hsf + ((r >> 7) * sf_words + w) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) = 0u;
+    for (int64_t b = I / 2 + 8 * lane; b < Ip / 2; b += 256) *reinterpret_cast<uint2*>(qr + b) = make_uint2(0u, 0u);
+    if (lane == 0) gh[r] = g;
+  }
+}
+
+cudaError_t launch_swiglu_quant(const void* d, const int32_t* perm, int64_t rows, const int32_t* nrows_dev,
+                                int64_t I, int64_t Ip, void* h_out, uint8_t* hq, uint8_t* hsf, float* gh,
+                                cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+  const auto* dp = static_cast<const __nv_bfloat16*>(d);
+  auto* hp = static_cast<__nv_bfloat16*>(h_out);
+  if (I <= 256) swiglu_quant_kernel<1><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
+  else if (I <= 512) swiglu_quant_kernel<2><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
+  else if (I <= 1024) swiglu_quant_kernel<4><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
+  else if (I <= 2048) swiglu_quant_kernel<8><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
+  else swiglu_quant_kernel<16><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,52 @@
+"""Helpers shared by the GPU parity tests (moving data between torch and the oracle's
+numpy arrays, and the tolerance checks).  No NVFP4 arithmetic lives here."""
+import numpy as np
+import torch
+
+from oracle import formats as F
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    """BF16 tensor -> uint16 bit patterns (numpy, CPU)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def npy(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().numpy()
+
+
+def dev(a: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def rel_err_floor(got: np.ndarray, ref: np.ndarray, floor_frac: float = 1e-2):
+    """max_i |got_i - ref_i| / max(|ref_i|, tau), tau = floor_frac * rms(ref); and the
+    normwise error ||got - ref|| / ||ref||."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    tau = floor_frac * np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    err = np.abs(got - ref) / np.maximum(np.abs(ref), tau)
+    nw = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+    return float(err.max()) if err.size else 0.0, float(nw)
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of BF16 values at |v| (subnormal spacing below 2^-126)."""
+    a = np.abs(np.asarray(v, np.float64))
+    _, e = np.frexp(a)
+    return np.exp2(np.maximum(e - 1, -126) - 7.0)
+
+
+def check_bf16_against(got_bits: np.ndarray, ref: np.ndarray, rel: float = 1e-3, floor_frac: float = 1e-2):
+    """A BF16 result against a float64 reference: within one BF16 ulp of the reference
+    plus the float32-accumulation allowance rel * max(|ref|, tau)."""
+    got = F.bf16_to_f32(got_bits).astype(np.float64)
+    ref = np.asarray(ref, np.float64)
+    tau = floor_frac * np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    bound = bf16_ulp(ref) + rel * np.maximum(np.abs(ref), tau)
+    bad = np.abs(got - ref) > bound
+    return int(bad.sum()), float((np.abs(got - ref) / np.maximum(bound, 1e-300)).max()) if ref.size else 0.0

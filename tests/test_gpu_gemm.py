@@ -1,0 +1,147 @@
+"""GPU parity of the W4A4 grouped GEMM against the oracle over the same quantised
+operands: exact cases bit for bit, random cases within 1e-3 relative (float32 output)
+or one BF16 ulp plus that allowance (BF16 output), ragged groups of 0, 1, 127, 128 and
+129+ rows, several row / column / K tiles."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import check_bf16_against, dev, npy, rel_err_floor, u16
+from oracle import formats as F
+from oracle import moe as M
+from oracle import quant as Q
+from nvfp4_w4a4_moe_quantize_gb300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+
+def _groups(counts):
+    counts = np.asarray(counts, np.int64)
+    padded = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)])
+    return counts.astype(np.int32), padded.astype(np.int32)
+
+
+def _operands_from_oracle(a_bits, counts, w_bits, a_scope="row"):
+    """Quantise with the oracle and lay the operands out the way the kernel reads them."""
+    E, N, K = w_bits.shape
+    counts, padded = _groups(counts)
+    M = int(padded[-1]) if padded[-1] > 0 else 128
+    qa = Q.quantize(a_bits, scope=a_scope)
+    a_codes = np.zeros((M, K), np.uint8)
+    a_sf = np.zeros((M, K // 16), np.uint8)
+    a_g = np.zeros(M, np.float32)
+    r = 0
+    for e in range(E):
+        n = int(counts[e])
+        a_codes[padded[e]:padded[e] + n] = qa["codes"][r:r + n]
+        a_sf[padded[e]:padded[e] + n] = qa["sf"][r:r + n]
+        a_g[padded[e]:padded[e] + n] = qa["g"][r:r + n] if a_scope == "row" else qa["g"][0]
+        r += n
+    qb = Q.quantize(w_bits.reshape(E * N, K), scope="group", group_rows=N)
+    ops = dict(a_codes=a_codes, a_sf=a_sf, a_g=a_g, b_codes=qb["codes"].reshape(E, N, K),
+               b_sf=qb["sf"].reshape(E, N, K // 16), b_g=qb["g"], counts=counts, padded=padded, M=M)
+    return ops
+
+
+def _run_gpu(lib, ops, N, K, out_dtype):
+    E = ops["b_codes"].shape[0]
+    A = dev(F.pack_e2m1(ops["a_codes"]))
+    SFA = dev(F.sf_swizzle(ops["a_sf"]))
+    B = dev(F.pack_e2m1(ops["b_codes"].reshape(E * N, K)))
+    SFB = dev(F.sf_swizzle(ops["b_sf"].reshape(E * N, K // 16)))
+    D = lib.nvfp4_grouped_gemm(A, SFA, dev(ops["a_g"]), B, SFB, dev(ops["b_g"]), dev(ops["padded"]),
+                               dev(ops["counts"]), N, K, E, out_dtype=out_dtype)
+    assert lib.nvfp4_status_check() == 0
+    return D
+
+
+def _oracle(ops):
+    return M.grouped_gemm(ops["a_codes"], ops["a_sf"], ops["a_g"], ops["b_codes"], ops["b_sf"], ops["b_g"],
+                          ops["padded"], ops["counts"])
+
+
+def _valid_rows(ops):
+    return np.concatenate([np.arange(p, p + c) for p, c in zip(ops["padded"][:-1], ops["counts"])]).astype(int)
+
+
+def test_gemm_single_tile_exact(cuda_lib):
+    """One expert, one 128x128 tile, K = 256; E2M1 grid values times powers of two so
+    every partial sum is exact in float32: the result must be bit-exact."""
+    rng = np.random.default_rng(0)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -2, -3, -4, -6])
+    s_a, s_w = 448 * 2.0 ** -11, 448 * 2.0 ** -13
+    xa = rng.choice(grid, (128, 256)) * s_a
+    xa[:, ::16] = 6 * s_a
+    w = rng.choice(grid, (1, 128, 256)) * s_w
+    w[:, :, ::16] = 6 * s_w
+    ops = _operands_from_oracle(F.bf16_round(xa), [128], F.bf16_round(w))
+    ref = _oracle(ops)
+    D = npy(_run_gpu(cuda_lib, ops, 128, 256, torch.float32))
+    np.testing.assert_array_equal(D, ref.astype(np.float32))
+    np.testing.assert_array_equal(ref, (xa @ w[0].T))          # lossless quantisation
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_ragged_groups(cuda_lib, out_dtype):
+    E, N, K = 6, 384, 512
+    counts = [0, 1, 127, 128, 129, 300]
+    a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=31))
+    w_bits = S.bf16_bits(S.randn_bf16((E, N, K), 0.02, seed=32))
+    ops = _operands_from_oracle(a_bits, counts, w_bits)
+    ref = _oracle(ops)
+    D = _run_gpu(cuda_lib, ops, N, K, out_dtype)
+    rows = _valid_rows(ops)
+    if out_dtype == torch.float32:
+        mx, nw = rel_err_floor(npy(D)[rows], ref[rows])
+        assert mx <= 1e-3, (mx, nw)
+        assert nw <= 1e-5
+    else:
+        nbad, worst = check_bf16_against(u16(D)[rows], ref[rows])
+        assert nbad == 0, worst
+
+
+def test_gemm_qwen_shaped_k_and_many_experts(cuda_lib):
+    """K = 2048 (8 K-stages), N = 1536, 16 experts with Zipf-like group sizes."""
+    E, N, K = 16, 1536, 2048
+    rng = np.random.default_rng(7)
+    counts = list(rng.integers(0, 400, E))
+    counts[3] = 0
+    a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=41))
+    w_bits = S.bf16_bits(S.randn_bf16((E, N, K), 0.02, seed=42))
+    ops = _operands_from_oracle(a_bits, counts, w_bits)
+    ref = _oracle(ops)
+    D = npy(_run_gpu(cuda_lib, ops, N, K, torch.float32))
+    rows = _valid_rows(ops)
+    mx, nw = rel_err_floor(D[rows], ref[rows])
+    assert mx <= 1e-3, (mx, nw)
+
+
+def test_gemm_leaves_rows_outside_groups_untouched(cuda_lib):
+    E, N, K = 2, 128, 256
+    counts = [5, 130]
+    a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=51))
+    w_bits = S.bf16_bits(S.randn_bf16((E, N, K), 0.02, seed=52))
+    ops = _operands_from_oracle(a_bits, counts, w_bits)
+    A = dev(F.pack_e2m1(ops["a_codes"]))
+    out = torch.full((ops["M"], N), 7.0, dtype=torch.float32, device="cuda")
+    cuda_lib.nvfp4_grouped_gemm(A, dev(F.sf_swizzle(ops["a_sf"])), dev(ops["a_g"]),
+                                dev(F.pack_e2m1(ops["b_codes"].reshape(E * N, K))),
+                                dev(F.sf_swizzle(ops["b_sf"].reshape(E * N, K // 16))), dev(ops["b_g"]),
+                                dev(ops["padded"]), dev(ops["counts"]), N, K, E, out=out)
+    o = npy(out)
+    valid = np.zeros(ops["M"], bool)
+    valid[_valid_rows(ops)] = True
+    assert np.all(o[~valid] == 7.0)
+    assert not np.any(o[valid] == 7.0)
+
+
+def test_gemm_is_deterministic(cuda_lib):
+    E, N, K = 4, 256, 1024
+    counts = [300, 17, 0, 200]
+    a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=61))
+    w_bits = S.bf16_bits(S.randn_bf16((E, N, K), 0.02, seed=62))
+    ops = _operands_from_oracle(a_bits, counts, w_bits)
+    d1 = npy(_run_gpu(cuda_lib, ops, N, K, torch.float32))
+    d2 = npy(_run_gpu(cuda_lib, ops, N, K, torch.float32))
+    rows = _valid_rows(ops)
+    np.testing.assert_array_equal(d1[rows], d2[rows])

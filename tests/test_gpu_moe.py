@@ -1,0 +1,373 @@
+"""GPU parity of the MoE expert block against the oracle: routing, grouping, combine,
+SwiGLU + requantisation, weight preparation and the whole forward, stage by stage, plus
+the execution-alignment properties (row invariance, determinism)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import bf16_tensor, check_bf16_against, dev, npy, rel_err_floor, u16
+from oracle import formats as F
+from oracle import moe as M
+from oracle import quant as Q
+from nvfp4_w4a4_moe_quantize_gb300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+
+def interleave_src(I: int) -> np.ndarray:
+    """Column (or row) j of the 64-chunk gate/up interleave holds canonical index src[j]."""
+    j = np.arange(2 * I)
+    chunk, within = j // 128, j % 128
+    return np.where(within < 64, chunk * 64 + within, I + chunk * 64 + within - 64)
+
+
+def _ws_views(ws, lay, T, k, E, H, I):
+    mcap = lay[13]
+    Ip = (I + 255) // 256 * 256
+
+    def view(i, n, dtype):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return ws[lay[i]:lay[i] + nbytes].view(dtype)
+    return dict(
+        counts=view(0, E, torch.int32), offsets=view(1, E + 1, torch.int32), padded=view(2, E + 1, torch.int32),
+        inv=view(3, T * k, torch.int32).view(T, k), perm=view(4, mcap, torch.int32),
+        aq=view(5, mcap * H // 2, torch.uint8).view(mcap, H // 2), sfa=ws[lay[6]:lay[7]],
+        ga=view(7, mcap, torch.float32), d=view(8, mcap * 2 * I, torch.bfloat16).view(mcap, 2 * I),
+        hq=view(9, mcap * Ip // 2, torch.uint8).view(mcap, Ip // 2), sfh=ws[lay[10]:lay[11]],
+        gh=view(11, mcap, torch.float32), y=view(12, mcap * H, torch.bfloat16).view(mcap, H), mcap=mcap)
+
+
+# ------------------------------------------------------------------ routing / grouping
+
+@pytest.mark.parametrize("T,E,k,kind", [(512, 8, 2, "normal"), (8192, 128, 8, "zipf"), (333, 1000, 32, "normal")])
+def test_route_topk(cuda_lib, T, E, k, kind):
+    logits = S.router_logits_zipf(T, E, seed=3) if kind == "zipf" else S.router_logits_normal(T, E, seed=3)
+    for renorm in (True, False):
+        ids, w = cuda_lib.moe_route_topk(logits.cuda(), k, renorm)
+        rid, rw = M.route_topk(logits.numpy(), k, renorm)
+        np.testing.assert_array_equal(npy(ids), rid)
+        np.testing.assert_allclose(npy(w), rw, rtol=1e-6, atol=1e-12)
+
+
+def test_route_topk_ties(cuda_lib):
+    logits = torch.randint(-2, 3, (256, 16), generator=torch.Generator().manual_seed(1)).float()
+    ids, w = cuda_lib.moe_route_topk(logits.cuda(), 4)
+    rid, rw = M.route_topk(logits.numpy(), 4)
+    np.testing.assert_array_equal(npy(ids), rid)
+    np.testing.assert_allclose(npy(w), rw, rtol=1e-6)
+
+
+@pytest.mark.parametrize("T,E,k", [(512, 8, 2), (8192, 128, 8), (1, 4, 4), (3000, 1024, 3)])
+def test_permute(cuda_lib, T, E, k):
+    logits = S.router_logits_zipf(T, E, seed=T)
+    rid, _ = M.route_topk(logits.numpy(), k)
+    p = cuda_lib.moe_permute(dev(rid), E)
+    r = M.permute(rid, E)
+    for key in ("counts", "offsets", "padded_offsets", "inv"):
+        np.testing.assert_array_equal(npy(p[key]), r[key], err_msg=key)
+    n = int(r["padded_offsets"][-1])
+    np.testing.assert_array_equal(npy(p["perm"])[:n], r["perm"])
+    assert cuda_lib.nvfp4_status_check() == 0
+
+
+def test_permute_bad_ids_set_status(cuda_lib):
+    ids = torch.tensor([[0, 1], [2, 9], [-1, 3]], dtype=torch.int32, device="cuda")
+    p = cuda_lib.moe_permute(ids, 4)
+    assert cuda_lib.nvfp4_status_check() == cuda_lib.Status.DEVICE_STATUS
+    assert cuda_lib.nvfp4_status_check() == 0                       # cleared
+    inv = npy(p["inv"])
+    assert inv[1, 1] == -1 and inv[2, 0] == -1
+    assert npy(p["counts"]).tolist() == [1, 1, 1, 1]
+
+
+def test_combine(cuda_lib):
+    T, k, H, Mr = 300, 8, 2048, 4000
+    rng = np.random.default_rng(3)
+    y = F.bf16_round(rng.standard_normal((Mr, H)))
+    inv = np.stack([rng.permutation(Mr)[:k] for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    out = u16(cuda_lib.moe_combine(bf16_tensor(y), dev(inv), dev(w)))
+    ref = M.combine(y, inv, w)
+    # float32 products and sums in order j: |err| <= (k+1) 2^-24 sum|w y| before rounding
+    yv = F.bf16_to_f32(y).astype(np.float64)
+    mag = sum(np.abs(w[:, j:j + 1].astype(np.float64) * yv[inv[:, j]]) for j in range(k))
+    exact = sum(w[:, j:j + 1].astype(np.float64) * yv[inv[:, j]] for j in range(k))
+    got = F.bf16_to_f32(out).astype(np.float64)
+    bound = 0.5 * np.exp2(np.frexp(np.abs(exact) + (k + 1) * 2.0 ** -24 * mag)[1] - 8.0) \
+        + (k + 1) * 2.0 ** -24 * mag
+    assert np.all(np.abs(got - exact) <= bound)
+    assert np.mean(out == ref) > 0.999
+
+
+# ------------------------------------------------------------------ SwiGLU + requant
+
+def test_swiglu_quantize_bit_exact(cuda_lib):
+    rows, I = 300, 768
+    rng = np.random.default_rng(5)
+    d_can = F.bf16_round(rng.standard_normal((rows, 2 * I)) * rng.choice([0.1, 1, 4, 30], (rows, 1)))
+    d_can[0, :I] = F.bf16_round(np.linspace(-120, 120, I))          # saturated gates
+    d_can[1, :5] = 0
+    d_can[2, I:I + 7] = 0x8000
+    perm = np.arange(rows, dtype=np.int32)
+    perm[7] = -1
+    d_il = d_can[:, interleave_src(I)]
+    h, hq, hsf, gh = cuda_lib.moe_swiglu_quantize(bf16_tensor(d_il), dev(perm), I)
+    live = perm >= 0
+    ref_h = M.swiglu(d_can, I)
+    np.testing.assert_array_equal(u16(h)[live], ref_h[live])
+    q = Q.quantize(ref_h[live], scope="row")
+    np.testing.assert_array_equal(npy(hq)[live], q["packed"])
+    np.testing.assert_array_equal(npy(gh)[live], q["g"])
+    sf = F.sf_unswizzle(npy(hsf), rows, I // 16)
+    np.testing.assert_array_equal(sf[live], q["sf"])
+
+
+def test_swiglu_quantize_pads_k(cuda_lib):
+    """I = 128: h is quantised into a 256-wide (zero-padded) row for the down GEMM."""
+    rows, I = 130, 128
+    d_can = S.bf16_bits(S.randn_bf16((rows, 2 * I), seed=8))
+    perm = np.arange(rows, dtype=np.int32)
+    _, hq, hsf, gh = cuda_lib.moe_swiglu_quantize(bf16_tensor(d_can[:, interleave_src(I)]), dev(perm), I)
+    q = Q.quantize(M.swiglu(d_can, I), scope="row")
+    hq = npy(hq)
+    np.testing.assert_array_equal(hq[:, :64], q["packed"])
+    assert not hq[:, 64:].any()
+    sf = F.sf_unswizzle(npy(hsf), rows, 16)
+    np.testing.assert_array_equal(sf[:, :8], q["sf"])
+    assert not sf[:, 8:].any()
+
+
+# ------------------------------------------------------------------ weights
+
+@pytest.mark.parametrize("name", ["tiny"])
+def test_prepare_weights(cuda_lib, name):
+    shape = S.WORKLOADS[name]
+    _, _, w13, w2 = S.moe_inputs(shape, seed=0)
+    pw = cuda_lib.moe_prepare_weights(w13.cuda(), w2.cuda())
+    ref = M.prepare_weights(S.bf16_bits(w13), S.bf16_bits(w2))
+    E, H, I = shape.E, shape.H, shape.I
+    src = interleave_src(I)
+    c13 = F.unpack_e2m1(npy(pw.w13_codes))
+    np.testing.assert_array_equal(c13, ref["w13_codes"][:, src, :])
+    sf13 = F.sf_unswizzle(npy(pw.w13_sf), E * 2 * I, H // 16).reshape(E, 2 * I, H // 16)
+    np.testing.assert_array_equal(sf13, ref["w13_sf"][:, src, :])
+    np.testing.assert_array_equal(npy(pw.w13_g), ref["w13_g"])
+    Ip = pw.Ip
+    c2 = F.unpack_e2m1(npy(pw.w2_codes))
+    np.testing.assert_array_equal(c2[:, :, :I], ref["w2_codes"])
+    assert not c2[:, :, I:].any()
+    sf2 = F.sf_unswizzle(npy(pw.w2_sf), E * H, Ip // 16).reshape(E, H, Ip // 16)
+    np.testing.assert_array_equal(sf2[:, :, :I // 16], ref["w2_sf"])
+    assert not sf2[:, :, I // 16:].any()
+    np.testing.assert_array_equal(npy(pw.w2_g), ref["w2_g"])
+
+
+# ------------------------------------------------------------------ forward
+
+def _forward(lib, x, ids, w, pw, T, k):
+    ws = lib.moe_forward_workspace(T, k, pw, "cuda")
+    out = lib.moe_expert_forward(x, ids, w, pw, workspace=ws)
+    assert lib.nvfp4_status_check() == 0
+    lay = lib.moe_forward_workspace_layout(T, k, pw.E, pw.H, pw.I)
+    return out, _ws_views(ws, lay, T, k, pw.E, pw.H, pw.I)
+
+
+def _stage_checks(lib, r, v, ids_np, w_np, pw, I, rows_check=None):
+    """Compare the forward's intermediates with the oracle stage by stage."""
+    pi = r["perm"]
+    n = int(pi["padded_offsets"][-1])
+    for key, ref in (("counts", pi["counts"]), ("padded", pi["padded_offsets"]), ("inv", pi["inv"])):
+        np.testing.assert_array_equal(npy(v[key]), ref, err_msg=key)
+    perm = npy(v["perm"])[:n]
+    np.testing.assert_array_equal(perm, pi["perm"])
+    live = np.nonzero(pi["perm"] >= 0)[0]
+    if rows_check is not None:
+        live = live[rows_check]
+    # per-token quantisation scattered to every slot: bit exact
+    aq = npy(v["aq"])
+    np.testing.assert_array_equal(aq[live], F.pack_e2m1(r["aq"]["codes"][live]))
+    np.testing.assert_array_equal(npy(v["ga"])[live], r["aq"]["g"][live])
+    H = aq.shape[1] * 2
+    sfa = F.sf_unswizzle(npy(v["sfa"]), v["mcap"], H // 16)
+    np.testing.assert_array_equal(sfa[live], r["aq"]["sf"][live])
+    # gate/up output (interleaved) against the float64 GEMM
+    d_gpu = u16(v["d"])[live][:, np.argsort(interleave_src(I))]
+    nbad, worst = check_bf16_against(d_gpu, r["d"][live])
+    assert nbad == 0, worst
+    # rows whose BF16 gate/up output matches the oracle bit for bit must give identical
+    # h codes, scales and g (SwiGLU is correctly rounded, the quantiser bit exact)
+    same = np.all(d_gpu == r["d_bits"][live], axis=1)
+    assert same.mean() > 0.5
+    Ip = npy(v["hq"]).shape[1] * 2
+    hq = F.unpack_e2m1(npy(v["hq"])[live])
+    np.testing.assert_array_equal(hq[same][:, :I], r["h_codes"][live][same])
+    np.testing.assert_array_equal(npy(v["gh"])[live][same], r["h_g"][live][same])
+    sfh = F.sf_unswizzle(npy(v["sfh"]), v["mcap"], Ip // 16)
+    np.testing.assert_array_equal(sfh[live][same][:, :I // 16], r["h_sf"][live][same])
+    # down output on those rows against the float64 GEMM over the same operands
+    y_gpu = u16(v["y"])[live][same]
+    nbad, worst = check_bf16_against(y_gpu, r["y"][live][same])
+    assert nbad == 0, worst
+    return same
+
+
+def test_forward_tiny_stagewise(cuda_lib):
+    shape = S.WORKLOADS["tiny"]
+    x, logits, w13, w2 = S.moe_inputs(shape, seed=0)
+    ids, w = M.route_topk(logits.numpy(), shape.k)
+    pw = cuda_lib.moe_prepare_weights(w13.cuda(), w2.cuda())
+    out, v = _forward(cuda_lib, x.cuda(), dev(ids), dev(w), pw, shape.T, shape.k)
+    r = M.moe_forward(S.bf16_bits(x), ids, w, S.bf16_bits(w13), S.bf16_bits(w2))
+    _stage_checks(cuda_lib, r, v, ids, w, pw, shape.I)
+    got = F.bf16_to_f32(u16(out)).astype(np.float64)
+    ref = F.bf16_to_f32(r["out"]).astype(np.float64)
+    mx, nw = rel_err_floor(got, ref)
+    assert nw < 1e-2, nw
+    assert np.mean(u16(out) == r["out"]) > 0.9
+
+
+def test_forward_exact_operands_bit_exact_through_requant(cuda_lib):
+    """Lossless inputs (grid values times powers of two): the gate/up output is exact, so
+    the whole chain up to the requantised h must match the oracle bit for bit."""
+    T, H, I, E, k = 256, 256, 128, 4, 2
+    rng = np.random.default_rng(9)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -2, -3, -4, -6])
+    s_x, s_w = 448 * 2.0 ** -11, 448 * 2.0 ** -13
+    xv = rng.choice(grid, (T, H)) * s_x
+    xv[:, ::16] = 6 * s_x
+    w13 = rng.choice(grid, (E, 2 * I, H)) * s_w
+    w13[:, :, ::16] = 6 * s_w
+    w2v = rng.choice(grid, (E, H, I)) * s_w
+    w2v[:, :, ::16] = 6 * s_w
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    wts = rng.random((T, k)).astype(np.float32)
+    xb, w13b, w2b = F.bf16_round(xv), F.bf16_round(w13), F.bf16_round(w2v)
+    pw = cuda_lib.moe_prepare_weights(bf16_tensor(w13b), bf16_tensor(w2b))
+    out, v = _forward(cuda_lib, bf16_tensor(xb), dev(ids), dev(wts), pw, T, k)
+    r = M.moe_forward(xb, ids, wts, w13b, w2b)
+    live = np.nonzero(r["perm"]["perm"] >= 0)[0]
+    d_gpu = u16(v["d"])[live][:, np.argsort(interleave_src(I))]
+    np.testing.assert_array_equal(d_gpu, r["d_bits"][live])
+    hq = F.unpack_e2m1(npy(v["hq"])[live])
+    np.testing.assert_array_equal(hq[:, :I], r["h_codes"][live])
+    np.testing.assert_array_equal(npy(v["gh"])[live], r["h_g"][live])
+    nbad, worst = check_bf16_against(u16(v["y"])[live], r["y"][live])
+    assert nbad == 0, worst
+
+
+def test_forward_matches_chain_of_standalone_kernels(cuda_lib):
+    """The forward equals route -> permute -> quantise/scatter -> GEMM -> SwiGLU+requant
+    -> GEMM -> combine run as separate library calls, bit for bit."""
+    shape = S.WORKLOADS["tiny"]
+    x, logits, w13, w2 = S.moe_inputs(shape, seed=2)
+    ids, w = cuda_lib.moe_route_topk(logits.cuda(), shape.k)
+    pw = cuda_lib.moe_prepare_weights(w13.cuda(), w2.cuda())
+    out, v = _forward(cuda_lib, x.cuda(), ids, w, pw, shape.T, shape.k)
+    p = cuda_lib.moe_permute(ids, shape.E)
+    mcap = v["mcap"]
+    d = torch.empty(mcap, 2 * shape.I, dtype=torch.bfloat16, device="cuda")
+    cuda_lib.nvfp4_grouped_gemm(v["aq"], v["sfa"], v["ga"], pw.w13_codes, pw.w13_sf, pw.w13_g,
+                                p["padded_offsets"], p["counts"], 2 * shape.I, shape.H, shape.E, out=d)
+    n = int(npy(p["padded_offsets"])[-1])
+    live = npy(p["perm"])[:n] >= 0
+    np.testing.assert_array_equal(u16(d)[:n][live], u16(v["d"])[:n][live])
+    _, hq, hsf, gh = cuda_lib.moe_swiglu_quantize(d[:n], p["perm"][:n], shape.I, want_h=False)
+    np.testing.assert_array_equal(npy(hq)[live], npy(v["hq"])[:n][live])
+    y = torch.empty(mcap, shape.H, dtype=torch.bfloat16, device="cuda")
+    hq_full = v["hq"].clone()
+    cuda_lib.nvfp4_grouped_gemm(hq_full, v["sfh"], v["gh"], pw.w2_codes, pw.w2_sf, pw.w2_g,
+                                p["padded_offsets"], p["counts"], shape.H, pw.Ip, shape.E, out=y)
+    np.testing.assert_array_equal(u16(y)[:n][live], u16(v["y"])[:n][live])
+    o2 = cuda_lib.moe_combine(y, p["inv"], w)
+    np.testing.assert_array_equal(u16(o2), u16(out))
+
+
+def test_forward_row_invariance_and_determinism_tiny(cuda_lib):
+    shape = S.WORKLOADS["tiny"]
+    x, logits, w13, w2 = S.moe_inputs(shape, seed=4)
+    ids, w = cuda_lib.moe_route_topk(logits.cuda(), shape.k)
+    pw = cuda_lib.moe_prepare_weights(w13.cuda(), w2.cuda())
+    xc = x.cuda()
+    full = u16(cuda_lib.moe_expert_forward(xc, ids, w, pw))
+    again = u16(cuda_lib.moe_expert_forward(xc, ids, w, pw))
+    np.testing.assert_array_equal(full, again)
+    for lo, hi in [(0, 1), (100, 333), (511, 512)]:
+        part = u16(cuda_lib.moe_expert_forward(xc[lo:hi].contiguous(), ids[lo:hi].contiguous(),
+                                               w[lo:hi].contiguous(), pw))
+        np.testing.assert_array_equal(part, full[lo:hi])
+    # a permuted token order gives the permuted output
+    pidx = torch.randperm(shape.T, generator=torch.Generator().manual_seed(0)).cuda()
+    permuted = u16(cuda_lib.moe_expert_forward(xc[pidx].contiguous(), ids[pidx].contiguous(),
+                                               w[pidx].contiguous(), pw))
+    np.testing.assert_array_equal(permuted, full[npy(pidx)])
+
+
+@pytest.mark.slow
+def test_forward_full_size_sampled_and_row_invariant(cuda_lib):
+    """The Qwen3-30B-A3B-shaped forward (T=16384, H=2048, I=768, E=128, top-8, Zipf
+    routing), in the launch configuration the benchmark times: grouping and per-token
+    quantisation checked in full, GEMM / SwiGLU / requant / down stages on sampled rows,
+    out on sampled tokens; then the first 1024 tokens re-run alone give identical rows."""
+    shape = S.WORKLOADS["forward"]
+    x, logits, w13, w2 = S.moe_inputs(shape, seed=0)
+    ids, w = cuda_lib.moe_route_topk(logits.cuda(), shape.k)
+    rid, rw = M.route_topk(logits.numpy(), shape.k)
+    np.testing.assert_array_equal(npy(ids), rid)
+    pw = cuda_lib.moe_prepare_weights(w13.cuda(), w2.cuda())
+    xc = x.cuda()
+    out, v = _forward(cuda_lib, xc, ids, w, pw, shape.T, shape.k)
+    # grouping and per-token quantisation: everything
+    pi = M.permute(rid, shape.E)
+    n = int(pi["padded_offsets"][-1])
+    np.testing.assert_array_equal(npy(v["inv"]), pi["inv"])
+    np.testing.assert_array_equal(npy(v["perm"])[:n], pi["perm"])
+    xb = S.bf16_bits(x)
+    qx = Q.quantize(xb, scope="row")
+    live = np.nonzero(pi["perm"] >= 0)[0]
+    tok = pi["perm"][live]
+    np.testing.assert_array_equal(npy(v["aq"])[live], qx["packed"][tok])
+    np.testing.assert_array_equal(npy(v["ga"])[live], qx["g"][tok])
+    # sampled routed rows through both GEMMs against the oracle
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(live, 48, replace=False))
+    experts = np.searchsorted(pi["padded_offsets"], sample, side="right") - 1
+    w13b, w2b = S.bf16_bits(w13), S.bf16_bits(w2)
+    src = interleave_src(shape.I)
+    d_all = u16(v["d"])
+    y_all = u16(v["y"])
+    cache = {}
+    for s_row, e in zip(sample, experts):
+        if e not in cache:
+            cache[e] = (Q.quantize(w13b[e], scope="tensor"), Q.quantize(w2b[e], scope="tensor"))
+        q13, q2 = cache[e]
+        t = pi["perm"][s_row]
+        dref = M.gemm_rows(qx["codes"][t:t + 1], qx["sf"][t:t + 1], qx["g"][t:t + 1], q13["codes"], q13["sf"],
+                           q13["g"][0])
+        dg = d_all[s_row:s_row + 1][:, np.argsort(src)]
+        nbad, worst = check_bf16_against(dg, dref)
+        assert nbad == 0, (s_row, worst)
+        dbits = F.bf16_round(dref)
+        if np.array_equal(dg, dbits):
+            hq = Q.quantize(M.swiglu(dbits, shape.I), scope="row")
+            got_hq = F.unpack_e2m1(npy(v["hq"])[s_row:s_row + 1])[:, :shape.I]
+            np.testing.assert_array_equal(got_hq, hq["codes"])
+            yref = M.gemm_rows(hq["codes"], hq["sf"], hq["g"], q2["codes"], q2["sf"], q2["g"][0])
+            nbad, worst = check_bf16_against(y_all[s_row:s_row + 1], yref)
+            assert nbad == 0, (s_row, worst)
+    # sampled tokens end to end
+    toks = [0, 1, 4095, 8191, 16383]
+    sub_e = sorted(set(rid[toks].reshape(-1).tolist()))
+    pref = {"w13_codes": {}, "w13_sf": {}, "w13_g": {}, "w2_codes": {}, "w2_sf": {}, "w2_g": {}}
+    for e in sub_e:
+        q13, q2 = cache.get(e) or (Q.quantize(w13b[e], scope="tensor"), Q.quantize(w2b[e], scope="tensor"))
+        pref["w13_codes"][e], pref["w13_sf"][e], pref["w13_g"][e] = q13["codes"], q13["sf"], q13["g"][0]
+        pref["w2_codes"][e], pref["w2_sf"][e], pref["w2_g"][e] = q2["codes"], q2["sf"], q2["g"][0]
+    oref = M.moe_forward_tokens(xb, rid, rw, pref, toks)
+    got = F.bf16_to_f32(u16(out)[toks]).astype(np.float64)
+    ref = F.bf16_to_f32(oref).astype(np.float64)
+    _, nw = rel_err_floor(got, ref)
+    assert nw < 1e-2, nw
+    # row invariance: the first 1024 tokens alone
+    part = u16(cuda_lib.moe_expert_forward(xc[:1024].contiguous(), ids[:1024].contiguous(),
+                                           w[:1024].contiguous(), pw))
+    np.testing.assert_array_equal(part, u16(out)[:1024])

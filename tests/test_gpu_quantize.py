@@ -1,0 +1,109 @@
+"""GPU parity of the NVFP4 quantiser against the oracle: codes, scales and global scales
+bit for bit, in every scope and rounding mode, including ragged shapes and degenerate
+inputs."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import read_golden
+from gpu_util import bf16_tensor, dev, npy, u16
+from oracle import formats as F
+from oracle import quant as Q
+from nvfp4_w4a4_moe_quantize_gb300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+MODES = {"tensor": 0, "row": 1, "group": 2}
+
+
+def _gpu_quant(lib, bits, scope, rounding="rne", seed=0, off=0, group_rows=0, g_in=None):
+    x = bf16_tensor(bits)
+    codes, sf, g = lib.nvfp4_quantize(x, MODES[scope], 1 if rounding == "sr" else 0, seed, off, group_rows,
+                                      None if g_in is None else dev(np.asarray(g_in, np.float32)))
+    assert lib.nvfp4_status_check() == 0
+    return npy(codes), npy(sf), npy(g)
+
+
+def _compare(lib, bits, scope, rounding="rne", seed=0, off=0, group_rows=0, g_in=None):
+    rows, cols = bits.shape
+    codes, sf, g = _gpu_quant(lib, bits, scope, rounding, seed, off, group_rows, g_in)
+    ref = Q.quantize(bits, scope=scope, rounding=rounding, seed=seed, rng_offset=off,
+                     group_rows=group_rows or None, global_scale_in=g_in)
+    np.testing.assert_array_equal(g[:ref["g"].size], ref["g"])
+    np.testing.assert_array_equal(codes, ref["packed"])
+    np.testing.assert_array_equal(sf, F.sf_swizzle(ref["sf"]))
+    return ref
+
+
+@pytest.mark.parametrize("scope", ["tensor", "row"])
+@pytest.mark.parametrize("shape", [(1, 16), (3, 48), (130, 272), (257, 2048), (64, 4096)])
+def test_quantize_rne_matches_oracle(cuda_lib, scope, shape):
+    bits = S.bf16_bits(S.outlier_channels_bf16(*shape, seed=shape[0] * 7 + shape[1]))
+    _compare(cuda_lib, bits, scope)
+
+
+@pytest.mark.parametrize("shape", [(130, 272), (256, 2048)])
+def test_quantize_sr_matches_oracle(cuda_lib, shape):
+    bits = S.bf16_bits(S.randn_bf16(shape, seed=11))
+    for seed, off in [(0, 0), (0xDEADBEEF12345, 77)]:
+        _compare(cuda_lib, bits, "tensor", "sr", seed, off)
+        _compare(cuda_lib, bits, "row", "sr", seed, off)
+
+
+def test_quantize_group_scope(cuda_lib):
+    bits = S.bf16_bits(S.randn_bf16((4 * 96, 512), 0.02, seed=5))
+    _compare(cuda_lib, bits, "group", group_rows=96)
+
+
+def test_worked_example_on_gpu(cuda_lib):
+    gd = read_golden("quant_worked_example.txt")
+    x = np.array([int(t, 16) for t in gd["x_bf16"].split()], np.uint16).reshape(1, 32)
+    codes, sf, g = _gpu_quant(cuda_lib, x, "row")
+    assert list(codes[0]) == [int(t, 16) for t in gd["packed"].split()]
+    assert list(F.sf_unswizzle(sf, 1, 2)[0]) == [int(t, 16) for t in gd["sf"].split()]
+    assert g[0] == np.float32(float(gd["g"]))
+
+
+def test_every_bf16_value_and_every_tie(cuda_lib):
+    """All finite BF16 patterns, quantised with forced global scales so that every E2M1
+    tie, the saturation region and E4M3 subnormal block scales all occur."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    fin = np.isfinite(F.bf16_to_f32(bits))
+    bits = bits[fin]
+    bits = bits[: bits.size // 256 * 256].reshape(-1, 256)
+    for g in (np.float32(2.0 ** -10), np.float32(1.0), np.float32(1e-20), np.float32(6.0 / 2688)):
+        _compare(cuda_lib, bits, "tensor", g_in=[g])
+        _compare(cuda_lib, bits, "tensor", "sr", 3, 0, g_in=[g])
+    _compare(cuda_lib, bits, "row")
+
+
+def test_degenerate_rows(cuda_lib):
+    bits = np.zeros((5, 64), np.uint16)
+    bits[1] = 0x0001                         # smallest subnormal
+    bits[2, ::3] = 0x8000                    # negative zeros
+    bits[3] = F.bf16_round(np.linspace(-1e-38, 1e-38, 64))
+    bits[4, 7] = 0x7F7F                      # largest finite BF16
+    for scope in ("row", "tensor"):
+        _compare(cuda_lib, bits, scope)
+
+
+def test_quantize_is_deterministic(cuda_lib):
+    bits = S.bf16_bits(S.randn_bf16((512, 2048), seed=21))
+    a = _gpu_quant(cuda_lib, bits, "tensor", "sr", 5)
+    b = _gpu_quant(cuda_lib, bits, "tensor", "sr", 5)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
+
+
+def test_quantiser_workload_full_size(cuda_lib):
+    """The standalone-quantiser workload at full size (16384 x 2048, 1% outlier channels),
+    per-tensor scale, RNE and SR, against the oracle over the whole tensor."""
+    bits = S.bf16_bits(S.outlier_channels_bf16(*S.QUANTISER_SHAPE, seed=0))
+    _compare(cuda_lib, bits, "tensor")
+    _compare(cuda_lib, bits, "tensor", "sr", 0, 0)
+
+
+def test_bad_arguments_raise(cuda_lib):
+    x = torch.zeros(4, 24, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cuda_lib.NVFP4Error):
+        cuda_lib.nvfp4_quantize(x)
