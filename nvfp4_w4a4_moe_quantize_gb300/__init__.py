@@ -179,11 +179,14 @@ def nvfp4_grouped_gemm(A, SFA, gA, B, SFB, gB, group_offsets, group_rows, N: int
 
 # --------------------------------------------------------------------------- MoE helpers
 
-def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool = True, stream=None):
+def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool = True, out=None, stream=None):
     lib = load()
     T, E = logits.shape
-    ids = torch.empty(T, k, dtype=torch.int32, device=_dev(logits))
-    w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    if out is None:
+        ids = torch.empty(T, k, dtype=torch.int32, device=_dev(logits))
+        w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    else:
+        ids, w = out
     _check(lib.moe_route_topk(_p(logits.contiguous()), T, E, k, int(renormalize), _p(ids), _p(w),
                               _stream(stream)), "moe_route_topk")
     return ids, w

@@ -213,9 +213,10 @@ def moe_forward(x_bits, topk_ids, topk_w, w13_bits, w2_bits, prepared=None, num_
 
 def moe_forward_tokens(x_bits, topk_ids, topk_w, prepared, tokens):
     """out rows for a subset of tokens only, computed token by token (bounded CPU sample
-    of a large workload; each token's result does not depend on the others)."""
+    of a large workload; each token's result does not depend on the others).
+    ``prepared`` maps each weight field to something indexable by expert id (the arrays
+    of prepare_weights, or dicts holding only the experts the tokens use)."""
     H = x_bits.shape[1]
-    I = prepared["w2_codes"].shape[2]
     out = np.zeros((len(tokens), H), np.uint16)
     for n, t in enumerate(tokens):
         q = Q.quantize(x_bits[t:t + 1], scope="row")
@@ -225,7 +226,7 @@ def moe_forward_tokens(x_bits, topk_ids, topk_w, prepared, tokens):
             d = gemm_rows(q["codes"], q["sf"], q["g"], prepared["w13_codes"][e],
                           prepared["w13_sf"][e], prepared["w13_g"][e])
             d_bits = F.bf16_round(d)
-            h_bits = swiglu(d_bits, I)
+            h_bits = swiglu(d_bits, d.shape[1] // 2)
             hq = Q.quantize(h_bits, scope="row")
             y = gemm_rows(hq["codes"], hq["sf"], hq["g"], prepared["w2_codes"][e],
                           prepared["w2_sf"][e], prepared["w2_g"][e])
