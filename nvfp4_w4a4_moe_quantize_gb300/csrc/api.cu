@@ -50,16 +50,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// 2-D map over a [rows, row_bytes] byte matrix, box = 128 bytes x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, uint32_t box_rows) {
+// 2-D map over a [rows, cols] matrix of `elt`-byte elements with row pitch `pitch_bytes`;
+// box = 128 bytes x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t pitch_bytes, uint32_t box_rows,
+              CUtensorMapDataType dt, int elt) {
   auto enc = encoder();
   if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {128u, box_rows};
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)pitch_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), box_rows};
   cuuint32_t es[2] = {1u, 1u};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -104,8 +106,11 @@ ForwardLayout forward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t
 nvfp4_status gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const uint8_t* B, const uint8_t* SFB,
                   const float* gB, const int32_t* offsets, const int32_t* rows, int64_t M_total, int64_t N, int64_t K,
                   int32_t E, void* D, int out_f32, int64_t ldd, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, A, M_total, K / 2, 128) || !make_map(&mb, B, (int64_t)E * N, K / 2, 128))
+  CUtensorMap ma, mb, md;
+  if (!make_map(&ma, A, M_total, K / 2, K / 2, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
+      !make_map(&mb, B, (int64_t)E * N, K / 2, K / 2, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
+      !make_map(&md, D, M_total, N, ldd * (out_f32 ? 4 : 2), 32,
+                out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_f32 ? 4 : 2))
     return NVFP4_ERR_CUDA;
   GemmArgs g;
   g.sfa = SFA;
@@ -121,7 +126,7 @@ nvfp4_status gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const u
   g.ldd = ldd;
   g.out_f32 = out_f32;
   g.status = device_status_ptr();
-  return from_cuda(launch_grouped_gemm(ma, mb, g, M_total / 128, s));
+  return from_cuda(launch_grouped_gemm(ma, mb, md, g, M_total / 128, s));
 }
 
 }  // namespace

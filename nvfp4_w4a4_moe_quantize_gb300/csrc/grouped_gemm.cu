@@ -15,7 +15,9 @@
 //           K=64) into a TMEM accumulator; tcgen05.commit frees the stage.  Two
 //           accumulators let the epilogue of one tile overlap the main loop of the next.
 //   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns, scale by gA[r] * gB[e] in
-//           float32, round to BF16 (or keep float32), store rows of the group only.
+//           float32, round to BF16 (or keep float32); whole 32-row blocks of a group go
+//           through a swizzled shared-memory box and a TMA store, the last partial block
+//           of a group is stored row by row, so rows outside the groups are never written.
 // Tiles are (128-row block of the padded group layout) x (128 output columns); tile t
 // is row block t / (N/128), column block t % (N/128), so CTAs running at the same time
 // share A tiles and one expert's weights in L2.  The K loop has a fixed order and no
@@ -33,7 +35,7 @@ namespace gg {
 constexpr int kBM = 128;          // rows per tile (one per TMEM lane)
 constexpr int kBN = 128;          // output columns per tile
 constexpr int kBKBytes = 128;     // K bytes per stage = 256 FP4 values (one 128-byte swizzle row)
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kABytes = kBM * kBKBytes;
 constexpr int kBBytes = kBN * kBKBytes;
 constexpr int kSFABytes = 4 * 512;           // 4 k-groups of 64 x 128 rows
@@ -43,14 +45,17 @@ constexpr int kTmemCols = 512;
 constexpr int kAccCols = kBN;                // one accumulator: 128 lanes x kBN float32
 constexpr int kSFCol0 = 2 * kAccCols;        // scale factors after the two accumulators
 constexpr int kSFStageCols = 16 + 4 * 4 * (kBN / 128);
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxE = 1024;
+constexpr int kOutBox = 32 * 128;            // one 32-row x 128-byte swizzled store box
 
 struct Smem {
   uint8_t a[kStages][kABytes];
   uint8_t b[kStages][kBBytes];
   uint8_t sfa[kStages][kSFABytes];
   uint8_t sfb[kStages][kSFBBytes];
+  uint8_t out[kEpiWarps][2][kOutBox];        // double-buffered store staging per epilogue warp
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t accf[2];
@@ -58,6 +63,8 @@ struct Smem {
   uint32_t tmem_base;
   int abort;
   int32_t offsets[kMaxE + 1];
+  int32_t rows[kMaxE];
+  float gb[kMaxE];
 };
 static_assert(kSFCol0 + kStages * kSFStageCols <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
@@ -76,13 +83,17 @@ __device__ __forceinline__ int find_group(const int32_t* off, int E, int32_t row
 
 __global__ void __launch_bounds__(gg::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
-                        const GemmArgs g) {
+                        const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
   using namespace gg;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
+  for (int i = threadIdx.x; i < g.E; i += blockDim.x) {
+    sm.rows[i] = g.rows[i];
+    sm.gb[i] = g.gb[i];
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -90,7 +101,7 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sm.accf[a], 1);
-      mbar_init(&sm.acce[a], 4 * 32);
+      mbar_init(&sm.acce[a], kEpiWarps * 32);
     }
     sm.abort = 0;
     fence_mbar_init();
@@ -98,6 +109,7 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tma);
     prefetch_tensormap(&tmb);
+    prefetch_tensormap(&tmd);
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -184,59 +196,90 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
     mma_done:;
     }
   } else {
-    // epilogue: warps 2..5; TMEM lane quadrant = warp % 4
+    // epilogue: warps 2..5; TMEM lane quadrant = warp % 4.  Each warp owns 32 rows of the
+    // tile.  When all 32 rows belong to the group, the rows are staged in a 128-byte
+    // swizzled shared-memory box and written by a TMA store (full lines); otherwise the
+    // valid rows are stored thread by thread, so rows outside the groups stay untouched.
     const int q = warp & 3;
+    const int ew = warp - 2;
+    const int elt = g.out_f32 ? 4 : 2;
+    const int box_cols = 128 / elt;
+    uint32_t cur = 0;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const uint32_t acc = it & 1, acc_phase = (it >> 1) & 1;
-      if (!mbar_wait(&sm.accf[acc], acc_phase, g.status, abort)) break;
-      tc_fence_after();
       const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
       const int32_t row0 = m_tile * kBM;
       const int e = find_group(sm.offsets, g.E, row0);
-      const int32_t r_in_group = row0 - sm.offsets[e] + q * 32 + lane;
-      const bool valid = r_in_group < g.rows[e];
+      const int32_t in_group = sm.rows[e] - (row0 - sm.offsets[e]);   // valid rows of this tile
+      const bool valid = q * 32 + lane < in_group;
+      const bool full_warp = q * 32 + 32 <= in_group;
       const int64_t row = (int64_t)row0 + q * 32 + lane;
-      const float scale = valid ? __fmul_rn(g.ga[row], g.gb[e]) : 0.0f;
+      const float ga = valid ? g.ga[row] : 0.0f;                        // load before the wait
+      if (!mbar_wait(&sm.accf[acc], acc_phase, g.status, abort)) break;
+      tc_fence_after();
+      const float scale = __fmul_rn(ga, sm.gb[e]);
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
 #pragma unroll 1
       for (int c0 = 0; c0 < kBN; c0 += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + c0, v);
         tmem_ld_wait();
-        if (valid) {
-          const int64_t n0 = (int64_t)n_tile * kBN + c0;
-          if (g.out_f32) {
-            float* dp = static_cast<float*>(g.d) + row * g.ldd + n0;
+        if (c0 + 32 == kBN) {   // accumulator fully read: hand it back to the MMA warp
+          tc_fence_before();
+          mbar_arrive(&sm.acce[acc]);
+        }
+        const int64_t n0 = (int64_t)n_tile * kBN + c0;
+        uint32_t w[32];
+        int nw;
+        if (g.out_f32) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              float4 o;
-              o.x = __fmul_rn(__uint_as_float(v[4 * u + 0]), scale);
-              o.y = __fmul_rn(__uint_as_float(v[4 * u + 1]), scale);
-              o.z = __fmul_rn(__uint_as_float(v[4 * u + 2]), scale);
-              o.w = __fmul_rn(__uint_as_float(v[4 * u + 3]), scale);
-              *reinterpret_cast<float4*>(dp + 4 * u) = o;
-            }
-          } else {
-            __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(g.d) + row * g.ldd + n0;
+          for (int u = 0; u < 32; ++u) w[u] = __float_as_uint(__fmul_rn(__uint_as_float(v[u]), scale));
+          nw = 32;
+        } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint32_t w[4];
+          for (int u = 0; u < 16; ++u) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * u]), scale),
+                                                            __fmul_rn(__uint_as_float(v[2 * u + 1]), scale));
+            w[u] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          nw = 16;
+        }
+        if (full_warp) {
+          const int boff = (c0 * elt) & 127;        // byte offset of this chunk inside its box row
+          if (boff == 0) {
+            if (lane == 0) bulk_wait_read<1>();   // the group that last read this buffer is done
+            __syncwarp();
+          }
+          uint8_t* buf = sm.out[ew][cur];
 #pragma unroll
-              for (int p = 0; p < 4; ++p) {
-                const __nv_bfloat162 b2 =
-                    __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[8 * u + 2 * p]), scale),
-                                          __fmul_rn(__uint_as_float(v[8 * u + 2 * p + 1]), scale));
-                w[p] = *reinterpret_cast<const uint32_t*>(&b2);
-              }
-              *reinterpret_cast<uint4*>(dp + 8 * u) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int u = 0; u < 8; ++u) {
+            if (u * 4 < nw) {
+              const int j = (boff >> 4) + u;
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                  make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
             }
           }
+          if (boff + 32 * elt == 128) {   // box complete: hand it to the TMA engine
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmd, buf, (int32_t)(n0 + 32 - box_cols), row0 + q * 32);
+              bulk_commit();
+            }
+            cur ^= 1u;
+          }
+        } else if (valid) {
+          uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + n0) * elt;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u * 4 < nw)
+              *reinterpret_cast<uint4*>(dp + 16 * u) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&sm.acce[acc]);
     }
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -245,8 +288,8 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
-                                int64_t max_m_tiles, cudaStream_t s) {
+cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
+                                const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
   static bool attr_set[64] = {};   // the attribute is set once per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -260,7 +303,7 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, 
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
-  grouped_gemm_kernel<<<grid, gg::kThreads, gg::kSmemBytes, s>>>(tma, tmb, g);
+  grouped_gemm_kernel<<<grid, gg::kThreads, gg::kSmemBytes, s>>>(tma, tmb, tmd, g);
   return cudaGetLastError();
 }
 

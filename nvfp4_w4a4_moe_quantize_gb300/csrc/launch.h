@@ -56,8 +56,8 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, i
 cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s);
 
 // Grouped GEMM: tensor maps are built by the caller (api.cu).
-cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
-                                int64_t max_m_tiles, cudaStream_t s);
+cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
+                                const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s);
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renorm, int32_t* ids,
                               float* w, cudaStream_t s);

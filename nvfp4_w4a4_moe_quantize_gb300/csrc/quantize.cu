@@ -17,6 +17,7 @@
 
 #include "encode.cuh"
 #include "launch.h"
+#include "ptx.cuh"
 #include "status.cuh"
 
 namespace nvfp4 {
@@ -82,6 +83,41 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
   }
 }
 
+// Max |x| of a contiguous tensor seen as n16 16-byte chunks: four independent loads in
+// flight per thread, one atomicMax per block.
+__global__ void __launch_bounds__(256) amax_flat_kernel(const uint4* __restrict__ x, int64_t n16,
+                                                        uint32_t* amax_bits) {
+  float m = 0.0f;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = ld_nc_v4(x + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float f[8];
+      bf16x8_to_f32(v[u], f);
+      m = fmaxf(m, absmax8(f));
+    }
+  }
+  for (; i < n16; i += stride) {
+    float f[8];
+    bf16x8_to_f32(ld_nc_v4(x + i), f);
+    m = fmaxf(m, absmax8(f));
+  }
+  m = warp_max(m);
+  __shared__ float sm[8];
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) sm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = sm[0];
+    for (int k = 1; k < 8; ++k) b = fmaxf(b, sm[k]);
+    if (b > 0.0f) atomicMax(&amax_bits[0], __float_as_uint(b));
+  }
+}
+
 // ------------------------------------------------------------------ row quantiser
 
 __device__ __forceinline__ int64_t interleave_row(int64_t r, int64_t I) {
@@ -96,98 +132,168 @@ __device__ __forceinline__ int64_t interleave_row(int64_t r, int64_t I) {
   return e * n2 + o;
 }
 
+// Encode one input row held in registers (lane l owns the 16-byte chunks at columns
+// 8l + 256i) and write its codes, scale words and global scale to every output row.
+template <int RND, int MAXC>
+__device__ __forceinline__ void quantize_row(const QuantArgs& a, int64_t row, const uint4 (&q)[MAXC], int lane) {
+  const int64_t data_words = (a.cols + 63) / 64;
+  float bm[MAXC];
+  float rmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < MAXC; ++i) {
+    float f[8];
+    bf16x8_to_f32(q[i], f);
+    const float cm = absmax8(f);
+    bm[i] = fmaxf(cm, __shfl_xor_sync(kFull, cm, 1));
+    rmax = fmaxf(rmax, bm[i]);
+  }
+  float g;
+  if (a.mode == kScopeRow) {
+    rmax = warp_max(rmax);
+    g = a.g_in ? a.g_in[row] : __fdiv_rn(rmax, kGlobalDivisor);
+  } else if (a.mode == kScopeTensor) {
+    g = a.g_in ? a.g_in[0] : __fdiv_rn(__uint_as_float(a.amax_bits[0]), kGlobalDivisor);
+  } else {
+    const int64_t gi = row / a.group_rows;
+    g = a.g_in ? a.g_in[gi] : __fdiv_rn(__uint_as_float(a.amax_bits[gi]), kGlobalDivisor);
+  }
+  const float six_g = __fmul_rn(6.0f, g);
+
+  const int nout = a.map == kMapScatter ? a.k : 1;
+  const int64_t orow0 = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
+  int32_t my_slot = 0;
+  if (a.map == kMapScatter && lane < a.k) my_slot = a.inv[row * a.k + lane];
+
+#pragma unroll
+  for (int i = 0; i < MAXC; ++i) {
+    const int64_t col = 8 * lane + 256 * i;
+    const bool active = col < a.cols;
+    const BlockScale bs = block_scale(bm[i], g, six_g);
+    float f[8], v[8];
+    bf16x8_to_f32(q[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(f[e], bs.r);
+    uint32_t word;
+    if (RND == kRoundSR) {
+      const uint64_t j = a.rng_offset + (uint64_t)(row * a.cols + col) / 8u;
+      const uint4 rnd = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), (uint32_t)a.seed,
+                                      (uint32_t)(a.seed >> 32));
+      word = e2m1x8_sr(v, rnd);
+    } else {
+      word = e2m1x8_rn(v);
+    }
+    const uint32_t sfb = active ? bs.sf : 0u;
+    const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
+    const uint32_t s4 = __shfl_down_sync(kFull, sfb, 4);
+    const uint32_t s6 = __shfl_down_sync(kFull, sfb, 6);
+    const uint32_t sfw = sfb | (s2 << 8) | (s4 << 16) | (s6 << 24);
+    for (int j = 0; j < nout; ++j) {
+      const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
+      if (orow < 0) continue;   // entry whose expert id was rejected: no slot
+      if (active) *reinterpret_cast<uint32_t*>(a.codes + orow * a.codes_ld + col / 2) = word;
+      if ((lane & 7) == 0 && active)
+        *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, 4 * i + lane / 8, a.sf_words)) = sfw;
+    }
+  }
+  for (int j = 0; j < nout; ++j) {
+    const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
+    if (orow < 0) continue;
+    for (int64_t w = data_words + lane; w < a.sf_words; w += 32)
+      *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, w, a.sf_words)) = 0u;
+    for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
+      *reinterpret_cast<uint2*>(a.codes + orow * a.codes_ld + b) = make_uint2(0u, 0u);
+    if (lane == 0 && a.g_out != nullptr) {
+      if (a.mode == kScopeRow) a.g_out[a.map == kMapScatter ? orow : row] = g;
+      else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
+      else if (a.mode == kScopeGroup && row % a.group_rows == 0) a.g_out[row / a.group_rows] = g;
+    }
+  }
+}
+
+// Zero scale words of the tile-grid padding rows (rows .. rows_total - 1).
+__device__ __forceinline__ void zero_pad_rows(const QuantArgs& a, int64_t warp, int64_t nwarp, int lane) {
+  for (int64_t row = a.rows + warp; row < a.rows_total; row += nwarp)
+    for (int64_t w = lane; w < a.sf_words; w += 32)
+      *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(row, w, a.sf_words)) = 0u;
+}
+
+// Register path (any width up to 8192 columns): the warp loads its row straight into
+// registers.
 template <int RND, int MAXC>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(QuantArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t nwarp = (int64_t)gridDim.x * 8;
-  const int64_t data_words = (a.cols + 63) / 64;
-
-  for (int64_t row = warp; row < a.rows_total; row += nwarp) {
-    if (row >= a.rows) {  // padding row of the tile grid: its scales are zero
-      for (int64_t w = lane; w < a.sf_words; w += 32)
-        *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(row, w, a.sf_words)) = 0u;
-      continue;
-    }
+  for (int64_t row = warp; row < a.rows; row += nwarp) {
     uint4 q[MAXC];
-    float bm[MAXC];
     const __nv_bfloat16* xr = a.x + row * a.ld;
 #pragma unroll
     for (int i = 0; i < MAXC; ++i) {
       const int64_t col = 8 * lane + 256 * i;
       q[i] = col < a.cols ? ld_nc_v4(xr + col) : make_uint4(0, 0, 0, 0);
     }
-    float rmax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-      float f[8];
-      bf16x8_to_f32(q[i], f);
-      const float cm = absmax8(f);
-      bm[i] = fmaxf(cm, __shfl_xor_sync(kFull, cm, 1));
-      rmax = fmaxf(rmax, bm[i]);
-    }
-    float g;
-    if (a.mode == kScopeRow) {
-      rmax = warp_max(rmax);
-      g = a.g_in ? a.g_in[row] : __fdiv_rn(rmax, kGlobalDivisor);
-    } else if (a.mode == kScopeTensor) {
-      g = a.g_in ? a.g_in[0] : __fdiv_rn(__uint_as_float(a.amax_bits[0]), kGlobalDivisor);
-    } else {
-      const int64_t gi = row / a.group_rows;
-      g = a.g_in ? a.g_in[gi] : __fdiv_rn(__uint_as_float(a.amax_bits[gi]), kGlobalDivisor);
-    }
-    const float six_g = __fmul_rn(6.0f, g);
+    quantize_row<RND, MAXC>(a, row, q, lane);
+  }
+  zero_pad_rows(a, warp, nwarp, lane);
+}
 
-    const int nout = a.map == kMapScatter ? a.k : 1;
-    const int64_t orow0 = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
-    int32_t my_slot = 0;
-    if (a.map == kMapScatter && lane < a.k) my_slot = a.inv[row * a.k + lane];
+// Streaming path (rows up to 2048 columns): every warp keeps kQStages rows in flight in
+// a shared-memory ring filled by bulk async copies (cp.async.bulk, completion on an
+// mbarrier), so HBM sees several rows per warp while the warp encodes the current one.
+constexpr int kQStages = 4;
+constexpr int kQRowBytes = 4096;
+constexpr size_t kQSmem = 8 * kQStages * kQRowBytes + 8 * kQStages * sizeof(uint64_t) + 16;
 
-#pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-      const int64_t col = 8 * lane + 256 * i;
-      const bool active = col < a.cols;
-      const BlockScale bs = block_scale(bm[i], g, six_g);
-      float f[8], v[8];
-      bf16x8_to_f32(q[i], f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(f[e], bs.r);
-      uint32_t word;
-      if (RND == kRoundSR) {
-        const uint64_t j = a.rng_offset + (uint64_t)(row * a.cols + col) / 8u;
-        const uint4 rnd = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u),
-                                        (uint32_t)a.seed, (uint32_t)(a.seed >> 32));
-        word = e2m1x8_sr(v, rnd);
-      } else {
-        word = e2m1x8_rn(v);
-      }
-      const uint32_t sfb = active ? bs.sf : 0u;
-      const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
-      const uint32_t s4 = __shfl_down_sync(kFull, sfb, 4);
-      const uint32_t s6 = __shfl_down_sync(kFull, sfb, 6);
-      const uint32_t sfw = sfb | (s2 << 8) | (s4 << 16) | (s6 << 24);
-      for (int j = 0; j < nout; ++j) {
-        const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
-        if (orow < 0) continue;   // entry whose expert id was rejected: no slot
-        if (active) *reinterpret_cast<uint32_t*>(a.codes + orow * a.codes_ld + col / 2) = word;
-        if ((lane & 7) == 0 && active)
-          *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, 4 * i + lane / 8, a.sf_words)) = sfw;
-      }
-    }
-    for (int j = 0; j < nout; ++j) {
-      const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
-      if (orow < 0) continue;
-      for (int64_t w = data_words + lane; w < a.sf_words; w += 32)
-        *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, w, a.sf_words)) = 0u;
-      for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
-        *reinterpret_cast<uint2*>(a.codes + orow * a.codes_ld + b) = make_uint2(0u, 0u);
-      if (lane == 0 && a.g_out != nullptr) {
-        if (a.mode == kScopeRow) a.g_out[a.map == kMapScatter ? orow : row] = g;
-        else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
-        else if (a.mode == kScopeGroup && row % a.group_rows == 0) a.g_out[row / a.group_rows] = g;
+template <int RND, int MAXC>
+__global__ void __launch_bounds__(256, 1) quantize_rows_stream_kernel(QuantArgs a) {
+  extern __shared__ __align__(128) uint8_t qsm[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + wib;
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  uint8_t* ring = qsm + (size_t)wib * kQStages * kQRowBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + 8 * kQStages * kQRowBytes) + wib * kQStages;
+  volatile int* abort = reinterpret_cast<volatile int*>(qsm + 8 * kQStages * kQRowBytes + 8 * kQStages * 8);
+  if (threadIdx.x == 0) *abort = 0;
+  const uint32_t row_bytes = (uint32_t)(a.cols * 2);
+  if (lane == 0) {
+    for (int s = 0; s < kQStages; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (lane == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      const int64_t r = warp + s * nwarp;
+      if (r < a.rows) {
+        mbar_arrive_expect_tx(&bars[s], row_bytes);
+        bulk_load(ring + s * kQRowBytes, a.x + r * a.ld, row_bytes, &bars[s]);
       }
     }
   }
+  uint32_t parity = 0;
+  int s = 0;
+  for (int64_t row = warp; row < a.rows; row += nwarp) {
+    if (!mbar_wait(&bars[s], (parity >> s) & 1u, a.status, abort)) break;
+    parity ^= 1u << s;
+    uint4 q[MAXC];
+    const uint8_t* buf = ring + s * kQRowBytes;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int64_t col = 8 * lane + 256 * i;
+      q[i] = col < a.cols ? *reinterpret_cast<const uint4*>(buf + col * 2) : make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();   // reads of this buffer precede the next bulk write into it
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t r2 = row + (int64_t)kQStages * nwarp;
+      if (r2 < a.rows) {
+        mbar_arrive_expect_tx(&bars[s], row_bytes);
+        bulk_load(ring + s * kQRowBytes, a.x + r2 * a.ld, row_bytes, &bars[s]);
+      }
+    }
+    quantize_row<RND, MAXC>(a, row, q, lane);
+    s = s + 1 == kQStages ? 0 : s + 1;
+  }
+  zero_pad_rows(a, warp, nwarp, lane);
 }
 
 template <int RND>
@@ -203,12 +309,44 @@ static cudaError_t launch_quant_rnd(const QuantArgs& a, int maxc, int grid, cuda
   return cudaGetLastError();
 }
 
+template <int RND, int MAXC>
+static cudaError_t launch_stream(const QuantArgs& a, int grid, cudaStream_t s) {
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(quantize_rows_stream_kernel<RND, MAXC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr[dev] = true;
+  }
+  quantize_rows_stream_kernel<RND, MAXC><<<grid, 256, kQSmem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int RND>
+static cudaError_t launch_stream_rnd(const QuantArgs& a, int maxc, int grid, cudaStream_t s) {
+  switch (maxc) {
+    case 1: return launch_stream<RND, 1>(a, grid, s);
+    case 2: return launch_stream<RND, 2>(a, grid, s);
+    case 4: return launch_stream<RND, 4>(a, grid, s);
+    default: return launch_stream<RND, 8>(a, grid, s);
+  }
+}
+
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t group_rows,
                         uint32_t* amax_bits, int64_t n_scopes, cudaStream_t s) {
   cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t) * n_scopes, s);
   if (err != cudaSuccess) return err;
   if (rows == 0) return cudaSuccess;
   const int sms = num_sms();
+  if (group_rows == 0 && ld == cols) {   // one scope over contiguous rows: flat pass
+    const int64_t n16 = rows * cols / 8;
+    int64_t blocks = (n16 + 255) / 256;
+    if (blocks > 4 * sms) blocks = 4 * sms;
+    amax_flat_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(x), n16, amax_bits);
+    return cudaGetLastError();
+  }
   int64_t blocks = (rows + 7) / 8;
   if (blocks > 4 * sms) blocks = 4 * sms;
   amax_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, group_rows,
@@ -222,6 +360,12 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
   while (maxc * 256 < a.cols) maxc *= 2;
   const int sms = num_sms();
   int64_t blocks = (a.rows_total + 7) / 8;
+  // rows of up to 2048 columns whose pitch keeps every row 16-byte aligned: streaming path
+  if (maxc <= 8 && (a.ld * 2) % 16 == 0) {
+    if (blocks > sms) blocks = sms;
+    return rounding == kRoundSR ? launch_stream_rnd<kRoundSR>(a, maxc, (int)blocks, s)
+                                : launch_stream_rnd<kRoundRNE>(a, maxc, (int)blocks, s);
+  }
   const int64_t cap = (int64_t)(maxc <= 8 ? 8 : 4) * sms;
   if (blocks > cap) blocks = cap;
   return rounding == kRoundSR ? launch_quant_rnd<kRoundSR>(a, maxc, (int)blocks, s)

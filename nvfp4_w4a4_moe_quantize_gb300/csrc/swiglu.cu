@@ -6,12 +6,13 @@
 // recipe not sufficient for RL?": per-token activation scales).
 //
 // h = BF16(silu(gate) * up) is the BF16 value nearest to the exact real number.  The
-// float32 evaluation (expf <= 2 ulp, three correctly rounded operations) is within
-// 7 ulps of it; when that float32 value lies within 64 ulps of a BF16 rounding midpoint,
-// or outside the range where the bound holds, h is recomputed in float64 and rounded
-// once to BF16 through a round-to-odd float32 step.  The result equals the rounding of
-// the exact value except when the exact value sits within ~1e-15 (relative) of a
-// midpoint, which silu(g)*u with g != 0 never reaches exactly.
+// float32 evaluation h32 = (g * rcp(1 + expf(-g))) * u (expf within 2 ulp, four correctly
+// rounded operations) has relative error below 2^-22 + 4 * 2^-24, i.e. under 8 ulps of
+// h32; when h32 lies within 16 ulps of a BF16 rounding midpoint, or outside the range
+// where the bound holds, h is recomputed in float64 and rounded once to BF16 through a
+// round-to-odd float32 step.  The result equals the rounding of the exact value except
+// when the exact value sits within ~1e-15 (relative) of a midpoint, which silu(g)*u
+// with g != 0 never reaches exactly.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -43,13 +44,13 @@ __device__ __noinline__ uint32_t swiglu_f64(float g, float u) {
 
 __device__ __forceinline__ uint32_t swiglu_bf16(float g, float u) {
   const float e = expf(-g);
-  const float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), u);
+  const float h = __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, e))), u);
   const uint32_t b = __float_as_uint(h);
   const uint32_t low = b & 0xFFFFu;
   const float ah = fabsf(h);
   const bool exact_zero = (g == 0.0f) || (u == 0.0f);
   const bool in_range = ah >= 1e-30f && ah <= 1e30f && e <= 3.0e38f;
-  const bool near_mid = low >= 0x8000u - 64u && low <= 0x8000u + 64u;
+  const bool near_mid = low >= 0x8000u - 16u && low <= 0x8000u + 16u;
   if (exact_zero || (in_range && !near_mid)) return f32_to_bf16_rne_bits(b);
   return swiglu_f64(g, u);
 }
@@ -145,6 +146,7 @@ cudaError_t launch_swiglu_quant(const void* d, const int32_t* perm, int64_t rows
   auto* hp = static_cast<__nv_bfloat16*>(h_out);
   if (I <= 256) swiglu_quant_kernel<1><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
   else if (I <= 512) swiglu_quant_kernel<2><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
+  else if (I <= 768) swiglu_quant_kernel<3><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
   else if (I <= 1024) swiglu_quant_kernel<4><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
   else if (I <= 2048) swiglu_quant_kernel<8><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
   else swiglu_quant_kernel<16><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
