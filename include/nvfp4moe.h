@@ -134,6 +134,26 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
                             float* global_scale_out, uint8_t* codes_out, uint8_t* sf_out,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same quantisation as nvfp4_quantize, for callers that cannot allocate device
+ * memory (for example a host plug-in that is handed only the tensors it reads and
+ * writes, with no allocator or memory pool it may use).  The pages have no counterpart:
+ * it is a deployment convenience, not part of the method.
+ *   Same arguments as nvfp4_quantize without the workspace.  The amax scratch of the
+ *   per-tensor and per-group modes lives in a fixed 16 KB device array owned by the
+ *   library (at most 4096 scopes: per-group calls with more than 4096 groups and no
+ *   global_scale_in return NVFP4_ERR_UNSUPPORTED).  Every GPU that loads the library
+ *   holds that array until the process exits.
+ *   The first call on each device resolves the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ *   All calls share the one array and each call clears the words it uses before use:
+ *   calls whose kernels overlap on the GPU (different streams, no ordering) race on it.
+ *   The library calls no allocator (no cudaMalloc / cudaFree) here. */
+nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld_elems,
+                                    nvfp4_scale_mode mode, int64_t group_rows,
+                                    nvfp4_rounding rounding, uint64_t seed, uint64_t rng_offset,
+                                    const float* global_scale_in, float* global_scale_out,
+                                    uint8_t* codes_out, uint8_t* sf_out, void* stream);
+
 /* ---------------------------------------------------------------- grouped GEMM */
 
 /* W4A4 grouped GEMM over ragged expert groups ("Low-Bit Precision Training Is Ready

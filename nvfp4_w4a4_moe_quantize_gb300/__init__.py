@@ -18,7 +18,7 @@ from . import build as _build
 
 __all__ = [
     "load", "library_path", "Status", "NVFP4Error",
-    "nvfp4_quantize", "nvfp4_grouped_gemm", "moe_route_topk", "moe_permute", "moe_combine",
+    "nvfp4_quantize", "nvfp4_quantize_noalloc", "nvfp4_grouped_gemm", "moe_route_topk", "moe_permute", "moe_combine",
     "moe_swiglu_quantize", "moe_prepare_weights", "moe_expert_forward", "moe_forward_workspace",
     "moe_forward_workspace_layout", "nvfp4_status_check", "nvfp4_sf_bytes", "NVFP4MoEWeights",
     "SCALE_PER_TENSOR", "SCALE_PER_ROW", "SCALE_PER_GROUP", "ROUND_RNE", "ROUND_STOCHASTIC",
@@ -56,6 +56,8 @@ _SIGS = {
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_quantize": (ctypes.c_int, [_vp, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int, _u64, _u64,
                                       _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "nvfp4_quantize_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int, _u64, _u64,
+                                              _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                           _vp, ctypes.c_int, _i64, _vp]),
     "moe_route_topk": (ctypes.c_int, [_vp, _i64, _i32, _i32, ctypes.c_int, _vp, _vp, _vp]),
@@ -158,6 +160,28 @@ def nvfp4_quantize(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, rounding: int 
     _check(lib.nvfp4_quantize(_p(x), rows, cols, x.stride(0), mode, group_rows, rounding, seed, rng_offset,
                               _p(global_scale), _p(g), _p(codes), _p(sf), _p(workspace), workspace.numel(),
                               _stream(stream)), "nvfp4_quantize")
+    return codes, sf, g
+
+
+def nvfp4_quantize_noalloc(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, rounding: int = ROUND_RNE,
+                           seed: int = 0, rng_offset: int = 0, group_rows: int = 0,
+                           global_scale: torch.Tensor | None = None, out=None, stream=None):
+    """nvfp4_quantize without a workspace: the library keeps the amax scratch in its own
+    fixed device array (for callers that cannot allocate).  Outputs as nvfp4_quantize."""
+    lib = load()
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    dev = _dev(x)
+    n_g = 1 if mode == SCALE_PER_TENSOR else (rows if mode == SCALE_PER_ROW else rows // max(group_rows, 1))
+    if out is None:
+        codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
+        sf = torch.empty(max(nvfp4_sf_bytes(rows, cols), 16), dtype=torch.uint8, device=dev)
+        g = torch.empty(max(n_g, 1), dtype=torch.float32, device=dev)
+    else:
+        codes, sf, g = out
+    _check(lib.nvfp4_quantize_noalloc(_p(x), rows, cols, x.stride(0), mode, group_rows, rounding, seed, rng_offset,
+                                      _p(global_scale), _p(g), _p(codes), _p(sf), _stream(stream)),
+           "nvfp4_quantize_noalloc")
     return codes, sf, g
 
 
