@@ -232,25 +232,20 @@ def run_ours(args, rank, world, local_rank):
         nbytes = n * torch.empty((), dtype=dtype).element_size()
         return ws[lay[i]:lay[i] + nbytes].view(dtype)
     counts, padded = view(0, E, torch.int32), view(2, E + 1, torch.int32)
-    inv, perm = view(3, T * k, torch.int32).view(T, k), view(4, mcap, torch.int32)
-    aq, sfa, ga = view(5, mcap * H // 2, torch.uint8).view(mcap, H // 2), ws[lay[6]:lay[7]], view(7, mcap, torch.float32)
-    dbuf = view(8, mcap * 2 * I, torch.bfloat16).view(mcap, 2 * I)
-    hq, sfh, gh = view(9, mcap * pw.Ip // 2, torch.uint8).view(mcap, pw.Ip // 2), ws[lay[10]:lay[11]], view(11, mcap, torch.float32)
+    inv = view(3, T * k, torch.int32).view(T, k)
+    aq, ga = ws[lay[5]:lay[7]], view(7, mcap, torch.float32)
+    hbuf = view(8, mcap * I, torch.bfloat16).view(mcap, I)
+    hq, gh = ws[lay[9]:lay[11]], view(11, mcap, torch.float32)
     ybuf = view(12, mcap * H, torch.bfloat16).view(mcap, H)
     n_rows = T * k
     iters = max(10, min(50, args.steps))
 
     def gemm13():
-        L.nvfp4_grouped_gemm(aq, sfa, ga, pw.w13_codes, pw.w13_sf, pw.w13_g, padded, counts, 2 * I, H, E, out=dbuf)
+        L.nvfp4_grouped_gemm_tiled(aq, ga, pw.w13, pw.w13_g, padded, counts, mcap, 2 * I, H, E,
+                                   epilogue=L.EPILOGUE_SWIGLU, out=hbuf)
 
     def gemm2():
-        L.nvfp4_grouped_gemm(hq, sfh, gh, pw.w2_codes, pw.w2_sf, pw.w2_g, padded, counts, H, pw.Ip, E, out=ybuf)
-
-    n_pad = int(padded[-1].item())
-
-    def swiglu():
-        lib = L.load()
-        lib.moe_swiglu_quantize(L._p(dbuf), L._p(perm), n_pad, I, None, L._p(hq), L._p(sfh), L._p(gh), L._stream())
+        L.nvfp4_grouped_gemm_tiled(hq, gh, pw.w2, pw.w2_g, padded, counts, mcap, H, pw.Ip, E, out=ybuf)
 
     def combine():
         L.load().moe_combine(L._p(ybuf), L._p(inv), L._p(wts), T, k, H, L._p(out), L._stream())
@@ -259,17 +254,16 @@ def run_ours(args, rank, world, local_rank):
         L.moe_route_topk(logits, k, True, out=(ids, wts))
 
     stages = {}
-    for name, fn in (("route_topk", route), ("gateup_gemm", gemm13), ("swiglu_requant", swiglu),
-                     ("down_gemm", gemm2), ("combine", combine)):
+    for name, fn in (("route_topk", route), ("gateup_gemm_swiglu", gemm13), ("down_gemm", gemm2),
+                     ("combine", combine)):
         stages[name] = time_launches(fn, iters, flush, stream)[0]
-    stages["permute_quant_rest"] = max(ms_per_step - sum(stages.values()), 0.0)
+    stages["grouping_quantise_requant"] = max(ms_per_step - sum(stages.values()), 0.0)
     torch.cuda.synchronize()
 
-    # dominant kernel: the gate/up grouped GEMM
-    t13 = stages["gateup_gemm"] * 1e-3
+    # dominant kernel: the gate/up grouped GEMM with the SwiGLU epilogue
+    t13 = stages["gateup_gemm_swiglu"] * 1e-3
     flops13 = 2.0 * n_rows * (2 * I) * H
-    bytes13 = (n_rows * H / 2 + n_rows * H / 16 + n_rows * 4 + E * 2 * I * H / 2 + E * 2 * I * H / 16
-               + n_rows * 2 * I * 2)
+    bytes13 = (n_rows * H / 2 * 1.125 + n_rows * 4 + E * 2 * I * H / 2 * 1.125 + n_rows * I * 2)
     tflops13 = flops13 / t13 / 1e12
     gbs13 = bytes13 / t13 / 1e9
     hbm_peak = float(peaks["hbm_gbs"])
@@ -277,16 +271,17 @@ def run_ours(args, rank, world, local_rank):
     t_hbm = bytes13 / (hbm_peak * 1e9)
     t_tc = flops13 / (fp4_peak * 1e12)
     traffic, _ = profiled_traffic(os.path.join(ROOT, "profiles", "gateup_gemm_forward_T16384.md"),
-                                  os.path.join(ROOT, "nvfp4_w4a4_moe_quantize_gb300", "csrc", "grouped_gemm.cu"))
+                                  os.path.join(ROOT, "nvfp4_w4a4_moe_quantize_gb300", "csrc", "gemm_tiled.cu"))
     if t_hbm >= t_tc:
         roofline = {"bound": "hbm", "achieved": round(gbs13, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(gbs13 / hbm_peak, 4), "traffic": traffic}
     else:
         roofline = {"bound": "tensor", "achieved": round(tflops13, 1), "peak": round(fp4_peak, 1),
                     "unit": "TFLOP/s", "frac": round(tflops13 / fp4_peak, 4), "traffic": traffic}
-    roofline.update({"kernel": "nvfp4 grouped GEMM gate/up (forward workload)", "peak_source": peak_src,
-                     "algorithmic_bytes": bytes13, "algorithmic_flops": flops13, "launch_ms": round(t13 * 1e3, 4),
-                     "tflops": round(tflops13, 1), "frac_of_9pf": round(tflops13 / PF_TARGET, 4)})
+    roofline.update({"kernel": "grouped_gemm_tiled_kernel<SwiGLU> (gate/up projection, forward workload)",
+                     "peak_source": peak_src, "algorithmic_bytes": bytes13, "algorithmic_flops": flops13,
+                     "launch_ms": round(t13 * 1e3, 4), "tflops": round(tflops13, 1),
+                     "frac_of_9pf": round(tflops13 / PF_TARGET, 4)})
 
     # ---------------------------------------------------------------- grouped-GEMM workload
     gshape = S.WORKLOADS["gateup"]
@@ -298,12 +293,11 @@ def run_ours(args, rank, world, local_rank):
     glay = L.moe_forward_workspace_layout(gshape.T, k, E, H, I)
     gm = glay[13]
     gview = lambda i, n, dt: gws[glay[i]:glay[i] + n * torch.empty((), dtype=dt).element_size()].view(dt)  # noqa: E731
-    g_aq = gview(5, gm * H // 2, torch.uint8).view(gm, H // 2)
-    g_sfa, g_ga = gws[glay[6]:glay[7]], gview(7, gm, torch.float32)
+    g_aq, g_ga = gws[glay[5]:glay[7]], gview(7, gm, torch.float32)
     g_cnt, g_pad = gview(0, E, torch.int32), gview(2, E + 1, torch.int32)
     g_d = torch.empty(gm, 2 * I, dtype=torch.bfloat16, device=dev)
-    gt, _ = time_launches(lambda: L.nvfp4_grouped_gemm(g_aq, g_sfa, g_ga, pw.w13_codes, pw.w13_sf, pw.w13_g, g_pad,
-                                                       g_cnt, 2 * I, H, E, out=g_d), iters, flush, stream)
+    gt, _ = time_launches(lambda: L.nvfp4_grouped_gemm_tiled(g_aq, g_ga, pw.w13, pw.w13_g, g_pad, g_cnt, gm, 2 * I,
+                                                             H, E, out=g_d), iters, flush, stream)
     gflops = 2.0 * gshape.T * k * 2 * I * H
     gemm_tflops = gflops / (gt * 1e-3) / 1e12
     tiles = int(g_pad[-1].item()) // 128
@@ -366,7 +360,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x_h, logits_h, w13_h, w2_h, shape, budget_s=args.cpu_seconds)
 
-    launches_per_step = 1 + 8      # route + (3 grouping, quantise/scatter, 2 GEMMs, SwiGLU, combine)
+    launches_per_step = 1 + 8      # route + (3 grouping, quantise/scatter, gate/up+SwiGLU GEMM, requant, down GEMM, combine)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
@@ -442,11 +436,11 @@ def run_profile(args):
     lay = L.moe_forward_workspace_layout(T, k, E, H, I)
     m = lay[13]
     vw = lambda i, n, dt: ws[lay[i]:lay[i] + n * torch.empty((), dtype=dt).element_size()].view(dt)  # noqa: E731
-    aq = vw(5, m * H // 2, torch.uint8).view(m, H // 2)
-    d = vw(8, m * 2 * I, torch.bfloat16).view(m, 2 * I)
+    h = vw(8, m * I, torch.bfloat16).view(m, I)
     for _ in range(args.steps):
-        L.nvfp4_grouped_gemm(aq, ws[lay[6]:lay[7]], vw(7, m, torch.float32), pw.w13_codes, pw.w13_sf, pw.w13_g,
-                             vw(2, E + 1, torch.int32), vw(0, E, torch.int32), 2 * I, H, E, out=d)
+        L.nvfp4_grouped_gemm_tiled(ws[lay[5]:lay[7]], vw(7, m, torch.float32), pw.w13, pw.w13_g,
+                                   vw(2, E + 1, torch.int32), vw(0, E, torch.int32), m, 2 * I, H, E,
+                                   epilogue=L.EPILOGUE_SWIGLU, out=h)
     torch.cuda.synchronize()
     assert L.nvfp4_status_check() == 0
 

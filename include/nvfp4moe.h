@@ -67,20 +67,31 @@ typedef enum {
 
 typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 } nvfp4_out_dtype;
 
+/* GEMM-tiled operand layout (the layout the expert block's GEMMs read).  An NVFP4
+ * operand of K columns (K % 256 == 0) is stored as blocks of R rows (R = 128 for
+ * activations, 256 for weights) by 256 K-values; block (b, kb) starts at byte
+ * (b * K/256 + kb) * R * 144 and holds
+ *   R * 128 bytes of codes in 128-byte-swizzled K-major order: row rr of the block at
+ *   rr * 128, its 16-byte chunk j at ((j ^ (rr % 8)) * 16);
+ *   (R/128) * 2048 bytes of E4M3 scales: row group g = rr/128, k-group q of 64 values:
+ *   a 512-byte atom at g*2048 + q*512, scale (rr, c) at (rr%32)*16 + ((rr%128)/32)*4 + c%4.
+ * Each block is the exact shared-memory image of one GEMM pipeline stage, so the GEMM
+ * reads it with one bulk copy.  Size: nvfp4_tiled_bytes(rows, K, R). */
+size_t nvfp4_tiled_bytes(int64_t rows, int64_t K, int32_t block_rows);
+
 /* Prepared (quantised) expert weights.  Caller-allocated device buffers, sizes from
- * moe_weights_sizes().  W13 rows are stored with gate and up interleaved in chunks of
- * 64 rows ([gate 0..63, up 0..63, gate 64..127, up 64..127, ...]) so that one 128-column
- * output tile holds matching gate and up columns; W2's contraction dimension is
+ * moe_weights_sizes().  Both matrices are in the GEMM-tiled layout with 256-row blocks.
+ * W13 rows are stored with gate and up interleaved in chunks of 64 rows ([gate 0..63,
+ * up 0..63, gate 64..127, up 64..127, ...]) so that one 256-column output tile holds the
+ * gate and up columns of the same 128 h columns; W2's contraction dimension is
  * zero-padded to Ip = round_up(I, 256). */
 typedef struct {
   int32_t E;          /* experts */
   int64_t H;          /* hidden size (gate/up contraction, down output) */
   int64_t I;          /* intermediate size */
-  uint8_t* w13_codes; /* device [E, 2I, H/2] */
-  uint8_t* w13_sf;    /* device, tiled layout over E*2I rows, H/16 scale columns */
+  uint8_t* w13;       /* device, GEMM-tiled over E*2I rows, K = H */
   float* w13_g;       /* device [E] */
-  uint8_t* w2_codes;  /* device [E, H, Ip/2] */
-  uint8_t* w2_sf;     /* device, tiled layout over E*H rows, Ip/16 scale columns */
+  uint8_t* w2;        /* device, GEMM-tiled over E*H rows, K = Ip */
   float* w2_g;        /* device [E] */
 } nvfp4_moe_weights;
 
@@ -89,9 +100,9 @@ typedef struct {
 /* Bytes of the tiled scale-factor buffer for a rows x cols NVFP4 tensor. */
 size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
 
-/* Byte sizes of the six nvfp4_moe_weights buffers, in struct order
- * (w13_codes, w13_sf, w13_g, w2_codes, w2_sf, w2_g). */
-nvfp4_status moe_weights_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[6]);
+/* Byte sizes of the four nvfp4_moe_weights buffers, in struct order
+ * (w13, w13_g, w2, w2_g). */
+nvfp4_status moe_weights_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[4]);
 
 /* Workspace bytes for each entry point (0 when none is needed).  `op` is one of: */
 enum {
@@ -182,6 +193,28 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const floa
                                 int64_t M_total, int64_t N, int64_t K, int32_t E, void* D,
                                 nvfp4_out_dtype out_dtype, int64_t ldd, void* stream);
 
+/* The same grouped GEMM over operands in the GEMM-tiled layout: A with 128-row blocks
+ * (M_total rows, a multiple of 128), B with 256-row blocks (E*N rows), scales inside the
+ * tiles.  N % 256 == 0, K % 256 == 0, E <= 512.  gA, gB, group arrays as above.
+ *   epilogue NVFP4_EPILOGUE_STORE: D as nvfp4_grouped_gemm.
+ *   epilogue NVFP4_EPILOGUE_SWIGLU: B holds gate/up rows interleaved in 64-row chunks
+ *     (as nvfp4_moe_weights.w13); D receives BF16 h [M_total, N/2] (row pitch N/2,
+ *     ldd and out_dtype ignored) with h = BF16(silu(gate) * up) from the BF16-rounded gate
+ *     and up outputs -- the value nearest to the exact real number. */
+enum { NVFP4_EPILOGUE_STORE = 0, NVFP4_EPILOGUE_SWIGLU = 1 };
+nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A_tiled, const float* gA, const uint8_t* B_tiled,
+                                      const float* gB, const int32_t* group_offsets,
+                                      const int32_t* group_rows, int64_t M_total, int64_t N,
+                                      int64_t K, int32_t E, void* D, nvfp4_out_dtype out_dtype,
+                                      int64_t ldd, int32_t epilogue, void* stream);
+
+/* Repack row-major codes [rows, K/2] with their 128x4 tiled scales (nvfp4_quantize's
+ * output) into the GEMM-tiled layout with `block_rows`-row blocks (128 or 256); rows
+ * beyond `rows` up to the next block are zero.  K % 256 == 0.  out: device,
+ * nvfp4_tiled_bytes(rows, K, block_rows) bytes. */
+nvfp4_status nvfp4_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K,
+                              int32_t block_rows, uint8_t* out, void* stream);
+
 /* ---------------------------------------------------------------- MoE helpers */
 
 /* Top-k routing of router logits.  ids[t, :] = the k experts with the largest logits,
@@ -225,7 +258,8 @@ nvfp4_status moe_swiglu_quantize(const void* d, const int32_t* perm, int64_t row
  * §"Why is the NVFP4 pretraining recipe not sufficient for RL?": weights use per-block
  * E4M3 scales and one FP32 global scale; each expert matrix is its own tensor).
  *   w13: device BF16 [E, 2I, H] (gate rows 0..I-1, up rows I..2I-1);
- *   w2:  device BF16 [E, H, I].  H % 256 == 0, I % 64 == 0.
+ *   w2:  device BF16 [E, H, I].  H % 256 == 0, I % 128 == 0, H <= 2048, I <= 2048,
+ *   E <= 512.
  *   out: struct of caller-allocated buffers (moe_weights_sizes). */
 nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int64_t H,
                                  int64_t I, const nvfp4_moe_weights* out, void* workspace,
@@ -234,27 +268,30 @@ nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int
 /* The expert block forward ("Low-Bit Precision Training Is Ready for Production...",
  * §"What W4A4 GEMM Actually Changes": W4A4 on the expert layers; "The 4-bitter
  * Lesson...", per-token activation scales, fused per-token quantiser):
- *   permute -> per-token NVFP4 of x written to every routed slot -> gate/up grouped GEMM
- *   (BF16) -> SwiGLU + per-row requantisation -> down grouped GEMM (BF16) -> weighted
- *   combine (BF16).
+ *   permute -> per-token NVFP4 of x written to every routed slot (GEMM-tiled) -> gate/up
+ *   grouped GEMM with the SwiGLU epilogue (BF16 h) -> per-row NVFP4 of h (GEMM-tiled) ->
+ *   down grouped GEMM (BF16 y) -> weighted combine (BF16).  The bits equal those of the
+ *   unfused chain nvfp4_grouped_gemm -> moe_swiglu_quantize -> nvfp4_grouped_gemm ->
+ *   moe_combine over the same operands.
  *   x: device BF16 [T, H] and out: device BF16 [T, H], 16-byte aligned;
  *   ids: device int32 [T, k] and w: device float [T, k], 4-byte aligned;
  *   weights: prepared weights (16-byte aligned buffers).
  *   workspace: nvfp4_workspace_size(NVFP4_OP_MOE_FORWARD, T, k, E, H, I) bytes; its
  *   layout (for inspection) is given by moe_forward_workspace_layout().
- *   1 <= k <= 32, T*k < 2^31. */
+ *   1 <= k <= 32, T*k < 2^31; the weights' E <= 512. */
 nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* w, int64_t T,
                                 int32_t k, const nvfp4_moe_weights* weights, void* out,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* Byte offsets of the forward's intermediates inside its workspace, in this order:
  * [0] counts int32[E], [1] offsets int32[E+1], [2] padded_offsets int32[E+1],
- * [3] inv int32[T*k], [4] perm int32[M_cap], [5] Aq codes [M_cap, H/2],
- * [6] Aq scales (tiled, M_cap rows, H/16 cols), [7] gA float[M_cap],
- * [8] D BF16 [M_cap, 2I] (interleaved gate/up), [9] hq codes [M_cap, Ip/2],
- * [10] hq scales (tiled, M_cap rows, Ip/16 cols), [11] gh float[M_cap],
- * [12] y BF16 [M_cap, H], [13] M_cap (a row count, not an offset),
- * [14] total bytes.  Only rows below padded_offsets[E] are meaningful. */
+ * [3] inv int32[T*k], [4] perm int32[M_cap],
+ * [5] Aq: GEMM-tiled (128-row blocks) codes and scales of the routed rows, K = H,
+ * [6] equal to [5] (the scales live inside the tiles), [7] gA float[M_cap],
+ * [8] h BF16 [M_cap, I], [9] hq: GEMM-tiled (128-row blocks), K = Ip,
+ * [10] equal to [9], [11] gh float[M_cap], [12] y BF16 [M_cap, H],
+ * [13] M_cap (a row count, not an offset), [14] total bytes.
+ * Only rows below padded_offsets[E] whose perm entry is >= 0 are meaningful. */
 nvfp4_status moe_forward_workspace_layout(int64_t T, int32_t k, int32_t E, int64_t H,
                                           int64_t I, int64_t layout_out[15]);
 

@@ -21,6 +21,7 @@ __all__ = [
     "nvfp4_quantize", "nvfp4_quantize_noalloc", "nvfp4_grouped_gemm", "moe_route_topk", "moe_permute", "moe_combine",
     "moe_swiglu_quantize", "moe_prepare_weights", "moe_expert_forward", "moe_forward_workspace",
     "moe_forward_workspace_layout", "nvfp4_status_check", "nvfp4_sf_bytes", "NVFP4MoEWeights",
+    "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled", "nvfp4_tiled_bytes",
     "SCALE_PER_TENSOR", "SCALE_PER_ROW", "SCALE_PER_GROUP", "ROUND_RNE", "ROUND_STOCHASTIC",
 ]
 
@@ -44,12 +45,16 @@ class NVFP4Error(RuntimeError):
 
 
 class _Weights(ctypes.Structure):
-    _fields_ = [("E", _i32), ("H", _i64), ("I", _i64), ("w13_codes", _vp), ("w13_sf", _vp),
-                ("w13_g", _vp), ("w2_codes", _vp), ("w2_sf", _vp), ("w2_g", _vp)]
+    _fields_ = [("E", _i32), ("H", _i64), ("I", _i64), ("w13", _vp), ("w13_g", _vp), ("w2", _vp),
+                ("w2_g", _vp)]
 
 
 _SIGS = {
     "nvfp4_sf_bytes": (_sz, [_i64, _i64]),
+    "nvfp4_tiled_bytes": (_sz, [_i64, _i64, _i32]),
+    "nvfp4_grouped_gemm_tiled": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp,
+                                                ctypes.c_int, _i64, _i32, _vp]),
+    "nvfp4_pack_tiled": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
     "moe_weights_sizes": (ctypes.c_int, [_i32, _i64, _i64, ctypes.POINTER(_sz)]),
     "nvfp4_workspace_size": (_sz, [ctypes.c_int, _i64, _i64, _i64, _i64, _i64]),
     "nvfp4_status_check": (ctypes.c_int, [_vp]),
@@ -131,6 +136,10 @@ def nvfp4_sf_bytes(rows: int, cols: int) -> int:
     return int(load().nvfp4_sf_bytes(rows, cols))
 
 
+def nvfp4_tiled_bytes(rows: int, K: int, block_rows: int) -> int:
+    return int(load().nvfp4_tiled_bytes(rows, K, block_rows))
+
+
 def nvfp4_status_check(stream=None) -> int:
     """Synchronise the stream; return (and clear) the device status word."""
     return int(load().nvfp4_status_check(_stream(stream)))
@@ -201,6 +210,36 @@ def nvfp4_grouped_gemm(A, SFA, gA, B, SFB, gB, group_offsets, group_rows, N: int
     return out
 
 
+EPILOGUE_STORE, EPILOGUE_SWIGLU = 0, 1
+
+
+def nvfp4_grouped_gemm_tiled(A_tiled, gA, B_tiled, gB, group_offsets, group_rows, M_total: int, N: int, K: int,
+                             E: int, out_dtype=torch.bfloat16, epilogue: int = EPILOGUE_STORE,
+                             out: torch.Tensor | None = None, stream=None):
+    """Grouped GEMM over GEMM-tiled operands.  EPILOGUE_SWIGLU returns h [M_total, N/2]."""
+    lib = load()
+    dev = _dev(A_tiled)
+    if out is None:
+        if epilogue == EPILOGUE_SWIGLU:
+            out = torch.empty(M_total, N // 2, dtype=torch.bfloat16, device=dev)
+        else:
+            out = torch.empty(M_total, N, dtype=out_dtype, device=dev)
+    code = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.nvfp4_grouped_gemm_tiled(_p(A_tiled), _p(gA), _p(B_tiled), _p(gB), _p(group_offsets), _p(group_rows),
+                                        M_total, N, K, E, _p(out), code, out.stride(0), epilogue, _stream(stream)),
+           "nvfp4_grouped_gemm_tiled")
+    return out
+
+
+def nvfp4_pack_tiled(codes: torch.Tensor, sf: torch.Tensor, rows: int, K: int, block_rows: int, stream=None):
+    """Row-major codes + 128x4 tiled scales -> the GEMM-tiled layout (block_rows 128 / 256)."""
+    lib = load()
+    out = torch.empty(nvfp4_tiled_bytes(rows, K, block_rows), dtype=torch.uint8, device=_dev(codes))
+    _check(lib.nvfp4_pack_tiled(_p(codes), _p(sf), rows, K, block_rows, _p(out), _stream(stream)),
+           "nvfp4_pack_tiled")
+    return out
+
+
 # --------------------------------------------------------------------------- MoE helpers
 
 def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool = True, out=None, stream=None):
@@ -261,23 +300,21 @@ def moe_swiglu_quantize(d: torch.Tensor, perm: torch.Tensor, I: int, want_h: boo
 
 
 class NVFP4MoEWeights:
-    """Quantised expert weights (device tensors) plus the C struct that points at them."""
+    """Quantised expert weights (GEMM-tiled device buffers) plus the C struct that points
+    at them."""
 
     def __init__(self, E: int, H: int, I: int, device):
         lib = load()
-        sizes = (_sz * 6)()
+        sizes = (_sz * 4)()
         _check(lib.moe_weights_sizes(E, H, I, sizes), "moe_weights_sizes")
         Ip = (I + 255) // 256 * 256
         self.E, self.H, self.I, self.Ip = E, H, I, Ip
-        self.w13_codes = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
-        self.w13_sf = torch.empty(sizes[1], dtype=torch.uint8, device=device)
+        self.w13 = torch.empty(sizes[0], dtype=torch.uint8, device=device)
         self.w13_g = torch.empty(E, dtype=torch.float32, device=device)
-        self.w2_codes = torch.empty(E, H, Ip // 2, dtype=torch.uint8, device=device)
-        self.w2_sf = torch.empty(sizes[4], dtype=torch.uint8, device=device)
+        self.w2 = torch.empty(sizes[2], dtype=torch.uint8, device=device)
         self.w2_g = torch.empty(E, dtype=torch.float32, device=device)
-        assert self.w13_codes.numel() == sizes[0] and self.w2_codes.numel() == sizes[3]
-        self.struct = _Weights(E, H, I, self.w13_codes.data_ptr(), self.w13_sf.data_ptr(), self.w13_g.data_ptr(),
-                               self.w2_codes.data_ptr(), self.w2_sf.data_ptr(), self.w2_g.data_ptr())
+        self.struct = _Weights(E, H, I, self.w13.data_ptr(), self.w13_g.data_ptr(), self.w2.data_ptr(),
+                               self.w2_g.data_ptr())
 
 
 def moe_prepare_weights(w13: torch.Tensor, w2: torch.Tensor, stream=None) -> NVFP4MoEWeights:

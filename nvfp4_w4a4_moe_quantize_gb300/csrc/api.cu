@@ -12,6 +12,7 @@
 #include "nvfp4moe.h"
 #include "launch.h"
 #include "status.cuh"
+#include "tiled.cuh"
 
 namespace nvfp4 {
 
@@ -69,7 +70,7 @@ struct ForwardLayout {
   int64_t off[15];
 };
 
-// hist | counts | offsets | padded | inv | perm | Aq | SFA | gA | D | hq | SFH | gH | y
+// hist | counts | offsets | padded | inv | perm | Aq (tiled) | gA | h | hq (tiled) | gH | y
 ForwardLayout forward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t I, size_t* hist_off,
                              size_t* hist_bytes) {
   ForwardLayout L;
@@ -90,12 +91,12 @@ ForwardLayout forward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t
   L.off[2] = take(4 * (E + 1));
   L.off[3] = take(4 * T * k);
   L.off[4] = take(4 * mcap);
-  L.off[5] = take((size_t)mcap * (H / 2));
-  L.off[6] = take(nvfp4_sf_bytes(mcap, H));
+  L.off[5] = take((size_t)tiled_bytes(mcap, H, 128));
+  L.off[6] = L.off[5];
   L.off[7] = take(4 * mcap);
-  L.off[8] = take((size_t)mcap * 2 * I * 2);
-  L.off[9] = take((size_t)mcap * (Ip / 2));
-  L.off[10] = take(nvfp4_sf_bytes(mcap, Ip));
+  L.off[8] = take((size_t)mcap * I * 2);
+  L.off[9] = take((size_t)tiled_bytes(mcap, Ip, 128));
+  L.off[10] = L.off[9];
   L.off[11] = take(4 * mcap);
   L.off[12] = take((size_t)mcap * H * 2);
   L.off[13] = mcap;
@@ -106,12 +107,6 @@ ForwardLayout forward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t
 nvfp4_status gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const uint8_t* B, const uint8_t* SFB,
                   const float* gB, const int32_t* offsets, const int32_t* rows, int64_t M_total, int64_t N, int64_t K,
                   int32_t E, void* D, int out_f32, int64_t ldd, cudaStream_t s) {
-  CUtensorMap ma, mb, md;
-  if (!make_map(&ma, A, M_total, K / 2, K / 2, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
-      !make_map(&mb, B, (int64_t)E * N, K / 2, K / 2, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
-      !make_map(&md, D, M_total, N, ldd * (out_f32 ? 4 : 2), 32,
-                out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_f32 ? 4 : 2))
-    return NVFP4_ERR_CUDA;
   GemmArgs g;
   g.sfa = SFA;
   g.sfb = SFB;
@@ -126,6 +121,15 @@ nvfp4_status gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const u
   g.ldd = ldd;
   g.out_f32 = out_f32;
   g.status = device_status_ptr();
+  const bool wide = n256_supported(g);   // its B map also has 128-row boxes (one per CTA of a pair)
+  CUtensorMap ma, mb, md;
+  if (!make_map(&ma, A, M_total, K / 2, K / 2, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
+      !make_map(&mb, B, (int64_t)E * N, K / 2, K / 2, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1))
+    return NVFP4_ERR_CUDA;
+  if (wide) return from_cuda(launch_grouped_gemm_n256(ma, mb, g, M_total / 128, s));
+  if (!make_map(&md, D, M_total, N, ldd * (out_f32 ? 4 : 2), 32,
+                out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_f32 ? 4 : 2))
+    return NVFP4_ERR_CUDA;
   return from_cuda(launch_grouped_gemm(ma, mb, md, g, M_total / 128, s));
 }
 
@@ -161,16 +165,19 @@ size_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
   return (size_t)((rows + 127) / 128) * (size_t)((cols + 63) / 64) * 512u;
 }
 
-nvfp4_status moe_weights_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[6]) {
+nvfp4_status moe_weights_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[4]) {
   if (E <= 0 || H <= 0 || I <= 0 || sizes_out == nullptr) return NVFP4_ERR_INVALID_ARG;
   const int64_t Ip = round_up(I, 256);
-  sizes_out[0] = (size_t)E * 2 * I * (H / 2);
-  sizes_out[1] = nvfp4_sf_bytes((int64_t)E * 2 * I, H);
-  sizes_out[2] = 4u * (size_t)E;
-  sizes_out[3] = (size_t)E * H * (Ip / 2);
-  sizes_out[4] = nvfp4_sf_bytes((int64_t)E * H, Ip);
-  sizes_out[5] = 4u * (size_t)E;
+  sizes_out[0] = (size_t)tiled_bytes((int64_t)E * 2 * I, H, 256);
+  sizes_out[1] = 4u * (size_t)E;
+  sizes_out[2] = (size_t)tiled_bytes((int64_t)E * H, Ip, 256);
+  sizes_out[3] = 4u * (size_t)E;
   return NVFP4_OK;
+}
+
+size_t nvfp4_tiled_bytes(int64_t rows, int64_t K, int32_t block_rows) {
+  if (rows <= 0 || K <= 0 || K % 256 != 0 || (block_rows != 128 && block_rows != 256)) return 0;
+  return (size_t)tiled_bytes(rows, K, block_rows);
 }
 
 size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t E, int64_t H, int64_t I) {
@@ -291,6 +298,52 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const floa
               out_dtype == NVFP4_OUT_F32, ldd, static_cast<cudaStream_t>(stream));
 }
 
+nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A, const float* gA, const uint8_t* B, const float* gB,
+                                      const int32_t* group_offsets, const int32_t* group_rows, int64_t M_total,
+                                      int64_t N, int64_t K, int32_t E, void* D, nvfp4_out_dtype out_dtype,
+                                      int64_t ldd, int32_t epilogue, void* stream) {
+  if (E <= 0 || E > tiled_max_experts() || N <= 0 || K <= 0 || M_total < 0 || M_total % 128 != 0)
+    return NVFP4_ERR_INVALID_ARG;
+  if (N % 256 != 0 || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((int64_t)E * N >= (int64_t)1 << 31 || M_total >= (int64_t)1 << 31 || K >= (int64_t)1 << 20)
+    return NVFP4_ERR_UNSUPPORTED;
+  if (epilogue != NVFP4_EPILOGUE_STORE && epilogue != NVFP4_EPILOGUE_SWIGLU) return NVFP4_ERR_INVALID_ARG;
+  if (epilogue == NVFP4_EPILOGUE_STORE) {
+    if (ldd < N || ldd % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_INVALID_ARG;
+  }
+  if (M_total == 0) return NVFP4_OK;
+  const void* ptrs[] = {A, B, D};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned4(gA) || !aligned4(gB) || !aligned4(group_offsets) || !aligned4(group_rows))
+    return NVFP4_ERR_INVALID_ARG;
+  GemmArgs g{};
+  g.ga = gA;
+  g.gb = gB;
+  g.offsets = group_offsets;
+  g.rows = group_rows;
+  g.E = E;
+  g.N = (int32_t)N;
+  g.K = (int32_t)K;
+  g.d = D;
+  g.ldd = ldd;
+  g.out_f32 = out_dtype == NVFP4_OUT_F32;
+  g.status = device_status_ptr();
+  g.h = static_cast<__nv_bfloat16*>(D);
+  g.I = N / 2;
+  return from_cuda(launch_grouped_gemm_tiled(A, B, g, M_total / 128, epilogue == NVFP4_EPILOGUE_SWIGLU,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K, int32_t block_rows,
+                              uint8_t* out, void* stream) {
+  if (rows < 0 || K <= 0 || K % 256 != 0 || (block_rows != 128 && block_rows != 256)) return NVFP4_ERR_INVALID_ARG;
+  if (rows == 0) return NVFP4_OK;
+  if (!codes || !sf || !out || !aligned16(codes) || !aligned16(sf) || !aligned16(out)) return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_pack_tiled(codes, sf, rows, K, block_rows, out, static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status moe_route_topk(const float* logits, int64_t T, int32_t E, int32_t k, int renormalize, int32_t* ids,
                             float* weights, void* stream) {
   if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > 32 || k > E) return NVFP4_ERR_INVALID_ARG;
@@ -333,10 +386,10 @@ nvfp4_status moe_swiglu_quantize(const void* d, const int32_t* perm, int64_t row
 
 nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int64_t H, int64_t I,
                                  const nvfp4_moe_weights* out, void* ws, size_t ws_bytes, void* stream) {
-  if (E <= 0 || E > 1024 || H <= 0 || I <= 0 || out == nullptr) return NVFP4_ERR_INVALID_ARG;
-  if (H % 256 != 0 || I % 64 != 0 || H > 8192 || I > 4096) return NVFP4_ERR_UNSUPPORTED;
+  if (E <= 0 || H <= 0 || I <= 0 || out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (E > tiled_max_experts() || H % 256 != 0 || I % 128 != 0 || H > 2048 || I > 2048) return NVFP4_ERR_UNSUPPORTED;
   if (out->E != E || out->H != H || out->I != I) return NVFP4_ERR_INVALID_ARG;
-  const void* ptrs[] = {w13, w2, out->w13_codes, out->w13_sf, out->w13_g, out->w2_codes, out->w2_sf, out->w2_g};
+  const void* ptrs[] = {w13, w2, out->w13, out->w13_g, out->w2, out->w2_g};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
   if (ws == nullptr || ws_bytes < nvfp4_workspace_size(NVFP4_OP_PREPARE_WEIGHTS, E, 0, 0, 0, 0) || !aligned16(ws))
@@ -355,15 +408,15 @@ nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int
   a.group_rows = 2 * I;
   a.amax_bits = amax;
   a.g_out = out->w13_g;
-  a.codes = out->w13_codes;
-  a.codes_ld = H / 2;
-  a.sf = out->w13_sf;
+  a.codes = out->w13;
   a.sf_words = H / 64;
   a.cols_pad = H;
   a.rows_total = a.rows;
   a.map = kMapInterleave;
   a.map_I = I;
   a.status = device_status_ptr();
+  a.tiled_R = 256;
+  a.kblocks = H / 256;
   e = launch_quantize_rows(a, kRoundRNE, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
   uint32_t* amax2 = amax + E;
@@ -378,14 +431,14 @@ nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int
   b.group_rows = H;
   b.amax_bits = amax2;
   b.g_out = out->w2_g;
-  b.codes = out->w2_codes;
-  b.codes_ld = Ip / 2;
-  b.sf = out->w2_sf;
+  b.codes = out->w2;
   b.sf_words = Ip / 64;
   b.cols_pad = Ip;
   b.rows_total = b.rows;
   b.map = kMapIdentity;
   b.status = device_status_ptr();
+  b.tiled_R = 256;
+  b.kblocks = Ip / 256;
   return from_cuda(launch_quantize_rows(b, kRoundRNE, s));
 }
 
@@ -394,11 +447,11 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   if (wt == nullptr || T < 0 || k <= 0 || k > 32) return NVFP4_ERR_INVALID_ARG;
   const int32_t E = wt->E;
   const int64_t H = wt->H, I = wt->I;
-  if (E <= 0 || E > 1024 || k > E) return NVFP4_ERR_INVALID_ARG;
-  if (H % 256 != 0 || I % 64 != 0 || H > 8192 || I > 4096) return NVFP4_ERR_UNSUPPORTED;
+  if (E <= 0 || E > tiled_max_experts() || k > E) return NVFP4_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0 || H > 2048 || I > 2048) return NVFP4_ERR_UNSUPPORTED;
   if (T * k >= ((int64_t)1 << 31) - (int64_t)E * 128) return NVFP4_ERR_UNSUPPORTED;
   if (T == 0) return NVFP4_OK;
-  const void* ptrs[] = {x, out, ws, wt->w13_codes, wt->w13_sf, wt->w13_g, wt->w2_codes, wt->w2_sf, wt->w2_g};
+  const void* ptrs[] = {x, out, ws, wt->w13, wt->w13_g, wt->w2, wt->w2_g};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
   if (!aligned4(ids) || !aligned4(w)) return NVFP4_ERR_INVALID_ARG;   // read element by element
@@ -414,21 +467,21 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   int32_t* inv = reinterpret_cast<int32_t*>(at(3));
   int32_t* perm = reinterpret_cast<int32_t*>(at(4));
   uint8_t* aq = at(5);
-  uint8_t* sfa = at(6);
   float* ga = reinterpret_cast<float*>(at(7));
-  void* dbuf = at(8);
+  __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(at(8));
   uint8_t* hq = at(9);
-  uint8_t* sfh = at(10);
   float* gh = reinterpret_cast<float*>(at(11));
   void* ybuf = at(12);
   const int64_t mcap = L.off[13];
   const int64_t Ip = round_up(I, 256);
   int* status = device_status_ptr();
 
+  // 1. expert grouping
   cudaError_t e = launch_permute(ids, T, k, E, counts, offsets, padded, inv, perm,
                                  reinterpret_cast<int32_t*>(base + hist_off), permute_chunks(T * k), status, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
+  // 2. per-token NVFP4 of x, written to every routed slot in the GEMM-tiled layout
   QuantArgs a{};
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.rows = T;
@@ -437,8 +490,6 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   a.mode = kScopeRow;
   a.g_out = ga;
   a.codes = aq;
-  a.codes_ld = H / 2;
-  a.sf = sfa;
   a.sf_words = H / 64;
   a.cols_pad = H;
   a.rows_total = T;
@@ -446,16 +497,64 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   a.inv = inv;
   a.k = k;
   a.status = status;
+  a.tiled_R = 128;
+  a.kblocks = H / 256;
   e = launch_quantize_rows(a, kRoundRNE, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
-  nvfp4_status st = gemm(aq, sfa, ga, wt->w13_codes, wt->w13_sf, wt->w13_g, padded, counts, mcap, 2 * I, H, E,
-                         dbuf, 0, 2 * I, s);
-  if (st != NVFP4_OK) return st;
-  e = launch_swiglu_quant(dbuf, perm, mcap, padded + E, I, Ip, nullptr, hq, sfh, gh, s);
+  // 3. gate/up GEMM with the SwiGLU epilogue: h = BF16(silu(gate) * up)
+  GemmArgs g1{};
+  g1.ga = ga;
+  g1.gb = wt->w13_g;
+  g1.offsets = padded;
+  g1.rows = counts;
+  g1.E = E;
+  g1.N = (int32_t)(2 * I);
+  g1.K = (int32_t)H;
+  g1.status = status;
+  g1.h = hbuf;
+  g1.I = I;
+  e = launch_grouped_gemm_tiled(aq, wt->w13, g1, mcap / 128, true, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-  st = gemm(hq, sfh, gh, wt->w2_codes, wt->w2_sf, wt->w2_g, padded, counts, mcap, H, Ip, E, ybuf, 0, H, s);
-  if (st != NVFP4_OK) return st;
+
+  // 4. per-row NVFP4 of h (routed rows only), K zero-padded to Ip, GEMM-tiled
+  QuantArgs r{};
+  r.x = hbuf;
+  r.rows = mcap;
+  r.rows_dev = padded + E;
+  r.row_filter = perm;
+  r.cols = I;
+  r.ld = I;
+  r.mode = kScopeRow;
+  r.g_out = gh;
+  r.codes = hq;
+  r.sf_words = Ip / 64;
+  r.cols_pad = Ip;
+  r.rows_total = mcap;
+  r.map = kMapIdentity;
+  r.status = status;
+  r.tiled_R = 128;
+  r.kblocks = Ip / 256;
+  e = launch_quantize_rows(r, kRoundRNE, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+
+  // 5. down GEMM -> y (BF16)
+  GemmArgs g2{};
+  g2.ga = gh;
+  g2.gb = wt->w2_g;
+  g2.offsets = padded;
+  g2.rows = counts;
+  g2.E = E;
+  g2.N = (int32_t)H;
+  g2.K = (int32_t)Ip;
+  g2.d = ybuf;
+  g2.ldd = H;
+  g2.out_f32 = 0;
+  g2.status = status;
+  e = launch_grouped_gemm_tiled(hq, wt->w2, g2, mcap / 128, false, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+
+  // 6. weighted un-permute
   return from_cuda(launch_combine(ybuf, inv, w, T, k, H, out, s));
 }
 

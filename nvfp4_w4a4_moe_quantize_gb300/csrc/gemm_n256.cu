@@ -1,0 +1,303 @@
+// W4A4 grouped GEMM, 128 x 256 output tiles, CTA pairs sharing the weight tile: the
+// same computation as grouped_gemm.cu ("Low-Bit Precision Training Is Ready for
+// Production...", §"What W4A4 GEMM Actually Changes"), issued as M=128, N=256, K=64
+// block-scaled MMAs.  An N=256 instruction costs the tensor pipe about the same time as
+// an N=128 one, so this shape doubles the work per instruction; it is used whenever N is
+// a multiple of 256.
+//
+// Feeding shared memory from L2 is what limits these GEMMs, so the CTAs run in clusters
+// of two that work on two consecutive 128-row tiles of the same expert and the same 256
+// output columns: each CTA loads its own A tile and one half of the weight tile (and of
+// its scale blocks) with a multicast TMA that lands in both CTAs, which cuts the L2 reads
+// per stage from 54 KB to 36 KB.  A stage is refilled only when the MMAs of both CTAs have
+// consumed it (each MMA warp commits to the stage's "empty" barrier in both CTAs).  An
+// expert with an odd number of row tiles gives the second CTA a duplicate of the first
+// tile whose results are discarded.
+//
+// One 256-column TMEM accumulator per CTA (the scale factors of the stages take the rest
+// of TMEM), 4 stages of 54 KB, and 8 epilogue warps (two per TMEM lane quadrant, 128
+// columns each) that drain the accumulator into registers at once and release it before
+// converting and storing.  Rows outside the groups are never written.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "group.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+namespace g256 {
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBKBytes = 128;                // 256 FP4 values of K per stage
+#ifndef NVFP4_N256_STAGES
+#define NVFP4_N256_STAGES 4
+#endif
+constexpr int kStages = NVFP4_N256_STAGES;   // build-time tunable
+constexpr int kABytes = kBM * kBKBytes;      // 16 KB
+constexpr int kBBytes = kBN * kBKBytes;      // 32 KB
+constexpr int kSFABytes = 4 * 512;           // 4 k-groups x (128 rows x 4 scales)
+constexpr int kSFBBytes = 2 * 4 * 512;       // 2 row groups of 128
+constexpr uint32_t kStageTx = kABytes + kBBytes + kSFABytes + kSFBBytes;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = kBN;                // one accumulator: 128 lanes x 256 float32
+constexpr int kSFCol0 = kAccCols;
+constexpr int kSFStageCols = 16 + 32;        // A: 4 x 4 columns, B: 4 x 8 columns
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kMaxE = 512;
+constexpr uint16_t kPair = 0x3;              // both CTAs of the cluster
+
+struct Smem {
+  uint8_t a[kStages][kABytes];
+  uint8_t b[kStages][kBBytes];
+  uint8_t sfa[kStages][kSFABytes];
+  uint8_t sfb[kStages][kSFBBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t accf;
+  uint64_t acce;
+  uint32_t tmem_base;
+  int abort;
+  int32_t offsets[kMaxE + 1];
+  int32_t pair_off[kMaxE + 1];               // exclusive scan of ceil(row tiles / 2) per expert
+  int32_t rows[kMaxE];
+  float gb[kMaxE];
+};
+static_assert(kSFCol0 + kStages * kSFStageCols <= kTmemCols, "TMEM budget");
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+}  // namespace g256
+
+// Tile (128 rows, 256 columns) of pair-unit u for CTA `rank` of the cluster.
+struct PairTile {
+  int e, n_tile;
+  int local;       // this CTA's row tile inside the expert's group
+  int a_tile;      // row tile whose A is loaded (the partner's for a duplicate)
+};
+
+__device__ __forceinline__ PairTile pair_tile(const g256::Smem& sm, int E, int n_tiles, int u, uint32_t rank) {
+  PairTile pt;
+  const int pu = u / n_tiles;
+  pt.n_tile = u - pu * n_tiles;
+  pt.e = find_group(sm.pair_off, E, pu);
+  const int p = pu - sm.pair_off[pt.e];
+  const int tiles_e = (sm.offsets[pt.e + 1] - sm.offsets[pt.e]) / g256::kBM;
+  pt.local = 2 * p + (int)rank;
+  pt.a_tile = sm.offsets[pt.e] / g256::kBM + (pt.local < tiles_e ? pt.local : 2 * p);
+  return pt;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
+    grouped_gemm_n256_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                             const GemmArgs g) {
+  using namespace g256;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+  for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
+  for (int i = threadIdx.x; i < g.E; i += blockDim.x) {
+    sm.rows[i] = g.rows[i];
+    sm.gb[i] = g.gb[i];
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 2);          // the MMA warps of both CTAs release a stage
+    }
+    mbar_init(&sm.accf, 1);
+    mbar_init(&sm.acce, kEpiWarps * 32);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tma);
+    prefetch_tensormap(&tmb);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  if (warp == 0) {   // pair-unit offsets: exclusive scan of ceil(tiles_e / 2)
+    const int per = (g.E + 31) / 32;
+    const int b0 = lane * per, b1 = min(g.E, b0 + per);
+    int local = 0;
+    for (int e = b0; e < b1; ++e) local += ((sm.offsets[e + 1] - sm.offsets[e]) / kBM + 1) / 2;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - local;
+    for (int e = b0; e < b1; ++e) {
+      sm.pair_off[e] = run;
+      run += ((sm.offsets[e + 1] - sm.offsets[e]) / kBM + 1) / 2;
+    }
+    if (lane == 31) sm.pair_off[g.E] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();    // the partner's barriers exist before any multicast reaches them
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort = &sm.abort;
+
+  const int n_tiles = g.N / kBN;
+  const int total = sm.pair_off[g.E] * n_tiles;
+  const int kblocks = g.K / (2 * kBKBytes);
+  const int64_t sf_kgroups = g.K / 64;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      for (int u = cl; u < total; u += ncl) {
+        const PairTile pt = pair_tile(sm, g.E, n_tiles, u, rank);
+        const int32_t row0 = pt.a_tile * kBM;
+        const int32_t brow = pt.e * g.N + pt.n_tile * kBN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, g.status, abort)) goto producer_done;
+          mbar_arrive_expect_tx(&sm.full[stage], kStageTx);
+          tma_load_2d(sm.a[stage], &tma, kb * kBKBytes, row0, &sm.full[stage]);
+          tma_load_2d_mc(sm.b[stage] + rank * (kBBytes / 2), &tmb, kb * kBKBytes, brow + (int)rank * 128,
+                         &sm.full[stage], kPair);
+          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)pt.a_tile * sf_kgroups + kb * 4) * 512, kSFABytes,
+                    &sm.full[stage]);
+          bulk_load_mc(sm.sfb[stage] + rank * 2048,
+                       g.sfb + ((int64_t)(brow / 128 + (int)rank) * sf_kgroups + kb * 4) * 512, 2048,
+                       &sm.full[stage], kPair);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      for (int u = cl; u < total; u += ncl, ++it) {
+        if (!mbar_wait(&sm.acce, (it & 1) ^ 1u, g.status, abort)) break;   // accumulator drained
+        tc_fence_after();
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&sm.full[stage], phase, g.status, abort)) goto mma_done;
+          tc_fence_after();
+          const uint32_t sfa_t = tmem + kSFCol0 + stage * kSFStageCols;
+          const uint32_t sfb_t = sfa_t + 16;
+          const uint32_t sa = smem_u32(sm.a[stage]), sb = smem_u32(sm.b[stage]);
+          const uint32_t ssfa = smem_u32(sm.sfa[stage]), ssfb = smem_u32(sm.sfb[stage]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
+            tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
+            tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
+            tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit_mc(&sm.empty[stage], kPair);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        tc_commit(&sm.accf);
+      }
+    mma_done:;
+    }
+  } else {
+    // epilogue: warps 2..9.  Lane quadrant q = warp % 4, column half = (warp - 2) / 4.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int elt = g.out_f32 ? 4 : 2;
+    int it = 0;
+    for (int u = cl; u < total; u += ncl, ++it) {
+      const PairTile pt = pair_tile(sm, g.E, n_tiles, u, rank);
+      const int e = pt.e;
+      const int32_t in_group = sm.rows[e] - pt.local * kBM;   // <= 0 for a duplicate tile
+      const bool valid = q * 32 + lane < in_group;
+      const int64_t row = (int64_t)sm.offsets[e] + pt.local * kBM + q * 32 + lane;
+      const float ga = valid ? g.ga[row] : 0.0f;
+      if (!mbar_wait(&sm.accf, it & 1, g.status, abort)) break;
+      tc_fence_after();
+      const float scale = __fmul_rn(ga, sm.gb[e]);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + half * 128;
+      uint32_t v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) NVFP4_TMEM_LD_X32(taddr + 32 * c, v[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.acce);
+      if (valid) {
+        uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + (int64_t)pt.n_tile * kBN + half * 128) * elt;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (g.out_f32) {
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4)
+              *reinterpret_cast<float4*>(dp + (32 * c + 4 * u4) * 4) =
+                  make_float4(__fmul_rn(__uint_as_float(v[c][4 * u4]), scale),
+                              __fmul_rn(__uint_as_float(v[c][4 * u4 + 1]), scale),
+                              __fmul_rn(__uint_as_float(v[c][4 * u4 + 2]), scale),
+                              __fmul_rn(__uint_as_float(v[c][4 * u4 + 3]), scale));
+          } else {
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+              uint32_t w[4];
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const __nv_bfloat162 b2 =
+                    __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][8 * u4 + 2 * p]), scale),
+                                          __fmul_rn(__uint_as_float(v[c][8 * u4 + 2 * p + 1]), scale));
+                w[p] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              *reinterpret_cast<uint4*>(dp + (32 * c + 8 * u4) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();    // no multicast or remote arrive may target a CTA that has exited
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+bool n256_supported(const GemmArgs& g) { return g.N % g256::kBN == 0 && g.E <= g256::kMaxE; }
+
+cudaError_t launch_grouped_gemm_n256(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
+                                     int64_t max_m_tiles, cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_n256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)g256::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int64_t units = (max_m_tiles + g.E + 1) / 2 * (g.N / g256::kBN);   // bound on pair units
+  if (max_m_tiles == 0) return cudaSuccess;
+  int64_t clusters = num_sms() / 2;
+  if (units < clusters) clusters = units;
+  const int grid = (int)(2 * clusters);
+  grouped_gemm_n256_kernel<<<grid, g256::kThreads, g256::kSmemBytes, s>>>(tma, tmb, g);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

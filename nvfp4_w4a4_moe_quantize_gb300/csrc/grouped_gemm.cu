@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "group.cuh"
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -70,16 +71,6 @@ static_assert(kSFCol0 + kStages * kSFStageCols <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 }  // namespace gg
-
-__device__ __forceinline__ int find_group(const int32_t* off, int E, int32_t row0) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (off[mid] <= row0) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
 
 __global__ void __launch_bounds__(gg::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
@@ -220,15 +211,17 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
       tc_fence_after();
       const float scale = __fmul_rn(ga, sm.gb[e]);
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-#pragma unroll 1
+      // the whole 128-column accumulator row in four loads, one wait, then hand the
+      // accumulator back to the MMA warp before converting and storing
+      uint32_t vall[kBN / 32][32];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) NVFP4_TMEM_LD_X32(taddr + 32 * c, vall[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.acce[acc]);
+#pragma unroll
       for (int c0 = 0; c0 < kBN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + c0, v);
-        tmem_ld_wait();
-        if (c0 + 32 == kBN) {   // accumulator fully read: hand it back to the MMA warp
-          tc_fence_before();
-          mbar_arrive(&sm.acce[acc]);
-        }
+        const uint32_t (&v)[32] = vall[c0 / 32];
         const int64_t n0 = (int64_t)n_tile * kBN + c0;
         uint32_t w[32];
         int nw;

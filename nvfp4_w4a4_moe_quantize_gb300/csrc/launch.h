@@ -31,6 +31,11 @@ struct QuantArgs {
   int k;
   uint64_t seed, rng_offset;
   int* status;
+  int tiled_R;             // 0: row-major codes + 128x4 scales; 128 / 256: GEMM-tiled output
+                           //    (codes and scales both in `codes`, see tiled.cuh)
+  int64_t kblocks;         // tiled: cols_pad / 256
+  const int32_t* row_filter;  // nullable: rows with row_filter[row] < 0 are skipped
+  const int32_t* rows_dev;    // nullable: device count capping `rows`
 };
 
 struct GemmArgs {
@@ -46,6 +51,8 @@ struct GemmArgs {
   int64_t ldd;
   int out_f32;
   int* status;
+  __nv_bfloat16* h;        // SwiGLU epilogue: h [M, I]
+  int64_t I;
 };
 
 int num_sms();
@@ -55,9 +62,22 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, i
                         uint32_t* amax_bits, int64_t n_scopes, cudaStream_t s);
 cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s);
 
-// Grouped GEMM: tensor maps are built by the caller (api.cu).
+// Grouped GEMM: tensor maps are built by the caller (api.cu), all with 128-row boxes.
+// The clustered 128 x 256 tile kernel serves N % 256 == 0 and E <= 512; the 128 x 128
+// kernel serves the rest.
+bool n256_supported(const GemmArgs& g);
+cudaError_t launch_grouped_gemm_n256(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
+                                     int64_t max_m_tiles, cudaStream_t s);
 cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
                                 const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s);
+
+// GEMM over GEMM-tiled operands (tiled.cuh): N % 256 == 0, K % 256 == 0, E <= 512.
+// swiglu: the gate/up epilogue writes h = BF16(silu(gate) * up) to g.h instead of D.
+cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const GemmArgs& g, int64_t max_m_tiles,
+                                      bool swiglu, cudaStream_t s);
+int tiled_max_experts();
+cudaError_t launch_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K, int R,
+                              uint8_t* out, cudaStream_t s);
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renorm, int32_t* ids,
                               float* w, cudaStream_t s);
@@ -71,7 +91,7 @@ cudaError_t launch_swiglu_quant(const void* d, const int32_t* perm, int64_t rows
                                 int64_t I, int64_t Ip, void* h_out, uint8_t* hq, uint8_t* hsf, float* gh,
                                 cudaStream_t s);
 
-constexpr int64_t kPermuteChunk = 1024;   // (token, j) entries per warp in the permute
+constexpr int64_t kPermuteChunk = 256;    // (token, j) entries per warp in the permute
 inline int64_t permute_chunks(int64_t entries) { return (entries + kPermuteChunk - 1) / kPermuteChunk; }
 
 }  // namespace nvfp4

@@ -19,6 +19,7 @@
 #include "launch.h"
 #include "ptx.cuh"
 #include "status.cuh"
+#include "tiled.cuh"
 
 namespace nvfp4 {
 
@@ -26,6 +27,16 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 
 __device__ __forceinline__ int64_t sf_word_offset(int64_t r, int64_t w, int64_t sf_words) {
   return ((r >> 7) * sf_words + w) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+}
+
+// Output addressing for both layouts: 8 bytes of codes at byte `b` of output row `orow`,
+// and the 32-bit word holding scale columns 4w .. 4w+3.
+__device__ __forceinline__ uint8_t* code_ptr(const QuantArgs& a, int64_t orow, int64_t b) {
+  return a.tiled_R ? a.codes + tiled_code_offset(orow, b, a.kblocks, a.tiled_R) : a.codes + orow * a.codes_ld + b;
+}
+__device__ __forceinline__ uint8_t* sfw_ptr(const QuantArgs& a, int64_t orow, int64_t w) {
+  return a.tiled_R ? a.codes + tiled_sf_offset(orow, 4 * w, a.kblocks, a.tiled_R)
+                   : a.sf + sf_word_offset(orow, w, a.sf_words);
 }
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
@@ -237,24 +248,72 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(QuantArgs a) {
   zero_pad_rows(a, warp, nwarp, lane);
 }
 
-// Streaming path (rows up to 2048 columns): every warp keeps kQStages rows in flight in
+// Streaming path (rows up to 2048 columns).  Every warp keeps kQStages rows in flight in
 // a shared-memory ring filled by bulk async copies (cp.async.bulk, completion on an
 // mbarrier), so HBM sees several rows per warp while the warp encodes the current one.
-constexpr int kQStages = 4;
+// Encoding works lane per 16-value block: block b of the row belongs to lane b % 32, so
+// each lane computes its block scale once, stores 8 bytes of codes (a warp stores 256
+// contiguous bytes) and four neighbouring lanes gather one 32-bit scale word.
+constexpr int kQStages = 2;
 constexpr int kQRowBytes = 4096;
-constexpr size_t kQSmem = 8 * kQStages * kQRowBytes + 8 * kQStages * sizeof(uint64_t) + 16;
+constexpr int kQWarps = 8;
+constexpr size_t kQSmem = kQWarps * kQStages * kQRowBytes + kQWarps * kQStages * sizeof(uint64_t) + 16;
 
-template <int RND, int MAXC>
-__global__ void __launch_bounds__(256, 1) quantize_rows_stream_kernel(QuantArgs a) {
+template <int RND>
+__device__ __forceinline__ void encode_block(const QuantArgs& a, int64_t row, int64_t blk, const uint8_t* src,
+                                             float g, float six_g, uint32_t& sf_out, uint2& codes_out) {
+  const uint4 q0 = *reinterpret_cast<const uint4*>(src);
+  const uint4 q1 = *reinterpret_cast<const uint4*>(src + 16);
+  float f[16];
+  {
+    float h0[8], h1[8];
+    bf16x8_to_f32(q0, h0);
+    bf16x8_to_f32(q1, h1);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      f[e] = h0[e];
+      f[8 + e] = h1[e];
+    }
+  }
+  float am = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(f[e]));
+  const BlockScale bs = block_scale(am, g, six_g);
+  float v0[8], v1[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    v0[e] = __fmul_rn(f[e], bs.r);
+    v1[e] = __fmul_rn(f[8 + e], bs.r);
+  }
+  if (RND == kRoundSR) {
+    const uint64_t j = a.rng_offset + (uint64_t)(row * a.cols + blk * 16) / 8u;
+    const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
+    codes_out.x = e2m1x8_sr(v0, philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), k0, k1));
+    codes_out.y = e2m1x8_sr(v1, philox4x32_10(make_uint4((uint32_t)(j + 1), (uint32_t)((j + 1) >> 32), 0u, 0u),
+                                              k0, k1));
+  } else {
+    codes_out.x = e2m1x8_rn(v0);
+    codes_out.y = e2m1x8_rn(v1);
+  }
+  sf_out = bs.sf;
+}
+
+template <int RND>
+__global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(QuantArgs a) {
   extern __shared__ __align__(128) uint8_t qsm[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int64_t warp = (int64_t)blockIdx.x * 8 + wib;
-  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  const int64_t warp = (int64_t)blockIdx.x * kQWarps + wib;
+  const int64_t nwarp = (int64_t)gridDim.x * kQWarps;
   uint8_t* ring = qsm + (size_t)wib * kQStages * kQRowBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + 8 * kQStages * kQRowBytes) + wib * kQStages;
-  volatile int* abort = reinterpret_cast<volatile int*>(qsm + 8 * kQStages * kQRowBytes + 8 * kQStages * 8);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + kQWarps * kQStages * kQRowBytes) + wib * kQStages;
+  volatile int* abort = reinterpret_cast<volatile int*>(qsm + kQWarps * kQStages * kQRowBytes +
+                                                        kQWarps * kQStages * sizeof(uint64_t));
   if (threadIdx.x == 0) *abort = 0;
   const uint32_t row_bytes = (uint32_t)(a.cols * 2);
+  const int64_t nblk = a.cols / 16;
+  const int64_t data_words = (a.cols + 63) / 64;
+  int64_t nrows = a.rows;
+  if (a.rows_dev != nullptr && (int64_t)*a.rows_dev < nrows) nrows = *a.rows_dev;
   if (lane == 0) {
     for (int s = 0; s < kQStages; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -263,37 +322,94 @@ __global__ void __launch_bounds__(256, 1) quantize_rows_stream_kernel(QuantArgs 
   if (lane == 0) {
     for (int s = 0; s < kQStages; ++s) {
       const int64_t r = warp + s * nwarp;
-      if (r < a.rows) {
+      if (r < nrows) {
         mbar_arrive_expect_tx(&bars[s], row_bytes);
         bulk_load(ring + s * kQRowBytes, a.x + r * a.ld, row_bytes, &bars[s]);
       }
     }
   }
+  const int nout = a.map == kMapScatter ? a.k : 1;
   uint32_t parity = 0;
   int s = 0;
-  for (int64_t row = warp; row < a.rows; row += nwarp) {
+  for (int64_t row = warp; row < nrows; row += nwarp) {
     if (!mbar_wait(&bars[s], (parity >> s) & 1u, a.status, abort)) break;
     parity ^= 1u << s;
-    uint4 q[MAXC];
     const uint8_t* buf = ring + s * kQRowBytes;
-#pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-      const int64_t col = 8 * lane + 256 * i;
-      q[i] = col < a.cols ? *reinterpret_cast<const uint4*>(buf + col * 2) : make_uint4(0, 0, 0, 0);
+    if (a.row_filter != nullptr && a.row_filter[row] < 0) {   // a padding slot: nothing to encode
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int64_t r2 = row + (int64_t)kQStages * nwarp;
+        if (r2 < nrows) {
+          mbar_arrive_expect_tx(&bars[s], row_bytes);
+          bulk_load(ring + s * kQRowBytes, a.x + r2 * a.ld, row_bytes, &bars[s]);
+        }
+      }
+      s = s + 1 == kQStages ? 0 : s + 1;
+      continue;
     }
-    fence_proxy_async_smem();   // reads of this buffer precede the next bulk write into it
+    float g;
+    if (a.mode == kScopeRow) {
+      float m = 0.0f;
+      for (int64_t b = lane; b < nblk; b += 32) {
+        float h0[8], h1[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(buf + b * 32), h0);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(buf + b * 32 + 16), h1);
+        m = fmaxf(m, fmaxf(absmax8(h0), absmax8(h1)));
+      }
+      m = warp_max(m);
+      g = a.g_in ? a.g_in[row] : __fdiv_rn(m, kGlobalDivisor);
+    } else if (a.mode == kScopeTensor) {
+      g = a.g_in ? a.g_in[0] : __fdiv_rn(__uint_as_float(a.amax_bits[0]), kGlobalDivisor);
+    } else {
+      const int64_t gi = row / a.group_rows;
+      g = a.g_in ? a.g_in[gi] : __fdiv_rn(__uint_as_float(a.amax_bits[gi]), kGlobalDivisor);
+    }
+    const float six_g = __fmul_rn(6.0f, g);
+    const int64_t orow0 = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
+    int32_t my_slot = 0;
+    if (a.map == kMapScatter && lane < a.k) my_slot = a.inv[row * a.k + lane];
+    for (int64_t b0 = 0; b0 < nblk; b0 += 32) {
+      const int64_t blk = b0 + lane;
+      const bool active = blk < nblk;
+      uint32_t sfb = 0;
+      uint2 cw = make_uint2(0u, 0u);
+      if (active) encode_block<RND>(a, row, blk, buf + blk * 32, g, six_g, sfb, cw);
+      const uint32_t s1 = __shfl_down_sync(kFull, sfb, 1);
+      const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
+      const uint32_t s3 = __shfl_down_sync(kFull, sfb, 3);
+      const uint32_t sfw = sfb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      for (int j = 0; j < nout; ++j) {
+        const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
+        if (orow < 0) continue;   // entry whose expert id was rejected: no slot
+        if (active) *reinterpret_cast<uint2*>(code_ptr(a, orow, blk * 8)) = cw;
+        if ((lane & 3) == 0 && active) *reinterpret_cast<uint32_t*>(sfw_ptr(a, orow, blk / 4)) = sfw;
+      }
+    }
+    fence_proxy_async_smem();   // this row's reads of the buffer precede the next bulk write
     __syncwarp();
     if (lane == 0) {
       const int64_t r2 = row + (int64_t)kQStages * nwarp;
-      if (r2 < a.rows) {
+      if (r2 < nrows) {
         mbar_arrive_expect_tx(&bars[s], row_bytes);
         bulk_load(ring + s * kQRowBytes, a.x + r2 * a.ld, row_bytes, &bars[s]);
       }
     }
-    quantize_row<RND, MAXC>(a, row, q, lane);
+    for (int j = 0; j < nout; ++j) {
+      const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
+      if (orow < 0) continue;
+      for (int64_t w = data_words + lane; w < a.sf_words; w += 32) *reinterpret_cast<uint32_t*>(sfw_ptr(a, orow, w)) = 0u;
+      for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
+        *reinterpret_cast<uint2*>(code_ptr(a, orow, b)) = make_uint2(0u, 0u);
+      if (lane == 0 && a.g_out != nullptr) {
+        if (a.mode == kScopeRow) a.g_out[a.map == kMapScatter ? orow : row] = g;
+        else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
+        else if (a.mode == kScopeGroup && row % a.group_rows == 0) a.g_out[row / a.group_rows] = g;
+      }
+    }
     s = s + 1 == kQStages ? 0 : s + 1;
   }
-  zero_pad_rows(a, warp, nwarp, lane);
+  if (a.tiled_R == 0) zero_pad_rows(a, warp, nwarp, lane);
 }
 
 template <int RND>
@@ -309,29 +425,19 @@ static cudaError_t launch_quant_rnd(const QuantArgs& a, int maxc, int grid, cuda
   return cudaGetLastError();
 }
 
-template <int RND, int MAXC>
+template <int RND>
 static cudaError_t launch_stream(const QuantArgs& a, int grid, cudaStream_t s) {
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(quantize_rows_stream_kernel<RND, MAXC>,
+    cudaError_t e = cudaFuncSetAttribute(quantize_rows_stream_kernel<RND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr[dev] = true;
   }
-  quantize_rows_stream_kernel<RND, MAXC><<<grid, 256, kQSmem, s>>>(a);
+  quantize_rows_stream_kernel<RND><<<grid, kQWarps * 32, kQSmem, s>>>(a);
   return cudaGetLastError();
-}
-
-template <int RND>
-static cudaError_t launch_stream_rnd(const QuantArgs& a, int maxc, int grid, cudaStream_t s) {
-  switch (maxc) {
-    case 1: return launch_stream<RND, 1>(a, grid, s);
-    case 2: return launch_stream<RND, 2>(a, grid, s);
-    case 4: return launch_stream<RND, 4>(a, grid, s);
-    default: return launch_stream<RND, 8>(a, grid, s);
-  }
 }
 
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t group_rows,
@@ -361,10 +467,18 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
   const int sms = num_sms();
   int64_t blocks = (a.rows_total + 7) / 8;
   // rows of up to 2048 columns whose pitch keeps every row 16-byte aligned: streaming path
-  if (maxc <= 8 && (a.ld * 2) % 16 == 0) {
-    if (blocks > sms) blocks = sms;
-    return rounding == kRoundSR ? launch_stream_rnd<kRoundSR>(a, maxc, (int)blocks, s)
-                                : launch_stream_rnd<kRoundRNE>(a, maxc, (int)blocks, s);
+  // (the only one that writes the GEMM-tiled layout or takes a row filter / device count)
+  const bool stream_ok = maxc <= 8 && (a.ld * 2) % 16 == 0;
+  if (!stream_ok && (a.tiled_R != 0 || a.row_filter != nullptr || a.rows_dev != nullptr)) return cudaErrorInvalidValue;
+  if (stream_ok) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_rows_stream_kernel<kRoundRNE>,
+                                                      kQWarps * 32, kQSmem) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    const int64_t cap_s = (int64_t)per_sm * sms;
+    int64_t b = (a.rows_total + kQWarps - 1) / kQWarps;
+    if (b > cap_s) b = cap_s;
+    return rounding == kRoundSR ? launch_stream<kRoundSR>(a, (int)b, s) : launch_stream<kRoundRNE>(a, (int)b, s);
   }
   const int64_t cap = (int64_t)(maxc <= 8 ? 8 : 4) * sms;
   if (blocks > cap) blocks = cap;

@@ -50,3 +50,40 @@ def check_bf16_against(got_bits: np.ndarray, ref: np.ndarray, rel: float = 1e-3,
     bound = bf16_ulp(ref) + rel * np.maximum(np.abs(ref), tau)
     bad = np.abs(got - ref) > bound
     return int(bad.sum()), float((np.abs(got - ref) / np.maximum(bound, 1e-300)).max()) if ref.size else 0.0
+
+
+# --------------------------------------------------------------------------- GEMM-tiled layout
+# Host implementation of the layout documented in include/nvfp4moe.h (blocks of R rows x
+# 256 K-values: R*128 bytes of 128-byte-swizzled codes, then (R/128)*2048 bytes of scales).
+
+def _tiled_index(rows_pad, K, R):
+    kb = K // 256
+    r = np.arange(rows_pad)[:, None]
+    b = np.arange(K // 2)[None, :]
+    blk, rr = r // R, r % R
+    code_off = (blk * kb + b // 128) * (R * 144) + rr * 128 + (((b % 128) // 16) ^ (rr % 8)) * 16 + (b % 16)
+    c = np.arange(K // 16)[None, :]
+    cc = c % 16
+    sf_off = ((blk * kb + c // 16) * (R * 144) + R * 128 + (rr // 128) * 2048 + (cc // 4) * 512
+              + (rr % 128 % 32) * 16 + (rr % 128 // 32) * 4 + cc % 4)
+    return code_off, sf_off
+
+
+def pack_tiled_host(codes_nib: np.ndarray, sf_rowmajor: np.ndarray, R: int) -> np.ndarray:
+    """codes nibbles [rows, K] + row-major scales [rows, K/16] -> tiled bytes (pad rows 0)."""
+    rows, K = codes_nib.shape
+    rows_pad = (rows + R - 1) // R * R
+    out = np.zeros(rows_pad // R * (K // 256) * R * 144, np.uint8)
+    co, so = _tiled_index(rows_pad, K, R)
+    packed = F.pack_e2m1(codes_nib)
+    out[co[:rows]] = packed
+    out[so[:rows]] = sf_rowmajor
+    return out
+
+
+def untile_host(buf: np.ndarray, rows: int, K: int, R: int):
+    """tiled bytes -> (codes nibbles [rows, K], row-major scales [rows, K/16])."""
+    rows_pad = (rows + R - 1) // R * R
+    co, so = _tiled_index(rows_pad, K, R)
+    buf = np.asarray(buf, np.uint8)
+    return F.unpack_e2m1(buf[co[:rows]]), buf[so[:rows]]

@@ -20,7 +20,8 @@ def test_every_declared_function_is_exported(lib):
     expected = {"nvfp4_quantize", "nvfp4_grouped_gemm", "moe_expert_forward", "moe_route_topk", "moe_permute",
                 "moe_combine", "moe_swiglu_quantize", "moe_prepare_weights", "nvfp4_status_check",
                 "nvfp4_status_string", "nvfp4_sf_bytes", "moe_weights_sizes", "nvfp4_workspace_size",
-                "moe_forward_workspace_layout"}
+                "moe_forward_workspace_layout", "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled",
+                "nvfp4_tiled_bytes", "nvfp4_quantize_noalloc"}
     assert expected <= set(names)
     for n in names:
         assert hasattr(lib, n), n
@@ -31,13 +32,15 @@ def test_sf_bytes_and_weight_sizes(lib):
     assert L.nvfp4_sf_bytes(16384, 2048) == 128 * 32 * 512
     assert L.nvfp4_sf_bytes(1, 16) == 512
     assert L.nvfp4_sf_bytes(129, 80) == 2 * 2 * 512
-    sizes = (ctypes.c_size_t * 6)()
+    sizes = (ctypes.c_size_t * 4)()
     assert lib.moe_weights_sizes(128, 2048, 768, sizes) == 0
-    assert list(sizes) == [128 * 1536 * 1024, 128 * 1536 // 128 * 32 * 512, 512,
-                           128 * 2048 * 384, 128 * 2048 // 128 * 12 * 512, 512]
+    # GEMM-tiled: 256-row blocks of 256 K-values, 144 bytes per row per block (128 codes + 16 scales)
+    assert list(sizes) == [128 * 1536 // 256 * 8 * 256 * 144, 512, 128 * 2048 // 256 * 3 * 256 * 144, 512]
     # I not a multiple of 256: the down projection's K is zero-padded to 256
     assert lib.moe_weights_sizes(8, 256, 128, sizes) == 0
-    assert sizes[3] == 8 * 256 * 128 and sizes[4] == 8 * 256 // 128 * 4 * 512
+    assert sizes[2] == 8 * 256 // 256 * 1 * 256 * 144
+    assert L.nvfp4_tiled_bytes(129, 512, 128) == 2 * 2 * 128 * 144
+    assert L.nvfp4_tiled_bytes(100, 300, 128) == 0          # K not a multiple of 256
 
 
 def test_forward_workspace_layout(lib):
@@ -49,7 +52,9 @@ def test_forward_workspace_layout(lib):
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lay[12] + mcap * H * 2 <= lay[14]
     assert lib.nvfp4_workspace_size(L.OP_MOE_FORWARD, T, k, E, H, I) == lay[14]
-    assert lay[6] - lay[5] >= mcap * H // 2
+    assert lay[6] == lay[5] and lay[10] == lay[9]              # scales live inside the tiles
+    assert lay[7] - lay[5] >= mcap // 128 * 8 * 128 * 144      # Aq tiled, K = H
+    assert lay[11] - lay[9] >= mcap // 128 * 3 * 128 * 144     # hq tiled, K = Ip
 
 
 def test_host_argument_checks_return_before_any_cuda_call(lib):

@@ -64,26 +64,29 @@ def _valid_rows(ops):
     return np.concatenate([np.arange(p, p + c) for p, c in zip(ops["padded"][:-1], ops["counts"])]).astype(int)
 
 
-def test_gemm_single_tile_exact(cuda_lib):
-    """One expert, one 128x128 tile, K = 256; E2M1 grid values times powers of two so
-    every partial sum is exact in float32: the result must be bit-exact."""
+@pytest.mark.parametrize("N", [128, 256])
+def test_gemm_single_tile_exact(cuda_lib, N):
+    """One expert, one 128xN tile (both tile widths of the kernel), K = 256; E2M1 grid
+    values times powers of two so every partial sum is exact in float32: the result
+    must be bit-exact."""
     rng = np.random.default_rng(0)
     grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -2, -3, -4, -6])
     s_a, s_w = 448 * 2.0 ** -11, 448 * 2.0 ** -13
     xa = rng.choice(grid, (128, 256)) * s_a
     xa[:, ::16] = 6 * s_a
-    w = rng.choice(grid, (1, 128, 256)) * s_w
+    w = rng.choice(grid, (1, N, 256)) * s_w
     w[:, :, ::16] = 6 * s_w
     ops = _operands_from_oracle(F.bf16_round(xa), [128], F.bf16_round(w))
     ref = _oracle(ops)
-    D = npy(_run_gpu(cuda_lib, ops, 128, 256, torch.float32))
+    D = npy(_run_gpu(cuda_lib, ops, N, 256, torch.float32))
     np.testing.assert_array_equal(D, ref.astype(np.float32))
     np.testing.assert_array_equal(ref, (xa @ w[0].T))          # lossless quantisation
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_gemm_ragged_groups(cuda_lib, out_dtype):
-    E, N, K = 6, 384, 512
+@pytest.mark.parametrize("N", [384, 512])
+def test_gemm_ragged_groups(cuda_lib, out_dtype, N):
+    E, K = 6, 512
     counts = [0, 1, 127, 128, 129, 300]
     a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=31))
     w_bits = S.bf16_bits(S.randn_bf16((E, N, K), 0.02, seed=32))
@@ -116,8 +119,9 @@ def test_gemm_qwen_shaped_k_and_many_experts(cuda_lib):
     assert mx <= 1e-3, (mx, nw)
 
 
-def test_gemm_leaves_rows_outside_groups_untouched(cuda_lib):
-    E, N, K = 2, 128, 256
+@pytest.mark.parametrize("N", [128, 256])
+def test_gemm_leaves_rows_outside_groups_untouched(cuda_lib, N):
+    E, K = 2, 256
     counts = [5, 130]
     a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=51))
     w_bits = S.bf16_bits(S.randn_bf16((E, N, K), 0.02, seed=52))
@@ -145,3 +149,80 @@ def test_gemm_is_deterministic(cuda_lib):
     d2 = npy(_run_gpu(cuda_lib, ops, N, K, torch.float32))
     rows = _valid_rows(ops)
     np.testing.assert_array_equal(d1[rows], d2[rows])
+
+
+# ------------------------------------------------------------------ GEMM-tiled operands
+
+def _run_tiled(lib, ops, N, K, out_dtype=torch.float32, epilogue=0):
+    from gpu_util import pack_tiled_host
+    E = ops["b_codes"].shape[0]
+    A = dev(pack_tiled_host(ops["a_codes"], ops["a_sf"], 128))
+    B = dev(pack_tiled_host(ops["b_codes"].reshape(E * N, K), ops["b_sf"].reshape(E * N, K // 16), 256))
+    D = lib.nvfp4_grouped_gemm_tiled(A, dev(ops["a_g"]), B, dev(ops["b_g"]), dev(ops["padded"]), dev(ops["counts"]),
+                                     ops["M"], N, K, E, out_dtype=out_dtype, epilogue=epilogue)
+    assert lib.nvfp4_status_check() == 0
+    return D
+
+
+def test_tiled_gemm_exact_single_tile(cuda_lib):
+    rng = np.random.default_rng(0)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -2, -3, -4, -6])
+    s_a, s_w = 448 * 2.0 ** -11, 448 * 2.0 ** -13
+    xa = rng.choice(grid, (128, 512)) * s_a
+    xa[:, ::16] = 6 * s_a
+    w = rng.choice(grid, (1, 256, 512)) * s_w
+    w[:, :, ::16] = 6 * s_w
+    ops = _operands_from_oracle(F.bf16_round(xa), [128], F.bf16_round(w))
+    D = npy(_run_tiled(cuda_lib, ops, 256, 512))
+    np.testing.assert_array_equal(D, (xa @ w[0].T).astype(np.float32))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_tiled_gemm_ragged_groups_matches_oracle_and_row_major_kernel(cuda_lib, out_dtype):
+    E, N, K = 6, 512, 768
+    counts = [0, 1, 127, 128, 129, 300]
+    a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=71))
+    w_bits = S.bf16_bits(S.randn_bf16((E, N, K), 0.02, seed=72))
+    ops = _operands_from_oracle(a_bits, counts, w_bits)
+    ref = _oracle(ops)
+    Dt = _run_tiled(cuda_lib, ops, N, K, out_dtype)
+    Dr = _run_gpu(cuda_lib, ops, N, K, out_dtype)
+    rows = _valid_rows(ops)
+    if out_dtype == torch.float32:
+        mx, nw = rel_err_floor(npy(Dt)[rows], ref[rows])
+        assert mx <= 1e-3, (mx, nw)
+    else:
+        nbad, worst = check_bf16_against(u16(Dt)[rows], ref[rows])
+        assert nbad == 0, worst
+    # same MMA sequence as the row-major kernel: identical bits
+    np.testing.assert_array_equal(npy(Dt.view(torch.int32) if out_dtype == torch.float32 else Dt.view(torch.int16))[rows],
+                                  npy(Dr.view(torch.int32) if out_dtype == torch.float32 else Dr.view(torch.int16))[rows])
+
+
+def test_pack_tiled_matches_host_layout(cuda_lib):
+    from gpu_util import pack_tiled_host
+    rows, K = 300, 512
+    bits = S.bf16_bits(S.randn_bf16((rows, K), seed=81))
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    codes, sf, _ = cuda_lib.nvfp4_quantize(x, cuda_lib.SCALE_PER_ROW)
+    q = Q.quantize(bits, scope="row")
+    for R in (128, 256):
+        got = npy(cuda_lib.nvfp4_pack_tiled(codes, sf, rows, K, R))
+        np.testing.assert_array_equal(got, pack_tiled_host(q["codes"], q["sf"], R))
+
+
+def test_tiled_swiglu_epilogue_equals_standalone_swiglu(cuda_lib):
+    """gate/up GEMM with the SwiGLU epilogue == BF16 GEMM output followed by the
+    standalone SwiGLU kernel (64-row interleaved gate/up weights), bit for bit."""
+    E, I, K = 3, 256, 512
+    counts = [200, 0, 77]
+    a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=91))
+    w_bits = S.bf16_bits(S.randn_bf16((E, 2 * I, K), 0.05, seed=92))
+    ops = _operands_from_oracle(a_bits, counts, w_bits)
+    h_fused = u16(_run_tiled(cuda_lib, ops, 2 * I, K, epilogue=1))
+    D = _run_gpu(cuda_lib, ops, 2 * I, K, torch.bfloat16)
+    perm = np.full(ops["M"], -1, np.int32)
+    perm[_valid_rows(ops)] = 0
+    h, _, _, _ = cuda_lib.moe_swiglu_quantize(D, dev(perm), I)
+    rows = _valid_rows(ops)
+    np.testing.assert_array_equal(h_fused[rows], u16(h)[rows])
