@@ -200,7 +200,7 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const floa
  *   epilogue NVFP4_EPILOGUE_SWIGLU: B holds gate/up rows interleaved in 64-row chunks
  *     (as nvfp4_moe_weights.w13); D receives BF16 h [M_total, N/2] (row pitch N/2,
  *     ldd and out_dtype ignored) with h = BF16(silu(gate) * up) from the BF16-rounded gate
- *     and up outputs -- the value nearest to the exact real number. */
+ *     and up outputs: silu(gate) * up evaluated in float64 and rounded once to BF16. */
 enum { NVFP4_EPILOGUE_STORE = 0, NVFP4_EPILOGUE_SWIGLU = 1 };
 nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A_tiled, const float* gA, const uint8_t* B_tiled,
                                       const float* gB, const int32_t* group_offsets,
@@ -245,7 +245,7 @@ nvfp4_status moe_combine(const void* y, const int32_t* inv, const float* w, int6
 
 /* SwiGLU of the interleaved gate/up output followed by per-row NVFP4 requantisation.
  * For each row r with perm[r] >= 0 and each c < I:
- *     h[r, c] = BF16( silu(gate) * up )   (the nearest BF16 to the exact value)
+ *     h[r, c] = BF16( silu(gate) * up )   (evaluated in float64, rounded once)
  * where gate/up are D's columns in the 64-chunk interleave of nvfp4_moe_weights; then
  * h's row is quantised with a per-row scale into hq [rows, Ip/2] (zero-padded to
  * Ip = round_up(I, 256)), tiled scales (Ip/16 columns) and gh [rows].

@@ -332,8 +332,14 @@ nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A, const float* gA, const u
   g.status = device_status_ptr();
   g.h = static_cast<__nv_bfloat16*>(D);
   g.I = N / 2;
-  return from_cuda(launch_grouped_gemm_tiled(A, B, g, M_total / 128, epilogue == NVFP4_EPILOGUE_SWIGLU,
-                                             static_cast<cudaStream_t>(stream)));
+  const bool swiglu = epilogue == NVFP4_EPILOGUE_SWIGLU;
+  CUtensorMap md;
+  const bool ok = swiglu ? make_map(&md, D, M_total, N / 2, N, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2)
+                         : make_map(&md, D, M_total, N, ldd * (g.out_f32 ? 4 : 2), 32,
+                                    g.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                    g.out_f32 ? 4 : 2);
+  if (!ok) return NVFP4_ERR_CUDA;
+  return from_cuda(launch_grouped_gemm_tiled(A, B, md, g, M_total / 128, swiglu, static_cast<cudaStream_t>(stream)));
 }
 
 nvfp4_status nvfp4_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K, int32_t block_rows,
@@ -514,7 +520,11 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   g1.status = status;
   g1.h = hbuf;
   g1.I = I;
-  e = launch_grouped_gemm_tiled(aq, wt->w13, g1, mcap / 128, true, s);
+  CUtensorMap mh, my;
+  if (!make_map(&mh, hbuf, mcap, I, I * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2) ||
+      !make_map(&my, ybuf, mcap, H, H * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2))
+    return NVFP4_ERR_CUDA;
+  e = launch_grouped_gemm_tiled(aq, wt->w13, mh, g1, mcap / 128, true, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
   // 4. per-row NVFP4 of h (routed rows only), K zero-padded to Ip, GEMM-tiled
@@ -551,7 +561,7 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   g2.ldd = H;
   g2.out_f32 = 0;
   g2.status = status;
-  e = launch_grouped_gemm_tiled(hq, wt->w2, g2, mcap / 128, false, s);
+  e = launch_grouped_gemm_tiled(hq, wt->w2, my, g2, mcap / 128, false, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
   // 6. weighted un-permute

@@ -18,9 +18,14 @@
 //               K=64) into a 256-column TMEM accumulator, tcgen05.commit;
 //   warps 3-10  epilogue, two per TMEM lane quadrant (128 columns each): drain the
 //               accumulator into registers, release it, scale by gA[r]*gB[e] in float32
-//               and store BF16 / float32 rows of the group -- or, in the SwiGLU mode of
+//               and write BF16 / float32 rows of the group -- or, in the SwiGLU mode of
 //               the gate/up projection, form h = BF16(silu(gate) * up) from the BF16-
-//               rounded gate and up columns and store h only.
+//               rounded gate and up columns and write h only.  Each warp stages its 32
+//               rows x 128 bytes in a 128-byte-swizzled shared-memory box and hands it to
+//               one TMA store: a thread-per-row register layout stored directly would cost
+//               one 16-byte L2 request per row and chunk, and paced the kernel when K is
+//               small.  The 32-row slab of a group's last, partial tile is stored row by
+//               row, so rows outside the groups are never written.
 // Tiles are (128-row block) x (256 columns), row-block-major; no split-K, fixed K order.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -37,7 +42,8 @@ namespace nvfp4 {
 namespace gt {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
+constexpr int kOutBox = 32 * 128;           // one epilogue warp's staged output box
 constexpr int kABlock = 128 * 144;          // 16 KB codes + 2 KB scales
 constexpr int kBBlock = 256 * 144;          // 32 KB codes + 4 KB scales
 constexpr int kACodes = 128 * 128;
@@ -54,6 +60,7 @@ constexpr int kMaxE = 512;
 struct Smem {
   uint8_t a[kStages][kABlock];
   uint8_t b[kStages][kBBlock];
+  uint8_t out[kEpiWarps][kOutBox];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t accf;
@@ -70,9 +77,29 @@ static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 }  // namespace gt
 
+// One lane's 128-byte row of a warp's 32-row output box, written 128-byte swizzled (16-byte
+// chunk j at (j ^ (row % 8)) * 16, the TMA SWIZZLE_128B image), then one TMA store of the
+// box at column x, row y.  The buffer is reused only after the previous store read it.
+__device__ __forceinline__ void store_box(uint8_t* buf, const uint32_t (&w)[32], int lane,
+                                          const CUtensorMap* map, int32_t x, int32_t y) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, x, y);
+    bulk_commit();
+  }
+}
+
 template <bool kSwiGLU>
 __global__ void __launch_bounds__(gt::kThreads, 1)
-    grouped_gemm_tiled_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, const GemmArgs g) {
+    grouped_gemm_tiled_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B,
+                              const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
   using namespace gt;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -173,10 +200,11 @@ __global__ void __launch_bounds__(gt::kThreads, 1)
     mma_done:;
     }
   } else {
-    // epilogue: lane quadrant q = warp % 4, column half of the tile = (warp - 3) / 4
+    // epilogue: TMEM lane quadrant q = warp % 4 (the lanes this warp may read), column
+    // half of the tile = (warp - 3) / 4
     const int q = warp & 3;
     const int half = (warp - kFirstEpiWarp) >> 2;
-    const int elt = g.out_f32 ? 4 : 2;
+    uint8_t* buf = sm.out[warp - kFirstEpiWarp];
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
@@ -184,72 +212,158 @@ __global__ void __launch_bounds__(gt::kThreads, 1)
       const int e = find_group(sm.offsets, g.E, row0);
       const int32_t in_group = sm.rows[e] - (row0 - sm.offsets[e]);
       const bool valid = q * 32 + lane < in_group;
+      const bool full_warp = q * 32 + 32 <= in_group;             // warp-uniform
       const int64_t row = (int64_t)row0 + q * 32 + lane;
       const float ga = valid ? g.ga[row] : 0.0f;
-      if (!mbar_wait(&sm.accf, it & 1, g.status, abort)) break;
+      // every lane waits (bounded), then the warp leaves together if any lane gave up
+      const bool acc_ready = mbar_wait(&sm.accf, it & 1, g.status, abort);
+      if (!__all_sync(0xFFFFFFFFu, acc_ready)) break;
       tc_fence_after();
       const float scale = __fmul_rn(ga, sm.gb[e]);
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + half * 128;
-      uint32_t v[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) NVFP4_TMEM_LD_X32(taddr + 32 * c, v[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.acce);
-      if (!valid) continue;
+      // Skip only warp-uniformly: every lane of a partial slab computes (whatever the
+      // rows past the group hold, the arithmetic below ends), so the warp-wide votes and
+      // syncs see all 32 lanes; only the row-by-row stores of a partial slab depend on
+      // the lane.
+      const bool skip = q * 32 >= in_group;
+      const int32_t y = row0 + q * 32;
       if (kSwiGLU) {
         // columns [0, 64) of this half are gate, [64, 128) up, for h columns
-        // n_tile*128 + half*64 + [0, 64) (64-row gate/up interleave of W13)
-        __nv_bfloat16* hp = g.h + row * g.I + (int64_t)n_tile * 128 + half * 64;
-#pragma unroll
+        // n_tile*128 + half*64 + [0, 64) (64-row gate/up interleave of W13).  Two rounds
+        // of 32 gate + 32 up columns keep the live registers low; the accumulator is
+        // released after the second drain (the load stages cover that wait).  In each
+        // round all 32 values take the branch-free float32 path first (independent
+        // chains the compiler can interleave) and the rare values it cannot settle are
+        // redone after, warp-uniformly; the round's 64 bytes of h go straight to the
+        // staging box (full slabs) or to global memory (a group's partial slab).
+        if (full_warp) {
+          if (lane == 0) bulk_wait_read<0>();   // the previous box has been read
+          __syncwarp();
+        }
+#pragma unroll 1
         for (int c = 0; c < 2; ++c) {
+          uint32_t vg[32], vu[32];
+          NVFP4_TMEM_LD_X32(taddr + 32 * c, vg);
+          NVFP4_TMEM_LD_X32(taddr + 64 + 32 * c, vu);
+          tmem_ld_wait();
+          if (c == 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.acce);
+          }
+          if (skip) continue;
+          // gu: BF16 gate | BF16 up << 16, one rounding instruction per pair
+          uint32_t gu[32];
 #pragma unroll
-          for (int u8 = 0; u8 < 4; ++u8) {
-            uint32_t w[4];
+          for (int i = 0; i < 32; ++i) {
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(vg[i]), scale),
+                                                            __fmul_rn(__uint_as_float(vu[i]), scale));
+            gu[i] = *reinterpret_cast<const uint32_t*>(&pr);
+          }
+          uint32_t w[16];
+          uint32_t redo = 0;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              uint32_t hb[2];
+          for (int p = 0; p < 16; ++p) {
+            uint32_t hb[2];
 #pragma unroll
-              for (int s2 = 0; s2 < 2; ++s2) {
-                const int i = 8 * u8 + 2 * p + s2;
-                const float gate = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__uint_as_float(v[c][i]), scale)));
-                const float up = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__uint_as_float(v[c + 2][i]), scale)));
-                hb[s2] = swiglu_bf16(gate, up);
-              }
-              w[p] = hb[0] | (hb[1] << 16);
+            for (int s2 = 0; s2 < 2; ++s2) {
+              const uint32_t x2 = gu[2 * p + s2];
+              if (!swiglu_fast(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u), hb[s2]))
+                redo |= 1u << (2 * p + s2);
             }
-            *reinterpret_cast<uint4*>(hp + 32 * c + 8 * u8) = make_uint4(w[0], w[1], w[2], w[3]);
+            w[p] = hb[0] | (hb[1] << 16);
+          }
+          // each round of the redo: every lane with a pending value selects its lowest
+          // one (unrolled selects, no indexed registers), one inlined exact evaluation
+          // serves the warp, the result is patched into w
+          while (__any_sync(0xFFFFFFFFu, redo != 0)) {
+            const int idx = redo != 0 ? __ffs((int)redo) - 1 : -1;
+            uint32_t x2 = 0x3F803F80u;   // lanes with nothing pending evaluate gate = up = 1
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x2 = idx == j ? gu[j] : x2;
+            const uint32_t hb = swiglu_exact(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              uint32_t& word = w[j >> 1];
+              const uint32_t patched = (j & 1) ? (word & 0xFFFFu) | (hb << 16) : (word & 0xFFFF0000u) | hb;
+              word = idx == j ? patched : word;
+            }
+            redo &= redo - 1;
+          }
+          if (full_warp) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + (((4 * c + j) ^ (lane & 7)) << 4)) =
+                  make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          } else if (valid) {
+            __nv_bfloat16* hp = g.h + row * g.I + n_tile * 128 + half * 64 + 32 * c;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(hp + 8 * j) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
+        }
+        if (full_warp) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmd, buf, n_tile * 128 + half * 64, y);
+            bulk_commit();
           }
         }
       } else {
-        uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + (int64_t)n_tile * kBN + half * 128) * elt;
+        uint32_t v[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (g.out_f32) {
+        for (int c = 0; c < 4; ++c) NVFP4_TMEM_LD_X32(taddr + 32 * c, v[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.acce);
+        if (skip) continue;
+        if (!g.out_f32) {
 #pragma unroll
-            for (int u4 = 0; u4 < 8; ++u4)
-              *reinterpret_cast<float4*>(dp + (32 * c + 4 * u4) * 4) =
-                  make_float4(__fmul_rn(__uint_as_float(v[c][4 * u4]), scale),
-                              __fmul_rn(__uint_as_float(v[c][4 * u4 + 1]), scale),
-                              __fmul_rn(__uint_as_float(v[c][4 * u4 + 2]), scale),
-                              __fmul_rn(__uint_as_float(v[c][4 * u4 + 3]), scale));
-          } else {
+          for (int b2 = 0; b2 < 2; ++b2) {
+            uint32_t w[32];
 #pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4) {
-              uint32_t w[4];
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
-              for (int p = 0; p < 4; ++p) {
-                const __nv_bfloat162 b2 =
-                    __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][8 * u4 + 2 * p]), scale),
-                                          __fmul_rn(__uint_as_float(v[c][8 * u4 + 2 * p + 1]), scale));
-                w[p] = *reinterpret_cast<const uint32_t*>(&b2);
+              for (int p = 0; p < 16; ++p) {
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(
+                    __fmul_rn(__uint_as_float(v[2 * b2 + c][2 * p]), scale),
+                    __fmul_rn(__uint_as_float(v[2 * b2 + c][2 * p + 1]), scale));
+                w[16 * c + p] = *reinterpret_cast<const uint32_t*>(&pr);
               }
-              *reinterpret_cast<uint4*>(dp + (32 * c + 8 * u4) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            const int32_t x = n_tile * kBN + half * 128 + 64 * b2;
+            if (full_warp) {
+              store_box(buf, w, lane, &tmd, x, y);
+            } else if (valid) {
+              uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + x) * 2;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(dp + 16 * j) =
+                    make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__fmul_rn(__uint_as_float(v[c][i]), scale));
+            const int32_t x = n_tile * kBN + half * 128 + 32 * c;
+            if (full_warp) {
+              store_box(buf, w, lane, &tmd, x, y);
+            } else if (valid) {
+              uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + x) * 4;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(dp + 16 * j) =
+                    make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
             }
           }
         }
       }
     }
+    if (lane == 0) bulk_wait_all<0>();   // the last boxes are read before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -259,8 +373,8 @@ __global__ void __launch_bounds__(gt::kThreads, 1)
 }
 
 template <bool kSwiGLU>
-static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const GemmArgs& g, int64_t max_m_tiles,
-                                cudaStream_t s) {
+static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
+                                int64_t max_m_tiles, cudaStream_t s) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -274,13 +388,13 @@ static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const GemmAr
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
-  grouped_gemm_tiled_kernel<kSwiGLU><<<grid, gt::kThreads, gt::kSmemBytes, s>>>(A, B, g);
+  grouped_gemm_tiled_kernel<kSwiGLU><<<grid, gt::kThreads, gt::kSmemBytes, s>>>(A, B, tmd, g);
   return cudaGetLastError();
 }
 
-cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const GemmArgs& g, int64_t max_m_tiles,
-                                      bool swiglu, cudaStream_t s) {
-  return swiglu ? launch_tiled<true>(A, B, g, max_m_tiles, s) : launch_tiled<false>(A, B, g, max_m_tiles, s);
+cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
+                                      int64_t max_m_tiles, bool swiglu, cudaStream_t s) {
+  return swiglu ? launch_tiled<true>(A, B, tmd, g, max_m_tiles, s) : launch_tiled<false>(A, B, tmd, g, max_m_tiles, s);
 }
 
 int tiled_max_experts() { return gt::kMaxE; }

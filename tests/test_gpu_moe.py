@@ -121,6 +121,53 @@ def test_swiglu_quantize_bit_exact(cuda_lib):
     np.testing.assert_array_equal(sf[live], q["sf"])
 
 
+def _swiglu_hard_pairs(n_random=8_000_000, seed=11):
+    """(gate, up) BF16 pairs whose SwiGLU value lies near a BF16 rounding midpoint: the
+    cases the float32 fast path hands to its slower exact path.  Three families:
+    (a) random pairs whose float64 value is within 2^-14 BF16 ulp of a midpoint;
+    (b) gate in [8, 48] with gate*up exactly a midpoint, where silu(gate)*up sits just
+        below it by exp(-gate) (the float64 reference ties to even once 1 + exp(-gate)
+        rounds to 1, above gate = 36.74);
+    (c) range edges: |gate| near and beyond 80, tiny and huge products."""
+    rng = np.random.default_rng(seed)
+    bf = lambda v: F.bf16_to_f32(F.bf16_round(v)).astype(np.float64)  # noqa: E731
+    g = bf(rng.standard_normal(n_random) * rng.choice([0.05, 0.3, 1, 4, 20], n_random))
+    u = bf(rng.standard_normal(n_random) * rng.choice([0.01, 1, 100], n_random))
+    ref = M.silu(g) * u
+    _, ex = np.frexp(np.abs(ref))
+    pos = np.abs(ref) / np.exp2(ex - 8.0)                  # in BF16 ulps; midpoints at .5
+    near = (np.abs(pos - np.floor(pos) - 0.5) < 2.0 ** -14) & (ref != 0)
+    ga, ua = g[near], u[near]
+    gs = bf(np.linspace(8, 48, 321))
+    us = bf(rng.standard_normal(3000) * 2)
+    G2, U2 = (a.ravel() for a in np.meshgrid(gs, us))
+    prod = (G2.astype(np.float32) * U2.astype(np.float32)).view(np.uint32)
+    mid = (prod & 0xFFFF) == 0x8000
+    gb, ub = G2[mid], U2[mid]
+    gc = bf(np.array([79.5, 80, 80.5, 81, -79.5, -80, -80.5, -81, -87, -88.5, -100, -200, 1e-20, -1e-20, 1e-3, 3e4]))
+    uc = bf(np.array([1.5, -3, 1e30, 2e-30, 1e38, -1e37, 1e35, 7e38, 1e-30, 1e25, 5e-39, 1.0, 1e20, 1e-10, 3e33,
+                      -2e-35]))
+    return np.concatenate([ga, gb, gc]), np.concatenate([ua, ub, uc]), (ga.size, gb.size)
+
+
+def test_swiglu_hard_cases_bit_exact(cuda_lib):
+    """Near-midpoint SwiGLU values: every h bit equals the oracle's float64 rounding."""
+    g, u, (na, nb) = _swiglu_hard_pairs()
+    assert na > 2000 and nb > 2000
+    I = 1024
+    rows = (g.size + I - 1) // I
+    pad = rows * I - g.size
+    g = np.concatenate([g, np.ones(pad)])
+    u = np.concatenate([u, np.ones(pad)])
+    d_can = np.concatenate([F.bf16_round(g).reshape(rows, I), F.bf16_round(u).reshape(rows, I)], axis=1)
+    perm = np.arange(rows, dtype=np.int32)
+    h, _, _, _ = cuda_lib.moe_swiglu_quantize(bf16_tensor(d_can[:, interleave_src(I)]), dev(perm), I)
+    got, ref = u16(h), M.swiglu(d_can, I)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, [(float(g.reshape(rows, I)[r, c]), float(u.reshape(rows, I)[r, c]), hex(got[r, c]),
+                            hex(ref[r, c])) for r, c in bad[:8]]
+
+
 def test_swiglu_quantize_pads_k(cuda_lib):
     """I = 128: h is quantised into a 256-wide (zero-padded) row for the down GEMM."""
     rows, I = 130, 128
