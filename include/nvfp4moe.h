@@ -268,9 +268,9 @@ nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int
 /* The expert block forward ("Low-Bit Precision Training Is Ready for Production...",
  * §"What W4A4 GEMM Actually Changes": W4A4 on the expert layers; "The 4-bitter
  * Lesson...", per-token activation scales, fused per-token quantiser):
- *   permute -> per-token NVFP4 of x written to every routed slot (GEMM-tiled) -> gate/up
- *   grouped GEMM with the SwiGLU epilogue (BF16 h) -> per-row NVFP4 of h (GEMM-tiled) ->
- *   down grouped GEMM (BF16 y) -> weighted combine (BF16).  The bits equal those of the
+ *   permute -> per-token NVFP4 of x (token order, GEMM-tiled) gathered into every routed
+ *   slot -> gate/up grouped GEMM with the SwiGLU epilogue (BF16 h) -> per-row NVFP4 of h
+ *   (GEMM-tiled) -> down grouped GEMM (BF16 y) -> weighted combine (BF16).  The bits equal those of the
  *   unfused chain nvfp4_grouped_gemm -> moe_swiglu_quantize -> nvfp4_grouped_gemm ->
  *   moe_combine over the same operands.
  *   x: device BF16 [T, H] and out: device BF16 [T, H], 16-byte aligned;
@@ -289,7 +289,8 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
  * [5] Aq: GEMM-tiled (128-row blocks) codes and scales of the routed rows, K = H,
  * [6] equal to [5] (the scales live inside the tiles), [7] gA float[M_cap],
  * [8] h BF16 [M_cap, I], [9] hq: GEMM-tiled (128-row blocks), K = Ip,
- * [10] equal to [9], [11] gh float[M_cap], [12] y BF16 [M_cap, H],
+ * [10] equal to [9], [11] gh float[M_cap], [12] y BF16 [M_cap, H] (before the down
+ * GEMM this region holds the token-ordered quantised x and its per-token scales),
  * [13] M_cap (a row count, not an offset), [14] total bytes.
  * Only rows below padded_offsets[E] whose perm entry is >= 0 are meaningful. */
 nvfp4_status moe_forward_workspace_layout(int64_t T, int32_t k, int32_t E, int64_t H,

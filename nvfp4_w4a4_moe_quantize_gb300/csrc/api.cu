@@ -487,25 +487,32 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
                                  reinterpret_cast<int32_t*>(base + hist_off), permute_chunks(T * k), status, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
-  // 2. per-token NVFP4 of x, written to every routed slot in the GEMM-tiled layout
+  // 2. per-token NVFP4 of x into a token-ordered GEMM-tiled operand (parked in y's region,
+  //    free until the down GEMM), then gathered into every routed slot with the token's
+  //    global scale
+  uint8_t* xq = static_cast<uint8_t*>(ybuf);
+  float* gx = reinterpret_cast<float*>(xq + align256(tiled_bytes(T, H, 128)));
   QuantArgs a{};
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.rows = T;
   a.cols = H;
   a.ld = H;
   a.mode = kScopeRow;
-  a.g_out = ga;
-  a.codes = aq;
+  a.g_out = gx;
+  a.codes = xq;
   a.sf_words = H / 64;
   a.cols_pad = H;
   a.rows_total = T;
-  a.map = kMapScatter;
-  a.inv = inv;
-  a.k = k;
+  a.map = kMapIdentity;
   a.status = status;
   a.tiled_R = 128;
   a.kblocks = H / 256;
   e = launch_quantize_rows(a, kRoundRNE, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  // per-row max |h|, accumulated by the gate/up epilogue; it lives in y's region after the
+  // token operand (consumed by the gather before the epilogue starts)
+  uint32_t* h_amax = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(gx) + align256(sizeof(float) * T));
+  e = launch_gather_tiled(xq, gx, perm, padded + E, mcap, H, aq, ga, h_amax, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
   // 3. gate/up GEMM with the SwiGLU epilogue: h = BF16(silu(gate) * up)
@@ -520,6 +527,7 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   g1.status = status;
   g1.h = hbuf;
   g1.I = I;
+  g1.h_amax = h_amax;
   CUtensorMap mh, my;
   if (!make_map(&mh, hbuf, mcap, I, I * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2) ||
       !make_map(&my, ybuf, mcap, H, H * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2))
@@ -527,25 +535,9 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   e = launch_grouped_gemm_tiled(aq, wt->w13, mh, g1, mcap / 128, true, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
-  // 4. per-row NVFP4 of h (routed rows only), K zero-padded to Ip, GEMM-tiled
-  QuantArgs r{};
-  r.x = hbuf;
-  r.rows = mcap;
-  r.rows_dev = padded + E;
-  r.row_filter = perm;
-  r.cols = I;
-  r.ld = I;
-  r.mode = kScopeRow;
-  r.g_out = gh;
-  r.codes = hq;
-  r.sf_words = Ip / 64;
-  r.cols_pad = Ip;
-  r.rows_total = mcap;
-  r.map = kMapIdentity;
-  r.status = status;
-  r.tiled_R = 128;
-  r.kblocks = Ip / 256;
-  e = launch_quantize_rows(r, kRoundRNE, s);
+  // 4. per-row NVFP4 of h (routed rows only), K zero-padded to Ip, GEMM-tiled, with the
+  //    row maxima the epilogue gathered
+  e = launch_requant_tiled(hbuf, h_amax, perm, padded + E, mcap, I, Ip, hq, gh, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
   // 5. down GEMM -> y (BF16)

@@ -36,6 +36,7 @@ struct QuantArgs {
   int64_t kblocks;         // tiled: cols_pad / 256
   const int32_t* row_filter;  // nullable: rows with row_filter[row] < 0 are skipped
   const int32_t* rows_dev;    // nullable: device count capping `rows`
+  int q_stages, q_stride;     // streaming path: ring stages per warp, bytes per stage (set by the launcher)
 };
 
 struct GemmArgs {
@@ -53,6 +54,7 @@ struct GemmArgs {
   int* status;
   __nv_bfloat16* h;        // SwiGLU epilogue: h [M, I]
   int64_t I;
+  uint32_t* h_amax;        // SwiGLU epilogue, nullable: per-row max |h| (float bits), atomicMax-combined
 };
 
 int num_sms();
@@ -78,6 +80,20 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, 
 cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
                                       int64_t max_m_tiles, bool swiglu, cudaStream_t s);
 int tiled_max_experts();
+// Slot r (r < min(*n_rows_dev, max_rows), a multiple of 128) of the 128-row-block tiled
+// `dst` gets token perm[r]'s row of the 128-row-block tiled `src` and dst_g[r] = src_g[perm[r]];
+// slots with perm[r] < 0 are not written.  K % 256 == 0.
+// amax_zero (nullable): amax_zero[r] = 0 for every slot r < min(*n_rows_dev, max_rows).
+cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const int32_t* perm, const int32_t* n_rows_dev,
+                                int64_t max_rows, int64_t K, uint8_t* dst, float* dst_g, uint32_t* amax_zero,
+                                cudaStream_t s);
+// Per-row NVFP4 of h [rows, I] (BF16) whose row maxima |h| are already known (amax_bits,
+// float bits): g[r] = amax / 2688, codes and scales into the GEMM-tiled layout with
+// 128-row blocks and K = Ip (columns I .. Ip-1 zero).  Rows r < min(*n_rows_dev, max_rows)
+// with perm[r] >= 0 are encoded; the others are not written.
+cudaError_t launch_requant_tiled(const __nv_bfloat16* h, const uint32_t* amax_bits, const int32_t* perm,
+                                 const int32_t* n_rows_dev, int64_t max_rows, int64_t I, int64_t Ip, uint8_t* out,
+                                 float* g_out, cudaStream_t s);
 cudaError_t launch_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K, int R,
                               uint8_t* out, cudaStream_t s);
 

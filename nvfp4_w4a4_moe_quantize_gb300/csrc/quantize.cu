@@ -248,16 +248,20 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(QuantArgs a) {
   zero_pad_rows(a, warp, nwarp, lane);
 }
 
-// Streaming path (rows up to 2048 columns).  Every warp keeps kQStages rows in flight in
-// a shared-memory ring filled by bulk async copies (cp.async.bulk, completion on an
+// Streaming path (rows up to 2048 columns).  Every warp keeps a.q_stages rows in flight
+// in a shared-memory ring filled by bulk async copies (cp.async.bulk, completion on an
 // mbarrier), so HBM sees several rows per warp while the warp encodes the current one.
+// The ring is sized to the row (stride a.q_stride bytes): short rows get more stages and
+// more warps per SM, so that about 200 KB per SM are in flight whatever the width.
 // Encoding works lane per 16-value block: block b of the row belongs to lane b % 32, so
 // each lane computes its block scale once, stores 8 bytes of codes (a warp stores 256
 // contiguous bytes) and four neighbouring lanes gather one 32-bit scale word.
-constexpr int kQStages = 2;
-constexpr int kQRowBytes = 4096;
 constexpr int kQWarps = 8;
-constexpr size_t kQSmem = kQWarps * kQStages * kQRowBytes + kQWarps * kQStages * sizeof(uint64_t) + 16;
+constexpr int kQMaxStages = 8;
+constexpr size_t kQSmemMax = 200 * 1024;
+__host__ __device__ constexpr size_t stream_smem_bytes(int stages, int stride) {
+  return (size_t)kQWarps * stages * stride + (size_t)kQWarps * stages * sizeof(uint64_t) + 16;
+}
 
 template <int RND>
 __device__ __forceinline__ void encode_block(const QuantArgs& a, int64_t row, int64_t blk, const uint8_t* src,
@@ -304,10 +308,11 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t warp = (int64_t)blockIdx.x * kQWarps + wib;
   const int64_t nwarp = (int64_t)gridDim.x * kQWarps;
-  uint8_t* ring = qsm + (size_t)wib * kQStages * kQRowBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + kQWarps * kQStages * kQRowBytes) + wib * kQStages;
-  volatile int* abort = reinterpret_cast<volatile int*>(qsm + kQWarps * kQStages * kQRowBytes +
-                                                        kQWarps * kQStages * sizeof(uint64_t));
+  const int kQStages = a.q_stages, stride = a.q_stride;
+  uint8_t* ring = qsm + (size_t)wib * kQStages * stride;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + (size_t)kQWarps * kQStages * stride) + wib * kQStages;
+  volatile int* abort = reinterpret_cast<volatile int*>(qsm + (size_t)kQWarps * kQStages * stride +
+                                                        (size_t)kQWarps * kQStages * sizeof(uint64_t));
   if (threadIdx.x == 0) *abort = 0;
   const uint32_t row_bytes = (uint32_t)(a.cols * 2);
   const int64_t nblk = a.cols / 16;
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
       const int64_t r = warp + s * nwarp;
       if (r < nrows) {
         mbar_arrive_expect_tx(&bars[s], row_bytes);
-        bulk_load(ring + s * kQRowBytes, a.x + r * a.ld, row_bytes, &bars[s]);
+        bulk_load(ring + s * stride, a.x + r * a.ld, row_bytes, &bars[s]);
       }
     }
   }
@@ -334,7 +339,7 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
   for (int64_t row = warp; row < nrows; row += nwarp) {
     if (!mbar_wait(&bars[s], (parity >> s) & 1u, a.status, abort)) break;
     parity ^= 1u << s;
-    const uint8_t* buf = ring + s * kQRowBytes;
+    const uint8_t* buf = ring + s * stride;
     if (a.row_filter != nullptr && a.row_filter[row] < 0) {   // a padding slot: nothing to encode
       fence_proxy_async_smem();
       __syncwarp();
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
         const int64_t r2 = row + (int64_t)kQStages * nwarp;
         if (r2 < nrows) {
           mbar_arrive_expect_tx(&bars[s], row_bytes);
-          bulk_load(ring + s * kQRowBytes, a.x + r2 * a.ld, row_bytes, &bars[s]);
+          bulk_load(ring + s * stride, a.x + r2 * a.ld, row_bytes, &bars[s]);
         }
       }
       s = s + 1 == kQStages ? 0 : s + 1;
@@ -392,7 +397,7 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
       const int64_t r2 = row + (int64_t)kQStages * nwarp;
       if (r2 < nrows) {
         mbar_arrive_expect_tx(&bars[s], row_bytes);
-        bulk_load(ring + s * kQRowBytes, a.x + r2 * a.ld, row_bytes, &bars[s]);
+        bulk_load(ring + s * stride, a.x + r2 * a.ld, row_bytes, &bars[s]);
       }
     }
     for (int j = 0; j < nout; ++j) {
@@ -412,6 +417,70 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
   if (a.tiled_R == 0) zero_pad_rows(a, warp, nwarp, lane);
 }
 
+// Per-row NVFP4 of rows whose max |x| is already known (the SwiGLU epilogue folds it
+// into amax_bits while it writes h): no row-wide reduction is left, so every thread
+// encodes one 16-value block on its own -- 32 bytes in, 8 bytes of codes and one scale
+// byte out -- and four neighbouring lanes (blocks 4w .. 4w+3 of a row) gather the
+// 32-bit scale word.  Blocks past I (up to Ip) are written as zeros.
+__global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16* __restrict__ h,
+                                                            const uint32_t* __restrict__ amax_bits,
+                                                            const int32_t* __restrict__ perm,
+                                                            const int32_t* __restrict__ n_rows_dev, int64_t max_rows,
+                                                            int64_t I, int64_t Ip, uint8_t* __restrict__ out,
+                                                            float* __restrict__ g_out) {
+  const int lane = threadIdx.x & 31;
+  int64_t rows = *n_rows_dev;
+  if (rows > max_rows) rows = max_rows;
+  const int64_t nb = Ip / 16, nb_data = I / 16, kblocks = Ip / 256;
+  const int64_t total = rows * nb;   // nb % 4 == 0: lane groups of 4 hold blocks 4w .. 4w+3 of one row
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += stride) {
+    const int64_t i = base + threadIdx.x;
+    const bool in = i < total;
+    const int64_t row = in ? i / nb : 0, blk = in ? i - (i / nb) * nb : 0;
+    const bool live = in && perm[row] >= 0;
+    uint32_t sfb = 0;
+    uint2 cw = make_uint2(0u, 0u);
+    if (live && blk < nb_data) {
+      const float g = __fdiv_rn(__uint_as_float(amax_bits[row]), kGlobalDivisor);
+      const uint4 q0 = ld_nc_v4(h + row * I + blk * 16);
+      const uint4 q1 = ld_nc_v4(h + row * I + blk * 16 + 8);
+      float v0[8], v1[8];
+      bf16x8_to_f32(q0, v0);
+      bf16x8_to_f32(q1, v1);
+      const BlockScale bs = block_scale(fmaxf(absmax8(v0), absmax8(v1)), g, __fmul_rn(6.0f, g));
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v0[e] = __fmul_rn(v0[e], bs.r);
+        v1[e] = __fmul_rn(v1[e], bs.r);
+      }
+      sfb = bs.sf;
+      cw = make_uint2(e2m1x8_rn(v0), e2m1x8_rn(v1));
+      if (blk == 0) g_out[row] = g;
+    }
+    const uint32_t s1 = __shfl_down_sync(kFull, sfb, 1);
+    const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
+    const uint32_t s3 = __shfl_down_sync(kFull, sfb, 3);
+    if (live) {
+      *reinterpret_cast<uint2*>(out + tiled_code_offset(row, blk * 8, kblocks, 128)) = cw;
+      if ((lane & 3) == 0)
+        *reinterpret_cast<uint32_t*>(out + tiled_sf_offset(row, blk, kblocks, 128)) =
+            sfb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
+  }
+}
+
+cudaError_t launch_requant_tiled(const __nv_bfloat16* h, const uint32_t* amax_bits, const int32_t* perm,
+                                 const int32_t* n_rows_dev, int64_t max_rows, int64_t I, int64_t Ip, uint8_t* out,
+                                 float* g_out, cudaStream_t s) {
+  const int64_t total = max_rows * (Ip / 16);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
+  requant_tiled_kernel<<<(int)blocks, 256, 0, s>>>(h, amax_bits, perm, n_rows_dev, max_rows, I, Ip, out, g_out);
+  return cudaGetLastError();
+}
+
 template <int RND>
 static cudaError_t launch_quant_rnd(const QuantArgs& a, int maxc, int grid, cudaStream_t s) {
   switch (maxc) {
@@ -426,17 +495,17 @@ static cudaError_t launch_quant_rnd(const QuantArgs& a, int maxc, int grid, cuda
 }
 
 template <int RND>
-static cudaError_t launch_stream(const QuantArgs& a, int grid, cudaStream_t s) {
+static cudaError_t launch_stream(const QuantArgs& a, int grid, size_t smem, cudaStream_t s) {
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr[dev]) {
     cudaError_t e = cudaFuncSetAttribute(quantize_rows_stream_kernel<RND>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmemMax + 4096);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr[dev] = true;
   }
-  quantize_rows_stream_kernel<RND><<<grid, kQWarps * 32, kQSmem, s>>>(a);
+  quantize_rows_stream_kernel<RND><<<grid, kQWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -471,14 +540,30 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
   const bool stream_ok = maxc <= 8 && (a.ld * 2) % 16 == 0;
   if (!stream_ok && (a.tiled_R != 0 || a.row_filter != nullptr || a.rows_dev != nullptr)) return cudaErrorInvalidValue;
   if (stream_ok) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_rows_stream_kernel<kRoundRNE>,
-                                                      kQWarps * 32, kQSmem) != cudaSuccess || per_sm < 1)
-      per_sm = 1;
-    const int64_t cap_s = (int64_t)per_sm * sms;
-    int64_t b = (a.rows_total + kQWarps - 1) / kQWarps;
-    if (b > cap_s) b = cap_s;
-    return rounding == kRoundSR ? launch_stream<kRoundSR>(a, (int)b, s) : launch_stream<kRoundRNE>(a, (int)b, s);
+    // ring sizing: stride = the row rounded up to 128 bytes; up to 4 blocks (32 warps) per
+    // SM (the register file's limit at 64 registers), at least 2 stages per warp, and as
+    // many stages as keep the SM's ring near kQSmemMax
+    QuantArgs b = a;
+    b.q_stride = (int)((a.cols * 2 + 127) / 128 * 128);
+    int blocks_per_sm = (int)(kQSmemMax / stream_smem_bytes(2, b.q_stride));
+    if (blocks_per_sm > 4) blocks_per_sm = 4;
+    if (blocks_per_sm < 1) blocks_per_sm = 1;
+    int stages = (int)((kQSmemMax / blocks_per_sm - 16) / ((size_t)kQWarps * (b.q_stride + sizeof(uint64_t))));
+    if (stages > kQMaxStages) stages = kQMaxStages;
+    if (stages < 2) stages = 2;
+    b.q_stages = stages;
+    const size_t smem = stream_smem_bytes(stages, b.q_stride);
+    int resident = 0;   // the registers of the rounding variant may allow fewer blocks
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident,
+                                                      rounding == kRoundSR ? quantize_rows_stream_kernel<kRoundSR>
+                                                                           : quantize_rows_stream_kernel<kRoundRNE>,
+                                                      kQWarps * 32, smem) == cudaSuccess &&
+        resident >= 1 && resident < blocks_per_sm)
+      blocks_per_sm = resident;
+    int64_t nb = (a.rows_total + kQWarps - 1) / kQWarps;
+    if (nb > (int64_t)blocks_per_sm * sms) nb = (int64_t)blocks_per_sm * sms;
+    return rounding == kRoundSR ? launch_stream<kRoundSR>(b, (int)nb, smem, s)
+                                : launch_stream<kRoundRNE>(b, (int)nb, smem, s);
   }
   const int64_t cap = (int64_t)(maxc <= 8 ? 8 : 4) * sms;
   if (blocks > cap) blocks = cap;
