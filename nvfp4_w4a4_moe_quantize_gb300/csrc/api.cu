@@ -53,17 +53,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 // 2-D map over a [rows, cols] matrix of `elt`-byte elements with row pitch `pitch_bytes`;
 // box = 128 bytes x box_rows, 128-byte swizzle.
+// 2-D tensor map with boxes of box_rows rows x box_bytes bytes (128: 128-byte swizzle,
+// 64: 64-byte swizzle).
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t pitch_bytes, uint32_t box_rows,
-              CUtensorMapDataType dt, int elt) {
+              CUtensorMapDataType dt, int elt, int box_bytes = 128) {
   auto enc = encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)pitch_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)(box_bytes / elt), box_rows};
   cuuint32_t es[2] = {1u, 1u};
   return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct ForwardLayout {
@@ -334,7 +336,7 @@ nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A, const float* gA, const u
   g.I = N / 2;
   const bool swiglu = epilogue == NVFP4_EPILOGUE_SWIGLU;
   CUtensorMap md;
-  const bool ok = swiglu ? make_map(&md, D, M_total, N / 2, N, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2)
+  const bool ok = swiglu ? make_map(&md, D, M_total, N / 2, N, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64)
                          : make_map(&md, D, M_total, N, ldd * (g.out_f32 ? 4 : 2), 32,
                                     g.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                     g.out_f32 ? 4 : 2);
@@ -529,7 +531,7 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   g1.I = I;
   g1.h_amax = h_amax;
   CUtensorMap mh, my;
-  if (!make_map(&mh, hbuf, mcap, I, I * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2) ||
+  if (!make_map(&mh, hbuf, mcap, I, I * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64) ||
       !make_map(&my, ybuf, mcap, H, H * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2))
     return NVFP4_ERR_CUDA;
   e = launch_grouped_gemm_tiled(aq, wt->w13, mh, g1, mcap / 128, true, s);

@@ -43,7 +43,7 @@ namespace gt {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kStages = 3;
-constexpr int kOutBox = 32 * 128;           // one epilogue warp's staged output box
+constexpr int kOutBytes = 32 * 1024;        // staged output boxes of all epilogue warps
 constexpr int kABlock = 128 * 144;          // 16 KB codes + 2 KB scales
 constexpr int kBBlock = 256 * 144;          // 32 KB codes + 4 KB scales
 constexpr int kACodes = 128 * 128;
@@ -52,15 +52,18 @@ constexpr int kTmemCols = 512;
 constexpr int kAccCols = kBN;
 constexpr int kSFCol0 = kAccCols;
 constexpr int kSFStageCols = 16 + 32;       // A: 4 x 4 columns, B: 4 x 8 columns
-constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 3;
-constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+// Epilogue warps: 8 for the plain store (two per TMEM lane quadrant, 128 columns each);
+// 16 for the SwiGLU epilogue, whose per-value arithmetic needs the latency hiding of four
+// warps per quadrant (each one 32-column gate slice and its up slice).
+__host__ __device__ constexpr int epi_warps(bool swiglu) { return swiglu ? 16 : 8; }
+__host__ __device__ constexpr int threads(bool swiglu) { return 32 * (kFirstEpiWarp + epi_warps(swiglu)); }
 constexpr int kMaxE = 512;
 
 struct Smem {
   uint8_t a[kStages][kABlock];
   uint8_t b[kStages][kBBlock];
-  uint8_t out[kEpiWarps][kOutBox];
+  uint8_t out[kOutBytes];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t accf;
@@ -97,10 +100,11 @@ __device__ __forceinline__ void store_box(uint8_t* buf, const uint32_t (&w)[32],
 }
 
 template <bool kSwiGLU>
-__global__ void __launch_bounds__(gt::kThreads, 1)
+__global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
     grouped_gemm_tiled_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B,
                               const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
   using namespace gt;
+  constexpr int kEpiWarps = epi_warps(kSwiGLU);
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,8 +207,10 @@ __global__ void __launch_bounds__(gt::kThreads, 1)
     // epilogue: TMEM lane quadrant q = warp % 4 (the lanes this warp may read), column
     // half of the tile = (warp - 3) / 4
     const int q = warp & 3;
-    const int half = (warp - kFirstEpiWarp) >> 2;
-    uint8_t* buf = sm.out[warp - kFirstEpiWarp];
+    const int ew = warp - kFirstEpiWarp;
+    const int half = kSwiGLU ? ew >> 3 : ew >> 2;        // 128-column half of the tile
+    const int sub = kSwiGLU ? (ew >> 2) & 1 : 0;         // SwiGLU: 32-column slice of the half
+    uint8_t* buf = sm.out + ew * (kOutBytes / kEpiWarps);
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
@@ -228,98 +234,89 @@ __global__ void __launch_bounds__(gt::kThreads, 1)
       const bool skip = q * 32 >= in_group;
       const int32_t y = row0 + q * 32;
       if (kSwiGLU) {
-        // columns [0, 64) of this half are gate, [64, 128) up, for h columns
-        // n_tile*128 + half*64 + [0, 64) (64-row gate/up interleave of W13).  Two rounds
-        // of 32 gate + 32 up columns keep the live registers low; the accumulator is
-        // released after the second drain (the load stages cover that wait).  In each
-        // round all 32 values take the branch-free float32 path first (independent
-        // chains the compiler can interleave) and the rare values it cannot settle are
-        // redone after, warp-uniformly; the round's 64 bytes of h go straight to the
-        // staging box (full slabs) or to global memory (a group's partial slab).
+        // Columns [0, 64) of this half are gate, [64, 128) up (64-row gate/up interleave
+        // of W13); this warp takes gate columns sub*32 + [0, 32) and the matching up
+        // columns, i.e. h columns n_tile*128 + half*64 + sub*32 + [0, 32).  All 32 values
+        // take the branch-free float32 path first (independent chains the compiler can
+        // interleave); the rare values it cannot settle are redone after, warp-uniformly.
+        uint32_t vg[32], vu[32];
+        NVFP4_TMEM_LD_X32(taddr + 32 * sub, vg);
+        NVFP4_TMEM_LD_X32(taddr + 64 + 32 * sub, vu);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.acce);
+        if (skip) continue;
+        // gu: BF16 gate | BF16 up << 16, one rounding instruction per pair
+        uint32_t gu[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const __nv_bfloat162 pr = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(vg[i]), scale),
+                                                          __fmul_rn(__uint_as_float(vu[i]), scale));
+          gu[i] = *reinterpret_cast<const uint32_t*>(&pr);
+        }
+        uint32_t w[16];
+        uint32_t redo = 0;
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {
+          uint32_t hb[2];
+#pragma unroll
+          for (int s2 = 0; s2 < 2; ++s2) {
+            const uint32_t x2 = gu[2 * p + s2];
+            if (!swiglu_fast(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u), hb[s2]))
+              redo |= 1u << (2 * p + s2);
+          }
+          w[p] = hb[0] | (hb[1] << 16);
+        }
+        // each round of the redo: every lane with a pending value selects its lowest one
+        // (unrolled selects, no indexed registers), one inlined exact evaluation serves
+        // the warp, the result is patched into w
+        while (__any_sync(0xFFFFFFFFu, redo != 0)) {
+          const int idx = redo != 0 ? __ffs((int)redo) - 1 : -1;
+          uint32_t x2 = 0x3F803F80u;   // lanes with nothing pending evaluate gate = up = 1
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x2 = idx == j ? gu[j] : x2;
+          const uint32_t hb = swiglu_exact(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u));
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            uint32_t& word = w[j >> 1];
+            const uint32_t patched = (j & 1) ? (word & 0xFFFFu) | (hb << 16) : (word & 0xFFFF0000u) | hb;
+            word = idx == j ? patched : word;
+          }
+          redo &= redo - 1;
+        }
+        const int32_t x = n_tile * 128 + half * 64 + sub * 32;
         if (full_warp) {
+          // 32 rows x 64 bytes, 64-byte swizzled (16-byte chunk j of row r at
+          // (j ^ ((r >> 1) & 3)) * 16, the TMA SWIZZLE_64B image), one TMA store
           if (lane == 0) bulk_wait_read<0>();   // the previous box has been read
           __syncwarp();
-        }
-        uint32_t hmax = 0;
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t vg[32], vu[32];
-          NVFP4_TMEM_LD_X32(taddr + 32 * c, vg);
-          NVFP4_TMEM_LD_X32(taddr + 64 + 32 * c, vu);
-          tmem_ld_wait();
-          if (c == 1) {
-            tc_fence_before();
-            mbar_arrive(&sm.acce);
-          }
-          if (skip) continue;
-          // gu: BF16 gate | BF16 up << 16, one rounding instruction per pair
-          uint32_t gu[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const __nv_bfloat162 pr = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(vg[i]), scale),
-                                                            __fmul_rn(__uint_as_float(vu[i]), scale));
-            gu[i] = *reinterpret_cast<const uint32_t*>(&pr);
-          }
-          uint32_t w[16];
-          uint32_t redo = 0;
-#pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            uint32_t hb[2];
-#pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-              const uint32_t x2 = gu[2 * p + s2];
-              if (!swiglu_fast(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u), hb[s2]))
-                redo |= 1u << (2 * p + s2);
-            }
-            w[p] = hb[0] | (hb[1] << 16);
-          }
-          // each round of the redo: every lane with a pending value selects its lowest
-          // one (unrolled selects, no indexed registers), one inlined exact evaluation
-          // serves the warp, the result is patched into w
-          while (__any_sync(0xFFFFFFFFu, redo != 0)) {
-            const int idx = redo != 0 ? __ffs((int)redo) - 1 : -1;
-            uint32_t x2 = 0x3F803F80u;   // lanes with nothing pending evaluate gate = up = 1
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x2 = idx == j ? gu[j] : x2;
-            const uint32_t hb = swiglu_exact(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u));
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              uint32_t& word = w[j >> 1];
-              const uint32_t patched = (j & 1) ? (word & 0xFFFFu) | (hb << 16) : (word & 0xFFFF0000u) | hb;
-              word = idx == j ? patched : word;
-            }
-            redo &= redo - 1;
-          }
-          if (g.h_amax != nullptr) {
-            // max |h| of the row's 32 values as BF16 magnitude bits (integers order like
-            // the magnitudes; NaN patterns are ignored, as a float max would)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
-              hmax = max(hmax, max(lo <= 0x7F80u ? lo : 0u, hi <= 0x7F80u ? hi : 0u));
-            }
-          }
-          if (full_warp) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(buf + lane * 128 + (((4 * c + j) ^ (lane & 7)) << 4)) =
-                  make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          } else if (valid) {
-            __nv_bfloat16* hp = g.h + row * g.I + n_tile * 128 + half * 64 + 32 * c;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(hp + 8 * j) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          }
-        }
-        if (full_warp) {
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmd, buf, n_tile * 128 + half * 64, y);
+            tma_store_2d(&tmd, buf, x, y);
             bulk_commit();
           }
+        } else if (valid) {
+          __nv_bfloat16* hp = g.h + row * g.I + x;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(hp + 8 * j) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
-        if (g.h_amax != nullptr && valid && hmax != 0u) atomicMax(g.h_amax + row, hmax << 16);
+        if (g.h_amax != nullptr && valid) {
+          // max |h| of the row's 32 values as BF16 magnitude bits (integers order like
+          // the magnitudes; NaN patterns are ignored, as a float max would)
+          uint32_t hmax = 0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+            hmax = max(hmax, max(lo <= 0x7F80u ? lo : 0u, hi <= 0x7F80u ? hi : 0u));
+          }
+          if (hmax != 0u) atomicMax(g.h_amax + row, hmax << 16);
+        }
       } else {
         uint32_t v[4][32];
 #pragma unroll
@@ -399,7 +396,7 @@ static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtens
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
-  grouped_gemm_tiled_kernel<kSwiGLU><<<grid, gt::kThreads, gt::kSmemBytes, s>>>(A, B, tmd, g);
+  grouped_gemm_tiled_kernel<kSwiGLU><<<grid, gt::threads(kSwiGLU), gt::kSmemBytes, s>>>(A, B, tmd, g);
   return cudaGetLastError();
 }
 

@@ -75,8 +75,8 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, 
 
 // GEMM over GEMM-tiled operands (tiled.cuh): N % 256 == 0, K % 256 == 0, E <= 512.
 // swiglu: the gate/up epilogue writes h = BF16(silu(gate) * up) to g.h instead of D.
-// tmd: tensor map of the output (D, or h [M_total, N/2] BF16), 32-row boxes of 128 bytes,
-// 128-byte swizzle.
+// tmd: tensor map of the output, 32-row boxes: D with 128-byte boxes (128-byte swizzle),
+// or h [M_total, N/2] BF16 with 64-byte boxes (64-byte swizzle).
 cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
                                       int64_t max_m_tiles, bool swiglu, cudaStream_t s);
 int tiled_max_experts();
