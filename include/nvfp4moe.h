@@ -200,7 +200,10 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const floa
  *   epilogue NVFP4_EPILOGUE_SWIGLU: B holds gate/up rows interleaved in 64-row chunks
  *     (as nvfp4_moe_weights.w13); D receives BF16 h [M_total, N/2] (row pitch N/2,
  *     ldd and out_dtype ignored) with h = BF16(silu(gate) * up) from the BF16-rounded gate
- *     and up outputs: silu(gate) * up evaluated in float64 and rounded once to BF16. */
+ *     and up outputs: silu(gate) * up evaluated in float64 and rounded once to BF16.
+ *     The first SwiGLU call on a device (this one, moe_swiglu_quantize or
+ *     moe_expert_forward) builds a 512 KB table of silu over the BF16 values with one
+ *     kernel on `stream` and waits for it; make that first call outside stream capture. */
 enum { NVFP4_EPILOGUE_STORE = 0, NVFP4_EPILOGUE_SWIGLU = 1 };
 nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A_tiled, const float* gA, const uint8_t* B_tiled,
                                       const float* gB, const int32_t* group_offsets,

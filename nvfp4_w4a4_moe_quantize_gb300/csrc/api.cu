@@ -335,6 +335,7 @@ nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A, const float* gA, const u
   g.h = static_cast<__nv_bfloat16*>(D);
   g.I = N / 2;
   const bool swiglu = epilogue == NVFP4_EPILOGUE_SWIGLU;
+  if (swiglu && (g.silu_tab = silu_table(static_cast<cudaStream_t>(stream))) == nullptr) return NVFP4_ERR_CUDA;
   CUtensorMap md;
   const bool ok = swiglu ? make_map(&md, D, M_total, N / 2, N, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64)
                          : make_map(&md, D, M_total, N, ldd * (g.out_f32 ? 4 : 2), 32,
@@ -530,6 +531,8 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   g1.h = hbuf;
   g1.I = I;
   g1.h_amax = h_amax;
+  g1.silu_tab = silu_table(s);
+  if (g1.silu_tab == nullptr) return NVFP4_ERR_CUDA;
   CUtensorMap mh, my;
   if (!make_map(&mh, hbuf, mcap, I, I * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64) ||
       !make_map(&my, ybuf, mcap, H, H * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2))

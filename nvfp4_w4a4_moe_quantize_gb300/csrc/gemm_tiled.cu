@@ -211,6 +211,40 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
     const int half = kSwiGLU ? ew >> 3 : ew >> 2;        // 128-column half of the tile
     const int sub = kSwiGLU ? (ew >> 2) & 1 : 0;         // SwiGLU: 32-column slice of the half
     uint8_t* buf = sm.out + ew * (kOutBytes / kEpiWarps);
+    const ff* silu_tab = static_cast<const ff*>(g.silu_tab);
+    // SwiGLU: the values of a tile that the float32 path could not settle (one in about
+    // 2000) are recorded during that pass -- the first two per lane in registers, any
+    // further ones in a small per-lane array -- and evaluated exactly after the next tile's
+    // accumulator has been drained and released, off the path accumulator -> drain ->
+    // next MMA.  The fix-up is stored once the box holding the value has been written,
+    // and joins the row max.
+    uint32_t d_x2a = 0, d_x2b = 0, d_mask = 0;   // d_mask: columns (bits) still to settle
+    int d_n = 0;
+    uint32_t d_ovf[30];
+    __nv_bfloat16* d_hp = nullptr;
+    int64_t d_row = 0;
+    auto flush_deferred = [&]() {
+      if (!__any_sync(0xFFFFFFFFu, d_n != 0)) return;
+      if (lane == 0) bulk_wait_all<0>();   // this warp's boxes have reached global memory
+      fence_proxy_async_global();
+      __syncwarp();
+      for (int k = 0; __any_sync(0xFFFFFFFFu, d_n > k); ++k) {
+        const bool has = d_n > k;
+        uint32_t x2 = 0x3F803F80u;         // lanes with nothing left evaluate gate = up = 1
+        if (has) x2 = k == 0 ? d_x2a : (k == 1 ? d_x2b : d_ovf[k - 2]);
+        const uint32_t hb = swiglu_exact(silu_tab, __uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u));
+        if (has) {
+          const int j = __ffs((int)d_mask) - 1;   // recorded in increasing column order
+          d_mask &= d_mask - 1;
+          *reinterpret_cast<uint16_t*>(d_hp + j) = (uint16_t)hb;
+          const uint32_t mag = hb & 0x7FFFu;
+          if (g.h_amax != nullptr && mag != 0u && mag <= 0x7F80u) atomicMax(g.h_amax + d_row, mag << 16);
+        }
+      }
+      d_n = 0;
+      d_mask = 0;
+    };
+    bool aborted = false;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
@@ -223,7 +257,10 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
       const float ga = valid ? g.ga[row] : 0.0f;
       // every lane waits (bounded), then the warp leaves together if any lane gave up
       const bool acc_ready = mbar_wait(&sm.accf, it & 1, g.status, abort);
-      if (!__all_sync(0xFFFFFFFFu, acc_ready)) break;
+      if (!__all_sync(0xFFFFFFFFu, acc_ready)) {
+        aborted = true;
+        break;
+      }
       tc_fence_after();
       const float scale = __fmul_rn(ga, sm.gb[e]);
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + half * 128;
@@ -238,13 +275,14 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
         // of W13); this warp takes gate columns sub*32 + [0, 32) and the matching up
         // columns, i.e. h columns n_tile*128 + half*64 + sub*32 + [0, 32).  All 32 values
         // take the branch-free float32 path first (independent chains the compiler can
-        // interleave); the rare values it cannot settle are redone after, warp-uniformly.
+        // interleave); the rare values it cannot settle are recorded for the next tile.
         uint32_t vg[32], vu[32];
         NVFP4_TMEM_LD_X32(taddr + 32 * sub, vg);
         NVFP4_TMEM_LD_X32(taddr + 64 + 32 * sub, vu);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&sm.acce);
+        flush_deferred();   // the previous tile's leftovers (its box is written by now)
         if (skip) continue;
         // gu: BF16 gate | BF16 up << 16, one rounding instruction per pair
         uint32_t gu[32];
@@ -254,37 +292,26 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
                                                           __fmul_rn(__uint_as_float(vu[i]), scale));
           gu[i] = *reinterpret_cast<const uint32_t*>(&pr);
         }
+        const int32_t x = n_tile * 128 + half * 64 + sub * 32;
+        d_hp = g.h + row * g.I + x;
+        d_row = row;
         uint32_t w[16];
-        uint32_t redo = 0;
 #pragma unroll
         for (int p = 0; p < 16; ++p) {
           uint32_t hb[2];
 #pragma unroll
           for (int s2 = 0; s2 < 2; ++s2) {
             const uint32_t x2 = gu[2 * p + s2];
-            if (!swiglu_fast(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u), hb[s2]))
-              redo |= 1u << (2 * p + s2);
+            if (!swiglu_fast(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u), hb[s2]) && valid) {
+              if (d_n == 0) d_x2a = x2;
+              else if (d_n == 1) d_x2b = x2;
+              else d_ovf[d_n - 2] = x2;
+              ++d_n;
+              d_mask |= 1u << (2 * p + s2);
+            }
           }
           w[p] = hb[0] | (hb[1] << 16);
         }
-        // each round of the redo: every lane with a pending value selects its lowest one
-        // (unrolled selects, no indexed registers), one inlined exact evaluation serves
-        // the warp, the result is patched into w
-        while (__any_sync(0xFFFFFFFFu, redo != 0)) {
-          const int idx = redo != 0 ? __ffs((int)redo) - 1 : -1;
-          uint32_t x2 = 0x3F803F80u;   // lanes with nothing pending evaluate gate = up = 1
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x2 = idx == j ? gu[j] : x2;
-          const uint32_t hb = swiglu_exact(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u));
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            uint32_t& word = w[j >> 1];
-            const uint32_t patched = (j & 1) ? (word & 0xFFFFu) | (hb << 16) : (word & 0xFFFF0000u) | hb;
-            word = idx == j ? patched : word;
-          }
-          redo &= redo - 1;
-        }
-        const int32_t x = n_tile * 128 + half * 64 + sub * 32;
         if (full_warp) {
           // 32 rows x 64 bytes, 64-byte swizzled (16-byte chunk j of row r at
           // (j ^ ((r >> 1) & 3)) * 16, the TMA SWIZZLE_64B image), one TMA store
@@ -309,10 +336,12 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
         if (g.h_amax != nullptr && valid) {
           // max |h| of the row's 32 values as BF16 magnitude bits (integers order like
           // the magnitudes; NaN patterns are ignored, as a float max would)
+          // (deferred values join the max when they are settled)
           uint32_t hmax = 0;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+            const uint32_t lo = (d_mask >> (2 * j)) & 1u ? 0u : w[j] & 0x7FFFu;
+            const uint32_t hi = (d_mask >> (2 * j + 1)) & 1u ? 0u : (w[j] >> 16) & 0x7FFFu;
             hmax = max(hmax, max(lo <= 0x7F80u ? lo : 0u, hi <= 0x7F80u ? hi : 0u));
           }
           if (hmax != 0u) atomicMax(g.h_amax + row, hmax << 16);
@@ -370,6 +399,7 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
         }
       }
     }
+    if (kSwiGLU && !aborted) flush_deferred();
     if (lane == 0) bulk_wait_all<0>();   // the last boxes are read before the CTA exits
     __syncwarp();
   }
@@ -383,6 +413,7 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
 template <bool kSwiGLU>
 static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
                                 int64_t max_m_tiles, cudaStream_t s) {
+  if (kSwiGLU && g.silu_tab == nullptr) return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

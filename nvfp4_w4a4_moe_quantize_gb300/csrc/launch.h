@@ -55,7 +55,12 @@ struct GemmArgs {
   __nv_bfloat16* h;        // SwiGLU epilogue: h [M, I]
   int64_t I;
   uint32_t* h_amax;        // SwiGLU epilogue, nullable: per-row max |h| (float bits), atomicMax-combined
+  const void* silu_tab;    // SwiGLU epilogue: silu_table()
 };
+
+// Device address of the per-device silu table of the SwiGLU exact path (built by one
+// kernel on stream s, waited for, on the first call per device); nullptr on failure.
+const void* silu_table(cudaStream_t s);
 
 int num_sms();
 int* device_status_ptr();

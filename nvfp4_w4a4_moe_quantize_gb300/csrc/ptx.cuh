@@ -152,6 +152,11 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Order global-memory accesses of the async proxy (completed TMA stores) and of the
+// generic proxy of this thread.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ------------------------------------------------------------------ tcgen05
 

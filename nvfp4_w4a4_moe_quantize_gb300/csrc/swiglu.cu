@@ -5,7 +5,7 @@
 // Balancing Stability and Performance in NVFP4 RL", §"Why is the NVFP4 pretraining
 // recipe not sufficient for RL?": per-token activation scales).
 //
-// h = BF16(silu(gate) * up) is correctly rounded (see swiglu.cuh).
+// h = BF16(silu(gate) * up) rounded as the float64 reference does (see swiglu.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -17,6 +17,30 @@ namespace nvfp4 {
 
 constexpr unsigned kAll = 0xFFFFFFFFu;
 
+// silu of every BF16 bit pattern as a float-float (swiglu.cuh), built on first use per
+// device; every call shares it read-only.
+static __device__ __align__(256) ff g_silu_tab[kSiluTableSize];
+
+__global__ void __launch_bounds__(256) silu_table_kernel(ff* __restrict__ tab) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < kSiluTableSize) tab[i] = silu_ff(__uint_as_float((uint32_t)i << 16));
+}
+
+const void* silu_table(cudaStream_t s) {
+  static const void* ptr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_silu_tab) != cudaSuccess) return nullptr;
+    silu_table_kernel<<<kSiluTableSize / 256, 256, 0, s>>>(static_cast<ff*>(p));
+    // wait once, so that calls on other streams never read a table still being built
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return nullptr;
+    ptr[dev] = p;
+  }
+  return ptr[dev];
+}
+
 // One warp per routed row.  Lane l owns h columns 8l + 256i; gate of h column c sits at
 // D column (c/64)*128 + c%64 and up at the same plus 64 (64-row interleave of W13).
 template <int MAXC>
@@ -26,7 +50,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(const __nv_bfloat16* 
                                                            int64_t Ip,
                                                            __nv_bfloat16* __restrict__ h_out,
                                                            uint8_t* __restrict__ hq, uint8_t* __restrict__ hsf,
-                                                           float* __restrict__ gh) {
+                                                           float* __restrict__ gh, const ff* __restrict__ tab) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t nwarp = (int64_t)gridDim.x * 8;
@@ -53,7 +77,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(const __nv_bfloat16* 
         uint32_t hb[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          hb[e] = swiglu_bf16(gf[e], uf[e]);
+          hb[e] = swiglu_bf16(tab, gf[e], uf[e]);
           cm = fmaxf(cm, fabsf(__uint_as_float(hb[e] << 16)));
         }
         hv[i] = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
@@ -101,17 +125,19 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(const __nv_bfloat16* 
 cudaError_t launch_swiglu_quant(const void* d, const int32_t* perm, int64_t rows, const int32_t* nrows_dev,
                                 int64_t I, int64_t Ip, void* h_out, uint8_t* hq, uint8_t* hsf, float* gh,
                                 cudaStream_t s) {
+  const ff* tab = static_cast<const ff*>(silu_table(s));
+  if (tab == nullptr) return cudaErrorUnknown;
   if (rows == 0) return cudaSuccess;
   int64_t blocks = (rows + 7) / 8;
   if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
   const auto* dp = static_cast<const __nv_bfloat16*>(d);
   auto* hp = static_cast<__nv_bfloat16*>(h_out);
-  if (I <= 256) swiglu_quant_kernel<1><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
-  else if (I <= 512) swiglu_quant_kernel<2><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
-  else if (I <= 768) swiglu_quant_kernel<3><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
-  else if (I <= 1024) swiglu_quant_kernel<4><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
-  else if (I <= 2048) swiglu_quant_kernel<8><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
-  else swiglu_quant_kernel<16><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh);
+  if (I <= 256) swiglu_quant_kernel<1><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh, tab);
+  else if (I <= 512) swiglu_quant_kernel<2><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh, tab);
+  else if (I <= 768) swiglu_quant_kernel<3><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh, tab);
+  else if (I <= 1024) swiglu_quant_kernel<4><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh, tab);
+  else if (I <= 2048) swiglu_quant_kernel<8><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh, tab);
+  else swiglu_quant_kernel<16><<<(int)blocks, 256, 0, s>>>(dp, perm, rows, nrows_dev, I, Ip, hp, hq, hsf, gh, tab);
   return cudaGetLastError();
 }
 

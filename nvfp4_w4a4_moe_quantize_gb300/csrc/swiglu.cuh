@@ -22,7 +22,9 @@
 // 1 + e to 1 when e <= 2^-53 (gate > 36.74) and then ties to even; for larger e it lands
 // strictly below the midpoint.  The float-float path reproduces both cases by dropping e
 // at the same threshold.  Inputs out of the float-float range (|gate| > 80, or |h| outside
-// [2^-100, 2^100], where BF16 subnormals need care) take a float64 path.
+// [2^-100, 2^100], where BF16 subnormals need care) take a float64 path.  The gate is a
+// BF16 value, so silu(gate) as a float-float comes from a 65536-entry table built once per
+// device with this arithmetic; the exact path is then one load and a float-float product.
 #pragma once
 #include <cstdint>
 
@@ -108,9 +110,10 @@ __device__ __forceinline__ ff ff_exp(float t) {
 
 constexpr uint32_t kSwigluNeedF64 = 0xFFFFFFFFu;
 
-// The float-float evaluation; kSwigluNeedF64 when the inputs are out of its range.
-__device__ __forceinline__ uint32_t swiglu_ff(float g, float u) {
-  if (!(fabsf(g) <= 80.0f)) return kSwigluNeedF64;
+// silu(g) = g / (1 + exp(-g)) as a float-float, |g| <= 80; a NaN hi part otherwise (the
+// float64 path takes those).
+__device__ __forceinline__ ff silu_ff(float g) {
+  if (!(fabsf(g) <= 80.0f)) return {__int_as_float(0x7FC00000), 0.0f};
   const ff e = ff_exp(-g);
   ff d = {1.0f, 0.0f};                       // float64 rounds 1 + e to 1 for e <= 2^-53
   if (e.hi > 0x1p-53f) {
@@ -122,7 +125,13 @@ __device__ __forceinline__ uint32_t swiglu_ff(float g, float u) {
   const ff pq = ff_two_prod(q1, d.hi);
   float rem = __fsub_rn(__fsub_rn(g, pq.hi), pq.lo);
   rem = __fsub_rn(rem, __fmul_rn(q1, d.lo));
-  const ff s = ff_fast_two_sum(q1, __fdiv_rn(rem, d.hi));
+  return ff_fast_two_sum(q1, __fdiv_rn(rem, d.hi));
+}
+
+// BF16 rounding of s * u from the float-float s = silu(g); kSwigluNeedF64 when s is
+// marked out of range or |s * u| is outside [2^-100, 2^100].
+__device__ __forceinline__ uint32_t swiglu_finish(ff s, float u) {
+  if (s.hi != s.hi) return kSwigluNeedF64;
   ff x = ff_two_prod(s.hi, u);
   x = ff_fast_two_sum(x.hi, __fadd_rn(x.lo, __fmul_rn(s.lo, u)));
   const float ax = fabsf(x.hi);
@@ -132,6 +141,11 @@ __device__ __forceinline__ uint32_t swiglu_ff(float g, float u) {
   // x.hi is a BF16 rounding midpoint: the sign of x.lo relative to x.hi decides
   return ((x.lo > 0.0f) == (x.hi > 0.0f)) ? (b >> 16) + 1u : (b >> 16);
 }
+
+// Gate values are BF16, so silu(g) takes 65536 values: the exact path reads its
+// float-float silu from a table built once per device by silu_table_kernel (same
+// arithmetic as silu_ff, entry i for the BF16 bit pattern i).
+constexpr int kSiluTableSize = 65536;
 
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
@@ -154,16 +168,18 @@ __device__ __forceinline__ bool swiglu_fast(float g, float u, uint32_t& out) {
 
 // The exact path for the values the fast path hands over, inlined at one warp-uniform
 // site by its callers (a rarely taken call inside an unrolled epilogue loop cost far more
-// than the work it did).
-__device__ __forceinline__ uint32_t swiglu_exact(float g, float u) {
-  const uint32_t r = swiglu_ff(g, u);
+// than the work it did).  g must be a BF16 value; tab is the silu table.
+__device__ __forceinline__ uint32_t swiglu_exact(const ff* __restrict__ tab, float g, float u) {
+  const uint32_t r = swiglu_finish(tab[__float_as_uint(g) >> 16], u);
   return r != kSwigluNeedF64 ? r : swiglu_f64(g, u);
 }
-static __device__ __noinline__ uint32_t swiglu_slow(float g, float u) { return swiglu_exact(g, u); }
+static __device__ __noinline__ uint32_t swiglu_slow(const ff* __restrict__ tab, float g, float u) {
+  return swiglu_exact(tab, g, u);
+}
 
-__device__ __forceinline__ uint32_t swiglu_bf16(float g, float u) {
+__device__ __forceinline__ uint32_t swiglu_bf16(const ff* __restrict__ tab, float g, float u) {
   uint32_t b;
-  return swiglu_fast(g, u, b) ? b : swiglu_slow(g, u);
+  return swiglu_fast(g, u, b) ? b : swiglu_slow(tab, g, u);
 }
 
 }  // namespace nvfp4

@@ -219,6 +219,13 @@ def test_tiled_swiglu_epilogue_equals_standalone_swiglu(cuda_lib):
     a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=91))
     w_bits = S.bf16_bits(S.randn_bf16((E, 2 * I, K), 0.05, seed=92))
     ops = _operands_from_oracle(a_bits, counts, w_bits)
+    # rows whose global scale is blown up or shrunk: gate values below -80 and products
+    # outside [2^-100, 2^100] leave the float32 path for many values of one row, so the
+    # epilogue's deferred exact path runs with more than two values per row and tile,
+    # in full 32-row slabs and in the partial slab of the last group
+    ops["a_g"][0:64] *= 3000.0
+    ops["a_g"][64:96] *= 1e-30
+    ops["a_g"][256 + 40:256 + 77] *= 3000.0
     h_fused = u16(_run_tiled(cuda_lib, ops, 2 * I, K, epilogue=1))
     D = _run_gpu(cuda_lib, ops, 2 * I, K, torch.bfloat16)
     perm = np.full(ops["M"], -1, np.int32)
@@ -226,3 +233,12 @@ def test_tiled_swiglu_epilogue_equals_standalone_swiglu(cuda_lib):
     h, _, _, _ = cuda_lib.moe_swiglu_quantize(D, dev(perm), I)
     rows = _valid_rows(ops)
     np.testing.assert_array_equal(h_fused[rows], u16(h)[rows])
+    # and against the oracle's SwiGLU of the same BF16 gate/up values
+    j = np.arange(2 * I)
+    src = np.where(j % 128 < 64, (j // 128) * 64 + j % 128, I + (j // 128) * 64 + j % 128 - 64)
+    d_il = u16(D)[rows]
+    d_can = np.empty_like(d_il)
+    d_can[:, src] = d_il
+    np.testing.assert_array_equal(h_fused[rows], M.swiglu(d_can, I))
+    gate = F.bf16_to_f32(d_can[:, :I])
+    assert (gate < -80).sum() > 2000            # the exact path did run, many per row
