@@ -257,7 +257,7 @@ def run_ours(args, rank, world, local_rank):
     for name, fn in (("route_topk", route), ("gateup_gemm_swiglu", gemm13), ("down_gemm", gemm2),
                      ("combine", combine)):
         stages[name] = time_launches(fn, iters, flush, stream)[0]
-    stages["grouping_quantise_requant"] = max(ms_per_step - sum(stages.values()), 0.0)
+    stages["grouping_quantise_gather_requant"] = max(ms_per_step - sum(stages.values()), 0.0)
     torch.cuda.synchronize()
 
     # dominant kernel: the gate/up grouped GEMM with the SwiGLU epilogue
@@ -360,7 +360,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x_h, logits_h, w13_h, w2_h, shape, budget_s=args.cpu_seconds)
 
-    launches_per_step = 1 + 8      # route + (3 grouping, quantise/scatter, gate/up+SwiGLU GEMM, requant, down GEMM, combine)
+    launches_per_step = 1 + 9      # route + (3 grouping, token quantise, slot gather, gate/up+SwiGLU GEMM, requant, down GEMM, combine)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,

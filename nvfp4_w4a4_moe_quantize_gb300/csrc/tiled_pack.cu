@@ -1,0 +1,120 @@
+// Data movement into the GEMM-tiled operand layout (tiled.cuh): packing of row-major
+// codes and scales, and the gather of token rows into the expert-grouped routed slots
+// ("Low-Bit Precision Training Is Ready for Production...", §"What W4A4 GEMM Actually
+// Changes": the expert GEMMs read these operands).
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "tiled.cuh"
+
+namespace nvfp4 {
+
+// Row-major codes [rows, K/2] + 128x4 tiled scales -> GEMM-tiled layout with R-row blocks;
+// rows rows .. round_up(rows, R) - 1 are written as zeros.  One thread per 16-byte code
+// chunk or 32-bit scale word of the output.
+__global__ void __launch_bounds__(256) pack_tiled_kernel(const uint8_t* __restrict__ codes,
+                                                         const uint8_t* __restrict__ sf, int64_t rows, int64_t K,
+                                                         int R, uint8_t* __restrict__ out) {
+  const int64_t kb = K / 256, rows_pad = (rows + R - 1) / R * R;
+  const int64_t chunks = K / 32, words = K / 64, per_row = chunks + words;
+  const int64_t total = rows_pad * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / per_row, u = i - r * per_row;
+    if (u < chunks) {
+      const uint4 v = r < rows ? *reinterpret_cast<const uint4*>(codes + r * (K / 2) + 16 * u) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(out + tiled_code_offset(r, 16 * u, kb, R)) = v;
+    } else {
+      const int64_t w = u - chunks;
+      const uint32_t v = r < rows ? *reinterpret_cast<const uint32_t*>(
+                                        sf + ((r >> 7) * words + w) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4)
+                                  : 0u;
+      *reinterpret_cast<uint32_t*>(out + tiled_sf_offset(r, 4 * w, kb, R)) = v;
+    }
+  }
+}
+
+// Gather of routed rows in the GEMM-tiled layout (128-row blocks): slot r of the
+// expert-grouped order receives token perm[r]'s row of the per-token operand `src` --
+// its codes and scales of every 256-K block -- and its global scale.  Slots with
+// perm[r] < 0 (group padding) are not written.  One warp per (128-row block, K block)
+// chunk of the output: 8 lanes move a row's 128 code bytes (re-swizzled for the
+// destination row, four rows per instruction), then the chunk's 512 scale words.  The
+// per-token operand is small next to L2, so the k-fold reads mostly hit there while the
+// writes go out as whole lines.
+__global__ void __launch_bounds__(256) gather_tiled_kernel(const uint8_t* __restrict__ src,
+                                                           const float* __restrict__ src_g,
+                                                           const int32_t* __restrict__ perm,
+                                                           const int32_t* __restrict__ n_rows_dev, int64_t max_rows,
+                                                           int64_t kblocks, uint8_t* __restrict__ dst,
+                                                           float* __restrict__ dst_g,
+                                                           uint32_t* __restrict__ amax_zero) {
+  constexpr int R = 128;
+  constexpr int64_t kChunk = R * 144;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  int64_t rows = *n_rows_dev;
+  if (rows > max_rows) rows = max_rows;
+  const int64_t chunks = rows / R * kblocks;
+  for (int64_t c = warp; c < chunks; c += nwarp) {
+    const int64_t b = c / kblocks, kb = c - (c / kblocks) * kblocks;
+    int32_t pr[4];   // tokens of rows lane + 32 i of this block
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pr[i] = perm[b * R + lane + 32 * i];
+    uint8_t* dchunk = dst + (b * kblocks + kb) * kChunk;
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+      const int rr = 4 * p + (lane >> 3), j = lane & 7;
+      const int32_t t = __shfl_sync(0xFFFFFFFFu, pr[p >> 3], rr & 31);
+      if (t >= 0) {
+        const int ts = t & (R - 1);
+        const uint8_t* schunk = src + ((int64_t)(t / R) * kblocks + kb) * kChunk;
+        const uint4 v = *reinterpret_cast<const uint4*>(schunk + ts * 128 + ((j ^ (ts & 7)) << 4));
+        *reinterpret_cast<uint4*>(dchunk + rr * 128 + ((j ^ (rr & 7)) << 4)) = v;
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      const int wi = 32 * p + lane, rr = wi >> 2, q = wi & 3;
+      const int32_t t = __shfl_sync(0xFFFFFFFFu, pr[p >> 2], rr & 31);
+      if (t >= 0) {
+        const int ts = t & (R - 1);
+        const uint8_t* schunk = src + ((int64_t)(t / R) * kblocks + kb) * kChunk;
+        *reinterpret_cast<uint32_t*>(dchunk + R * 128 + q * 512 + (rr & 31) * 16 + (rr >> 5) * 4) =
+            *reinterpret_cast<const uint32_t*>(schunk + R * 128 + q * 512 + (ts & 31) * 16 + (ts >> 5) * 4);
+      }
+    }
+    if (kb == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (pr[i] >= 0) dst_g[b * R + lane + 32 * i] = src_g[pr[i]];
+        if (amax_zero != nullptr) amax_zero[b * R + lane + 32 * i] = 0u;
+      }
+    }
+  }
+}
+
+cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const int32_t* perm, const int32_t* n_rows_dev,
+                                int64_t max_rows, int64_t K, uint8_t* dst, float* dst_g, uint32_t* amax_zero,
+                                cudaStream_t s) {
+  const int64_t chunks = max_rows / 128 * (K / 256);
+  if (chunks == 0) return cudaSuccess;
+  int64_t blocks = (chunks + 7) / 8;
+  if (blocks > 4 * (int64_t)num_sms()) blocks = 4 * (int64_t)num_sms();
+  gather_tiled_kernel<<<(int)blocks, 256, 0, s>>>(src, src_g, perm, n_rows_dev, max_rows, K / 256, dst, dst_g,
+                                                  amax_zero);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K, int R, uint8_t* out,
+                              cudaStream_t s) {
+  const int64_t rows_pad = (rows + R - 1) / R * R;
+  const int64_t total = rows_pad * (K / 32 + K / 64);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
+  pack_tiled_kernel<<<(int)blocks, 256, 0, s>>>(codes, sf, rows, K, R, out);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4
