@@ -409,9 +409,10 @@ def cpu_baseline(x_h, logits_h, w13_h, w2_h, shape, budget_s=15.0, tokens=None):
 
 
 def run_profile(args):
-    """A short launch sequence of one kernel on a small case, for ncu captures: the
-    gate/up grouped GEMM of a forward over --tokens tokens (Zipf routing, Qwen3 shapes),
-    or the standalone quantiser on a --tokens x 2048 tensor.  Prints nothing else."""
+    """A short launch sequence on a small case, for ncu captures: the gate/up grouped GEMM
+    of a forward over --tokens tokens (Zipf routing, Qwen3 shapes), whole forward steps
+    (routing + expert block) over --tokens tokens, or the standalone quantiser on a
+    --tokens x 2048 tensor.  Prints nothing else."""
     import __graft_entry__ as G
     G.build()
     import nvfp4_w4a4_moe_quantize_gb300 as L
@@ -433,6 +434,14 @@ def run_profile(args):
     ids, w = L.moe_route_topk(logits, k)
     ws = L.moe_forward_workspace(T, k, pw, dev)
     L.moe_expert_forward(x, ids, w, pw, workspace=ws)
+    if args.profile == "forward":      # whole forward steps: routing + the expert block
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        for _ in range(args.steps):
+            L.moe_route_topk(logits, k, True, out=(ids, w))
+            L.moe_expert_forward(x, ids, w, pw, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        assert L.nvfp4_status_check() == 0
+        return
     lay = L.moe_forward_workspace_layout(T, k, E, H, I)
     m = lay[13]
     vw = lambda i, n, dt: ws[lay[i]:lay[i] + n * torch.empty((), dtype=dt).element_size()].view(dt)  # noqa: E731
@@ -500,7 +509,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens-per-step", type=int, default=2)
-    ap.add_argument("--profile", choices=["none", "gateup", "quantiser"], default="none",
+    ap.add_argument("--profile", choices=["none", "gateup", "quantiser", "forward"], default="none",
                     help="run only a short launch sequence of one kernel (for ncu captures)")
     ap.add_argument("--tokens", type=int, default=2048, help="tokens (rows) of the --profile case")
     args = ap.parse_args()

@@ -81,7 +81,7 @@ ForwardLayout forward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t
   const int64_t nchunks = permute_chunks(T * k);
   size_t p = 0;
   *hist_off = p;
-  *hist_bytes = align256(sizeof(int32_t) * (size_t)(E * (nchunks > 0 ? nchunks : 1)));
+  *hist_bytes = align256(sizeof(int32_t) * (size_t)(E * (nchunks > 0 ? nchunks : 1) + 1));
   p += *hist_bytes;
   auto take = [&](size_t bytes) {
     const size_t o = p;
@@ -194,7 +194,7 @@ size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t E, int64_t H, 
     }
     case NVFP4_OP_MOE_PERMUTE: {
       const int64_t n = permute_chunks(a * b);
-      return align256(4u * (size_t)(E * (n > 0 ? n : 1)));
+      return align256(4u * (size_t)(E * (n > 0 ? n : 1) + 1));   // chunk histograms + a completion counter
     }
     default:
       return 0;

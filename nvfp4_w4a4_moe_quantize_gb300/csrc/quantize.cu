@@ -419,9 +419,26 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
 
 // Per-row NVFP4 of rows whose max |x| is already known (the SwiGLU epilogue folds it
 // into amax_bits while it writes h): no row-wide reduction is left, so every thread
-// encodes one 16-value block on its own -- 32 bytes in, 8 bytes of codes and one scale
-// byte out -- and four neighbouring lanes (blocks 4w .. 4w+3 of a row) gather the
-// 32-bit scale word.  Blocks past I (up to Ip) are written as zeros.
+// encodes two neighbouring 16-value blocks on its own -- 64 bytes in (four 16-byte loads
+// issued before anything waits on them), 16 bytes of codes and two scale bytes out --
+// and two neighbouring lanes (blocks 4w .. 4w+3 of a row) form the 32-bit scale word.
+// Blocks past I (up to Ip) are written as zeros.
+__device__ __forceinline__ void requant_block(const uint4& q0, const uint4& q1, float g, uint32_t& sf,
+                                              uint32_t& c0, uint32_t& c1) {
+  float v0[8], v1[8];
+  bf16x8_to_f32(q0, v0);
+  bf16x8_to_f32(q1, v1);
+  const BlockScale bs = block_scale(fmaxf(absmax8(v0), absmax8(v1)), g, __fmul_rn(6.0f, g));
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    v0[e] = __fmul_rn(v0[e], bs.r);
+    v1[e] = __fmul_rn(v1[e], bs.r);
+  }
+  sf = bs.sf;
+  c0 = e2m1x8_rn(v0);
+  c1 = e2m1x8_rn(v1);
+}
+
 __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16* __restrict__ h,
                                                             const uint32_t* __restrict__ amax_bits,
                                                             const int32_t* __restrict__ perm,
@@ -431,41 +448,36 @@ __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16*
   const int lane = threadIdx.x & 31;
   int64_t rows = *n_rows_dev;
   if (rows > max_rows) rows = max_rows;
-  const int64_t nb = Ip / 16, nb_data = I / 16, kblocks = Ip / 256;
-  const int64_t total = rows * nb;   // nb % 4 == 0: lane groups of 4 hold blocks 4w .. 4w+3 of one row
+  const int64_t np = Ip / 32, np_data = I / 32, kblocks = Ip / 256;
+  const int64_t total = rows * np;   // np % 2 == 0: lane pairs hold blocks 4w .. 4w+3 of one row
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += stride) {
     const int64_t i = base + threadIdx.x;
     const bool in = i < total;
-    const int64_t row = in ? i / nb : 0, blk = in ? i - (i / nb) * nb : 0;
-    const bool live = in && perm[row] >= 0;
-    uint32_t sfb = 0;
-    uint2 cw = make_uint2(0u, 0u);
-    if (live && blk < nb_data) {
-      const float g = __fdiv_rn(__uint_as_float(amax_bits[row]), kGlobalDivisor);
-      const uint4 q0 = ld_nc_v4(h + row * I + blk * 16);
-      const uint4 q1 = ld_nc_v4(h + row * I + blk * 16 + 8);
-      float v0[8], v1[8];
-      bf16x8_to_f32(q0, v0);
-      bf16x8_to_f32(q1, v1);
-      const BlockScale bs = block_scale(fmaxf(absmax8(v0), absmax8(v1)), g, __fmul_rn(6.0f, g));
+    const int64_t row = in ? i / np : 0, pr = in ? i - (i / np) * np : 0;
+    const bool data = in && pr < np_data;
+    uint4 q[4] = {};
+    if (data) {
+      const __nv_bfloat16* src = h + row * I + pr * 32;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        v0[e] = __fmul_rn(v0[e], bs.r);
-        v1[e] = __fmul_rn(v1[e], bs.r);
-      }
-      sfb = bs.sf;
-      cw = make_uint2(e2m1x8_rn(v0), e2m1x8_rn(v1));
-      if (blk == 0) g_out[row] = g;
+      for (int j = 0; j < 4; ++j) q[j] = ld_nc_v4(src + 8 * j);
     }
-    const uint32_t s1 = __shfl_down_sync(kFull, sfb, 1);
-    const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
-    const uint32_t s3 = __shfl_down_sync(kFull, sfb, 3);
+    const bool live = in && perm[row] >= 0;
+    uint32_t sf2 = 0;
+    uint4 cw = make_uint4(0u, 0u, 0u, 0u);
+    if (live && data) {
+      const float g = __fdiv_rn(__uint_as_float(amax_bits[row]), kGlobalDivisor);
+      uint32_t sa, sb;
+      requant_block(q[0], q[1], g, sa, cw.x, cw.y);
+      requant_block(q[2], q[3], g, sb, cw.z, cw.w);
+      sf2 = sa | (sb << 8);
+      if (pr == 0) g_out[row] = g;
+    }
+    const uint32_t s1 = __shfl_down_sync(kFull, sf2, 1);
     if (live) {
-      *reinterpret_cast<uint2*>(out + tiled_code_offset(row, blk * 8, kblocks, 128)) = cw;
-      if ((lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(out + tiled_sf_offset(row, blk, kblocks, 128)) =
-            sfb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      *reinterpret_cast<uint4*>(out + tiled_code_offset(row, pr * 16, kblocks, 128)) = cw;
+      if ((lane & 1) == 0)
+        *reinterpret_cast<uint32_t*>(out + tiled_sf_offset(row, 2 * pr, kblocks, 128)) = sf2 | (s1 << 16);
     }
   }
 }
@@ -473,7 +485,7 @@ __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16*
 cudaError_t launch_requant_tiled(const __nv_bfloat16* h, const uint32_t* amax_bits, const int32_t* perm,
                                  const int32_t* n_rows_dev, int64_t max_rows, int64_t I, int64_t Ip, uint8_t* out,
                                  float* g_out, cudaStream_t s) {
-  const int64_t total = max_rows * (Ip / 16);
+  const int64_t total = max_rows * (Ip / 32);
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();

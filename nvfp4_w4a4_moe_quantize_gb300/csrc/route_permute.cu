@@ -19,9 +19,19 @@ constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
 // ------------------------------------------------------------------ top-k routing
 
+// Float bits -> a key whose unsigned order is the float order (-0 is folded onto +0 so the
+// two compare equal, as floats do; NaN sorts below every number).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+  if (v != v) return 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // One warp per token.  Lane l holds experts l, l+32, ...; k rounds of a warp arg-max
-// with (larger logit, then lower id) as the order.  Weights: expf relative to the top
-// logit, then divided by the sum over the chosen k (or over all experts).
+// with (larger logit, then lower id) as the order: each round one warp max-reduction of
+// the order keys (redux.sync) and one min-reduction of the expert ids holding that key.
+// Weights: expf relative to the top logit, then divided by the sum over the chosen k (or
+// over all experts).
 template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
                                                          int renorm, int32_t* __restrict__ ids,
@@ -31,38 +41,39 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const int64_t nwarp = (int64_t)gridDim.x * 8;
   for (int64_t t = warp; t < T; t += nwarp) {
     float v[EPL];
+    uint32_t key[EPL];
     const float* lr = logits + t * E;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
       v[i] = e < E ? lr[e] : -INFINITY;
     }
-    uint32_t taken = 0;
+    uint32_t live = 0;   // bit i: expert lane + 32 i exists and is not taken yet
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      key[i] = order_key(v[i]);
+      if (lane + 32 * i < E) live |= 1u << i;
+    }
     int my_id = 0;
     float my_v = 0.0f;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7FFFFFFF;
+      uint32_t best = 0;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
+      for (int i = 0; i < EPL; ++i)
+        if ((live >> i) & 1u) best = max(best, key[i]);
+      const uint32_t wbest = __reduce_max_sync(kFullMask, best);
+      uint32_t cand = 0xFFFFFFFFu;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(kFullMask, bv, o);
-        const int oi = __shfl_xor_sync(kFullMask, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      for (int i = EPL - 1; i >= 0; --i)
+        if (((live >> i) & 1u) && key[i] == wbest) cand = (uint32_t)(lane + 32 * i);
+      const uint32_t bi = __reduce_min_sync(kFullMask, cand);
+      float bv = 0.0f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) bv = (uint32_t)(lane + 32 * i) == bi ? v[i] : bv;
+      if ((int)(bi & 31u) == lane) live &= ~(1u << (bi >> 5));
+      bv = __shfl_sync(kFullMask, bv, (int)(bi & 31u));
       if (lane == j) {
-        my_id = bi;
+        my_id = (int)bi;
         my_v = bv;
       }
     }
@@ -108,28 +119,36 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int 
 // ------------------------------------------------------------------ expert grouping
 
 // Pass 1: per chunk of kPermuteChunk flattened entries (one warp each), the count of
-// entries per expert.  hist is [E][nchunks].  Matching lanes are found with
-// __match_any_sync; the lowest lane of each match group adds the group's size.
+// entries per expert.  hist is [E][nchunks].  The warp loads its whole chunk first (one
+// round trip), then finds matching lanes with __match_any_sync; the lowest lane of each
+// match group adds the group's size.  Block 0 also clears the completion counter that
+// pass 2 uses (hist[E * nchunks]).
+constexpr int kPermuteSteps = kPermuteChunk / 32;
 __global__ void __launch_bounds__(256) permute_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int E,
                                                            int64_t nchunks, int32_t* __restrict__ hist,
                                                            int* status) {
   extern __shared__ int32_t sh[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  if (blockIdx.x == 0 && threadIdx.x == 0) hist[(int64_t)E * nchunks] = 0;
   const int64_t c = (int64_t)blockIdx.x * 8 + wib;
   if (c >= nchunks) return;
   int32_t* cnt = sh + wib * E;
   for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  const int64_t begin = c * kPermuteChunk;
+  int ev[kPermuteSteps];
+#pragma unroll
+  for (int u = 0; u < kPermuteSteps; ++u) {
+    const int64_t i = begin + 32 * u + lane;
+    ev[u] = i < n ? ids[i] : -1;
+  }
   __syncwarp();
-  const int64_t end = min(n, (c + 1) * kPermuteChunk);
-  for (int64_t base = c * kPermuteChunk; base < end; base += 32) {
-    const int64_t i = base + lane;
-    int e = -1;
-    if (i < end) {
-      e = ids[i];
-      if (e < 0 || e >= E) {
-        set_status(status, kStatusBadInput);
-        e = -1;
-      }
+#pragma unroll
+  for (int u = 0; u < kPermuteSteps; ++u) {
+    const int64_t i = begin + 32 * u + lane;
+    int e = ev[u];
+    if (i < n && (e < 0 || e >= E)) {
+      set_status(status, kStatusBadInput);
+      e = -1;
     }
     const unsigned peers = __match_any_sync(kFullMask, e);
     if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
@@ -138,9 +157,10 @@ __global__ void __launch_bounds__(256) permute_hist_kernel(const int32_t* __rest
   for (int e = lane; e < E; e += 32) hist[(int64_t)e * nchunks + c] = cnt[e];
 }
 
-// Pass 2 (one block): exclusive scan of every expert's chunk counts (in place), the
-// per-expert totals, the unpadded and 128-padded exclusive scans over experts, and -1
-// in the padding slots of perm.
+// Pass 2: one warp per expert scans that expert's chunk counts in place (exclusive) and
+// writes its total.  The last block to finish -- a completion counter, no block waits
+// for another -- runs the unpadded and 128-padded exclusive scans over the experts
+// (E <= 1024) and writes -1 into the padding slots of perm.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ hist, int64_t nchunks, int E,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets,
@@ -149,9 +169,11 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
   __shared__ int32_t s_cnt[1024];
   __shared__ int32_t s_pad[1025];
   __shared__ int32_t s_wsum[2][32];
+  __shared__ int s_last;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
   constexpr int kVec = 8;
-  for (int e = wid; e < E; e += 32) {
+  for (int e = blockIdx.x * nw + wid; e < E; e += gridDim.x * nw) {
     int32_t* h = hist + (int64_t)e * nchunks;
     int32_t carry = 0;
     for (int64_t c0 = 0; c0 < nchunks; c0 += 32 * kVec) {
@@ -174,12 +196,26 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
         carry += __shfl_sync(kFullMask, x, 31);
       }
     }
-    if (lane == 0) s_cnt[e] = carry;
+    if (lane == 0) counts[e] = carry;
+  }
+  // completion: the last block sees every count
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int* done = hist + (int64_t)E * nchunks;
+    if (gridDim.x == 1) {
+      s_last = 1;                     // a single block needs no counter
+    } else {
+      s_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+      if (s_last) *done = 0;
+    }
   }
   __syncthreads();
-  // block scans over experts (E <= 1024): one thread per expert
+  if (!s_last) return;
+  __threadfence();
   const int e = threadIdx.x;
-  const int32_t cnt = e < E ? s_cnt[e] : 0;
+  const int32_t cnt = e < E ? *reinterpret_cast<volatile int32_t*>(counts + e) : 0;
+  if (e < E) s_cnt[e] = cnt;
   const int32_t pc = (cnt + 127) / 128 * 128;
   int32_t x0 = cnt, x1 = pc;
 #pragma unroll
@@ -214,7 +250,6 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
   const int32_t excl0 = x0 - cnt + s_wsum[0][wid];
   const int32_t excl1 = x1 - pc + s_wsum[1][wid];
   if (e < E) {
-    counts[e] = cnt;
     offsets[e] = excl0;
     padded[e] = excl1;
     s_pad[e] = excl1;
@@ -252,14 +287,18 @@ __global__ void __launch_bounds__(256) permute_rank_kernel(const int32_t* __rest
   for (int e = lane; e < E; e += 32) run[e] = hist[(int64_t)e * nchunks + c];
   __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
-  const int64_t end = min(n, (c + 1) * kPermuteChunk);
-  for (int64_t base = c * kPermuteChunk; base < end; base += 32) {
-    const int64_t i = base + lane;
-    int e = -1;
-    if (i < end) {
-      e = ids[i];
-      if (e < 0 || e >= E) e = -1;
-    }
+  const int64_t begin = c * kPermuteChunk, end = min(n, (c + 1) * kPermuteChunk);
+  int ev[kPermuteSteps];   // the whole chunk first: one round trip
+#pragma unroll
+  for (int u = 0; u < kPermuteSteps; ++u) {
+    const int64_t i = begin + 32 * u + lane;
+    ev[u] = i < end ? ids[i] : -1;
+  }
+#pragma unroll
+  for (int u = 0; u < kPermuteSteps; ++u) {
+    const int64_t i = begin + 32 * u + lane;
+    int e = ev[u];
+    if (e >= E) e = -1;
     const unsigned peers = __match_any_sync(kFullMask, e);
     if (e >= 0) {
       const int32_t slot = s_pad[e] + run[e] + __popc(peers & lt);
@@ -284,7 +323,11 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t*
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  permute_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, E, counts, offsets, padded, perm);
+  if (nchunks == 0) {   // no entries: the scan still writes counts / offsets (one block)
+    permute_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, E, counts, offsets, padded, perm);
+  } else {
+    permute_scan_kernel<<<(E + 31) / 32, 1024, 0, s>>>(hist, nchunks, E, counts, offsets, padded, perm);
+  }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || nchunks == 0) return err;
   permute_rank_kernel<<<blocks, 256, 9 * E * sizeof(int32_t), s>>>(ids, n, k, E, nchunks, hist, padded, inv, perm);

@@ -39,8 +39,9 @@ __global__ void __launch_bounds__(256) pack_tiled_kernel(const uint8_t* __restri
 // perm[r] < 0 (group padding) are not written.  One warp per (128-row block, K block)
 // chunk of the output: 8 lanes move a row's 128 code bytes (re-swizzled for the
 // destination row, four rows per instruction), then the chunk's 512 scale words.  The
-// per-token operand is small next to L2, so the k-fold reads mostly hit there while the
-// writes go out as whole lines.
+// per-token operand is small next to L2, so the k-fold reads hit there; the writes go out
+// as whole lines with the streaming (evict-first) store hint, so that they do not push
+// the per-token operand out of L2.
 __global__ void __launch_bounds__(256) gather_tiled_kernel(const uint8_t* __restrict__ src,
                                                            const float* __restrict__ src_g,
                                                            const int32_t* __restrict__ perm,
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(256) gather_tiled_kernel(const uint8_t* __rest
         const int ts = t & (R - 1);
         const uint8_t* schunk = src + ((int64_t)(t / R) * kblocks + kb) * kChunk;
         const uint4 v = *reinterpret_cast<const uint4*>(schunk + ts * 128 + ((j ^ (ts & 7)) << 4));
-        *reinterpret_cast<uint4*>(dchunk + rr * 128 + ((j ^ (rr & 7)) << 4)) = v;
+        __stcs(reinterpret_cast<uint4*>(dchunk + rr * 128 + ((j ^ (rr & 7)) << 4)), v);
       }
     }
 #pragma unroll
@@ -80,8 +81,8 @@ __global__ void __launch_bounds__(256) gather_tiled_kernel(const uint8_t* __rest
       if (t >= 0) {
         const int ts = t & (R - 1);
         const uint8_t* schunk = src + ((int64_t)(t / R) * kblocks + kb) * kChunk;
-        *reinterpret_cast<uint32_t*>(dchunk + R * 128 + q * 512 + (rr & 31) * 16 + (rr >> 5) * 4) =
-            *reinterpret_cast<const uint32_t*>(schunk + R * 128 + q * 512 + (ts & 31) * 16 + (ts >> 5) * 4);
+        __stcs(reinterpret_cast<unsigned int*>(dchunk + R * 128 + q * 512 + (rr & 31) * 16 + (rr >> 5) * 4),
+               *reinterpret_cast<const unsigned int*>(schunk + R * 128 + q * 512 + (ts & 31) * 16 + (ts >> 5) * 4));
       }
     }
     if (kb == 0) {
