@@ -94,19 +94,21 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
   }
 }
 
-// Max |x| of a contiguous tensor seen as n16 16-byte chunks: four independent loads in
-// flight per thread, one atomicMax per block.
+// Max |x| of a contiguous tensor seen as n16 16-byte chunks: eight independent loads in
+// flight per thread (up to 2048 threads per SM: ~256 KB in flight), one atomicMax per
+// block.
 __global__ void __launch_bounds__(256) amax_flat_kernel(const uint4* __restrict__ x, int64_t n16,
                                                         uint32_t* amax_bits) {
+  constexpr int kU = 8;
   float m = 0.0f;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < n16; i += 4 * stride) {
-    uint4 v[4];
+  for (; i + (kU - 1) * stride < n16; i += kU * stride) {
+    uint4 v[kU];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = ld_nc_v4(x + i + u * stride);
+    for (int u = 0; u < kU; ++u) v[u] = ld_nc_v4(x + i + u * stride);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kU; ++u) {
       float f[8];
       bf16x8_to_f32(v[u], f);
       m = fmaxf(m, absmax8(f));
@@ -263,11 +265,12 @@ __host__ __device__ constexpr size_t stream_smem_bytes(int stages, int stride) {
   return (size_t)kQWarps * stages * stride + (size_t)kQWarps * stages * sizeof(uint64_t) + 16;
 }
 
+// One 16-value block (two 16-byte chunks of BF16) -> its E4M3 scale byte and 8 bytes of
+// codes, given the scope's g and 6g.
 template <int RND>
-__device__ __forceinline__ void encode_block(const QuantArgs& a, int64_t row, int64_t blk, const uint8_t* src,
-                                             float g, float six_g, uint32_t& sf_out, uint2& codes_out) {
-  const uint4 q0 = *reinterpret_cast<const uint4*>(src);
-  const uint4 q1 = *reinterpret_cast<const uint4*>(src + 16);
+__device__ __forceinline__ void encode_regs(const QuantArgs& a, int64_t row, int64_t blk, const uint4& q0,
+                                            const uint4& q1, float g, float six_g, uint32_t& sf_out,
+                                            uint2& codes_out) {
   float f[16];
   {
     float h0[8], h1[8];
@@ -300,6 +303,66 @@ __device__ __forceinline__ void encode_block(const QuantArgs& a, int64_t row, in
     codes_out.y = e2m1x8_rn(v1);
   }
   sf_out = bs.sf;
+}
+
+template <int RND>
+__device__ __forceinline__ void encode_block(const QuantArgs& a, int64_t row, int64_t blk, const uint8_t* src,
+                                             float g, float six_g, uint32_t& sf_out, uint2& codes_out) {
+  encode_regs<RND>(a, row, blk, *reinterpret_cast<const uint4*>(src), *reinterpret_cast<const uint4*>(src + 16), g,
+                   six_g, sf_out, codes_out);
+}
+
+// Scopes whose global scale is known before encoding (per tensor, per group: after the
+// amax pass, or given): every 64-value group of a row is independent.  One thread per
+// group: 128 bytes in (eight 16-byte loads issued together), four blocks encoded, 8 bytes
+// of codes per block and one 32-bit scale word out -- no row reduction, no cross-lane
+// traffic.  The (row, group) position advances by the grid stride without divisions.
+// Groups past the data (up to cols_pad) are written as zeros, and so are the scale words
+// of rows .. rows_total-1.
+template <int RND>
+__global__ void __launch_bounds__(256) quantize_known_scale_kernel(QuantArgs a) {
+  const int64_t words = a.sf_words, nb = a.cols / 16, nb_pad = a.cols_pad / 16;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t s_row = stride / words, s_w = stride - s_row * words;
+  int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t row = i0 / words, w = i0 - row * words;
+  float g0 = 0.0f;
+  if (a.mode == kScopeTensor)
+    g0 = a.g_in ? a.g_in[0] : __fdiv_rn(__uint_as_float(a.amax_bits[0]), kGlobalDivisor);
+  for (; row < a.rows; row += s_row, w += s_w) {
+    if (w >= words) {
+      w -= words;
+      if (++row >= a.rows) break;
+    }
+    const int64_t blk0 = 4 * w;
+    uint4 q[8];
+    const __nv_bfloat16* xr = a.x + row * a.ld + blk0 * 16;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = blk0 + j / 2 < nb ? ld_nc_v4(xr + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
+    float g = g0;
+    int64_t gi = 0;
+    if (a.mode != kScopeTensor) {
+      gi = (int64_t)((uint32_t)row / (uint32_t)a.group_rows);
+      g = a.g_in ? a.g_in[gi] : __fdiv_rn(__uint_as_float(a.amax_bits[gi]), kGlobalDivisor);
+    }
+    const float six_g = __fmul_rn(6.0f, g);
+    uint32_t sfw = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t blk = blk0 + b;
+      uint32_t sf = 0;
+      uint2 cw = make_uint2(0u, 0u);
+      if (blk < nb) encode_regs<RND>(a, row, blk, q[2 * b], q[2 * b + 1], g, six_g, sf, cw);
+      sfw |= sf << (8 * b);
+      if (blk < nb_pad) *reinterpret_cast<uint2*>(code_ptr(a, row, blk * 8)) = cw;
+    }
+    *reinterpret_cast<uint32_t*>(sfw_ptr(a, row, w)) = sfw;
+    if (w == 0 && a.g_out != nullptr && (a.mode == kScopeTensor ? row == 0 : row % a.group_rows == 0))
+      a.g_out[gi] = g;
+  }
+  if (a.tiled_R == 0)
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (a.rows_total - a.rows) * words; i += stride)
+      *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(a.rows + i / words, i % words, words)) = 0u;
 }
 
 template <int RND>
@@ -530,7 +593,7 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, i
   if (group_rows == 0 && ld == cols) {   // one scope over contiguous rows: flat pass
     const int64_t n16 = rows * cols / 8;
     int64_t blocks = (n16 + 255) / 256;
-    if (blocks > 4 * sms) blocks = 4 * sms;
+    if (blocks > 8 * sms) blocks = 8 * sms;
     amax_flat_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(x), n16, amax_bits);
     return cudaGetLastError();
   }
@@ -550,6 +613,17 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
   // rows of up to 2048 columns whose pitch keeps every row 16-byte aligned: streaming path
   // (the only one that writes the GEMM-tiled layout or takes a row filter / device count)
   const bool stream_ok = maxc <= 8 && (a.ld * 2) % 16 == 0;
+  // per-tensor / per-group scopes in row order: the elementwise kernel
+  if (a.mode != kScopeRow && a.map == kMapIdentity && a.row_filter == nullptr && a.rows_dev == nullptr &&
+      (a.ld * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) {
+    const int64_t total = (a.rows > a.rows_total - a.rows ? a.rows : a.rows_total - a.rows) * a.sf_words;
+    int64_t nb = (total + 255) / 256;
+    if (nb > 8 * (int64_t)sms) nb = 8 * (int64_t)sms;
+    if (nb < 1) nb = 1;
+    if (rounding == kRoundSR) quantize_known_scale_kernel<kRoundSR><<<(int)nb, 256, 0, s>>>(a);
+    else quantize_known_scale_kernel<kRoundRNE><<<(int)nb, 256, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   if (!stream_ok && (a.tiled_R != 0 || a.row_filter != nullptr || a.rows_dev != nullptr)) return cudaErrorInvalidValue;
   if (stream_ok) {
     // ring sizing: stride = the row rounded up to 128 bytes; up to 4 blocks (32 warps) per
