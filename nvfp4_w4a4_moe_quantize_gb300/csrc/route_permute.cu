@@ -338,7 +338,10 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t*
 
 // One warp per token; lane l owns columns 8l + 256i.  out = BF16 of the float32 sum, in
 // order j = 0..k-1, of float32 products w[t, j] * y[slot]; a slot of -1 (an entry whose
-// expert id was rejected) contributes nothing.
+// expert id was rejected) contributes nothing.  For k <= KM the k slot rows of a column
+// chunk are loaded before any is summed (k loads in flight per lane); a missing slot
+// loads zeros with weight 0, whose +0 product leaves the (never -0) sum unchanged.
+template <int KM>
 __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ y,
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int64_t T, int k, int64_t H,
@@ -353,20 +356,41 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
       my_slot = inv[t * k + lane];
       my_w = w[t * k + lane];
     }
+    if (my_slot < 0) my_w = 0.0f;
     for (int64_t c = 8 * lane; c < H; c += 256) {
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        const int32_t sl = __shfl_sync(kFullMask, my_slot, j);
-        const float wj = __shfl_sync(kFullMask, my_w, j);
-        if (sl < 0) continue;
-        const uint4 q = *reinterpret_cast<const uint4*>(y + (int64_t)sl * H + c);
-        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+      if constexpr (KM > 0) {
+        uint4 q[KM];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wj, __uint_as_float(wd[e] << 16)));
-          acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wj, __uint_as_float(wd[e] & 0xFFFF0000u)));
+        for (int j = 0; j < KM; ++j) {
+          const int32_t sl = __shfl_sync(kFullMask, my_slot, j);
+          q[j] = j < k && sl >= 0 ? *reinterpret_cast<const uint4*>(y + (int64_t)sl * H + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+          if (j >= k) break;
+          const float wj = __shfl_sync(kFullMask, my_w, j);
+          const uint32_t wd[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wj, __uint_as_float(wd[e] << 16)));
+            acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wj, __uint_as_float(wd[e] & 0xFFFF0000u)));
+          }
+        }
+      } else {
+        for (int j = 0; j < k; ++j) {
+          const int32_t sl = __shfl_sync(kFullMask, my_slot, j);
+          const float wj = __shfl_sync(kFullMask, my_w, j);
+          if (sl < 0) continue;
+          const uint4 q = *reinterpret_cast<const uint4*>(y + (int64_t)sl * H + c);
+          const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wj, __uint_as_float(wd[e] << 16)));
+            acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wj, __uint_as_float(wd[e] & 0xFFFF0000u)));
+          }
         }
       }
       uint4 o;
@@ -386,8 +410,10 @@ cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, in
   if (T == 0) return cudaSuccess;
   int64_t blocks = (T + 7) / 8;
   if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
-  combine_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(y), inv, w, T, k, H,
-                                             static_cast<__nv_bfloat16*>(out));
+  const auto* yp = static_cast<const __nv_bfloat16*>(y);
+  auto* op = static_cast<__nv_bfloat16*>(out);
+  if (k <= 8) combine_kernel<8><<<(int)blocks, 256, 0, s>>>(yp, inv, w, T, k, H, op);
+  else combine_kernel<0><<<(int)blocks, 256, 0, s>>>(yp, inv, w, T, k, H, op);
   return cudaGetLastError();
 }
 
