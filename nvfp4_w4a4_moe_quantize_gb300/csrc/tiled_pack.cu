@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(256) pack_tiled_kernel(const uint8_t* __restri
 // per-token operand is small next to L2, so the k-fold reads hit there; the writes go out
 // as whole lines with the streaming (evict-first) store hint, so that they do not push
 // the per-token operand out of L2.
-__global__ void __launch_bounds__(256) gather_tiled_kernel(const uint8_t* __restrict__ src,
+__global__ void __launch_bounds__(256, 4) gather_tiled_kernel(const uint8_t* __restrict__ src,
                                                            const float* __restrict__ src_g,
                                                            const int32_t* __restrict__ perm,
                                                            const int32_t* __restrict__ n_rows_dev, int64_t max_rows,
