@@ -2,7 +2,7 @@
 """Benchmark of the NVFP4 W4A4 MoE expert block on GB300.
 
 One step = one pass of the whole hot path over one batch: top-k routing of the router
-logits, then the expert-block forward (grouping, per-token NVFP4 quantisation scattered
+logits, then the expert-block forward (grouping, per-token NVFP4 quantisation gathered
 to every routed slot, gate/up W4A4 grouped GEMM, SwiGLU + requantisation, down W4A4
 grouped GEMM, weighted un-permute).  Weight quantisation is done once before timing
 (it runs once per weight update).  Workload: the Qwen3-30B-A3B-shaped block, T = 16384
@@ -157,6 +157,22 @@ def time_launches(fn, iters, flush, stream):
     return float(np.mean(ts)), float(np.median(ts))
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (replicas run side by side; the job takes as long as its
+    slowest rank).  One all-reduce on the process group's device (NCCL on GPUs, gloo on CPU)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time (weak scaling:
+    each replica runs the full per-GPU workload)."""
+    return world * tokens_per_rank * steps / (total_ms / 1e3)
+
+
 def run_ours(args, rank, world, local_rank):
     import __graft_entry__ as G
     G.build()
@@ -215,12 +231,8 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     wall_s = time.time() - t_wall
     clocks = sampler.stop()
-    total_ms = float(np.sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * T * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(float(np.sum(step_ms)), world, dev)
+    value = job_tokens_per_s(world, T, args.steps, total_ms)
     ms_per_step = total_ms / args.steps
     assert L.nvfp4_status_check() == 0
 
