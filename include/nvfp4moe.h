@@ -165,6 +165,20 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, i
                                     const float* global_scale_in, float* global_scale_out,
                                     uint8_t* codes_out, uint8_t* sf_out, void* stream);
 
+/* Dequantisation DQ ("The 4-bitter Lesson...", §"Improving Gradient Stability",
+ * footnote 6: DQ(Q(w)) = code value x block scale x global scale, the operand of the
+ * dequantised backward):
+ *     out[r, c] = value(code[r, c]) * decode(sf[r, c/16]) * g[scope(r)]
+ * rounded once (round to nearest even) from the exact value to out_dtype.
+ *   codes: device [rows, cols/2] (element 2i in the low nibble of byte i); sf: device,
+ *   128x4 tiled scales for rows x cols/16 (as nvfp4_quantize writes them); g: device
+ *   float, 1 (per tensor), rows (per row) or rows/group_rows (per group) values.
+ *   out: device [rows, ldo] of out_dtype.  cols % 16 == 0, ldo >= cols, ldo % 8 == 0;
+ *   codes, sf and out 16-byte aligned, g 4-byte aligned.  No workspace. */
+nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows,
+                              int64_t cols, nvfp4_scale_mode mode, int64_t group_rows, void* out,
+                              nvfp4_out_dtype out_dtype, int64_t ldo, void* stream);
+
 /* ---------------------------------------------------------------- grouped GEMM */
 
 /* W4A4 grouped GEMM over ragged expert groups ("Low-Bit Precision Training Is Ready

@@ -18,7 +18,7 @@ from . import build as _build
 
 __all__ = [
     "load", "library_path", "Status", "NVFP4Error",
-    "nvfp4_quantize", "nvfp4_quantize_noalloc", "nvfp4_grouped_gemm", "moe_route_topk", "moe_permute", "moe_combine",
+    "nvfp4_quantize", "nvfp4_quantize_noalloc", "nvfp4_dequantize", "nvfp4_grouped_gemm", "moe_route_topk", "moe_permute", "moe_combine",
     "moe_swiglu_quantize", "moe_prepare_weights", "moe_expert_forward", "moe_forward_workspace",
     "moe_forward_workspace_layout", "nvfp4_status_check", "nvfp4_sf_bytes", "NVFP4MoEWeights",
     "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled", "nvfp4_tiled_bytes",
@@ -63,6 +63,8 @@ _SIGS = {
                                       _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int, _u64, _u64,
                                               _vp, _vp, _vp, _vp, _vp]),
+    "nvfp4_dequantize": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _i64, _vp, ctypes.c_int, _i64,
+                                        _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                           _vp, ctypes.c_int, _i64, _vp]),
     "moe_route_topk": (ctypes.c_int, [_vp, _i64, _i32, _i32, ctypes.c_int, _vp, _vp, _vp]),
@@ -192,6 +194,21 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, roundi
                                       _p(global_scale), _p(g), _p(codes), _p(sf), _stream(stream)),
            "nvfp4_quantize_noalloc")
     return codes, sf, g
+
+
+def nvfp4_dequantize(codes: torch.Tensor, sf: torch.Tensor, g: torch.Tensor, cols: int,
+                     mode: int = SCALE_PER_TENSOR, group_rows: int = 0, out_dtype=torch.bfloat16,
+                     out: torch.Tensor | None = None, stream=None):
+    """DQ: out[rows, cols] = value(code) * block scale * global scale, rounded once to
+    out_dtype (BF16 or float32), from nvfp4_quantize's codes, tiled scales and g."""
+    lib = load()
+    rows = codes.shape[0]
+    if out is None:
+        out = torch.empty(rows, cols, dtype=out_dtype, device=_dev(codes))
+    _check(lib.nvfp4_dequantize(_p(codes), _p(sf), _p(g), rows, cols, mode, group_rows, _p(out),
+                                1 if out.dtype == torch.float32 else 0, out.stride(0), _stream(stream)),
+           "nvfp4_dequantize")
+    return out
 
 
 # --------------------------------------------------------------------------- GEMM

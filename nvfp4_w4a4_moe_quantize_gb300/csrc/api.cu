@@ -280,6 +280,20 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   return from_cuda(launch_quantize_rows(a, rounding, s));
 }
 
+nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows, int64_t cols,
+                              nvfp4_scale_mode mode, int64_t group_rows, void* out, nvfp4_out_dtype out_dtype,
+                              int64_t ldo, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0 || ldo < cols || ldo % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (mode < NVFP4_SCALE_PER_TENSOR || mode > NVFP4_SCALE_PER_GROUP) return NVFP4_ERR_INVALID_ARG;
+  if (mode == NVFP4_SCALE_PER_GROUP && (group_rows <= 0 || rows % group_rows != 0)) return NVFP4_ERR_INVALID_ARG;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_INVALID_ARG;
+  if (rows == 0) return NVFP4_OK;
+  if (!codes || !sf || !g || !out || !aligned16(codes) || !aligned16(sf) || !aligned16(out) || !aligned4(g))
+    return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_dequantize(codes, sf, g, rows, cols, mode, group_rows, out, out_dtype == NVFP4_OUT_F32, ldo,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const uint8_t* B,
                                 const uint8_t* SFB, const float* gB, const int32_t* group_offsets,
                                 const int32_t* group_rows, int64_t M_total, int64_t N, int64_t K, int32_t E,

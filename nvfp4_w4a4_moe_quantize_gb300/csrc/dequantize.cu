@@ -1,0 +1,91 @@
+// NVFP4 -> BF16 / float32: DQ(Q(x)) = value(code) * decode(block scale) * global scale,
+// the operand of the dequantised backward ("The 4-bitter Lesson: Balancing Stability and
+// Performance in NVFP4 RL", §"Improving Gradient Stability", footnote 6: Q and DQ).
+//
+// The exact value has at most 2 + 4 + 24 significant bits: value(code) * decode(sf) is
+// exact in float32, and the product with g is formed exactly as a float-float (product
+// and its fma remainder), then rounded once to the output type: float32 by the product
+// itself, BF16 by round-to-nearest-even of the product with the remainder breaking a tie
+// at a BF16 midpoint.  Magnitudes below 2^-100 (where the remainder could underflow) take
+// a float64 path.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "swiglu.cuh"
+
+namespace nvfp4 {
+
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  // 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives
+  const uint32_t m = code & 7u;
+  const float mag = m < 4u ? 0.5f * (float)m : (float)(m == 7u ? 6u : m - 2u);
+  return (code & 8u) ? -mag : mag;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 0xFu, m = b & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
+}
+
+// BF16 rounding of the exact product p = a * g (a exact in float32).
+__device__ __forceinline__ uint32_t dq_bf16_bits(float a, float g) {
+  const float hi = __fmul_rn(a, g);
+  if (hi == 0.0f) return __float_as_uint(hi) >> 16;            // exact zero (keeps its sign)
+  const float ahi = fabsf(hi);
+  if (!(ahi >= 0x1p-100f) || !(ahi <= 3.0e38f)) return f64_to_bf16_bits((double)a * (double)g);
+  const float lo = __fmaf_rn(a, g, -hi);
+  const uint32_t b = __float_as_uint(hi);
+  if ((b & 0xFFFFu) != 0x8000u || lo == 0.0f) return f32_to_bf16_rne_bits(b);
+  return ((lo > 0.0f) == (hi > 0.0f)) ? (b >> 16) + 1u : (b >> 16);
+}
+
+// One thread per 8 values (4 code bytes) of a row: 8 BF16 (16 bytes) or float32 (32
+// bytes) out; a warp covers 256 consecutive values of a row.
+template <bool kF32>
+__global__ void __launch_bounds__(256) dequantize_kernel(const uint8_t* __restrict__ codes,
+                                                         const uint8_t* __restrict__ sf,
+                                                         const float* __restrict__ g, int64_t rows, int64_t cols,
+                                                         int mode, int64_t group_rows, void* __restrict__ out,
+                                                         int64_t ldo) {
+  const int64_t chunks = cols / 8, total = rows * chunks, sf_words = (cols / 16 + 3) / 4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / chunks, c8 = i - r * chunks;
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(codes + r * (cols / 2) + 4 * c8);
+    const int64_t blk = c8 / 2;
+    const uint32_t sfb = sf[((r >> 7) * sf_words + blk / 4) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (blk & 3)];
+    const float gs = g[mode == kScopeTensor ? 0 : (mode == kScopeRow ? r : r / group_rows)];
+    const float s = e4m3_value(sfb);
+    if (kF32) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(__fmul_rn(e2m1_value((word >> (4 * e)) & 0xFu), s), gs);
+      float* o = static_cast<float*>(out) + r * ldo + 8 * c8;
+      *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(o + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      uint32_t h[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[e] = dq_bf16_bits(__fmul_rn(e2m1_value((word >> (4 * e)) & 0xFu), s), gs);
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + r * ldo + 8 * c8;
+      *reinterpret_cast<uint4*>(o) =
+          make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    }
+  }
+}
+
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows, int64_t cols,
+                              int mode, int64_t group_rows, void* out, bool out_f32, int64_t ldo, cudaStream_t s) {
+  const int64_t total = rows * (cols / 8);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 16 * (int64_t)num_sms()) blocks = 16 * (int64_t)num_sms();
+  if (out_f32)
+    dequantize_kernel<true><<<(int)blocks, 256, 0, s>>>(codes, sf, g, rows, cols, mode, group_rows, out, ldo);
+  else
+    dequantize_kernel<false><<<(int)blocks, 256, 0, s>>>(codes, sf, g, rows, cols, mode, group_rows, out, ldo);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -96,6 +96,9 @@ cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const in
 // float bits): g[r] = amax / 2688, codes and scales into the GEMM-tiled layout with
 // 128-row blocks and K = Ip (columns I .. Ip-1 zero).  Rows r < min(*n_rows_dev, max_rows)
 // with perm[r] >= 0 are encoded; the others are not written.
+// DQ of row-major codes + 128x4 tiled scales into BF16 or float32 rows of pitch ldo.
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows, int64_t cols,
+                              int mode, int64_t group_rows, void* out, bool out_f32, int64_t ldo, cudaStream_t s);
 cudaError_t launch_requant_tiled(const __nv_bfloat16* h, const uint32_t* amax_bits, const int32_t* perm,
                                  const int32_t* n_rows_dev, int64_t max_rows, int64_t I, int64_t Ip, uint8_t* out,
                                  float* g_out, cudaStream_t s);

@@ -457,3 +457,28 @@ def test_forward_full_size_sampled_and_row_invariant(cuda_lib):
     part = u16(cuda_lib.moe_expert_forward(xc[:1024].contiguous(), ids[:1024].contiguous(),
                                            w[:1024].contiguous(), pw))
     np.testing.assert_array_equal(part, u16(out)[:1024])
+
+
+@pytest.mark.parametrize("sizes", [(1, 7, 64), (3, 16, 33)])
+def test_decode_shaped_launches_match_the_learner_shaped_launch(cuda_lib, sizes):
+    """Execution alignment between a sampler-shaped and a learner-shaped launch ("Low-Bit
+    Precision Training Is Ready for Production...", §"The Cross-Engine Alignment Problem"):
+    tokens run through decode-size batches (1 to 64 tokens, one or a few row tiles per
+    expert, most experts empty) give exactly the bits the same tokens get inside the full
+    16,384-token batch of the forward workload, whose groups span many row tiles."""
+    shape = S.WORKLOADS["forward"]
+    x, logits, w13, w2 = S.moe_inputs(shape, seed=3)
+    ids, w = cuda_lib.moe_route_topk(logits.cuda(), shape.k)
+    pw = cuda_lib.moe_prepare_weights(w13.cuda(), w2.cuda())
+    xc = x.cuda()
+    learner = u16(cuda_lib.moe_expert_forward(xc, ids, w, pw))
+    start = 5000
+    for n in sizes:
+        sl = slice(start, start + n)
+        dec = u16(cuda_lib.moe_expert_forward(xc[sl].contiguous(), ids[sl].contiguous(), w[sl].contiguous(), pw))
+        np.testing.assert_array_equal(dec, learner[sl])
+        # the router too: top-k of a decode batch equals the rows of the full launch
+        dids, dw = cuda_lib.moe_route_topk(logits[sl].contiguous().cuda(), shape.k)
+        np.testing.assert_array_equal(npy(dids), npy(ids)[sl])
+        np.testing.assert_array_equal(npy(dw), npy(w)[sl])
+        start += n

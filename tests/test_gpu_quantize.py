@@ -107,3 +107,34 @@ def test_bad_arguments_raise(cuda_lib):
     x = torch.zeros(4, 24, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(cuda_lib.NVFP4Error):
         cuda_lib.nvfp4_quantize(x)
+
+
+@pytest.mark.parametrize("scope", ["tensor", "row", "group"])
+@pytest.mark.parametrize("shape", [(1, 16), (130, 272), (256, 2048)])
+def test_dequantize_matches_oracle(cuda_lib, scope, shape):
+    """DQ(Q(x)) on the GPU equals the oracle's exact float64 dequantisation rounded once:
+    BF16 and float32 outputs, bit for bit -- including rows whose tiny global scale puts
+    values in the BF16 subnormal range and rows of zeros."""
+    rows, cols = shape
+    rng = np.random.default_rng(rows + cols)
+    x = rng.standard_normal((rows, cols)) * rng.choice([1e-36, 1e-3, 1.0, 300.0], (rows, 1))
+    x[0, :16] = 0.0
+    xb = F.bf16_round(x)
+    group_rows = 2 if scope == "group" and rows % 2 == 0 else 0
+    if scope == "group" and group_rows == 0:
+        pytest.skip("group scope needs rows divisible by the group")
+    q = Q.quantize(xb, scope=scope, group_rows=group_rows if group_rows else None)
+    codes = dev(F.pack_e2m1(q["codes"]))
+    sf = dev(F.sf_swizzle(q["sf"]))
+    g = dev(np.asarray(q["g"], np.float32))
+    mode = {"tensor": cuda_lib.SCALE_PER_TENSOR, "row": cuda_lib.SCALE_PER_ROW, "group": cuda_lib.SCALE_PER_GROUP}[scope]
+    g_rows = np.asarray(q["g"], np.float64)
+    if scope == "tensor":
+        g_rows = np.full(rows, g_rows[0])
+    elif scope == "group":
+        g_rows = np.repeat(g_rows, group_rows)
+    exact = Q.dequantize(q["codes"], q["sf"], g_rows)
+    got_bf16 = u16(cuda_lib.nvfp4_dequantize(codes, sf, g, cols, mode, group_rows))
+    np.testing.assert_array_equal(got_bf16, F.bf16_round(exact))
+    got_f32 = npy(cuda_lib.nvfp4_dequantize(codes, sf, g, cols, mode, group_rows, out_dtype=torch.float32))
+    np.testing.assert_array_equal(got_f32.view(np.uint32), exact.astype(np.float32).view(np.uint32))
