@@ -109,7 +109,8 @@ enum {
   NVFP4_OP_QUANTIZE = 0,        /* args: rows, cols (others 0) */
   NVFP4_OP_PREPARE_WEIGHTS = 1, /* args: E, H, I */
   NVFP4_OP_MOE_FORWARD = 2,     /* args: T, k, E, H, I */
-  NVFP4_OP_MOE_PERMUTE = 3      /* args: T, k, E */
+  NVFP4_OP_MOE_PERMUTE = 3,     /* args: T, k, E */
+  NVFP4_OP_QUANTIZE_T = 4       /* args: batches * C (rows of the transpose), R */
 };
 size_t nvfp4_workspace_size(int op, int64_t T_or_rows, int64_t k_or_cols, int64_t E,
                             int64_t H, int64_t I);
@@ -164,6 +165,28 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, i
                                     nvfp4_rounding rounding, uint64_t seed, uint64_t rng_offset,
                                     const float* global_scale_in, float* global_scale_out,
                                     uint8_t* codes_out, uint8_t* sf_out, void* stream);
+
+/* Transposed quantisation, the layout of the backward's W4A4 GEMMs ("The 4-bitter
+ * Lesson...", §"Why is the NVFP4 pretraining recipe not sufficient for RL?": the
+ * backward GEMMs quantise their operands along the contraction of each GEMM -- the
+ * weights along their output dimension for dgrad, activations and gradients along
+ * tokens for wgrad -- with stochastic rounding as the recipe's option for gradients).
+ * x is `batches` stacked BF16 matrices [R, C] (pitch ld elements, batch b at rows b*R);
+ * the result is NVFP4 of their stacked transposes [batches*C, R], blocks of 16 along R:
+ * exactly nvfp4_quantize applied to that transposed BF16 matrix -- same scopes (per
+ * tensor; per row of the transpose; per group of group_rows rows of the transpose, so
+ * group_rows = C gives one scale per batch), same rounding modes and Philox stream
+ * (element index = row-major index in the transpose).
+ *   codes_out [batches*C, R/2], sf_out tiled for batches*C rows x R/16, as nvfp4_quantize.
+ *   workspace: nvfp4_workspace_size(NVFP4_OP_QUANTIZE_T, batches*C, R, 0, 0, 0) bytes
+ *   (the transposed BF16 copy and the amax scratch).  R % 16 == 0, R <= 8192, ld >= C,
+ *   ld % 8 == 0; x 16-byte aligned. */
+nvfp4_status nvfp4_quantize_transposed(const void* x, int64_t batches, int64_t R, int64_t C, int64_t ld,
+                                       nvfp4_scale_mode mode, int64_t group_rows,
+                                       nvfp4_rounding rounding, uint64_t seed, uint64_t rng_offset,
+                                       const float* global_scale_in, float* global_scale_out,
+                                       uint8_t* codes_out, uint8_t* sf_out, void* workspace,
+                                       size_t workspace_bytes, void* stream);
 
 /* Dequantisation DQ ("The 4-bitter Lesson...", §"Improving Gradient Stability",
  * footnote 6: DQ(Q(w)) = code value x block scale x global scale, the operand of the

@@ -18,7 +18,8 @@ from . import build as _build
 
 __all__ = [
     "load", "library_path", "Status", "NVFP4Error",
-    "nvfp4_quantize", "nvfp4_quantize_noalloc", "nvfp4_dequantize", "nvfp4_grouped_gemm", "moe_route_topk", "moe_permute", "moe_combine",
+    "nvfp4_quantize", "nvfp4_quantize_noalloc", "nvfp4_quantize_transposed", "nvfp4_dequantize",
+    "nvfp4_grouped_gemm", "moe_route_topk", "moe_permute", "moe_combine",
     "moe_swiglu_quantize", "moe_prepare_weights", "moe_expert_forward", "moe_forward_workspace",
     "moe_forward_workspace_layout", "nvfp4_status_check", "nvfp4_sf_bytes", "NVFP4MoEWeights",
     "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled", "nvfp4_tiled_bytes",
@@ -28,7 +29,7 @@ __all__ = [
 SCALE_PER_TENSOR, SCALE_PER_ROW, SCALE_PER_GROUP = 0, 1, 2
 ROUND_RNE, ROUND_STOCHASTIC = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
-OP_QUANTIZE, OP_PREPARE_WEIGHTS, OP_MOE_FORWARD, OP_MOE_PERMUTE = 0, 1, 2, 3
+OP_QUANTIZE, OP_PREPARE_WEIGHTS, OP_MOE_FORWARD, OP_MOE_PERMUTE, OP_QUANTIZE_T = 0, 1, 2, 3, 4
 
 _lib = None
 _vp, _i64, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t
@@ -63,6 +64,8 @@ _SIGS = {
                                       _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int, _u64, _u64,
                                               _vp, _vp, _vp, _vp, _vp]),
+    "nvfp4_quantize_transposed": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int,
+                                                 _u64, _u64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "nvfp4_dequantize": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _i64, _vp, ctypes.c_int, _i64,
                                         _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
@@ -193,6 +196,31 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, roundi
     _check(lib.nvfp4_quantize_noalloc(_p(x), rows, cols, x.stride(0), mode, group_rows, rounding, seed, rng_offset,
                                       _p(global_scale), _p(g), _p(codes), _p(sf), _stream(stream)),
            "nvfp4_quantize_noalloc")
+    return codes, sf, g
+
+
+def nvfp4_quantize_transposed(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, rounding: int = ROUND_RNE,
+                              seed: int = 0, rng_offset: int = 0, group_rows: int = 0,
+                              global_scale: torch.Tensor | None = None, stream=None):
+    """NVFP4 of the transposes of BF16 matrices: x [R, C] or [batches, R, C] -> codes of
+    the stacked transposes [batches*C, R/2], tiled scales and g, exactly as nvfp4_quantize
+    of that transposed matrix (blocks of 16 along R)."""
+    lib = load()
+    assert x.dtype == torch.bfloat16 and x.stride(-1) == 1
+    x3 = x if x.dim() == 3 else x.unsqueeze(0)
+    assert x3.is_contiguous() or x.dim() == 2
+    batches, R, C = x3.shape
+    ld = x.stride(-2)
+    rows_t = batches * C
+    dev = _dev(x)
+    n_g = 1 if mode == SCALE_PER_TENSOR else (rows_t if mode == SCALE_PER_ROW else rows_t // max(group_rows, 1))
+    codes = torch.empty(rows_t, R // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(max(nvfp4_sf_bytes(rows_t, R), 16), dtype=torch.uint8, device=dev)
+    g = torch.empty(max(n_g, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(int(lib.nvfp4_workspace_size(OP_QUANTIZE_T, rows_t, R, 0, 0, 0)), dtype=torch.uint8, device=dev)
+    _check(lib.nvfp4_quantize_transposed(_p(x), batches, R, C, ld, mode, group_rows, rounding, seed, rng_offset,
+                                         _p(global_scale), _p(g), _p(codes), _p(sf), _p(ws), ws.numel(),
+                                         _stream(stream)), "nvfp4_quantize_transposed")
     return codes, sf, g
 
 

@@ -196,6 +196,8 @@ size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t E, int64_t H, 
       const int64_t n = permute_chunks(a * b);
       return align256(4u * (size_t)(E * (n > 0 ? n : 1) + 1));   // chunk histograms + a completion counter
     }
+    case NVFP4_OP_QUANTIZE_T:   // transposed BF16 copy [a, b] + amax scratch for up to a scopes
+      return align256(2u * (size_t)a * (size_t)b) + align256(4u * (size_t)(a > 1 ? a : 1));
     default:
       return 0;
   }
@@ -278,6 +280,24 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   a.rng_offset = rng_offset;
   a.status = device_status_ptr();
   return from_cuda(launch_quantize_rows(a, rounding, s));
+}
+
+nvfp4_status nvfp4_quantize_transposed(const void* x, int64_t batches, int64_t R, int64_t C, int64_t ld,
+                                       nvfp4_scale_mode mode, int64_t group_rows, nvfp4_rounding rounding,
+                                       uint64_t seed, uint64_t rng_offset, const float* g_in, float* g_out,
+                                       uint8_t* codes, uint8_t* sf, void* ws, size_t ws_bytes, void* stream) {
+  if (batches < 0 || R <= 0 || C <= 0 || R % 16 != 0 || ld < C || ld % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (R > 8192) return NVFP4_ERR_UNSUPPORTED;
+  if (batches == 0) return NVFP4_OK;
+  if (!x || !aligned16(x)) return NVFP4_ERR_INVALID_ARG;
+  const int64_t rows_t = batches * C;
+  const size_t t_bytes = align256(2u * (size_t)rows_t * (size_t)R);
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < nvfp4_workspace_size(NVFP4_OP_QUANTIZE_T, rows_t, R, 0, 0, 0))
+    return NVFP4_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_transpose_bf16(x, batches, R, C, ld, ws, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  return nvfp4_quantize(ws, rows_t, R, R, mode, group_rows, rounding, seed, rng_offset, g_in, g_out, codes, sf,
+                        static_cast<uint8_t*>(ws) + t_bytes, ws_bytes - t_bytes, stream);
 }
 
 nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows, int64_t cols,

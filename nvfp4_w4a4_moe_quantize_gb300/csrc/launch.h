@@ -96,6 +96,9 @@ cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const in
 // float bits): g[r] = amax / 2688, codes and scales into the GEMM-tiled layout with
 // 128-row blocks and K = Ip (columns I .. Ip-1 zero).  Rows r < min(*n_rows_dev, max_rows)
 // with perm[r] >= 0 are encoded; the others are not written.
+// out[b*C + c, r] = x[b*R + r, c] (BF16, `batches` stacked [R, C] matrices of pitch ld).
+cudaError_t launch_transpose_bf16(const void* x, int64_t batches, int64_t R, int64_t C, int64_t ld, void* out,
+                                  cudaStream_t s);
 // DQ of row-major codes + 128x4 tiled scales into BF16 or float32 rows of pitch ldo.
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows, int64_t cols,
                               int mode, int64_t group_rows, void* out, bool out_f32, int64_t ldo, cudaStream_t s);

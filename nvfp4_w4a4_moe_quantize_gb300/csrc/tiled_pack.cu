@@ -107,6 +107,33 @@ cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const in
   return cudaGetLastError();
 }
 
+// out[b*C + c, r] = x[b*R + r, c] for `batches` stacked [R, C] BF16 matrices (pitch ld):
+// 32 x 32 tiles through shared memory (one padding column: no bank conflicts), loads and
+// stores both along rows.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
+                                                             int64_t ld, uint16_t* __restrict__ out) {
+  __shared__ uint16_t tile[32][33];
+  const int64_t b = blockIdx.z, c0 = (int64_t)blockIdx.x * 32, r0 = (int64_t)blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int j = ty; j < 32; j += 8) {
+    const int64_t r = r0 + j, c = c0 + tx;
+    if (r < R && c < C) tile[j][tx] = x[(b * R + r) * ld + c];
+  }
+  __syncthreads();
+  for (int j = ty; j < 32; j += 8) {
+    const int64_t c = c0 + j, r = r0 + tx;
+    if (r < R && c < C) out[(b * C + c) * R + r] = tile[tx][j];
+  }
+}
+
+cudaError_t launch_transpose_bf16(const void* x, int64_t batches, int64_t R, int64_t C, int64_t ld, void* out,
+                                  cudaStream_t s) {
+  if (batches == 0 || R == 0 || C == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((C + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)batches);
+  transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), R, C, ld, static_cast<uint16_t*>(out));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K, int R, uint8_t* out,
                               cudaStream_t s) {
   const int64_t rows_pad = (rows + R - 1) / R * R;

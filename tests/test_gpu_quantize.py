@@ -138,3 +138,59 @@ def test_dequantize_matches_oracle(cuda_lib, scope, shape):
     np.testing.assert_array_equal(got_bf16, F.bf16_round(exact))
     got_f32 = npy(cuda_lib.nvfp4_dequantize(codes, sf, g, cols, mode, group_rows, out_dtype=torch.float32))
     np.testing.assert_array_equal(got_f32.view(np.uint32), exact.astype(np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("scope", ["tensor", "row", "group"])
+@pytest.mark.parametrize("rounding", ["rne", "sr"])
+@pytest.mark.parametrize("shape", [(3, 48, 40), (1, 256, 2048), (2, 2048, 72)])
+def test_quantize_transposed_matches_oracle(cuda_lib, scope, rounding, shape):
+    """Transposed quantisation (blocks of 16 along the original rows) equals the oracle's
+    quantisation of the stacked transposes, codes / scales / global scales bit for bit,
+    for every scope and both roundings (group = one scale per stacked matrix)."""
+    B, R, C = shape
+    rng = np.random.default_rng(B * R + C)
+    x = rng.standard_normal((B, R, C)) * rng.choice([1e-3, 1.0, 40.0], (B, 1, C))
+    xb = F.bf16_round(x)
+    xt = np.ascontiguousarray(xb.transpose(0, 2, 1)).reshape(B * C, R)
+    group_rows = C if scope == "group" else 0
+    q = Q.quantize(xt, scope=scope, rounding=rounding, seed=11, group_rows=group_rows if group_rows else None)
+    mode = {"tensor": cuda_lib.SCALE_PER_TENSOR, "row": cuda_lib.SCALE_PER_ROW, "group": cuda_lib.SCALE_PER_GROUP}[scope]
+    rnd = cuda_lib.ROUND_RNE if rounding == "rne" else cuda_lib.ROUND_STOCHASTIC
+    codes, sf, g = cuda_lib.nvfp4_quantize_transposed(bf16_tensor(xb.reshape(B, R, C)), mode, rnd, seed=11,
+                                                      group_rows=group_rows)
+    np.testing.assert_array_equal(npy(codes), q["packed"])
+    np.testing.assert_array_equal(F.sf_unswizzle(npy(sf), B * C, R // 16), q["sf"])
+    np.testing.assert_array_equal(npy(g), np.asarray(q["g"], np.float32))
+
+
+def test_down_projection_dgrad_w4a4(cuda_lib):
+    """The dgrad GEMM of the down projection in W4A4: dh[r, i] = sum_h dY[r, h] W2_e[h, i]
+    with dY quantised per row along H and each expert's W2 quantised transposed (blocks
+    along H, one global scale per expert) -- the grouped GEMM over those operands against
+    the oracle's float64 GEMM over the same dequantised operands."""
+    from oracle import moe as M
+    from gpu_util import check_bf16_against
+    E, H, I = 3, 256, 256
+    counts = np.array([200, 0, 77])
+    padded = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)]).astype(np.int32)
+    Mt = int(padded[-1])
+    rng = np.random.default_rng(21)
+    w2 = F.bf16_round(rng.standard_normal((E, H, I)) * 0.02)
+    dy = np.zeros((Mt, H), np.uint16)
+    for e in range(E):
+        dy[padded[e]:padded[e] + counts[e]] = F.bf16_round(rng.standard_normal((counts[e], H)) * 1e-3)
+    # GPU operands
+    qa_c, qa_sf, qa_g = cuda_lib.nvfp4_quantize(bf16_tensor(dy), cuda_lib.SCALE_PER_ROW)
+    qb_c, qb_sf, qb_g = cuda_lib.nvfp4_quantize_transposed(bf16_tensor(w2), cuda_lib.SCALE_PER_GROUP, group_rows=I)
+    dh = cuda_lib.nvfp4_grouped_gemm(qa_c, qa_sf, qa_g, qb_c, qb_sf, qb_g, dev(padded),
+                                     dev(counts.astype(np.int32)), I, H, E)
+    # oracle: the same quantisation, then the float64 grouped GEMM
+    qa = Q.quantize(dy, scope="row")
+    w2t = np.ascontiguousarray(w2.transpose(0, 2, 1)).reshape(E * I, H)
+    qb = Q.quantize(w2t, scope="group", group_rows=I)
+    np.testing.assert_array_equal(npy(qb_c), qb["packed"])
+    ref = M.grouped_gemm(qa["codes"], qa["sf"], qa["g"], qb["codes"].reshape(E, I, H), qb["sf"].reshape(E, I, H // 16),
+                         qb["g"], padded, counts)
+    rows = np.concatenate([np.arange(p, p + c) for p, c in zip(padded[:-1], counts)]).astype(int)
+    nbad, worst = check_bf16_against(u16(dh)[rows], ref[rows])
+    assert nbad == 0, worst
