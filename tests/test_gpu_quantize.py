@@ -194,3 +194,37 @@ def test_down_projection_dgrad_w4a4(cuda_lib):
     rows = np.concatenate([np.arange(p, p + c) for p, c in zip(padded[:-1], counts)]).astype(int)
     nbad, worst = check_bf16_against(u16(dh)[rows], ref[rows])
     assert nbad == 0, worst
+
+
+def test_expert_wgrad_w4a4_with_stochastic_rounding(cuda_lib):
+    """The wgrad GEMM of an expert layer in W4A4: dW_e[n, h] = sum over the expert's
+    tokens t of dY[t, n] X[t, h].  The contraction runs over each expert's own (ragged)
+    token count, zero-padded to 256; dY is quantised transposed (blocks of 16 along tokens)
+    with Philox stochastic rounding, X transposed with RNE, one global scale per expert
+    matrix.  One GEMM per expert against the oracle's float64 GEMM over the same operands."""
+    from oracle import moe as M
+    from gpu_util import check_bf16_against
+    N, H = 256, 256
+    counts = [300, 77, 512]
+    rng = np.random.default_rng(33)
+    for e, n_tok in enumerate(counts):
+        Tp = (n_tok + 255) // 256 * 256
+        x = np.zeros((Tp, H), np.uint16)
+        dy = np.zeros((Tp, N), np.uint16)
+        x[:n_tok] = F.bf16_round(rng.standard_normal((n_tok, H)))
+        dy[:n_tok] = F.bf16_round(rng.standard_normal((n_tok, N)) * 1e-3)
+        seed = 100 + e
+        a_c, a_sf, a_g = cuda_lib.nvfp4_quantize_transposed(bf16_tensor(dy), cuda_lib.SCALE_PER_TENSOR,
+                                                            cuda_lib.ROUND_STOCHASTIC, seed=seed)
+        b_c, b_sf, b_g = cuda_lib.nvfp4_quantize_transposed(bf16_tensor(x), cuda_lib.SCALE_PER_TENSOR)
+        offs = dev(np.array([0, N], np.int32))
+        dw = cuda_lib.nvfp4_grouped_gemm(a_c, a_sf, a_g.expand(N).contiguous(), b_c, b_sf, b_g, offs,
+                                         dev(np.array([N], np.int32)), H, Tp, 1)
+        qa = Q.quantize(np.ascontiguousarray(dy.T), scope="tensor", rounding="sr", seed=seed)
+        qb = Q.quantize(np.ascontiguousarray(x.T), scope="tensor")
+        np.testing.assert_array_equal(npy(a_c), qa["packed"])
+        np.testing.assert_array_equal(npy(b_c), qb["packed"])
+        ref = M.grouped_gemm(qa["codes"], qa["sf"], np.full(N, qa["g"][0]), qb["codes"][None], qb["sf"][None],
+                             np.asarray(qb["g"], np.float64)[:1], np.array([0, N]), np.array([N]))
+        nbad, worst = check_bf16_against(u16(dw), ref)
+        assert nbad == 0, (e, worst)
