@@ -9,7 +9,7 @@ namespace nvfp4 {
 
 enum : int { kScopeTensor = 0, kScopeRow = 1, kScopeGroup = 2 };
 enum : int { kRoundRNE = 0, kRoundSR = 1 };
-enum : int { kMapIdentity = 0, kMapInterleave = 1, kMapScatter = 2 };
+enum : int { kMapIdentity = 0, kMapInterleave = 1 };
 
 struct QuantArgs {
   const __nv_bfloat16* x;  // input rows [rows, ld]
@@ -27,8 +27,6 @@ struct QuantArgs {
   int64_t rows_total;      // rows visited; rows..rows_total-1 only get zero scales
   int map;                 // kMap*
   int64_t map_I;           // interleave: intermediate size I
-  const int32_t* inv;      // scatter: output rows inv[row * k + j]
-  int k;
   uint64_t seed, rng_offset;
   int* status;
   int tiled_R;             // 0: row-major codes + 128x4 scales; 128 / 256: GEMM-tiled output

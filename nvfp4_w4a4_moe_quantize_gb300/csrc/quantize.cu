@@ -146,7 +146,7 @@ __device__ __forceinline__ int64_t interleave_row(int64_t r, int64_t I) {
 }
 
 // Encode one input row held in registers (lane l owns the 16-byte chunks at columns
-// 8l + 256i) and write its codes, scale words and global scale to every output row.
+// 8l + 256i) and write its codes, scale words and global scale to its output row.
 template <int RND, int MAXC>
 __device__ __forceinline__ void quantize_row(const QuantArgs& a, int64_t row, const uint4 (&q)[MAXC], int lane) {
   const int64_t data_words = (a.cols + 63) / 64;
@@ -172,10 +172,7 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, int64_t row, co
   }
   const float six_g = __fmul_rn(6.0f, g);
 
-  const int nout = a.map == kMapScatter ? a.k : 1;
-  const int64_t orow0 = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
-  int32_t my_slot = 0;
-  if (a.map == kMapScatter && lane < a.k) my_slot = a.inv[row * a.k + lane];
+  const int64_t orow = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
 
 #pragma unroll
   for (int i = 0; i < MAXC; ++i) {
@@ -200,26 +197,18 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, int64_t row, co
     const uint32_t s4 = __shfl_down_sync(kFull, sfb, 4);
     const uint32_t s6 = __shfl_down_sync(kFull, sfb, 6);
     const uint32_t sfw = sfb | (s2 << 8) | (s4 << 16) | (s6 << 24);
-    for (int j = 0; j < nout; ++j) {
-      const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
-      if (orow < 0) continue;   // entry whose expert id was rejected: no slot
-      if (active) *reinterpret_cast<uint32_t*>(a.codes + orow * a.codes_ld + col / 2) = word;
-      if ((lane & 7) == 0 && active)
-        *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, 4 * i + lane / 8, a.sf_words)) = sfw;
-    }
+    if (active) *reinterpret_cast<uint32_t*>(a.codes + orow * a.codes_ld + col / 2) = word;
+    if ((lane & 7) == 0 && active)
+      *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, 4 * i + lane / 8, a.sf_words)) = sfw;
   }
-  for (int j = 0; j < nout; ++j) {
-    const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
-    if (orow < 0) continue;
-    for (int64_t w = data_words + lane; w < a.sf_words; w += 32)
-      *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, w, a.sf_words)) = 0u;
-    for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
-      *reinterpret_cast<uint2*>(a.codes + orow * a.codes_ld + b) = make_uint2(0u, 0u);
-    if (lane == 0 && a.g_out != nullptr) {
-      if (a.mode == kScopeRow) a.g_out[a.map == kMapScatter ? orow : row] = g;
-      else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
-      else if (a.mode == kScopeGroup && row % a.group_rows == 0) a.g_out[row / a.group_rows] = g;
-    }
+  for (int64_t w = data_words + lane; w < a.sf_words; w += 32)
+    *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, w, a.sf_words)) = 0u;
+  for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
+    *reinterpret_cast<uint2*>(a.codes + orow * a.codes_ld + b) = make_uint2(0u, 0u);
+  if (lane == 0 && a.g_out != nullptr) {
+    if (a.mode == kScopeRow) a.g_out[row] = g;
+    else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
+    else if (a.mode == kScopeGroup && row % a.group_rows == 0) a.g_out[row / a.group_rows] = g;
   }
 }
 
@@ -396,7 +385,6 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
       }
     }
   }
-  const int nout = a.map == kMapScatter ? a.k : 1;
   uint32_t parity = 0;
   int s = 0;
   for (int64_t row = warp; row < nrows; row += nwarp) {
@@ -434,9 +422,7 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
       g = a.g_in ? a.g_in[gi] : __fdiv_rn(__uint_as_float(a.amax_bits[gi]), kGlobalDivisor);
     }
     const float six_g = __fmul_rn(6.0f, g);
-    const int64_t orow0 = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
-    int32_t my_slot = 0;
-    if (a.map == kMapScatter && lane < a.k) my_slot = a.inv[row * a.k + lane];
+    const int64_t orow = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
     for (int64_t b0 = 0; b0 < nblk; b0 += 32) {
       const int64_t blk = b0 + lane;
       const bool active = blk < nblk;
@@ -447,12 +433,8 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
       const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
       const uint32_t s3 = __shfl_down_sync(kFull, sfb, 3);
       const uint32_t sfw = sfb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-      for (int j = 0; j < nout; ++j) {
-        const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
-        if (orow < 0) continue;   // entry whose expert id was rejected: no slot
-        if (active) *reinterpret_cast<uint2*>(code_ptr(a, orow, blk * 8)) = cw;
-        if ((lane & 3) == 0 && active) *reinterpret_cast<uint32_t*>(sfw_ptr(a, orow, blk / 4)) = sfw;
-      }
+      if (active) *reinterpret_cast<uint2*>(code_ptr(a, orow, blk * 8)) = cw;
+      if ((lane & 3) == 0 && active) *reinterpret_cast<uint32_t*>(sfw_ptr(a, orow, blk / 4)) = sfw;
     }
     fence_proxy_async_smem();   // this row's reads of the buffer precede the next bulk write
     __syncwarp();
@@ -463,17 +445,13 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
         bulk_load(ring + s * stride, a.x + r2 * a.ld, row_bytes, &bars[s]);
       }
     }
-    for (int j = 0; j < nout; ++j) {
-      const int64_t orow = a.map == kMapScatter ? (int64_t)__shfl_sync(kFull, my_slot, j) : orow0;
-      if (orow < 0) continue;
-      for (int64_t w = data_words + lane; w < a.sf_words; w += 32) *reinterpret_cast<uint32_t*>(sfw_ptr(a, orow, w)) = 0u;
-      for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
-        *reinterpret_cast<uint2*>(code_ptr(a, orow, b)) = make_uint2(0u, 0u);
-      if (lane == 0 && a.g_out != nullptr) {
-        if (a.mode == kScopeRow) a.g_out[a.map == kMapScatter ? orow : row] = g;
-        else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
-        else if (a.mode == kScopeGroup && row % a.group_rows == 0) a.g_out[row / a.group_rows] = g;
-      }
+    for (int64_t w = data_words + lane; w < a.sf_words; w += 32) *reinterpret_cast<uint32_t*>(sfw_ptr(a, orow, w)) = 0u;
+    for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
+      *reinterpret_cast<uint2*>(code_ptr(a, orow, b)) = make_uint2(0u, 0u);
+    if (lane == 0 && a.g_out != nullptr) {
+      if (a.mode == kScopeRow) a.g_out[row] = g;
+      else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
+      else if (a.mode == kScopeGroup && row % a.group_rows == 0) a.g_out[row / a.group_rows] = g;
     }
     s = s + 1 == kQStages ? 0 : s + 1;
   }
