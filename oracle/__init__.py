@@ -25,6 +25,9 @@ Pages cited (by title and section):
   Need to Know Before Adopting NVFP4" -- §"What W4A4 GEMM Actually Changes" (both GEMM
   operands in FP4; expert GEMMs), §"The Cross-Engine Alignment Problem" (execution-level
   alignment: composition and accumulation order decide the result).
+* [4BL] §"Improving Gradient Stability", "Results Validation with MXFP8" -- the MXFP8
+  recipe the fix is first validated with (``mx.py``; the format itself is read from the
+  OCP Microscaling Formats v1.0 definition, which the pages name but do not restate).
 * [miniTE] "miniTE identifies and closes the execution gap in native NVFP4 reinforcement
   learning" -- §Development (NVFP4 kernels, scaling, grouped GEMMs).
 
@@ -36,4 +39,4 @@ fixed by the format definitions, closed forms, brute force or an independent
 high-precision library (see tests/test_oracle_*.py); none is "parity unpinned".
 """
 
-from . import formats, philox, quant, moe  # noqa: F401
+from . import formats, philox, quant, moe, mx  # noqa: F401
