@@ -202,6 +202,57 @@ nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const flo
                               int64_t cols, nvfp4_scale_mode mode, int64_t group_rows, void* out,
                               nvfp4_out_dtype out_dtype, int64_t ldo, void* stream);
 
+/* ---------------------------------------------------------------- MXFP8 */
+
+/* MXFP8, the format of the recipe's validation runs ("The 4-bitter Lesson...",
+ * §"Improving Gradient Stability", Results Validation with MXFP8: quantised forward and
+ * backward, and quantised forward with dequantised weights in the backward).  The pages
+ * name the format without defining it.  It is read as OCP MX v1.0 MXFP8:
+ *   - E4M3 elements, blocks of 32 values along a row;
+ *   - one E8M0 scale per block, b = max(floor(log2 amax_block) - 8 + 127, 0);
+ *   - code = E4M3_rn_satfinite(x * 2^(127 - b)), zero magnitudes encoded as +0;
+ *   - no global scale: DQ(x) = value(code) * 2^(b - 127).
+ * Storage:
+ *   codes:  uint8 [rows, cols], one E4M3 byte per element.
+ *   scales: E8M0 bytes in the same 128x4 tiled layout as the NVFP4 scales, with
+ *           C = cols/32 scale columns: byte ((r/128)*ceil(C/4) + c/4)*512 +
+ *           (r%32)*16 + ((r%128)/32)*4 + c%4; rows padded to a multiple of 128; size
+ *           mxfp8_sf_bytes(rows, cols). */
+size_t mxfp8_sf_bytes(int64_t rows, int64_t cols);
+
+/* MXFP8 quantisation of a BF16 matrix.
+ *   x:         device BF16 [rows, ld_elems]; the first `cols` of each row are used.
+ *   cols % 128 == 0 (else NVFP4_ERR_UNSUPPORTED); ld_elems >= cols, ld_elems % 8 == 0.
+ *   codes_out: device uint8 [rows, cols].
+ *   sf_out:    device uint8 [mxfp8_sf_bytes(rows, cols)], tiled layout; the scale words
+ *              of the padding rows are written as 0.
+ * x, codes_out and sf_out are 16-byte aligned.  No workspace; deterministic. */
+nvfp4_status mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_elems,
+                            uint8_t* codes_out, uint8_t* sf_out, void* stream);
+
+/* MXFP8 DQ: out[r, c] = value(code[r, c]) * 2^(sf[r, c/32] - 127).  The product is
+ * exact in float32.  For BF16 output it is rounded once, to nearest even.
+ *   codes: device [rows, cols]; sf: device, tiled as mxfp8_quantize writes it.
+ *   out:   device [rows, ldo] of out_dtype.  cols % 128 == 0, ldo >= cols, ldo % 8 == 0;
+ *   codes, sf and out 16-byte aligned.  No workspace. */
+nvfp4_status mxfp8_dequantize(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t cols,
+                              void* out, nvfp4_out_dtype out_dtype, int64_t ldo, void* stream);
+
+/* MXFP8 x MXFP8 grouped GEMM over ragged expert groups, on the tensor cores' block-scaled
+ * FP8 MMA.  For every expert e and every row r of its group:
+ *     D[r, n] = sum_k DQ(A)[r, k] * DQ(B_e)[n, k]
+ * This is accumulated in FP32 in a fixed order (no split-K), then rounded once to out_dtype.
+ *   A, SFA: device, codes [M_total, K], tiled scales for M_total rows.
+ *   B, SFB: device, codes [E, N, K], tiled scales for E*N rows.
+ *   group_offsets, group_rows, M_total, D, ldd: as nvfp4_grouped_gemm.
+ *   N % 128 == 0, K % 128 == 0, E <= 1024.  A, SFA, B, SFB and D are 16-byte aligned; the
+ *   group arrays 4-byte aligned.  No workspace. */
+nvfp4_status mxfp8_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
+                                const uint8_t* SFB, const int32_t* group_offsets,
+                                const int32_t* group_rows, int64_t M_total, int64_t N, int64_t K,
+                                int32_t E, void* D, nvfp4_out_dtype out_dtype, int64_t ldd,
+                                void* stream);
+
 /* ---------------------------------------------------------------- grouped GEMM */
 
 /* W4A4 grouped GEMM over ragged expert groups ("Low-Bit Precision Training Is Ready

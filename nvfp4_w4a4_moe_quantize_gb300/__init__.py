@@ -23,6 +23,7 @@ __all__ = [
     "moe_swiglu_quantize", "moe_prepare_weights", "moe_expert_forward", "moe_forward_workspace",
     "moe_forward_workspace_layout", "nvfp4_status_check", "nvfp4_sf_bytes", "NVFP4MoEWeights",
     "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled", "nvfp4_tiled_bytes",
+    "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_grouped_gemm", "mxfp8_sf_bytes",
     "SCALE_PER_TENSOR", "SCALE_PER_ROW", "SCALE_PER_GROUP", "ROUND_RNE", "ROUND_STOCHASTIC",
 ]
 
@@ -70,6 +71,11 @@ _SIGS = {
                                         _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                           _vp, ctypes.c_int, _i64, _vp]),
+    "mxfp8_sf_bytes": (_sz, [_i64, _i64]),
+    "mxfp8_quantize": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "mxfp8_dequantize": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, ctypes.c_int, _i64, _vp]),
+    "mxfp8_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, ctypes.c_int,
+                                          _i64, _vp]),
     "moe_route_topk": (ctypes.c_int, [_vp, _i64, _i32, _i32, ctypes.c_int, _vp, _vp, _vp]),
     "moe_permute": (ctypes.c_int, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _i64, _vp, _vp]),
@@ -252,6 +258,54 @@ def nvfp4_grouped_gemm(A, SFA, gA, B, SFB, gB, group_offsets, group_rows, N: int
     _check(lib.nvfp4_grouped_gemm(_p(A), _p(SFA), _p(gA), _p(B), _p(SFB), _p(gB), _p(group_offsets),
                                   _p(group_rows), M_total, N, K, E, _p(out), code, out.stride(0),
                                   _stream(stream)), "nvfp4_grouped_gemm")
+    return out
+
+
+# --------------------------------------------------------------------------- MXFP8
+
+def mxfp8_sf_bytes(rows: int, cols: int) -> int:
+    return int(load().mxfp8_sf_bytes(rows, cols))
+
+
+def mxfp8_quantize(x: torch.Tensor, codes: torch.Tensor | None = None, sf: torch.Tensor | None = None,
+                   stream=None):
+    """MXFP8 of a BF16 matrix [rows, cols] (cols % 128 == 0): E4M3 codes [rows, cols]
+    and E8M0 scales (one per 32 values, 128x4 tiled).  Returns (codes, sf)."""
+    lib = load()
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D BF16 tensor with unit column stride")
+    rows, cols = x.shape
+    if codes is None:
+        codes = torch.empty(rows, cols, dtype=torch.uint8, device=_dev(x))
+    if sf is None:
+        sf = torch.empty(max(mxfp8_sf_bytes(rows, cols), 1), dtype=torch.uint8, device=_dev(x))
+    _check(lib.mxfp8_quantize(_p(x), rows, cols, x.stride(0), _p(codes), _p(sf), _stream(stream)),
+           "mxfp8_quantize")
+    return codes, sf
+
+
+def mxfp8_dequantize(codes: torch.Tensor, sf: torch.Tensor, out_dtype=torch.bfloat16,
+                     out: torch.Tensor | None = None, stream=None):
+    """MXFP8 DQ: out[rows, cols] = value(code) * 2^(b - 127), rounded once to out_dtype."""
+    lib = load()
+    rows, cols = codes.shape
+    if out is None:
+        out = torch.empty(rows, cols, dtype=out_dtype, device=_dev(codes))
+    _check(lib.mxfp8_dequantize(_p(codes), _p(sf), rows, cols, _p(out), 1 if out.dtype == torch.float32 else 0,
+                                out.stride(0), _stream(stream)), "mxfp8_dequantize")
+    return out
+
+
+def mxfp8_grouped_gemm(A, SFA, B, SFB, group_offsets, group_rows, N: int, K: int, E: int,
+                       out_dtype=torch.bfloat16, out: torch.Tensor | None = None, stream=None):
+    """D[M_total, N] = grouped MXFP8 x MXFP8 GEMM (rows outside the groups are left unwritten)."""
+    lib = load()
+    M_total = A.shape[0]
+    if out is None:
+        out = torch.empty(M_total, N, dtype=out_dtype, device=_dev(A))
+    code = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.mxfp8_grouped_gemm(_p(A), _p(SFA), _p(B), _p(SFB), _p(group_offsets), _p(group_rows), M_total, N, K,
+                                  E, _p(out), code, out.stride(0), _stream(stream)), "mxfp8_grouped_gemm")
     return out
 
 

@@ -334,6 +334,73 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const floa
               out_dtype == NVFP4_OUT_F32, ldd, static_cast<cudaStream_t>(stream));
 }
 
+size_t mxfp8_sf_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return (size_t)((rows + 127) / 128) * (size_t)((cols + 127) / 128) * 512u;
+}
+
+nvfp4_status mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_elems, uint8_t* codes_out,
+                            uint8_t* sf_out, void* stream) {
+  if (rows < 0 || cols <= 0 || ld_elems < cols || ld_elems % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (cols % 128 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if (rows == 0) return NVFP4_OK;
+  if (!x || !codes_out || !sf_out || !aligned16(x) || !aligned16(codes_out) || !aligned16(sf_out))
+    return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_mx_quantize(x, rows, cols, ld_elems, codes_out, sf_out, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status mxfp8_dequantize(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t cols, void* out,
+                              nvfp4_out_dtype out_dtype, int64_t ldo, void* stream) {
+  if (rows < 0 || cols <= 0 || ldo < cols || ldo % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (cols % 128 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_INVALID_ARG;
+  if (rows == 0) return NVFP4_OK;
+  if (!codes || !sf || !out || !aligned16(codes) || !aligned16(sf) || !aligned16(out)) return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_mx_dequantize(codes, sf, rows, cols, out, out_dtype == NVFP4_OUT_F32, ldo,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status mxfp8_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                                const int32_t* group_offsets, const int32_t* group_rows, int64_t M_total, int64_t N,
+                                int64_t K, int32_t E, void* D, nvfp4_out_dtype out_dtype, int64_t ldd,
+                                void* stream) {
+  if (E <= 0 || E > 1024 || N <= 0 || K <= 0 || M_total < 0 || M_total % 128 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((int64_t)E * N >= (int64_t)1 << 31 || M_total >= (int64_t)1 << 31 || K >= (int64_t)1 << 20)
+    return NVFP4_ERR_UNSUPPORTED;
+  if (ldd < N || ldd % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_INVALID_ARG;
+  if (M_total == 0) return NVFP4_OK;
+  const void* ptrs[] = {A, SFA, B, SFB, D};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned4(group_offsets) || !aligned4(group_rows)) return NVFP4_ERR_INVALID_ARG;
+  const bool out_f32 = out_dtype == NVFP4_OUT_F32;
+  GemmArgs g{};
+  g.sfa = SFA;
+  g.sfb = SFB;
+  g.offsets = group_offsets;
+  g.rows = group_rows;
+  g.E = E;
+  g.N = (int32_t)N;
+  g.K = (int32_t)K;
+  g.d = D;
+  g.ldd = ldd;
+  g.out_f32 = out_f32;
+  g.status = device_status_ptr();
+  CUtensorMap ma, mb, md;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!make_map(&ma, A, M_total, K, K, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
+      !make_map(&mb, B, (int64_t)E * N, K, K, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1))
+    return NVFP4_ERR_CUDA;
+  // N % 256 == 0: clustered 128 x 256 tiles (weight tile shared by a CTA pair); else 128 x 128
+  if (n256_supported(g)) return from_cuda(launch_grouped_gemm_n256_mx(ma, mb, g, M_total / 128, s));
+  if (!make_map(&md, D, M_total, N, ldd * (out_f32 ? 4 : 2), 32,
+                out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_f32 ? 4 : 2))
+    return NVFP4_ERR_CUDA;
+  return from_cuda(launch_grouped_gemm_mx(ma, mb, md, g, M_total / 128, s));
+}
+
 nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A, const float* gA, const uint8_t* B, const float* gB,
                                       const int32_t* group_offsets, const int32_t* group_rows, int64_t M_total,
                                       int64_t N, int64_t K, int32_t E, void* D, nvfp4_out_dtype out_dtype,

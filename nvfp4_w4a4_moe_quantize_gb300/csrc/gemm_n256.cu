@@ -18,6 +18,12 @@
 // of TMEM), 4 stages of 54 KB, and 8 epilogue warps (two per TMEM lane quadrant, 128
 // columns each) that drain the accumulator into registers at once and release it before
 // converting and storing.  Rows outside the groups are never written.
+//
+// Instantiated with kMX, the same kernel runs the MXFP8 grouped GEMM (E4M3 operands,
+// E8M0 scales per 32 values, no global scales; see grouped_gemm.cu): a stage holds 128
+// K-values, one 512-byte scale tile per 128 rows, and four
+// kind::mxf8f6f4.block_scale.scale_vec::1X MMAs (K = 32) that pick byte j of the scale
+// words through their scale-factor ids.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,7 +46,6 @@ constexpr int kABytes = kBM * kBKBytes;      // 16 KB
 constexpr int kBBytes = kBN * kBKBytes;      // 32 KB
 constexpr int kSFABytes = 4 * 512;           // 4 k-groups x (128 rows x 4 scales)
 constexpr int kSFBBytes = 2 * 4 * 512;       // 2 row groups of 128
-constexpr uint32_t kStageTx = kABytes + kBBytes + kSFABytes + kSFBBytes;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = kBN;                // one accumulator: 128 lanes x 256 float32
 constexpr int kSFCol0 = kAccCols;
@@ -90,10 +95,16 @@ __device__ __forceinline__ PairTile pair_tile(const g256::Smem& sm, int E, int n
   return pt;
 }
 
+template <bool kMX>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
     grouped_gemm_n256_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                              const GemmArgs g) {
   using namespace g256;
+  constexpr int kStageK = kMX ? 128 : 256;            // K values per stage
+  constexpr int kSFA = kMX ? 512 : kSFABytes;         // A's scales per stage
+  constexpr int kSFB128 = kMX ? 512 : 2048;           // scales per stage of one 128-row half of B
+  constexpr uint32_t kTx = kABytes + kBBytes + kSFA + 2 * kSFB128;
+  constexpr int kSFTiles = kMX ? 1 : 4;               // 512-byte scale tiles per stage and 128 rows
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -103,7 +114,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
   for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
   for (int i = threadIdx.x; i < g.E; i += blockDim.x) {
     sm.rows[i] = g.rows[i];
-    sm.gb[i] = g.gb[i];
+    sm.gb[i] = kMX ? 1.0f : g.gb[i];
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -151,8 +162,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
 
   const int n_tiles = g.N / kBN;
   const int total = sm.pair_off[g.E] * n_tiles;
-  const int kblocks = g.K / (2 * kBKBytes);
-  const int64_t sf_kgroups = g.K / 64;
+  const int kblocks = g.K / kStageK;
+  const int64_t sf_kgroups = g.K / (kMX ? 128 : 64);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -163,14 +174,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
         const int32_t brow = pt.e * g.N + pt.n_tile * kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, g.status, abort)) goto producer_done;
-          mbar_arrive_expect_tx(&sm.full[stage], kStageTx);
+          mbar_arrive_expect_tx(&sm.full[stage], kTx);
           tma_load_2d(sm.a[stage], &tma, kb * kBKBytes, row0, &sm.full[stage]);
           tma_load_2d_mc(sm.b[stage] + rank * (kBBytes / 2), &tmb, kb * kBKBytes, brow + (int)rank * 128,
                          &sm.full[stage], kPair);
-          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)pt.a_tile * sf_kgroups + kb * 4) * 512, kSFABytes,
+          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)pt.a_tile * sf_kgroups + kb * kSFTiles) * 512, kSFA,
                     &sm.full[stage]);
-          bulk_load_mc(sm.sfb[stage] + rank * 2048,
-                       g.sfb + ((int64_t)(brow / 128 + (int)rank) * sf_kgroups + kb * 4) * 512, 2048,
+          bulk_load_mc(sm.sfb[stage] + rank * kSFB128,
+                       g.sfb + ((int64_t)(brow / 128 + (int)rank) * sf_kgroups + kb * kSFTiles) * 512, kSFB128,
                        &sm.full[stage], kPair);
           if (++stage == kStages) {
             stage = 0;
@@ -182,7 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
+      constexpr uint32_t idesc = kMX ? idesc_mxf8(kBM, kBN, 0) : idesc_nvf4(kBM, kBN);
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int u = cl; u < total; u += ncl, ++it) {
@@ -195,17 +206,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
           const uint32_t sfb_t = sfa_t + 16;
           const uint32_t sa = smem_u32(sm.a[stage]), sb = smem_u32(sm.b[stage]);
           const uint32_t ssfa = smem_u32(sm.sfa[stage]), ssfb = smem_u32(sm.sfb[stage]);
+          if constexpr (kMX) {
+            tc_cp_32x128b_warpx4(sfa_t, smem_desc(ssfa, 0, 128, 0));
+            tc_cp_32x128b_warpx4(sfb_t, smem_desc(ssfb, 0, 128, 0));
+            tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(ssfb + 512, 0, 128, 0));
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
-            tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
-            tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
-          }
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
+              const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
+              tc_mma_mxf8(tmem, adesc, bdesc, idesc_mxf8(kBM, kBN, (uint32_t)j), sfa_t, sfb_t,
+                          (kb | j) != 0 ? 1u : 0u);
+            }
+          } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
-            tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+            for (int j = 0; j < 4; ++j) {
+              tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
+              tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
+              tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
+              const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
+              tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+            }
           }
           tc_commit_mc(&sm.empty[stage], kPair);
           if (++stage == kStages) {
@@ -229,7 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
       const int32_t in_group = sm.rows[e] - pt.local * kBM;   // <= 0 for a duplicate tile
       const bool valid = q * 32 + lane < in_group;
       const int64_t row = (int64_t)sm.offsets[e] + pt.local * kBM + q * 32 + lane;
-      const float ga = valid ? g.ga[row] : 0.0f;
+      const float ga = kMX ? 1.0f : (valid ? g.ga[row] : 0.0f);
       if (!mbar_wait(&sm.accf, it & 1, g.status, abort)) break;
       tc_fence_after();
       const float scale = __fmul_rn(ga, sm.gb[e]);
@@ -280,13 +304,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
 
 bool n256_supported(const GemmArgs& g) { return g.N % g256::kBN == 0 && g.E <= g256::kMaxE; }
 
-cudaError_t launch_grouped_gemm_n256(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
-                                     int64_t max_m_tiles, cudaStream_t s) {
+template <bool kMX>
+static cudaError_t launch_n256(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
+                               int64_t max_m_tiles, cudaStream_t s) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_n256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_n256_kernel<kMX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)g256::kSmemBytes);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -296,8 +321,18 @@ cudaError_t launch_grouped_gemm_n256(const CUtensorMap& tma, const CUtensorMap& 
   int64_t clusters = num_sms() / 2;
   if (units < clusters) clusters = units;
   const int grid = (int)(2 * clusters);
-  grouped_gemm_n256_kernel<<<grid, g256::kThreads, g256::kSmemBytes, s>>>(tma, tmb, g);
+  grouped_gemm_n256_kernel<kMX><<<grid, g256::kThreads, g256::kSmemBytes, s>>>(tma, tmb, g);
   return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm_n256(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
+                                     int64_t max_m_tiles, cudaStream_t s) {
+  return launch_n256<false>(tma, tmb, g, max_m_tiles, s);
+}
+
+cudaError_t launch_grouped_gemm_n256_mx(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
+                                        int64_t max_m_tiles, cudaStream_t s) {
+  return launch_n256<true>(tma, tmb, g, max_m_tiles, s);
 }
 
 }  // namespace nvfp4

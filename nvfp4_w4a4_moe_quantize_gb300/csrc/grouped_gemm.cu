@@ -22,6 +22,15 @@
 // is row block t / (N/128), column block t % (N/128), so CTAs running at the same time
 // share A tiles and one expert's weights in L2.  The K loop has a fixed order and no
 // split, so every output element has one accumulation order whatever the batch.
+//
+// The same kernel, instantiated with kMX, is the MXFP8 grouped GEMM of the recipe's
+// validation format ("The 4-bitter Lesson...", §"Improving Gradient Stability", Results
+// Validation with MXFP8): E4M3 operands with one E8M0 scale per 32 values of K, no global
+// scales.  A stage is then 128 K-values (one 128-byte swizzle row of 8-bit codes).  The
+// stage's scales are one 512-byte tile of the 128x4 layout per 128 rows, copied into TMEM
+// with one tcgen05.cp.  Four tcgen05.mma.kind::mxf8f6f4.block_scale.scale_vec::1X
+// (K = 32 each) follow; MMA j reads byte j of each 32-bit scale word through the
+// scale-factor ids of its instruction descriptor.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,7 +50,6 @@ constexpr int kABytes = kBM * kBKBytes;
 constexpr int kBBytes = kBN * kBKBytes;
 constexpr int kSFABytes = 4 * 512;           // 4 k-groups of 64 x 128 rows
 constexpr int kSFBBytes = (kBN / 128) * 4 * 512;
-constexpr uint32_t kStageTx = kABytes + kBBytes + kSFABytes + kSFBBytes;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = kBN;                // one accumulator: 128 lanes x kBN float32
 constexpr int kSFCol0 = 2 * kAccCols;        // scale factors after the two accumulators
@@ -72,10 +80,16 @@ static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 }  // namespace gg
 
+template <bool kMX>
 __global__ void __launch_bounds__(gg::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                         const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
   using namespace gg;
+  // per stage: K values, bytes of A's scales, bytes of one 128-row block of B's scales
+  constexpr int kStageK = kMX ? 128 : 256;
+  constexpr int kSFA = kMX ? 512 : kSFABytes;
+  constexpr int kSFB128 = kMX ? 512 : 2048;
+  constexpr uint32_t kTx = kABytes + kBBytes + kSFA + (kBN / 128) * kSFB128;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,7 +97,7 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
   for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
   for (int i = threadIdx.x; i < g.E; i += blockDim.x) {
     sm.rows[i] = g.rows[i];
-    sm.gb[i] = g.gb[i];
+    sm.gb[i] = kMX ? 1.0f : g.gb[i];
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -115,8 +129,9 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
   const int n_tiles = g.N / kBN;
   const int m_tiles = sm.offsets[g.E] / kBM;
   const int total = m_tiles * n_tiles;
-  const int kblocks = g.K / (2 * kBKBytes);
-  const int64_t sf_kgroups = g.K / 64;   // 512-byte scale blocks per 128-row block
+  const int kblocks = g.K / kStageK;
+  const int64_t sf_kgroups = g.K / (kMX ? 128 : 64);   // 512-byte scale tiles per 128-row block
+  constexpr int kSFTiles = kMX ? 1 : 4;                 // scale tiles per stage and 128 rows
 
   if (warp == 0) {
     if (lane == 0) {
@@ -128,15 +143,16 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
         const int32_t brow = e * g.N + n_tile * kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, g.status, abort)) goto producer_done;
-          mbar_arrive_expect_tx(&sm.full[stage], kStageTx);
+          mbar_arrive_expect_tx(&sm.full[stage], kTx);
           tma_load_2d(sm.a[stage], &tma, kb * kBKBytes, row0, &sm.full[stage]);
           tma_load_2d(sm.b[stage], &tmb, kb * kBKBytes, brow, &sm.full[stage]);
-          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)m_tile * sf_kgroups + kb * 4) * 512, kSFABytes,
+          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)m_tile * sf_kgroups + kb * kSFTiles) * 512, kSFA,
                     &sm.full[stage]);
 #pragma unroll
           for (int h = 0; h < kBN / 128; ++h)
-            bulk_load(sm.sfb[stage] + h * 2048, g.sfb + ((int64_t)(brow / 128 + h) * sf_kgroups + kb * 4) * 512,
-                      2048, &sm.full[stage]);
+            bulk_load(sm.sfb[stage] + h * kSFB128,
+                      g.sfb + ((int64_t)(brow / 128 + h) * sf_kgroups + kb * kSFTiles) * 512, kSFB128,
+                      &sm.full[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -147,7 +163,7 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
+      constexpr uint32_t idesc = kMX ? idesc_mxf8(kBM, kBN, 0) : idesc_nvf4(kBM, kBN);
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -162,19 +178,33 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
           const uint32_t sfb_t = sfa_t + 16;
           const uint32_t sa = smem_u32(sm.a[stage]), sb = smem_u32(sm.b[stage]);
           const uint32_t ssfa = smem_u32(sm.sfa[stage]), ssfb = smem_u32(sm.sfb[stage]);
+          if constexpr (kMX) {
+            tc_cp_32x128b_warpx4(sfa_t, smem_desc(ssfa, 0, 128, 0));
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
+            for (int h = 0; h < kBN / 128; ++h) tc_cp_32x128b_warpx4(sfb_t + 4 * h, smem_desc(ssfb + 512 * h, 0, 128, 0));
 #pragma unroll
-            for (int h = 0; h < kBN / 128; ++h)
-              tc_cp_32x128b_warpx4(sfb_t + 4 * (kBN / 128) * j + 4 * h, smem_desc(ssfb + 2048 * h + 512 * j, 0, 128, 0));
-          }
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
+              const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
+              tc_mma_mxf8(d_tmem, adesc, bdesc, idesc_mxf8(kBM, kBN, (uint32_t)j), sfa_t, sfb_t,
+                          (kb | j) != 0 ? 1u : 0u);
+            }
+          } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
-            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * (kBN / 128) * j,
-                        (kb | j) != 0 ? 1u : 0u);
+            for (int j = 0; j < 4; ++j) {
+              tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
+#pragma unroll
+              for (int h = 0; h < kBN / 128; ++h)
+                tc_cp_32x128b_warpx4(sfb_t + 4 * (kBN / 128) * j + 4 * h,
+                                     smem_desc(ssfb + 2048 * h + 512 * j, 0, 128, 0));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
+              const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
+              tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * (kBN / 128) * j,
+                          (kb | j) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&sm.empty[stage]);
           if (++stage == kStages) {
@@ -206,7 +236,7 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
       const bool valid = q * 32 + lane < in_group;
       const bool full_warp = q * 32 + 32 <= in_group;
       const int64_t row = (int64_t)row0 + q * 32 + lane;
-      const float ga = valid ? g.ga[row] : 0.0f;                        // load before the wait
+      const float ga = kMX ? 1.0f : (valid ? g.ga[row] : 0.0f);         // load before the wait
       if (!mbar_wait(&sm.accf[acc], acc_phase, g.status, abort)) break;
       tc_fence_after();
       const float scale = __fmul_rn(ga, sm.gb[e]);
@@ -281,13 +311,14 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
-                                const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
+template <bool kMX>
+static cudaError_t launch_gg(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
+                             const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
   static bool attr_set[64] = {};   // the attribute is set once per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kMX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)gg::kSmemBytes);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -296,8 +327,18 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, 
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
-  grouped_gemm_kernel<<<grid, gg::kThreads, gg::kSmemBytes, s>>>(tma, tmb, tmd, g);
+  grouped_gemm_kernel<kMX><<<grid, gg::kThreads, gg::kSmemBytes, s>>>(tma, tmb, tmd, g);
   return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
+                                const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
+  return launch_gg<false>(tma, tmb, tmd, g, max_m_tiles, s);
+}
+
+cudaError_t launch_grouped_gemm_mx(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
+                                   const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
+  return launch_gg<true>(tma, tmb, tmd, g, max_m_tiles, s);
 }
 
 }  // namespace nvfp4

@@ -73,8 +73,22 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
 bool n256_supported(const GemmArgs& g);
 cudaError_t launch_grouped_gemm_n256(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
                                      int64_t max_m_tiles, cudaStream_t s);
+// MXFP8 operands on the clustered 128 x 256 tile kernel (N % 256 == 0, E <= 512).
+cudaError_t launch_grouped_gemm_n256_mx(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
+                                        int64_t max_m_tiles, cudaStream_t s);
 cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
                                 const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s);
+// The same 128 x 128 tile kernel over MXFP8 operands (E4M3 codes [rows, K] bytes, E8M0
+// scales per 32 values in the 128x4 tiled layout; g.ga / g.gb unused).  K % 128 == 0.
+cudaError_t launch_grouped_gemm_mx(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
+                                   const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s);
+// MXFP8 quantiser: x BF16 [rows, ld] -> E4M3 codes [rows, cols] + E8M0 scales, 128x4 tiled
+// for rows padded to 128 (padding words 0).  cols % 128 == 0.
+cudaError_t launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes, uint8_t* sf,
+                               cudaStream_t s);
+// MXFP8 DQ into BF16 or float32 rows of pitch ldo.  cols % 128 == 0.
+cudaError_t launch_mx_dequantize(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t cols, void* out,
+                                 bool out_f32, int64_t ldo, cudaStream_t s);
 
 // GEMM over GEMM-tiled operands (tiled.cuh): N % 256 == 0, K % 256 == 0, E <= 512.
 // swiglu: the gate/up epilogue writes h = BF16(silu(gate) * up) to g.h instead of D.

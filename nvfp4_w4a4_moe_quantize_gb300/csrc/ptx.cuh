@@ -232,6 +232,26 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
   return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// D(tmem) (+)= A(smem) * B(smem)^T with MX block scaling: E4M3 operands, one UE8M0 scale
+// per 32 elements of K (scale_vec::1X), scales read from TMEM.  K = 32 per op.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Instruction descriptor for kind::mxf8f6f4: A and B E4M3 (format 0) K-major, UE8M0
+// scales (bit 23 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.  With one scale byte
+// per row and op, sf_id (0..3) picks the byte of each 32-bit scale word, for A (bits
+// 29-30) and B (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t sf_id) {
+  return ((sf_id & 3u) << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | ((sf_id & 3u) << 29);
+}
+
 // 32 lanes x 32 columns of 32-bit TMEM words: thread i of the warp gets row (lane base
 // + i), columns [col, col+32).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
