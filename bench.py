@@ -157,6 +157,12 @@ def time_launches(fn, iters, flush, stream):
     return float(np.mean(ts)), float(np.median(ts))
 
 
+def time_launches_median(fn, iters, flush, stream):
+    """Median device time (ms) of fn() over iters launches, L2 flushed before each: the
+    per-kernel figures (standalone quantisers, grouped GEMMs) are medians."""
+    return time_launches(fn, iters, flush, stream)[1]
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The slowest rank's value (replicas run side by side; the job takes as long as its
     slowest rank).  One all-reduce on the process group's device (NCCL on GPUs, gloo on CPU)."""
@@ -308,12 +314,13 @@ def run_ours(args, rank, world, local_rank):
     g_aq, g_ga = gws[glay[5]:glay[7]], gview(7, gm, torch.float32)
     g_cnt, g_pad = gview(0, E, torch.int32), gview(2, E + 1, torch.int32)
     g_d = torch.empty(gm, 2 * I, dtype=torch.bfloat16, device=dev)
-    gt, _ = time_launches(lambda: L.nvfp4_grouped_gemm_tiled(g_aq, g_ga, pw.w13, pw.w13_g, g_pad, g_cnt, gm, 2 * I,
+    gt = time_launches_median(lambda: L.nvfp4_grouped_gemm_tiled(g_aq, g_ga, pw.w13, pw.w13_g, g_pad, g_cnt, gm, 2 * I,
                                                              H, E, out=g_d), iters, flush, stream)
     gflops = 2.0 * gshape.T * k * 2 * I * H
     gemm_tflops = gflops / (gt * 1e-3) / 1e12
     tiles = int(g_pad[-1].item()) // 128
-    grouped = {"workload": "gate/up grouped GEMM, T=8192 top-8 of 128 experts (65,536 routed rows, Zipf 1.1), "
+    grouped = {"timing": f"median of {iters} launches, L2 flushed before each",
+               "workload": "gate/up grouped GEMM, T=8192 top-8 of 128 experts (65,536 routed rows, Zipf 1.1), "
                            "K=2048, N=1536, BF16 out", "ms": round(gt, 4), "tflops": round(gemm_tflops, 1),
                "frac_of_9pf": round(gemm_tflops / PF_TARGET, 4), "frac_of_13_5pf": round(gemm_tflops / PF_B300, 4),
                "frac_of_fp4_peak_from_measured_bf16": round(gemm_tflops / fp4_peak, 4), "row_tiles": tiles}
@@ -327,15 +334,16 @@ def run_ours(args, rank, world, local_rank):
     qg = torch.empty(1, dtype=torch.float32, device=dev)
     qws = torch.empty(4096, dtype=torch.uint8, device=dev)
     qbytes = qrows * qcols * 2 + qrows * qcols // 2 + L.nvfp4_sf_bytes(qrows, qcols)
-    quant = {"workload": "standalone quantiser 16384x2048 BF16, 1% outlier channels x50, per-tensor scale",
+    quant = {"timing": f"median of {iters} launches, L2 flushed before each",
+             "workload": "standalone quantiser 16384x2048 BF16, 1% outlier channels x50, per-tensor scale",
              "algorithmic_bytes": qbytes, "bytes_note": "one read of x + codes + scales (the amax pass re-reads x)"}
     for rnd, name in ((L.ROUND_RNE, "rne"), (L.ROUND_STOCHASTIC, "sr")):
-        qt, _ = time_launches(lambda: L.nvfp4_quantize(qx, L.SCALE_PER_TENSOR, rnd, 0, 0, out=(qcodes, qsf, qg),
+        qt = time_launches_median(lambda: L.nvfp4_quantize(qx, L.SCALE_PER_TENSOR, rnd, 0, 0, out=(qcodes, qsf, qg),
                                                        workspace=qws), iters, flush, stream)
         quant[f"{name}_us"] = round(qt * 1e3, 2)
         quant[f"{name}_gbs"] = round(qbytes / (qt * 1e-3) / 1e9, 1)
         quant[f"{name}_frac_hbm"] = round(qbytes / (qt * 1e-3) / 1e9 / hbm_peak, 4)
-    qt_row, _ = time_launches(lambda: L.nvfp4_quantize(qx, L.SCALE_PER_ROW, L.ROUND_RNE, 0, 0, out=(qcodes, qsf,
+    qt_row = time_launches_median(lambda: L.nvfp4_quantize(qx, L.SCALE_PER_ROW, L.ROUND_RNE, 0, 0, out=(qcodes, qsf,
                               torch.empty(qrows, dtype=torch.float32, device=dev)), workspace=qws), iters, flush, stream)
     quant["per_row_rne_gbs"] = round(qbytes / (qt_row * 1e-3) / 1e9, 1)
     quant["per_row_rne_frac_hbm"] = round(qbytes / (qt_row * 1e-3) / 1e9 / hbm_peak, 4)
@@ -348,18 +356,19 @@ def run_ours(args, rank, world, local_rank):
     mcodes = torch.empty(qrows, qcols, dtype=torch.uint8, device=dev)
     msf = torch.empty(L.mxfp8_sf_bytes(qrows, qcols), dtype=torch.uint8, device=dev)
     mbytes = qrows * qcols * 2 + qrows * qcols + L.mxfp8_sf_bytes(qrows, qcols)
-    mq, _ = time_launches(lambda: L.mxfp8_quantize(qx, mcodes, msf), iters, flush, stream)
+    mq = time_launches_median(lambda: L.mxfp8_quantize(qx, mcodes, msf), iters, flush, stream)
     mdq_out = torch.empty(qrows, qcols, dtype=torch.bfloat16, device=dev)
-    mdq, _ = time_launches(lambda: L.mxfp8_dequantize(mcodes, msf, out=mdq_out), iters, flush, stream)
+    mdq = time_launches_median(lambda: L.mxfp8_dequantize(mcodes, msf, out=mdq_out), iters, flush, stream)
     ma_bf16 = S.randn_bf16((gm, H), 1.0, 3).to(dev)
     ma, msfa = L.mxfp8_quantize(ma_bf16)
     mb, msfb = L.mxfp8_quantize(w13_h.to(dev).reshape(E * 2 * I, H))
     mg_d = torch.empty(gm, 2 * I, dtype=torch.bfloat16, device=dev)
-    mgt, _ = time_launches(lambda: L.mxfp8_grouped_gemm(ma, msfa, mb, msfb, g_pad, g_cnt, 2 * I, H, E, out=mg_d),
+    mgt = time_launches_median(lambda: L.mxfp8_grouped_gemm(ma, msfa, mb, msfb, g_pad, g_cnt, 2 * I, H, E, out=mg_d),
                            iters, flush, stream)
     fp8_peak = float(peaks.get("bf16_tflops", 1900.0)) * 2.0      # nominal FP8 : BF16 ratio 2
     mx_tflops = gflops / (mgt * 1e-3) / 1e12
-    mxfp8 = {"quantiser": {"workload": "16384x2048 BF16 (the standalone quantiser's matrix)",
+    mxfp8 = {"timing": f"median of {iters} launches, L2 flushed before each",
+             "quantiser": {"workload": "16384x2048 BF16 (the standalone quantiser's matrix)",
                            "algorithmic_bytes": mbytes, "us": round(mq * 1e3, 2),
                            "gbs": round(mbytes / (mq * 1e-3) / 1e9, 1),
                            "frac_hbm": round(mbytes / (mq * 1e-3) / 1e9 / hbm_peak, 4)},

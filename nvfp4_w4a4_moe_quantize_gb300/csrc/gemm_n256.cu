@@ -197,8 +197,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int u = cl; u < total; u += ncl, ++it) {
-        if (!mbar_wait(&sm.acce, (it & 1) ^ 1u, g.status, abort)) break;   // accumulator drained
-        tc_fence_after();
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&sm.full[stage], phase, g.status, abort)) goto mma_done;
           tc_fence_after();
@@ -206,10 +204,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
           const uint32_t sfb_t = sfa_t + 16;
           const uint32_t sa = smem_u32(sm.a[stage]), sb = smem_u32(sm.b[stage]);
           const uint32_t ssfa = smem_u32(sm.sfa[stage]), ssfb = smem_u32(sm.sfb[stage]);
+          // The first stage's scale copies go out before the accumulator wait: they do not
+          // touch the accumulator, and tcgen05 ops of one thread execute in issue order.
+          const bool first = kb == 0;
           if constexpr (kMX) {
             tc_cp_32x128b_warpx4(sfa_t, smem_desc(ssfa, 0, 128, 0));
             tc_cp_32x128b_warpx4(sfb_t, smem_desc(ssfb, 0, 128, 0));
             tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(ssfb + 512, 0, 128, 0));
+            if (first) {
+              if (!mbar_wait(&sm.acce, (it & 1) ^ 1u, g.status, abort)) goto mma_done;   // accumulator drained
+              tc_fence_after();
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
@@ -223,6 +228,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
               tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
               tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
               tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
+            }
+            if (first) {
+              if (!mbar_wait(&sm.acce, (it & 1) ^ 1u, g.status, abort)) goto mma_done;   // accumulator drained
+              tc_fence_after();
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {

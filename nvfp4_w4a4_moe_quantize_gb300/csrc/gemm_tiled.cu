@@ -174,8 +174,6 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-        if (!mbar_wait(&sm.acce, (it & 1) ^ 1u, g.status, abort)) break;   // accumulator drained
-        tc_fence_after();
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&sm.full[stage], phase, g.status, abort)) goto mma_done;
           tc_fence_after();
@@ -188,6 +186,13 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
             tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
             tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
             tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
+          }
+          if (kb == 0) {
+            // The first stage's scale copies are issued before this wait: they do not touch
+            // the accumulator, so the tensor pipe runs them while the epilogue drains the
+            // previous tile (tcgen05 ops of one thread execute in issue order).
+            if (!mbar_wait(&sm.acce, (it & 1) ^ 1u, g.status, abort)) goto mma_done;
+            tc_fence_after();
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
