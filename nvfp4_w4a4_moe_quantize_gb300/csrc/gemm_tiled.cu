@@ -305,11 +305,13 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
         uint32_t w[16];
 #pragma unroll
         for (int p = 0; p < 16; ++p) {
-          uint32_t hb[2];
+          float hf[2];
 #pragma unroll
           for (int s2 = 0; s2 < 2; ++s2) {
             const uint32_t x2 = gu[2 * p + s2];
-            if (!swiglu_fast(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u), hb[s2]) && valid) {
+            bool ok;
+            hf[s2] = swiglu_fast_f32(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u), ok);
+            if (!ok && valid) {
               if (d_n == 0) d_x2a = x2;
               else if (d_n == 1) d_x2b = x2;
               else d_ovf[d_n - 2] = x2;
@@ -317,7 +319,8 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
               d_mask |= 1u << (2 * p + s2);
             }
           }
-          w[p] = hb[0] | (hb[1] << 16);
+          const __nv_bfloat162 hp = __floats2bfloat162_rn(hf[0], hf[1]);
+          w[p] = *reinterpret_cast<const uint32_t*>(&hp);
         }
         if (full_warp) {
           // 32 rows x 64 bytes, 64-byte swizzled (16-byte chunk j of row r at
@@ -344,12 +347,20 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
           // max |h| of the row's 32 values as BF16 magnitude bits (integers order like
           // the magnitudes; NaN patterns are ignored, as a float max would)
           // (deferred values join the max when they are settled)
-          uint32_t hmax = 0;
+          uint32_t m2 = 0;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t lo = (d_mask >> (2 * j)) & 1u ? 0u : w[j] & 0x7FFFu;
-            const uint32_t hi = (d_mask >> (2 * j + 1)) & 1u ? 0u : (w[j] >> 16) & 0x7FFFu;
-            hmax = max(hmax, max(lo <= 0x7F80u ? lo : 0u, hi <= 0x7F80u ? hi : 0u));
+          for (int j = 0; j < 16; ++j) m2 = __vmaxu2(m2, w[j] & 0x7FFF7FFFu);   // both halves at once
+          uint32_t hmax = max(m2 & 0xFFFFu, m2 >> 16);
+          if (d_mask != 0u || hmax > 0x7F80u) {
+            // values still to be settled (they join when they are) or NaN patterns: the
+            // element-wise max without them
+            hmax = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t lo = (d_mask >> (2 * j)) & 1u ? 0u : w[j] & 0x7FFFu;
+              const uint32_t hi = (d_mask >> (2 * j + 1)) & 1u ? 0u : (w[j] >> 16) & 0x7FFFu;
+              hmax = max(hmax, max(lo <= 0x7F80u ? lo : 0u, hi <= 0x7F80u ? hi : 0u));
+            }
           }
           if (hmax != 0u) atomicMax(g.h_amax + row, hmax << 16);
         }

@@ -166,6 +166,19 @@ __device__ __forceinline__ bool swiglu_fast(float g, float u, uint32_t& out) {
   return exact_zero | (in_range & !near_mid);
 }
 
+// The same fast path returning the float32 h (the caller rounds pairs to BF16 with one
+// conversion instruction, which is the same round-to-nearest-even for finite h).
+__device__ __forceinline__ float swiglu_fast_f32(float g, float u, bool& ok) {
+  const float e = expf(-g);
+  const float h = __fmul_rn(__fmul_rn(g, rcp_approx(__fadd_rn(1.0f, e))), u);
+  const uint32_t b = __float_as_uint(h);
+  const bool exact_zero = (g == 0.0f) | (u == 0.0f);
+  const bool in_range = ((b >> 23) & 0xFFu) - 27u <= 200u;          // 2^-100 <= |h| < 2^101
+  const bool near_mid = (b & 0xFFFFu) - (0x8000u - 16u) <= 32u;     // within 16 ulps
+  ok = exact_zero | (in_range & !near_mid);
+  return h;
+}
+
 // The exact path for the values the fast path hands over, inlined at one warp-uniform
 // site by its callers (a rarely taken call inside an unrolled epilogue loop cost far more
 // than the work it did).  g must be a BF16 value; tab is the silu table.
