@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "ptx.cuh"
 #include "tiled.cuh"
 
 namespace nvfp4 {
@@ -36,54 +37,67 @@ __global__ void __launch_bounds__(256) pack_tiled_kernel(const uint8_t* __restri
 // Gather of routed rows in the GEMM-tiled layout (128-row blocks): slot r of the
 // expert-grouped order receives token perm[r]'s row of the per-token operand `src` --
 // its codes and scales of every 256-K block -- and its global scale.  Slots with
-// perm[r] < 0 (group padding) are not written.  One warp per (128-row block, K block)
-// chunk of the output: 8 lanes move a row's 128 code bytes (re-swizzled for the
-// destination row, four rows per instruction), then the chunk's 512 scale words.  The
-// per-token operand is small next to L2, so the k-fold reads hit there; the writes go out
-// as whole lines with the streaming (evict-first) store hint, so that they do not push
-// the per-token operand out of L2.
-__global__ void __launch_bounds__(256, 4) gather_tiled_kernel(const uint8_t* __restrict__ src,
-                                                           const float* __restrict__ src_g,
-                                                           const int32_t* __restrict__ perm,
-                                                           const int32_t* __restrict__ n_rows_dev, int64_t max_rows,
-                                                           int64_t kblocks, uint8_t* __restrict__ dst,
-                                                           float* __restrict__ dst_g,
-                                                           uint32_t* __restrict__ amax_zero) {
+// perm[r] < 0 (group padding) get zero codes and scales.  One warp per (128-row block,
+// K block) chunk of the output, assembled in shared memory: asynchronous 16-byte copies
+// move each row's 128 code bytes (8 lanes per row, re-swizzled for the destination row)
+// and 4-byte copies the chunk's 512 scale words, then one bulk store writes the 18 KB
+// image as whole lines.  The per-token operand is small next to L2, so the k-fold reads
+// hit there, and with no register staging each lane keeps its 48 copies in flight.
+__global__ void __launch_bounds__(32) gather_tiled_kernel(const uint8_t* __restrict__ src,
+                                                          const float* __restrict__ src_g,
+                                                          const int32_t* __restrict__ perm,
+                                                          const int32_t* __restrict__ n_rows_dev, int64_t max_rows,
+                                                          int64_t kblocks, uint8_t* __restrict__ dst,
+                                                          float* __restrict__ dst_g,
+                                                          uint32_t* __restrict__ amax_zero) {
   constexpr int R = 128;
   constexpr int64_t kChunk = R * 144;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  extern __shared__ __align__(128) uint8_t gsm[];
+  const int lane = threadIdx.x;
+  const uint32_t sb = smem_u32(gsm);
   int64_t rows = *n_rows_dev;
   if (rows > max_rows) rows = max_rows;
   const int64_t chunks = rows / R * kblocks;
-  for (int64_t c = warp; c < chunks; c += nwarp) {
+  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
     const int64_t b = c / kblocks, kb = c - (c / kblocks) * kblocks;
     int32_t pr[4];   // tokens of rows lane + 32 i of this block
 #pragma unroll
     for (int i = 0; i < 4; ++i) pr[i] = perm[b * R + lane + 32 * i];
-    uint8_t* dchunk = dst + (b * kblocks + kb) * kChunk;
+    if (lane == 0) bulk_wait_read<0>();   // the previous chunk's store has read the buffer
+    __syncwarp();
+    // codes: row rr's 16-byte chunk j, re-swizzled for the destination row
 #pragma unroll
     for (int p = 0; p < 32; ++p) {
       const int rr = 4 * p + (lane >> 3), j = lane & 7;
       const int32_t t = __shfl_sync(0xFFFFFFFFu, pr[p >> 3], rr & 31);
+      const uint32_t d = sb + rr * 128 + ((j ^ (rr & 7)) << 4);
       if (t >= 0) {
         const int ts = t & (R - 1);
-        const uint8_t* schunk = src + ((int64_t)(t / R) * kblocks + kb) * kChunk;
-        const uint4 v = *reinterpret_cast<const uint4*>(schunk + ts * 128 + ((j ^ (ts & 7)) << 4));
-        __stcs(reinterpret_cast<uint4*>(dchunk + rr * 128 + ((j ^ (rr & 7)) << 4)), v);
+        cp_async_16(d, src + ((int64_t)(t / R) * kblocks + kb) * kChunk + ts * 128 + ((j ^ (ts & 7)) << 4));
+      } else {
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
       }
     }
+    // scales: the chunk's 512 words, each moved to the destination row's position
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
       const int wi = 32 * p + lane, rr = wi >> 2, q = wi & 3;
       const int32_t t = __shfl_sync(0xFFFFFFFFu, pr[p >> 2], rr & 31);
+      const uint32_t d = sb + R * 128 + q * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
       if (t >= 0) {
         const int ts = t & (R - 1);
-        const uint8_t* schunk = src + ((int64_t)(t / R) * kblocks + kb) * kChunk;
-        __stcs(reinterpret_cast<unsigned int*>(dchunk + R * 128 + q * 512 + (rr & 31) * 16 + (rr >> 5) * 4),
-               *reinterpret_cast<const unsigned int*>(schunk + R * 128 + q * 512 + (ts & 31) * 16 + (ts >> 5) * 4));
+        cp_async_4(d, src + ((int64_t)(t / R) * kblocks + kb) * kChunk + R * 128 + q * 512 + (ts & 31) * 16 +
+                          (ts >> 5) * 4);
+      } else {
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(d), "r"(0u) : "memory");
       }
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      bulk_store(dst + (b * kblocks + kb) * kChunk, gsm, (uint32_t)kChunk);
+      bulk_commit();
     }
     if (kb == 0) {
 #pragma unroll
@@ -93,17 +107,29 @@ __global__ void __launch_bounds__(256, 4) gather_tiled_kernel(const uint8_t* __r
       }
     }
   }
+  if (lane == 0) bulk_wait_all<0>();   // the last store is complete before the CTA exits
+  __syncwarp();
 }
 
 cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const int32_t* perm, const int32_t* n_rows_dev,
                                 int64_t max_rows, int64_t K, uint8_t* dst, float* dst_g, uint32_t* amax_zero,
                                 cudaStream_t s) {
+  constexpr int kSmem = 128 * 144;
   const int64_t chunks = max_rows / 128 * (K / 256);
   if (chunks == 0) return cudaSuccess;
-  int64_t blocks = (chunks + 7) / 8;
-  if (blocks > 4 * (int64_t)num_sms()) blocks = 4 * (int64_t)num_sms();
-  gather_tiled_kernel<<<(int)blocks, 256, 0, s>>>(src, src_g, perm, n_rows_dev, max_rows, K / 256, dst, dst_g,
-                                                  amax_zero);
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(gather_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  // one warp per block and one 18 KB chunk image per warp: 12 per SM fit in shared memory
+  int64_t blocks = chunks;
+  if (blocks > 12 * (int64_t)num_sms()) blocks = 12 * (int64_t)num_sms();
+  gather_tiled_kernel<<<(int)blocks, 32, kSmem, s>>>(src, src_g, perm, n_rows_dev, max_rows, K / 256, dst, dst_g,
+                                                     amax_zero);
   return cudaGetLastError();
 }
 
