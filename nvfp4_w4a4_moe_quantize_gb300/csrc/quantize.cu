@@ -354,6 +354,70 @@ __global__ void __launch_bounds__(256) quantize_known_scale_kernel(QuantArgs a) 
       *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(a.rows + i / words, i % words, words)) = 0u;
 }
 
+// Known-scale scopes over row-major rows of a multiple of 64 columns: the same encoding
+// with one 16-value block per lane, consecutive lanes on consecutive blocks.  Each load
+// instruction of a warp reads 1 KB contiguous, each code store writes 256 B contiguous,
+// and the scale arithmetic runs once per block.  Lanes 4q .. 4q+3 gather one 32-bit
+// scale word.  Each warp loads kSlabs slabs of 32 blocks before encoding them, to keep
+// 64 bytes per lane in flight.  Idx is the block index type (32-bit when every index
+// fits).
+template <int RND, typename Idx>
+__global__ void __launch_bounds__(256) quantize_known_coalesced_kernel(QuantArgs a) {
+  constexpr int kSlabs = 2;
+  const int lane = threadIdx.x & 31;
+  const int64_t bpr = a.cols / 16, total = a.rows * bpr;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  float g0 = 0.0f;
+  if (a.mode == kScopeTensor)
+    g0 = a.g_in ? a.g_in[0] : __fdiv_rn(__uint_as_float(a.amax_bits[0]), kGlobalDivisor);
+  for (int64_t base = warp0 * 32 * kSlabs; base < total; base += wstride * 32 * kSlabs) {
+    uint4 v0[kSlabs], v1[kSlabs];
+    int64_t row[kSlabs], cb[kSlabs];
+    bool live[kSlabs];
+#pragma unroll
+    for (int s2 = 0; s2 < kSlabs; ++s2) {
+      const int64_t u = base + 32 * s2 + lane;
+      live[s2] = u < total;
+      const Idx r = live[s2] ? (Idx)u / (Idx)bpr : (Idx)0;
+      row[s2] = (int64_t)r;
+      cb[s2] = live[s2] ? (int64_t)((Idx)u - r * (Idx)bpr) : 0;
+      v0[s2] = v1[s2] = make_uint4(0u, 0u, 0u, 0u);
+      if (live[s2]) {
+        const __nv_bfloat16* src = a.x + row[s2] * a.ld + 16 * cb[s2];
+        v0[s2] = ld_nc_v4(src);
+        v1[s2] = ld_nc_v4(src + 8);
+      }
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < kSlabs; ++s2) {
+      float g = g0;
+      int64_t gi = 0;
+      if (a.mode != kScopeTensor) {
+        gi = (int64_t)((uint64_t)row[s2] / (uint64_t)a.group_rows);
+        g = a.g_in ? a.g_in[gi] : __fdiv_rn(__uint_as_float(a.amax_bits[gi]), kGlobalDivisor);
+      }
+      uint32_t sf = 0;
+      uint2 cw = make_uint2(0u, 0u);
+      encode_regs<RND>(a, row[s2], cb[s2], v0[s2], v1[s2], g, __fmul_rn(6.0f, g), sf, cw);
+      if (live[s2]) *reinterpret_cast<uint2*>(a.codes + row[s2] * a.codes_ld + 8 * cb[s2]) = cw;
+      // the scale word of this lane's 64-value group: block k of it sits at lane 4q + k
+      const int q0 = lane & ~3;
+      uint32_t word = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) word |= __shfl_sync(kFull, sf, q0 + k) << (8 * k);
+      if (live[s2] && (lane & 3) == 0)
+        *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(row[s2], cb[s2] / 4, a.sf_words)) = word;
+      if (live[s2] && cb[s2] == 0 && a.g_out != nullptr &&
+          (a.mode == kScopeTensor ? row[s2] == 0 : row[s2] % a.group_rows == 0))
+        a.g_out[gi] = g;
+    }
+  }
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x, words = a.sf_words;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (a.rows_total - a.rows) * words; i += stride)
+    *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(a.rows + i / words, i % words, words)) = 0u;
+}
+
 template <int RND>
 __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(QuantArgs a) {
   extern __shared__ __align__(128) uint8_t qsm[];
@@ -594,6 +658,22 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
   // per-tensor / per-group scopes in row order: the elementwise kernel
   if (a.mode != kScopeRow && a.map == kMapIdentity && a.row_filter == nullptr && a.rows_dev == nullptr &&
       (a.ld * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) {
+    if (a.tiled_R == 0 && a.cols % 64 == 0 && a.cols_pad == a.cols) {
+      // row-major output, rows of whole 64-value groups: the lane-interleaved kernel
+      const int64_t units = a.rows * (a.cols / 16);
+      int64_t nb = (units + 511) / 512;     // 64 blocks per warp and iteration
+      if (nb > 64 * (int64_t)sms) nb = 64 * (int64_t)sms;
+      if (nb < 1) nb = 1;
+      const bool i32 = units + 128 < ((int64_t)1 << 32);
+      if (rounding == kRoundSR) {
+        if (i32) quantize_known_coalesced_kernel<kRoundSR, uint32_t><<<(int)nb, 256, 0, s>>>(a);
+        else quantize_known_coalesced_kernel<kRoundSR, int64_t><<<(int)nb, 256, 0, s>>>(a);
+      } else {
+        if (i32) quantize_known_coalesced_kernel<kRoundRNE, uint32_t><<<(int)nb, 256, 0, s>>>(a);
+        else quantize_known_coalesced_kernel<kRoundRNE, int64_t><<<(int)nb, 256, 0, s>>>(a);
+      }
+      return cudaGetLastError();
+    }
     const int64_t total = (a.rows > a.rows_total - a.rows ? a.rows : a.rows_total - a.rows) * a.sf_words;
     int64_t nb = (total + 255) / 256;
     if (nb > 8 * (int64_t)sms) nb = 8 * (int64_t)sms;
