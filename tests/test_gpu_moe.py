@@ -387,12 +387,14 @@ def test_forward_row_invariance_and_determinism_tiny(cuda_lib):
 
 
 @pytest.mark.slow
-def test_forward_full_size_sampled_and_row_invariant(cuda_lib):
-    """The Qwen3-30B-A3B-shaped forward (T=16384, H=2048, I=768, E=128, top-8, Zipf
-    routing), in the launch configuration the benchmark times: grouping and per-token
-    quantisation checked in full, GEMM / SwiGLU / requant / down stages on sampled rows,
-    out on sampled tokens; then the first 1024 tokens re-run alone give identical rows."""
-    shape = S.WORKLOADS["forward"]
+@pytest.mark.parametrize("name", ["forward", "learner"])
+def test_forward_full_size_sampled_and_row_invariant(cuda_lib, name):
+    """The Qwen3-30B-A3B-shaped forward in the launch configuration the benchmark times
+    (forward: T=16384, Zipf routing; learner: T=32768, uniform routing; H=2048, I=768,
+    E=128, top-8).  Grouping and per-token quantisation are checked in full.  The GEMM,
+    SwiGLU, requant and down stages are checked on sampled rows, and out on sampled
+    tokens.  Then the first 1024 tokens re-run alone must give identical rows."""
+    shape = S.WORKLOADS[name]
     x, logits, w13, w2 = S.moe_inputs(shape, seed=0)
     ids, w = cuda_lib.moe_route_topk(logits.cuda(), shape.k)
     rid, rw = M.route_topk(logits.numpy(), shape.k)
@@ -441,7 +443,7 @@ def test_forward_full_size_sampled_and_row_invariant(cuda_lib):
             nbad, worst = check_bf16_against(y_all[s_row:s_row + 1], yref)
             assert nbad == 0, (s_row, worst)
     # sampled tokens end to end
-    toks = [0, 1, 4095, 8191, 16383]
+    toks = [0, 1, 4095, 8191, shape.T - 1]
     sub_e = sorted(set(rid[toks].reshape(-1).tolist()))
     pref = {"w13_codes": {}, "w13_sf": {}, "w13_g": {}, "w2_codes": {}, "w2_sf": {}, "w2_g": {}}
     for e in sub_e:
@@ -457,6 +459,44 @@ def test_forward_full_size_sampled_and_row_invariant(cuda_lib):
     part = u16(cuda_lib.moe_expert_forward(xc[:1024].contiguous(), ids[:1024].contiguous(),
                                            w[:1024].contiguous(), pw))
     np.testing.assert_array_equal(part, u16(out)[:1024])
+
+
+@pytest.mark.slow
+def test_gateup_workload_full_size_sampled(cuda_lib):
+    """The gate/up grouped-GEMM workload (T=8192 top-8 of 128 experts, Zipf(1.1) routing:
+    65,536 routed rows, K=2048, N=1536, BF16 out), in the launch the benchmark times:
+    nvfp4_grouped_gemm_tiled with the plain store over the forward's own grouped operand.
+    Sampled rows are checked against the oracle GEMM; output columns follow the prepared
+    W13 row order (gate and up interleaved in chunks of 64)."""
+    shape = S.WORKLOADS["gateup"]
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    x, logits, w13, w2 = S.moe_inputs(shape, seed=1)
+    ids, w = cuda_lib.moe_route_topk(logits.cuda(), k)
+    rid, _ = M.route_topk(logits.numpy(), k)
+    pw = cuda_lib.moe_prepare_weights(w13.cuda(), w2.cuda())
+    _, v = _forward(cuda_lib, x.cuda(), ids, w, pw, T, k)
+    pi = M.permute(rid, E)
+    d = cuda_lib.nvfp4_grouped_gemm_tiled(v["aq"], v["ga"], pw.w13, pw.w13_g, v["padded"], v["counts"], v["mcap"],
+                                          2 * I, H, E, out_dtype=torch.bfloat16)
+    assert cuda_lib.nvfp4_status_check() == 0
+    d_all = u16(d)
+    orig = interleave_src(I)   # column j of the prepared order holds W13 row orig[j]
+    live = np.nonzero(pi["perm"] >= 0)[0]
+    rng = np.random.default_rng(1)
+    sample = np.sort(rng.choice(live, 64, replace=False))
+    experts = np.searchsorted(pi["padded_offsets"], sample, side="right") - 1
+    xb, w13b = S.bf16_bits(x), S.bf16_bits(w13)
+    qx = Q.quantize(xb, scope="row")
+    cache = {}
+    for s_row, e in zip(sample, experts):
+        if e not in cache:
+            cache[e] = Q.quantize(w13b[e], scope="tensor")
+        q13 = cache[e]
+        t = pi["perm"][s_row]
+        dref = M.gemm_rows(qx["codes"][t:t + 1], qx["sf"][t:t + 1], qx["g"][t:t + 1], q13["codes"], q13["sf"],
+                           q13["g"][0])
+        nbad, worst = check_bf16_against(d_all[s_row:s_row + 1], dref[:, orig])
+        assert nbad == 0, (s_row, worst)
 
 
 @pytest.mark.parametrize("sizes", [(1, 7, 64), (3, 16, 33)])
