@@ -506,8 +506,9 @@ def cpu_baseline(x_h, logits_h, w13_h, w2_h, shape, budget_s=15.0, tokens=None):
 def run_profile(args):
     """A short launch sequence on a small case, for ncu captures: the gate/up grouped GEMM
     of a forward over --tokens tokens (Zipf routing, Qwen3 shapes), whole forward steps
-    (routing + expert block) over --tokens tokens, or the standalone quantiser on a
-    --tokens x 2048 tensor.  Prints nothing else."""
+    (routing + expert block) over --tokens tokens, the standalone quantiser on a
+    --tokens x 2048 tensor, or the MXFP8 grouped GEMM over the routed groups of --tokens
+    tokens.  Prints nothing else."""
     import __graft_entry__ as G
     G.build()
     import nvfp4_w4a4_moe_quantize_gb300 as L
@@ -519,6 +520,20 @@ def run_profile(args):
         for _ in range(args.steps):
             L.nvfp4_quantize(qx, L.SCALE_PER_TENSOR, L.ROUND_RNE)
         torch.cuda.synchronize()
+        return
+    if args.profile == "mxgemm":       # MXFP8 grouped GEMM on the routed groups of --tokens tokens
+        glog = S.router_logits_zipf(T, E, shape.zipf_s, 2).to(dev)
+        gids, _ = L.moe_route_topk(glog, k)
+        grp = L.moe_permute(gids, E)
+        counts, padded = grp["counts"], grp["padded_offsets"]
+        m = int(padded[-1].item())
+        a, sfa = L.mxfp8_quantize(S.randn_bf16((max(m, 128), H), 1.0, 3).to(dev))
+        b, sfb = L.mxfp8_quantize(S.randn_bf16((E * 2 * I, H), 0.02, 4).to(dev))
+        d = torch.empty(max(m, 128), 2 * I, dtype=torch.bfloat16, device=dev)
+        for _ in range(args.steps):
+            L.mxfp8_grouped_gemm(a, sfa, b, sfb, padded, counts, 2 * I, H, E, out=d)
+        torch.cuda.synchronize()
+        assert L.nvfp4_status_check() == 0
         return
     x = S.randn_bf16((T, H), 1.0, 1).to(dev)
     logits = S.router_logits_zipf(T, E, shape.zipf_s, 2).to(dev)
@@ -604,7 +619,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens-per-step", type=int, default=2)
-    ap.add_argument("--profile", choices=["none", "gateup", "quantiser", "forward"], default="none",
+    ap.add_argument("--profile", choices=["none", "gateup", "quantiser", "forward", "mxgemm"], default="none",
                     help="run only a short launch sequence of one kernel (for ncu captures)")
     ap.add_argument("--tokens", type=int, default=2048, help="tokens (rows) of the --profile case")
     args = ap.parse_args()

@@ -99,6 +99,94 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
+// The same routing for E <= 32 * EPL with EPL <= 4: each lane first sorts its EPL
+// (key, expert id) pairs by (larger key, then lower id) with a small comparator network,
+// so a round compares only the 32 list heads: one max-reduction of the head keys, one
+// min-reduction of the ids whose head holds that key, and the owning lane pops its head.
+// Experts past E have key 0 and id 0xFFFFFFFF, below every real expert.
+__device__ __forceinline__ void route_ce(uint32_t& ka, uint32_t& ia, float& va, uint32_t& kb, uint32_t& ib,
+                                         float& vb) {
+  const bool sw = kb > ka || (kb == ka && ib < ia);
+  const uint32_t tk = sw ? kb : ka, ti = sw ? ib : ia;
+  const float tv = sw ? vb : va;
+  kb = sw ? ka : kb;
+  ib = sw ? ia : ib;
+  vb = sw ? va : vb;
+  ka = tk;
+  ia = ti;
+  va = tv;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_sorted_kernel(const float* __restrict__ logits, int64_t T, int E,
+                                                                int k, int renorm, int32_t* __restrict__ ids,
+                                                                float* __restrict__ w) {
+  static_assert(EPL == 1 || EPL == 2 || EPL == 4, "lists of 1, 2 or 4");
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  for (int64_t t = warp; t < T; t += nwarp) {
+    float v[EPL], sv[EPL];
+    uint32_t key[EPL], id[EPL];
+    const float* lr = logits + t * E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? lr[e] : -INFINITY;
+      sv[i] = v[i];
+      key[i] = e < E ? order_key(v[i]) : 0u;
+      id[i] = e < E ? (uint32_t)e : 0xFFFFFFFFu;
+    }
+    if (EPL >= 2) route_ce(key[0], id[0], sv[0], key[1 % EPL], id[1 % EPL], sv[1 % EPL]);
+    if (EPL == 4) {
+      route_ce(key[2 % EPL], id[2 % EPL], sv[2 % EPL], key[3 % EPL], id[3 % EPL], sv[3 % EPL]);
+      route_ce(key[0], id[0], sv[0], key[2 % EPL], id[2 % EPL], sv[2 % EPL]);
+      route_ce(key[1 % EPL], id[1 % EPL], sv[1 % EPL], key[3 % EPL], id[3 % EPL], sv[3 % EPL]);
+      route_ce(key[1 % EPL], id[1 % EPL], sv[1 % EPL], key[2 % EPL], id[2 % EPL], sv[2 % EPL]);
+    }
+    int my_id = 0;
+    float my_v = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const uint32_t wbest = __reduce_max_sync(kFullMask, key[0]);
+      const uint32_t bi = __reduce_min_sync(kFullMask, key[0] == wbest ? id[0] : 0xFFFFFFFFu);
+      const float bv = __shfl_sync(kFullMask, sv[0], (int)(bi & 31u));
+      if (id[0] == bi) {   // pop this lane's head
+#pragma unroll
+        for (int i = 0; i + 1 < EPL; ++i) {
+          key[i] = key[i + 1];
+          id[i] = id[i + 1];
+          sv[i] = sv[i + 1];
+        }
+        key[EPL - 1] = 0u;
+        id[EPL - 1] = 0xFFFFFFFFu;
+      }
+      if (lane == j) {
+        my_id = (int)bi;
+        my_v = bv;
+      }
+    }
+    const float top = __shfl_sync(kFullMask, my_v, 0);
+    const float ex = lane < k ? expf(my_v - top) : 0.0f;
+    float den;
+    if (renorm) {
+      den = ex;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFullMask, den, o);
+    } else {
+      den = 0.0f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i < E) den += expf(v[i] - top);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFullMask, den, o);
+    }
+    if (lane < k) {
+      ids[t * k + lane] = my_id;
+      w[t * k + lane] = __fdiv_rn(ex, den);
+    }
+  }
+}
+
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renorm, int32_t* ids, float* w,
                               cudaStream_t s) {
   if (T == 0) return cudaSuccess;
@@ -106,13 +194,16 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int 
   if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
   const int epl = (E + 31) / 32;
 #define NVFP4_ROUTE(N) route_topk_kernel<N><<<(int)blocks, 256, 0, s>>>(logits, T, E, k, renorm, ids, w)
-  if (epl <= 1) NVFP4_ROUTE(1);
-  else if (epl <= 2) NVFP4_ROUTE(2);
-  else if (epl <= 4) NVFP4_ROUTE(4);
+#define NVFP4_ROUTE_SORTED(N) \
+  route_topk_sorted_kernel<N><<<(int)blocks, 256, 0, s>>>(logits, T, E, k, renorm, ids, w)
+  if (epl <= 1) NVFP4_ROUTE_SORTED(1);
+  else if (epl <= 2) NVFP4_ROUTE_SORTED(2);
+  else if (epl <= 4) NVFP4_ROUTE_SORTED(4);
   else if (epl <= 8) NVFP4_ROUTE(8);
   else if (epl <= 16) NVFP4_ROUTE(16);
   else NVFP4_ROUTE(32);
 #undef NVFP4_ROUTE
+#undef NVFP4_ROUTE_SORTED
   return cudaGetLastError();
 }
 
