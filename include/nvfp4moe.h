@@ -202,6 +202,31 @@ nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const flo
                               int64_t cols, nvfp4_scale_mode mode, int64_t group_rows, void* out,
                               nvfp4_out_dtype out_dtype, int64_t ldo, void* stream);
 
+/* ---------------------------------------------------------------- dequantised backward */
+
+/* BF16 grouped GEMM, the GEMM of the dequantised backward ("The 4-bitter Lesson...",
+ * §"Improving Gradient Stability": the backward pass multiplies by the dequantised
+ * weights DQ(Q(W)) -- see nvfp4_dequantize -- so that it differentiates the forward that
+ * was actually run).  For every expert e and every row r of its group:
+ *     D[r, n] = sum_k A[r, k] * B_e[n, k]
+ * with BF16 operands, accumulated in FP32 on the tensor cores in a fixed order (no
+ * split-K), then rounded once to out_dtype.
+ *   A: device BF16 [M_total, K] (rows outside the groups are read but their results are
+ *      not stored).  B: device BF16 [E, N, K].
+ *   group_offsets, group_rows, M_total, D, ldd: as nvfp4_grouped_gemm.
+ *   N % 128 == 0, K % 64 == 0, E <= 1024.  A, B and D 16-byte aligned; the group arrays
+ *   4-byte aligned.  No workspace. */
+nvfp4_status bf16_grouped_gemm(const void* A, const void* B, const int32_t* group_offsets,
+                               const int32_t* group_rows, int64_t M_total, int64_t N, int64_t K,
+                               int32_t E, void* D, nvfp4_out_dtype out_dtype, int64_t ldd,
+                               void* stream);
+
+/* Transpose of `batches` stacked BF16 matrices: out[b*C + c, r] = x[b*R + r, c] (x has
+ * pitch ld >= C elements; out is [batches*C, R], dense).  It produces the K-major form of
+ * a transposed operand, e.g. DQ(W)^T for a dgrad GEMM.  x and out are 4-byte aligned. */
+nvfp4_status bf16_transpose(const void* x, int64_t batches, int64_t R, int64_t C, int64_t ld, void* out,
+                            void* stream);
+
 /* ---------------------------------------------------------------- MXFP8 */
 
 /* MXFP8, the format of the recipe's validation runs ("The 4-bitter Lesson...",

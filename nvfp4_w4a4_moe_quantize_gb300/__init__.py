@@ -24,6 +24,7 @@ __all__ = [
     "moe_forward_workspace_layout", "nvfp4_status_check", "nvfp4_sf_bytes", "NVFP4MoEWeights",
     "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled", "nvfp4_tiled_bytes",
     "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_grouped_gemm", "mxfp8_sf_bytes",
+    "bf16_grouped_gemm", "bf16_transpose",
     "SCALE_PER_TENSOR", "SCALE_PER_ROW", "SCALE_PER_GROUP", "ROUND_RNE", "ROUND_STOCHASTIC",
 ]
 
@@ -71,6 +72,8 @@ _SIGS = {
                                         _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                           _vp, ctypes.c_int, _i64, _vp]),
+    "bf16_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, ctypes.c_int, _i64, _vp]),
+    "bf16_transpose": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "mxfp8_sf_bytes": (_sz, [_i64, _i64]),
     "mxfp8_quantize": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "mxfp8_dequantize": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, ctypes.c_int, _i64, _vp]),
@@ -258,6 +261,32 @@ def nvfp4_grouped_gemm(A, SFA, gA, B, SFB, gB, group_offsets, group_rows, N: int
     _check(lib.nvfp4_grouped_gemm(_p(A), _p(SFA), _p(gA), _p(B), _p(SFB), _p(gB), _p(group_offsets),
                                   _p(group_rows), M_total, N, K, E, _p(out), code, out.stride(0),
                                   _stream(stream)), "nvfp4_grouped_gemm")
+    return out
+
+
+# --------------------------------------------------------------------------- dequantised backward
+
+def bf16_grouped_gemm(A, B, group_offsets, group_rows, N: int, K: int, E: int, out_dtype=torch.bfloat16,
+                      out: torch.Tensor | None = None, stream=None):
+    """D[M_total, N] = grouped BF16 GEMM: A [M_total, K] BF16, B [E*N, K] BF16 (rows outside
+    the groups are left unwritten)."""
+    lib = load()
+    M_total = A.shape[0]
+    if out is None:
+        out = torch.empty(M_total, N, dtype=out_dtype, device=_dev(A))
+    code = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.bf16_grouped_gemm(_p(A), _p(B), _p(group_offsets), _p(group_rows), M_total, N, K, E, _p(out), code,
+                                 out.stride(0), _stream(stream)), "bf16_grouped_gemm")
+    return out
+
+
+def bf16_transpose(x: torch.Tensor, batches: int = 1, stream=None):
+    """out[b*C + c, r] = x[b*R + r, c] for x = `batches` stacked [R, C] BF16 matrices."""
+    lib = load()
+    rows, C = x.shape
+    R = rows // batches
+    out = torch.empty(batches * C, R, dtype=torch.bfloat16, device=_dev(x))
+    _check(lib.bf16_transpose(_p(x), batches, R, C, x.stride(0), _p(out), _stream(stream)), "bf16_transpose")
     return out
 
 

@@ -401,6 +401,49 @@ nvfp4_status mxfp8_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const uint
   return from_cuda(launch_grouped_gemm_mx(ma, mb, md, g, M_total / 128, s));
 }
 
+nvfp4_status bf16_grouped_gemm(const void* A, const void* B, const int32_t* group_offsets,
+                               const int32_t* group_rows, int64_t M_total, int64_t N, int64_t K, int32_t E, void* D,
+                               nvfp4_out_dtype out_dtype, int64_t ldd, void* stream) {
+  if (E <= 0 || E > 1024 || N <= 0 || K <= 0 || M_total < 0 || M_total % 128 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 64 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((int64_t)E * N >= (int64_t)1 << 31 || M_total >= (int64_t)1 << 31 || K >= (int64_t)1 << 20)
+    return NVFP4_ERR_UNSUPPORTED;
+  if (ldd < N || ldd % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_INVALID_ARG;
+  if (M_total == 0) return NVFP4_OK;
+  const void* ptrs[] = {A, B, D};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned4(group_offsets) || !aligned4(group_rows)) return NVFP4_ERR_INVALID_ARG;
+  const bool out_f32 = out_dtype == NVFP4_OUT_F32;
+  GemmArgs g{};
+  g.offsets = group_offsets;
+  g.rows = group_rows;
+  g.E = E;
+  g.N = (int32_t)N;
+  g.K = (int32_t)K;
+  g.d = D;
+  g.ldd = ldd;
+  g.out_f32 = out_f32;
+  g.status = device_status_ptr();
+  // the BF16 operands as byte matrices: 128-byte boxes are 64 values of K
+  CUtensorMap ma, mb, md;
+  if (!make_map(&ma, A, M_total, 2 * K, 2 * K, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
+      !make_map(&mb, B, (int64_t)E * N, 2 * K, 2 * K, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
+      !make_map(&md, D, M_total, N, ldd * (out_f32 ? 4 : 2), 32,
+                out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_f32 ? 4 : 2))
+    return NVFP4_ERR_CUDA;
+  return from_cuda(launch_grouped_gemm_bf16(ma, mb, md, g, M_total / 128, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status bf16_transpose(const void* x, int64_t batches, int64_t R, int64_t C, int64_t ld, void* out,
+                            void* stream) {
+  if (batches < 0 || R < 0 || C < 0 || ld < C) return NVFP4_ERR_INVALID_ARG;
+  if (batches == 0 || R == 0 || C == 0) return NVFP4_OK;
+  if (x == nullptr || out == nullptr || !aligned4(x) || !aligned4(out)) return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_transpose_bf16(x, batches, R, C, ld, out, static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A, const float* gA, const uint8_t* B, const float* gB,
                                       const int32_t* group_offsets, const int32_t* group_rows, int64_t M_total,
                                       int64_t N, int64_t K, int32_t E, void* D, nvfp4_out_dtype out_dtype,

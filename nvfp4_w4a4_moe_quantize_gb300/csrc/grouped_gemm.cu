@@ -23,7 +23,12 @@
 // share A tiles and one expert's weights in L2.  The K loop has a fixed order and no
 // split, so every output element has one accumulation order whatever the batch.
 //
-// The same kernel, instantiated with kMX, is the MXFP8 grouped GEMM of the recipe's
+// The same kernel is also the BF16 grouped GEMM of the dequantised backward ("The
+// 4-bitter Lesson...", §"Improving Gradient Stability": the backward GEMMs take the
+// dequantised weights DQ(Q(W)), in BF16): kind::f16 MMAs (M=128, N=128, K=16) on BF16
+// operands, 64 K-values per stage, no scale factors, no global scales.
+//
+// Instantiated with the MX format it is the MXFP8 grouped GEMM of the recipe's
 // validation format ("The 4-bitter Lesson...", §"Improving Gradient Stability", Results
 // Validation with MXFP8): E4M3 operands with one E8M0 scale per 32 values of K, no global
 // scales.  A stage is then 128 K-values (one 128-byte swizzle row of 8-bit codes).  The
@@ -40,6 +45,8 @@
 #include "ptx.cuh"
 
 namespace nvfp4 {
+
+enum : int { kGemmNVF4 = 0, kGemmMXF8 = 1, kGemmBF16 = 2 };
 
 namespace gg {
 constexpr int kBM = 128;          // rows per tile (one per TMEM lane)
@@ -80,15 +87,16 @@ static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 }  // namespace gg
 
-template <bool kMX>
+template <int kFmt>
 __global__ void __launch_bounds__(gg::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                         const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
   using namespace gg;
   // per stage: K values, bytes of A's scales, bytes of one 128-row block of B's scales
-  constexpr int kStageK = kMX ? 128 : 256;
-  constexpr int kSFA = kMX ? 512 : kSFABytes;
-  constexpr int kSFB128 = kMX ? 512 : 2048;
+  constexpr bool kMX = kFmt == kGemmMXF8, kBF = kFmt == kGemmBF16;
+  constexpr int kStageK = kBF ? 64 : (kMX ? 128 : 256);
+  constexpr int kSFA = kBF ? 0 : (kMX ? 512 : kSFABytes);
+  constexpr int kSFB128 = kBF ? 0 : (kMX ? 512 : 2048);
   constexpr uint32_t kTx = kABytes + kBBytes + kSFA + (kBN / 128) * kSFB128;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -97,7 +105,7 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
   for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
   for (int i = threadIdx.x; i < g.E; i += blockDim.x) {
     sm.rows[i] = g.rows[i];
-    sm.gb[i] = kMX ? 1.0f : g.gb[i];
+    sm.gb[i] = kFmt != kGemmNVF4 ? 1.0f : g.gb[i];
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -146,13 +154,15 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
           mbar_arrive_expect_tx(&sm.full[stage], kTx);
           tma_load_2d(sm.a[stage], &tma, kb * kBKBytes, row0, &sm.full[stage]);
           tma_load_2d(sm.b[stage], &tmb, kb * kBKBytes, brow, &sm.full[stage]);
-          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)m_tile * sf_kgroups + kb * kSFTiles) * 512, kSFA,
-                    &sm.full[stage]);
-#pragma unroll
-          for (int h = 0; h < kBN / 128; ++h)
-            bulk_load(sm.sfb[stage] + h * kSFB128,
-                      g.sfb + ((int64_t)(brow / 128 + h) * sf_kgroups + kb * kSFTiles) * 512, kSFB128,
+          if constexpr (!kBF) {
+            bulk_load(sm.sfa[stage], g.sfa + ((int64_t)m_tile * sf_kgroups + kb * kSFTiles) * 512, kSFA,
                       &sm.full[stage]);
+#pragma unroll
+            for (int h = 0; h < kBN / 128; ++h)
+              bulk_load(sm.sfb[stage] + h * kSFB128,
+                        g.sfb + ((int64_t)(brow / 128 + h) * sf_kgroups + kb * kSFTiles) * 512, kSFB128,
+                        &sm.full[stage]);
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -163,7 +173,7 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = kMX ? idesc_mxf8(kBM, kBN, 0) : idesc_nvf4(kBM, kBN);
+      constexpr uint32_t idesc = kBF ? idesc_bf16(kBM, kBN) : (kMX ? idesc_mxf8(kBM, kBN, 0) : idesc_nvf4(kBM, kBN));
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -178,7 +188,15 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
           const uint32_t sfb_t = sfa_t + 16;
           const uint32_t sa = smem_u32(sm.a[stage]), sb = smem_u32(sm.b[stage]);
           const uint32_t ssfa = smem_u32(sm.sfa[stage]), ssfb = smem_u32(sm.sfb[stage]);
-          if constexpr (kMX) {
+          if constexpr (kBF) {
+            // 64 BF16 values of K per 128-byte row: four K=16 steps of 32 bytes
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
+              const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
+              tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | j) != 0 ? 1u : 0u);
+            }
+          } else if constexpr (kMX) {
             tc_cp_32x128b_warpx4(sfa_t, smem_desc(ssfa, 0, 128, 0));
 #pragma unroll
             for (int h = 0; h < kBN / 128; ++h) tc_cp_32x128b_warpx4(sfb_t + 4 * h, smem_desc(ssfb + 512 * h, 0, 128, 0));
@@ -236,7 +254,7 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
       const bool valid = q * 32 + lane < in_group;
       const bool full_warp = q * 32 + 32 <= in_group;
       const int64_t row = (int64_t)row0 + q * 32 + lane;
-      const float ga = kMX ? 1.0f : (valid ? g.ga[row] : 0.0f);         // load before the wait
+      const float ga = kFmt != kGemmNVF4 ? 1.0f : (valid ? g.ga[row] : 0.0f);   // load before the wait
       if (!mbar_wait(&sm.accf[acc], acc_phase, g.status, abort)) break;
       tc_fence_after();
       const float scale = __fmul_rn(ga, sm.gb[e]);
@@ -311,14 +329,14 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool kMX>
+template <int kFmt>
 static cudaError_t launch_gg(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
                              const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
   static bool attr_set[64] = {};   // the attribute is set once per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kMX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)gg::kSmemBytes);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -327,18 +345,23 @@ static cudaError_t launch_gg(const CUtensorMap& tma, const CUtensorMap& tmb, con
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
-  grouped_gemm_kernel<kMX><<<grid, gg::kThreads, gg::kSmemBytes, s>>>(tma, tmb, tmd, g);
+  grouped_gemm_kernel<kFmt><<<grid, gg::kThreads, gg::kSmemBytes, s>>>(tma, tmb, tmd, g);
   return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
                                 const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
-  return launch_gg<false>(tma, tmb, tmd, g, max_m_tiles, s);
+  return launch_gg<kGemmNVF4>(tma, tmb, tmd, g, max_m_tiles, s);
 }
 
 cudaError_t launch_grouped_gemm_mx(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
                                    const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
-  return launch_gg<true>(tma, tmb, tmd, g, max_m_tiles, s);
+  return launch_gg<kGemmMXF8>(tma, tmb, tmd, g, max_m_tiles, s);
+}
+
+cudaError_t launch_grouped_gemm_bf16(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
+                                     const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
+  return launch_gg<kGemmBF16>(tma, tmb, tmd, g, max_m_tiles, s);
 }
 
 }  // namespace nvfp4

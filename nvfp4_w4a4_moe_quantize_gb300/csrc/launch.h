@@ -82,6 +82,11 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, 
 // scales per 32 values in the 128x4 tiled layout; g.ga / g.gb unused).  K % 128 == 0.
 cudaError_t launch_grouped_gemm_mx(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
                                    const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s);
+// BF16 grouped GEMM (the dequantised backward): A [M_total, K], B [E*N, K] BF16, both as
+// byte maps with 128-byte boxes; g.sfa / g.sfb / g.ga / g.gb unused.  N % 128 == 0,
+// K % 64 == 0.
+cudaError_t launch_grouped_gemm_bf16(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
+                                     const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s);
 // MXFP8 quantiser: x BF16 [rows, ld] -> E4M3 codes [rows, cols] + E8M0 scales, 128x4 tiled
 // for rows padded to 128 (padding words 0).  cols % 128 == 0.
 cudaError_t launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes, uint8_t* sf,

@@ -262,6 +262,23 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D(tmem) (+)= A(smem) * B(smem)^T, kind::f16 (no block scaling).  K = 16 per op for
+// 16-bit operands.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor for kind::f16 with BF16 A and B (format 1) K-major and a
+// float32 accumulator (D format 1 at bits 4-5), N >> 3 at bits 17-22, M >> 4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Instruction descriptor for kind::mxf8f6f4: A and B E4M3 (format 0) K-major, UE8M0
 // scales (bit 23 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.  With one scale byte
 // per row and op, sf_id (0..3) picks the byte of each 32-bit scale word, for A (bits

@@ -22,7 +22,8 @@ def test_every_declared_function_is_exported(lib):
                 "nvfp4_status_string", "nvfp4_sf_bytes", "moe_weights_sizes", "nvfp4_workspace_size",
                 "moe_forward_workspace_layout", "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled",
                 "nvfp4_tiled_bytes", "nvfp4_quantize_noalloc", "nvfp4_dequantize", "nvfp4_quantize_transposed",
-                "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_grouped_gemm", "mxfp8_sf_bytes"}
+                "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_grouped_gemm", "mxfp8_sf_bytes",
+                "bf16_grouped_gemm", "bf16_transpose"}
     assert expected <= set(names)
     for n in names:
         assert hasattr(lib, n), n
