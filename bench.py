@@ -382,6 +382,37 @@ def run_ours(args, rank, world, local_rank):
                               "frac_of_fp8_peak_from_measured_bf16": round(mx_tflops / fp8_peak, 4)}}
     del ma_bf16, ma, msfa, mb, msfb, mg_d, mdq_out, mcodes, msf
 
+    # ---------------------------------------------------------------- dequantised backward
+    # The recipe's backward GEMM on the dequantised weights: dgrad of the gate/up
+    # projection, dX = dGU . DQ(W13), over the gate/up groups (65,536 routed rows): DQ of
+    # all 128 experts' W13 to BF16 (from a per-expert NVFP4 quantisation), transposed to
+    # [E, H, 2I], then the BF16 grouped GEMM (N = H = 2048, K = 2I = 1536).
+    w13_dev = w13_h.to(dev).reshape(E * 2 * I, H)
+    wc, wsf, wg = L.nvfp4_quantize(w13_dev, L.SCALE_PER_GROUP, group_rows=2 * I)
+    del w13_dev
+    wdq = torch.empty(E * 2 * I, H, dtype=torch.bfloat16, device=dev)
+    dq_t = time_launches_median(lambda: L.nvfp4_dequantize(wc, wsf, wg, H, L.SCALE_PER_GROUP, group_rows=2 * I,
+                                                           out=wdq), iters, flush, stream)
+    wdqt = L.bf16_transpose(wdq, batches=E)
+    del wdq, wc, wsf
+    dgu = S.randn_bf16((gm, 2 * I), 1e-3, 5).to(dev)
+    dx = torch.empty(gm, H, dtype=torch.bfloat16, device=dev)
+    bt = time_launches_median(lambda: L.bf16_grouped_gemm(dgu, wdqt, g_pad, g_cnt, H, 2 * I, E, out=dx),
+                              iters, flush, stream)
+    bf16_tflops = gflops / (bt * 1e-3) / 1e12
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    dq_bytes = E * 2 * I * H // 2 + L.nvfp4_sf_bytes(E * 2 * I, H) + E * 2 * I * H * 2
+    dqbwd = {"timing": f"median of {iters} launches, L2 flushed before each",
+             "dequantize_w13": {"workload": "DQ of W13, 128 experts x 1536 x 2048, NVFP4 -> BF16",
+                                "algorithmic_bytes": dq_bytes, "us": round(dq_t * 1e3, 2),
+                                "gbs": round(dq_bytes / (dq_t * 1e-3) / 1e9, 1),
+                                "frac_hbm": round(dq_bytes / (dq_t * 1e-3) / 1e9 / hbm_peak, 4)},
+             "bf16_grouped_gemm": {"workload": "dgrad of the gate/up projection on the gate/up groups "
+                                               "(65,536 routed rows), N=2048, K=1536, BF16 x BF16, BF16 out",
+                                   "ms": round(bt, 4), "tflops": round(bf16_tflops, 1),
+                                   "frac_of_measured_bf16": round(bf16_tflops / bf16_peak, 4)}}
+    del wdqt, dgu, dx
+
     # ---------------------------------------------------------------- end to end (host buffers)
     # Every step copies its inputs (x, router logits) from pinned host memory and reads its
     # result back.  Serial: copy in, compute, copy out on one stream.  Pipelined (the
@@ -468,7 +499,8 @@ def run_ours(args, rank, world, local_rank):
                    "weight_prep_s": round(prep_s, 3), "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps, "stages_ms": {k_: round(v_, 4) for k_, v_ in stages.items()},
-        "grouped_gemm": grouped, "quantiser": quant, "mxfp8": mxfp8, "wall_s_timed": round(wall_s, 3),
+        "grouped_gemm": grouped, "quantiser": quant, "mxfp8": mxfp8, "dequantised_backward": dqbwd,
+        "wall_s_timed": round(wall_s, 3),
     }
     return line
 
