@@ -135,6 +135,29 @@ def swiglu(d_bits: np.ndarray, inter: int) -> np.ndarray:
     return F.bf16_round(silu(gate) * up)
 
 
+def swiglu_backward(d_bits: np.ndarray, dh_bits: np.ndarray, inter: int) -> np.ndarray:
+    """Gradient of h = silu(gate) * up for the backward pass, with gate and up read from the
+    BF16 gate/up output as in ``swiglu`` and dh the BF16 gradient of h:
+
+        dgate = dh * up * silu'(gate),  silu'(g) = s(g) * (1 + g * (1 - s(g))),  s = sigmoid
+        dup   = dh * silu(gate)
+
+    formed in float64 and each rounded once to BF16.  Returns the BF16 bits of
+    [dgate | dup], shaped like d_bits (columns [0, I) and [I, 2I)).  Reading: the pages
+    do not give the backward's precision; the forward's rule (float64, one rounding) is
+    kept."""
+    d = F.bf16_to_f32(d_bits).astype(np.float64)
+    dh = F.bf16_to_f32(dh_bits).astype(np.float64)
+    g, u = d[:, :inter], d[:, inter:2 * inter]
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-g))
+    dsilu = s * (1.0 + g * (1.0 - s))
+    out = np.empty_like(d)
+    out[:, :inter] = dh * u * dsilu
+    out[:, inter:2 * inter] = dh * (g * s)
+    return F.bf16_round(out)
+
+
 # --------------------------------------------------------------------------- combine
 
 def combine(y_bits: np.ndarray, inv: np.ndarray, topk_w: np.ndarray) -> np.ndarray:

@@ -178,6 +178,39 @@ def test_swiglu_against_mpmath():
                 assert h[r, c] == code, (r, c)
 
 
+def test_swiglu_backward_against_mpmath_derivative():
+    """The SwiGLU backward against mpmath: dgate = dh * d/dg[silu(g) u], the derivative
+    taken numerically by mpmath.diff of the forward expression (not the closed form the
+    oracle uses), and dup = dh * silu(g).  Both are rounded once to BF16."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    rng = np.random.default_rng(6)
+    I = 16
+    d = F.bf16_round(rng.standard_normal((6, 2 * I)) * 3)
+    d[0, 0] = 0x0000                      # g = 0: dgate = dh * u / 2, dup = 0
+    d[0, 1] = 0x41F0                      # g = 30: silu' ~ 1
+    d[0, 2] = 0xC1F0                      # g = -30: silu' ~ -29 e^-30
+    dh = F.bf16_round(rng.standard_normal((6, I)))
+    out = M.swiglu_backward(d, dh, I)
+    dv, dhv = F.bf16_to_f32(d), F.bf16_to_f32(dh)
+    for r in range(6):
+        for c in range(I):
+            g, u, gh = (mpmath.mpf(float(dv[r, c])), mpmath.mpf(float(dv[r, I + c])),
+                        mpmath.mpf(float(dhv[r, c])))
+            dg = gh * mpmath.diff(lambda z: z / (1 + mpmath.exp(-z)) * u, g)
+            du = gh * g / (1 + mpmath.exp(-g))
+            for col, exact in ((c, dg), (I + c, du)):
+                if exact == 0:
+                    assert (out[r, col] & 0x7FFF) == 0, (r, col)
+                    continue
+                code, _ = _bf16_nearest_mp(mpmath, exact)
+                assert out[r, col] == code, (r, col)
+    # g = 0: silu'(0) = 1/2, silu(0) = 0
+    g0 = F.bf16_to_f32(out[0:1, 0:1])[0, 0]
+    assert g0 == F.bf16_to_f32(F.bf16_round(np.array([[0.5 * dhv[0, 0] * dv[0, I]]])))[0, 0]
+    assert (out[0, I] & 0x7FFF) == 0
+
+
 def test_combine_against_mpmath():
     mpmath = pytest.importorskip("mpmath")
     mpmath.mp.dps = 60
