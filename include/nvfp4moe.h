@@ -221,6 +221,17 @@ nvfp4_status bf16_grouped_gemm(const void* A, const void* B, const int32_t* grou
                                int32_t E, void* D, nvfp4_out_dtype out_dtype, int64_t ldd,
                                void* stream);
 
+/* SwiGLU backward of the expert block: for h = silu(gate) * up,
+ *     dgate = dh * up * silu'(gate),  silu'(g) = s * (1 + g * (1 - s)),  s = sigmoid(g),
+ *     dup   = dh * silu(gate),
+ * each evaluated in float32 and rounded once to BF16 (within one BF16 ulp of the float64
+ * evaluation, plus float32 round-off where silu' cancels).
+ *   gu:  device BF16 [rows, 2I], gate in columns [0, I), up in [I, 2I);
+ *   dh:  device BF16 [rows, I];  dgu: device BF16 [rows, 2I], [dgate | dup].
+ *   I % 8 == 0; all three 16-byte aligned.  No workspace. */
+nvfp4_status moe_swiglu_backward(const void* gu, const void* dh, int64_t rows, int64_t I, void* dgu,
+                                 void* stream);
+
 /* Transpose of `batches` stacked BF16 matrices: out[b*C + c, r] = x[b*R + r, c] (x has
  * pitch ld >= C elements; out is [batches*C, R], dense).  It produces the K-major form of
  * a transposed operand, e.g. DQ(W)^T for a dgrad GEMM.  x and out are 4-byte aligned. */

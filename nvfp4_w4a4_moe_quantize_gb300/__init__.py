@@ -24,7 +24,7 @@ __all__ = [
     "moe_forward_workspace_layout", "nvfp4_status_check", "nvfp4_sf_bytes", "NVFP4MoEWeights",
     "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled", "nvfp4_tiled_bytes",
     "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_grouped_gemm", "mxfp8_sf_bytes",
-    "bf16_grouped_gemm", "bf16_transpose",
+    "bf16_grouped_gemm", "bf16_transpose", "moe_swiglu_backward",
     "SCALE_PER_TENSOR", "SCALE_PER_ROW", "SCALE_PER_GROUP", "ROUND_RNE", "ROUND_STOCHASTIC",
 ]
 
@@ -74,6 +74,7 @@ _SIGS = {
                                           _vp, ctypes.c_int, _i64, _vp]),
     "bf16_grouped_gemm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, ctypes.c_int, _i64, _vp]),
     "bf16_transpose": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "moe_swiglu_backward": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
     "mxfp8_sf_bytes": (_sz, [_i64, _i64]),
     "mxfp8_quantize": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "mxfp8_dequantize": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, ctypes.c_int, _i64, _vp]),
@@ -287,6 +288,17 @@ def bf16_transpose(x: torch.Tensor, batches: int = 1, stream=None):
     R = rows // batches
     out = torch.empty(batches * C, R, dtype=torch.bfloat16, device=_dev(x))
     _check(lib.bf16_transpose(_p(x), batches, R, C, x.stride(0), _p(out), _stream(stream)), "bf16_transpose")
+    return out
+
+
+def moe_swiglu_backward(gu: torch.Tensor, dh: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    """[dgate | dup] (BF16 [rows, 2I]) of h = silu(gate) * up, from gu = [gate | up] and dh."""
+    lib = load()
+    rows, I = dh.shape
+    if out is None:
+        out = torch.empty(rows, 2 * I, dtype=torch.bfloat16, device=_dev(dh))
+    _check(lib.moe_swiglu_backward(_p(gu.contiguous()), _p(dh.contiguous()), rows, I, _p(out), _stream(stream)),
+           "moe_swiglu_backward")
     return out
 
 

@@ -436,6 +436,14 @@ nvfp4_status bf16_grouped_gemm(const void* A, const void* B, const int32_t* grou
   return from_cuda(launch_grouped_gemm_bf16(ma, mb, md, g, M_total / 128, static_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status moe_swiglu_backward(const void* gu, const void* dh, int64_t rows, int64_t I, void* dgu,
+                                 void* stream) {
+  if (rows < 0 || I <= 0 || I % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (rows == 0) return NVFP4_OK;
+  if (!gu || !dh || !dgu || !aligned16(gu) || !aligned16(dh) || !aligned16(dgu)) return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_swiglu_backward(gu, dh, rows, I, dgu, static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status bf16_transpose(const void* x, int64_t batches, int64_t R, int64_t C, int64_t ld, void* out,
                             void* stream) {
   if (batches < 0 || R < 0 || C < 0 || ld < C) return NVFP4_ERR_INVALID_ARG;

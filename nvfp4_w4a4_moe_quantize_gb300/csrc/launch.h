@@ -132,6 +132,10 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t*
                            int* status, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int64_t T, int k, int64_t H,
                            void* out, cudaStream_t s);
+// SwiGLU backward: [dgate | dup] (BF16 [rows, 2I]) from [gate | up] (BF16 [rows, 2I]) and dh
+// (BF16 [rows, I]); I % 8 == 0.
+cudaError_t launch_swiglu_backward(const void* gu, const void* dh, int64_t rows, int64_t I, void* dgu,
+                                   cudaStream_t s);
 // rows: rows of d to visit; nrows_dev (nullable): device count that caps rows.
 cudaError_t launch_swiglu_quant(const void* d, const int32_t* perm, int64_t rows, const int32_t* nrows_dev,
                                 int64_t I, int64_t Ip, void* h_out, uint8_t* hq, uint8_t* hsf, float* gh,

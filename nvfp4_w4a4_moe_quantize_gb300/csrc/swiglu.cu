@@ -122,6 +122,58 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(const __nv_bfloat16* 
   }
 }
 
+// SwiGLU backward: for h = silu(g) * u with s = sigmoid(g),
+//     dgate = dh * u * s * (1 + g * (1 - s)),   dup = dh * g * s,
+// each in float32 (s = 1 / (1 + e^-g) with expf and a correctly rounded division), rounded
+// once to BF16.  One thread per 8 columns of a row: gate and up from [gate | up] rows of
+// pitch 2I, dh from rows of pitch I, [dgate | dup] out like the input.
+__global__ void __launch_bounds__(256) swiglu_backward_kernel(const __nv_bfloat16* __restrict__ gu,
+                                                              const __nv_bfloat16* __restrict__ dh, int64_t rows,
+                                                              int64_t I, __nv_bfloat16* __restrict__ dgu) {
+  const int64_t chunks = I / 8, total = rows * chunks;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / chunks, c = 8 * (i - r * chunks);
+    const uint4 gq = *reinterpret_cast<const uint4*>(gu + r * 2 * I + c);
+    const uint4 uq = *reinterpret_cast<const uint4*>(gu + r * 2 * I + I + c);
+    const uint4 hq = *reinterpret_cast<const uint4*>(dh + r * I + c);
+    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w}, uw[4] = {uq.x, uq.y, uq.z, uq.w},
+                   hw[4] = {hq.x, hq.y, hq.z, hq.w};
+    uint32_t dg[4], du[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      float rg[2], ru[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float g = __uint_as_float(e ? gw[p] & 0xFFFF0000u : gw[p] << 16);
+        const float u = __uint_as_float(e ? uw[p] & 0xFFFF0000u : uw[p] << 16);
+        const float d = __uint_as_float(e ? hw[p] & 0xFFFF0000u : hw[p] << 16);
+        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+        const float ds = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, sg))));
+        rg[e] = __fmul_rn(__fmul_rn(d, u), ds);
+        ru[e] = __fmul_rn(d, __fmul_rn(g, sg));
+      }
+      const __nv_bfloat162 a = __floats2bfloat162_rn(rg[0], rg[1]);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(ru[0], ru[1]);
+      dg[p] = *reinterpret_cast<const uint32_t*>(&a);
+      du[p] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(dgu + r * 2 * I + c) = make_uint4(dg[0], dg[1], dg[2], dg[3]);
+    *reinterpret_cast<uint4*>(dgu + r * 2 * I + I + c) = make_uint4(du[0], du[1], du[2], du[3]);
+  }
+}
+
+cudaError_t launch_swiglu_backward(const void* gu, const void* dh, int64_t rows, int64_t I, void* dgu,
+                                   cudaStream_t s) {
+  const int64_t total = rows * (I / 8);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 16 * (int64_t)num_sms()) blocks = 16 * (int64_t)num_sms();
+  swiglu_backward_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(gu),
+                                                     static_cast<const __nv_bfloat16*>(dh), rows, I,
+                                                     static_cast<__nv_bfloat16*>(dgu));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_swiglu_quant(const void* d, const int32_t* perm, int64_t rows, const int32_t* nrows_dev,
                                 int64_t I, int64_t Ip, void* h_out, uint8_t* hq, uint8_t* hsf, float* gh,
                                 cudaStream_t s) {

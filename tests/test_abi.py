@@ -23,7 +23,7 @@ def test_every_declared_function_is_exported(lib):
                 "moe_forward_workspace_layout", "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled",
                 "nvfp4_tiled_bytes", "nvfp4_quantize_noalloc", "nvfp4_dequantize", "nvfp4_quantize_transposed",
                 "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_grouped_gemm", "mxfp8_sf_bytes",
-                "bf16_grouped_gemm", "bf16_transpose"}
+                "bf16_grouped_gemm", "bf16_transpose", "moe_swiglu_backward"}
     assert expected <= set(names)
     for n in names:
         assert hasattr(lib, n), n

@@ -127,3 +127,23 @@ def test_bf16_gemm_argument_checks(cuda_lib):
     rows = torch.tensor([128], dtype=torch.int32, device="cuda")
     with pytest.raises(Exception):
         cuda_lib.bf16_grouped_gemm(a, a, offs, rows, 128, 96, 1)
+
+
+@pytest.mark.parametrize("rows,I", [(1, 8), (333, 768), (64, 128)])
+def test_swiglu_backward_matches_oracle(cuda_lib, rows, I):
+    """The SwiGLU backward between the down-projection dgrad and the gate/up dgrad: float32
+    on the device against the oracle's float64, each result within one BF16 ulp plus the
+    float32 round-off allowance where silu' cancels."""
+    from oracle import moe as M
+    rng = np.random.default_rng(rows + I)
+    gu = F.bf16_round(rng.standard_normal((rows, 2 * I)) * 3)
+    gu[0, 0] = 0x0000                                  # gate 0
+    if I > 1:
+        gu[0, 1] = 0xC2C8                              # gate -100: e^-g overflows, s = 0
+    dh = F.bf16_round(rng.standard_normal((rows, I)))
+    got = u16(cuda_lib.moe_swiglu_backward(bf16_tensor(gu), bf16_tensor(dh)))
+    assert cuda_lib.nvfp4_status_check() == 0
+    ref = M.swiglu_backward(gu, dh, I)
+    for part in (slice(0, I), slice(I, 2 * I)):
+        nbad, worst = check_bf16_against(got[:, part], F.bf16_to_f32(ref[:, part]).astype(np.float64))
+        assert nbad == 0, (part, worst)
