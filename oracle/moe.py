@@ -110,6 +110,39 @@ def grouped_gemm(a_codes, a_sf, a_g, b_codes, b_sf, b_g, padded_offsets, counts)
     return out
 
 
+def expert_wgrad(dy_bits: np.ndarray, x_bits: np.ndarray, counts, rounding_dy: str = "sr", seed: int = 0):
+    """Weight gradient of every expert in W4A4: dW_e[n, h] = sum over expert e's tokens t of
+    dY[t, n] * X[t, h], with both operands quantised along the tokens (the contraction) --
+    dY_e^T and X_e^T each as one tensor (one FP32 global scale per expert matrix, blocks of
+    16 consecutive tokens), the gradient with stochastic rounding and seed ``seed + e``, the
+    activations with RNE -- and each expert's token count zero-padded to a multiple of 256
+    ([4BL] §"Why is the NVFP4 pretraining recipe not sufficient for RL?": stochastic
+    rounding for gradients; the transposed quantisation of the backward's operands).
+
+    dy_bits [T, N] and x_bits [T, H] hold the tokens grouped by expert (counts[e] rows
+    each, in order).  Returns dW [E, N, H] in float64 (the exact GEMM of the dequantised
+    operands) and the per-expert operands (codes, sf, g of dY_e^T and X_e^T)."""
+    counts = [int(c) for c in counts]
+    N, H = dy_bits.shape[1], x_bits.shape[1]
+    out = np.zeros((len(counts), N, H))
+    ops = []
+    r = 0
+    for e, n in enumerate(counts):
+        tp = max(256, (n + 255) // 256 * 256)
+        dyt = np.zeros((N, tp), np.uint16)
+        xt = np.zeros((H, tp), np.uint16)
+        dyt[:, :n] = dy_bits[r:r + n].T
+        xt[:, :n] = x_bits[r:r + n].T
+        qa = Q.quantize(dyt, scope="tensor", rounding=rounding_dy, seed=seed + e)
+        qb = Q.quantize(xt, scope="tensor")
+        a = Q.dq_unscaled(qa["codes"], qa["sf"]) * np.float64(qa["g"][0])
+        b = Q.dq_unscaled(qb["codes"], qb["sf"]) * np.float64(qb["g"][0])
+        out[e] = a @ b.T
+        ops.append((qa, qb))
+        r += n
+    return out, ops
+
+
 def gemm_rows(a_codes_rows, a_sf_rows, a_g_rows, b_codes_e, b_sf_e, b_g_e):
     """The same product for a few rows against one expert's matrix (sampled checks)."""
     A = Q.dq_unscaled(a_codes_rows, a_sf_rows)

@@ -211,6 +211,38 @@ def test_swiglu_backward_against_mpmath_derivative():
     assert (out[0, I] & 0x7FFF) == 0
 
 
+def test_expert_wgrad_brute_force_and_exact_case():
+    """Expert wgrad against a brute-force triple loop over the dequantised operands (tiny
+    sizes).  Also an exact case: E2M1 grid values times 448 * 2^-k, with every 16-token
+    block reaching 6 * 448 * 2^-k, quantise losslessly (g = 2^-k, block scales 448), so dW
+    equals the float64 product of the unquantised values."""
+    rng = np.random.default_rng(13)
+    counts = [3, 0, 17]
+    N, H = 16, 16
+    dy = F.bf16_round(rng.standard_normal((sum(counts), N)) * 1e-2)
+    x = F.bf16_round(rng.standard_normal((sum(counts), H)))
+    dw, ops = M.expert_wgrad(dy, x, counts, rounding_dy="sr", seed=4)
+    assert dw.shape == (3, N, H)
+    assert not np.any(dw[1])                            # an expert with no tokens
+    qa, qb = ops[2]
+    a = Q.dq_unscaled(qa["codes"], qa["sf"]) * qa["g"][0]
+    b = Q.dq_unscaled(qb["codes"], qb["sf"]) * qb["g"][0]
+    for n_ in range(N):
+        for h_ in range(H):
+            acc = sum(a[n_, t] * b[h_, t] for t in range(a.shape[1]))
+            assert dw[2, n_, h_] == pytest.approx(acc, rel=1e-12, abs=1e-300)
+    # exact case: one expert, 32 tokens, RNE on both operands; amax = 2688 * 2^-k makes
+    # g = 2^-k and every block scale 448, so the quantisation is lossless
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0])
+    s_dy, s_x = 448 * 2.0 ** -14, 448 * 2.0 ** -8
+    dyv = rng.choice(grid, (32, N)) * rng.choice([-1, 1], (32, N)) * s_dy
+    xv = rng.choice(grid, (32, H)) * rng.choice([-1, 1], (32, H)) * s_x
+    dyv[0::16, :] = 6 * s_dy                            # each 16-token block reaches 6 * scale
+    xv[0::16, :] = 6 * s_x
+    dw2, _ = M.expert_wgrad(F.bf16_round(dyv), F.bf16_round(xv), [32], rounding_dy="rne")
+    np.testing.assert_array_equal(dw2[0], dyv.T @ xv)
+
+
 def test_combine_against_mpmath():
     mpmath = pytest.importorskip("mpmath")
     mpmath.mp.dps = 60
