@@ -109,13 +109,14 @@ ForwardLayout forward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t
 nvfp4_status gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const uint8_t* B, const uint8_t* SFB,
                   const float* gB, const int32_t* offsets, const int32_t* rows, int64_t M_total, int64_t N, int64_t K,
                   int32_t E, void* D, int out_f32, int64_t ldd, cudaStream_t s) {
-  GemmArgs g;
+  GemmArgs g{};
   g.sfa = SFA;
   g.sfb = SFB;
   g.ga = gA;
   g.gb = gB;
   g.offsets = offsets;
   g.rows = rows;
+  g.m_total = M_total;
   g.E = E;
   g.N = (int32_t)N;
   g.K = (int32_t)K;
@@ -123,7 +124,7 @@ nvfp4_status gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const u
   g.ldd = ldd;
   g.out_f32 = out_f32;
   g.status = device_status_ptr();
-  const bool wide = n256_supported(g);   // its B map also has 128-row boxes (one per CTA of a pair)
+  const bool wide = n256_supported(g);   // its B map also has 128-row boxes (two per 256-row tile)
   CUtensorMap ma, mb, md;
   if (!make_map(&ma, A, M_total, K / 2, K / 2, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
       !make_map(&mb, B, (int64_t)E * N, K / 2, K / 2, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1))
@@ -381,6 +382,7 @@ nvfp4_status mxfp8_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const uint
   g.sfb = SFB;
   g.offsets = group_offsets;
   g.rows = group_rows;
+  g.m_total = M_total;
   g.E = E;
   g.N = (int32_t)N;
   g.K = (int32_t)K;
@@ -393,7 +395,7 @@ nvfp4_status mxfp8_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const uint
   if (!make_map(&ma, A, M_total, K, K, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1) ||
       !make_map(&mb, B, (int64_t)E * N, K, K, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1))
     return NVFP4_ERR_CUDA;
-  // N % 256 == 0: clustered 128 x 256 tiles (weight tile shared by a CTA pair); else 128 x 128
+  // N % 256 == 0: 128 x 256 tiles; else 128 x 128
   if (n256_supported(g)) return from_cuda(launch_grouped_gemm_n256_mx(ma, mb, g, M_total / 128, s));
   if (!make_map(&md, D, M_total, N, ldd * (out_f32 ? 4 : 2), 32,
                 out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_f32 ? 4 : 2))
@@ -419,6 +421,7 @@ nvfp4_status bf16_grouped_gemm(const void* A, const void* B, const int32_t* grou
   GemmArgs g{};
   g.offsets = group_offsets;
   g.rows = group_rows;
+  g.m_total = M_total;
   g.E = E;
   g.N = (int32_t)N;
   g.K = (int32_t)K;
@@ -477,6 +480,7 @@ nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A, const float* gA, const u
   g.gb = gB;
   g.offsets = group_offsets;
   g.rows = group_rows;
+  g.m_total = M_total;
   g.E = E;
   g.N = (int32_t)N;
   g.K = (int32_t)K;
@@ -676,6 +680,7 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   g1.gb = wt->w13_g;
   g1.offsets = padded;
   g1.rows = counts;
+  g1.m_total = mcap;
   g1.E = E;
   g1.N = (int32_t)(2 * I);
   g1.K = (int32_t)H;
@@ -703,6 +708,7 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   g2.gb = wt->w2_g;
   g2.offsets = padded;
   g2.rows = counts;
+  g2.m_total = mcap;
   g2.E = E;
   g2.N = (int32_t)H;
   g2.K = (int32_t)Ip;

@@ -1,18 +1,15 @@
-// W4A4 grouped GEMM, 128 x 256 output tiles, CTA pairs sharing the weight tile: the
-// same computation as grouped_gemm.cu ("Low-Bit Precision Training Is Ready for
+// W4A4 grouped GEMM with 128 x 256 output tiles over row-major operands: the same
+// computation as grouped_gemm.cu ("Low-Bit Precision Training Is Ready for
 // Production...", §"What W4A4 GEMM Actually Changes"), issued as M=128, N=256, K=64
 // block-scaled MMAs.  An N=256 instruction costs the tensor pipe about the same time as
 // an N=128 one, so this shape doubles the work per instruction; it is used whenever N is
 // a multiple of 256.
 //
-// Feeding shared memory from L2 is what limits these GEMMs, so the CTAs run in clusters
-// of two that work on two consecutive 128-row tiles of the same expert and the same 256
-// output columns: each CTA loads its own A tile and one half of the weight tile (and of
-// its scale blocks) with a multicast TMA that lands in both CTAs, which cuts the L2 reads
-// per stage from 54 KB to 36 KB.  A stage is refilled only when the MMAs of both CTAs have
-// consumed it (each MMA warp commits to the stage's "empty" barrier in both CTAs).  An
-// expert with an odd number of row tiles gives the second CTA a duplicate of the first
-// tile whose results are discarded.
+// One persistent CTA per SM; every CTA loads its own operands (TMA boxes of 128 rows:
+// one for A, two for the 256 weight rows, plus the matching scale blocks by bulk copy),
+// so no CTA ever waits on another.  Tiles are (128-row block of the padded group layout)
+// x (256 output columns), row-block-major, so CTAs running at the same time share A
+// tiles and one expert's weights in L2.
 //
 // One 256-column TMEM accumulator per CTA (the scale factors of the stages take the rest
 // of TMEM), 4 stages of 54 KB, and 8 epilogue warps (two per TMEM lane quadrant, 128
@@ -53,7 +50,6 @@ constexpr int kSFStageCols = 16 + 32;        // A: 4 x 4 columns, B: 4 x 8 colum
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxE = 512;
-constexpr uint16_t kPair = 0x3;              // both CTAs of the cluster
 
 struct Smem {
   uint8_t a[kStages][kABytes];
@@ -67,7 +63,6 @@ struct Smem {
   uint32_t tmem_base;
   int abort;
   int32_t offsets[kMaxE + 1];
-  int32_t pair_off[kMaxE + 1];               // exclusive scan of ceil(row tiles / 2) per expert
   int32_t rows[kMaxE];
   float gb[kMaxE];
 };
@@ -76,27 +71,8 @@ static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 }  // namespace g256
 
-// Tile (128 rows, 256 columns) of pair-unit u for CTA `rank` of the cluster.
-struct PairTile {
-  int e, n_tile;
-  int local;       // this CTA's row tile inside the expert's group
-  int a_tile;      // row tile whose A is loaded (the partner's for a duplicate)
-};
-
-__device__ __forceinline__ PairTile pair_tile(const g256::Smem& sm, int E, int n_tiles, int u, uint32_t rank) {
-  PairTile pt;
-  const int pu = u / n_tiles;
-  pt.n_tile = u - pu * n_tiles;
-  pt.e = find_group(sm.pair_off, E, pu);
-  const int p = pu - sm.pair_off[pt.e];
-  const int tiles_e = (sm.offsets[pt.e + 1] - sm.offsets[pt.e]) / g256::kBM;
-  pt.local = 2 * p + (int)rank;
-  pt.a_tile = sm.offsets[pt.e] / g256::kBM + (pt.local < tiles_e ? pt.local : 2 * p);
-  return pt;
-}
-
 template <bool kMX>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
+__global__ void __launch_bounds__(g256::kThreads, 1)
     grouped_gemm_n256_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                              const GemmArgs g) {
   using namespace g256;
@@ -108,18 +84,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
   for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
   for (int i = threadIdx.x; i < g.E; i += blockDim.x) {
     sm.rows[i] = g.rows[i];
     sm.gb[i] = kMX ? 1.0f : g.gb[i];
   }
+  __syncthreads();
+  if (!groups_valid(sm.offsets, sm.rows, g.E, g.m_total)) {   // nothing is read or written
+    if (threadIdx.x == 0) set_status(g.status, kStatusBadInput);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 2);          // the MMA warps of both CTAs release a stage
+      mbar_init(&sm.empty[s], 1);
     }
     mbar_init(&sm.accf, 1);
     mbar_init(&sm.acce, kEpiWarps * 32);
@@ -134,55 +113,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  __syncthreads();
-  if (warp == 0) {   // pair-unit offsets: exclusive scan of ceil(tiles_e / 2)
-    const int per = (g.E + 31) / 32;
-    const int b0 = lane * per, b1 = min(g.E, b0 + per);
-    int local = 0;
-    for (int e = b0; e < b1; ++e) local += ((sm.offsets[e + 1] - sm.offsets[e]) / kBM + 1) / 2;
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int run = incl - local;
-    for (int e = b0; e < b1; ++e) {
-      sm.pair_off[e] = run;
-      run += ((sm.offsets[e + 1] - sm.offsets[e]) / kBM + 1) / 2;
-    }
-    if (lane == 31) sm.pair_off[g.E] = incl;
-  }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();    // the partner's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
   const int n_tiles = g.N / kBN;
-  const int total = sm.pair_off[g.E] * n_tiles;
+  const int total = sm.offsets[g.E] / kBM * n_tiles;
   const int kblocks = g.K / kStageK;
   const int64_t sf_kgroups = g.K / (kMX ? 128 : 64);
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      for (int u = cl; u < total; u += ncl) {
-        const PairTile pt = pair_tile(sm, g.E, n_tiles, u, rank);
-        const int32_t row0 = pt.a_tile * kBM;
-        const int32_t brow = pt.e * g.N + pt.n_tile * kBN;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
+        const int32_t row0 = m_tile * kBM;
+        const int e = find_group(sm.offsets, g.E, row0);
+        const int32_t brow = e * g.N + n_tile * kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, g.status, abort)) goto producer_done;
           mbar_arrive_expect_tx(&sm.full[stage], kTx);
           tma_load_2d(sm.a[stage], &tma, kb * kBKBytes, row0, &sm.full[stage]);
-          tma_load_2d_mc(sm.b[stage] + rank * (kBBytes / 2), &tmb, kb * kBKBytes, brow + (int)rank * 128,
-                         &sm.full[stage], kPair);
-          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)pt.a_tile * sf_kgroups + kb * kSFTiles) * 512, kSFA,
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(sm.b[stage] + h * (kBBytes / 2), &tmb, kb * kBKBytes, brow + h * 128, &sm.full[stage]);
+          bulk_load(sm.sfa[stage], g.sfa + ((int64_t)m_tile * sf_kgroups + kb * kSFTiles) * 512, kSFA,
                     &sm.full[stage]);
-          bulk_load_mc(sm.sfb[stage] + rank * kSFB128,
-                       g.sfb + ((int64_t)(brow / 128 + (int)rank) * sf_kgroups + kb * kSFTiles) * 512, kSFB128,
-                       &sm.full[stage], kPair);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            bulk_load(sm.sfb[stage] + h * kSFB128,
+                      g.sfb + ((int64_t)(brow / 128 + h) * sf_kgroups + kb * kSFTiles) * 512, kSFB128,
+                      &sm.full[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -196,7 +159,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
       constexpr uint32_t idesc = kMX ? idesc_mxf8(kBM, kBN, 0) : idesc_nvf4(kBM, kBN);
       uint32_t stage = 0, phase = 0;
       int it = 0;
-      for (int u = cl; u < total; u += ncl, ++it) {
+      for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&sm.full[stage], phase, g.status, abort)) goto mma_done;
           tc_fence_after();
@@ -240,7 +203,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
               tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
             }
           }
-          tc_commit_mc(&sm.empty[stage], kPair);
+          tc_commit(&sm.empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -256,12 +219,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
     const int half = (warp - 2) >> 2;
     const int elt = g.out_f32 ? 4 : 2;
     int it = 0;
-    for (int u = cl; u < total; u += ncl, ++it) {
-      const PairTile pt = pair_tile(sm, g.E, n_tiles, u, rank);
-      const int e = pt.e;
-      const int32_t in_group = sm.rows[e] - pt.local * kBM;   // <= 0 for a duplicate tile
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
+      const int32_t row0 = m_tile * kBM;
+      const int e = find_group(sm.offsets, g.E, row0);
+      const int32_t in_group = sm.rows[e] - (row0 - sm.offsets[e]);   // valid rows of this tile
       const bool valid = q * 32 + lane < in_group;
-      const int64_t row = (int64_t)sm.offsets[e] + pt.local * kBM + q * 32 + lane;
+      const int64_t row = (int64_t)row0 + q * 32 + lane;
       const float ga = kMX ? 1.0f : (valid ? g.ga[row] : 0.0f);
       if (!mbar_wait(&sm.accf, it & 1, g.status, abort)) break;
       tc_fence_after();
@@ -274,7 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&sm.acce);
       if (valid) {
-        uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + (int64_t)pt.n_tile * kBN + half * 128) * elt;
+        uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + (int64_t)n_tile * kBN + half * 128) * elt;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (g.out_f32) {
@@ -306,7 +270,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g256::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();    // no multicast or remote arrive may target a CTA that has exited
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -316,20 +279,13 @@ bool n256_supported(const GemmArgs& g) { return g.N % g256::kBN == 0 && g.E <= g
 template <bool kMX>
 static cudaError_t launch_n256(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
                                int64_t max_m_tiles, cudaStream_t s) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_n256_kernel<kMX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)g256::kSmemBytes);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
-  const int64_t units = (max_m_tiles + g.E + 1) / 2 * (g.N / g256::kBN);   // bound on pair units
-  if (max_m_tiles == 0) return cudaSuccess;
-  int64_t clusters = num_sms() / 2;
-  if (units < clusters) clusters = units;
-  const int grid = (int)(2 * clusters);
+  static std::atomic<bool> attr_set[64];
+  cudaError_t err = set_smem_attr_once(attr_set, (const void*)grouped_gemm_n256_kernel<kMX>, (int)g256::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int64_t tiles = max_m_tiles * (g.N / g256::kBN);
+  if (tiles == 0) return cudaSuccess;
+  int grid = num_sms();
+  if (tiles < grid) grid = (int)tiles;
   grouped_gemm_n256_kernel<kMX><<<grid, g256::kThreads, g256::kSmemBytes, s>>>(tma, tmb, g);
   return cudaGetLastError();
 }

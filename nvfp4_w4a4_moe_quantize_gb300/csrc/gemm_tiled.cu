@@ -116,6 +116,11 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
     sm.rows[i] = g.rows[i];
     sm.gb[i] = g.gb[i];
   }
+  __syncthreads();
+  if (!groups_valid(sm.offsets, sm.rows, g.E, g.m_total)) {   // nothing is read or written
+    if (threadIdx.x == 0) set_status(g.status, kStatusBadInput);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 2);            // the A and the B producer arrive
@@ -432,15 +437,9 @@ template <bool kSwiGLU>
 static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
                                 int64_t max_m_tiles, cudaStream_t s) {
   if (kSwiGLU && g.silu_tab == nullptr) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tiled_kernel<kSwiGLU>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gt::kSmemBytes);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[64];   // the attribute is set once per device
+  cudaError_t err = set_smem_attr_once(attr_set, (const void*)grouped_gemm_tiled_kernel<kSwiGLU>, (int)gt::kSmemBytes);
+  if (err != cudaSuccess) return err;
   const int64_t tiles = max_m_tiles * (g.N / gt::kBN);
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();

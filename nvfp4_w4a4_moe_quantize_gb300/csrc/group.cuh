@@ -15,4 +15,19 @@ __device__ __forceinline__ int find_group(const int32_t* off, int E, int32_t row
   return lo;
 }
 
+// Checks the group arrays of a grouped GEMM (already in shared memory) before any tile
+// is touched: offsets[0..E] non-decreasing multiples of 128 starting at >= 0 with
+// offsets[E] <= m_total, and 0 <= rows[e] <= offsets[e+1] - offsets[e].  Every thread of
+// the block must call it (it ends with a block-wide vote); the result is the same in all
+// of them.
+__device__ __forceinline__ bool groups_valid(const int32_t* off, const int32_t* rows, int E, int64_t m_total) {
+  int bad = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    const int32_t a = off[i], b = off[i + 1], r = rows[i];
+    if (a < 0 || (a & 127) != 0 || b < a || (b & 127) != 0 || r < 0 || r > b - a) bad = 1;
+  }
+  if (threadIdx.x == 0 && (E < 1 || (int64_t)off[E] > m_total)) bad = 1;
+  return __syncthreads_or(bad) == 0;
+}
+
 }  // namespace nvfp4

@@ -107,6 +107,11 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
     sm.rows[i] = g.rows[i];
     sm.gb[i] = kFmt != kGemmNVF4 ? 1.0f : g.gb[i];
   }
+  __syncthreads();
+  if (!groups_valid(sm.offsets, sm.rows, g.E, g.m_total)) {   // nothing is read or written
+    if (threadIdx.x == 0) set_status(g.status, kStatusBadInput);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -332,15 +337,9 @@ __global__ void __launch_bounds__(gg::kThreads, 1)
 template <int kFmt>
 static cudaError_t launch_gg(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,
                              const GemmArgs& g, int64_t max_m_tiles, cudaStream_t s) {
-  static bool attr_set[64] = {};   // the attribute is set once per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)gg::kSmemBytes);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[64];   // the attribute is set once per device
+  cudaError_t err = set_smem_attr_once(attr_set, (const void*)grouped_gemm_kernel<kFmt>, (int)gg::kSmemBytes);
+  if (err != cudaSuccess) return err;
   const int64_t tiles = max_m_tiles * (g.N / gg::kBN);
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();

@@ -1,5 +1,6 @@
 // Internal launch interface between the C ABI (api.cu) and the kernel files.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,6 +45,7 @@ struct GemmArgs {
   const float* gb;         // [E]
   const int32_t* offsets;  // [E+1] padded group starts
   const int32_t* rows;     // [E] valid rows per group
+  int64_t m_total;         // rows of A, D (and ga): every group must lie inside [0, m_total)
   int32_t E;
   int32_t N, K;
   void* d;
@@ -63,17 +65,29 @@ const void* silu_table(cudaStream_t s);
 int num_sms();
 int* device_status_ptr();
 
+// Sets a kernel's dynamic shared-memory limit once per device (flags: one per device,
+// 64 devices).  Concurrent first calls may both set it, which is harmless.
+inline cudaError_t set_smem_attr_once(std::atomic<bool>* flags, const void* func, int bytes) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && flags[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess && cached) flags[dev].store(true, std::memory_order_release);
+  return err;
+}
+
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t group_rows,
                         uint32_t* amax_bits, int64_t n_scopes, cudaStream_t s);
 cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s);
 
 // Grouped GEMM: tensor maps are built by the caller (api.cu), all with 128-row boxes.
-// The clustered 128 x 256 tile kernel serves N % 256 == 0 and E <= 512; the 128 x 128
+// The 128 x 256 tile kernel serves N % 256 == 0 and E <= 512; the 128 x 128
 // kernel serves the rest.
 bool n256_supported(const GemmArgs& g);
 cudaError_t launch_grouped_gemm_n256(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
                                      int64_t max_m_tiles, cudaStream_t s);
-// MXFP8 operands on the clustered 128 x 256 tile kernel (N % 256 == 0, E <= 512).
+// MXFP8 operands on the 128 x 256 tile kernel (N % 256 == 0, E <= 512).
 cudaError_t launch_grouped_gemm_n256_mx(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmArgs& g,
                                         int64_t max_m_tiles, cudaStream_t s);
 cudaError_t launch_grouped_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmd,

@@ -613,14 +613,10 @@ static cudaError_t launch_quant_rnd(const QuantArgs& a, int maxc, int grid, cuda
 
 template <int RND>
 static cudaError_t launch_stream(const QuantArgs& a, int grid, size_t smem, cudaStream_t s) {
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(quantize_rows_stream_kernel<RND>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmemMax + 4096);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr[dev] = true;
+  static std::atomic<bool> attr_set[64];   // the attribute is set once per device
+  {
+    const cudaError_t err = set_smem_attr_once(attr_set, (const void*)quantize_rows_stream_kernel<RND>, (int)kQSmemMax + 4096);
+    if (err != cudaSuccess) return err;
   }
   quantize_rows_stream_kernel<RND><<<grid, kQWarps * 32, smem, s>>>(a);
   return cudaGetLastError();

@@ -117,13 +117,10 @@ cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const in
   constexpr int kSmem = 128 * 144;
   const int64_t chunks = max_rows / 128 * (K / 256);
   if (chunks == 0) return cudaSuccess;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(gather_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  static std::atomic<bool> attr_set[64];   // the attribute is set once per device
+  {
+    const cudaError_t err = set_smem_attr_once(attr_set, (const void*)gather_tiled_kernel, kSmem);
     if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   // one warp per block and one 18 KB chunk image per warp: 12 per SM fit in shared memory
   int64_t blocks = chunks;

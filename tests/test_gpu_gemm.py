@@ -242,3 +242,41 @@ def test_tiled_swiglu_epilogue_equals_standalone_swiglu(cuda_lib):
     np.testing.assert_array_equal(h_fused[rows], M.swiglu(d_can, I))
     gate = F.bf16_to_f32(d_can[:, :I])
     assert (gate < -80).sum() > 2000            # the exact path did run, many per row
+
+
+@pytest.mark.parametrize("N", [128, 256])
+@pytest.mark.parametrize("fault", ["rows_over_span", "offsets_past_m_total", "unaligned_offset"])
+def test_gemm_rejects_inconsistent_group_arrays(cuda_lib, N, fault):
+    """Group arrays that break the documented contract (rows[e] larger than its padded
+    span, offsets past M_total, a start that is not a multiple of 128) set the device
+    status and leave D untouched, on both tile widths and on the GEMM-tiled kernel."""
+    E, K = 2, 256
+    counts = [100, 60]
+    a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=51))
+    w_bits = S.bf16_bits(S.randn_bf16((E, N, K), 0.02, seed=52))
+    ops = _operands_from_oracle(a_bits, counts, w_bits)
+    rows, padded = ops["counts"].copy(), ops["padded"].copy()
+    if fault == "rows_over_span":
+        rows[0] = 129
+    elif fault == "offsets_past_m_total":
+        padded[-1] = ops["M"] + 128
+    else:
+        padded[1] = 64
+    A = dev(F.pack_e2m1(ops["a_codes"]))
+    SFA = dev(F.sf_swizzle(ops["a_sf"]))
+    B = dev(F.pack_e2m1(ops["b_codes"].reshape(E * N, K)))
+    SFB = dev(F.sf_swizzle(ops["b_sf"].reshape(E * N, K // 16)))
+    sentinel = torch.full((ops["M"], N), 7.0, dtype=torch.float32, device="cuda")
+    D = sentinel.clone()
+    cuda_lib.nvfp4_grouped_gemm(A, SFA, dev(ops["a_g"]), B, SFB, dev(ops["b_g"]), dev(padded), dev(rows), N, K, E,
+                                out=D)
+    assert cuda_lib.nvfp4_status_check() == cuda_lib.Status.DEVICE_STATUS
+    assert torch.equal(D, sentinel)
+    if N == 256:
+        At = cuda_lib.nvfp4_pack_tiled(A, SFA, ops["M"], K, 128)
+        Bt = cuda_lib.nvfp4_pack_tiled(B, SFB, E * N, K, 256)
+        D2 = sentinel.clone()
+        cuda_lib.nvfp4_grouped_gemm_tiled(At, dev(ops["a_g"]), Bt, dev(ops["b_g"]), dev(padded), dev(rows),
+                                          ops["M"], N, K, E, out=D2)
+        assert cuda_lib.nvfp4_status_check() == cuda_lib.Status.DEVICE_STATUS
+        assert torch.equal(D2, sentinel)
