@@ -78,6 +78,60 @@ def e2m1_encode_sr(v, r16) -> np.ndarray:
     return (code | (sign << 3)).astype(np.uint8)
 
 
+# Midpoints between neighbouring E2M1 magnitudes: m_i separates code i from code i + 1.
+E2M1_MIDPOINTS = (E2M1_MAGNITUDES[:-1] + E2M1_MAGNITUDES[1:]) / 2      # 0.25, 0.75, ..., 5
+
+
+def e2m1_round_quotient(x, s) -> np.ndarray:
+    """E2M1 code of round(x / s): [4BL] footnote 6's clip(round(w / s), -6, 6) with the
+    quotient taken exactly, ties to the even code, saturating at 6.
+
+    ``x`` holds float32 values (here BF16 inputs), ``s`` float32 scales > 0, both given as
+    float64 (broadcastable).  The quotient is never formed: |x| / s > m holds exactly when
+    |x| > m * s, and every product m * s of a midpoint (at most 3 significant bits) with
+    a float32 scale (24 bits) is exact in float64, so each comparison is exact.  The
+    magnitude code is the number of midpoints strictly below |x| / s; at a midpoint
+    itself (|x| == m_i * s) the tie goes to the even code of i and i + 1.  Zero
+    magnitude encodes as +0 (the reading of ``e2m1_encode_rne``).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    s = np.asarray(s, dtype=np.float64)
+    a = np.abs(x)
+    code = np.zeros(np.broadcast(a, s).shape, dtype=np.int64)
+    for i, m in enumerate(E2M1_MIDPOINTS):
+        t = m * s                                  # exact
+        code += a > t
+        if i % 2 == 1:                             # tie between odd i and even i + 1: round up
+            code += a == t
+    sign = (np.signbit(x) & (code != 0)).astype(np.int64)
+    return (code | (sign << 3)).astype(np.uint8)
+
+
+def e2m1_sr_quotient(x, s, r16) -> np.ndarray:
+    """Stochastic rounding of the exact quotient q = |x| / s to E2M1 (the rule of
+    ``e2m1_encode_sr`` applied to q instead of a rounded float32 value).
+
+    With lo <= q < hi the neighbouring magnitudes and p = (q - lo) / (hi - lo), q rounds
+    up iff r16 < p * 2^16, i.e. iff |x| > (lo + r16 * (hi - lo) / 2^16) * s.  That
+    threshold has at most 19 significant bits and s 24, so the product is exact in
+    float64; lo itself is found exactly as the largest magnitude G with G * s <= |x|.
+    q >= 6 saturates at 6.  Zero magnitude encodes as +0.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    s = np.asarray(s, dtype=np.float64)
+    r16 = np.asarray(r16, dtype=np.float64)
+    a = np.abs(x)
+    lo = np.zeros(np.broadcast(a, s, r16).shape, dtype=np.int64)
+    for j in range(1, 8):
+        lo += a >= E2M1_MAGNITUDES[j] * s           # exact: G has at most 2 significant bits
+    hi = np.minimum(lo + 1, 7)
+    gap = E2M1_MAGNITUDES[hi] - E2M1_MAGNITUDES[lo]
+    thresh = (E2M1_MAGNITUDES[lo] + r16 * gap / 65536.0) * s     # exact
+    code = np.where(lo >= 7, 7, lo + (a > thresh))
+    sign = (np.signbit(x) & (code != 0)).astype(np.int64)
+    return (code | (sign << 3)).astype(np.uint8)
+
+
 def pack_e2m1(codes: np.ndarray) -> np.ndarray:
     """Pack codes [..., 2n] into bytes [..., n]: element 2i in the low nibble, 2i+1 in the
     high nibble (reading: the pages do not give a packing)."""

@@ -11,9 +11,9 @@ scale per block of 16 consecutive values along the last (contraction) dimension,
   across the hidden dimension"), which keeps a token's codes independent of the rest
   of the batch.
 
-Scale arithmetic (reading: the pages fix the formats, not the arithmetic).  All steps
-are single IEEE float32 operations, round to nearest even, in this order, so that a
-second implementation reproduces every code bit for bit:
+Scale arithmetic (reading: the pages fix the formats, not the arithmetic).  The scale
+steps are single IEEE float32 operations, round to nearest even, in this order, so that
+a second implementation reproduces every scale bit for bit:
 
     amax   = max |x| over the scope                        (exact)
     g      = amax / 2688                                    2688 = 6 * 448; g is the
@@ -21,14 +21,15 @@ second implementation reproduces every code bit for bit:
     per block b of 16 values, amax_b = max |x| over b:
     sf_b   = E4M3_rne_satfinite( amax_b / (6 * g) )         the block scale byte
     s_b    = decode(sf_b) * g                               effective decode scale
-    r_b    = 1 / s_b                                        encode multiplier
-    code   = E2M1( x * r_b )                                RNE or stochastic
 
-so that the dequantised value is DQ(code) = value(code) * decode(sf_b) * g, and the code
-is [4BL] footnote 6's clip(round(x / s), -6, 6) with the division done as a
-multiplication by the block's reciprocal scale.  Degenerate cases: g == 0 (an all-zero
-scope), s_b == 0 or a non-finite r_b (scales below 2^-128) give sf_b and codes that
-decode to zero for the block (sf_b is still the encoded t when g > 0).
+and each element's code is [4BL] footnote 6's Q = clip(round(x / s_b), -6, 6) on the E2M1
+grid with the quotient x / s_b taken exactly (round to nearest, ties to the even code,
+or stochastic rounding), so that DQ(code) = value(code) * decode(sf_b) * g.  The exact
+quotient is decided by comparisons in float64 (formats.e2m1_round_quotient /
+e2m1_sr_quotient), never by a rounded float32 quotient or reciprocal.  Degenerate
+cases: g == 0 (an all-zero scope) gives sf_b = 0 and zero codes; s_b == 0 (a block
+scale that encodes or multiplies out to zero) gives zero codes, sf_b still the encoded
+byte when g > 0.
 """
 from __future__ import annotations
 
@@ -70,19 +71,17 @@ def quantize_rows(x32: np.ndarray, g_rows: np.ndarray, rounding: str = "rne",
     t = t.astype(np.float32)
     sf = F.e4m3_encode_rne_satfinite(t)
     s = (F.e4m3_decode(sf).astype(np.float32) * g).astype(np.float32)  # exact decode, fp32 mul
-    with np.errstate(divide="ignore", over="ignore"):
-        r = np.where(s > 0, np.float32(1.0) / np.where(s > 0, s, np.float32(1)), np.float32(0))
-    r = r.astype(np.float32)
-    live = (s > 0) & np.isfinite(r)                                       # [rows, nb]
-    v = (xb * np.where(live, r, np.float32(0))[:, :, None]).astype(np.float32)
+    live = s > 0                                                          # [rows, nb]
+    x64 = xb.astype(np.float64)
+    s64 = np.where(live, s, np.float32(1)).astype(np.float64)[:, :, None]
     if rounding == "rne":
-        codes = F.e2m1_encode_rne(v)
+        codes = F.e2m1_round_quotient(x64, s64)
     elif rounding == "sr":
         tc = cols if total_cols is None else total_cols
         idx = (np.arange(rows, dtype=np.uint64)[:, None] + np.uint64(row_base)) * np.uint64(tc) \
             + np.arange(cols, dtype=np.uint64)[None, :]
         r16 = philox.sr_bits16(idx, seed, rng_offset).reshape(rows, nb, BLOCK)
-        codes = F.e2m1_encode_sr(v, r16)
+        codes = F.e2m1_sr_quotient(x64, s64, r16)
     else:
         raise ValueError(rounding)
     codes = np.where(live[:, :, None], codes, np.uint8(0)).astype(np.uint8)

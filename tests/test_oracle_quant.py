@@ -94,11 +94,16 @@ def test_zero_and_tiny_scopes():
     z = np.zeros((2, 32), np.uint16)
     q = Q.quantize(z, scope="row")
     assert not q["codes"].any() and not q["sf"].any() and not q["g"].any()
-    # a row of the smallest BF16 subnormals: g and the scales underflow, codes decode to 0
+    # a row of the smallest BF16 subnormals (2^-133): g = fl32(2^-133 / 2688) is the
+    # float32 subnormal 24 * 2^-149, t = 2^-133 / (6 g) = 455.1 saturates to sf = 448, and
+    # s = 448 g = 10752 * 2^-149 exactly; x / s = 65536 / 10752 = 6.095 rounds to 6
     tiny = np.full((1, 32), 0x0001, np.uint16)
     q = Q.quantize(tiny, scope="row")
+    assert q["g"][0] == np.float32(24 * 2.0 ** -149)
+    assert np.all(q["sf"] == 0x7E)
+    assert np.all(q["codes"] == 7)
     dq = Q.dequantize(q["codes"], q["sf"], q["g"])
-    assert np.all(np.isfinite(dq))
+    assert np.all(dq == 6 * 448 * 24 * 2.0 ** -149)
 
 
 def test_sr_outputs_are_neighbours_and_grid_values_stay():
@@ -135,7 +140,7 @@ def test_sr_is_unbiased():
     mean = acc / n
     var = acc2 / n - mean ** 2
     sigma = np.sqrt(np.maximum(var, 1e-30) / n)
-    # E[DQ] = s_b * (x * fl(1/s_b)) up to the 2^-16 threshold granularity
+    # E[DQ] = x up to the 2^-16 threshold granularity
     assert np.all(np.abs(mean - x32) <= 4 * sigma + 1e-4 * np.abs(x32))
 
 
@@ -145,3 +150,118 @@ def test_rne_sr_differ_only_in_rounding():
     b = Q.quantize(bits, scope="row", rounding="sr", seed=3)
     assert np.array_equal(a["sf"], b["sf"]) and np.array_equal(a["g"], b["g"])
     assert not np.array_equal(a["codes"], b["codes"])
+
+
+# --------------------------------------------------------------------------- exact quotient
+# [4BL] footnote 6: Q = clip(round(w / s), qmin, qmax).  The pins below compute round(x / s)
+# with exact rational arithmetic (fractions.Fraction), independently of the oracle's
+# float64 comparisons, on the inputs where a rounded quotient would decide differently.
+
+import math  # noqa: E402
+from fractions import Fraction  # noqa: E402
+
+_GRID = [Fraction(v) for v in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+
+
+def _round_rational(q: Fraction) -> int:
+    """Magnitude code of round(q) on the E2M1 grid, ties to the even code, clip at 6."""
+    if q >= 6:
+        return 7
+    lo = max(i for i in range(8) if _GRID[i] <= q)
+    if _GRID[lo] == q:
+        return lo
+    hi = lo + 1
+    d_lo, d_hi = q - _GRID[lo], _GRID[hi] - q
+    if d_lo != d_hi:
+        return lo if d_lo < d_hi else hi
+    return lo if lo % 2 == 0 else hi
+
+
+def _scales(q):
+    """Effective decode scale s_b = decode(sf_b) * g of every element, float32 (the
+    oracle's own scale steps are pinned separately by the worked example)."""
+    rows = q["codes"].shape[0]
+    g = np.broadcast_to(np.asarray(q["g"], np.float32), (rows,)) if q["g"].size == 1 else q["g"]
+    return np.repeat((F.e4m3_decode(q["sf"]).astype(np.float32) * g[:, None]).astype(np.float32), 16, axis=1)
+
+
+def test_round_of_exact_quotient_at_structured_near_ties():
+    """N(0,1) rows, row scope: g = amax / 2688 is rounded, so x / s lands within an ulp of
+    an E2M1 midpoint for many x that share digits with the row max.  Every element on
+    which the float32 reciprocal product fl(x * fl(1/s)) or the float32 quotient fl(x / s)
+    rounds differently from the exact quotient, plus a random sample, must get the code
+    of the exact rational round(x / s)."""
+    rng = np.random.default_rng(0)
+    bits = F.bf16_round(rng.standard_normal((1500, 2048)))
+    q = Q.quantize(bits, scope="row")
+    x = F.bf16_to_f32(bits)
+    s = _scales(q)
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        v_rcp = (x * (np.float32(1) / s).astype(np.float32)).astype(np.float32)
+        v_div = (x / s).astype(np.float32)
+    suspects = np.flatnonzero((F.e2m1_encode_rne(v_rcp) != q["codes"]).ravel() |
+                              (F.e2m1_encode_rne(v_div) != q["codes"]).ravel())
+    assert suspects.size > 100          # the structured near-ties are there
+    sample = rng.choice(x.size, 3000, replace=False)
+    for i in np.concatenate([suspects, sample]):
+        xv, sv = Fraction(float(x.flat[i])), Fraction(float(s.flat[i]))
+        mag = _round_rational(abs(xv) / sv)
+        want = mag | (8 if (xv < 0 and mag) else 0)
+        assert q["codes"].flat[i] == want, (i, float(x.flat[i]), float(s.flat[i]))
+
+
+def test_round_of_exact_quotient_hand_case():
+    """A row with max 3.34375 gives g = fl32(3.34375 / 2688), rounded up.  The block holding
+    1.4296875 gets sf = 192 (0x74), so s = 192 g and x = 0.8359375 = 3.34375 / 4 has
+    x / s = 3.5 / (1 + d) with d > 0, just below the midpoint 3.5: the code is 5 (3.0),
+    not the 6 (4.0) that a tie-to-even at a rounded 3.5 would give."""
+    row = np.zeros(32, np.float64)
+    row[0] = 3.34375
+    row[16] = 1.4296875
+    row[17] = 0.8359375
+    q = Q.quantize(F.bf16_round(row[None, :]), scope="row")
+    g = np.float32(np.float32(3.34375) / np.float32(2688))
+    assert q["g"][0] == g and Fraction(float(g)) > Fraction(3.34375) / 2688
+    assert q["sf"][0, 1] == 0x74
+    s = Fraction(float(np.float32(np.float32(192) * g)))
+    assert Fraction(0.8359375) / s < Fraction(7, 2)
+    assert q["codes"][0, 17] == 5
+
+
+def test_rne_exact_ties_go_to_even():
+    """Quotients that are exact midpoints (x = m * s with s a power of two times an odd
+    number) round to the even code; one BF16 ulp either side rounds away from the tie."""
+    s = np.float32(0.375)                       # 3 * 2^-3
+    for m, tie_code in [(0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6)]:
+        x = m * float(s)
+        xb = F.bf16_round(np.array([x]))
+        assert F.bf16_to_f32(xb)[0] == x        # representable
+        assert F.e2m1_round_quotient(np.array([x]), float(s))[0] == tie_code
+        assert F.e2m1_round_quotient(np.array([-x]), float(s))[0] == (tie_code | 8 if tie_code else 0)
+        up = float(F.bf16_to_f32(xb + np.uint16(1))[0])
+        dn = float(F.bf16_to_f32(xb - np.uint16(1))[0])
+        assert F.e2m1_round_quotient(np.array([up]), float(s))[0] == _round_rational(Fraction(up) / Fraction(float(s)))
+        assert F.e2m1_round_quotient(np.array([dn]), float(s))[0] == _round_rational(Fraction(dn) / Fraction(float(s)))
+
+
+@pytest.mark.parametrize("x, s", [(0.8359375, 0.2388393), (1.3, 0.7), (0.11, 0.3), (5.9, 1.0), (2.0, 1.0),
+                                  (0.7421875, 0.125 * 3), (4.5, 0.8)])
+def test_sr_rounds_up_for_exactly_ceil_p_of_the_2_16_draws(x, s):
+    """Stochastic rounding over all 65,536 values of the 16 random bits: the number that
+    round up is ceil(p * 2^16) with p = (q - lo) / (hi - lo) of the exact quotient q = x / s
+    (rational arithmetic), and every result is lo or hi."""
+    xs = float(F.bf16_to_f32(F.bf16_round(np.array([x])))[0])
+    ss = float(np.float32(s))
+    r16 = np.arange(65536)
+    codes = F.e2m1_sr_quotient(np.full(65536, xs), ss, r16)
+    q = Fraction(xs) / Fraction(ss)
+    lo = max(i for i in range(8) if _GRID[i] <= min(q, Fraction(6)))
+    if lo == 7:
+        assert np.all(codes == 7)
+        return
+    p = (q - _GRID[lo]) / (_GRID[lo + 1] - _GRID[lo])
+    n_up = int(np.sum(codes == lo + 1))
+    assert n_up == math.ceil(p * 65536)
+    assert np.all((codes == lo) | (codes == lo + 1))
+    # the draws that round up are exactly the smallest ones
+    assert np.all(codes[:n_up] == lo + 1) and np.all(codes[n_up:] == lo)
