@@ -39,4 +39,4 @@ fixed by the format definitions, closed forms, brute force or an independent
 high-precision library (see tests/test_oracle_*.py); none is "parity unpinned".
 """
 
-from . import formats, philox, quant, moe, mx  # noqa: F401
+from . import formats, philox, quant, moe, mx, backward  # noqa: F401
