@@ -413,6 +413,54 @@ def run_ours(args, rank, world, local_rank):
                                    "frac_of_measured_bf16": round(bf16_tflops / bf16_peak, 4)}}
     del wdqt, dgu, dx
 
+    # ---------------------------------------------------------------- learner step (forward + W4A4 backward)
+    # The learner-step expert GEMMs: T=32768 tokens, uniform routing (i.i.d. N(0,1) logits),
+    # top-8 of 128 experts, dOut ~ N(0, 1e-3): routing + forward + the W4A4 backward (dgrad
+    # and wgrad of both projections, stochastic rounding on gradients).  Algorithmic work:
+    # 3 x the forward's 2 * T*k * (2I*H + H*I) flops (the backward's recomputation of the
+    # gate/up output is not counted).
+    lshape = S.WORKLOADS["learner"]
+    lx_h, llog_h, _, _ = S.moe_inputs(lshape, seed=0)
+    lx, llog = lx_h.to(dev), llog_h.to(dev)
+    ldout = S.randn_bf16((lshape.T, H), 1e-3, 9).to(dev)
+    pt = L.moe_prepare_weights_backward(w13_h.to(dev), w2_h.to(dev))
+    lids = torch.empty(lshape.T, k, dtype=torch.int32, device=dev)
+    lwts = torch.empty(lshape.T, k, dtype=torch.float32, device=dev)
+    lout = torch.empty(lshape.T, H, dtype=torch.bfloat16, device=dev)
+    lfws = L.moe_forward_workspace(lshape.T, k, pw, dev)
+    lbws = L.moe_backward_workspace(lshape.T, k, pw, dev)
+    lgrads = (torch.empty(lshape.T, H, dtype=torch.bfloat16, device=dev),
+              torch.empty(lshape.T, k, dtype=torch.float32, device=dev),
+              torch.empty(E, 2 * I, H, dtype=torch.float32, device=dev),
+              torch.empty(E, H, I, dtype=torch.float32, device=dev))
+
+    def learner_fwd():
+        L.moe_route_topk(llog, k, True, out=(lids, lwts))
+        L.moe_expert_forward(lx, lids, lwts, pw, out=lout, workspace=lfws)
+
+    def learner_bwd():
+        L.moe_expert_backward(ldout, lx, lwts, pw, pt, lfws, seed=7, out=lgrads, workspace=lbws)
+
+    def learner_step():
+        learner_fwd()
+        learner_bwd()
+
+    l_iters = 5
+    lt = time_launches_median(learner_step, l_iters, flush, stream)
+    lf = time_launches_median(learner_fwd, l_iters, flush, stream)
+    learner_fwd()
+    lb = time_launches_median(learner_bwd, l_iters, flush, stream)
+    assert L.nvfp4_status_check() == 0
+    l_fwd_flops = 2.0 * lshape.T * k * (2 * I * H + H * I)
+    l_tflops = 3 * l_fwd_flops / (lt * 1e-3) / 1e12
+    learner = {"timing": f"median of {l_iters} launches, L2 flushed before each",
+               "workload": "learner step: T=32768, hidden 2048, intermediate 768, 128 experts, top-8, uniform "
+                           "routing; routing + W4A4 forward + W4A4 backward (dgrad and wgrad, SR on gradients)",
+               "algorithmic_tflop": round(3 * l_fwd_flops / 1e12, 3), "ms": round(lt, 4),
+               "fwd_ms": round(lf, 4), "bwd_ms": round(lb, 4), "tflops": round(l_tflops, 1),
+               "frac_of_9pf": round(l_tflops / PF_TARGET, 4), "tokens_per_s": round(lshape.T / (lt * 1e-3), 1)}
+    del lfws, lbws, lgrads, pt, lx, llog, ldout, lout
+
     # ---------------------------------------------------------------- end to end (host buffers)
     # Every step copies its inputs (x, router logits) from pinned host memory and reads its
     # result back.  Serial: copy in, compute, copy out on one stream.  Pipelined (the
@@ -500,6 +548,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps, "stages_ms": {k_: round(v_, 4) for k_, v_ in stages.items()},
         "grouped_gemm": grouped, "quantiser": quant, "mxfp8": mxfp8, "dequantised_backward": dqbwd,
+        "learner_step": learner,
         "wall_s_timed": round(wall_s, 3),
     }
     return line
@@ -549,9 +598,29 @@ def run_profile(args):
     T, H, I, E, k = args.tokens, shape.H, shape.I, shape.E, shape.k
     if args.profile == "quantiser":
         qx = S.outlier_channels_bf16(T, H, seed=0).to(dev)
+        mode = {"tensor": L.SCALE_PER_TENSOR, "row": L.SCALE_PER_ROW}[args.quant_scope]
+        rnd = L.ROUND_STOCHASTIC if args.quant_sr else L.ROUND_RNE
         for _ in range(args.steps):
-            L.nvfp4_quantize(qx, L.SCALE_PER_TENSOR, L.ROUND_RNE)
+            L.nvfp4_quantize(qx, mode, rnd)
         torch.cuda.synchronize()
+        return
+    if args.profile == "backward":     # forward + W4A4 backward over --tokens tokens (uniform routing)
+        bx = S.randn_bf16((T, H), 1.0, 1).to(dev)
+        blog = S.router_logits_normal(T, E, 2).to(dev)
+        bw13 = S.randn_bf16((E, 2 * I, H), 0.02, 3).to(dev)
+        bw2 = S.randn_bf16((E, H, I), 0.02, 4).to(dev)
+        bpw = L.moe_prepare_weights(bw13, bw2)
+        bpt = L.moe_prepare_weights_backward(bw13, bw2)
+        del bw13, bw2
+        bids, bwts = L.moe_route_topk(blog, k)
+        bfws = L.moe_forward_workspace(T, k, bpw, dev)
+        bbws = L.moe_backward_workspace(T, k, bpw, dev)
+        bdout = S.randn_bf16((T, H), 1e-3, 9).to(dev)
+        for _ in range(args.steps):
+            L.moe_expert_forward(bx, bids, bwts, bpw, workspace=bfws)
+            L.moe_expert_backward(bdout, bx, bwts, bpw, bpt, bfws, seed=7, workspace=bbws)
+        torch.cuda.synchronize()
+        assert L.nvfp4_status_check() == 0
         return
     if args.profile == "mxgemm":       # MXFP8 grouped GEMM on the routed groups of --tokens tokens
         glog = S.router_logits_zipf(T, E, shape.zipf_s, 2).to(dev)
@@ -651,9 +720,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens-per-step", type=int, default=2)
-    ap.add_argument("--profile", choices=["none", "gateup", "quantiser", "forward", "mxgemm"], default="none",
+    ap.add_argument("--profile", choices=["none", "gateup", "quantiser", "forward", "mxgemm", "backward"],
+                    default="none",
                     help="run only a short launch sequence of one kernel (for ncu captures)")
     ap.add_argument("--tokens", type=int, default=2048, help="tokens (rows) of the --profile case")
+    ap.add_argument("--quant-scope", choices=["tensor", "row"], default="tensor",
+                    help="scale scope of the --profile quantiser case")
+    ap.add_argument("--quant-sr", action="store_true", help="stochastic rounding in the --profile quantiser case")
     args = ap.parse_args()
     if args.profile != "none":
         run_profile(args)

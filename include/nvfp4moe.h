@@ -31,8 +31,11 @@
  *           padded to a multiple of 128 (size nvfp4_sf_bytes(rows, cols)).
  *   global scale g (decode direction): DQ(x) = value(code) * decode(sf) * g.
  * Scale arithmetic, every step one float32 operation rounded to nearest even:
- *   g = amax/2688; sf = E4M3_rn_satfinite(amax_block / (6*g)); s = decode(sf)*g;
- *   code = E2M1(x * (1/s)), zero magnitudes encoded as +0.
+ *   g = amax/2688; sf = E4M3_rn_satfinite(amax_block / (6*g)); s = decode(sf)*g.
+ * Element code ("The 4-bitter Lesson...", §"Improving Gradient Stability", footnote 6:
+ * Q = clip(round(w/s), qmin, qmax)): round(x / s) of the exact (unrounded) quotient onto
+ * the E2M1 grid, ties to the even code, saturating at +-6, or stochastic rounding of that
+ * quotient; zero magnitudes encoded as +0.
  */
 #ifndef NVFP4MOE_H
 #define NVFP4MOE_H
@@ -66,6 +69,11 @@ typedef enum {
 } nvfp4_rounding;
 
 typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 } nvfp4_out_dtype;
+
+typedef enum {
+  NVFP4_SF_SWIZZLED_128x4 = 0, /* the 128x4 tiled layout the block-scaled MMAs read (above) */
+  NVFP4_SF_ROWMAJOR = 1        /* plain [rows, cols/16] bytes, scale (r, c) at r*cols/16 + c */
+} nvfp4_sf_layout;
 
 /* GEMM-tiled operand layout (the layout the expert block's GEMMs read).  An NVFP4
  * operand of K columns (K % 256 == 0) is stored as blocks of R rows (R = 128 for
@@ -110,7 +118,9 @@ enum {
   NVFP4_OP_PREPARE_WEIGHTS = 1, /* args: E, H, I */
   NVFP4_OP_MOE_FORWARD = 2,     /* args: T, k, E, H, I */
   NVFP4_OP_MOE_PERMUTE = 3,     /* args: T, k, E */
-  NVFP4_OP_QUANTIZE_T = 4       /* args: batches * C (rows of the transpose), R */
+  NVFP4_OP_QUANTIZE_T = 4,      /* args: batches * C (rows of the transpose), R */
+  NVFP4_OP_MOE_BACKWARD = 5,    /* args: T, k, E, H, I */
+  NVFP4_OP_PREPARE_WEIGHTS_T = 6 /* args: E */
 };
 size_t nvfp4_workspace_size(int op, int64_t T_or_rows, int64_t k_or_cols, int64_t E,
                             int64_t H, int64_t I);
@@ -135,8 +145,11 @@ const char* nvfp4_status_string(nvfp4_status s);
  *                 rows/group_rows floats) instead of being computed from amax.
  *   global_scale_out: device float [1 | rows | rows/group_rows], receives g.
  *   codes_out:    device uint8 [rows, cols/2] (16-byte aligned).
- *   sf_out:       device uint8 [nvfp4_sf_bytes(rows, cols)], tiled layout; padding
- *                 rows/columns of the tile grid are written as 0.
+ *   sf_out:       device uint8, in `sf_layout`:
+ *                 NVFP4_SF_SWIZZLED_128x4: [nvfp4_sf_bytes(rows, cols)] bytes, padding
+ *                   rows/columns of the tile grid written as 0 (the GEMMs' input);
+ *                 NVFP4_SF_ROWMAJOR: [rows, cols/16] bytes; needs cols % 64 == 0 (else
+ *                   NVFP4_ERR_UNSUPPORTED).
  *   workspace:    device, nvfp4_workspace_size(NVFP4_OP_QUANTIZE, rows, cols, ...) bytes
  *                 (holds the amax of each scope for the per-tensor / per-group modes).
  */
@@ -144,13 +157,15 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
                             nvfp4_scale_mode mode, int64_t group_rows, nvfp4_rounding rounding,
                             uint64_t seed, uint64_t rng_offset, const float* global_scale_in,
                             float* global_scale_out, uint8_t* codes_out, uint8_t* sf_out,
-                            void* workspace, size_t workspace_bytes, void* stream);
+                            nvfp4_sf_layout sf_layout, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
 /* The same quantisation as nvfp4_quantize, for callers that cannot allocate device
  * memory (for example a host plug-in that is handed only the tensors it reads and
  * writes, with no allocator or memory pool it may use).  The pages have no counterpart:
  * it is a deployment convenience, not part of the method.
- *   Same arguments as nvfp4_quantize without the workspace.  The amax scratch of the
+ *   Same arguments as nvfp4_quantize without the workspace, scales always in the
+ *   NVFP4_SF_SWIZZLED_128x4 layout.  The amax scratch of the
  *   per-tensor and per-group modes lives in a fixed 16 KB device array owned by the
  *   library (at most 4096 scopes: per-group calls with more than 4096 groups and no
  *   global_scale_in return NVFP4_ERR_UNSUPPORTED).  Every GPU that loads the library
@@ -344,26 +359,40 @@ nvfp4_status nvfp4_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t r
 
 /* ---------------------------------------------------------------- MoE helpers */
 
-/* Top-k routing of router logits.  ids[t, :] = the k experts with the largest logits,
- * in descending order, ties to the lower expert id; weights = softmax over the chosen k
- * (renormalize != 0) or the full-softmax probabilities of the chosen experts.
+/* Top-k routing of router logits, the "token permute by router top-k" that feeds the
+ * expert GEMMs ("Low-Bit Precision Training Is Ready for Production...", §"What W4A4 GEMM
+ * Actually Changes": the W4A4 GEMMs are the MoE expert layers, each token running
+ * through the experts its router picks).  ids[t, :] = the k experts with the largest
+ * logits, in descending order, ties to the lower expert id; weights = softmax over the
+ * chosen k (renormalize != 0) or the full-softmax probabilities of the chosen experts.
+ * The pages do not give the weight rule; renormalising over the chosen k is this
+ * library's reading (the Qwen3 MoE convention), the other the flag's alternative.
  *   logits: device float [T, E]; ids: device int32 [T, k]; weights: device float [T, k].
  *   1 <= k <= 32, k <= E <= 1024. */
 nvfp4_status moe_route_topk(const float* logits, int64_t T, int32_t E, int32_t k,
                             int renormalize, int32_t* ids, float* weights, void* stream);
 
-/* Expert grouping of the T*k (token, j) entries: counts [E], offsets [E+1] (exclusive
- * scan of counts), padded_offsets [E+1] (each group starts at a multiple of 128),
- * inv [T, k] = slot of (t, j), perm [M_cap] = token of each slot, -1 for padding slots
- * below padded_offsets[E] (entries beyond it are not written).  Slots are ordered by
- * expert, then by token.  M_cap = round_up(T*k + E*127, 128) bounds padded_offsets[E].
- * Ids outside [0, E) set NVFP4_ERR_DEVICE_STATUS and are counted nowhere. */
+/* Expert grouping ("miniTE identifies and closes the execution gap...", §Development:
+ * grouped GEMMs over the experts need each expert's tokens contiguous; "Low-Bit Precision
+ * Training Is Ready for Production...", §"The Cross-Engine Alignment Problem": the
+ * composition of a batch must not change a token's result, so the slot order is a
+ * deterministic function of the ids alone).  Of the T*k (token, j) entries:
+ * counts [E], offsets [E+1] (exclusive scan of counts), padded_offsets [E+1] (each group
+ * starts at a multiple of 128), inv [T, k] = slot of (t, j), perm [M_cap] = token of each
+ * slot, -1 for padding slots below padded_offsets[E] (entries beyond it are not
+ * written).  Slots are ordered by expert, then by token.  M_cap = round_up(T*k + E*127,
+ * 128) bounds padded_offsets[E].  Ids outside [0, E) set NVFP4_ERR_DEVICE_STATUS and are
+ * counted nowhere. */
 nvfp4_status moe_permute(const int32_t* ids, int64_t T, int32_t k, int32_t E,
                          int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
                          int32_t* inv, int32_t* perm, void* workspace,
                          size_t workspace_bytes, void* stream);
 
-/* Router-weighted un-permute: out[t] = BF16( sum_{j=0..k-1} w[t, j] * y[inv[t, j]] ),
+/* Router-weighted un-permute, the last step of the expert block ("Low-Bit Precision
+ * Training Is Ready for Production...", §"What W4A4 GEMM Actually Changes": the expert
+ * layers' outputs return to their tokens weighted by the router; §"The Cross-Engine
+ * Alignment Problem": accumulation order decides the bits, so it is fixed):
+ * out[t] = BF16( sum_{j=0..k-1} w[t, j] * y[inv[t, j]] ),
  * each product and each partial sum a float32 operation, in the order j = 0..k-1.
  *   y: device BF16 [*, H]; inv: device int32 [T, k]; w: device float [T, k];
  *   out: device BF16 [T, H].  H % 8 == 0. */
@@ -409,6 +438,85 @@ nvfp4_status moe_prepare_weights(const void* w13, const void* w2, int32_t E, int
 nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* w, int64_t T,
                                 int32_t k, const nvfp4_moe_weights* weights, void* out,
                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- backward (W4A4) */
+
+/* Transposed expert weights for the backward's dgrad GEMMs ("The 4-bitter Lesson...",
+ * §"Why is the NVFP4 pretraining recipe not sufficient for RL?": the pretraining recipe
+ * runs the backward GEMMs in NVFP4 too; a dgrad GEMM dX = dY W contracts over W's output
+ * dimension, so W is quantised along it).  Caller-allocated device buffers, sizes from
+ * moe_weights_t_sizes() in struct order; both GEMM-tiled with 256-row blocks.
+ *   w13t: W13_e^T [H, 2I] per expert (rows e*H ..), K = 2I in the canonical [gate | up]
+ *         order, blocks of 16 along 2I, one FP32 global scale per expert (w13t_g [E]);
+ *   w2t:  W2_e^T [I, H] per expert, rows padded to Ip = round_up(I, 256) with zeros
+ *         (rows e*Ip ..), K = H, one global scale per expert (w2t_g [E]). */
+typedef struct {
+  int32_t E;
+  int64_t H;
+  int64_t I;
+  uint8_t* w13t;
+  float* w13t_g;
+  uint8_t* w2t;
+  float* w2t_g;
+} nvfp4_moe_weights_t;
+
+nvfp4_status moe_weights_t_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[4]);
+
+/* Quantise the transposed weights once per weight update (round to nearest).
+ *   w13: device BF16 [E, 2I, H]; w2: device BF16 [E, H, I] (the forward's inputs).
+ *   H % 256 == 0, I % 128 == 0, E <= 512.  workspace:
+ *   nvfp4_workspace_size(NVFP4_OP_PREPARE_WEIGHTS_T, E, 0, 0, 0, 0) bytes. */
+nvfp4_status moe_prepare_weights_backward(const void* w13, const void* w2, int32_t E, int64_t H, int64_t I,
+                                          const nvfp4_moe_weights_t* out, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/* The expert block's backward in W4A4 ("The 4-bitter Lesson...", §"Why is the NVFP4
+ * pretraining recipe not sufficient for RL?": every backward GEMM on NVFP4 operands with
+ * stochastic rounding of the gradients -- recipe (a), "quantized forward and backward", of
+ * §"Improving Gradient Stability", Results Validation).  For out = moe_expert_forward(x,
+ * ids, w, weights) and its upstream gradient dout:
+ *   dy[slot(t,j)] = BF16(w[t,j] dout[t]);          dw[t,j] = <dout[t], y[slot(t,j)]>  (float32)
+ *   dh = Q(dy) Q(W2^T)  (dgrad, BF16)              dW2_e = Q(dy_e^T) Q(h_e^T)   (wgrad, float32)
+ *   [dgate | dup] = SwiGLU backward of D = gate/up output (recomputed: the fused forward
+ *   keeps only h)
+ *   dxs = Q(dD) Q(W13^T) (dgrad, BF16 per slot)    dW13_e = Q(dD_e^T) Q(x_e^T)  (wgrad, float32)
+ *   dx[t] = BF16(sum_j dxs[slot(t,j)])
+ * Quantisation: dgrad operands along the contraction -- the gradient per routed row (one
+ * FP32 scale per row) with stochastic rounding, the weights from `weights_t`; wgrad
+ * operands transposed per expert along the tokens (one FP32 scale per expert matrix,
+ * each expert's tokens zero-padded to a multiple of 256, at least 256), the gradient
+ * with stochastic rounding, h and x to nearest.  Philox key of each stochastic
+ * quantisation: seed + (((stream << 10) + expert) << 40), stream 0 = dy by rows, 1 = dy^T,
+ * 2 = dD by rows, 3 = dD^T (expert 0 for the row quantisations), element index = row-major
+ * index in the quantised matrix (slot layout for rows, the expert's [features, tokens]
+ * transpose for wgrad).
+ *   dout, x: device BF16 [T, H]; w: device float [T, k] (the forward's router weights).
+ *   weights / weights_t: the forward's prepared weights and the transposed ones.
+ *   fwd_workspace: the workspace of the moe_expert_forward call on these inputs (its
+ *     grouping, routed activations, h and y are read; nothing in it is written), with
+ *     that call ordered before this one.
+ *   dx: device BF16 [T, H]; dw: device float [T, k]; dw13: device float [E, 2I, H]
+ *   (canonical gate/up rows); dw2: device float [E, H, I].
+ *   workspace: nvfp4_workspace_size(NVFP4_OP_MOE_BACKWARD, T, k, E, H, I) bytes; its
+ *   layout is given by moe_backward_workspace_layout().
+ *   H % 256 == 0, H <= 2048, I % 128 == 0, I <= 1024, 1 <= k <= 32, E <= 512; the
+ *   buffers 16-byte aligned (w, dw 4-byte). */
+nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w, int64_t T, int32_t k,
+                                 const nvfp4_moe_weights* weights, const nvfp4_moe_weights_t* weights_t,
+                                 const void* fwd_workspace, size_t fwd_workspace_bytes, uint64_t seed, void* dx,
+                                 float* dw, float* dw13, float* dw2, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* Byte offsets inside the backward's workspace: [0] dy BF16 [M_cap, H], [1] Q(dy)
+ * GEMM-tiled (128-row blocks, K = H), [2] its per-row scales float [M_cap], [3] dh BF16
+ * [M_cap, Ip], [4] D BF16 [M_cap, 2I] (gate/up interleaved as the prepared W13), [5] dD
+ * BF16 [M_cap, 2I] ([dgate | dup]), [6] Q(dD) GEMM-tiled (K = 2I), [7] its scales, [8] dxs
+ * BF16 [M_cap, H], [9] K-block prefix sums int32 [E+1], [10] per-expert amax bits
+ * [4E], [11] per-expert global scales float [4E] (dy^T, h^T, dD^T, x^T), [12] .. [15] the
+ * wgrad operands Q(dy^T) (128-row blocks), Q(h^T) (256-row blocks, Ip rows per expert),
+ * Q(dD^T), Q(x^T), [16] their capacity in 256-token K-blocks (a count), [17] total bytes. */
+nvfp4_status moe_backward_workspace_layout(int64_t T, int32_t k, int32_t E, int64_t H, int64_t I,
+                                           int64_t layout_out[18]);
 
 /* Byte offsets of the forward's intermediates inside its workspace, in this order:
  * [0] counts int32[E], [1] offsets int32[E+1], [2] padded_offsets int32[E+1],

@@ -26,12 +26,17 @@ __all__ = [
     "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_grouped_gemm", "mxfp8_sf_bytes",
     "bf16_grouped_gemm", "bf16_transpose", "moe_swiglu_backward",
     "SCALE_PER_TENSOR", "SCALE_PER_ROW", "SCALE_PER_GROUP", "ROUND_RNE", "ROUND_STOCHASTIC",
+    "SF_SWIZZLED_128x4", "SF_ROWMAJOR",
+    "NVFP4MoEWeightsT", "moe_prepare_weights_backward", "moe_expert_backward", "moe_backward_workspace",
+    "moe_backward_workspace_layout",
 ]
 
 SCALE_PER_TENSOR, SCALE_PER_ROW, SCALE_PER_GROUP = 0, 1, 2
 ROUND_RNE, ROUND_STOCHASTIC = 0, 1
+SF_SWIZZLED_128x4, SF_ROWMAJOR = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 OP_QUANTIZE, OP_PREPARE_WEIGHTS, OP_MOE_FORWARD, OP_MOE_PERMUTE, OP_QUANTIZE_T = 0, 1, 2, 3, 4
+OP_MOE_BACKWARD, OP_PREPARE_WEIGHTS_T = 5, 6
 
 _lib = None
 _vp, _i64, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t
@@ -52,6 +57,11 @@ class _Weights(ctypes.Structure):
                 ("w2_g", _vp)]
 
 
+class _WeightsT(ctypes.Structure):
+    _fields_ = [("E", _i32), ("H", _i64), ("I", _i64), ("w13t", _vp), ("w13t_g", _vp), ("w2t", _vp),
+                ("w2t_g", _vp)]
+
+
 _SIGS = {
     "nvfp4_sf_bytes": (_sz, [_i64, _i64]),
     "nvfp4_tiled_bytes": (_sz, [_i64, _i64, _i32]),
@@ -63,7 +73,7 @@ _SIGS = {
     "nvfp4_status_check": (ctypes.c_int, [_vp]),
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_quantize": (ctypes.c_int, [_vp, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int, _u64, _u64,
-                                      _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+                                      _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _sz, _vp]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int, _u64, _u64,
                                               _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_quantize_transposed": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int,
@@ -89,6 +99,13 @@ _SIGS = {
     "moe_expert_forward": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, ctypes.POINTER(_Weights), _vp, _vp,
                                           _sz, _vp]),
     "moe_forward_workspace_layout": (ctypes.c_int, [_i64, _i32, _i32, _i64, _i64, ctypes.POINTER(_i64)]),
+    "moe_weights_t_sizes": (ctypes.c_int, [_i32, _i64, _i64, ctypes.POINTER(_sz)]),
+    "moe_prepare_weights_backward": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i64, ctypes.POINTER(_WeightsT), _vp,
+                                                    _sz, _vp]),
+    "moe_expert_backward": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, ctypes.POINTER(_Weights),
+                                           ctypes.POINTER(_WeightsT), _vp, _sz, _u64, _vp, _vp, _vp, _vp, _vp, _sz,
+                                           _vp]),
+    "moe_backward_workspace_layout": (ctypes.c_int, [_i64, _i32, _i32, _i64, _i64, ctypes.POINTER(_i64)]),
 }
 
 
@@ -164,9 +181,11 @@ def nvfp4_status_check(stream=None) -> int:
 
 def nvfp4_quantize(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, rounding: int = ROUND_RNE, seed: int = 0,
                    rng_offset: int = 0, group_rows: int = 0, global_scale: torch.Tensor | None = None,
-                   out=None, workspace: torch.Tensor | None = None, stream=None):
+                   out=None, workspace: torch.Tensor | None = None, sf_layout: int = SF_SWIZZLED_128x4,
+                   stream=None):
     """NVFP4 of a BF16 matrix [rows, cols].  Returns (codes [rows, cols/2] uint8,
-    tiled scales uint8 [nvfp4_sf_bytes], g float32 [1 | rows | rows/group_rows])."""
+    scales uint8 (tiled [nvfp4_sf_bytes], or [rows, cols/16] with SF_ROWMAJOR),
+    g float32 [1 | rows | rows/group_rows])."""
     lib = load()
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     rows, cols = x.shape
@@ -174,7 +193,10 @@ def nvfp4_quantize(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, rounding: int 
     n_g = 1 if mode == SCALE_PER_TENSOR else (rows if mode == SCALE_PER_ROW else rows // max(group_rows, 1))
     if out is None:
         codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
-        sf = torch.empty(max(nvfp4_sf_bytes(rows, cols), 16), dtype=torch.uint8, device=dev)
+        if sf_layout == SF_ROWMAJOR:
+            sf = torch.empty(rows, cols // 16, dtype=torch.uint8, device=dev)
+        else:
+            sf = torch.empty(max(nvfp4_sf_bytes(rows, cols), 16), dtype=torch.uint8, device=dev)
         g = torch.empty(max(n_g, 1), dtype=torch.float32, device=dev)
     else:
         codes, sf, g = out
@@ -182,8 +204,8 @@ def nvfp4_quantize(x: torch.Tensor, mode: int = SCALE_PER_TENSOR, rounding: int 
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     _check(lib.nvfp4_quantize(_p(x), rows, cols, x.stride(0), mode, group_rows, rounding, seed, rng_offset,
-                              _p(global_scale), _p(g), _p(codes), _p(sf), _p(workspace), workspace.numel(),
-                              _stream(stream)), "nvfp4_quantize")
+                              _p(global_scale), _p(g), _p(codes), _p(sf), sf_layout, _p(workspace),
+                              workspace.numel(), _stream(stream)), "nvfp4_quantize")
     return codes, sf, g
 
 
@@ -498,3 +520,75 @@ def moe_expert_forward(x: torch.Tensor, ids: torch.Tensor, w: torch.Tensor, weig
     _check(lib.moe_expert_forward(_p(x), _p(ids), _p(w), T, k, ctypes.byref(weights.struct), _p(out),
                                   _p(workspace), workspace.numel(), _stream(stream)), "moe_expert_forward")
     return out
+
+
+# --------------------------------------------------------------------------- backward (W4A4)
+
+class NVFP4MoEWeightsT:
+    """Transposed quantised expert weights for the backward's dgrad GEMMs (GEMM-tiled
+    device buffers) plus the C struct that points at them."""
+
+    def __init__(self, E: int, H: int, I: int, device):
+        lib = load()
+        sizes = (_sz * 4)()
+        _check(lib.moe_weights_t_sizes(E, H, I, sizes), "moe_weights_t_sizes")
+        self.E, self.H, self.I, self.Ip = E, H, I, (I + 255) // 256 * 256
+        self.w13t = torch.empty(sizes[0], dtype=torch.uint8, device=device)
+        self.w13t_g = torch.empty(E, dtype=torch.float32, device=device)
+        self.w2t = torch.empty(sizes[2], dtype=torch.uint8, device=device)
+        self.w2t_g = torch.empty(E, dtype=torch.float32, device=device)
+        self.struct = _WeightsT(E, H, I, self.w13t.data_ptr(), self.w13t_g.data_ptr(), self.w2t.data_ptr(),
+                                self.w2t_g.data_ptr())
+
+
+def moe_prepare_weights_backward(w13: torch.Tensor, w2: torch.Tensor, stream=None) -> NVFP4MoEWeightsT:
+    """Quantise W13^T and W2^T per expert (along the dgrad contractions) from the BF16
+    W13 [E, 2I, H] and W2 [E, H, I]."""
+    lib = load()
+    E, N13, H = w13.shape
+    I = N13 // 2
+    pt = NVFP4MoEWeightsT(E, H, I, _dev(w13))
+    ws = torch.empty(int(lib.nvfp4_workspace_size(OP_PREPARE_WEIGHTS_T, E, 0, 0, 0, 0)), dtype=torch.uint8,
+                     device=w13.device)
+    _check(lib.moe_prepare_weights_backward(_p(w13.contiguous()), _p(w2.contiguous()), E, H, I,
+                                            ctypes.byref(pt.struct), _p(ws), ws.numel(), _stream(stream)),
+           "moe_prepare_weights_backward")
+    pt._ws = ws
+    return pt
+
+
+def moe_backward_workspace_layout(T: int, k: int, E: int, H: int, I: int) -> list:
+    lib = load()
+    out = (_i64 * 18)()
+    _check(lib.moe_backward_workspace_layout(T, k, E, H, I, out), "moe_backward_workspace_layout")
+    return list(out)
+
+
+def moe_backward_workspace(T: int, k: int, weights: NVFP4MoEWeights, device) -> torch.Tensor:
+    lib = load()
+    n = int(lib.nvfp4_workspace_size(OP_MOE_BACKWARD, T, k, weights.E, weights.H, weights.I))
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_expert_backward(dout: torch.Tensor, x: torch.Tensor, w: torch.Tensor, weights: NVFP4MoEWeights,
+                        weights_t: NVFP4MoEWeightsT, fwd_workspace: torch.Tensor, seed: int = 0, out=None,
+                        workspace: torch.Tensor | None = None, stream=None):
+    """The expert block's W4A4 backward for the forward whose workspace is fwd_workspace.
+    Returns (dx [T, H] BF16, dw [T, k] f32, dw13 [E, 2I, H] f32, dw2 [E, H, I] f32)."""
+    lib = load()
+    T, H = x.shape
+    k = w.shape[1]
+    E, I = weights.E, weights.I
+    dev = _dev(x)
+    if out is None:
+        out = (torch.empty(T, H, dtype=torch.bfloat16, device=dev), torch.empty(T, k, dtype=torch.float32, device=dev),
+               torch.empty(E, 2 * I, H, dtype=torch.float32, device=dev),
+               torch.empty(E, H, I, dtype=torch.float32, device=dev))
+    dx, dw, dw13, dw2 = out
+    if workspace is None:
+        workspace = moe_backward_workspace(T, k, weights, dev)
+    _check(lib.moe_expert_backward(_p(dout.contiguous()), _p(x), _p(w.contiguous()), T, k, ctypes.byref(weights.struct),
+                                   ctypes.byref(weights_t.struct), _p(fwd_workspace), fwd_workspace.numel(), seed,
+                                   _p(dx), _p(dw), _p(dw13), _p(dw2), _p(workspace), workspace.numel(),
+                                   _stream(stream)), "moe_expert_backward")
+    return dx, dw, dw13, dw2

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libnvfp4moe.so")
-SOURCES = ["api.cu", "quantize.cu", "route_permute.cu", "swiglu.cu", "grouped_gemm.cu", "gemm_n256.cu", "gemm_tiled.cu", "tiled_pack.cu", "dequantize.cu", "noalloc.cu", "mxfp8.cu"]
+SOURCES = ["api.cu", "quantize.cu", "route_permute.cu", "swiglu.cu", "grouped_gemm.cu", "gemm_n256.cu", "gemm_tiled.cu",
+           "tiled_pack.cu", "dequantize.cu", "noalloc.cu", "mxfp8.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere, so every float32 step of the scale
 # arithmetic is the single rounded operation the format contract names.

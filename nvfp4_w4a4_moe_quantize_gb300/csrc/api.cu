@@ -106,6 +106,44 @@ ForwardLayout forward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t
   return L;
 }
 
+struct BackwardLayout {
+  int64_t off[18];
+};
+
+// dy | dyq (tiled, K = H) | g_dy | dh [M, Ip] | D [M, 2I] | dD [M, 2I] | dDq (tiled, K = 2I) |
+// g_dD | dxs [M, H] | kofs | amax [4E] | g [4E] | wgrad operands: dy^T, h^T, dD^T, x^T
+BackwardLayout backward_layout(int64_t T, int64_t k, int64_t E, int64_t H, int64_t I) {
+  BackwardLayout L;
+  const int64_t Ip = round_up(I, 256);
+  const int64_t mcap = round_up(T * k + E * 127, 128);
+  const int64_t kb = T * k / 256 + E + 1;        // >= sum over experts of max(1, ceil(count / 256))
+  size_t p = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = p;
+    p += align256(bytes);
+    return (int64_t)o;
+  };
+  L.off[0] = take((size_t)mcap * H * 2);
+  L.off[1] = take((size_t)tiled_bytes(mcap, H, 128));
+  L.off[2] = take(4 * (size_t)mcap);
+  L.off[3] = take((size_t)mcap * Ip * 2);
+  L.off[4] = take((size_t)mcap * 2 * I * 2);
+  L.off[5] = take((size_t)mcap * 2 * I * 2);
+  L.off[6] = take((size_t)tiled_bytes(mcap, 2 * I, 128));
+  L.off[7] = take(4 * (size_t)mcap);
+  L.off[8] = take((size_t)mcap * H * 2);
+  L.off[9] = take(4 * (size_t)(E + 1));
+  L.off[10] = take(16 * (size_t)E);
+  L.off[11] = take(16 * (size_t)E);
+  L.off[12] = take((size_t)(H / 128) * kb * 128 * 144);
+  L.off[13] = take((size_t)(Ip / 256) * kb * 256 * 144);
+  L.off[14] = take((size_t)(2 * I / 128) * kb * 128 * 144);
+  L.off[15] = take((size_t)(H / 256) * kb * 256 * 144);
+  L.off[16] = kb;
+  L.off[17] = (int64_t)p;
+  return L;
+}
+
 nvfp4_status gemm(const uint8_t* A, const uint8_t* SFA, const float* gA, const uint8_t* B, const uint8_t* SFB,
                   const float* gB, const int32_t* offsets, const int32_t* rows, int64_t M_total, int64_t N, int64_t K,
                   int32_t E, void* D, int out_f32, int64_t ldd, cudaStream_t s) {
@@ -199,6 +237,10 @@ size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t E, int64_t H, 
     }
     case NVFP4_OP_QUANTIZE_T:   // transposed BF16 copy [a, b] + amax scratch for up to a scopes
       return align256(2u * (size_t)a * (size_t)b) + align256(4u * (size_t)(a > 1 ? a : 1));
+    case NVFP4_OP_MOE_BACKWARD:
+      return (size_t)backward_layout(a, b, E, H, I).off[17];
+    case NVFP4_OP_PREPARE_WEIGHTS_T:   // amax [2E] + K-block prefix sums [2(E+1)]
+      return align256(8u * (size_t)(a > 1 ? a : 1)) + align256(8u * (size_t)((a > 1 ? a : 1) + 1));
     default:
       return 0;
   }
@@ -242,10 +284,11 @@ const char* nvfp4_status_string(nvfp4_status s) {
 
 nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, nvfp4_scale_mode mode,
                             int64_t group_rows, nvfp4_rounding rounding, uint64_t seed, uint64_t rng_offset,
-                            const float* g_in, float* g_out, uint8_t* codes, uint8_t* sf, void* ws,
-                            size_t ws_bytes, void* stream) {
+                            const float* g_in, float* g_out, uint8_t* codes, uint8_t* sf,
+                            nvfp4_sf_layout sf_layout, void* ws, size_t ws_bytes, void* stream) {
   if (rows < 0 || cols <= 0 || cols % 16 != 0 || ld < cols || ld % 8 != 0) return NVFP4_ERR_INVALID_ARG;
-  if (cols > 8192) return NVFP4_ERR_UNSUPPORTED;
+  if (sf_layout != NVFP4_SF_SWIZZLED_128x4 && sf_layout != NVFP4_SF_ROWMAJOR) return NVFP4_ERR_INVALID_ARG;
+  if (cols > 8192 || (sf_layout == NVFP4_SF_ROWMAJOR && cols % 64 != 0)) return NVFP4_ERR_UNSUPPORTED;
   if (mode < NVFP4_SCALE_PER_TENSOR || mode > NVFP4_SCALE_PER_GROUP) return NVFP4_ERR_INVALID_ARG;
   if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_STOCHASTIC) return NVFP4_ERR_INVALID_ARG;
   if (mode == NVFP4_SCALE_PER_GROUP && (group_rows <= 0 || rows % group_rows != 0)) return NVFP4_ERR_INVALID_ARG;
@@ -274,8 +317,9 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   a.codes_ld = cols / 2;
   a.sf = sf;
   a.sf_words = (cols + 63) / 64;
+  a.sf_row_bytes = sf_layout == NVFP4_SF_ROWMAJOR ? cols / 16 : 0;
   a.cols_pad = cols;
-  a.rows_total = round_up(rows, 128);
+  a.rows_total = sf_layout == NVFP4_SF_ROWMAJOR ? rows : round_up(rows, 128);
   a.map = kMapIdentity;
   a.seed = seed;
   a.rng_offset = rng_offset;
@@ -298,7 +342,7 @@ nvfp4_status nvfp4_quantize_transposed(const void* x, int64_t batches, int64_t R
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_transpose_bf16(x, batches, R, C, ld, ws, s) != cudaSuccess) return NVFP4_ERR_CUDA;
   return nvfp4_quantize(ws, rows_t, R, R, mode, group_rows, rounding, seed, rng_offset, g_in, g_out, codes, sf,
-                        static_cast<uint8_t*>(ws) + t_bytes, ws_bytes - t_bytes, stream);
+                        NVFP4_SF_SWIZZLED_128x4, static_cast<uint8_t*>(ws) + t_bytes, ws_bytes - t_bytes, stream);
 }
 
 nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows, int64_t cols,
@@ -721,6 +765,208 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
 
   // 6. weighted un-permute
   return from_cuda(launch_combine(ybuf, inv, w, T, k, H, out, s));
+}
+
+nvfp4_status moe_weights_t_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[4]) {
+  if (E <= 0 || H <= 0 || I <= 0 || sizes_out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  const int64_t Ip = round_up(I, 256);
+  sizes_out[0] = (size_t)tiled_bytes((int64_t)E * H, 2 * I, 256);
+  sizes_out[1] = 4u * (size_t)E;
+  sizes_out[2] = (size_t)tiled_bytes((int64_t)E * Ip, H, 256);
+  sizes_out[3] = 4u * (size_t)E;
+  return NVFP4_OK;
+}
+
+nvfp4_status moe_prepare_weights_backward(const void* w13, const void* w2, int32_t E, int64_t H, int64_t I,
+                                          const nvfp4_moe_weights_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (E <= 0 || H <= 0 || I <= 0 || out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (E > tiled_max_experts() || H % 256 != 0 || I % 128 != 0 || H > 8192 || I > 4096) return NVFP4_ERR_UNSUPPORTED;
+  if (out->E != E || out->H != H || out->I != I) return NVFP4_ERR_INVALID_ARG;
+  const void* ptrs[] = {w13, w2, out->w13t, out->w13t_g, out->w2t, out->w2t_g};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < nvfp4_workspace_size(NVFP4_OP_PREPARE_WEIGHTS_T, E, 0, 0, 0, 0) || !aligned16(ws))
+    return NVFP4_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t Ip = round_up(I, 256);
+  uint32_t* amax = static_cast<uint32_t*>(ws);
+  int32_t* kofs = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + align256(8u * (size_t)E));
+  // W13_e [2I, H] -> W13_e^T [H, 2I]: the 2I rows of each expert are its "tokens"
+  if (launch_amax(w13, (int64_t)E * 2 * I, H, H, 2 * I, amax, E, s) != cudaSuccess ||
+      launch_kofs(nullptr, 2 * I, E, kofs, s) != cudaSuccess ||
+      launch_tquant(w13, H, nullptr, nullptr, nullptr, 2 * I, kofs, E, (int)H, (int)H, 256, amax, out->w13t_g,
+                    out->w13t, kRoundRNE, 0, 0, (int64_t)E * (2 * I / 256), s) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  // W2_e [H, I] -> W2_e^T [I, H], rows I .. Ip-1 zero
+  uint32_t* amax2 = amax + E;
+  int32_t* kofs2 = kofs + E + 1;
+  if (launch_amax(w2, (int64_t)E * H, I, I, H, amax2, E, s) != cudaSuccess ||
+      launch_kofs(nullptr, H, E, kofs2, s) != cudaSuccess ||
+      launch_tquant(w2, I, nullptr, nullptr, nullptr, H, kofs2, E, (int)I, (int)Ip, 256, amax2, out->w2t_g, out->w2t,
+                    kRoundRNE, 0, 0, (int64_t)E * (H / 256), s) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
+}
+
+nvfp4_status moe_backward_workspace_layout(int64_t T, int32_t k, int32_t E, int64_t H, int64_t I,
+                                           int64_t layout_out[18]) {
+  if (T < 0 || k <= 0 || E <= 0 || H <= 0 || I <= 0 || layout_out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  const BackwardLayout L = backward_layout(T, k, E, H, I);
+  std::memcpy(layout_out, L.off, sizeof(L.off));
+  return NVFP4_OK;
+}
+
+nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w, int64_t T, int32_t k,
+                                 const nvfp4_moe_weights* wt, const nvfp4_moe_weights_t* wtt, const void* fwd_ws,
+                                 size_t fwd_ws_bytes, uint64_t seed, void* dx, float* dw, float* dw13, float* dw2,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  if (wt == nullptr || wtt == nullptr || T < 0 || k <= 0 || k > 32) return NVFP4_ERR_INVALID_ARG;
+  const int32_t E = wt->E;
+  const int64_t H = wt->H, I = wt->I;
+  if (wtt->E != E || wtt->H != H || wtt->I != I) return NVFP4_ERR_INVALID_ARG;
+  if (E <= 0 || E > tiled_max_experts() || k > E) return NVFP4_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0 || H > 2048 || I > 1024) return NVFP4_ERR_UNSUPPORTED;
+  if (T * k >= ((int64_t)1 << 31) - (int64_t)E * 128) return NVFP4_ERR_UNSUPPORTED;
+  if (T == 0) return NVFP4_OK;
+  const void* ptrs[] = {dout, x, dx, dw13, dw2, ws, fwd_ws, wt->w13, wt->w13_g, wtt->w13t, wtt->w13t_g, wtt->w2t,
+                        wtt->w2t_g};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned4(w) || !aligned4(dw)) return NVFP4_ERR_INVALID_ARG;
+  size_t hist_off, hist_bytes;
+  const ForwardLayout F = forward_layout(T, k, E, H, I, &hist_off, &hist_bytes);
+  if (fwd_ws_bytes < (size_t)F.off[14]) return NVFP4_ERR_WORKSPACE;
+  const BackwardLayout L = backward_layout(T, k, E, H, I);
+  if (ws_bytes < (size_t)L.off[17]) return NVFP4_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* fb = static_cast<const uint8_t*>(fwd_ws);
+  const int32_t* counts = reinterpret_cast<const int32_t*>(fb + F.off[0]);
+  const int32_t* padded = reinterpret_cast<const int32_t*>(fb + F.off[2]);
+  const int32_t* inv = reinterpret_cast<const int32_t*>(fb + F.off[3]);
+  const int32_t* perm = reinterpret_cast<const int32_t*>(fb + F.off[4]);
+  const uint8_t* aq = fb + F.off[5];
+  const float* ga = reinterpret_cast<const float*>(fb + F.off[7]);
+  const void* hbuf = fb + F.off[8];
+  const void* ybuf = fb + F.off[12];
+  const int64_t mcap = F.off[13];
+  const int64_t Ip = round_up(I, 256);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  auto at = [&](int i) { return b + L.off[i]; };
+  void* dy = at(0);
+  uint8_t* dyq = at(1);
+  float* g_dy = reinterpret_cast<float*>(at(2));
+  void* dh = at(3);
+  void* dbuf = at(4);
+  void* dD = at(5);
+  uint8_t* dDq = at(6);
+  float* g_dD = reinterpret_cast<float*>(at(7));
+  void* dxs = at(8);
+  int32_t* kofs = reinterpret_cast<int32_t*>(at(9));
+  uint32_t* amax = reinterpret_cast<uint32_t*>(at(10));
+  float* gexp = reinterpret_cast<float*>(at(11));
+  const int64_t kb_cap = L.off[16];
+  int* status = device_status_ptr();
+  auto fail = [](cudaError_t e) { return e != cudaSuccess; };
+
+  // 1. weighted un-permute backward: dy per slot, dw per (token, j)
+  if (fail(launch_combine_backward(dout, inv, w, ybuf, T, k, H, dy, dw, s))) return NVFP4_ERR_CUDA;
+
+  // row quantisation of a slot-ordered gradient (per row, stochastic rounding) into the
+  // GEMM-tiled A operand; padding slots are skipped
+  auto quant_rows = [&](const void* src, int64_t cols, uint8_t* out, float* g_out, uint64_t key) {
+    QuantArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(src);
+    a.rows = mcap;
+    a.cols = cols;
+    a.ld = cols;
+    a.mode = kScopeRow;
+    a.g_out = g_out;
+    a.codes = out;
+    a.sf_words = cols / 64;
+    a.cols_pad = cols;
+    a.rows_total = mcap;
+    a.map = kMapIdentity;
+    a.seed = key;
+    a.status = status;
+    a.tiled_R = 128;
+    a.kblocks = cols / 256;
+    a.row_filter = perm;
+    a.rows_dev = padded + E;
+    return launch_quantize_rows(a, kRoundSR, s);
+  };
+  auto key = [&](int stream_id) { return seed + ((uint64_t)stream_id << 50); };   // expert 0's key of the stream
+  // grouped GEMM over GEMM-tiled operands with a plain BF16 store into [mcap, N] (pitch ld)
+  auto dgrad = [&](const uint8_t* A, const float* gA, const uint8_t* B, const float* gB, int64_t N, int64_t K,
+                   void* out, int64_t ld_cols, int64_t store_cols) {
+    GemmArgs g{};
+    g.ga = gA;
+    g.gb = gB;
+    g.offsets = padded;
+    g.rows = counts;
+    g.m_total = mcap;
+    g.E = E;
+    g.N = (int32_t)N;
+    g.K = (int32_t)K;
+    g.d = out;
+    g.ldd = ld_cols;
+    g.status = status;
+    CUtensorMap md;
+    if (!make_map(&md, out, mcap, store_cols, ld_cols * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2))
+      return cudaErrorInvalidValue;
+    return launch_grouped_gemm_tiled(A, B, md, g, mcap / 128, false, s);
+  };
+
+  // 2. dgrad of the down projection: dh = Q(dy) Q(W2^T), dh [mcap, Ip]
+  if (fail(quant_rows(dy, H, dyq, g_dy, key(0))) ||
+      fail(dgrad(dyq, g_dy, wtt->w2t, wtt->w2t_g, Ip, H, dh, Ip, Ip)))
+    return NVFP4_ERR_CUDA;
+  // 3. the gate/up output D again (the fused forward keeps only h), then the SwiGLU backward
+  //    into the canonical [dgate | dup]
+  if (fail(dgrad(aq, ga, wt->w13, wt->w13_g, 2 * I, H, dbuf, 2 * I, 2 * I)) ||
+      fail(launch_swiglu_backward(dbuf, dh, mcap, I, dD, s, true, Ip)))
+    return NVFP4_ERR_CUDA;
+  // 4. dgrad of gate/up: dxs = Q(dD) Q(W13^T), then dx = sum over each token's slots
+  if (fail(quant_rows(dD, 2 * I, dDq, g_dD, key(2))) ||
+      fail(dgrad(dDq, g_dD, wtt->w13t, wtt->w13t_g, H, 2 * I, dxs, H, H)) ||
+      fail(launch_combine(dxs, inv, nullptr, T, k, H, dx, s)))
+    return NVFP4_ERR_CUDA;
+
+  // 5. weight gradients: per-expert transposed quantisation along the tokens, then the
+  //    ragged-K grouped GEMM (float32 out)
+  if (fail(launch_kofs(counts, 0, E, kofs, s))) return NVFP4_ERR_CUDA;
+  auto wgrad = [&](const void* gsrc, int64_t Fa, const void* asrc, int64_t ld_a, const int32_t* rowmap, int64_t Fb,
+                   int64_t Fbp, int stream_id, int slot, uint8_t* Aw, uint8_t* Bw, float* out) {
+    uint32_t* am = amax + 2 * slot * E;
+    float* gg = gexp + 2 * slot * E;
+    if (fail(launch_group_amax(gsrc, Fa, Fa, nullptr, padded, counts, E, mcap, am, s)) ||
+        fail(launch_group_amax(asrc, ld_a, Fb, rowmap, padded, counts, E, mcap, am + E, s)) ||
+        fail(launch_tquant(gsrc, Fa, nullptr, padded, counts, 0, kofs, E, (int)Fa, (int)Fa, 128, am, gg, Aw, kRoundSR,
+                           seed, stream_id, kb_cap, s)) ||
+        fail(launch_tquant(asrc, ld_a, rowmap, padded, counts, 0, kofs, E, (int)Fb, (int)Fbp, 256, am + E, gg + E, Bw,
+                           kRoundRNE, 0, 0, kb_cap, s)))
+      return cudaErrorUnknown;
+    GemmArgs g{};
+    g.ga = gg;
+    g.gb = gg + E;
+    g.offsets = kofs;
+    g.m_total = kb_cap;
+    g.m_rows = (int32_t)Fa;
+    g.E = E;
+    g.N = (int32_t)Fbp;
+    g.K = 256;
+    g.d = out;
+    g.ldd = Fb;
+    g.out_f32 = 1;
+    g.status = status;
+    CUtensorMap md;
+    if (!make_map(&md, out, (int64_t)E * Fa, Fb, Fb * 4, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4))
+      return cudaErrorInvalidValue;
+    return launch_grouped_gemm_ragged_k(Aw, Bw, md, g, s);
+  };
+  if (fail(wgrad(dy, H, hbuf, I, nullptr, I, Ip, 1, 0, at(12), at(13), dw2)) ||
+      fail(wgrad(dD, 2 * I, x, H, perm, H, H, 3, 1, at(14), at(15), dw13)))
+    return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,352 @@
+// Kernels of the expert block's W4A4 backward ("The 4-bitter Lesson: Balancing Stability
+// and Performance in NVFP4 RL", §"Why is the NVFP4 pretraining recipe not sufficient for
+// RL?": the pretraining recipe quantises the backward GEMMs too, with stochastic rounding
+// of the gradients):
+//   combine_backward_kernel   dy[slot(t,j)] = BF16(w[t,j] dout[t]) and dw[t,j] = <dout[t], y[slot]>
+//   group_amax_kernel         max |x| over each expert's rows of a slot-ordered matrix
+//   kofs_kernel               per-expert token counts -> 256-token K-block prefix sums
+//   tquant_kernel             per-expert transposed NVFP4 (blocks of 16 tokens, one global
+//                             scale per expert matrix) straight into the GEMM-tiled layout:
+//                             the operands of the weight-gradient GEMMs, whose contraction
+//                             runs over each expert's own (ragged) token count.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "encode.cuh"
+#include "group.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+#include "status.cuh"
+#include "tiled.cuh"
+
+namespace nvfp4 {
+
+namespace {
+constexpr unsigned kAll = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// BF16 (bits) of the exact product w * d of a float32 and a BF16 value, rounded once to
+// nearest even.  p = fl32(w d) and the FMA residual e = w d - p (exact) give the exact
+// product p + e.  Rounding p to BF16 is the rounding of p + e unless p sits exactly on a
+// BF16 midpoint (low half 0x8000): no BF16 midpoint lies strictly between p + e and its
+// float32 rounding p, so only there can the side differ, and e's sign decides it.
+__device__ __forceinline__ uint32_t bf16_of_product(float w, float d) {
+  const float p = __fmul_rn(w, d);
+  const float e = __fmaf_rn(w, d, -p);
+  const uint32_t b = __float_as_uint(p);
+  if ((b & 0xFFFFu) == 0x8000u && e != 0.0f) {
+    // away from zero iff e has p's sign (|p + e| > |p|); the upper half is the truncation
+    const bool away = (__float_as_uint(e) >> 31) == (b >> 31);
+    return (b >> 16) + (away ? 1u : 0u);
+  }
+  const uint32_t lsb = (b >> 16) & 1u;
+  return (b + 0x7FFFu + lsb) >> 16;   // round to nearest even (finite inputs)
+}
+}  // namespace
+
+// One warp per token: for each of its k slots, dy = BF16(w dout) and dw = sum_h dout y in
+// float32 (each lane sums its columns in order with one rounding per term, then a
+// fixed-shape butterfly over the lanes: the same order on every run).
+__global__ void __launch_bounds__(256) combine_backward_kernel(const __nv_bfloat16* __restrict__ dout,
+                                                               const int32_t* __restrict__ inv,
+                                                               const float* __restrict__ w,
+                                                               const __nv_bfloat16* __restrict__ y, int64_t T, int k,
+                                                               int64_t H, __nv_bfloat16* __restrict__ dy,
+                                                               float* __restrict__ dw) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  for (int64_t t = warp; t < T; t += nwarp) {
+    for (int j = 0; j < k; ++j) {
+      const int32_t slot = inv[t * k + j];
+      const float wj = w[t * k + j];
+      float acc = 0.0f;
+      if (slot >= 0) {
+        for (int64_t c = 8 * lane; c < H; c += 256) {
+          const uint4 dq = ldg_nc(dout + t * H + c);
+          const uint4 yq = ldg_nc(y + (int64_t)slot * H + c);
+          const uint32_t dw4[4] = {dq.x, dq.y, dq.z, dq.w}, yw4[4] = {yq.x, yq.y, yq.z, yq.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const float d0 = __uint_as_float(dw4[p] << 16), d1 = __uint_as_float(dw4[p] & 0xFFFF0000u);
+            const float y0 = __uint_as_float(yw4[p] << 16), y1 = __uint_as_float(yw4[p] & 0xFFFF0000u);
+            o[p] = bf16_of_product(wj, d0) | (bf16_of_product(wj, d1) << 16);
+            acc = __fmaf_rn(d0, y0, acc);
+            acc = __fmaf_rn(d1, y1, acc);
+          }
+          *reinterpret_cast<uint4*>(dy + (int64_t)slot * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kAll, acc, o));
+      if (lane == 0) dw[t * k + j] = acc;
+    }
+  }
+}
+
+cudaError_t launch_combine_backward(const void* dout, const int32_t* inv, const float* w, const void* y, int64_t T,
+                                    int k, int64_t H, void* dy, float* dw, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  int64_t blocks = (T + 7) / 8;
+  if (blocks > 16 * (int64_t)num_sms()) blocks = 16 * (int64_t)num_sms();
+  combine_backward_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dout), inv, w,
+                                                      static_cast<const __nv_bfloat16*>(y), T, k, H,
+                                                      static_cast<__nv_bfloat16*>(dy), dw);
+  return cudaGetLastError();
+}
+
+// amax_bits[e] = max |src[row(r), 0..F)| over the rows r of expert e's group (slots
+// starts[e] .. starts[e] + counts[e] - 1), row(r) = rowmap[r] or r; float bits combined
+// with atomicMax (order-free for non-negative floats).  One warp per slot row.  amax_bits
+// must be zeroed first.
+__global__ void __launch_bounds__(256) group_amax_kernel(const __nv_bfloat16* __restrict__ src, int64_t ld, int64_t F,
+                                                         const int32_t* __restrict__ rowmap,
+                                                         const int32_t* __restrict__ starts,
+                                                         const int32_t* __restrict__ counts, int E, int64_t max_rows,
+                                                         uint32_t* __restrict__ amax_bits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t nwarp = (int64_t)gridDim.x * 8;
+  int64_t rows = starts[E];
+  if (rows > max_rows) rows = max_rows;
+  for (int64_t r = warp; r < rows; r += nwarp) {
+    const int e = find_group(starts, E, (int32_t)r);
+    if (r - starts[e] >= counts[e]) continue;               // group padding (warp-uniform)
+    const int64_t sr = rowmap != nullptr ? rowmap[r] : r;
+    uint32_t m = 0;
+    for (int64_t c = 8 * lane; c < F; c += 256) {
+      const uint4 q = ldg_nc(src + sr * ld + c);
+      const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(wv[i] & 0x7FFF7FFFu));
+    }
+    uint32_t mb = max(m & 0xFFFFu, m >> 16) << 16;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(kAll, mb, o));
+    if (lane == 0 && mb != 0u) atomicMax(amax_bits + e, mb);
+  }
+}
+
+cudaError_t launch_group_amax(const void* src, int64_t ld, int64_t F, const int32_t* rowmap, const int32_t* starts,
+                              const int32_t* counts, int E, int64_t max_rows, uint32_t* amax_bits, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t) * E, s);
+  if (err != cudaSuccess || max_rows == 0) return err;
+  int64_t blocks = (max_rows + 7) / 8;
+  if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
+  group_amax_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), ld, F, rowmap, starts, counts,
+                                                E, max_rows, amax_bits);
+  return cudaGetLastError();
+}
+
+// kofs[e] = sum over e' < e of max(1, ceil(counts[e'] / 256)) (counts == nullptr: every
+// group has `uniform` rows): the first 256-token K-block of each expert in the wgrad
+// operands.  One block of 1024 threads.
+__global__ void __launch_bounds__(1024) kofs_kernel(const int32_t* __restrict__ counts, int64_t uniform, int E,
+                                                    int32_t* __restrict__ kofs) {
+  __shared__ int32_t part[1024];
+  const int per = (E + 1023) / 1024;
+  const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+  int32_t local = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int64_t n = counts != nullptr ? counts[e] : uniform;
+    local += (int32_t)max((int64_t)1, (n + 255) / 256);
+  }
+  part[threadIdx.x] = local;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {   // inclusive scan
+    const int32_t v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int32_t run = part[threadIdx.x] - local;
+  for (int e = e0; e < e1; ++e) {
+    kofs[e] = run;
+    const int64_t n = counts != nullptr ? counts[e] : uniform;
+    run += (int32_t)max((int64_t)1, (n + 255) / 256);
+  }
+  if (threadIdx.x == 1023) kofs[E] = part[1023];
+}
+
+cudaError_t launch_kofs(const int32_t* counts, int64_t uniform, int E, int32_t* kofs, cudaStream_t s) {
+  kofs_kernel<<<1, 1024, 0, s>>>(counts, uniform, E, kofs);
+  return cudaGetLastError();
+}
+
+// Per-expert transposed NVFP4 into the GEMM-tiled layout.  For expert e, the source rows
+// are the expert's "tokens" t = 0 .. count_e - 1 (src row rowmap[start_e + t] or
+// start_e + t; uniform groups: e * uniform + t) and the columns its features f < F; the
+// quantised matrix is the transpose [Fp, tp_e] (tp_e = 256 * (kofs[e+1] - kofs[e]) tokens,
+// zero beyond count_e; rows F .. Fp - 1 zero), blocks of 16 along the tokens, one global
+// scale g_e = amax_e / 2688 for the matrix, RNE or stochastic rounding with key
+// seed + (((stream << 10) + e) << 40) and element index f * tp_e + t.  Output: R-row
+// blocks (128 or 256) by 256-token K-blocks; expert e's blocks start at block
+// (Fp / R) * kofs[e], row-block-major.
+//
+// One CTA per (expert, row block, K-block) unit: the 256 x R BF16 source tile goes into
+// shared memory with 16-byte asynchronous copies, each thread encodes pairs of features
+// (4-byte column reads, conflict-free across a warp) for one 16-token block at a time,
+// writes codes and scale bytes into the unit's shared-memory image, and one bulk store
+// writes the image (R * 144 bytes) whole.
+struct TQuant {
+  const __nv_bfloat16* src;
+  int64_t ld;
+  const int32_t* rowmap;     // nullable
+  const int32_t* starts;     // nullable: uniform groups
+  const int32_t* counts;     // nullable: uniform groups
+  int64_t uniform;
+  const int32_t* kofs;       // [E+1]
+  int E, F, Fp, R;
+  const uint32_t* amax_bits; // [E]
+  float* g_out;              // [E]
+  uint8_t* out;
+  int rounding;
+  uint64_t seed;
+  int stream;
+  int* status;
+};
+
+template <int R, int RND>
+__global__ void __launch_bounds__(256) tquant_kernel(const TQuant q) {
+  extern __shared__ __align__(128) uint8_t tsm[];
+  uint8_t* tile = tsm;                                        // [256 tokens][R features] BF16
+  uint8_t* img = tsm + 256 * R * 2;                           // the unit's R*144-byte image
+  const uint32_t tile_s = smem_u32(tile);
+  const int tid = threadIdx.x;
+  const int rblocks = q.Fp / R;
+  const int64_t units = (int64_t)q.kofs[q.E] * rblocks;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int32_t kg = (int32_t)(u / rblocks);
+    const int rb = (int)(u - (int64_t)kg * rblocks);
+    const int e = find_group(q.kofs, q.E, kg);
+    const int kb = kg - q.kofs[e];
+    const int64_t tp = 256 * (int64_t)(q.kofs[e + 1] - q.kofs[e]);
+    const int64_t start = q.starts != nullptr ? q.starts[e] : (int64_t)e * q.uniform;
+    const int64_t count = q.counts != nullptr ? q.counts[e] : q.uniform;
+    const int f0 = rb * R;
+    // 1. the source tile: tokens kb*256 .. +255 of the expert, features f0 .. f0+R-1
+    constexpr int kChunksPerRow = R * 2 / 16;
+    for (int i = tid; i < 256 * kChunksPerRow; i += 256) {
+      const int t = i / kChunksPerRow, ch = i - t * kChunksPerRow;
+      const int64_t tok = (int64_t)kb * 256 + t;
+      const int f = f0 + ch * 8;
+      const uint32_t dst = tile_s + (uint32_t)(t * R * 2 + ch * 16);
+      if (tok < count && f < q.F) {
+        const int64_t r = start + tok;
+        const int64_t sr = q.rowmap != nullptr ? q.rowmap[r] : r;
+        cp_async_16(dst, q.src + sr * q.ld + f);
+      } else {
+        *reinterpret_cast<uint4*>(tile + t * R * 2 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // 2. encode: feature pair (2p, 2p+1) of the unit, 16-token block b
+    const float g = __fdiv_rn(__uint_as_float(q.amax_bits[e]), kGlobalDivisor);
+    const float six_g = __fmul_rn(6.0f, g);
+    if (tid == 0 && kb == 0 && rb == 0) q.g_out[e] = g;
+    const uint64_t key = q.seed + ((((uint64_t)q.stream << 10) + (uint64_t)e) << 40);
+    for (int i = tid; i < (R / 2) * 16; i += 256) {
+      const int p = i % (R / 2), b = i / (R / 2);
+      float v[2][16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const uint32_t pr = *reinterpret_cast<const uint32_t*>(tile + (b * 16 + t) * R * 2 + p * 4);
+        v[0][t] = __uint_as_float(pr << 16);
+        v[1][t] = __uint_as_float(pr & 0xFFFF0000u);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rr = 2 * p + h;                          // row of the image
+        float am = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) am = fmaxf(am, fabsf(v[h][t]));
+        const BlockScale bs = block_scale(am, g, six_g);
+        float lo8[8], hi8[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          lo8[t] = v[h][t];
+          hi8[t] = v[h][8 + t];
+        }
+        uint2 cw;
+        if (RND == kRoundSR) {
+          const uint64_t j = ((uint64_t)(f0 + rr) * (uint64_t)tp + (uint64_t)kb * 256 + (uint64_t)b * 16) / 8u;
+          const uint32_t k0 = (uint32_t)key, k1 = (uint32_t)(key >> 32);
+          cw.x = e2m1x8_sr(lo8, bs, philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), k0, k1));
+          cw.y = e2m1x8_sr(hi8, bs, philox4x32_10(make_uint4((uint32_t)(j + 1), (uint32_t)((j + 1) >> 32), 0u, 0u),
+                                                  k0, k1));
+        } else {
+          cw = e2m1x16_rn(lo8, hi8, bs);
+        }
+        // codes: K-byte 8b of row rr, 128-byte swizzled; scale (rr, b)
+        *reinterpret_cast<uint2*>(img + rr * 128 + ((((b >> 1) ^ (rr & 7))) << 4) + (b & 1) * 8) = cw;
+        const int r128 = rr & 127;
+        img[R * 128 + (rr >> 7) * 2048 + (b >> 2) * 512 + (r128 & 31) * 16 + (r128 >> 5) * 4 + (b & 3)] =
+            (uint8_t)bs.sf;
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      uint8_t* dst = q.out + ((int64_t)rblocks * q.kofs[e] + (int64_t)rb * (tp / 256) + kb) * (int64_t)R * 144;
+      bulk_store(dst, img, R * 144);
+      bulk_commit();
+      bulk_wait_read<0>();     // the image is read before the next unit overwrites it
+    }
+    __syncthreads();
+  }
+  if (tid == 0) bulk_wait_all<0>();
+}
+
+template <int R, int RND>
+static cudaError_t launch_tq(const TQuant& q, int64_t max_units, cudaStream_t s) {
+  constexpr int kSmem = 256 * R * 2 + R * 144;
+  static std::atomic<bool> attr_set[64];
+  const cudaError_t err = set_smem_attr_once(attr_set, (const void*)tquant_kernel<R, RND>, kSmem);
+  if (err != cudaSuccess) return err;
+  int64_t grid = max_units;
+  const int64_t cap = (R == 128 ? 2 : 1) * (int64_t)num_sms();
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  tquant_kernel<R, RND><<<(int)grid, 256, kSmem, s>>>(q);
+  return cudaGetLastError();
+}
+
+// max_kblocks: an upper bound on kofs[E] (the grid is sized from it; the kernel reads the
+// exact count on the device).
+cudaError_t launch_tquant(const void* src, int64_t ld, const int32_t* rowmap, const int32_t* starts,
+                          const int32_t* counts, int64_t uniform, const int32_t* kofs, int E, int F, int Fp, int R,
+                          const uint32_t* amax_bits, float* g_out, uint8_t* out, int rounding, uint64_t seed,
+                          int stream_id, int64_t max_kblocks, cudaStream_t s) {
+  TQuant q;
+  q.src = static_cast<const __nv_bfloat16*>(src);
+  q.ld = ld;
+  q.rowmap = rowmap;
+  q.starts = starts;
+  q.counts = counts;
+  q.uniform = uniform;
+  q.kofs = kofs;
+  q.E = E;
+  q.F = F;
+  q.Fp = Fp;
+  q.R = R;
+  q.amax_bits = amax_bits;
+  q.g_out = g_out;
+  q.out = out;
+  q.rounding = rounding;
+  q.seed = seed;
+  q.stream = stream_id;
+  q.status = device_status_ptr();
+  const int64_t units = max_kblocks * (Fp / R);
+  if (R == 128)
+    return rounding == kRoundSR ? launch_tq<128, kRoundSR>(q, units, s) : launch_tq<128, kRoundRNE>(q, units, s);
+  return rounding == kRoundSR ? launch_tq<256, kRoundSR>(q, units, s) : launch_tq<256, kRoundRNE>(q, units, s);
+}
+
+}  // namespace nvfp4

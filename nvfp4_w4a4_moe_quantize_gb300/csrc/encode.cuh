@@ -1,11 +1,19 @@
 // NVFP4 element and scale encoding on the device (sm_103a).
 //
 // Scale arithmetic ("The 4-bitter Lesson: Balancing Stability and Performance in NVFP4
-// RL", §Baseline: E2M1 values, one E4M3 scale per 16 values, one FP32 global scale;
-// footnote 6 of §"Improving Gradient Stability": Q = clip(round(x/s), qmin, qmax)),
-// every step one IEEE float32 operation, round to nearest even, in this order:
-//   g = amax / 2688;  sf = E4M3_rn_satfinite(amax_block / (6 g));  s = decode(sf) * g;
-//   r = 1 / s;        code = E2M1(x * r)  (RNE, or stochastic rounding).
+// RL", §Baseline: E2M1 values, one E4M3 scale per 16 values, one FP32 global scale), every
+// step one IEEE float32 operation, round to nearest even, in this order:
+//   g = amax / 2688;  sf = E4M3_rn_satfinite(amax_block / (6 g));  s = decode(sf) * g.
+// Element code (footnote 6 of §"Improving Gradient Stability": Q = clip(round(x/s), qmin,
+// qmax)): round(x / s) of the exact quotient onto the E2M1 grid, ties to the even code,
+// or stochastic rounding of that quotient.  The quotient is never rounded before the
+// decision:
+//   * fast path: two float32 products |x| * r_lo <= |x| / s <= |x| * r_hi, with r_lo and r_hi
+//     bracketing 1/s; rounding is monotone, so where both round to the same code that is
+//     the code of the exact quotient (one in about 10^4 blocks fails this test);
+//   * exact path (the rest, and scales below 2^-60): the sign of |x| - m * s for each
+//     decision threshold m, from one fused multiply-add -- exact, because the exact
+//     difference is either zero or far above the smallest float32 subnormal.
 // All products / quotients use the explicit _rn intrinsics so that no FMA contraction or
 // approximate division can change a bit.
 #pragma once
@@ -24,6 +32,17 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
     f[2 * i] = __uint_as_float(w[i] << 16);
     f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
+}
+
+// max |x| of 16 BF16 values (two 16-byte chunks), as a float: sign-cleared BF16 bit
+// patterns order like the magnitudes (inputs are finite), two 16-bit maxima per
+// instruction.
+__device__ __forceinline__ float absmax16_bf16(const uint4& q0, const uint4& q1) {
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int i = 1; i < 8; ++i) asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(w[i] & 0x7FFF7FFFu));
+  return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
 }
 
 __device__ __forceinline__ float absmax8(const float (&f)[8]) {
@@ -46,28 +65,41 @@ __device__ __forceinline__ uint32_t e4m3_encode(float t) {
   return d & 0xFFu;
 }
 
+constexpr float kTinyScale = 8.673617379884035e-19f;   // 2^-60
+
 struct BlockScale {
   uint32_t sf;  // E4M3 byte written to the scale tensor
-  float r;      // encode multiplier 1/s, or 0 when the block decodes to zero
+  float s;      // effective decode scale decode(sf) * g; 0 when the block decodes to zero
+  float r_lo;   // fast path: 0 < r_lo * (1 + 2^-22) < 1/s < r_hi * (1 - 2^-22)  (0, 0 when s == 0)
+  float r_hi;
+  bool exact_only;  // 0 < s < 2^-60: every element takes the exact path
 };
 
 // Block scale of one 16-value block with max |x| = amax_b, given the scope's g and 6g.
+// The brackets come from the hardware reciprocal (rcp.approx.f32, at most one ulp from
+// 1/s): r * (1 -/+ 2^-18) leaves a margin of over 2^-19 on either side of 1/s, far more
+// than the rounding of the reciprocal, of the bracket product and of |x| * r (2^-23 +
+// 2 * 2^-24).
 __device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float six_g) {
   BlockScale bs;
+  bs.exact_only = false;
+  bs.r_lo = bs.r_hi = 0.0f;
   if (!(g > 0.0f)) {
     bs.sf = 0;
-    bs.r = 0.0f;
+    bs.s = 0.0f;
     return bs;
   }
   const float t = __fdiv_rn(amax_b, six_g);
   bs.sf = e4m3_encode(t);
-  const float s = __fmul_rn(e4m3_decode(bs.sf), g);
-  float r = 0.0f;
-  if (s > 0.0f) {
-    r = __frcp_rn(s);
-    if (!(r <= 3.402823466e38f)) r = 0.0f;   // s below 2^-128: reciprocal not finite
+  bs.s = __fmul_rn(e4m3_decode(bs.sf), g);
+  if (bs.s >= kTinyScale) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(bs.s));
+    bs.r_lo = __fmul_rn(r, 0.99999618530273438f);   // 1 - 2^-18
+    bs.r_hi = __fmul_rn(r, 1.0000038146972656f);    // 1 + 2^-18
+  } else if (bs.s > 0.0f) {
+    bs.exact_only = true;
   }
-  bs.r = r;
   return bs;
 }
 
@@ -78,8 +110,8 @@ __device__ __forceinline__ uint32_t canonical_zero(uint32_t w) {
 }
 
 // 8 scaled values -> 8 E2M1 codes (RNE, satfinite), element 2i in the low nibble of
-// byte i, packed little-endian into 32 bits.
-__device__ __forceinline__ uint32_t e2m1x8_rn(const float (&v)[8]) {
+// byte i, packed little-endian into 32 bits; zero magnitudes keep their sign bit.
+__device__ __forceinline__ uint32_t e2m1x8_raw(const float (&v)[8]) {
   uint32_t out;
   asm("{\n .reg .b8 b0, b1, b2, b3;\n"
       " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
@@ -89,7 +121,117 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float (&v)[8]) {
       " mov.b32 %0, {b0, b1, b2, b3};\n}"
       : "=r"(out)
       : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
-  return canonical_zero(out);
+  return out;
+}
+
+// v = f * r for 8 values, two per instruction (mul.rn.f32x2: each lane one IEEE product).
+__device__ __forceinline__ void scale8(const float (&f)[8], float r, float (&v)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %4};\n"
+        " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(v[2 * i]), "=f"(v[2 * i + 1])
+        : "f"(f[2 * i]), "f"(f[2 * i + 1]), "f"(r));
+}
+
+// |x| and s brought to where every product below stays exact in its sign: blocks with
+// s < 2^-60 are scaled by 2^64 (exact; their elements are at most about 9 s).
+__device__ __forceinline__ void exact_operands(float x, float s, float& a, float& t) {
+  a = fabsf(x);
+  t = s;
+  if (s < kTinyScale) {
+    a = __fmul_rn(a, 18446744073709551616.0f);   // 2^64
+    t = __fmul_rn(s, 18446744073709551616.0f);
+  }
+}
+
+// Exact round(|x| / s) (s > 0) onto the E2M1 grid, ties to the even code, saturating at 6:
+// the number of midpoints m (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) below the quotient, a
+// tie at m counting when the code above it is even.  |x| - m s is formed exactly by the
+// FMA and rounded once, which keeps its sign (zero only when it is exactly zero).
+__device__ __forceinline__ uint32_t e2m1_exact_rn(float x, float s) {
+  float a, t;
+  exact_operands(x, s, a, t);
+  const uint32_t c = (__fmaf_rn(-0.25f, t, a) > 0.0f) + (__fmaf_rn(-0.75f, t, a) >= 0.0f) +
+                     (__fmaf_rn(-1.25f, t, a) > 0.0f) + (__fmaf_rn(-1.75f, t, a) >= 0.0f) +
+                     (__fmaf_rn(-2.5f, t, a) > 0.0f) + (__fmaf_rn(-3.5f, t, a) >= 0.0f) +
+                     (__fmaf_rn(-5.0f, t, a) > 0.0f);
+  return c | ((__float_as_uint(x) >> 31) && c ? 8u : 0u);
+}
+
+// Element e of 8 values in registers (e is not a compile-time constant): a select tree,
+// no local-memory array.
+__device__ __forceinline__ float pick8(const float (&f)[8], uint32_t e) {
+  const float a = (e & 1u) ? f[1] : f[0], b = (e & 1u) ? f[3] : f[2];
+  const float c = (e & 1u) ? f[5] : f[4], d = (e & 1u) ? f[7] : f[6];
+  const float ab = (e & 2u) ? b : a, cd = (e & 2u) ? d : c;
+  return (e & 4u) ? cd : ab;
+}
+
+// E2M1 magnitude grid G and the midpoint between code c and c + 1 (c <= 6).
+__device__ __forceinline__ float e2m1_grid(uint32_t c) {
+  return c < 4u ? __fmul_rn((float)c, 0.5f) : (c < 6u ? (float)c - 2.0f : (c == 6u ? 4.0f : 6.0f));
+}
+__device__ __forceinline__ float e2m1_midpoint(uint32_t c) {
+  return c < 4u ? __fmaf_rn(0.5f, (float)c, 0.25f) : (c == 6u ? 5.0f : (float)c - 1.5f);
+}
+
+// 8 values of one block -> 8 E2M1 codes of round(x / s), packed as e2m1x8_raw, zero
+// magnitudes as +0.  The bracket codes lo (from |x| r_lo) and hi (|x| r_hi) differ only
+// where the quotient lies within the bracket's width of a midpoint, and there by one step
+// (midpoints are far apart relative to the bracket): those elements -- about 0.2% of
+// Gaussian data, most of them structured ties that the rounded g creates -- are settled
+// one at a time by the sign of |x| - m s for the one midpoint m between lo and hi.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float (&f)[8], const BlockScale& bs) {
+  if (!bs.exact_only) {
+    float vl[8], vh[8];
+    scale8(f, bs.r_lo, vl);
+    scale8(f, bs.r_hi, vh);
+    uint32_t lo = e2m1x8_raw(vl);
+    uint32_t diff = lo ^ e2m1x8_raw(vh);
+    while (diff != 0u) {
+      const uint32_t sh = (uint32_t)(__ffs((int)diff) - 1) & ~3u;
+      const uint32_t c = (lo >> sh) & 7u;                  // the lower candidate
+      const float x = pick8(f, sh >> 2);
+      const float d = __fmaf_rn(-e2m1_midpoint(c), bs.s, fabsf(x));
+      const uint32_t cnew = (d > 0.0f || (d == 0.0f && (c & 1u))) ? c + 1u : c;   // a tie goes to the even code
+      const uint32_t sign = cnew && (__float_as_uint(x) >> 31) ? 8u : 0u;
+      lo = (lo & ~(0xFu << sh)) | ((cnew | sign) << sh);
+      diff &= ~(0xFu << sh);
+    }
+    return canonical_zero(lo);
+  }
+  uint32_t out = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) out |= e2m1_exact_rn(f[e], bs.s) << (4 * e);
+  return out;
+}
+
+// One whole 16-value block (h0: values 0..7, h1: values 8..15) -> its 16 codes (x: 0..7,
+// y: 8..15), as e2m1x8_rn on both halves but with one settling loop for the block.
+__device__ __forceinline__ uint2 e2m1x16_rn(const float (&h0)[8], const float (&h1)[8], const BlockScale& bs) {
+  if (bs.exact_only) return make_uint2(e2m1x8_rn(h0, bs), e2m1x8_rn(h1, bs));
+  float vl[8], vh[8];
+  scale8(h0, bs.r_lo, vl);
+  scale8(h0, bs.r_hi, vh);
+  const uint32_t l0 = e2m1x8_raw(vl), d0 = l0 ^ e2m1x8_raw(vh);
+  scale8(h1, bs.r_lo, vl);
+  scale8(h1, bs.r_hi, vh);
+  const uint32_t l1 = e2m1x8_raw(vl), d1 = l1 ^ e2m1x8_raw(vh);
+  uint64_t lo = ((uint64_t)l1 << 32) | l0;
+  uint64_t diff = ((uint64_t)d1 << 32) | d0;
+  while (diff != 0ull) {
+    const uint32_t sh = (uint32_t)(__ffsll((long long)diff) - 1) & ~3u;
+    const uint32_t c = (uint32_t)(lo >> sh) & 7u;        // the lower candidate
+    const uint32_t e = sh >> 2;
+    const float x = (e & 8u) ? pick8(h1, e & 7u) : pick8(h0, e & 7u);
+    const float d = __fmaf_rn(-e2m1_midpoint(c), bs.s, fabsf(x));
+    const uint32_t cnew = (d > 0.0f || (d == 0.0f && (c & 1u))) ? c + 1u : c;   // a tie goes to the even code
+    const uint32_t sign = cnew && (__float_as_uint(x) >> 31) ? 8u : 0u;
+    lo = (lo & ~(0xFull << sh)) | ((uint64_t)(cnew | sign) << sh);
+    diff &= ~(0xFull << sh);
+  }
+  return make_uint2(canonical_zero((uint32_t)lo), canonical_zero((uint32_t)(lo >> 32)));
 }
 
 // Philox4x32-10 (Salmon et al., SC'11): 10 rounds of the Philox-4x32 bijection, key
@@ -106,9 +248,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Stochastic rounding of one scaled value to E2M1: lo <= |v| < hi neighbouring grid
+// Stochastic rounding of one scaled value v to E2M1: lo <= |v| < hi neighbouring grid
 // magnitudes, p = (|v| - lo) / (hi - lo) (exact), round up iff r16 < p * 2^16;
-// |v| >= 6 saturates.  Zero magnitude encodes as +0.
+// |v| >= 6 saturates.  Zero magnitude encodes as +0.  As a function of |v| this is the
+// number of thresholds tau_j = G_{j-1} + r16 (G_j - G_{j-1}) / 2^16 (j = 1..7, G the grid)
+// that |v| exceeds, so it is monotone in |v|.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
   const float a = fabsf(v);
   const uint32_t c = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) + (a >= 4.0f) +
@@ -125,15 +269,61 @@ __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
   return code | ((__float_as_uint(v) >> 31) && code ? 8u : 0u);
 }
 
-// 8 scaled values of one chunk with their Philox block output -> packed codes.
-__device__ __forceinline__ uint32_t e2m1x8_sr(const float (&v)[8], uint4 rnd) {
+// Exact stochastic rounding of the quotient |x| / s (s > 0): the number of thresholds
+// tau_j (above) with |x| > tau_j * s, each decided by the sign of one FMA (tau_j has at
+// most 19 significant bits, so |x| - tau_j s is either zero or far from underflow).
+__device__ __forceinline__ uint32_t e2m1_exact_sr(float x, float s, uint32_t r16) {
+  float a, t;
+  exact_operands(x, s, a, t);
+  const float u = __fmul_rn((float)r16, 1.52587890625e-05f);   // r16 / 2^16, exact
+  const float h = __fmul_rn(u, 0.5f);
+  const uint32_t c = (__fmaf_rn(-h, t, a) > 0.0f) + (__fmaf_rn(-__fadd_rn(0.5f, h), t, a) > 0.0f) +
+                     (__fmaf_rn(-__fadd_rn(1.0f, h), t, a) > 0.0f) +
+                     (__fmaf_rn(-__fadd_rn(1.5f, h), t, a) > 0.0f) +
+                     (__fmaf_rn(-__fadd_rn(2.0f, u), t, a) > 0.0f) +
+                     (__fmaf_rn(-__fadd_rn(3.0f, u), t, a) > 0.0f) +
+                     (__fmaf_rn(-__fadd_rn(4.0f, __fmul_rn(u, 2.0f)), t, a) > 0.0f);
+  return c | ((__float_as_uint(x) >> 31) && c ? 8u : 0u);
+}
+
+// 8 values of one chunk with their Philox block output -> packed codes of the
+// stochastically rounded exact quotients.  Bracketed like e2m1x8_rn: the count of
+// thresholds tau_j exceeded is monotone in |v|, and the thresholds are at least 0.5
+// apart, so where the bracket codes differ they differ by one step and the single
+// threshold tau between them decides: up iff |x| > tau s (an exact FMA sign).
+__device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockScale& bs, uint4 rnd) {
   const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+  if (!bs.exact_only) {
+    float vl[8], vh[8];
+    scale8(f, bs.r_lo, vl);
+    scale8(f, bs.r_hi, vh);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t r16 = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+      lo |= e2m1_sr(vl[e], r16) << (4 * e);
+      hi |= e2m1_sr(vh[e], r16) << (4 * e);
+    }
+    uint32_t diff = lo ^ hi;
+    while (diff != 0u) {
+      const uint32_t sh = (uint32_t)(__ffs((int)diff) - 1) & ~3u;
+      const uint32_t e = sh >> 2;
+      const uint32_t c = (lo >> sh) & 7u;                  // the lower candidate (< 7)
+      const uint32_t we = (e & 4u) ? ((e & 2u) ? w[3] : w[2]) : ((e & 2u) ? w[1] : w[0]);
+      const float u = __fmul_rn((float)((we >> (16 * (e & 1u))) & 0xFFFFu), 1.52587890625e-05f);
+      const float gap = c < 4u ? 0.5f : (c < 6u ? 1.0f : 2.0f);
+      const float tau = __fmaf_rn(u, gap, e2m1_grid(c));  // exact: at most 19 significant bits
+      const float x = pick8(f, e);
+      const uint32_t cnew = __fmaf_rn(-tau, bs.s, fabsf(x)) > 0.0f ? c + 1u : c;
+      const uint32_t sign = cnew && (__float_as_uint(x) >> 31) ? 8u : 0u;   // zero is +0
+      lo = (lo & ~(0xFu << sh)) | ((cnew | sign) << sh);
+      diff &= ~(0xFu << sh);
+    }
+    return lo;
+  }
   uint32_t out = 0;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const uint32_t r16 = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-    out |= e2m1_sr(v[e], r16) << (4 * e);
-  }
+  for (int e = 0; e < 8; ++e) out |= e2m1_exact_sr(f[e], bs.s, (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << (4 * e);
   return out;
 }
 

@@ -101,11 +101,59 @@ __device__ __forceinline__ void store_box(uint8_t* buf, const uint32_t (&w)[32],
   }
 }
 
-template <bool kSwiGLU>
-__global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
+// What one tile reads and writes.  Grouped rows (kRagged false): tile t is row block
+// t / n_tiles of the padded group layout and column block t % n_tiles; its expert is the
+// group holding the row block; K = g.K.  Ragged K (kRagged true, the weight gradients):
+// expert e = t / (m_tiles * n_tiles) owns g.m_rows rows of A and of D and its own
+// contraction of 256 * kb_e values (kb_e = kofs[e+1] - kofs[e]); A's blocks of expert e
+// start at block (m_rows / 128) * kofs[e], B's at (N / 256) * kofs[e], each row block's
+// kb_e K-blocks consecutive.
+struct TileJob {
+  const uint8_t* a;    // first K-block of A
+  const uint8_t* b;    // first K-block of B
+  int kblocks;
+  int e, n_tile;
+  int32_t row0;        // first output row
+  int32_t in_group;    // valid rows of the tile (>= 128: all)
+};
+
+template <bool kRagged>
+__device__ __forceinline__ TileJob tile_job(const GemmArgs& g, const int32_t* offsets, const int32_t* rows,
+                                            const uint8_t* A, const uint8_t* B, int t, int n_tiles, int m_tiles,
+                                            int kblocks) {
+  TileJob j;
+  if (kRagged) {
+    const int per_e = m_tiles * n_tiles;
+    j.e = t / per_e;
+    const int rem = t - j.e * per_e;
+    const int m_tile = rem / n_tiles;
+    j.n_tile = rem - m_tile * n_tiles;
+    const int32_t k0 = offsets[j.e];
+    j.kblocks = offsets[j.e + 1] - k0;
+    j.a = A + ((int64_t)m_tiles * k0 + (int64_t)m_tile * j.kblocks) * gt::kABlock;
+    j.b = B + ((int64_t)n_tiles * k0 + (int64_t)j.n_tile * j.kblocks) * gt::kBBlock;
+    j.row0 = j.e * g.m_rows + m_tile * gt::kBM;
+    j.in_group = gt::kBM;
+  } else {
+    const int m_tile = t / n_tiles;
+    j.n_tile = t - m_tile * n_tiles;
+    j.row0 = m_tile * gt::kBM;
+    j.e = find_group(offsets, g.E, j.row0);
+    j.kblocks = kblocks;
+    j.a = A + (int64_t)m_tile * kblocks * gt::kABlock;
+    j.b = B + ((int64_t)j.e * n_tiles + j.n_tile) * kblocks * gt::kBBlock;
+    j.in_group = rows[j.e] - (j.row0 - offsets[j.e]);
+  }
+  return j;
+}
+
+// kMode: 0 plain store, 1 SwiGLU epilogue, 2 plain store with ragged K per expert.
+template <int kMode>
+__global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
     grouped_gemm_tiled_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B,
                               const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
   using namespace gt;
+  constexpr bool kSwiGLU = kMode == 1, kRagged = kMode == 2;
   constexpr int kEpiWarps = epi_warps(kSwiGLU);
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -113,11 +161,13 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
 
   for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
   for (int i = threadIdx.x; i < g.E; i += blockDim.x) {
-    sm.rows[i] = g.rows[i];
+    sm.rows[i] = kRagged ? 0 : g.rows[i];
     sm.gb[i] = g.gb[i];
   }
   __syncthreads();
-  if (!groups_valid(sm.offsets, sm.rows, g.E, g.m_total)) {   // nothing is read or written
+  // nothing is read or written unless the group arrays are consistent (ragged K: g.offsets
+  // are the K-block prefix sums, every expert at least one block, at most g.m_total blocks)
+  if (kRagged ? !kblocks_valid(sm.offsets, g.E, g.m_total) : !groups_valid(sm.offsets, sm.rows, g.E, g.m_total)) {
     if (threadIdx.x == 0) set_status(g.status, kStatusBadInput);
     return;
   }
@@ -142,8 +192,8 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
   volatile int* abort = &sm.abort;
 
   const int n_tiles = g.N / kBN;
-  const int m_tiles = sm.offsets[g.E] / kBM;
-  const int total = m_tiles * n_tiles;
+  const int m_tiles = kRagged ? g.m_rows / kBM : sm.offsets[g.E] / kBM;   // ragged: per expert
+  const int total = kRagged ? g.E * m_tiles * n_tiles : m_tiles * n_tiles;
   const int kblocks = g.K / 256;
 
   if (warp < 2) {
@@ -151,16 +201,9 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
       const bool is_a = warp == 0;
       uint32_t stage = 0, phase = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
-        int64_t blk;
-        if (is_a) {
-          blk = m_tile;
-        } else {
-          const int e = find_group(sm.offsets, g.E, m_tile * kBM);
-          blk = (int64_t)e * n_tiles + n_tile;
-        }
-        const uint8_t* src = (is_a ? A : B) + blk * kblocks * (int64_t)(is_a ? kABlock : kBBlock);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const TileJob job = tile_job<kRagged>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks);
+        const uint8_t* src = is_a ? job.a : job.b;
+        for (int kb = 0; kb < job.kblocks; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, g.status, abort)) goto producer_done;
           const uint32_t bytes = is_a ? kABlock : kBBlock;
           mbar_arrive_expect_tx(&sm.full[stage], bytes);
@@ -179,7 +222,9 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const int kbt = kRagged ? tile_job<true>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks).kblocks
+                                : kblocks;
+        for (int kb = 0; kb < kbt; ++kb) {
           if (!mbar_wait(&sm.full[stage], phase, g.status, abort)) goto mma_done;
           tc_fence_after();
           const uint32_t sfa_t = tmem + kSFCol0 + stage * kSFStageCols;
@@ -259,14 +304,13 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
     bool aborted = false;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
-      const int32_t row0 = m_tile * kBM;
-      const int e = find_group(sm.offsets, g.E, row0);
-      const int32_t in_group = sm.rows[e] - (row0 - sm.offsets[e]);
+      const TileJob job = tile_job<kRagged>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks);
+      const int n_tile = job.n_tile, e = job.e;
+      const int32_t row0 = job.row0, in_group = job.in_group;
       const bool valid = q * 32 + lane < in_group;
       const bool full_warp = q * 32 + 32 <= in_group;             // warp-uniform
       const int64_t row = (int64_t)row0 + q * 32 + lane;
-      const float ga = valid ? g.ga[row] : 0.0f;
+      const float ga = kRagged ? g.ga[e] : (valid ? g.ga[row] : 0.0f);   // ragged: one scale per expert
       // every lane waits (bounded), then the warp leaves together if any lane gave up
       const bool acc_ready = mbar_wait(&sm.accf, it & 1, g.status, abort);
       if (!__all_sync(0xFFFFFFFFu, acc_ready)) {
@@ -433,24 +477,32 @@ __global__ void __launch_bounds__(gt::threads(kSwiGLU), 1)
   if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool kSwiGLU>
+template <int kMode>
 static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
-                                int64_t max_m_tiles, cudaStream_t s) {
-  if (kSwiGLU && g.silu_tab == nullptr) return cudaErrorInvalidValue;
+                                int64_t tiles, cudaStream_t s) {
+  if (kMode == 1 && g.silu_tab == nullptr) return cudaErrorInvalidValue;
   static std::atomic<bool> attr_set[64];   // the attribute is set once per device
-  cudaError_t err = set_smem_attr_once(attr_set, (const void*)grouped_gemm_tiled_kernel<kSwiGLU>, (int)gt::kSmemBytes);
+  cudaError_t err =
+      set_smem_attr_once(attr_set, (const void*)grouped_gemm_tiled_kernel<kMode>, (int)gt::kSmemBytes);
   if (err != cudaSuccess) return err;
-  const int64_t tiles = max_m_tiles * (g.N / gt::kBN);
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
-  grouped_gemm_tiled_kernel<kSwiGLU><<<grid, gt::threads(kSwiGLU), gt::kSmemBytes, s>>>(A, B, tmd, g);
+  grouped_gemm_tiled_kernel<kMode><<<grid, gt::threads(kMode == 1), gt::kSmemBytes, s>>>(A, B, tmd, g);
   return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
                                       int64_t max_m_tiles, bool swiglu, cudaStream_t s) {
-  return swiglu ? launch_tiled<true>(A, B, tmd, g, max_m_tiles, s) : launch_tiled<false>(A, B, tmd, g, max_m_tiles, s);
+  const int64_t tiles = max_m_tiles * (g.N / gt::kBN);
+  return swiglu ? launch_tiled<1>(A, B, tmd, g, tiles, s) : launch_tiled<0>(A, B, tmd, g, tiles, s);
+}
+
+cudaError_t launch_grouped_gemm_ragged_k(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd,
+                                         const GemmArgs& g, cudaStream_t s) {
+  if (g.m_rows <= 0 || g.m_rows % gt::kBM != 0) return cudaErrorInvalidValue;
+  const int64_t tiles = (int64_t)g.E * (g.m_rows / gt::kBM) * (g.N / gt::kBN);
+  return launch_tiled<2>(A, B, tmd, g, tiles, s);
 }
 
 int tiled_max_experts() { return gt::kMaxE; }

@@ -30,4 +30,15 @@ __device__ __forceinline__ bool groups_valid(const int32_t* off, const int32_t* 
   return __syncthreads_or(bad) == 0;
 }
 
+// The K-block prefix sums of a ragged-K grouped GEMM (already in shared memory):
+// kofs[0] == 0, every expert at least one block, kofs[E] <= cap.  Block-wide, like
+// groups_valid.
+__device__ __forceinline__ bool kblocks_valid(const int32_t* kofs, int E, int64_t cap) {
+  int bad = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    if (kofs[i + 1] - kofs[i] < 1) bad = 1;
+  if (threadIdx.x == 0 && (E < 1 || kofs[0] != 0 || (int64_t)kofs[E] > cap)) bad = 1;
+  return __syncthreads_or(bad) == 0;
+}
+
 }  // namespace nvfp4

@@ -22,8 +22,10 @@ struct QuantArgs {
   float* g_out;            // nullable
   uint8_t* codes;          // output codes, codes_ld bytes per output row
   int64_t codes_ld;
-  uint8_t* sf;             // tiled scales
+  uint8_t* sf;             // tiled scales (or row-major, see sf_row_bytes)
   int64_t sf_words;        // 4-scale words per row of the tile grid = ceil(cols_pad / 64)
+  int64_t sf_row_bytes;    // > 0: row-major scales [rows, cols/16] (cols % 64 == 0, no padding
+                           //      rows or words); 0: the 128x4 tiled layout
   int64_t cols_pad;        // stored columns (>= cols): codes / scales beyond cols are zero
   int64_t rows_total;      // rows visited; rows..rows_total-1 only get zero scales
   int map;                 // kMap*
@@ -46,6 +48,8 @@ struct GemmArgs {
   const int32_t* offsets;  // [E+1] padded group starts
   const int32_t* rows;     // [E] valid rows per group
   int64_t m_total;         // rows of A, D (and ga): every group must lie inside [0, m_total)
+                           // (ragged K: the K-blocks the operands hold)
+  int32_t m_rows;          // ragged K: rows of A and of D per expert (a multiple of 128)
   int32_t E;
   int32_t N, K;
   void* d;
@@ -116,6 +120,21 @@ cudaError_t launch_mx_dequantize(const uint8_t* codes, const uint8_t* sf, int64_
 cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
                                       int64_t max_m_tiles, bool swiglu, cudaStream_t s);
 int tiled_max_experts();
+// The same kernel over ragged K per expert (the weight-gradient GEMMs): g.offsets = the
+// K-block prefix sums kofs [E+1], g.m_rows rows of A and D per expert, g.ga / g.gb one
+// scale per expert, D [E * m_rows, N] through tmd (plain store).
+cudaError_t launch_grouped_gemm_ragged_k(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd,
+                                         const GemmArgs& g, cudaStream_t s);
+// Backward kernels (backward.cu).
+cudaError_t launch_combine_backward(const void* dout, const int32_t* inv, const float* w, const void* y, int64_t T,
+                                    int k, int64_t H, void* dy, float* dw, cudaStream_t s);
+cudaError_t launch_group_amax(const void* src, int64_t ld, int64_t F, const int32_t* rowmap, const int32_t* starts,
+                              const int32_t* counts, int E, int64_t max_rows, uint32_t* amax_bits, cudaStream_t s);
+cudaError_t launch_kofs(const int32_t* counts, int64_t uniform, int E, int32_t* kofs, cudaStream_t s);
+cudaError_t launch_tquant(const void* src, int64_t ld, const int32_t* rowmap, const int32_t* starts,
+                          const int32_t* counts, int64_t uniform, const int32_t* kofs, int E, int F, int Fp, int R,
+                          const uint32_t* amax_bits, float* g_out, uint8_t* out, int rounding, uint64_t seed,
+                          int stream_id, int64_t max_kblocks, cudaStream_t s);
 // Slot r (r < min(*n_rows_dev, max_rows), a multiple of 128) of the 128-row-block tiled
 // `dst` gets token perm[r]'s row of the 128-row-block tiled `src` and dst_g[r] = src_g[perm[r]];
 // slots with perm[r] < 0 are not written.  K % 256 == 0.
@@ -148,8 +167,10 @@ cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, in
                            void* out, cudaStream_t s);
 // SwiGLU backward: [dgate | dup] (BF16 [rows, 2I]) from [gate | up] (BF16 [rows, 2I]) and dh
 // (BF16 [rows, I]); I % 8 == 0.
+// gu_interleaved: gu holds gate/up in the 64-chunk interleave of the prepared W13;
+// dh_ld: row pitch of dh (0: I).
 cudaError_t launch_swiglu_backward(const void* gu, const void* dh, int64_t rows, int64_t I, void* dgu,
-                                   cudaStream_t s);
+                                   cudaStream_t s, bool gu_interleaved = false, int64_t dh_ld = 0);
 // rows: rows of d to visit; nrows_dev (nullable): device count that caps rows.
 cudaError_t launch_swiglu_quant(const void* d, const int32_t* perm, int64_t rows, const int32_t* nrows_dev,
                                 int64_t I, int64_t Ip, void* h_out, uint8_t* hq, uint8_t* hsf, float* gh,

@@ -58,5 +58,6 @@ extern "C" nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int6
   uint32_t* scratch = noalloc_scratch();
   if (scratch == nullptr) return NVFP4_ERR_CUDA;
   return nvfp4_quantize(x, rows, cols, ld_elems, mode, group_rows, rounding, seed, rng_offset, global_scale_in,
-                        global_scale_out, codes_out, sf_out, scratch, sizeof(uint32_t) * kNoAllocMaxScopes, stream);
+                        global_scale_out, codes_out, sf_out, NVFP4_SF_SWIZZLED_128x4, scratch,
+                        sizeof(uint32_t) * kNoAllocMaxScopes, stream);
 }

@@ -28,6 +28,12 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 __device__ __forceinline__ int64_t sf_word_offset(int64_t r, int64_t w, int64_t sf_words) {
   return ((r >> 7) * sf_words + w) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
+// The 32-bit word holding scale columns 4w .. 4w+3 of row r in the standalone output:
+// the 128x4 tiled layout, or row-major [rows, cols/16] when a.sf_row_bytes > 0.
+__device__ __forceinline__ uint32_t* sf_at(const QuantArgs& a, int64_t r, int64_t w) {
+  return reinterpret_cast<uint32_t*>(a.sf + (a.sf_row_bytes ? r * a.sf_row_bytes + 4 * w
+                                                              : sf_word_offset(r, w, a.sf_words)));
+}
 
 // Output addressing for both layouts: 8 bytes of codes at byte `b` of output row `orow`,
 // and the 32-bit word holding scale columns 4w .. 4w+3.
@@ -36,7 +42,54 @@ __device__ __forceinline__ uint8_t* code_ptr(const QuantArgs& a, int64_t orow, i
 }
 __device__ __forceinline__ uint8_t* sfw_ptr(const QuantArgs& a, int64_t orow, int64_t w) {
   return a.tiled_R ? a.codes + tiled_sf_offset(orow, 4 * w, a.kblocks, a.tiled_R)
-                   : a.sf + sf_word_offset(orow, w, a.sf_words);
+                   : reinterpret_cast<uint8_t*>(sf_at(a, orow, w));
+}
+
+// Output addressing of one row, set up once per row so that each block's code and scale
+// addresses are a few 32-bit operations.  Codes of block b (8 bytes) sit at
+//   codes + (b >> 4) * code_outer + ((((b >> 1) & 7) ^ swz) << 4) + (b & 1) * 8
+// (row-major: code_outer = 128, swz = 0; GEMM-tiled: code_outer = one K-block, swz = the
+// row's swizzle), and scale word w (columns 4w .. 4w+3) at
+//   sf + (w >> 2) * sf_outer + (w & 3) * sf_inner.
+struct RowOut {
+  uint8_t* codes;
+  uint8_t* sf;
+  uint32_t code_outer, swz, sf_outer, sf_inner;
+};
+
+__device__ __forceinline__ RowOut row_out(const QuantArgs& a, int64_t orow) {
+  RowOut o;
+  if (a.tiled_R) {
+    const int lg = tiled_log2_rows(a.tiled_R);
+    const int64_t blk = orow >> lg, rr = orow & (a.tiled_R - 1), r128 = rr & 127;
+    const int64_t base = blk * a.kblocks * tiled_block_bytes(a.tiled_R);
+    o.codes = a.codes + base + rr * 128;
+    o.sf = a.codes + base + (int64_t)a.tiled_R * 128 + (rr >> 7) * 2048 + (r128 & 31) * 16 + (r128 >> 5) * 4;
+    o.code_outer = o.sf_outer = (uint32_t)tiled_block_bytes(a.tiled_R);
+    o.swz = (uint32_t)(rr & 7);
+    o.sf_inner = 512;
+  } else {
+    o.codes = a.codes + orow * a.codes_ld;
+    o.code_outer = 128;
+    o.swz = 0;
+    if (a.sf_row_bytes) {
+      o.sf = a.sf + orow * a.sf_row_bytes;
+      o.sf_outer = 16;
+      o.sf_inner = 4;
+    } else {
+      o.sf = a.sf + ((orow >> 7) * a.sf_words) * 512 + (orow & 31) * 16 + ((orow >> 5) & 3) * 4;
+      o.sf_outer = 2048;
+      o.sf_inner = 512;
+    }
+  }
+  return o;
+}
+__device__ __forceinline__ uint2* row_codes(const RowOut& o, uint32_t b) {
+  return reinterpret_cast<uint2*>(o.codes + (b >> 4) * o.code_outer + ((((b >> 1) & 7u) ^ o.swz) << 4) +
+                                  (b & 1u) * 8);
+}
+__device__ __forceinline__ uint32_t* row_sf_word(const RowOut& o, uint32_t w) {
+  return reinterpret_cast<uint32_t*>(o.sf + (w >> 2) * o.sf_outer + (w & 3u) * o.sf_inner);
 }
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
@@ -179,18 +232,16 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, int64_t row, co
     const int64_t col = 8 * lane + 256 * i;
     const bool active = col < a.cols;
     const BlockScale bs = block_scale(bm[i], g, six_g);
-    float f[8], v[8];
+    float f[8];
     bf16x8_to_f32(q[i], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(f[e], bs.r);
     uint32_t word;
     if (RND == kRoundSR) {
       const uint64_t j = a.rng_offset + (uint64_t)(row * a.cols + col) / 8u;
       const uint4 rnd = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), (uint32_t)a.seed,
                                       (uint32_t)(a.seed >> 32));
-      word = e2m1x8_sr(v, rnd);
+      word = e2m1x8_sr(f, bs, rnd);
     } else {
-      word = e2m1x8_rn(v);
+      word = e2m1x8_rn(f, bs);
     }
     const uint32_t sfb = active ? bs.sf : 0u;
     const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
@@ -199,10 +250,10 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, int64_t row, co
     const uint32_t sfw = sfb | (s2 << 8) | (s4 << 16) | (s6 << 24);
     if (active) *reinterpret_cast<uint32_t*>(a.codes + orow * a.codes_ld + col / 2) = word;
     if ((lane & 7) == 0 && active)
-      *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, 4 * i + lane / 8, a.sf_words)) = sfw;
+      *sf_at(a, orow, 4 * i + lane / 8) = sfw;
   }
   for (int64_t w = data_words + lane; w < a.sf_words; w += 32)
-    *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(orow, w, a.sf_words)) = 0u;
+    *sf_at(a, orow, w) = 0u;
   for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
     *reinterpret_cast<uint2*>(a.codes + orow * a.codes_ld + b) = make_uint2(0u, 0u);
   if (lane == 0 && a.g_out != nullptr) {
@@ -216,7 +267,7 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, int64_t row, co
 __device__ __forceinline__ void zero_pad_rows(const QuantArgs& a, int64_t warp, int64_t nwarp, int lane) {
   for (int64_t row = a.rows + warp; row < a.rows_total; row += nwarp)
     for (int64_t w = lane; w < a.sf_words; w += 32)
-      *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(row, w, a.sf_words)) = 0u;
+      *sf_at(a, row, w) = 0u;
 }
 
 // Register path (any width up to 8192 columns): the warp loads its row straight into
@@ -249,6 +300,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(QuantArgs a) {
 // contiguous bytes) and four neighbouring lanes gather one 32-bit scale word.
 constexpr int kQWarps = 8;
 constexpr int kQMaxStages = 8;
+constexpr int kQMaxSlots = 4;           // 16-value blocks per lane: rows of up to 2048 columns
 constexpr size_t kQSmemMax = 200 * 1024;
 __host__ __device__ constexpr size_t stream_smem_bytes(int stages, int stride) {
   return (size_t)kQWarps * stages * stride + (size_t)kQWarps * stages * sizeof(uint64_t) + 16;
@@ -256,49 +308,25 @@ __host__ __device__ constexpr size_t stream_smem_bytes(int stages, int stride) {
 
 // One 16-value block (two 16-byte chunks of BF16) -> its E4M3 scale byte and 8 bytes of
 // codes, given the scope's g and 6g.
+// amax_b < 0: the block max is computed here.
 template <int RND>
 __device__ __forceinline__ void encode_regs(const QuantArgs& a, int64_t row, int64_t blk, const uint4& q0,
                                             const uint4& q1, float g, float six_g, uint32_t& sf_out,
-                                            uint2& codes_out) {
-  float f[16];
-  {
-    float h0[8], h1[8];
-    bf16x8_to_f32(q0, h0);
-    bf16x8_to_f32(q1, h1);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      f[e] = h0[e];
-      f[8 + e] = h1[e];
-    }
-  }
-  float am = 0.0f;
-#pragma unroll
-  for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(f[e]));
-  const BlockScale bs = block_scale(am, g, six_g);
-  float v0[8], v1[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    v0[e] = __fmul_rn(f[e], bs.r);
-    v1[e] = __fmul_rn(f[8 + e], bs.r);
-  }
+                                            uint2& codes_out, float amax_b = -1.0f) {
+  float h0[8], h1[8];
+  bf16x8_to_f32(q0, h0);
+  bf16x8_to_f32(q1, h1);
+  const BlockScale bs = block_scale(amax_b >= 0.0f ? amax_b : fmaxf(absmax8(h0), absmax8(h1)), g, six_g);
   if (RND == kRoundSR) {
     const uint64_t j = a.rng_offset + (uint64_t)(row * a.cols + blk * 16) / 8u;
     const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
-    codes_out.x = e2m1x8_sr(v0, philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), k0, k1));
-    codes_out.y = e2m1x8_sr(v1, philox4x32_10(make_uint4((uint32_t)(j + 1), (uint32_t)((j + 1) >> 32), 0u, 0u),
-                                              k0, k1));
+    codes_out.x = e2m1x8_sr(h0, bs, philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), k0, k1));
+    codes_out.y = e2m1x8_sr(h1, bs, philox4x32_10(make_uint4((uint32_t)(j + 1), (uint32_t)((j + 1) >> 32), 0u, 0u),
+                                                  k0, k1));
   } else {
-    codes_out.x = e2m1x8_rn(v0);
-    codes_out.y = e2m1x8_rn(v1);
+    codes_out = e2m1x16_rn(h0, h1, bs);
   }
   sf_out = bs.sf;
-}
-
-template <int RND>
-__device__ __forceinline__ void encode_block(const QuantArgs& a, int64_t row, int64_t blk, const uint8_t* src,
-                                             float g, float six_g, uint32_t& sf_out, uint2& codes_out) {
-  encode_regs<RND>(a, row, blk, *reinterpret_cast<const uint4*>(src), *reinterpret_cast<const uint4*>(src + 16), g,
-                   six_g, sf_out, codes_out);
 }
 
 // Scopes whose global scale is known before encoding (per tensor, per group: after the
@@ -351,7 +379,7 @@ __global__ void __launch_bounds__(256) quantize_known_scale_kernel(QuantArgs a) 
   }
   if (a.tiled_R == 0)
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (a.rows_total - a.rows) * words; i += stride)
-      *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(a.rows + i / words, i % words, words)) = 0u;
+      *sf_at(a, a.rows + i / words, i % words) = 0u;
 }
 
 // Known-scale scopes over row-major rows of a multiple of 64 columns: the same encoding
@@ -365,61 +393,77 @@ template <int RND, typename Idx>
 __global__ void __launch_bounds__(256) quantize_known_coalesced_kernel(QuantArgs a) {
   constexpr int kSlabs = 2;
   const int lane = threadIdx.x & 31;
-  const int64_t bpr = a.cols / 16, total = a.rows * bpr;
+  const Idx bpr = (Idx)(a.cols / 16);
+  const int64_t total = a.rows * (int64_t)bpr;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
   float g0 = 0.0f;
   if (a.mode == kScopeTensor)
     g0 = a.g_in ? a.g_in[0] : __fdiv_rn(__uint_as_float(a.amax_bits[0]), kGlobalDivisor);
-  for (int64_t base = warp0 * 32 * kSlabs; base < total; base += wstride * 32 * kSlabs) {
+  const float six_g0 = __fmul_rn(6.0f, g0);
+  // (row, block column) of this lane's block in slab 0, advanced without divisions: one
+  // iteration moves by `step` blocks, slab s by 32 s more
+  const int64_t step = wstride * 32 * kSlabs;
+  const Idx step_r = (Idx)(step / (int64_t)bpr), step_c = (Idx)(step % (int64_t)bpr);
+  int64_t base = warp0 * 32 * kSlabs;
+  Idx r0 = (Idx)((base + lane) / (int64_t)bpr), c0 = (Idx)((base + lane) % (int64_t)bpr);
+  for (; base < total; base += step) {
     uint4 v0[kSlabs], v1[kSlabs];
-    int64_t row[kSlabs], cb[kSlabs];
+    Idx row[kSlabs], cb[kSlabs];
     bool live[kSlabs];
 #pragma unroll
     for (int s2 = 0; s2 < kSlabs; ++s2) {
-      const int64_t u = base + 32 * s2 + lane;
-      live[s2] = u < total;
-      const Idx r = live[s2] ? (Idx)u / (Idx)bpr : (Idx)0;
-      row[s2] = (int64_t)r;
-      cb[s2] = live[s2] ? (int64_t)((Idx)u - r * (Idx)bpr) : 0;
+      Idx r = r0, c = c0 + 32 * s2;
+      while (c >= bpr) {
+        c -= bpr;
+        ++r;
+      }
+      row[s2] = r;
+      cb[s2] = c;
+      live[s2] = base + 32 * s2 + lane < total;
       v0[s2] = v1[s2] = make_uint4(0u, 0u, 0u, 0u);
       if (live[s2]) {
-        const __nv_bfloat16* src = a.x + row[s2] * a.ld + 16 * cb[s2];
+        const __nv_bfloat16* src = a.x + (int64_t)r * a.ld + 16 * (int64_t)c;
         v0[s2] = ld_nc_v4(src);
         v1[s2] = ld_nc_v4(src + 8);
       }
     }
+    c0 += step_c;
+    r0 += step_r;
+    if (c0 >= bpr) {
+      c0 -= bpr;
+      ++r0;
+    }
 #pragma unroll
     for (int s2 = 0; s2 < kSlabs; ++s2) {
-      float g = g0;
+      float g = g0, six_g = six_g0;
       int64_t gi = 0;
       if (a.mode != kScopeTensor) {
         gi = (int64_t)((uint64_t)row[s2] / (uint64_t)a.group_rows);
         g = a.g_in ? a.g_in[gi] : __fdiv_rn(__uint_as_float(a.amax_bits[gi]), kGlobalDivisor);
+        six_g = __fmul_rn(6.0f, g);
       }
       uint32_t sf = 0;
       uint2 cw = make_uint2(0u, 0u);
-      encode_regs<RND>(a, row[s2], cb[s2], v0[s2], v1[s2], g, __fmul_rn(6.0f, g), sf, cw);
-      if (live[s2]) *reinterpret_cast<uint2*>(a.codes + row[s2] * a.codes_ld + 8 * cb[s2]) = cw;
+      encode_regs<RND>(a, row[s2], cb[s2], v0[s2], v1[s2], g, six_g, sf, cw);
+      if (live[s2]) *reinterpret_cast<uint2*>(a.codes + (int64_t)row[s2] * a.codes_ld + 8 * (int64_t)cb[s2]) = cw;
       // the scale word of this lane's 64-value group: block k of it sits at lane 4q + k
-      const int q0 = lane & ~3;
-      uint32_t word = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) word |= __shfl_sync(kFull, sf, q0 + k) << (8 * k);
-      if (live[s2] && (lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(row[s2], cb[s2] / 4, a.sf_words)) = word;
+      const uint32_t s1 = __shfl_down_sync(kFull, sf, 1);
+      const uint32_t s2w = __shfl_down_sync(kFull, sf, 2);
+      const uint32_t s3 = __shfl_down_sync(kFull, sf, 3);
+      if (live[s2] && (lane & 3) == 0) *sf_at(a, row[s2], cb[s2] / 4) = sf | (s1 << 8) | (s2w << 16) | (s3 << 24);
       if (live[s2] && cb[s2] == 0 && a.g_out != nullptr &&
-          (a.mode == kScopeTensor ? row[s2] == 0 : row[s2] % a.group_rows == 0))
+          (a.mode == kScopeTensor ? row[s2] == 0 : (int64_t)row[s2] % a.group_rows == 0))
         a.g_out[gi] = g;
     }
   }
   const int64_t stride = (int64_t)gridDim.x * blockDim.x, words = a.sf_words;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (a.rows_total - a.rows) * words; i += stride)
-    *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(a.rows + i / words, i % words, words)) = 0u;
+    *sf_at(a, a.rows + i / words, i % words) = 0u;
 }
 
 template <int RND>
-__global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kQWarps * 32, RND == kRoundSR ? 2 : 3) quantize_rows_stream_kernel(QuantArgs a) {
   extern __shared__ __align__(128) uint8_t qsm[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t warp = (int64_t)blockIdx.x * kQWarps + wib;
@@ -468,15 +512,22 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
       s = s + 1 == kQStages ? 0 : s + 1;
       continue;
     }
+    // block maxima of the row from the packed BF16 bits (block b of the row at lane b % 32,
+    // slot b / 32; rows of up to 2048 columns), kept for the encode pass
+    float bmax[kQMaxSlots];
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kQMaxSlots; ++i) {
+      const int64_t blk = lane + 32 * i;
+      bmax[i] = 0.0f;
+      if (blk < nblk) {
+        bmax[i] = absmax16_bf16(*reinterpret_cast<const uint4*>(buf + blk * 32),
+                                *reinterpret_cast<const uint4*>(buf + blk * 32 + 16));
+        m = fmaxf(m, bmax[i]);
+      }
+    }
     float g;
     if (a.mode == kScopeRow) {
-      float m = 0.0f;
-      for (int64_t b = lane; b < nblk; b += 32) {
-        float h0[8], h1[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(buf + b * 32), h0);
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(buf + b * 32 + 16), h1);
-        m = fmaxf(m, fmaxf(absmax8(h0), absmax8(h1)));
-      }
       m = warp_max(m);
       g = a.g_in ? a.g_in[row] : __fdiv_rn(m, kGlobalDivisor);
     } else if (a.mode == kScopeTensor) {
@@ -487,18 +538,23 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
     }
     const float six_g = __fmul_rn(6.0f, g);
     const int64_t orow = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
-    for (int64_t b0 = 0; b0 < nblk; b0 += 32) {
-      const int64_t blk = b0 + lane;
+    const RowOut ro = row_out(a, orow);
+#pragma unroll
+    for (int i = 0; i < kQMaxSlots; ++i) {
+      if (32 * i >= nblk) break;                       // warp-uniform
+      const uint32_t blk = (uint32_t)lane + 32u * i;
       const bool active = blk < nblk;
       uint32_t sfb = 0;
       uint2 cw = make_uint2(0u, 0u);
-      if (active) encode_block<RND>(a, row, blk, buf + blk * 32, g, six_g, sfb, cw);
+      if (active)
+        encode_regs<RND>(a, row, blk, *reinterpret_cast<const uint4*>(buf + blk * 32),
+                         *reinterpret_cast<const uint4*>(buf + blk * 32 + 16), g, six_g, sfb, cw, bmax[i]);
       const uint32_t s1 = __shfl_down_sync(kFull, sfb, 1);
       const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
       const uint32_t s3 = __shfl_down_sync(kFull, sfb, 3);
       const uint32_t sfw = sfb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-      if (active) *reinterpret_cast<uint2*>(code_ptr(a, orow, blk * 8)) = cw;
-      if ((lane & 3) == 0 && active) *reinterpret_cast<uint32_t*>(sfw_ptr(a, orow, blk / 4)) = sfw;
+      if (active) *row_codes(ro, blk) = cw;
+      if ((lane & 3) == 0 && active) *row_sf_word(ro, blk >> 2) = sfw;
     }
     fence_proxy_async_smem();   // this row's reads of the buffer precede the next bulk write
     __syncwarp();
@@ -509,9 +565,8 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_stream_kernel(Quan
         bulk_load(ring + s * stride, a.x + r2 * a.ld, row_bytes, &bars[s]);
       }
     }
-    for (int64_t w = data_words + lane; w < a.sf_words; w += 32) *reinterpret_cast<uint32_t*>(sfw_ptr(a, orow, w)) = 0u;
-    for (int64_t b = a.cols / 2 + 8 * lane; b < a.cols_pad / 2; b += 256)
-      *reinterpret_cast<uint2*>(code_ptr(a, orow, b)) = make_uint2(0u, 0u);
+    for (int64_t w = data_words + lane; w < a.sf_words; w += 32) *row_sf_word(ro, (uint32_t)w) = 0u;
+    for (int64_t b = nblk + lane; b < a.cols_pad / 16; b += 32) *row_codes(ro, (uint32_t)b) = make_uint2(0u, 0u);
     if (lane == 0 && a.g_out != nullptr) {
       if (a.mode == kScopeRow) a.g_out[row] = g;
       else if (a.mode == kScopeTensor && row == 0) a.g_out[0] = g;
@@ -534,14 +589,10 @@ __device__ __forceinline__ void requant_block(const uint4& q0, const uint4& q1, 
   bf16x8_to_f32(q0, v0);
   bf16x8_to_f32(q1, v1);
   const BlockScale bs = block_scale(fmaxf(absmax8(v0), absmax8(v1)), g, __fmul_rn(6.0f, g));
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    v0[e] = __fmul_rn(v0[e], bs.r);
-    v1[e] = __fmul_rn(v1[e], bs.r);
-  }
   sf = bs.sf;
-  c0 = e2m1x8_rn(v0);
-  c1 = e2m1x8_rn(v1);
+  const uint2 c = e2m1x16_rn(v0, v1, bs);
+  c0 = c.x;
+  c1 = c.y;
 }
 
 __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16* __restrict__ h,
@@ -658,7 +709,7 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
       // row-major output, rows of whole 64-value groups: the lane-interleaved kernel
       const int64_t units = a.rows * (a.cols / 16);
       int64_t nb = (units + 511) / 512;     // 64 blocks per warp and iteration
-      if (nb > 64 * (int64_t)sms) nb = 64 * (int64_t)sms;
+      if (nb > 8 * (int64_t)sms) nb = 8 * (int64_t)sms;   // 8 CTAs of 8 warps per SM, several iterations each
       if (nb < 1) nb = 1;
       const bool i32 = units + 128 < ((int64_t)1 << 32);
       if (rounding == kRoundSR) {

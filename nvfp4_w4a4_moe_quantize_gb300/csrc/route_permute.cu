@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     float my_w = 0.0f;
     if (lane < k) {
       my_slot = inv[t * k + lane];
-      my_w = w[t * k + lane];
+      my_w = w != nullptr ? w[t * k + lane] : 1.0f;   // no weights: the plain sum (exact products)
     }
     if (my_slot < 0) my_w = 0.0f;
     for (int64_t c = 8 * lane; c < H; c += 256) {

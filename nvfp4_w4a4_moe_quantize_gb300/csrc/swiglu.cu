@@ -97,11 +97,9 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(const __nv_bfloat16* 
       const int64_t c = 8 * lane + 256 * i;
       const bool active = c < I;
       const BlockScale bs = block_scale(bm[i], g, six_g);
-      float f[8], v[8];
+      float f[8];
       bf16x8_to_f32(hv[i], f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(f[e], bs.r);
-      const uint32_t word = e2m1x8_rn(v);
+      const uint32_t word = e2m1x8_rn(f, bs);
       const uint32_t sfb = active ? bs.sf : 0u;
       const uint32_t s2 = __shfl_down_sync(kAll, sfb, 2);
       const uint32_t s4 = __shfl_down_sync(kAll, sfb, 4);
@@ -127,15 +125,21 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(const __nv_bfloat16* 
 // each in float32 (s = 1 / (1 + e^-g) with expf and a correctly rounded division), rounded
 // once to BF16.  One thread per 8 columns of a row: gate and up from [gate | up] rows of
 // pitch 2I, dh from rows of pitch I, [dgate | dup] out like the input.
+// gu_interleaved: gate/up columns in the 64-chunk interleave of the prepared W13 (gate
+// column c at (c/64)*128 + c%64, up column c 64 further), as the gate/up GEMM writes D;
+// otherwise [gate | up].  dh has row pitch dh_ld; dgu is always [dgate | dup].
 __global__ void __launch_bounds__(256) swiglu_backward_kernel(const __nv_bfloat16* __restrict__ gu,
                                                               const __nv_bfloat16* __restrict__ dh, int64_t rows,
-                                                              int64_t I, __nv_bfloat16* __restrict__ dgu) {
+                                                              int64_t I, int gu_interleaved, int64_t dh_ld,
+                                                              __nv_bfloat16* __restrict__ dgu) {
   const int64_t chunks = I / 8, total = rows * chunks;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / chunks, c = 8 * (i - r * chunks);
-    const uint4 gq = *reinterpret_cast<const uint4*>(gu + r * 2 * I + c);
-    const uint4 uq = *reinterpret_cast<const uint4*>(gu + r * 2 * I + I + c);
-    const uint4 hq = *reinterpret_cast<const uint4*>(dh + r * I + c);
+    const int64_t gcol = gu_interleaved ? (c >> 6) * 128 + (c & 63) : c;
+    const int64_t ucol = gu_interleaved ? gcol + 64 : I + c;
+    const uint4 gq = *reinterpret_cast<const uint4*>(gu + r * 2 * I + gcol);
+    const uint4 uq = *reinterpret_cast<const uint4*>(gu + r * 2 * I + ucol);
+    const uint4 hq = *reinterpret_cast<const uint4*>(dh + r * dh_ld + c);
     const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w}, uw[4] = {uq.x, uq.y, uq.z, uq.w},
                    hw[4] = {hq.x, hq.y, hq.z, hq.w};
     uint32_t dg[4], du[4];
@@ -163,13 +167,14 @@ __global__ void __launch_bounds__(256) swiglu_backward_kernel(const __nv_bfloat1
 }
 
 cudaError_t launch_swiglu_backward(const void* gu, const void* dh, int64_t rows, int64_t I, void* dgu,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, bool gu_interleaved, int64_t dh_ld) {
   const int64_t total = rows * (I / 8);
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 16 * (int64_t)num_sms()) blocks = 16 * (int64_t)num_sms();
   swiglu_backward_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(gu),
                                                      static_cast<const __nv_bfloat16*>(dh), rows, I,
+                                                     gu_interleaved ? 1 : 0, dh_ld > 0 ? dh_ld : I,
                                                      static_cast<__nv_bfloat16*>(dgu));
   return cudaGetLastError();
 }

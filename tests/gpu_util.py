@@ -52,6 +52,23 @@ def check_bf16_against(got_bits: np.ndarray, ref: np.ndarray, rel: float = 1e-3,
     return int(bad.sum()), float((np.abs(got - ref) / np.maximum(bound, 1e-300)).max()) if ref.size else 0.0
 
 
+def combine_violations(out_bits: np.ndarray, y_bits: np.ndarray, inv: np.ndarray, w: np.ndarray) -> int:
+    """The weighted un-permute out[t] = BF16(sum_j fl32(w[t,j] * y[inv[t,j]])), summed in
+    float32 in order j, against the exact float64 sum of the same BF16 y: each float32
+    product and sum adds at most 2^-24 of sum_j |w y| (k products, k - 1 sums, then the
+    BF16 rounding of the float32 total: half a BF16 ulp of a value that is itself within
+    that bound).  Returns the number of elements of out outside the bound."""
+    k = inv.shape[1]
+    yv = F.bf16_to_f32(y_bits).astype(np.float64)
+    wv = np.asarray(w, np.float32).astype(np.float64)
+    mag = sum(np.abs(wv[:, j:j + 1] * yv[inv[:, j]]) for j in range(k))
+    exact = sum(wv[:, j:j + 1] * yv[inv[:, j]] for j in range(k))
+    got = F.bf16_to_f32(out_bits).astype(np.float64)
+    slack = (k + 1) * 2.0 ** -24 * mag
+    bound = 0.5 * np.exp2(np.frexp(np.abs(exact) + slack)[1] - 8.0) + slack
+    return int(np.sum(np.abs(got - exact) > bound))
+
+
 # --------------------------------------------------------------------------- GEMM-tiled layout
 # Host implementation of the layout documented in include/nvfp4moe.h (blocks of R rows x
 # 256 K-values: R*128 bytes of 128-byte-swizzled codes, then (R/128)*2048 bytes of scales).

@@ -23,7 +23,8 @@ def test_every_declared_function_is_exported(lib):
                 "moe_forward_workspace_layout", "nvfp4_grouped_gemm_tiled", "nvfp4_pack_tiled",
                 "nvfp4_tiled_bytes", "nvfp4_quantize_noalloc", "nvfp4_dequantize", "nvfp4_quantize_transposed",
                 "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_grouped_gemm", "mxfp8_sf_bytes",
-                "bf16_grouped_gemm", "bf16_transpose", "moe_swiglu_backward"}
+                "bf16_grouped_gemm", "bf16_transpose", "moe_swiglu_backward", "moe_weights_t_sizes",
+                "moe_prepare_weights_backward", "moe_expert_backward", "moe_backward_workspace_layout"}
     assert expected <= set(names)
     for n in names:
         assert hasattr(lib, n), n
@@ -62,7 +63,11 @@ def test_forward_workspace_layout(lib):
 def test_host_argument_checks_return_before_any_cuda_call(lib):
     null = ctypes.c_void_p(0)
     # cols not a multiple of 16
-    assert lib.nvfp4_quantize(null, 4, 24, 24, 0, 0, 0, 0, 0, null, null, null, null, null, 0, null) == L.Status.INVALID_ARG
+    assert lib.nvfp4_quantize(null, 4, 24, 24, 0, 0, 0, 0, 0, null, null, null, null, 0, null, 0, null) == L.Status.INVALID_ARG
+    # an unknown scale layout; row-major scales need whole 64-value groups
+    assert lib.nvfp4_quantize(null, 4, 64, 64, 0, 0, 0, 0, 0, null, null, null, null, 7, null, 0, null) == L.Status.INVALID_ARG
+    assert lib.nvfp4_quantize(null, 4, 48, 48, 0, 0, 0, 0, 0, null, null, null, null, L.SF_ROWMAJOR, null, 0,
+                              null) == L.Status.UNSUPPORTED
     # K not a multiple of 256
     assert lib.nvfp4_grouped_gemm(null, null, null, null, null, null, null, null, 128, 128, 192, 1, null, 0, 128,
                                   null) == L.Status.UNSUPPORTED
@@ -71,7 +76,7 @@ def test_host_argument_checks_return_before_any_cuda_call(lib):
     # H not a multiple of 8 in the combine
     assert lib.moe_combine(null, null, null, 4, 2, 12, null, null) == L.Status.INVALID_ARG
     # empty inputs are a no-op
-    assert lib.nvfp4_quantize(null, 0, 32, 32, 0, 0, 0, 0, 0, null, null, null, null, null, 0, null) == L.Status.OK
+    assert lib.nvfp4_quantize(null, 0, 32, 32, 0, 0, 0, 0, 0, null, null, null, null, 0, null, 0, null) == L.Status.OK
     assert lib.nvfp4_status_string(L.Status.WORKSPACE) == b"workspace too small"
 
 

@@ -50,6 +50,27 @@ def test_quantize_sr_matches_oracle(cuda_lib, shape):
         _compare(cuda_lib, bits, "row", "sr", seed, off)
 
 
+@pytest.mark.parametrize("scope", ["tensor", "row"])
+@pytest.mark.parametrize("shape", [(5, 64), (130, 2048), (33, 4096)])
+def test_quantize_rowmajor_scales(cuda_lib, scope, shape):
+    """The row-major scale layout: the same codes and g as the tiled call, and scales that
+    equal the oracle's [rows, cols/16] bytes (the tiled layout's padding does not exist)."""
+    bits = S.bf16_bits(S.outlier_channels_bf16(*shape, seed=shape[0] + 3))
+    x = bf16_tensor(bits)
+    codes, sf, g = cuda_lib.nvfp4_quantize(x, MODES[scope], sf_layout=cuda_lib.SF_ROWMAJOR)
+    assert cuda_lib.nvfp4_status_check() == 0
+    ref = Q.quantize(bits, scope=scope)
+    assert tuple(sf.shape) == (shape[0], shape[1] // 16)
+    np.testing.assert_array_equal(npy(sf), ref["sf"])
+    np.testing.assert_array_equal(npy(codes), ref["packed"])
+    np.testing.assert_array_equal(npy(g)[:ref["g"].size], ref["g"])
+    for rounding in (1,):
+        c2, sf2, _ = cuda_lib.nvfp4_quantize(x, MODES[scope], rounding, 5, 9, sf_layout=cuda_lib.SF_ROWMAJOR)
+        ref2 = Q.quantize(bits, scope=scope, rounding="sr", seed=5, rng_offset=9)
+        np.testing.assert_array_equal(npy(c2), ref2["packed"])
+        np.testing.assert_array_equal(npy(sf2), ref2["sf"])
+
+
 def test_quantize_group_scope(cuda_lib):
     bits = S.bf16_bits(S.randn_bf16((4 * 96, 512), 0.02, seed=5))
     _compare(cuda_lib, bits, "group", group_rows=96)
