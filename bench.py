@@ -461,6 +461,34 @@ def run_ours(args, rank, world, local_rank):
                "frac_of_9pf": round(l_tflops / PF_TARGET, 4), "tokens_per_s": round(lshape.T / (lt * 1e-3), 1)}
     del lfws, lbws, lgrads, pt, lx, llog, ldout, lout
 
+    # ---------------------------------------------------------------- decode-shaped launches
+    # Sampler-shaped batches of 1, 8 and 64 tokens through the same calls (routing + the
+    # expert block) on the forward workload's weights: the tiles cover only the experts the
+    # batch routes to, so the floor is reading those experts' weights once.
+    decode = {"timing": f"median of {iters} launches, L2 flushed before each", "batches": []}
+    w13_e = L.nvfp4_tiled_bytes(2 * I, H, 256) + 4
+    w2_e = L.nvfp4_tiled_bytes(H, pw.Ip, 256) + 4
+    for dt in (1, 8, 64):
+        dx_ = x[:dt].contiguous()
+        dlog = logits[:dt].contiguous()
+        dids = torch.empty(dt, k, dtype=torch.int32, device=dev)
+        dwts = torch.empty(dt, k, dtype=torch.float32, device=dev)
+        dout_ = torch.empty(dt, H, dtype=torch.bfloat16, device=dev)
+        dws = L.moe_forward_workspace(dt, k, pw, dev)
+
+        def dstep():
+            L.moe_route_topk(dlog, k, True, out=(dids, dwts))
+            L.moe_expert_forward(dx_, dids, dwts, pw, out=dout_, workspace=dws)
+        dtime = time_launches_median(dstep, iters, flush, stream)
+        active = int(torch.unique(dids).numel())
+        dbytes = active * (w13_e + w2_e) + dt * H * 2 * 2 + dt * E * 4
+        decode["batches"].append({"tokens": dt, "active_experts": active, "us": round(dtime * 1e3, 2),
+                                  "tokens_per_s": round(dt / (dtime * 1e-3), 1),
+                                  "weight_bytes_read": active * (w13_e + w2_e),
+                                  "gbs": round(dbytes / (dtime * 1e-3) / 1e9, 1),
+                                  "frac_hbm": round(dbytes / (dtime * 1e-3) / 1e9 / hbm_peak, 4)})
+        del dws
+
     # ---------------------------------------------------------------- end to end (host buffers)
     # Every step copies its inputs (x, router logits) from pinned host memory and reads its
     # result back.  Serial: copy in, compute, copy out on one stream.  Pipelined (the
@@ -548,7 +576,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps, "stages_ms": {k_: round(v_, 4) for k_, v_ in stages.items()},
         "grouped_gemm": grouped, "quantiser": quant, "mxfp8": mxfp8, "dequantised_backward": dqbwd,
-        "learner_step": learner,
+        "learner_step": learner, "decode": decode,
         "wall_s_timed": round(wall_s, 3),
     }
     return line

@@ -142,7 +142,9 @@ def _check_backward(lib, shape, r):
             (dy_gpu, h_gpu, H, I, Ip, B.STREAM_WGRAD_DOWN, 0, 12, 13, r["dw2"]),
             (dD_gpu, x_slots, 2 * I, H, H, B.STREAM_WGRAD_GATEUP, 1, 14, 15, r["dw13"])):
         ref, ops = B.wgrad(gsrc, asrc, padded, counts, seed, stream)
-        abuf, bbuf = npy(bws[blay[ia]:blay[ia + 1]]), npy(bws[blay[ib]:blay[ib + 1]])
+        kb_cap = blay[16]
+        abuf = npy(bws[blay[ia]:blay[ia] + (Fa // 128) * kb_cap * 128 * 144])
+        bbuf = npy(bws[blay[ib]:blay[ib] + (Fbp // 256) * kb_cap * 256 * 144])
         for e in range(E):
             tp = 256 * int(kb[e])
             qa, qb = ops[e]
