@@ -560,7 +560,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(x_h, logits_h, w13_h, w2_h, shape, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(budget_s=args.cpu_seconds)
 
     launches_per_step = 1 + 9      # route + (3 grouping, token quantise, slot gather, gate/up+SwiGLU GEMM, requant, down GEMM, combine)
     line = {
@@ -582,34 +582,113 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def cpu_baseline(x_h, logits_h, w13_h, w2_h, shape, budget_s=15.0, tokens=None):
-    """The oracle (float64, numpy) timed on this host on a bounded sample of tokens.
-    Weight quantisation for the experts the sample touches is done before timing, as on
-    the GPU side.  Returns the cpu_baseline object."""
+def _cpu_worker_run(kind: str, seconds: float, index: int, workers: int) -> dict:
+    """One oracle timing worker (run as its own process): the oracle as it stands, on a
+    bounded share of one workload -- `index` of `workers` interleaved shares.  Expert
+    weights are drawn per expert from the workloads' distribution (N(0, 0.02) BF16, one
+    seed per expert), so a worker builds only the experts it touches.  Setup (inputs,
+    weight quantisation) is not timed."""
     from oracle import moe as M
     from oracle import quant as Q
-    xb = S.bf16_bits(x_h)
-    ids, w = M.route_topk(logits_h.numpy(), shape.k)
-    n = tokens or 64
-    toks = list(range(n))
-    need = sorted(set(ids[toks].reshape(-1).tolist()))
-    w13b, w2b = S.bf16_bits(w13_h), S.bf16_bits(w2_h)
+    shape = S.WORKLOADS["forward"]
+    H, I, E, k = shape.H, shape.I, shape.E, shape.k
+    w13_of = lambda e: S.bf16_bits(S.randn_bf16((2 * I, H), shape.w_std, 50_000 + e))  # noqa: E731
+    w2_of = lambda e: S.bf16_bits(S.randn_bf16((H, I), shape.w_std, 60_000 + e))       # noqa: E731
+    done, el = 0, 0.0
+    if kind == "quantiser":
+        rows, cols = S.QUANTISER_SHAPE
+        bits = S.bf16_bits(S.outlier_channels_bf16(rows, cols, seed=0))
+        g = Q.global_scale(np.array([np.max(np.abs(F_bf16(bits)))]))
+        chunk, r = 32, index * 32
+        t0 = time.perf_counter()
+        while r < rows and time.perf_counter() - t0 < seconds:
+            Q.quantize(bits[r:r + chunk], scope="tensor", global_scale_in=g)
+            done += chunk
+            r += chunk * workers
+        el = time.perf_counter() - t0
+        per_row = cols * 2 + cols // 2 + cols // 16
+        return {"kind": kind, "rate": done * per_row / el / 1e9, "unit": "GB/s", "units": done, "seconds": el}
+    if kind == "gemm":
+        g_shape = S.WORKLOADS["gateup"]
+        x = S.bf16_bits(S.randn_bf16((g_shape.T, H), 1.0, 1))
+        ids, _ = M.route_topk(S.router_logits_zipf(g_shape.T, E, g_shape.zipf_s, 2).numpy(), k)
+        counts = np.bincount(ids.reshape(-1), minlength=E)
+        order = [e for e in np.argsort(-counts, kind="stable") if counts[e] > 0][index::workers]
+        flops = 0.0
+        for e in order:
+            toks = np.nonzero((ids == e).any(axis=1))[0]
+            qa = Q.quantize(x[toks], scope="row")
+            qw = Q.quantize(w13_of(int(e)), scope="tensor")
+            t0 = time.perf_counter()
+            M.gemm_rows(qa["codes"], qa["sf"], qa["g"], qw["codes"], qw["sf"], qw["g"][0])
+            el += time.perf_counter() - t0
+            flops += 2.0 * len(toks) * 2 * I * H
+            done += len(toks)
+            if el > seconds:
+                break
+        return {"kind": kind, "rate": flops / max(el, 1e-9) / 1e12, "unit": "TFLOP/s", "units": done, "seconds": el}
+    # the expert-block forward, token by token
+    x = S.bf16_bits(S.randn_bf16((shape.T, H), 1.0, 1))
+    ids, w = M.route_topk(S.router_logits_zipf(shape.T, E, shape.zipf_s, 2).numpy(), k)
+    toks = list(range(index, shape.T, workers))[:4]
     prep = {"w13_codes": {}, "w13_sf": {}, "w13_g": {}, "w2_codes": {}, "w2_sf": {}, "w2_g": {}}
-    for e in need:
-        q13 = Q.quantize(w13b[e], scope="tensor")
-        q2 = Q.quantize(w2b[e], scope="tensor")
+    for e in sorted(set(ids[toks].reshape(-1).tolist())):
+        q13, q2 = Q.quantize(w13_of(e), scope="tensor"), Q.quantize(w2_of(e), scope="tensor")
         prep["w13_codes"][e], prep["w13_sf"][e], prep["w13_g"][e] = q13["codes"], q13["sf"], q13["g"][0]
         prep["w2_codes"][e], prep["w2_sf"][e], prep["w2_g"][e] = q2["codes"], q2["sf"], q2["g"][0]
-    done = 0
-    t0 = time.time()
-    while done < n and (time.time() - t0) < budget_s:
-        M.moe_forward_tokens(xb, ids, w, prep, [done])
+    t0 = time.perf_counter()
+    for t in toks:
+        M.moe_forward_tokens(x, ids, w, prep, [t])
         done += 1
-    el = time.time() - t0
+        if time.perf_counter() - t0 > seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"kind": kind, "rate": done / el, "unit": UNIT, "units": done, "seconds": el}
+
+
+def F_bf16(bits):
+    """BF16 bit patterns -> float32 (numpy), for the oracle workers' global scale."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _cpu_workers(kind: str, seconds: float, workers: int) -> list:
+    """`workers` single-threaded oracle workers side by side (own processes, BLAS and
+    OpenMP limited to one thread each); their reports."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    procs = [subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-worker", kind, "--cpu-seconds",
+                               str(seconds), "--worker-index", str(i), "--workers", str(workers)],
+                              stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, env=env, text=True)
+             for i in range(workers)]
+    out = []
+    for p in procs:
+        so, _ = p.communicate(timeout=600)
+        if p.returncode == 0 and so.strip():
+            out.append(json.loads(so.strip().splitlines()[-1]))
+    return out
+
+
+def cpu_baseline(budget_s: float = 4.0) -> dict:
+    """The oracle (float64 numpy, as it stands) timed on this host on bounded shares of the
+    three measured workloads, on 1 thread and on all cores (one single-threaded worker per
+    core, interleaved shares; the rates add up).  The headline value is the expert-block
+    forward on all cores, in the metric's unit."""
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": round(done / el, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} tokens of the T=16384 forward workload, token by token (float64 numpy; "
-                      f"BLAS may use all {cores} host threads), {el:.1f} s"}
+    res = {}
+    for kind, name in (("forward", "forward_tokens_per_s"), ("gemm", "grouped_gemm_tflops"),
+                       ("quantiser", "quantiser_gbs")):
+        one = _cpu_workers(kind, budget_s, 1)
+        many = _cpu_workers(kind, budget_s, cores)
+        res[name] = {"1_thread": round(one[0]["rate"], 6) if one else None,
+                     "all_cores": round(sum(r["rate"] for r in many), 6) if many else None,
+                     "units_timed_all_cores": int(sum(r["units"] for r in many))}
+    fwd = res["forward_tokens_per_s"]
+    return {"value": fwd["all_cores"], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the oracle (float64 numpy) on bounded interleaved shares of each workload, ~{budget_s:.0f} s "
+                      "per worker: the T=16384 forward token by token (up to 4 tokens per worker), the T=8192 "
+                      "gate/up grouped GEMM expert by expert, the 16384x2048 quantiser 32 rows at a time; "
+                      f"1 thread, and {cores} single-threaded workers side by side (all cores); expert weights "
+                      "drawn per expert from the workloads' distribution",
+            "configs": res}
 
 
 def run_profile(args):
@@ -746,7 +825,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=4.0, help="time budget of each oracle timing worker")
+    ap.add_argument("--cpu-worker", choices=["forward", "gemm", "quantiser"], default=None,
+                    help="(internal) run one oracle timing worker and print its report")
+    ap.add_argument("--worker-index", type=int, default=0)
+    ap.add_argument("--workers", type=int, default=1)
     ap.add_argument("--ref-tokens-per-step", type=int, default=2)
     ap.add_argument("--profile", choices=["none", "gateup", "quantiser", "forward", "mxgemm", "backward"],
                     default="none",
@@ -756,6 +839,9 @@ def main():
                     help="scale scope of the --profile quantiser case")
     ap.add_argument("--quant-sr", action="store_true", help="stochastic rounding in the --profile quantiser case")
     args = ap.parse_args()
+    if args.cpu_worker is not None:
+        print(json.dumps(_cpu_worker_run(args.cpu_worker, args.cpu_seconds, args.worker_index, args.workers)))
+        return
     if args.profile != "none":
         run_profile(args)
         return

@@ -189,11 +189,12 @@ cudaError_t launch_kofs(const int32_t* counts, int64_t uniform, int E, int32_t* 
 // blocks (128 or 256) by 256-token K-blocks; expert e's blocks start at block
 // (Fp / R) * kofs[e], row-block-major.
 //
-// One CTA per (expert, row block, K-block) unit: the 256 x R BF16 source tile goes into
-// shared memory with 16-byte asynchronous copies, each thread encodes pairs of features
-// (4-byte column reads, conflict-free across a warp) for one 16-token block at a time,
-// writes codes and scale bytes into the unit's shared-memory image, and one bulk store
-// writes the image (R * 144 bytes) whole.
+// One CTA per (expert, 128 output rows, K-block) unit, two CTAs per SM: the 256 x 128 BF16
+// source tile goes into shared memory with 16-byte asynchronous copies, each thread
+// encodes pairs of features (4-byte column reads, conflict-free across a warp) for one
+// 16-token block at a time, writes codes and scale bytes into the unit's 18 KB image (the
+// 128-row block of the layout), and bulk stores write it: whole for R = 128, as the codes
+// (16 KB) and scale (2 KB) halves of a 256-row block for R = 256.
 struct TQuant {
   const __nv_bfloat16* src;
   int64_t ld;
@@ -206,17 +207,19 @@ struct TQuant {
   const uint32_t* amax_bits; // [E]
   float* g_out;              // [E]
   uint8_t* out;
-  int rounding;
   uint64_t seed;
   int stream;
-  int* status;
 };
 
-template <int R, int RND>
+constexpr int kTQRows = 128;                                  // output rows per unit
+constexpr int kTQSmem = 256 * kTQRows * 2 + kTQRows * 144;    // source tile + image
+
+template <int RND>
 __global__ void __launch_bounds__(256) tquant_kernel(const TQuant q) {
   extern __shared__ __align__(128) uint8_t tsm[];
-  uint8_t* tile = tsm;                                        // [256 tokens][R features] BF16
-  uint8_t* img = tsm + 256 * R * 2;                           // the unit's R*144-byte image
+  constexpr int R = kTQRows;
+  uint8_t* tile = tsm;                                        // [256 tokens][128 features] BF16
+  uint8_t* img = tsm + 256 * R * 2;                           // the unit's 18 KB image
   const uint32_t tile_s = smem_u32(tile);
   const int tid = threadIdx.x;
   const int rblocks = q.Fp / R;
@@ -226,11 +229,12 @@ __global__ void __launch_bounds__(256) tquant_kernel(const TQuant q) {
     const int rb = (int)(u - (int64_t)kg * rblocks);
     const int e = find_group(q.kofs, q.E, kg);
     const int kb = kg - q.kofs[e];
-    const int64_t tp = 256 * (int64_t)(q.kofs[e + 1] - q.kofs[e]);
+    const int64_t kbe = q.kofs[e + 1] - q.kofs[e];
+    const int64_t tp = 256 * kbe;
     const int64_t start = q.starts != nullptr ? q.starts[e] : (int64_t)e * q.uniform;
     const int64_t count = q.counts != nullptr ? q.counts[e] : q.uniform;
     const int f0 = rb * R;
-    // 1. the source tile: tokens kb*256 .. +255 of the expert, features f0 .. f0+R-1
+    // 1. the source tile: tokens kb*256 .. +255 of the expert, features f0 .. f0+127
     constexpr int kChunksPerRow = R * 2 / 16;
     for (int i = tid; i < 256 * kChunksPerRow; i += 256) {
       const int t = i / kChunksPerRow, ch = i - t * kChunksPerRow;
@@ -286,16 +290,20 @@ __global__ void __launch_bounds__(256) tquant_kernel(const TQuant q) {
         }
         // codes: K-byte 8b of row rr, 128-byte swizzled; scale (rr, b)
         *reinterpret_cast<uint2*>(img + rr * 128 + ((((b >> 1) ^ (rr & 7))) << 4) + (b & 1) * 8) = cw;
-        const int r128 = rr & 127;
-        img[R * 128 + (rr >> 7) * 2048 + (b >> 2) * 512 + (r128 & 31) * 16 + (r128 >> 5) * 4 + (b & 3)] =
-            (uint8_t)bs.sf;
+        img[R * 128 + (b >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (b & 3)] = (uint8_t)bs.sf;
       }
     }
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
-      uint8_t* dst = q.out + ((int64_t)rblocks * q.kofs[e] + (int64_t)rb * (tp / 256) + kb) * (int64_t)R * 144;
-      bulk_store(dst, img, R * 144);
+      if (q.R == 128) {
+        bulk_store(q.out + ((int64_t)rblocks * q.kofs[e] + (int64_t)rb * kbe + kb) * (128 * 144), img, 128 * 144);
+      } else {   // one half of a 256-row block: its codes and its row group of scales
+        const int64_t blk = (int64_t)(rblocks / 2) * q.kofs[e] + (int64_t)(rb >> 1) * kbe + kb;
+        uint8_t* base = q.out + blk * (256 * 144);
+        bulk_store(base + (rb & 1) * (128 * 128), img, 128 * 128);
+        bulk_store(base + 256 * 128 + (rb & 1) * 2048, img + 128 * 128, 2048);
+      }
       bulk_commit();
       bulk_wait_read<0>();     // the image is read before the next unit overwrites it
     }
@@ -304,26 +312,25 @@ __global__ void __launch_bounds__(256) tquant_kernel(const TQuant q) {
   if (tid == 0) bulk_wait_all<0>();
 }
 
-template <int R, int RND>
+template <int RND>
 static cudaError_t launch_tq(const TQuant& q, int64_t max_units, cudaStream_t s) {
-  constexpr int kSmem = 256 * R * 2 + R * 144;
   static std::atomic<bool> attr_set[64];
-  const cudaError_t err = set_smem_attr_once(attr_set, (const void*)tquant_kernel<R, RND>, kSmem);
+  const cudaError_t err = set_smem_attr_once(attr_set, (const void*)tquant_kernel<RND>, kTQSmem);
   if (err != cudaSuccess) return err;
   int64_t grid = max_units;
-  const int64_t cap = (R == 128 ? 2 : 1) * (int64_t)num_sms();
-  if (grid > cap) grid = cap;
+  if (grid > 2 * (int64_t)num_sms()) grid = 2 * (int64_t)num_sms();
   if (grid < 1) grid = 1;
-  tquant_kernel<R, RND><<<(int)grid, 256, kSmem, s>>>(q);
+  tquant_kernel<RND><<<(int)grid, 256, kTQSmem, s>>>(q);
   return cudaGetLastError();
 }
 
 // max_kblocks: an upper bound on kofs[E] (the grid is sized from it; the kernel reads the
-// exact count on the device).
+// exact count on the device).  R: 128 or 256 (the output layout's row blocks); Fp % R == 0.
 cudaError_t launch_tquant(const void* src, int64_t ld, const int32_t* rowmap, const int32_t* starts,
                           const int32_t* counts, int64_t uniform, const int32_t* kofs, int E, int F, int Fp, int R,
                           const uint32_t* amax_bits, float* g_out, uint8_t* out, int rounding, uint64_t seed,
                           int stream_id, int64_t max_kblocks, cudaStream_t s) {
+  if ((R != 128 && R != 256) || Fp % R != 0) return cudaErrorInvalidValue;
   TQuant q;
   q.src = static_cast<const __nv_bfloat16*>(src);
   q.ld = ld;
@@ -339,14 +346,10 @@ cudaError_t launch_tquant(const void* src, int64_t ld, const int32_t* rowmap, co
   q.amax_bits = amax_bits;
   q.g_out = g_out;
   q.out = out;
-  q.rounding = rounding;
   q.seed = seed;
   q.stream = stream_id;
-  q.status = device_status_ptr();
-  const int64_t units = max_kblocks * (Fp / R);
-  if (R == 128)
-    return rounding == kRoundSR ? launch_tq<128, kRoundSR>(q, units, s) : launch_tq<128, kRoundRNE>(q, units, s);
-  return rounding == kRoundSR ? launch_tq<256, kRoundSR>(q, units, s) : launch_tq<256, kRoundRNE>(q, units, s);
+  const int64_t units = max_kblocks * (Fp / kTQRows);
+  return rounding == kRoundSR ? launch_tq<kRoundSR>(q, units, s) : launch_tq<kRoundRNE>(q, units, s);
 }
 
 }  // namespace nvfp4

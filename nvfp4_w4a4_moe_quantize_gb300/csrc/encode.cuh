@@ -72,6 +72,7 @@ struct BlockScale {
   float s;      // effective decode scale decode(sf) * g; 0 when the block decodes to zero
   float r_lo;   // fast path: 0 < r_lo * (1 + 2^-22) < 1/s < r_hi * (1 - 2^-22)  (0, 0 when s == 0)
   float r_hi;
+  float r;      // the reciprocal itself, within 2^-22 of 1/s (0 when s == 0)
   bool exact_only;  // 0 < s < 2^-60: every element takes the exact path
 };
 
@@ -83,7 +84,7 @@ struct BlockScale {
 __device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float six_g) {
   BlockScale bs;
   bs.exact_only = false;
-  bs.r_lo = bs.r_hi = 0.0f;
+  bs.r_lo = bs.r_hi = bs.r = 0.0f;
   if (!(g > 0.0f)) {
     bs.sf = 0;
     bs.s = 0.0f;
@@ -95,6 +96,7 @@ __device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float s
   if (bs.s >= kTinyScale) {
     float r;
     asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(bs.s));
+    bs.r = r;
     bs.r_lo = __fmul_rn(r, 0.99999618530273438f);   // 1 - 2^-18
     bs.r_hi = __fmul_rn(r, 1.0000038146972656f);    // 1 + 2^-18
   } else if (bs.s > 0.0f) {
@@ -248,27 +250,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Stochastic rounding of one scaled value v to E2M1: lo <= |v| < hi neighbouring grid
-// magnitudes, p = (|v| - lo) / (hi - lo) (exact), round up iff r16 < p * 2^16;
-// |v| >= 6 saturates.  Zero magnitude encodes as +0.  As a function of |v| this is the
-// number of thresholds tau_j = G_{j-1} + r16 (G_j - G_{j-1}) / 2^16 (j = 1..7, G the grid)
-// that |v| exceeds, so it is monotone in |v|.
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
-  const float a = fabsf(v);
-  const uint32_t c = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) + (a >= 4.0f) +
-                     (a >= 6.0f);
-  uint32_t code;
-  if (c >= 7) {
-    code = 7;
-  } else {
-    const float lo = c < 4 ? __fmul_rn((float)c, 0.5f) : (float)(c - 2);
-    const float inv_gap = c < 4 ? 2.0f : (c < 6 ? 1.0f : 0.5f);
-    const float p = __fmul_rn(__fsub_rn(a, lo), inv_gap);
-    code = c + (((float)r16 < __fmul_rn(p, 65536.0f)) ? 1u : 0u);
-  }
-  return code | ((__float_as_uint(v) >> 31) && code ? 8u : 0u);
-}
-
+// Stochastic rounding (the reading): with lo <= q < hi the neighbouring grid magnitudes
+// around the quotient q = |x|/s and p = (q - lo) / (hi - lo), round up iff r16 < p 2^16; q >= 6
+// saturates; zero magnitude encodes as +0.  As a function of q this is the number of
+// thresholds tau_j = G_{j-1} + r16 (G_j - G_{j-1}) / 2^16 (j = 1..7, G the grid) that q
+// exceeds.
 // Exact stochastic rounding of the quotient |x| / s (s > 0): the number of thresholds
 // tau_j (above) with |x| > tau_j * s, each decided by the sign of one FMA (tau_j has at
 // most 19 significant bits, so |x| - tau_j s is either zero or far from underflow).
@@ -287,39 +273,44 @@ __device__ __forceinline__ uint32_t e2m1_exact_sr(float x, float s, uint32_t r16
 }
 
 // 8 values of one chunk with their Philox block output -> packed codes of the
-// stochastically rounded exact quotients.  Bracketed like e2m1x8_rn: the count of
-// thresholds tau_j exceeded is monotone in |v|, and the thresholds are at least 0.5
-// apart, so where the bracket codes differ they differ by one step and the single
-// threshold tau between them decides: up iff |x| > tau s (an exact FMA sign).
+// stochastically rounded exact quotients.  One product v = |x| r per value (|v/q - 1| <=
+// 2^-21 for the exact quotient q = |x|/s).  On the grid segment holding v, t = (v - G)/gap
+// + (index of G) is exact given v (2v below 2, v - 2 below 4, v/2 - 2 above), and the
+// rounding goes up iff r16 < frac(t) 2^16.  In units of 2^-16 of a gap, v's error moves
+// t by at most 0.125, so the decision is the exact quotient's unless frac(t) 2^16 lies
+// within 0.25 of r16 or of 0 / 2^16 (the next grid point); those values -- about one in
+// 10^5 -- take the exact count of thresholds below q (e2m1_exact_sr).
 __device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockScale& bs, uint4 rnd) {
   const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+  if (!(bs.s > 0.0f)) return 0u;
   if (!bs.exact_only) {
-    float vl[8], vh[8];
-    scale8(f, bs.r_lo, vl);
-    scale8(f, bs.r_hi, vh);
-    uint32_t lo = 0, hi = 0;
+    float v[8];
+    scale8(f, bs.r, v);
+    uint32_t out = 0, amb = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const uint32_t r16 = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-      lo |= e2m1_sr(vl[e], r16) << (4 * e);
-      hi |= e2m1_sr(vh[e], r16) << (4 * e);
+      const float a = fabsf(v[e]);
+      const float r16 = (float)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+      const bool s0 = a < 2.0f, s1 = a < 4.0f;
+      const float t = s0 ? __fmul_rn(a, 2.0f) : (s1 ? __fsub_rn(a, 2.0f) : __fmaf_rn(a, 0.5f, -2.0f));
+      const float fl = floorf(t);
+      const float y = __fmul_rn(__fsub_rn(t, fl), 65536.0f);     // frac(t) 2^16, exact
+      const float cf = __fadd_rn(__fadd_rn(s0 ? 0.0f : (s1 ? 4.0f : 6.0f), fl), r16 < y ? 1.0f : 0.0f);
+      // the 3-bit code from the float's low mantissa bits (cf < 2^22), saturated at 7
+      uint32_t c = min(__float_as_uint(__fadd_rn(cf, 8388608.0f)) & 0xFFFFu, 7u);
+      if (a >= 6.0f) c = 7u;
+      const bool near = fabsf(__fsub_rn(y, r16)) < 0.25f || y < 0.25f || y > 65535.75f;
+      if (near && a < 6.0f && f[e] != 0.0f) amb |= 1u << e;
+      out |= (c | ((__float_as_uint(f[e]) >> 31) && c ? 8u : 0u)) << (4 * e);
     }
-    uint32_t diff = lo ^ hi;
-    while (diff != 0u) {
-      const uint32_t sh = (uint32_t)(__ffs((int)diff) - 1) & ~3u;
-      const uint32_t e = sh >> 2;
-      const uint32_t c = (lo >> sh) & 7u;                  // the lower candidate (< 7)
+    while (amb != 0u) {
+      const uint32_t e = (uint32_t)(__ffs((int)amb) - 1);
       const uint32_t we = (e & 4u) ? ((e & 2u) ? w[3] : w[2]) : ((e & 2u) ? w[1] : w[0]);
-      const float u = __fmul_rn((float)((we >> (16 * (e & 1u))) & 0xFFFFu), 1.52587890625e-05f);
-      const float gap = c < 4u ? 0.5f : (c < 6u ? 1.0f : 2.0f);
-      const float tau = __fmaf_rn(u, gap, e2m1_grid(c));  // exact: at most 19 significant bits
-      const float x = pick8(f, e);
-      const uint32_t cnew = __fmaf_rn(-tau, bs.s, fabsf(x)) > 0.0f ? c + 1u : c;
-      const uint32_t sign = cnew && (__float_as_uint(x) >> 31) ? 8u : 0u;   // zero is +0
-      lo = (lo & ~(0xFu << sh)) | ((cnew | sign) << sh);
-      diff &= ~(0xFu << sh);
+      const uint32_t c = e2m1_exact_sr(pick8(f, e), bs.s, (we >> (16 * (e & 1u))) & 0xFFFFu);
+      out = (out & ~(0xFu << (4 * e))) | (c << (4 * e));
+      amb &= amb - 1u;
     }
-    return lo;
+    return out;
   }
   uint32_t out = 0;
 #pragma unroll

@@ -404,10 +404,100 @@ __global__ void __launch_bounds__(256) permute_rank_kernel(const int32_t* __rest
   }
 }
 
+// Small batches (n = T*k <= 1024 entries: decode-shaped launches): the three passes in
+// one block of 1024 threads -- per-expert counts in shared memory, the unpadded and
+// 128-padded exclusive scans, and each entry's rank among the earlier entries of its
+// expert (a scan over at most n - 1 ids in shared memory): the same stable slot order.
+__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids, int n, int k, int E,
+                                                             int32_t* __restrict__ counts,
+                                                             int32_t* __restrict__ offsets,
+                                                             int32_t* __restrict__ padded,
+                                                             int32_t* __restrict__ inv, int32_t* __restrict__ perm,
+                                                             int* status) {
+  __shared__ int32_t s_id[1024], s_cnt[1024], s_wsum[2][32], s_off[1025], s_pad[1025];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  s_cnt[tid] = 0;
+  int e = -1;
+  if (tid < n) {
+    e = ids[tid];
+    if (e < 0 || e >= E) {
+      set_status(status, kStatusBadInput);
+      e = -1;
+    }
+  }
+  s_id[tid] = e;
+  __syncthreads();
+  if (e >= 0) atomicAdd(&s_cnt[e], 1);
+  __syncthreads();
+  // inclusive scans of the counts and of the 128-padded counts over the experts
+  const int32_t c = tid < E ? s_cnt[tid] : 0;
+  int32_t a = c, b = (c + 127) / 128 * 128;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t ya = __shfl_up_sync(kFullMask, a, o), yb = __shfl_up_sync(kFullMask, b, o);
+    if (lane >= o) {
+      a += ya;
+      b += yb;
+    }
+  }
+  if (lane == 31) {
+    s_wsum[0][wid] = a;
+    s_wsum[1][wid] = b;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    int32_t wa = s_wsum[0][lane], wb = s_wsum[1][lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t ya = __shfl_up_sync(kFullMask, wa, o), yb = __shfl_up_sync(kFullMask, wb, o);
+      if (lane >= o) {
+        wa += ya;
+        wb += yb;
+      }
+    }
+    s_wsum[0][lane] = wa;
+    s_wsum[1][lane] = wb;
+  }
+  __syncthreads();
+  const int32_t base_a = wid ? s_wsum[0][wid - 1] : 0, base_b = wid ? s_wsum[1][wid - 1] : 0;
+  const int32_t inc_a = a + base_a, inc_b = b + base_b;
+  if (tid < E) {
+    s_off[tid + 1] = inc_a;
+    s_pad[tid + 1] = inc_b;
+    counts[tid] = c;
+    offsets[tid + 1] = inc_a;
+    padded[tid + 1] = inc_b;
+  }
+  if (tid == 0) {
+    s_off[0] = s_pad[0] = 0;
+    offsets[0] = padded[0] = 0;
+  }
+  __syncthreads();
+  const int32_t total_pad = s_pad[E];
+  if (perm != nullptr)
+    for (int32_t slot = tid; slot < total_pad; slot += blockDim.x) perm[slot] = -1;
+  __syncthreads();
+  if (tid < n) {
+    if (e >= 0) {
+      int32_t rank = 0;
+      for (int i = 0; i < tid; ++i) rank += s_id[i] == e;
+      const int32_t slot = s_pad[e] + rank;
+      inv[tid] = slot;
+      if (perm != nullptr) perm[slot] = tid / k;
+    } else {
+      inv[tid] = -1;
+    }
+  }
+}
+
 cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
                            int32_t* padded, int32_t* inv, int32_t* perm, int32_t* hist, int64_t nchunks,
                            int* status, cudaStream_t s) {
   const int64_t n = T * k;
+  if (n > 0 && n <= 1024 && E <= 1024) {
+    permute_small_kernel<<<1, 1024, 0, s>>>(ids, (int)n, k, E, counts, offsets, padded, inv, perm, status);
+    return cudaGetLastError();
+  }
   const int blocks = (int)((nchunks + 7) / 8);
   if (nchunks > 0) {
     permute_hist_kernel<<<blocks, 256, 8 * E * sizeof(int32_t), s>>>(ids, n, E, nchunks, hist, status);
@@ -437,10 +527,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int64_t T, int k, int64_t H,
                                                       __nv_bfloat16* __restrict__ out) {
+  // one warp per (token, 256-column chunk): small batches still spread over the GPU
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t nwarp = (int64_t)gridDim.x * 8;
-  for (int64_t t = warp; t < T; t += nwarp) {
+  const int64_t nch = (H + 255) / 256;
+  for (int64_t item = warp; item < T * nch; item += nwarp) {
+    const int64_t t = item / nch, c0 = (item - t * nch) * 256;
     int32_t my_slot = -1;
     float my_w = 0.0f;
     if (lane < k) {
@@ -448,7 +541,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
       my_w = w != nullptr ? w[t * k + lane] : 1.0f;   // no weights: the plain sum (exact products)
     }
     if (my_slot < 0) my_w = 0.0f;
-    for (int64_t c = 8 * lane; c < H; c += 256) {
+    for (int64_t c = c0 + 8 * lane; c < min(H, c0 + 256); c += 256) {
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
@@ -499,7 +592,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int64_t T, int k, int64_t H, void* out,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  int64_t blocks = (T + 7) / 8;
+  int64_t blocks = (T * ((H + 255) / 256) + 7) / 8;
   if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
   const auto* yp = static_cast<const __nv_bfloat16*>(y);
   auto* op = static_cast<__nv_bfloat16*>(out);
