@@ -869,7 +869,7 @@ nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w
   auto fail = [](cudaError_t e) { return e != cudaSuccess; };
 
   // 1. weighted un-permute backward: dy per slot, dw per (token, j)
-  if (fail(launch_combine_backward(dout, inv, w, ybuf, T, k, H, dy, dw, s))) return NVFP4_ERR_CUDA;
+  if (fail(launch_combine_backward(dout, inv, w, ybuf, T, k, H, dy, dw, padded, E, amax, s))) return NVFP4_ERR_CUDA;
 
   // row quantisation of a slot-ordered gradient (per row, stochastic rounding) into the
   // GEMM-tiled A operand; padding slots are skipped
@@ -938,7 +938,8 @@ nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w
                    int64_t Fbp, int stream_id, int slot, uint8_t* Aw, uint8_t* Bw, float* out) {
     uint32_t* am = amax + 2 * slot * E;
     float* gg = gexp + 2 * slot * E;
-    if (fail(launch_group_amax(gsrc, Fa, Fa, nullptr, padded, counts, E, mcap, am, s)) ||
+    // dy's per-expert max comes from the combine backward (slot 0)
+    if ((slot != 0 && fail(launch_group_amax(gsrc, Fa, Fa, nullptr, padded, counts, E, mcap, am, s))) ||
         fail(launch_group_amax(asrc, ld_a, Fb, rowmap, padded, counts, E, mcap, am + E, s)) ||
         fail(launch_tquant(gsrc, Fa, nullptr, padded, counts, 0, kofs, E, (int)Fa, (int)Fa, 128, am, gg, Aw, kRoundSR,
                            seed, stream_id, kb_cap, s)) ||

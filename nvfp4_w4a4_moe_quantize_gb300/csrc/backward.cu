@@ -52,12 +52,16 @@ __device__ __forceinline__ uint32_t bf16_of_product(float w, float d) {
 // One warp per token: for each of its k slots, dy = BF16(w dout) and dw = sum_h dout y in
 // float32 (each lane sums its columns in order with one rounding per term, then a
 // fixed-shape butterfly over the lanes: the same order on every run).
+// Also (amax_bits != nullptr) the max |dy| of each expert's rows, for the transposed
+// quantisation of dy: the slot's expert is the group holding it (starts [E+1]).
 __global__ void __launch_bounds__(256) combine_backward_kernel(const __nv_bfloat16* __restrict__ dout,
                                                                const int32_t* __restrict__ inv,
                                                                const float* __restrict__ w,
                                                                const __nv_bfloat16* __restrict__ y, int64_t T, int k,
                                                                int64_t H, __nv_bfloat16* __restrict__ dy,
-                                                               float* __restrict__ dw) {
+                                                               float* __restrict__ dw,
+                                                               const int32_t* __restrict__ starts, int E,
+                                                               uint32_t* __restrict__ amax_bits) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t nwarp = (int64_t)gridDim.x * 8;
@@ -66,6 +70,7 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(const __nv_bfloat
       const int32_t slot = inv[t * k + j];
       const float wj = w[t * k + j];
       float acc = 0.0f;
+      uint32_t m = 0;
       if (slot >= 0) {
         for (int64_t c = 8 * lane; c < H; c += 256) {
           const uint4 dq = ldg_nc(dout + t * H + c);
@@ -79,6 +84,7 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(const __nv_bfloat
             o[p] = bf16_of_product(wj, d0) | (bf16_of_product(wj, d1) << 16);
             acc = __fmaf_rn(d0, y0, acc);
             acc = __fmaf_rn(d1, y1, acc);
+            asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(o[p] & 0x7FFF7FFFu));
           }
           *reinterpret_cast<uint4*>(dy + (int64_t)slot * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
         }
@@ -86,18 +92,29 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(const __nv_bfloat
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kAll, acc, o));
       if (lane == 0) dw[t * k + j] = acc;
+      if (amax_bits != nullptr && slot >= 0) {   // warp-uniform
+        uint32_t mb = max(m & 0xFFFFu, m >> 16) << 16;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(kAll, mb, o));
+        if (lane == 0 && mb != 0u) atomicMax(amax_bits + find_group(starts, E, slot), mb);
+      }
     }
   }
 }
 
 cudaError_t launch_combine_backward(const void* dout, const int32_t* inv, const float* w, const void* y, int64_t T,
-                                    int k, int64_t H, void* dy, float* dw, cudaStream_t s) {
+                                    int k, int64_t H, void* dy, float* dw, const int32_t* starts, int E,
+                                    uint32_t* amax_bits, cudaStream_t s) {
+  if (amax_bits != nullptr) {
+    const cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t) * E, s);
+    if (err != cudaSuccess) return err;
+  }
   if (T == 0) return cudaSuccess;
   int64_t blocks = (T + 7) / 8;
   if (blocks > 16 * (int64_t)num_sms()) blocks = 16 * (int64_t)num_sms();
   combine_backward_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dout), inv, w,
                                                       static_cast<const __nv_bfloat16*>(y), T, k, H,
-                                                      static_cast<__nv_bfloat16*>(dy), dw);
+                                                      static_cast<__nv_bfloat16*>(dy), dw, starts, E, amax_bits);
   return cudaGetLastError();
 }
 
@@ -212,7 +229,7 @@ struct TQuant {
 };
 
 constexpr int kTQRows = 128;                                  // output rows per unit
-constexpr int kTQSmem = 256 * kTQRows * 2 + kTQRows * 144;    // source tile + image
+constexpr int kTQSmem = 256 * kTQRows * 2 + kTQRows * 144 + 256 * 8;   // source tile + image + rows
 
 template <int RND>
 __global__ void __launch_bounds__(256) tquant_kernel(const TQuant q) {
@@ -220,6 +237,7 @@ __global__ void __launch_bounds__(256) tquant_kernel(const TQuant q) {
   constexpr int R = kTQRows;
   uint8_t* tile = tsm;                                        // [256 tokens][128 features] BF16
   uint8_t* img = tsm + 256 * R * 2;                           // the unit's 18 KB image
+  int64_t* srow = reinterpret_cast<int64_t*>(img + R * 144);  // source row of each tile token
   const uint32_t tile_s = smem_u32(tile);
   const int tid = threadIdx.x;
   const int rblocks = q.Fp / R;
@@ -234,16 +252,21 @@ __global__ void __launch_bounds__(256) tquant_kernel(const TQuant q) {
     const int64_t start = q.starts != nullptr ? q.starts[e] : (int64_t)e * q.uniform;
     const int64_t count = q.counts != nullptr ? q.counts[e] : q.uniform;
     const int f0 = rb * R;
-    // 1. the source tile: tokens kb*256 .. +255 of the expert, features f0 .. f0+127
+    // 1. the source tile: tokens kb*256 .. +255 of the expert, features f0 .. f0+127; the
+    //    tile's 256 source rows are looked up once (one per thread) before the copies
+    {
+      const int64_t tok = (int64_t)kb * 256 + tid;
+      const int64_t r = start + tok;
+      srow[tid] = tok < count ? (q.rowmap != nullptr ? (int64_t)q.rowmap[r] : r) : -1;
+    }
+    __syncthreads();
     constexpr int kChunksPerRow = R * 2 / 16;
     for (int i = tid; i < 256 * kChunksPerRow; i += 256) {
       const int t = i / kChunksPerRow, ch = i - t * kChunksPerRow;
-      const int64_t tok = (int64_t)kb * 256 + t;
       const int f = f0 + ch * 8;
       const uint32_t dst = tile_s + (uint32_t)(t * R * 2 + ch * 16);
-      if (tok < count && f < q.F) {
-        const int64_t r = start + tok;
-        const int64_t sr = q.rowmap != nullptr ? q.rowmap[r] : r;
+      const int64_t sr = srow[t];
+      if (sr >= 0 && f < q.F) {
         cp_async_16(dst, q.src + sr * q.ld + f);
       } else {
         *reinterpret_cast<uint4*>(tile + t * R * 2 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);

@@ -332,22 +332,27 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
         // columns, i.e. h columns n_tile*128 + half*64 + sub*32 + [0, 32).  All 32 values
         // take the branch-free float32 path first (independent chains the compiler can
         // interleave); the rare values it cannot settle are recorded for the next tile.
-        uint32_t vg[32], vu[32];
-        NVFP4_TMEM_LD_X32(taddr + 32 * sub, vg);
-        NVFP4_TMEM_LD_X32(taddr + 64 + 32 * sub, vu);
-        tmem_ld_wait();
+        // gu: BF16 gate | BF16 up << 16, one rounding instruction per pair.  The slice
+        // comes out of TMEM in two halves of 16 columns, each packed before the next is
+        // loaded, so that at most 48 of the accumulator's registers are live at once.
+        uint32_t gu[32];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t vg[16], vu[16];
+          NVFP4_TMEM_LD_X16(taddr + 32 * sub + 16 * hh, vg);
+          NVFP4_TMEM_LD_X16(taddr + 64 + 32 * sub + 16 * hh, vu);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(vg[i]), scale),
+                                                            __fmul_rn(__uint_as_float(vu[i]), scale));
+            gu[16 * hh + i] = *reinterpret_cast<const uint32_t*>(&pr);
+          }
+        }
         tc_fence_before();
         mbar_arrive(&sm.acce);
         flush_deferred();   // the previous tile's leftovers (its box is written by now)
         if (skip) continue;
-        // gu: BF16 gate | BF16 up << 16, one rounding instruction per pair
-        uint32_t gu[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const __nv_bfloat162 pr = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(vg[i]), scale),
-                                                          __fmul_rn(__uint_as_float(vu[i]), scale));
-          gu[i] = *reinterpret_cast<const uint32_t*>(&pr);
-        }
         const int32_t x = n_tile * 128 + half * 64 + sub * 32;
         d_hp = g.h + row * g.I + x;
         d_row = row;

@@ -126,8 +126,11 @@ int tiled_max_experts();
 cudaError_t launch_grouped_gemm_ragged_k(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd,
                                          const GemmArgs& g, cudaStream_t s);
 // Backward kernels (backward.cu).
+// amax_bits (nullable): zeroed, then the max |dy| of each expert's rows (starts: the
+// padded group offsets [E+1]).
 cudaError_t launch_combine_backward(const void* dout, const int32_t* inv, const float* w, const void* y, int64_t T,
-                                    int k, int64_t H, void* dy, float* dw, cudaStream_t s);
+                                    int k, int64_t H, void* dy, float* dw, const int32_t* starts, int E,
+                                    uint32_t* amax_bits, cudaStream_t s);
 cudaError_t launch_group_amax(const void* src, int64_t ld, int64_t F, const int32_t* rowmap, const int32_t* starts,
                               const int32_t* counts, int E, int64_t max_rows, uint32_t* amax_bits, cudaStream_t s);
 cudaError_t launch_kofs(const int32_t* counts, int64_t uniform, int E, int32_t* kofs, cudaStream_t s);

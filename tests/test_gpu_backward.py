@@ -95,7 +95,13 @@ def _check_backward(lib, shape, r):
     mag = np.stack([np.sum(np.abs(dv * yv[inv[:, j]]), axis=1) for j in range(k)], axis=1)
     assert np.all(np.abs(npy(r["dw"]) - dw_ref) <= (H + 2) * 2.0 ** -24 * mag + 1e-30)
 
-    # 2. dy rows quantised (stochastic rounding, stream 0), then dh = Q(dy) Q(W2^T)
+    # 2. dy rows quantised (stochastic rounding, stream 0), then dh = Q(dy) Q(W2^T); the
+    #    padding slots hold whatever the workspace held (never read by the kernels): zero
+    #    them for the oracle, which quantises the whole slot layout (row index = slot)
+    pad = np.ones(n, bool)
+    pad[live] = False
+    dy_gpu = dy_gpu.copy()
+    dy_gpu[pad] = 0
     dyq_c, dyq_sf = untile_host(npy(bws[blay[1]:blay[2]]), mcap, H, 128)
     q_dy = Q.quantize(dy_gpu, scope="row", rounding="sr", seed=B.sr_key(seed, B.STREAM_DGRAD_DOWN))
     np.testing.assert_array_equal(dyq_c[live], q_dy["codes"][live])
@@ -112,7 +118,8 @@ def _check_backward(lib, shape, r):
     d_can = np.empty_like(d_gpu)
     d_can[:, _src_interleave(I)] = d_gpu
     np.testing.assert_array_equal(M.swiglu(d_can[live], I), h_gpu[live])
-    dD_gpu = u16(_views(bws, blay, 5, mcap * 2 * I, torch.bfloat16).view(mcap, 2 * I))[:n]
+    dD_gpu = u16(_views(bws, blay, 5, mcap * 2 * I, torch.bfloat16).view(mcap, 2 * I))[:n].copy()
+    dD_gpu[pad] = 0
     dD_ref = M.swiglu_backward(d_can[live], dh_gpu[live][:, :I], I)
     for part in (slice(0, I), slice(I, 2 * I)):
         nbad, worst = check_bf16_against(dD_gpu[live][:, part], F.bf16_to_f32(dD_ref[:, part]).astype(np.float64))
