@@ -274,41 +274,49 @@ __device__ __forceinline__ uint32_t e2m1_exact_sr(float x, float s, uint32_t r16
 
 // 8 values of one chunk with their Philox block output -> packed codes of the
 // stochastically rounded exact quotients.  One product v = |x| r per value (|v/q - 1| <=
-// 2^-21 for the exact quotient q = |x|/s).  On the grid segment holding v, t = (v - G)/gap
-// + (index of G) is exact given v (2v below 2, v - 2 below 4, v/2 - 2 above), and the
-// rounding goes up iff r16 < frac(t) 2^16.  In units of 2^-16 of a gap, v's error moves
-// t by at most 0.125, so the decision is the exact quotient's unless frac(t) 2^16 lies
-// within 0.25 of r16 or of 0 / 2^16 (the next grid point); those values -- about one in
-// 10^5 -- take the exact count of thresholds below q (e2m1_exact_sr).
+// 2^-21 for the exact quotient q = |x|/s).  The rounding counts the thresholds
+// tau_j = G_{j-1} + r16 (G_j - G_{j-1}) / 2^16 below q; on the grid coordinate
+// X = 2^16 t (t = 2v below 2, v + 2 below 4, v/2 + 4 above, so that grid point G_i sits at
+// X = 2^16 i) they are the integers T_j = 2^16 (j - 1) + r16, and the code is the number of
+// T_j below X.  X4 = floor(4X) is formed without rounding: below v = 1 by one FMA rounded
+// down (v 2^19 counted in units of the last place of a float whose bits are offset by
+// 0x3F00000); from v = 1 on, t is linear within each binade of v with the binade's slope,
+// so X4 = (bits(v) - 0x3F000000) / 16 exactly.  v's error moves X by at most 1/8, so the
+// count is the exact quotient's unless X4 - 4 T_j is -1 or 0 for some j; those values --
+// about one in 10^5 -- take the exact count of thresholds below q (e2m1_exact_sr).  The
+// count from X4 is (X4 + 2^18 - 1 - 4 r16) / 2^18, saturated at 7.
 __device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockScale& bs, uint4 rnd) {
   const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
   if (!(bs.s > 0.0f)) return 0u;
   if (!bs.exact_only) {
-    float v[8];
-    scale8(f, bs.r, v);
-    uint32_t out = 0, amb = 0;
+    uint32_t out = 0, signs = 0, near = 0xFFFFFFFFu;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float a = fabsf(v[e]);
-      const float r16 = (float)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
-      const bool s0 = a < 2.0f, s1 = a < 4.0f;
-      const float t = s0 ? __fmul_rn(a, 2.0f) : (s1 ? __fsub_rn(a, 2.0f) : __fmaf_rn(a, 0.5f, -2.0f));
-      const float fl = floorf(t);
-      const float y = __fmul_rn(__fsub_rn(t, fl), 65536.0f);     // frac(t) 2^16, exact
-      const float cf = __fadd_rn(__fadd_rn(s0 ? 0.0f : (s1 ? 4.0f : 6.0f), fl), r16 < y ? 1.0f : 0.0f);
-      // the 3-bit code from the float's low mantissa bits (cf < 2^22), saturated at 7
-      uint32_t c = min(__float_as_uint(__fadd_rn(cf, 8388608.0f)) & 0xFFFFu, 7u);
-      if (a >= 6.0f) c = 7u;
-      const bool near = fabsf(__fsub_rn(y, r16)) < 0.25f || y < 0.25f || y > 65535.75f;
-      if (near && a < 6.0f && f[e] != 0.0f) amb |= 1u << e;
-      out |= (c | ((__float_as_uint(f[e]) >> 31) && c ? 8u : 0u)) << (4 * e);
+      const float v = __fmul_rn(fabsf(f[e]), bs.r);
+      const uint32_t vb = __float_as_uint(v);
+      // bits of v 2^-124 + 2^-120 (1 + 0x700000 / 2^23), rounded down: 0x3F00000 + floor(v 2^19)
+      const uint32_t lin = __float_as_uint(__fmaf_rd(v, 0x1p-124f, 0x1.ep-120f));
+      const uint32_t x4 = vb < 0x3F800000u ? lin : (vb >> 4);          // X4 + 0x3F00000
+      const uint32_t r16 = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+      const uint32_t a = x4 - 4u * r16 + (0x3FFFFu - 0x3F00000u);      // X4 + 2^18 - 1 - 4 r16
+      near = min(near, ~a & 0x3FFFEu);                                  // 0: X4 - 4 T_j in {-1, 0}
+      out |= min(a >> 18, 7u) << (4 * e);
+      signs |= (__float_as_uint(f[e]) >> 31) << (4 * e + 3);
     }
-    while (amb != 0u) {
-      const uint32_t e = (uint32_t)(__ffs((int)amb) - 1);
-      const uint32_t we = (e & 4u) ? ((e & 2u) ? w[3] : w[2]) : ((e & 2u) ? w[1] : w[0]);
-      const uint32_t c = e2m1_exact_sr(pick8(f, e), bs.s, (we >> (16 * (e & 1u))) & 0xFFFFu);
-      out = (out & ~(0xFu << (4 * e))) | (c << (4 * e));
-      amb &= amb - 1u;
+    out = canonical_zero(out | signs);
+    if (near == 0u) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t vb = __float_as_uint(__fmul_rn(fabsf(f[e]), bs.r));
+        const uint32_t lin = __float_as_uint(__fmaf_rd(__uint_as_float(vb), 0x1p-124f, 0x1.ep-120f));
+        const uint32_t x4 = vb < 0x3F800000u ? lin : (vb >> 4);
+        const uint32_t r16 = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+        const uint32_t a = x4 - 4u * r16 + (0x3FFFFu - 0x3F00000u);
+        if ((~a & 0x3FFFEu) == 0u) {
+          const uint32_t c = e2m1_exact_sr(f[e], bs.s, r16);
+          out = (out & ~(0xFu << (4 * e))) | (c << (4 * e));
+        }
+      }
     }
     return out;
   }
