@@ -342,7 +342,12 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* SFA, const floa
  *     and up outputs: silu(gate) * up evaluated in float64 and rounded once to BF16.
  *     The first SwiGLU call on a device (this one, moe_swiglu_quantize or
  *     moe_expert_forward) builds a 512 KB table of silu over the BF16 values with one
- *     kernel on `stream` and waits for it; make that first call outside stream capture. */
+ *     kernel on `stream` and waits for it; make that first call outside stream capture.
+ * Kernel form: one CTA per 128-row x 256-column tile by default.  With the environment
+ * variable NVFP4_GEMM_CTA_PAIR=1 (read at every launch) a cluster of two CTAs shares each
+ * 256-row x 256-column tile of one expert (tcgen05 cta_group::2, M=256); the results are
+ * identical.  The ragged-K weight-gradient GEMMs of moe_expert_backward always use one CTA
+ * per tile. */
 enum { NVFP4_EPILOGUE_STORE = 0, NVFP4_EPILOGUE_SWIGLU = 1 };
 nvfp4_status nvfp4_grouped_gemm_tiled(const uint8_t* A_tiled, const float* gA, const uint8_t* B_tiled,
                                       const float* gB, const int32_t* group_offsets,

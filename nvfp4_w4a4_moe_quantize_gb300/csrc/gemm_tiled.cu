@@ -29,6 +29,7 @@
 //               partial tile is stored row by row, so rows outside the groups are never
 //               written.
 // Tiles are (128-row block) x (256 columns), row-block-major; no split-K, fixed K order.
+#include <cstdlib>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,12 +45,13 @@ namespace nvfp4 {
 namespace gt {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
-constexpr int kStages = 3;
 constexpr int kOutBytes = 32 * 1024;        // staged output boxes of all epilogue warps
 constexpr int kABlock = 128 * 144;          // 16 KB codes + 2 KB scales
 constexpr int kBBlock = 256 * 144;          // 32 KB codes + 4 KB scales
 constexpr int kACodes = 128 * 128;
 constexpr int kBCodes = 256 * 128;
+constexpr int kBHalfCodes = 128 * 128;      // one CTA's half of a B block's codes (pair mode)
+constexpr int kBScales = 256 * 16;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = kBN;
 constexpr int kSFCol0 = kAccCols;
@@ -62,24 +64,43 @@ __host__ __device__ constexpr int epi_warps(bool swiglu) { return swiglu ? 16 : 
 __host__ __device__ constexpr int threads(bool swiglu) { return 32 * (kFirstEpiWarp + epi_warps(swiglu)); }
 constexpr int kMaxE = 512;
 
+// One pipeline stage in shared memory.  One SM per tile (kPair false): the A block
+// (codes, then scales) at 0 and the whole B block (codes, then scales) after it.  CTA
+// pair: this CTA's half of B's codes at 0, the A block at 16 KB (its scales at 32 KB) and
+// all of B's scales (both halves' rows, which each SM's MMA reads) at 34 KB.
+template <bool kPair>
+struct Layout {
+  static constexpr int kStages = kPair ? 4 : 3;
+  static constexpr int kStageBytes = kPair ? kBHalfCodes + kABlock + kBScales : kABlock + kBBlock;
+  static constexpr int kA = kPair ? kBHalfCodes : 0;
+  static constexpr int kB = kPair ? 0 : kABlock;
+  static constexpr int kSFA = kA + kACodes;
+  static constexpr int kSFB = kPair ? kBHalfCodes + kABlock : kABlock + kBCodes;
+};
+
+template <bool kPair>
 struct Smem {
-  uint8_t a[kStages][kABlock];
-  uint8_t b[kStages][kBBlock];
+  uint8_t stage[Layout<kPair>::kStages][Layout<kPair>::kStageBytes];
   uint8_t out[kOutBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[Layout<kPair>::kStages];
+  uint64_t empty[Layout<kPair>::kStages];
   uint64_t accf;
   uint64_t acce;
+  uint64_t fin;               // the MMA issuer's last operations have completed
   uint32_t tmem_base;
   int abort;
   int32_t offsets[kMaxE + 1];
   int32_t rows[kMaxE];
   float gb[kMaxE];
+  int32_t pairs[kMaxE + 1];   // CTA pair: row-block pairs before group e
 };
-static_assert(kABlock % 1024 == 0 && kBBlock % 1024 == 0, "1024-byte aligned stage images");
-static_assert(kSFCol0 + kStages * kSFStageCols <= kTmemCols, "TMEM budget");
-static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kABlock % 1024 == 0 && kBBlock % 1024 == 0 && kBHalfCodes % 1024 == 0, "1024-byte aligned images");
+static_assert(Layout<false>::kStageBytes % 1024 == 0 && Layout<true>::kStageBytes % 1024 == 0, "stage alignment");
+static_assert(kSFCol0 + Layout<false>::kStages * kSFStageCols <= kTmemCols, "TMEM budget");
+static_assert(kSFCol0 + Layout<true>::kStages * kSFStageCols <= kTmemCols, "TMEM budget");
+static_assert(sizeof(Smem<false>) + 1024 <= 232448 && sizeof(Smem<true>) + 1024 <= 232448, "shared memory budget");
+template <bool kPair>
+constexpr size_t smem_bytes() { return sizeof(Smem<kPair>) + 1024; }
 }  // namespace gt
 
 // One lane's 128-byte row of a warp's 32-row output box, written 128-byte swizzled (16-byte
@@ -114,7 +135,8 @@ struct TileJob {
   int kblocks;
   int e, n_tile;
   int32_t row0;        // first output row
-  int32_t in_group;    // valid rows of the tile (>= 128: all)
+  int32_t in_group;    // valid rows of the tile (>= 128: all; <= 0: none)
+  bool has_a;          // false: the pair's second row block lies past its group (no A load)
 };
 
 template <bool kRagged>
@@ -144,20 +166,53 @@ __device__ __forceinline__ TileJob tile_job(const GemmArgs& g, const int32_t* of
     j.b = B + ((int64_t)j.e * n_tiles + j.n_tile) * kblocks * gt::kBBlock;
     j.in_group = rows[j.e] - (j.row0 - offsets[j.e]);
   }
+  j.has_a = true;
+  return j;
+}
+
+// CTA pair: unit p of a group is the pair of row blocks (2 jj, 2 jj + 1) of the group
+// (jj = p - pairs[e]), CTA `rank` of the pair taking block 2 jj + rank; a group with an odd
+// number of row blocks leaves its last pair's second block empty (that CTA loads no A and
+// stores nothing; its half of the MMA is discarded).  Both row blocks are one expert's, so
+// the pair shares B's column tile.
+__device__ __forceinline__ TileJob tile_job_pair(const GemmArgs& g, const int32_t* offsets, const int32_t* rows,
+                                                 const int32_t* pairs, const uint8_t* A, const uint8_t* B, int t,
+                                                 int n_tiles, int kblocks, uint32_t rank) {
+  TileJob j;
+  const int p = t / n_tiles;
+  j.n_tile = t - p * n_tiles;
+  j.e = find_group(pairs, g.E, p);
+  const int32_t blocks_e = (offsets[j.e + 1] - offsets[j.e]) / gt::kBM;
+  const int32_t jb = 2 * (p - pairs[j.e]) + (int32_t)rank;   // row block within the group
+  j.has_a = jb < blocks_e;
+  j.row0 = offsets[j.e] + jb * gt::kBM;
+  j.kblocks = kblocks;
+  j.a = A + (int64_t)(j.row0 / gt::kBM) * kblocks * gt::kABlock;
+  j.b = B + ((int64_t)j.e * n_tiles + j.n_tile) * kblocks * gt::kBBlock;
+  j.in_group = j.has_a ? rows[j.e] - (j.row0 - offsets[j.e]) : 0;
   return j;
 }
 
 // kMode: 0 plain store, 1 SwiGLU epilogue, 2 plain store with ragged K per expert.
-template <int kMode>
+// kPair: a cluster of two CTAs on two SMs shares each M=256 x N=256 tile (cta_group::2):
+// CTA 0 issues the MMAs and the scale copies; each CTA loads its own A block, its half of
+// B's codes and all of B's scales into its own shared memory (no shared loads); CTA 1's
+// warp 2 tells CTA 0 when a stage of CTA 1 is full; CTA 0's commits free the stages and
+// fill the accumulators of both; both CTAs' epilogues release the accumulator to CTA 0.
+template <int kMode, bool kPair>
 __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
     grouped_gemm_tiled_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B,
                               const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
   using namespace gt;
+  using L = Layout<kPair>;
+  constexpr int kStages = L::kStages;
   constexpr bool kSwiGLU = kMode == 1, kRagged = kMode == 2;
+  static_assert(!(kPair && kRagged), "the CTA pair runs the grouped-row modes");
   constexpr int kEpiWarps = epi_warps(kSwiGLU);
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<kPair>& sm = *reinterpret_cast<Smem<kPair>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
 
   for (int i = threadIdx.x; i <= g.E; i += blockDim.x) sm.offsets[i] = g.offsets[i];
   for (int i = threadIdx.x; i < g.E; i += blockDim.x) {
@@ -166,48 +221,87 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
   }
   __syncthreads();
   // nothing is read or written unless the group arrays are consistent (ragged K: g.offsets
-  // are the K-block prefix sums, every expert at least one block, at most g.m_total blocks)
+  // are the K-block prefix sums, every expert at least one block, at most g.m_total blocks);
+  // both CTAs of a pair read the same arrays and leave together, before any cluster step
   if (kRagged ? !kblocks_valid(sm.offsets, g.E, g.m_total) : !groups_valid(sm.offsets, sm.rows, g.E, g.m_total)) {
     if (threadIdx.x == 0) set_status(g.status, kStatusBadInput);
     return;
   }
   if (threadIdx.x == 0) {
+    if (kPair) {
+      sm.pairs[0] = 0;
+      for (int e = 0; e < g.E; ++e)
+        sm.pairs[e + 1] = sm.pairs[e] + ((sm.offsets[e + 1] - sm.offsets[e]) / kBM + 1) / 2;
+    }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 2);            // the A and the B producer arrive
+      // the A and the B producer arrive; in a pair CTA 0 also hears from CTA 1's warp 2
+      mbar_init(&sm.full[s], kPair && rank == 0 ? 3 : 2);
       mbar_init(&sm.empty[s], 1);
     }
     mbar_init(&sm.accf, 1);
-    mbar_init(&sm.acce, kEpiWarps * 32);
+    mbar_init(&sm.fin, 1);
+    // pair: one arrival per epilogue warp of either CTA (on CTA 0's barrier)
+    mbar_init(&sm.acce, kPair ? 2 * kEpiWarps : kEpiWarps * 32);
     sm.abort = 0;
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(&sm.tmem_base, kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&sm.tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();   // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return kPair ? mbar_wait_cluster(bar, parity, g.status, abort) : mbar_wait(bar, parity, g.status, abort);
+  };
 
   const int n_tiles = g.N / kBN;
   const int m_tiles = kRagged ? g.m_rows / kBM : sm.offsets[g.E] / kBM;   // ragged: per expert
-  const int total = kRagged ? g.E * m_tiles * n_tiles : m_tiles * n_tiles;
+  const int total = kRagged ? g.E * m_tiles * n_tiles : (kPair ? sm.pairs[g.E] : m_tiles) * n_tiles;
   const int kblocks = g.K / 256;
+  const int first = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int stride = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  auto job_of = [&](int t) {
+    return kPair ? tile_job_pair(g, sm.offsets, sm.rows, sm.pairs, A, B, t, n_tiles, kblocks, rank)
+                 : tile_job<kRagged>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks);
+  };
 
   if (warp < 2) {
     if (lane == 0) {
       const bool is_a = warp == 0;
       uint32_t stage = 0, phase = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const TileJob job = tile_job<kRagged>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks);
-        const uint8_t* src = is_a ? job.a : job.b;
+      for (int t = first; t < total; t += stride) {
+        const TileJob job = job_of(t);
         for (int kb = 0; kb < job.kblocks; ++kb) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, g.status, abort)) goto producer_done;
-          const uint32_t bytes = is_a ? kABlock : kBBlock;
-          mbar_arrive_expect_tx(&sm.full[stage], bytes);
-          bulk_load(is_a ? sm.a[stage] : sm.b[stage], src + (int64_t)kb * bytes, bytes, &sm.full[stage]);
+          if (!wait(&sm.empty[stage], phase ^ 1u)) goto producer_done;
+          uint8_t* st = sm.stage[stage];
+          if (is_a) {
+            if (job.has_a) {
+              mbar_arrive_expect_tx(&sm.full[stage], kABlock);
+              bulk_load(st + L::kA, job.a + (int64_t)kb * kABlock, kABlock, &sm.full[stage]);
+            } else {
+              mbar_arrive(&sm.full[stage]);
+            }
+          } else {
+            const uint8_t* src = job.b + (int64_t)kb * kBBlock;
+            if (kPair) {
+              mbar_arrive_expect_tx(&sm.full[stage], kBHalfCodes + kBScales);
+              bulk_load(st + L::kB, src + rank * kBHalfCodes, kBHalfCodes, &sm.full[stage]);
+              bulk_load(st + L::kSFB, src + kBCodes, kBScales, &sm.full[stage]);
+            } else {
+              mbar_arrive_expect_tx(&sm.full[stage], kBBlock);
+              bulk_load(st + L::kB, src, kBBlock, &sm.full[stage]);
+            }
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -217,48 +311,89 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
     producer_done:;
     }
   } else if (warp == 2) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(kPair ? 2 * kBM : kBM, kBN);
       uint32_t stage = 0, phase = 0;
       int it = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      for (int t = first; t < total; t += stride, ++it) {
         const int kbt = kRagged ? tile_job<true>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks).kblocks
                                 : kblocks;
         for (int kb = 0; kb < kbt; ++kb) {
-          if (!mbar_wait(&sm.full[stage], phase, g.status, abort)) goto mma_done;
+          if (!wait(&sm.full[stage], phase)) goto mma_done;
           tc_fence_after();
           const uint32_t sfa_t = tmem + kSFCol0 + stage * kSFStageCols;
           const uint32_t sfb_t = sfa_t + 16;
-          const uint32_t sa = smem_u32(sm.a[stage]), sb = smem_u32(sm.b[stage]);
-          const uint32_t ssfa = sa + kACodes, ssfb = sb + kBCodes;
+          const uint32_t st = smem_u32(sm.stage[stage]);
+          const uint32_t sa = st + L::kA, sb = st + L::kB;
+          const uint32_t ssfa = st + L::kSFA, ssfb = st + L::kSFB;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
-            tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
-            tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
+            if (kPair) {
+              tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
+              tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
+              tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
+            } else {
+              tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
+              tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
+              tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
+            }
           }
           if (kb == 0) {
             // The first stage's scale copies are issued before this wait: they do not touch
             // the accumulator, so the tensor pipe runs them while the epilogue drains the
             // previous tile (tcgen05 ops of one thread execute in issue order).
-            if (!mbar_wait(&sm.acce, (it & 1) ^ 1u, g.status, abort)) goto mma_done;
+            if (!wait(&sm.acce, (it & 1) ^ 1u)) goto mma_done;
             tc_fence_after();
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
             const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
-            tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+            if (kPair)
+              tc_mma_nvf4_pair(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+            else
+              tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
           }
-          tc_commit(&sm.empty[stage]);
+          if (kPair) {
+            tc_commit_pair(cluster_addr(&sm.empty[stage], 0));
+            tc_commit_pair(cluster_addr(&sm.empty[stage], 1));
+          } else {
+            tc_commit(&sm.empty[stage]);
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        tc_commit(&sm.accf);
+        if (kPair) {
+          tc_commit_pair(cluster_addr(&sm.accf, 0));
+          tc_commit_pair(cluster_addr(&sm.accf, 1));
+        } else {
+          tc_commit(&sm.accf);
+        }
       }
-    mma_done:;
+    mma_done:
+      // whatever the exit, no MMA or scale copy of this thread is still running when
+      // the TMEM is freed (a bounded wait of its own, also after an abort)
+      if (kPair) tc_commit_pair(cluster_addr(&sm.fin, 0));
+      else tc_commit(&sm.fin);
+      volatile int no_abort = 0;
+      mbar_wait(&sm.fin, 0, g.status, &no_abort, 1000000000ull);
+    } else if (kPair && lane == 0) {
+      // CTA 1: each of this CTA's full stages counts as one arrival on CTA 0's barrier
+      uint32_t stage = 0, phase = 0;
+      const uint32_t full0 = cluster_addr(&sm.full[0], 0);
+      for (int t = first; t < total; t += stride) {
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait(&sm.full[stage], phase)) goto relay_done;
+          mbar_arrive_cluster(full0 + stage * (uint32_t)sizeof(uint64_t));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    relay_done:;
     }
   } else {
     // epilogue: TMEM lane quadrant q = warp % 4 (the lanes this warp may read), column
@@ -301,10 +436,22 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
       d_n = 0;
       d_mask = 0;
     };
+    // the accumulator is drained: every lane arrives on its CTA's barrier, or, in a pair,
+    // one lane per warp on CTA 0's
+    const uint32_t acce0 = kPair ? cluster_addr(&sm.acce, 0) : 0u;
+    auto release_acc = [&]() {
+      tc_fence_before();
+      if (kPair) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce0);
+      } else {
+        mbar_arrive(&sm.acce);
+      }
+    };
     bool aborted = false;
     int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const TileJob job = tile_job<kRagged>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks);
+    for (int t = first; t < total; t += stride, ++it) {
+      const TileJob job = job_of(t);
       const int n_tile = job.n_tile, e = job.e;
       const int32_t row0 = job.row0, in_group = job.in_group;
       const bool valid = q * 32 + lane < in_group;
@@ -312,7 +459,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
       const int64_t row = (int64_t)row0 + q * 32 + lane;
       const float ga = kRagged ? g.ga[e] : (valid ? g.ga[row] : 0.0f);   // ragged: one scale per expert
       // every lane waits (bounded), then the warp leaves together if any lane gave up
-      const bool acc_ready = mbar_wait(&sm.accf, it & 1, g.status, abort);
+      const bool acc_ready = wait(&sm.accf, it & 1);
       if (!__all_sync(0xFFFFFFFFu, acc_ready)) {
         aborted = true;
         break;
@@ -349,8 +496,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
             gu[16 * hh + i] = *reinterpret_cast<const uint32_t*>(&pr);
           }
         }
-        tc_fence_before();
-        mbar_arrive(&sm.acce);
+        release_acc();
         flush_deferred();   // the previous tile's leftovers (its box is written by now)
         if (skip) continue;
         const int32_t x = n_tile * 128 + half * 64 + sub * 32;
@@ -423,8 +569,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) NVFP4_TMEM_LD_X32(taddr + 32 * c, v[c]);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&sm.acce);
+        release_acc();
         if (skip) continue;
         if (!g.out_f32) {
 #pragma unroll
@@ -478,8 +623,12 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();   // no remote arrival or peer read is left in flight
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 2) {
+    if (kPair) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 template <int kMode>
@@ -487,19 +636,67 @@ static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtens
                                 int64_t tiles, cudaStream_t s) {
   if (kMode == 1 && g.silu_tab == nullptr) return cudaErrorInvalidValue;
   static std::atomic<bool> attr_set[64];   // the attribute is set once per device
-  cudaError_t err =
-      set_smem_attr_once(attr_set, (const void*)grouped_gemm_tiled_kernel<kMode>, (int)gt::kSmemBytes);
+  cudaError_t err = set_smem_attr_once(attr_set, (const void*)grouped_gemm_tiled_kernel<kMode, false>,
+                                       (int)gt::smem_bytes<false>());
   if (err != cudaSuccess) return err;
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
-  grouped_gemm_tiled_kernel<kMode><<<grid, gt::threads(kMode == 1), gt::kSmemBytes, s>>>(A, B, tmd, g);
+  grouped_gemm_tiled_kernel<kMode, false>
+      <<<grid, gt::threads(kMode == 1), gt::smem_bytes<false>(), s>>>(A, B, tmd, g);
   return cudaGetLastError();
+}
+
+// CTA-pair launch: clusters of two CTAs, as many clusters as fit on the device at once
+// (one CTA per SM), each looping over pair tiles.  `tiles` bounds the pair tiles.
+template <int kMode>
+static cudaError_t launch_pair(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
+                               int64_t tiles, cudaStream_t s) {
+  if (kMode == 1 && g.silu_tab == nullptr) return cudaErrorInvalidValue;
+  const void* fn = (const void*)grouped_gemm_tiled_kernel<kMode, true>;
+  static std::atomic<bool> attr_set[64];
+  cudaError_t err = set_smem_attr_once(attr_set, fn, (int)gt::smem_bytes<true>());
+  if (err != cudaSuccess) return err;
+  if (tiles == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(gt::threads(kMode == 1), 1, 1);
+  cfg.dynamicSmemBytes = gt::smem_bytes<true>();
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static std::atomic<int> resident[64];   // clusters resident at once, per device (0: not known yet)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int clusters = (dev >= 0 && dev < 64) ? resident[dev].load(std::memory_order_acquire) : 0;
+  if (clusters <= 0) {
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    err = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
+    if (err != cudaSuccess) return err;
+    if (clusters <= 0) return cudaErrorInvalidConfiguration;
+    if (dev >= 0 && dev < 64) resident[dev].store(clusters, std::memory_order_release);
+  }
+  if (tiles < clusters) clusters = (int)tiles;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tiled_kernel<kMode, true>, A, B, tmd, g);
+}
+
+// The CTA-pair kernel runs the grouped-row modes when NVFP4_GEMM_CTA_PAIR=1 (measured
+// slower than one CTA per tile on the forward's shapes, so not the default).
+static bool pair_enabled() {
+  const char* v = std::getenv("NVFP4_GEMM_CTA_PAIR");
+  return v != nullptr && v[0] == '1';
 }
 
 cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
                                       int64_t max_m_tiles, bool swiglu, cudaStream_t s) {
   const int64_t tiles = max_m_tiles * (g.N / gt::kBN);
+  if (pair_enabled())
+    return swiglu ? launch_pair<1>(A, B, tmd, g, tiles, s) : launch_pair<0>(A, B, tmd, g, tiles, s);
   return swiglu ? launch_tiled<1>(A, B, tmd, g, tiles, s) : launch_tiled<0>(A, B, tmd, g, tiles, s);
 }
 

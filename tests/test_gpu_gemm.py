@@ -153,6 +153,14 @@ def test_gemm_is_deterministic(cuda_lib):
 
 # ------------------------------------------------------------------ GEMM-tiled operands
 
+@pytest.fixture(params=["pair", "single"])
+def cta_mode(request, monkeypatch):
+    """The GEMM-tiled kernel in both forms: one CTA per M=128 tile (the default) and a
+    CTA pair per M=256 tile (NVFP4_GEMM_CTA_PAIR=1)."""
+    monkeypatch.setenv("NVFP4_GEMM_CTA_PAIR", "1" if request.param == "pair" else "0")
+    return request.param
+
+
 def _run_tiled(lib, ops, N, K, out_dtype=torch.float32, epilogue=0):
     from gpu_util import pack_tiled_host
     E = ops["b_codes"].shape[0]
@@ -164,7 +172,7 @@ def _run_tiled(lib, ops, N, K, out_dtype=torch.float32, epilogue=0):
     return D
 
 
-def test_tiled_gemm_exact_single_tile(cuda_lib):
+def test_tiled_gemm_exact_single_tile(cuda_lib, cta_mode):
     rng = np.random.default_rng(0)
     grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -2, -3, -4, -6])
     s_a, s_w = 448 * 2.0 ** -11, 448 * 2.0 ** -13
@@ -177,8 +185,41 @@ def test_tiled_gemm_exact_single_tile(cuda_lib):
     np.testing.assert_array_equal(D, (xa @ w[0].T).astype(np.float32))
 
 
+def _lossless_blocks(rng, rows, K, s, kmin=2):
+    """Values on the E2M1 grid times s * 2^(k-4), one k in [kmin, 4] per 16-value block,
+    each block holding a +-6 (so its scale is exactly s * 2^(k-4)) and each row one block
+    with k = 4 (so the row's global scale is exact): quantisation is lossless and every
+    partial sum of a K <= 512 product is a float32 number."""
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -2, -3, -4, -6])
+    k = rng.integers(kmin, 5, (rows, K // 16))
+    k[:, 0] = 4
+    x = rng.choice(grid, (rows, K)) * s * np.repeat(2.0 ** (k - 4), 16, axis=1)
+    x[:, ::16] = rng.choice([-6.0, 6.0], (rows, K // 16)) * s * 2.0 ** (k - 4)
+    return x
+
+
+def test_tiled_gemm_exact_block_scales_and_odd_row_blocks(cuda_lib, cta_mode):
+    """Bit-exact products with a different scale in every 16-value block of A and of W,
+    on groups of 3, 1 and 2 row blocks (the CTA pair's last pair of a group with an odd
+    block count has an empty second half): any scale read from the wrong row, column or
+    K block shows."""
+    rng = np.random.default_rng(7)
+    E, N, K = 3, 512, 512
+    counts = [269, 128, 256]
+    xa = _lossless_blocks(rng, sum(counts), K, 448 * 2.0 ** -11)
+    w = np.stack([_lossless_blocks(rng, N, K, 448 * 2.0 ** -13) for _ in range(E)])
+    ops = _operands_from_oracle(F.bf16_round(xa), counts, F.bf16_round(w))
+    D = npy(_run_tiled(cuda_lib, ops, N, K))
+    r = 0
+    for e, c in enumerate(counts):
+        p = int(ops["padded"][e])
+        want = (xa[r:r + c] @ w[e].T).astype(np.float32)
+        np.testing.assert_array_equal(D[p:p + c], want)
+        r += c
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_tiled_gemm_ragged_groups_matches_oracle_and_row_major_kernel(cuda_lib, out_dtype):
+def test_tiled_gemm_ragged_groups_matches_oracle_and_row_major_kernel(cuda_lib, out_dtype, cta_mode):
     E, N, K = 6, 512, 768
     counts = [0, 1, 127, 128, 129, 300]
     a_bits = S.bf16_bits(S.randn_bf16((sum(counts), K), seed=71))
@@ -211,7 +252,7 @@ def test_pack_tiled_matches_host_layout(cuda_lib):
         np.testing.assert_array_equal(got, pack_tiled_host(q["codes"], q["sf"], R))
 
 
-def test_tiled_swiglu_epilogue_equals_standalone_swiglu(cuda_lib):
+def test_tiled_swiglu_epilogue_equals_standalone_swiglu(cuda_lib, cta_mode):
     """gate/up GEMM with the SwiGLU epilogue == BF16 GEMM output followed by the
     standalone SwiGLU kernel (64-row interleaved gate/up weights), bit for bit."""
     E, I, K = 3, 256, 512
@@ -246,7 +287,7 @@ def test_tiled_swiglu_epilogue_equals_standalone_swiglu(cuda_lib):
 
 @pytest.mark.parametrize("N", [128, 256])
 @pytest.mark.parametrize("fault", ["rows_over_span", "offsets_past_m_total", "unaligned_offset"])
-def test_gemm_rejects_inconsistent_group_arrays(cuda_lib, N, fault):
+def test_gemm_rejects_inconsistent_group_arrays(cuda_lib, N, fault, cta_mode):
     """Group arrays that break the documented contract (rows[e] larger than its padded
     span, offsets past M_total, a start that is not a multiple of 128) set the device
     status and leave D untouched, on both tile widths and on the GEMM-tiled kernel."""
