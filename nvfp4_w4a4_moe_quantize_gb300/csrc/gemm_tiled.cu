@@ -14,9 +14,16 @@
 //
 // One CTA per SM:
 //   warp 0 / 1  producers of the A / B block of each stage (cp.async.bulk + mbarrier);
-//   warp 2      MMA issuer: tcgen05.cp of the stage's scales into TMEM, four
-//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=256,
-//               K=64) into a 256-column TMEM accumulator, tcgen05.commit;
+//   warp 2      MMA issuer: four tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//               (M=128, N=256, K=64) per stage into a 256-column TMEM accumulator,
+//               tcgen05.commit;
+//   last 4      scale warps, one per TMEM lane quadrant: each reads the stage's twelve
+//               512-byte scale blocks from shared memory and writes them into its 32 TMEM
+//               lanes with tcgen05.st, in the image a tcgen05.cp.32x128b.warpx4 of the
+//               block would leave (every quadrant holds the block's 32 x 16 bytes).  Done
+//               by tcgen05.cp, the twelve copies share the tensor pipe with the four MMAs
+//               and, measured on this GPU, stretch a stage from 512 to about 800 cycles;
+//               tcgen05.st leaves the pipe to the MMAs;
 //   warps 3..   epilogue (8 warps, two per TMEM lane quadrant, for the plain store; 16,
 //               four per quadrant, for SwiGLU): drain the accumulator into registers,
 //               release it, scale by gA[r]*gB[e] in float32 and write BF16 / float32 rows
@@ -57,11 +64,15 @@ constexpr int kAccCols = kBN;
 constexpr int kSFCol0 = kAccCols;
 constexpr int kSFStageCols = 16 + 32;       // A: 4 x 4 columns, B: 4 x 8 columns
 constexpr int kFirstEpiWarp = 3;
+constexpr int kScaleWarps = 4;              // one CTA per tile: one per TMEM lane quadrant
 // Epilogue warps: 8 for the plain store (two per TMEM lane quadrant, 128 columns each);
 // 16 for the SwiGLU epilogue, whose per-value arithmetic needs the latency hiding of four
 // warps per quadrant (each one 32-column gate slice and its up slice).
 __host__ __device__ constexpr int epi_warps(bool swiglu) { return swiglu ? 16 : 8; }
-__host__ __device__ constexpr int threads(bool swiglu) { return 32 * (kFirstEpiWarp + epi_warps(swiglu)); }
+// The CTA pair keeps the scale copies on tcgen05.cp (issued by CTA 0 for both SMs).
+__host__ __device__ constexpr int threads(bool swiglu, bool pair) {
+  return 32 * (kFirstEpiWarp + epi_warps(swiglu) + (pair ? 0 : kScaleWarps));
+}
 constexpr int kMaxE = 512;
 
 // One pipeline stage in shared memory.  One SM per tile (kPair false): the A block
@@ -84,6 +95,7 @@ struct Smem {
   uint8_t out[kOutBytes];
   uint64_t full[Layout<kPair>::kStages];
   uint64_t empty[Layout<kPair>::kStages];
+  uint64_t sfready[Layout<kPair>::kStages];   // one CTA per tile: the stage's scales are in TMEM
   uint64_t accf;
   uint64_t acce;
   uint64_t fin;               // the MMA issuer's last operations have completed
@@ -200,7 +212,7 @@ __device__ __forceinline__ TileJob tile_job_pair(const GemmArgs& g, const int32_
 // warp 2 tells CTA 0 when a stage of CTA 1 is full; CTA 0's commits free the stages and
 // fill the accumulators of both; both CTAs' epilogues release the accumulator to CTA 0.
 template <int kMode, bool kPair>
-__global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
+__global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
     grouped_gemm_tiled_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B,
                               const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
   using namespace gt;
@@ -237,6 +249,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
       // the A and the B producer arrive; in a pair CTA 0 also hears from CTA 1's warp 2
       mbar_init(&sm.full[s], kPair && rank == 0 ? 3 : 2);
       mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.sfready[s], kScaleWarps);
     }
     mbar_init(&sm.accf, 1);
     mbar_init(&sm.fin, 1);
@@ -320,28 +333,25 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
                                 : kblocks;
         for (int kb = 0; kb < kbt; ++kb) {
           if (!wait(&sm.full[stage], phase)) goto mma_done;
+          if (!kPair && !wait(&sm.sfready[stage], phase)) goto mma_done;
           tc_fence_after();
           const uint32_t sfa_t = tmem + kSFCol0 + stage * kSFStageCols;
           const uint32_t sfb_t = sfa_t + 16;
           const uint32_t st = smem_u32(sm.stage[stage]);
           const uint32_t sa = st + L::kA, sb = st + L::kB;
-          const uint32_t ssfa = st + L::kSFA, ssfb = st + L::kSFB;
+          if (kPair) {
+            const uint32_t ssfa = st + L::kSFA, ssfb = st + L::kSFB;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (kPair) {
+            for (int j = 0; j < 4; ++j) {
               tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
               tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
               tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
-            } else {
-              tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
-              tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
-              tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
             }
           }
           if (kb == 0) {
-            // The first stage's scale copies are issued before this wait: they do not touch
-            // the accumulator, so the tensor pipe runs them while the epilogue drains the
-            // previous tile (tcgen05 ops of one thread execute in issue order).
+            // (pair) the first stage's scale copies are issued before this wait: they do
+            // not touch the accumulator, so the tensor pipe runs them while the epilogue
+            // drains the previous tile (tcgen05 ops of one thread execute in issue order)
             if (!wait(&sm.acce, (it & 1) ^ 1u)) goto mma_done;
             tc_fence_after();
           }
@@ -395,6 +405,45 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
       }
     relay_done:;
     }
+  } else if (!kPair && warp >= kFirstEpiWarp + kEpiWarps) {
+    // scale warps: the stage's A scales (four 512-byte blocks, one per MMA) go to columns
+    // [0, 16) of the stage's scale slot, B's (two blocks per MMA: rows 0-127, then
+    // 128-255) to [16, 48), block j at 4j / 16 + 8j (+4), each as 32 lanes x 16 bytes in
+    // every lane quadrant.  A stage's slot is rewritten only after its full barrier has
+    // completed again, i.e. after the MMAs that read the previous contents (their commit
+    // freed the stage before it was refilled).
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    uint32_t stage = 0, phase = 0;
+    for (int t = first; t < total; t += stride) {
+      const int kbt = kRagged ? tile_job<true>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks).kblocks
+                              : kblocks;
+      for (int kb = 0; kb < kbt; ++kb) {
+        const bool ok = wait(&sm.full[stage], phase);
+        if (!__all_sync(0xFFFFFFFFu, ok)) goto sf_done;
+        const uint4* sfa = reinterpret_cast<const uint4*>(sm.stage[stage] + L::kSFA) + lane;
+        const uint4* sfb = reinterpret_cast<const uint4*>(sm.stage[stage] + L::kSFB) + lane;
+        uint32_t ra[16], rb[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 a = sfa[32 * j], b0 = sfb[32 * j], b1 = sfb[128 + 32 * j];
+          ra[4 * j] = a.x, ra[4 * j + 1] = a.y, ra[4 * j + 2] = a.z, ra[4 * j + 3] = a.w;
+          rb[8 * j] = b0.x, rb[8 * j + 1] = b0.y, rb[8 * j + 2] = b0.z, rb[8 * j + 3] = b0.w;
+          rb[8 * j + 4] = b1.x, rb[8 * j + 5] = b1.y, rb[8 * j + 6] = b1.z, rb[8 * j + 7] = b1.w;
+        }
+        const uint32_t taddr = tmem + lane_base + kSFCol0 + stage * kSFStageCols;
+        tmem_st_32x32b_x16(taddr, ra);
+        tmem_st_32x32b_x32(taddr + 16, rb);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sfready[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  sf_done:;
   } else {
     // epilogue: TMEM lane quadrant q = warp % 4 (the lanes this warp may read), column
     // half of the tile = (warp - 3) / 4
@@ -564,53 +613,66 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1), 1)
           }
           if (hmax != 0u) atomicMax(g.h_amax + row, hmax << 16);
         }
-      } else {
-        uint32_t v[4][32];
+      } else if (!g.out_f32) {
+        // BF16: each pair of 32-column chunks is packed as soon as it is loaded, so at most
+        // 64 accumulator values are live next to the 64 packed words
+        uint32_t w[2][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) NVFP4_TMEM_LD_X32(taddr + 32 * c, v[c]);
-        tmem_ld_wait();
-        release_acc();
-        if (skip) continue;
-        if (!g.out_f32) {
+        for (int b2 = 0; b2 < 2; ++b2) {
+          uint32_t v[2][32];
+          NVFP4_TMEM_LD_X32(taddr + 64 * b2, v[0]);
+          NVFP4_TMEM_LD_X32(taddr + 64 * b2 + 32, v[1]);
+          tmem_ld_wait();
 #pragma unroll
-          for (int b2 = 0; b2 < 2; ++b2) {
-            uint32_t w[32];
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-#pragma unroll
-              for (int p = 0; p < 16; ++p) {
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(
-                    __fmul_rn(__uint_as_float(v[2 * b2 + c][2 * p]), scale),
-                    __fmul_rn(__uint_as_float(v[2 * b2 + c][2 * p + 1]), scale));
-                w[16 * c + p] = *reinterpret_cast<const uint32_t*>(&pr);
-              }
-            }
-            const int32_t x = n_tile * kBN + half * 128 + 64 * b2;
-            if (full_warp) {
-              store_box(buf, w, lane, &tmd, x, y);
-            } else if (valid) {
-              uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + x) * 2;
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4*>(dp + 16 * j) =
-                    make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            for (int p = 0; p < 16; ++p) {
+              const __nv_bfloat162 pr = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][2 * p]), scale),
+                                                              __fmul_rn(__uint_as_float(v[c][2 * p + 1]), scale));
+              w[b2][16 * c + p] = *reinterpret_cast<const uint32_t*>(&pr);
             }
           }
-        } else {
+        }
+        release_acc();
+        if (skip) continue;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t w[32];
+        for (int b2 = 0; b2 < 2; ++b2) {
+          const int32_t x = n_tile * kBN + half * 128 + 64 * b2;
+          if (full_warp) {
+            store_box(buf, w[b2], lane, &tmd, x, y);
+          } else if (valid) {
+            uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + x) * 2;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__fmul_rn(__uint_as_float(v[c][i]), scale));
-            const int32_t x = n_tile * kBN + half * 128 + 32 * c;
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(dp + 16 * j) =
+                  make_uint4(w[b2][4 * j], w[b2][4 * j + 1], w[b2][4 * j + 2], w[b2][4 * j + 3]);
+          }
+        }
+      } else {
+        // float32: the half's first 64 columns are stored before the last 64 are loaded,
+        // so at most 64 accumulator values are live; the accumulator is released once the
+        // last load has completed
+#pragma unroll
+        for (int b2 = 0; b2 < 2; ++b2) {
+          uint32_t v[2][32];
+          NVFP4_TMEM_LD_X32(taddr + 64 * b2, v[0]);
+          NVFP4_TMEM_LD_X32(taddr + 64 * b2 + 32, v[1]);
+          tmem_ld_wait();
+          if (b2 == 1) release_acc();
+          if (skip) continue;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[c][i] = __float_as_uint(__fmul_rn(__uint_as_float(v[c][i]), scale));
+            const int32_t x = n_tile * kBN + half * 128 + 64 * b2 + 32 * c;
             if (full_warp) {
-              store_box(buf, w, lane, &tmd, x, y);
+              store_box(buf, v[c], lane, &tmd, x, y);
             } else if (valid) {
               uint8_t* dp = static_cast<uint8_t*>(g.d) + (row * g.ldd + x) * 4;
 #pragma unroll
               for (int j = 0; j < 8; ++j)
                 *reinterpret_cast<uint4*>(dp + 16 * j) =
-                    make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    make_uint4(v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2], v[c][4 * j + 3]);
             }
           }
         }
@@ -643,7 +705,7 @@ static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtens
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
   grouped_gemm_tiled_kernel<kMode, false>
-      <<<grid, gt::threads(kMode == 1), gt::smem_bytes<false>(), s>>>(A, B, tmd, g);
+      <<<grid, gt::threads(kMode == 1, false), gt::smem_bytes<false>(), s>>>(A, B, tmd, g);
   return cudaGetLastError();
 }
 
@@ -664,7 +726,7 @@ static cudaError_t launch_pair(const uint8_t* A, const uint8_t* B, const CUtenso
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(gt::threads(kMode == 1), 1, 1);
+  cfg.blockDim = dim3(gt::threads(kMode == 1, true), 1, 1);
   cfg.dynamicSmemBytes = gt::smem_bytes<true>();
   cfg.stream = s;
   cfg.attrs = attr;
