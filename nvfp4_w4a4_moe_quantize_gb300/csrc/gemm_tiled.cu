@@ -95,6 +95,7 @@ struct Smem {
   uint8_t out[kOutBytes];
   uint64_t full[Layout<kPair>::kStages];
   uint64_t empty[Layout<kPair>::kStages];
+  uint64_t sfull[Layout<kPair>::kStages];     // one CTA per tile: the stage's scale bytes have landed
   uint64_t sfready[Layout<kPair>::kStages];   // one CTA per tile: the stage's scales are in TMEM
   uint64_t accf;
   uint64_t acce;
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
       // the A and the B producer arrive; in a pair CTA 0 also hears from CTA 1's warp 2
       mbar_init(&sm.full[s], kPair && rank == 0 ? 3 : 2);
       mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.sfull[s], 2);
       mbar_init(&sm.sfready[s], kScaleWarps);
     }
     mbar_init(&sm.accf, 1);
@@ -297,7 +299,17 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
         for (int kb = 0; kb < job.kblocks; ++kb) {
           if (!wait(&sm.empty[stage], phase ^ 1u)) goto producer_done;
           uint8_t* st = sm.stage[stage];
-          if (is_a) {
+          if (!kPair) {
+            // the scale bytes first, on their own barrier: the scale warps move them into
+            // TMEM while the codes are still arriving
+            const uint8_t* src = is_a ? job.a + (int64_t)kb * kABlock : job.b + (int64_t)kb * kBBlock;
+            const uint32_t codes = is_a ? kACodes : kBCodes, scales = is_a ? kABlock - kACodes : kBScales;
+            uint8_t* dst = st + (is_a ? L::kA : L::kB);
+            mbar_arrive_expect_tx(&sm.sfull[stage], scales);
+            bulk_load(dst + codes, src + codes, scales, &sm.sfull[stage]);
+            mbar_arrive_expect_tx(&sm.full[stage], codes);
+            bulk_load(dst, src, codes, &sm.full[stage]);
+          } else if (is_a) {
             if (job.has_a) {
               mbar_arrive_expect_tx(&sm.full[stage], kABlock);
               bulk_load(st + L::kA, job.a + (int64_t)kb * kABlock, kABlock, &sm.full[stage]);
@@ -306,14 +318,9 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
             }
           } else {
             const uint8_t* src = job.b + (int64_t)kb * kBBlock;
-            if (kPair) {
-              mbar_arrive_expect_tx(&sm.full[stage], kBHalfCodes + kBScales);
-              bulk_load(st + L::kB, src + rank * kBHalfCodes, kBHalfCodes, &sm.full[stage]);
-              bulk_load(st + L::kSFB, src + kBCodes, kBScales, &sm.full[stage]);
-            } else {
-              mbar_arrive_expect_tx(&sm.full[stage], kBBlock);
-              bulk_load(st + L::kB, src, kBBlock, &sm.full[stage]);
-            }
+            mbar_arrive_expect_tx(&sm.full[stage], kBHalfCodes + kBScales);
+            bulk_load(st + L::kB, src + rank * kBHalfCodes, kBHalfCodes, &sm.full[stage]);
+            bulk_load(st + L::kSFB, src + kBCodes, kBScales, &sm.full[stage]);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -324,22 +331,33 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
     producer_done:;
     }
   } else if (warp == 2) {
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
+      // The whole warp runs the loop (its waits, descriptors and TMEM addresses are
+      // warp-uniform values); lane 0 issues the tcgen05 operations.  Measured: one lane
+      // alone running it spent about 300 cycles a stage on its scalar work, sharing the
+      // issue slots of its SM sub-partition with five busy warps.
       constexpr uint32_t idesc = idesc_nvf4(kPair ? 2 * kBM : kBM, kBN);
+      // operand descriptors of stage 0; stage s and K-step j add (s * stage bytes + 32 j) / 16
+      // to the start-address field (every address stays below 2^18, so no carry leaves it)
+      const uint32_t st0 = smem_u32(sm.stage[0]);
+      const uint64_t adesc0 = smem_desc(st0 + L::kA, 16, 1024, 2), bdesc0 = smem_desc(st0 + L::kB, 16, 1024, 2);
+      constexpr uint32_t kStageDesc = L::kStageBytes >> 4;
+      const bool leader = lane == 0;
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int t = first; t < total; t += stride, ++it) {
         const int kbt = kRagged ? tile_job<true>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks).kblocks
                                 : kblocks;
         for (int kb = 0; kb < kbt; ++kb) {
-          if (!wait(&sm.full[stage], phase)) goto mma_done;
-          if (!kPair && !wait(&sm.sfready[stage], phase)) goto mma_done;
+          bool ok = wait(&sm.full[stage], phase);
+          if (!kPair) ok = ok && wait(&sm.sfready[stage], phase);
+          if (!__all_sync(0xFFFFFFFFu, ok)) goto mma_done;
           tc_fence_after();
           const uint32_t sfa_t = tmem + kSFCol0 + stage * kSFStageCols;
           const uint32_t sfb_t = sfa_t + 16;
-          const uint32_t st = smem_u32(sm.stage[stage]);
-          const uint32_t sa = st + L::kA, sb = st + L::kB;
-          if (kPair) {
+          const uint64_t adesc = adesc0 + stage * kStageDesc, bdesc = bdesc0 + stage * kStageDesc;
+          if (kPair && leader) {
+            const uint32_t st = st0 + stage * (uint32_t)L::kStageBytes;
             const uint32_t ssfa = st + L::kSFA, ssfb = st + L::kSFB;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -352,43 +370,52 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
             // (pair) the first stage's scale copies are issued before this wait: they do
             // not touch the accumulator, so the tensor pipe runs them while the epilogue
             // drains the previous tile (tcgen05 ops of one thread execute in issue order)
-            if (!wait(&sm.acce, (it & 1) ^ 1u)) goto mma_done;
+            if (!__all_sync(0xFFFFFFFFu, wait(&sm.acce, (it & 1) ^ 1u))) goto mma_done;
             tc_fence_after();
           }
+          if (leader) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t adesc = smem_desc(sa + 32 * j, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(sb + 32 * j, 16, 1024, 2);
-            if (kPair)
-              tc_mma_nvf4_pair(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
-            else
-              tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+            for (int j = 0; j < 4; ++j) {
+              if (kPair)
+                tc_mma_nvf4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
+                                 (kb | j) != 0 ? 1u : 0u);
+              else
+                tc_mma_nvf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
+                            (kb | j) != 0 ? 1u : 0u);
+            }
+            if (kPair) {
+              tc_commit_pair(cluster_addr(&sm.empty[stage], 0));
+              tc_commit_pair(cluster_addr(&sm.empty[stage], 1));
+            } else {
+              tc_commit(&sm.empty[stage]);
+            }
           }
-          if (kPair) {
-            tc_commit_pair(cluster_addr(&sm.empty[stage], 0));
-            tc_commit_pair(cluster_addr(&sm.empty[stage], 1));
-          } else {
-            tc_commit(&sm.empty[stage]);
-          }
+          __syncwarp();
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (kPair) {
-          tc_commit_pair(cluster_addr(&sm.accf, 0));
-          tc_commit_pair(cluster_addr(&sm.accf, 1));
-        } else {
-          tc_commit(&sm.accf);
+        if (leader) {
+          if (kPair) {
+            tc_commit_pair(cluster_addr(&sm.accf, 0));
+            tc_commit_pair(cluster_addr(&sm.accf, 1));
+          } else {
+            tc_commit(&sm.accf);
+          }
         }
+        __syncwarp();
       }
     mma_done:
-      // whatever the exit, no MMA or scale copy of this thread is still running when
+      // whatever the exit, no MMA or scale copy of the issuing lane is still running when
       // the TMEM is freed (a bounded wait of its own, also after an abort)
-      if (kPair) tc_commit_pair(cluster_addr(&sm.fin, 0));
-      else tc_commit(&sm.fin);
-      volatile int no_abort = 0;
-      mbar_wait(&sm.fin, 0, g.status, &no_abort, 1000000000ull);
+      if (leader) {
+        if (kPair) tc_commit_pair(cluster_addr(&sm.fin, 0));
+        else tc_commit(&sm.fin);
+        volatile int no_abort = 0;
+        mbar_wait(&sm.fin, 0, g.status, &no_abort, 1000000000ull);
+      }
+      __syncwarp();
     } else if (kPair && lane == 0) {
       // CTA 1: each of this CTA's full stages counts as one arrival on CTA 0's barrier
       uint32_t stage = 0, phase = 0;
@@ -409,7 +436,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
     // scale warps: the stage's A scales (four 512-byte blocks, one per MMA) go to columns
     // [0, 16) of the stage's scale slot, B's (two blocks per MMA: rows 0-127, then
     // 128-255) to [16, 48), block j at 4j / 16 + 8j (+4), each as 32 lanes x 16 bytes in
-    // every lane quadrant.  A stage's slot is rewritten only after its full barrier has
+    // every lane quadrant.  A stage's slot is rewritten only after its scale barrier has
     // completed again, i.e. after the MMAs that read the previous contents (their commit
     // freed the stage before it was refilled).
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -418,7 +445,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
       const int kbt = kRagged ? tile_job<true>(g, sm.offsets, sm.rows, A, B, t, n_tiles, m_tiles, kblocks).kblocks
                               : kblocks;
       for (int kb = 0; kb < kbt; ++kb) {
-        const bool ok = wait(&sm.full[stage], phase);
+        const bool ok = wait(&sm.sfull[stage], phase);
         if (!__all_sync(0xFFFFFFFFu, ok)) goto sf_done;
         const uint4* sfa = reinterpret_cast<const uint4*>(sm.stage[stage] + L::kSFA) + lane;
         const uint4* sfb = reinterpret_cast<const uint4*>(sm.stage[stage] + L::kSFB) + lane;
