@@ -15,6 +15,10 @@
  *   - Errors found on the device (an expert id out of range, a device-side wait that
  *     ran out of time) are recorded in a per-device status word; nvfp4_status_check()
  *     synchronises the stream, returns and clears it.  No kernel traps.
+ *   - The library resolves a few per-device addresses once (the status word, the silu
+ *     table, the scratch of nvfp4_quantize_noalloc) and keeps them for the life of the
+ *     device's primary context: after cudaDeviceReset the process must not call the
+ *     library on that device again.
  *   - Inputs are finite; NaN or Inf inputs give unspecified (but memory-safe) results.
  *   - Results are deterministic, and a token's output bits do not depend on the other
  *     tokens of the batch (per-token activation scales, a fixed accumulation order,
@@ -171,7 +175,8 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
  *   global_scale_in return NVFP4_ERR_UNSUPPORTED).  Every GPU that loads the library
  *   holds that array until the process exits.
  *   The first call on each device resolves the array's device address (with that
- *   device current); make that first call before any stream capture.
+ *   device current) and keeps it while the device's primary context lives (see the
+ *   preamble on cudaDeviceReset); make that first call before any stream capture.
  *   All calls share the one array and each call clears the words it uses before use:
  *   calls whose kernels overlap on the GPU (different streams, no ordering) race on it.
  *   The library calls no allocator (no cudaMalloc / cudaFree) here. */
