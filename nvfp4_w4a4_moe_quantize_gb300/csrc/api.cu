@@ -934,13 +934,17 @@ nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w
   // 5. weight gradients: per-expert transposed quantisation along the tokens, then the
   //    ragged-K grouped GEMM (float32 out)
   if (fail(launch_kofs(counts, 0, E, kofs, s))) return NVFP4_ERR_CUDA;
-  auto wgrad = [&](const void* gsrc, int64_t Fa, const void* asrc, int64_t ld_a, const int32_t* rowmap, int64_t Fb,
-                   int64_t Fbp, int stream_id, int slot, uint8_t* Aw, uint8_t* Bw, float* out) {
+  // the per-expert maxima of the wgrad operands: dy's from the combine backward; dD's, h's
+  // and x's from the per-row global scales their row quantisations left (g_dD, the
+  // forward's gH and the per-slot token scales gA), without another pass over the rows
+  auto wgrad = [&](const void* gsrc, int64_t Fa, const float* g_gsrc, const void* asrc, int64_t ld_a,
+                   const float* g_asrc, const int32_t* rowmap, int64_t Fb, int64_t Fbp, int stream_id, int slot,
+                   uint8_t* Aw, uint8_t* Bw, float* out) {
     uint32_t* am = amax + 2 * slot * E;
     float* gg = gexp + 2 * slot * E;
-    // dy's per-expert max comes from the combine backward (slot 0)
-    if ((slot != 0 && fail(launch_group_amax(gsrc, Fa, Fa, nullptr, padded, counts, E, mcap, am, s))) ||
-        fail(launch_group_amax(asrc, ld_a, Fb, rowmap, padded, counts, E, mcap, am + E, s)) ||
+    if ((g_gsrc != nullptr &&
+         fail(launch_group_amax_g(g_gsrc, gsrc, Fa, Fa, nullptr, padded, counts, E, mcap, am, s))) ||
+        fail(launch_group_amax_g(g_asrc, asrc, ld_a, Fb, rowmap, padded, counts, E, mcap, am + E, s)) ||
         fail(launch_tquant(gsrc, Fa, nullptr, padded, counts, 0, kofs, E, (int)Fa, (int)Fa, 128, am, gg, Aw, kRoundSR,
                            seed, stream_id, kb_cap, s)) ||
         fail(launch_tquant(asrc, ld_a, rowmap, padded, counts, 0, kofs, E, (int)Fb, (int)Fbp, 256, am + E, gg + E, Bw,
@@ -964,8 +968,9 @@ nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w
       return cudaErrorInvalidValue;
     return launch_grouped_gemm_ragged_k(Aw, Bw, md, g, s);
   };
-  if (fail(wgrad(dy, H, hbuf, I, nullptr, I, Ip, 1, 0, at(12), at(13), dw2)) ||
-      fail(wgrad(dD, 2 * I, x, H, perm, H, H, 3, 1, at(14), at(15), dw13)))
+  const float* gh = reinterpret_cast<const float*>(fb + F.off[11]);
+  if (fail(wgrad(dy, H, nullptr, hbuf, I, gh, nullptr, I, Ip, 1, 0, at(12), at(13), dw2)) ||
+      fail(wgrad(dD, 2 * I, g_dD, x, H, ga, perm, H, H, 3, 1, at(14), at(15), dw13)))
     return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }

@@ -4,6 +4,8 @@
 // of the gradients):
 //   combine_backward_kernel   dy[slot(t,j)] = BF16(w[t,j] dout[t]) and dw[t,j] = <dout[t], y[slot]>
 //   group_amax_kernel         max |x| over each expert's rows of a slot-ordered matrix
+//   group_amax_g_kernel       the same maximum from the rows' own global scales, where the
+//                             rows were already quantised per row
 //   kofs_kernel               per-expert token counts -> 256-token K-block prefix sums
 //   tquant_kernel             per-expert transposed NVFP4 (blocks of 16 tokens, one global
 //                             scale per expert matrix) straight into the GEMM-tiled layout:
@@ -158,6 +160,63 @@ cudaError_t launch_group_amax(const void* src, int64_t ld, int64_t F, const int3
   if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
   group_amax_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), ld, F, rowmap, starts, counts,
                                                 E, max_rows, amax_bits);
+  return cudaGetLastError();
+}
+
+// amax_bits[e] = max |src[row(r), 0..F)| over the rows r of expert e's group, as
+// group_amax_kernel, for rows that already carry a per-row global scale g_rows[r] =
+// fl32(amax_r / 2688) (the forward's per-token and per-row scales, the backward's dD rows):
+// amax_r is a BF16 value, and where g_rows[r] is a normal float32 (>= 2^-125), g * 2688 is
+// within 2^-23 (relative) of it, so rounding that product to BF16 gives amax_r exactly;
+// smaller non-zero scales (rows whose max is below about 2^-113) read the row.  One thread
+// per row, the warp's rows combined per expert before one atomicMax each.  amax_bits must
+// be zeroed first.
+__global__ void __launch_bounds__(256) group_amax_g_kernel(const float* __restrict__ g_rows,
+                                                           const __nv_bfloat16* __restrict__ src, int64_t ld,
+                                                           int64_t F, const int32_t* __restrict__ rowmap,
+                                                           const int32_t* __restrict__ starts,
+                                                           const int32_t* __restrict__ counts, int E,
+                                                           int64_t max_rows, uint32_t* __restrict__ amax_bits) {
+  int64_t rows = starts[E];
+  if (rows > max_rows) rows = max_rows;
+  const int lane = threadIdx.x & 31;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < rows; base += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = base + threadIdx.x;   // the loop is uniform over the block (votes below)
+    int e = -1;
+    uint32_t v = 0;
+    if (r < rows) {
+      e = find_group(starts, E, (int32_t)r);
+      if (r - starts[e] < counts[e]) {
+        const float g = g_rows[r];
+        if (g >= 0x1p-125f) {
+          const uint32_t b = __float_as_uint(__fmul_rn(g, 2688.0f));
+          v = ((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16) << 16;
+        } else if (g > 0.0f) {
+          const int64_t sr = rowmap != nullptr ? rowmap[r] : r;
+          const uint16_t* q = reinterpret_cast<const uint16_t*>(src + sr * ld);
+          uint32_t m = 0;
+          for (int64_t c = 0; c < F; ++c) m = max(m, (uint32_t)(q[c] & 0x7FFFu));
+          v = m << 16;
+        }
+      } else {
+        e = -1;   // group padding
+      }
+    }
+    const unsigned same = __match_any_sync(kAll, e);
+    const uint32_t m = __reduce_max_sync(same, v);
+    if (e >= 0 && m != 0u && lane == __ffs((int)same) - 1) atomicMax(amax_bits + e, m);
+  }
+}
+
+cudaError_t launch_group_amax_g(const float* g_rows, const void* src, int64_t ld, int64_t F, const int32_t* rowmap,
+                                const int32_t* starts, const int32_t* counts, int E, int64_t max_rows,
+                                uint32_t* amax_bits, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t) * E, s);
+  if (err != cudaSuccess || max_rows == 0) return err;
+  int64_t blocks = (max_rows + 255) / 256;
+  if (blocks > 2 * (int64_t)num_sms()) blocks = 2 * (int64_t)num_sms();
+  group_amax_g_kernel<<<(int)blocks, 256, 0, s>>>(g_rows, static_cast<const __nv_bfloat16*>(src), ld, F, rowmap,
+                                                  starts, counts, E, max_rows, amax_bits);
   return cudaGetLastError();
 }
 

@@ -133,6 +133,11 @@ cudaError_t launch_combine_backward(const void* dout, const int32_t* inv, const 
                                     uint32_t* amax_bits, cudaStream_t s);
 cudaError_t launch_group_amax(const void* src, int64_t ld, int64_t F, const int32_t* rowmap, const int32_t* starts,
                               const int32_t* counts, int E, int64_t max_rows, uint32_t* amax_bits, cudaStream_t s);
+// The same maximum from per-row global scales g_rows = fl32(row max / 2688) (rows with a
+// tiny non-zero scale are read).
+cudaError_t launch_group_amax_g(const float* g_rows, const void* src, int64_t ld, int64_t F, const int32_t* rowmap,
+                                const int32_t* starts, const int32_t* counts, int E, int64_t max_rows,
+                                uint32_t* amax_bits, cudaStream_t s);
 cudaError_t launch_kofs(const int32_t* counts, int64_t uniform, int E, int32_t* kofs, cudaStream_t s);
 cudaError_t launch_tquant(const void* src, int64_t ld, const int32_t* rowmap, const int32_t* starts,
                           const int32_t* counts, int64_t uniform, const int32_t* kofs, int E, int F, int Fp, int R,

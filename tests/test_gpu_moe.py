@@ -139,9 +139,12 @@ def _swiglu_hard_pairs(n_random=8_000_000, seed=11):
     prod = (G2.astype(np.float32) * U2.astype(np.float32)).view(np.uint32)
     mid = (prod & 0xFFFF) == 0x8000
     gb, ub = G2[mid], U2[mid]
-    gc = bf(np.array([79.5, 80, 80.5, 81, -79.5, -80, -80.5, -81, -87, -88.5, -100, -200, 1e-20, -1e-20, 1e-3, 3e4]))
+    # large |gate|, and gates at or below the float32 normal range with large up (silu(gate)
+    # itself subnormal)
+    gc = bf(np.array([79.5, 80, 80.5, 81, -79.5, -80, -80.5, -81, -87, -88.5, -100, -200, 1e-20, -1e-20, 1e-3, 3e4,
+                      16.5, -17, 24, -30, 1e-39, -3e-40, 2e-41, 1.2e-38, -5e-39, 3e-30]))
     uc = bf(np.array([1.5, -3, 1e30, 2e-30, 1e38, -1e37, 1e35, 7e38, 1e-30, 1e25, 5e-39, 1.0, 1e20, 1e-10, 3e33,
-                      -2e-35]))
+                      -2e-35, 3.0, -1e10, 7.0, 2e20, 1e30, -3e35, 1e38, 2e25, 7e33, 1e30]))
     return np.concatenate([ga, gb, gc]), np.concatenate([ua, ub, uc]), (ga.size, gb.size)
 
 
