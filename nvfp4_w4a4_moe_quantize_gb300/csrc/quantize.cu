@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(256) quantize_known_coalesced_kernel(QuantArgs
 }
 
 template <int RND>
-__global__ void __launch_bounds__(kQWarps * 32, RND == kRoundSR ? 2 : 3) quantize_rows_stream_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kQWarps * 32, 3) quantize_rows_stream_kernel(QuantArgs a) {
   extern __shared__ __align__(128) uint8_t qsm[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t warp = (int64_t)blockIdx.x * kQWarps + wib;
@@ -539,16 +539,21 @@ __global__ void __launch_bounds__(kQWarps * 32, RND == kRoundSR ? 2 : 3) quantiz
     const float six_g = __fmul_rn(6.0f, g);
     const int64_t orow = a.map == kMapInterleave ? interleave_row(row, a.map_I) : row;
     const RowOut ro = row_out(a, orow);
-#pragma unroll
+    // stochastic rounding: one block at a time (the block max read again from shared
+    // memory), so that three CTAs of its registers fit on an SM
+    constexpr int kUnroll = RND == kRoundSR ? 1 : kQMaxSlots;
+#pragma unroll kUnroll
     for (int i = 0; i < kQMaxSlots; ++i) {
       if (32 * i >= nblk) break;                       // warp-uniform
       const uint32_t blk = (uint32_t)lane + 32u * i;
       const bool active = blk < nblk;
       uint32_t sfb = 0;
       uint2 cw = make_uint2(0u, 0u);
-      if (active)
-        encode_regs<RND>(a, row, blk, *reinterpret_cast<const uint4*>(buf + blk * 32),
-                         *reinterpret_cast<const uint4*>(buf + blk * 32 + 16), g, six_g, sfb, cw, bmax[i]);
+      if (active) {
+        const uint4 q0 = *reinterpret_cast<const uint4*>(buf + blk * 32);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(buf + blk * 32 + 16);
+        encode_regs<RND>(a, row, blk, q0, q1, g, six_g, sfb, cw, RND == kRoundSR ? absmax16_bf16(q0, q1) : bmax[i]);
+      }
       const uint32_t s1 = __shfl_down_sync(kFull, sfb, 1);
       const uint32_t s2 = __shfl_down_sync(kFull, sfb, 2);
       const uint32_t s3 = __shfl_down_sync(kFull, sfb, 3);
