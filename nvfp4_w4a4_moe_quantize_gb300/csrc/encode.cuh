@@ -285,11 +285,13 @@ __device__ __forceinline__ uint32_t e2m1_exact_sr(float x, float s, uint32_t r16
 // count is the exact quotient's unless X4 - 4 T_j is -1 or 0 for some j; those values --
 // about one in 10^5 -- take the exact count of thresholds below q (e2m1_exact_sr).  The
 // count from X4 is (X4 + 2^18 - 1 - 4 r16) / 2^18, saturated at 7.
+// Codes and signs are placed with integer multiply-adds (code * 16^e + out), which can
+// run on the FMA pipe next to the ALU work.
 __device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockScale& bs, uint4 rnd) {
   const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
   if (!(bs.s > 0.0f)) return 0u;
   if (!bs.exact_only) {
-    uint32_t out = 0, signs = 0, near = 0xFFFFFFFFu;
+    uint32_t out = 0, near = 0xFFFFFFFFu;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float v = __fmul_rn(fabsf(f[e]), bs.r);
@@ -300,10 +302,10 @@ __device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockSc
       const uint32_t r16 = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
       const uint32_t a = x4 - 4u * r16 + (0x3FFFFu - 0x3F00000u);      // X4 + 2^18 - 1 - 4 r16
       near = min(near, ~a & 0x3FFFEu);                                  // 0: X4 - 4 T_j in {-1, 0}
-      out |= min(a >> 18, 7u) << (4 * e);
-      signs |= (__float_as_uint(f[e]) >> 31) << (4 * e + 3);
+      out += min(a >> 18, 7u) * (1u << (4 * e));
+      out += (__float_as_uint(f[e]) >> 31) * (8u << (4 * e));
     }
-    out = canonical_zero(out | signs);
+    out = canonical_zero(out);
     if (near == 0u) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
