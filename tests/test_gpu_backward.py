@@ -202,3 +202,139 @@ def test_backward_is_deterministic_and_seeded(cuda_lib):
     for key in ("dx", "dw", "dw13", "dw2"):
         assert torch.equal(a[key], b[key]), key
     assert not torch.equal(a["dw13"], c["dw13"])      # another Philox key draws other roundings
+
+
+def _tiled_block(buf, block, K, R=128):
+    """Codes and row-major scales of one R-row block of a GEMM-tiled buffer (device)."""
+    nbytes = (K // 256) * R * 144
+    return untile_host(npy(buf[block * nbytes:(block + 1) * nbytes]), R, K, R)
+
+
+def test_backward_learner_size_sampled(cuda_lib):
+    """The learner-step workload at full size (T=32768, H=2048, I=768, 128 experts, top-8,
+    uniform routing, dout N(0, 1e-3)), through the calls and sizes the bench times.  Two
+    experts are checked stage by stage on a 128-row block of their groups (dy, the
+    SR-quantised dy and dD rows and their scales bit exact; dh, dD and dxs within the GEMM
+    and SwiGLU tolerances; the recomputed D gives the forward's h bit for bit), dx on the
+    tokens of those rows, and each of the two experts' weight gradients whole: the
+    transposed operands bit exact and dW within the GEMM tolerance."""
+    lib = cuda_lib
+    shape = S.WORKLOADS["learner"]
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    Ip = (I + 255) // 256 * 256
+    x, logits, w13, w2 = S.moe_inputs(shape, seed=0)
+    dout = S.randn_bf16((T, H), 1e-3, 9)
+    seed = 7
+    xc = x.cuda()
+    ids, w = lib.moe_route_topk(logits.cuda(), k)
+    pw = lib.moe_prepare_weights(w13.cuda(), w2.cuda())
+    pt = lib.moe_prepare_weights_backward(w13.cuda(), w2.cuda())
+    fws = lib.moe_forward_workspace(T, k, pw, "cuda")
+    lib.moe_expert_forward(xc, ids, w, pw, workspace=fws)
+    bws = lib.moe_backward_workspace(T, k, pw, "cuda")
+    dx, _, dw13, dw2 = lib.moe_expert_backward(dout.cuda(), xc, w, pw, pt, fws, seed=seed, workspace=bws)
+    assert lib.nvfp4_status_check() == 0
+
+    flay = lib.moe_forward_workspace_layout(T, k, E, H, I)
+    blay = lib.moe_backward_workspace_layout(T, k, E, H, I)
+    mcap = flay[13]
+    counts = npy(_views(fws, flay, 0, E, torch.int32))
+    padded = npy(_views(fws, flay, 2, E + 1, torch.int32))
+    inv = npy(_views(fws, flay, 3, T * k, torch.int32)).reshape(T, k)
+    perm_d = _views(fws, flay, 4, mcap, torch.int32)
+    h_d = _views(fws, flay, 8, mcap * I, torch.bfloat16).view(mcap, I)
+    dy_d = _views(bws, blay, 0, mcap * H, torch.bfloat16).view(mcap, H)
+    dh_d = _views(bws, blay, 3, mcap * Ip, torch.bfloat16).view(mcap, Ip)
+    d_d = _views(bws, blay, 4, mcap * 2 * I, torch.bfloat16).view(mcap, 2 * I)
+    dD_d = _views(bws, blay, 5, mcap * 2 * I, torch.bfloat16).view(mcap, 2 * I)
+    dxs_d = _views(bws, blay, 8, mcap * H, torch.bfloat16).view(mcap, H)
+    g_dy = _views(bws, blay, 2, mcap, torch.float32)
+    g_dD = _views(bws, blay, 7, mcap, torch.float32)
+    kofs = npy(_views(bws, blay, 9, E + 1, torch.int32))
+    gexp = npy(_views(bws, blay, 11, 4 * E, torch.float32))
+    w_np, dout_b, xb = npy(w), S.bf16_bits(dout), S.bf16_bits(x)
+    w13b, w2b = S.bf16_bits(w13), S.bf16_bits(w2)
+    kb_cap = blay[16]
+
+    for e in (0, 77):
+        assert counts[e] >= 128
+        r0 = int(padded[e])
+        rows = slice(r0, r0 + 128)
+        tok = npy(perm_d[rows]).astype(np.int64)
+        jj = np.array([int(np.nonzero(inv[t] == r0 + i)[0][0]) for i, t in enumerate(tok)])
+        # dy = BF16(w dout), bit exact
+        dy_b = u16(dy_d[rows])
+        dyv = F.bf16_to_f32(dout_b[tok]).astype(np.float64) * w_np[tok, jj].astype(np.float64)[:, None]
+        np.testing.assert_array_equal(dy_b, F.bf16_round(dyv))
+        # the SR-quantised dy rows (row-major element index over the slot layout)
+        q_dy = Q.quantize(dy_b, scope="row", rounding="sr", seed=B.sr_key(seed, B.STREAM_DGRAD_DOWN),
+                          rng_offset=r0 * H // 8)
+        c, sf = _tiled_block(bws[blay[1]:blay[2]], r0 // 128, H)
+        np.testing.assert_array_equal(c, q_dy["codes"])
+        np.testing.assert_array_equal(sf, q_dy["sf"])
+        np.testing.assert_array_equal(npy(g_dy[rows]), q_dy["g"])
+        # dh = Q(dy) Q(W2_e^T)
+        w2q_t = B.quantize_weights_transposed(w2b[e:e + 1])
+        one = (np.array([0, 128]), np.array([128]))
+        dh_ref = M.grouped_gemm(q_dy["codes"], q_dy["sf"], q_dy["g"], w2q_t["codes"], w2q_t["sf"], w2q_t["g"], *one)
+        dh_b = u16(dh_d[rows])
+        nbad, worst = check_bf16_against(dh_b[:, :I], dh_ref)
+        assert nbad == 0, (e, "dh", worst)
+        # D recomputed gives the forward's h; the SwiGLU backward
+        d_b = u16(d_d[rows])
+        d_can = np.empty_like(d_b)
+        d_can[:, _src_interleave(I)] = d_b
+        np.testing.assert_array_equal(M.swiglu(d_can, I), u16(h_d[rows]))
+        dD_b = u16(dD_d[rows])
+        dD_ref = M.swiglu_backward(d_can, dh_b[:, :I], I)
+        for part in (slice(0, I), slice(I, 2 * I)):
+            nbad, worst = check_bf16_against(dD_b[:, part], F.bf16_to_f32(dD_ref[:, part]).astype(np.float64))
+            assert nbad == 0, (e, "dD", worst)
+        # the SR-quantised dD rows, then dxs = Q(dD) Q(W13_e^T)
+        q_dD = Q.quantize(dD_b, scope="row", rounding="sr", seed=B.sr_key(seed, B.STREAM_DGRAD_GATEUP),
+                          rng_offset=r0 * 2 * I // 8)
+        c, sf = _tiled_block(bws[blay[6]:blay[7]], r0 // 128, 2 * I)
+        np.testing.assert_array_equal(c, q_dD["codes"])
+        np.testing.assert_array_equal(sf, q_dD["sf"])
+        np.testing.assert_array_equal(npy(g_dD[rows]), q_dD["g"])
+        w13q_t = B.quantize_weights_transposed(w13b[e:e + 1])
+        dxs_ref = M.grouped_gemm(q_dD["codes"], q_dD["sf"], q_dD["g"], w13q_t["codes"], w13q_t["sf"], w13q_t["g"],
+                                 *one)
+        nbad, worst = check_bf16_against(u16(dxs_d[rows]), dxs_ref)
+        assert nbad == 0, (e, "dxs", worst)
+        # dx of these rows' tokens: the sum of their k slots' dxs
+        ts = tok[:32]
+        slots = inv[ts]
+        dxs_rows = u16(dxs_d[torch.from_numpy(slots.reshape(-1)).long().cuda()]).reshape(len(ts) * k, H)
+        assert combine_violations(u16(dx[torch.from_numpy(ts).cuda()]), dxs_rows,
+                                  np.arange(len(ts) * k).reshape(len(ts), k), np.ones((len(ts), k), np.float32)) == 0
+
+        # weight gradients of expert e, whole: transposed operands and dW
+        n = int(counts[e])
+        gr = slice(r0, r0 + n)
+        tp = 256 * int(kofs[e + 1] - kofs[e])
+        for (gsrc, asrc, Fa, Fb, Fbp, stream, slot, ia, ib, got) in (
+                (u16(dy_d[gr]), u16(h_d[gr]), H, I, Ip, B.STREAM_WGRAD_DOWN, 0, 12, 13, dw2),
+                (u16(dD_d[gr]), xb[npy(perm_d[gr]).astype(np.int64)], 2 * I, H, H, B.STREAM_WGRAD_GATEUP, 1, 14, 15,
+                 dw13)):
+            gt = np.zeros((Fa, tp), np.uint16)
+            at = np.zeros((Fb, tp), np.uint16)
+            gt[:, :n] = gsrc.T
+            at[:, :n] = asrc.T
+            qa = Q.quantize(gt, scope="tensor", rounding="sr", seed=B.sr_key(seed, stream, e))
+            qb = Q.quantize(at, scope="tensor")
+            abuf = bws[blay[ia]:blay[ia] + (Fa // 128) * kb_cap * 128 * 144]
+            bbuf = bws[blay[ib]:blay[ib] + (Fbp // 256) * kb_cap * 256 * 144]
+            a0 = (Fa // 128) * int(kofs[e]) * 128 * 144
+            ac, asf = untile_host(npy(abuf[a0:a0 + (Fa // 128) * (tp // 256) * 128 * 144]), Fa, tp, 128)
+            np.testing.assert_array_equal(ac, qa["codes"], err_msg=f"A codes, expert {e}")
+            np.testing.assert_array_equal(asf, qa["sf"], err_msg=f"A scales, expert {e}")
+            b0 = (Fbp // 256) * int(kofs[e]) * 256 * 144
+            bc, bsf = untile_host(npy(bbuf[b0:b0 + (Fbp // 256) * (tp // 256) * 256 * 144]), Fbp, tp, 256)
+            np.testing.assert_array_equal(bc[:Fb], qb["codes"], err_msg=f"B codes, expert {e}")
+            np.testing.assert_array_equal(bsf[:Fb], qb["sf"], err_msg=f"B scales, expert {e}")
+            assert gexp[2 * slot * E + e] == qa["g"][0] and gexp[2 * slot * E + E + e] == qb["g"][0]
+            ref = (Q.dq_unscaled(qa["codes"], qa["sf"]) * np.float64(qa["g"][0])) @ \
+                  (Q.dq_unscaled(qb["codes"], qb["sf"]) * np.float64(qb["g"][0])).T
+            mx, nw = rel_err_floor(npy(got[e]).reshape(-1), ref.reshape(-1))
+            assert mx <= 1e-3, (e, stream, mx, nw)
