@@ -868,8 +868,11 @@ nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w
   int* status = device_status_ptr();
   auto fail = [](cudaError_t e) { return e != cudaSuccess; };
 
-  // 1. weighted un-permute backward: dy per slot, dw per (token, j)
-  if (fail(launch_combine_backward(dout, inv, w, ybuf, T, k, H, dy, dw, padded, E, amax, s))) return NVFP4_ERR_CUDA;
+  auto key = [&](int stream_id) { return seed + ((uint64_t)stream_id << 50); };   // expert 0's key of the stream
+  // 1. weighted un-permute backward: dy per slot, dw per (token, j), and dy's rows
+  //    quantised (per row, stochastic rounding) into the dgrad's A operand
+  if (fail(launch_combine_backward(dout, inv, w, ybuf, T, k, H, dy, dw, padded, E, amax, dyq, g_dy, key(0), s)))
+    return NVFP4_ERR_CUDA;
 
   // row quantisation of a slot-ordered gradient (per row, stochastic rounding) into the
   // GEMM-tiled A operand; padding slots are skipped
@@ -894,7 +897,6 @@ nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w
     a.rows_dev = padded + E;
     return launch_quantize_rows(a, kRoundSR, s);
   };
-  auto key = [&](int stream_id) { return seed + ((uint64_t)stream_id << 50); };   // expert 0's key of the stream
   // grouped GEMM over GEMM-tiled operands with a plain BF16 store into [mcap, N] (pitch ld)
   auto dgrad = [&](const uint8_t* A, const float* gA, const uint8_t* B, const float* gB, int64_t N, int64_t K,
                    void* out, int64_t ld_cols, int64_t store_cols) {
@@ -917,8 +919,7 @@ nvfp4_status moe_expert_backward(const void* dout, const void* x, const float* w
   };
 
   // 2. dgrad of the down projection: dh = Q(dy) Q(W2^T), dh [mcap, Ip]
-  if (fail(quant_rows(dy, H, dyq, g_dy, key(0))) ||
-      fail(dgrad(dyq, g_dy, wtt->w2t, wtt->w2t_g, Ip, H, dh, Ip, Ip)))
+  if (fail(dgrad(dyq, g_dy, wtt->w2t, wtt->w2t_g, Ip, H, dh, Ip, Ip)))
     return NVFP4_ERR_CUDA;
   // 3. the gate/up output D again (the fused forward keeps only h), then the SwiGLU backward
   //    into the canonical [dgate | dup]

@@ -53,52 +53,108 @@ __device__ __forceinline__ uint32_t bf16_of_product(float w, float d) {
 
 // One warp per token: for each of its k slots, dy = BF16(w dout) and dw = sum_h dout y in
 // float32 (each lane sums its columns in order with one rounding per term, then a
-// fixed-shape butterfly over the lanes: the same order on every run).
+// fixed-shape butterfly over the lanes: the same order on every run); and dy's row of the
+// slot layout quantised at once -- per-row scale, stochastic rounding with Philox key
+// `key`, element index slot * H + column -- into the GEMM-tiled dyq (128-row blocks) with
+// its global scale g_dy[slot], exactly as the row quantiser would from dy.  Lane l owns
+// the 16-value blocks b = l + 32 i of the row, so each lane encodes whole blocks.  The
+// row max needs no pass over dy: BF16 rounding is monotone, so max_h |BF16(w dout_h)| =
+// BF16(|w| max_h |dout_h|), from the token's max |dout| taken once.
 // Also (amax_bits != nullptr) the max |dy| of each expert's rows, for the transposed
 // quantisation of dy: the slot's expert is the group holding it (starts [E+1]).
-__global__ void __launch_bounds__(256) combine_backward_kernel(const __nv_bfloat16* __restrict__ dout,
-                                                               const int32_t* __restrict__ inv,
-                                                               const float* __restrict__ w,
-                                                               const __nv_bfloat16* __restrict__ y, int64_t T, int k,
-                                                               int64_t H, __nv_bfloat16* __restrict__ dy,
-                                                               float* __restrict__ dw,
-                                                               const int32_t* __restrict__ starts, int E,
-                                                               uint32_t* __restrict__ amax_bits) {
+__global__ void __launch_bounds__(256, 3) combine_backward_kernel(const __nv_bfloat16* __restrict__ dout,
+                                                                  const int32_t* __restrict__ inv,
+                                                                  const float* __restrict__ w,
+                                                                  const __nv_bfloat16* __restrict__ y, int64_t T,
+                                                                  int k, int64_t H, __nv_bfloat16* __restrict__ dy,
+                                                                  float* __restrict__ dw,
+                                                                  const int32_t* __restrict__ starts, int E,
+                                                                  uint32_t* __restrict__ amax_bits, uint8_t* dyq,
+                                                                  float* __restrict__ g_dy, uint64_t key) {
+  constexpr int kMaxSlots = 4;                  // 16-value blocks per lane: H <= 2048
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t nwarp = (int64_t)gridDim.x * 8;
+  const int nb = (int)(H / 16);
+  const int64_t kblocks = H / 256;
+  const uint32_t k0 = (uint32_t)key, k1 = (uint32_t)(key >> 32);
   for (int64_t t = warp; t < T; t += nwarp) {
+    // the token's max |dout| (its row is read again per slot, from L1)
+    uint32_t dm = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxSlots; ++i) {
+      const int b = lane + 32 * i;
+      if (b < nb)
+        dm = max(dm, __float_as_uint(absmax16_bf16(ldg_nc(dout + t * H + 16 * b), ldg_nc(dout + t * H + 16 * b + 8))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dm = max(dm, __shfl_xor_sync(kAll, dm, o));
     for (int j = 0; j < k; ++j) {
       const int32_t slot = inv[t * k + j];
+      if (slot < 0) continue;                   // warp-uniform
       const float wj = w[t * k + j];
+      // the row's max |dy| (float bits of a BF16 value) and its global scale
+      const uint32_t mb = bf16_of_product(fabsf(wj), __uint_as_float(dm)) << 16;
+      const float g = __fdiv_rn(__uint_as_float(mb), kGlobalDivisor);
+      const float six_g = __fmul_rn(6.0f, g);
+      const int64_t rr = slot & 127;
+      uint8_t* rcodes = dyq + (slot >> 7) * kblocks * tiled_block_bytes(128) + rr * 128;
+      uint8_t* rsf = dyq + (slot >> 7) * kblocks * tiled_block_bytes(128) + 128 * 128 + (rr & 31) * 16 + (rr >> 5) * 4;
       float acc = 0.0f;
-      uint32_t m = 0;
-      if (slot >= 0) {
-        for (int64_t c = 8 * lane; c < H; c += 256) {
-          const uint4 dq = ldg_nc(dout + t * H + c);
-          const uint4 yq = ldg_nc(y + (int64_t)slot * H + c);
-          const uint32_t dw4[4] = {dq.x, dq.y, dq.z, dq.w}, yw4[4] = {yq.x, yq.y, yq.z, yq.w};
-          uint32_t o[4];
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const float d0 = __uint_as_float(dw4[p] << 16), d1 = __uint_as_float(dw4[p] & 0xFFFF0000u);
-            const float y0 = __uint_as_float(yw4[p] << 16), y1 = __uint_as_float(yw4[p] & 0xFFFF0000u);
+      for (int i = 0; i < kMaxSlots; ++i) {
+        if (32 * i >= nb) break;                // warp-uniform
+        const int b = lane + 32 * i;
+        const bool active = b < nb;
+        uint32_t o[8];
+        uint32_t sfb = 0;
+        uint2 cw = make_uint2(0u, 0u);
+        if (active) {
+          const uint4 y0 = ldg_nc(y + (int64_t)slot * H + 16 * b);
+          const uint4 y1 = ldg_nc(y + (int64_t)slot * H + 16 * b + 8);
+          const uint4 d0q = ldg_nc(dout + t * H + 16 * b), d1q = ldg_nc(dout + t * H + 16 * b + 8);
+          const uint32_t dw8[8] = {d0q.x, d0q.y, d0q.z, d0q.w, d1q.x, d1q.y, d1q.z, d1q.w};
+          const uint32_t yw8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+          float lo8[8], hi8[8];
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const float d0 = __uint_as_float(dw8[p] << 16), d1 = __uint_as_float(dw8[p] & 0xFFFF0000u);
+            const float y0f = __uint_as_float(yw8[p] << 16), y1f = __uint_as_float(yw8[p] & 0xFFFF0000u);
             o[p] = bf16_of_product(wj, d0) | (bf16_of_product(wj, d1) << 16);
-            acc = __fmaf_rn(d0, y0, acc);
-            acc = __fmaf_rn(d1, y1, acc);
-            asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(o[p] & 0x7FFF7FFFu));
+            acc = __fmaf_rn(d0, y0f, acc);
+            acc = __fmaf_rn(d1, y1f, acc);
+            float* dst = p < 4 ? lo8 : hi8;
+            dst[2 * (p & 3)] = __uint_as_float(o[p] << 16);
+            dst[2 * (p & 3) + 1] = __uint_as_float(o[p] & 0xFFFF0000u);
           }
-          *reinterpret_cast<uint4*>(dy + (int64_t)slot * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+          uint4* dyp = reinterpret_cast<uint4*>(dy + (int64_t)slot * H + 16 * b);
+          dyp[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dyp[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          const BlockScale bs = block_scale(fmaxf(absmax8(lo8), absmax8(hi8)), g, six_g);
+          const uint64_t jc = (uint64_t)(slot * H + 16 * b) / 8u;
+          cw.x = e2m1x8_sr(lo8, bs, philox4x32_10(make_uint4((uint32_t)jc, (uint32_t)(jc >> 32), 0u, 0u), k0, k1));
+          cw.y = e2m1x8_sr(hi8, bs, philox4x32_10(make_uint4((uint32_t)(jc + 1), (uint32_t)((jc + 1) >> 32), 0u, 0u),
+                                                  k0, k1));
+          sfb = bs.sf;
+        }
+        const uint32_t s1 = __shfl_down_sync(kAll, sfb, 1);
+        const uint32_t s2 = __shfl_down_sync(kAll, sfb, 2);
+        const uint32_t s3 = __shfl_down_sync(kAll, sfb, 3);
+        if (active) {
+          *reinterpret_cast<uint2*>(rcodes + (b >> 4) * tiled_block_bytes(128) + ((((b >> 1) & 7) ^ (rr & 7)) << 4) +
+                                    (b & 1) * 8) = cw;
+          const int wd = b >> 2;
+          if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(rsf + (wd >> 2) * tiled_block_bytes(128) + (wd & 3) * 512) =
+                sfb | (s1 << 8) | (s2 << 16) | (s3 << 24);
         }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kAll, acc, o));
-      if (lane == 0) dw[t * k + j] = acc;
-      if (amax_bits != nullptr && slot >= 0) {   // warp-uniform
-        uint32_t mb = max(m & 0xFFFFu, m >> 16) << 16;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(kAll, mb, o));
-        if (lane == 0 && mb != 0u) atomicMax(amax_bits + find_group(starts, E, slot), mb);
+      if (lane == 0) {
+        dw[t * k + j] = acc;
+        g_dy[slot] = g;
+        if (amax_bits != nullptr && mb != 0u) atomicMax(amax_bits + find_group(starts, E, slot), mb);
       }
     }
   }
@@ -106,7 +162,8 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(const __nv_bfloat
 
 cudaError_t launch_combine_backward(const void* dout, const int32_t* inv, const float* w, const void* y, int64_t T,
                                     int k, int64_t H, void* dy, float* dw, const int32_t* starts, int E,
-                                    uint32_t* amax_bits, cudaStream_t s) {
+                                    uint32_t* amax_bits, uint8_t* dyq, float* g_dy, uint64_t key, cudaStream_t s) {
+  if (H % 256 != 0 || H > 2048) return cudaErrorInvalidValue;
   if (amax_bits != nullptr) {
     const cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t) * E, s);
     if (err != cudaSuccess) return err;
@@ -116,7 +173,8 @@ cudaError_t launch_combine_backward(const void* dout, const int32_t* inv, const 
   if (blocks > 16 * (int64_t)num_sms()) blocks = 16 * (int64_t)num_sms();
   combine_backward_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dout), inv, w,
                                                       static_cast<const __nv_bfloat16*>(y), T, k, H,
-                                                      static_cast<__nv_bfloat16*>(dy), dw, starts, E, amax_bits);
+                                                      static_cast<__nv_bfloat16*>(dy), dw, starts, E, amax_bits,
+                                                      dyq, g_dy, key);
   return cudaGetLastError();
 }
 

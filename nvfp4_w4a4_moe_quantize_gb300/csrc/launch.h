@@ -127,10 +127,12 @@ cudaError_t launch_grouped_gemm_ragged_k(const uint8_t* A, const uint8_t* B, con
                                          const GemmArgs& g, cudaStream_t s);
 // Backward kernels (backward.cu).
 // amax_bits (nullable): zeroed, then the max |dy| of each expert's rows (starts: the
-// padded group offsets [E+1]).
+// padded group offsets [E+1]).  dy's rows are also quantised per row with stochastic
+// rounding (Philox key `key`) into the GEMM-tiled dyq (128-row blocks, K = H) and g_dy.
+// H % 256 == 0, H <= 2048.
 cudaError_t launch_combine_backward(const void* dout, const int32_t* inv, const float* w, const void* y, int64_t T,
                                     int k, int64_t H, void* dy, float* dw, const int32_t* starts, int E,
-                                    uint32_t* amax_bits, cudaStream_t s);
+                                    uint32_t* amax_bits, uint8_t* dyq, float* g_dy, uint64_t key, cudaStream_t s);
 cudaError_t launch_group_amax(const void* src, int64_t ld, int64_t F, const int32_t* rowmap, const int32_t* starts,
                               const int32_t* counts, int E, int64_t max_rows, uint32_t* amax_bits, cudaStream_t s);
 // The same maximum from per-row global scales g_rows = fl32(row max / 2688) (rows with a
