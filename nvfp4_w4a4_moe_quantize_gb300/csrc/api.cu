@@ -685,38 +685,44 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   const int64_t Ip = round_up(I, 256);
   int* status = device_status_ptr();
 
-  // 1. expert grouping
-  cudaError_t e = launch_permute(ids, T, k, E, counts, offsets, padded, inv, perm,
-                                 reinterpret_cast<int32_t*>(base + hist_off), permute_chunks(T * k), status, s);
-  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-
-  // 2. per-token NVFP4 of x into a token-ordered GEMM-tiled operand (parked in y's region,
-  //    free until the down GEMM), then gathered into every routed slot with the token's
-  //    global scale
+  // per-token operand and scales (parked in y's region, free until the down GEMM), then
+  // the per-row max |h| that the gate/up epilogue accumulates
   uint8_t* xq = static_cast<uint8_t*>(ybuf);
   float* gx = reinterpret_cast<float*>(xq + align256(tiled_bytes(T, H, 128)));
-  QuantArgs a{};
-  a.x = static_cast<const __nv_bfloat16*>(x);
-  a.rows = T;
-  a.cols = H;
-  a.ld = H;
-  a.mode = kScopeRow;
-  a.g_out = gx;
-  a.codes = xq;
-  a.sf_words = H / 64;
-  a.cols_pad = H;
-  a.rows_total = T;
-  a.map = kMapIdentity;
-  a.status = status;
-  a.tiled_R = 128;
-  a.kblocks = H / 256;
-  e = launch_quantize_rows(a, kRoundRNE, s);
-  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-  // per-row max |h|, accumulated by the gate/up epilogue; it lives in y's region after the
-  // token operand (consumed by the gather before the epilogue starts)
   uint32_t* h_amax = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(gx) + align256(sizeof(float) * T));
-  e = launch_gather_tiled(xq, gx, perm, padded + E, mcap, H, aq, ga, h_amax, s);
-  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  cudaError_t e;
+  if (T * k <= 1024 && E <= 1024) {
+    // 1-2. decode-size batches: grouping, per-token NVFP4 of x and its placement in every
+    //      routed slot in one launch (one CTA per token)
+    e = launch_prologue_small(ids, T, k, E, counts, offsets, padded, inv, perm, status, x, H, aq, ga, h_amax, s);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  } else {
+    // 1. expert grouping
+    e = launch_permute(ids, T, k, E, counts, offsets, padded, inv, perm, reinterpret_cast<int32_t*>(base + hist_off),
+                       permute_chunks(T * k), status, s);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    // 2. per-token NVFP4 of x into a token-ordered GEMM-tiled operand, then gathered into
+    //    every routed slot with the token's global scale (padding slots zero, h_amax zero)
+    QuantArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.rows = T;
+    a.cols = H;
+    a.ld = H;
+    a.mode = kScopeRow;
+    a.g_out = gx;
+    a.codes = xq;
+    a.sf_words = H / 64;
+    a.cols_pad = H;
+    a.rows_total = T;
+    a.map = kMapIdentity;
+    a.status = status;
+    a.tiled_R = 128;
+    a.kblocks = H / 256;
+    e = launch_quantize_rows(a, kRoundRNE, s);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    e = launch_gather_tiled(xq, gx, perm, padded + E, mcap, H, aq, ga, h_amax, s);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
 
   // 3. gate/up GEMM with the SwiGLU epilogue: h = BF16(silu(gate) * up)
   GemmArgs g1{};

@@ -170,6 +170,13 @@ cudaError_t launch_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t r
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renorm, int32_t* ids,
                               float* w, cudaStream_t s);
+// The forward's prologue for T*k <= 1024: the permutation (as launch_permute), each
+// token's row of x quantised per row (RNE) straight into its k slots of the GEMM-tiled aq
+// (128-row blocks, K = H), ga[slot] = the token's global scale, h_amax[slot] = 0.
+// E <= 1024, H % 256 == 0, H <= 2048.
+cudaError_t launch_prologue_small(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
+                                  int32_t* padded, int32_t* inv, int32_t* perm, int* status, const void* x, int64_t H,
+                                  uint8_t* aq, float* ga, uint32_t* h_amax, cudaStream_t s);
 cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
                            int32_t* padded, int32_t* inv, int32_t* perm, int32_t* hist, int64_t nchunks,
                            int* status, cudaStream_t s);

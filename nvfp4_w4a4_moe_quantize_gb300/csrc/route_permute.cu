@@ -10,8 +10,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "encode.cuh"
 #include "launch.h"
 #include "status.cuh"
+#include "tiled.cuh"
 
 namespace nvfp4 {
 
@@ -408,29 +410,32 @@ __global__ void __launch_bounds__(256) permute_rank_kernel(const int32_t* __rest
 // one block of 1024 threads -- per-expert counts in shared memory, the unpadded and
 // 128-padded exclusive scans, and each entry's rank among the earlier entries of its
 // expert (a scan over at most n - 1 ids in shared memory): the same stable slot order.
-__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids, int n, int k, int E,
-                                                             int32_t* __restrict__ counts,
-                                                             int32_t* __restrict__ offsets,
-                                                             int32_t* __restrict__ padded,
-                                                             int32_t* __restrict__ inv, int32_t* __restrict__ perm,
-                                                             int* status) {
-  __shared__ int32_t s_id[1024], s_cnt[1024], s_wsum[2][32], s_off[1025], s_pad[1025];
+// s_inv receives every entry's slot (-1 for an id out of range).  `write`: this block
+// also stores counts, offsets, padded, inv and perm, and flags bad ids.
+struct PermuteSmem {
+  int32_t id[1024], cnt[1024], wsum[2][32], off[1025], pad[1025], inv[1024];
+};
+
+__device__ __forceinline__ void permute_small_block(const int32_t* __restrict__ ids, int n, int k, int E, bool write,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ padded, int32_t* __restrict__ inv,
+                                                    int32_t* __restrict__ perm, int* status, PermuteSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  s_cnt[tid] = 0;
+  sm.cnt[tid] = 0;
   int e = -1;
   if (tid < n) {
     e = ids[tid];
     if (e < 0 || e >= E) {
-      set_status(status, kStatusBadInput);
+      if (write) set_status(status, kStatusBadInput);
       e = -1;
     }
   }
-  s_id[tid] = e;
+  sm.id[tid] = e;
   __syncthreads();
-  if (e >= 0) atomicAdd(&s_cnt[e], 1);
+  if (e >= 0) atomicAdd(&sm.cnt[e], 1);
   __syncthreads();
   // inclusive scans of the counts and of the 128-padded counts over the experts
-  const int32_t c = tid < E ? s_cnt[tid] : 0;
+  const int32_t c = tid < E ? sm.cnt[tid] : 0;
   int32_t a = c, b = (c + 127) / 128 * 128;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -441,12 +446,12 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
     }
   }
   if (lane == 31) {
-    s_wsum[0][wid] = a;
-    s_wsum[1][wid] = b;
+    sm.wsum[0][wid] = a;
+    sm.wsum[1][wid] = b;
   }
   __syncthreads();
   if (wid == 0) {
-    int32_t wa = s_wsum[0][lane], wb = s_wsum[1][lane];
+    int32_t wa = sm.wsum[0][lane], wb = sm.wsum[1][lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int32_t ya = __shfl_up_sync(kFullMask, wa, o), yb = __shfl_up_sync(kFullMask, wb, o);
@@ -455,39 +460,145 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
         wb += yb;
       }
     }
-    s_wsum[0][lane] = wa;
-    s_wsum[1][lane] = wb;
+    sm.wsum[0][lane] = wa;
+    sm.wsum[1][lane] = wb;
   }
   __syncthreads();
-  const int32_t base_a = wid ? s_wsum[0][wid - 1] : 0, base_b = wid ? s_wsum[1][wid - 1] : 0;
+  const int32_t base_a = wid ? sm.wsum[0][wid - 1] : 0, base_b = wid ? sm.wsum[1][wid - 1] : 0;
   const int32_t inc_a = a + base_a, inc_b = b + base_b;
   if (tid < E) {
-    s_off[tid + 1] = inc_a;
-    s_pad[tid + 1] = inc_b;
-    counts[tid] = c;
-    offsets[tid + 1] = inc_a;
-    padded[tid + 1] = inc_b;
+    sm.off[tid + 1] = inc_a;
+    sm.pad[tid + 1] = inc_b;
+    if (write) {
+      counts[tid] = c;
+      offsets[tid + 1] = inc_a;
+      padded[tid + 1] = inc_b;
+    }
   }
   if (tid == 0) {
-    s_off[0] = s_pad[0] = 0;
-    offsets[0] = padded[0] = 0;
+    sm.off[0] = sm.pad[0] = 0;
+    if (write) offsets[0] = padded[0] = 0;
   }
   __syncthreads();
-  const int32_t total_pad = s_pad[E];
-  if (perm != nullptr)
+  const int32_t total_pad = sm.pad[E];
+  if (write && perm != nullptr)
     for (int32_t slot = tid; slot < total_pad; slot += blockDim.x) perm[slot] = -1;
   __syncthreads();
   if (tid < n) {
+    int32_t slot = -1;
     if (e >= 0) {
       int32_t rank = 0;
-      for (int i = 0; i < tid; ++i) rank += s_id[i] == e;
-      const int32_t slot = s_pad[e] + rank;
-      inv[tid] = slot;
-      if (perm != nullptr) perm[slot] = tid / k;
-    } else {
-      inv[tid] = -1;
+      for (int i = 0; i < tid; ++i) rank += sm.id[i] == e;
+      slot = sm.pad[e] + rank;
+      if (write && perm != nullptr) perm[slot] = tid / k;
+    }
+    sm.inv[tid] = slot;
+    if (write) inv[tid] = slot;
+  }
+}
+
+__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids, int n, int k, int E,
+                                                             int32_t* __restrict__ counts,
+                                                             int32_t* __restrict__ offsets,
+                                                             int32_t* __restrict__ padded,
+                                                             int32_t* __restrict__ inv, int32_t* __restrict__ perm,
+                                                             int* status) {
+  __shared__ PermuteSmem sm;
+  permute_small_block(ids, n, k, E, true, counts, offsets, padded, inv, perm, status, sm);
+}
+
+// The forward's whole prologue for small batches (n = T*k <= 1024): one CTA per token.
+// Every CTA forms the same slot order (permute_small_block; CTA 0 stores it), then its
+// warp 0 quantises the token's row of x (per-row scale, round to nearest: the row
+// quantiser's arithmetic) and writes it into each of the token's k slots of the
+// GEMM-tiled operand aq (128-row blocks, K = H), with the token's global scale in ga and
+// a zero in h_amax.  This replaces the permutation, the token-order quantisation and the
+// slot gather (three to five launches) for decode-size batches; slots of group padding
+// are left as they are (no kernel stores their results).
+__global__ void __launch_bounds__(1024) moe_prologue_small_kernel(
+    const int32_t* __restrict__ ids, int n, int k, int E, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ padded, int32_t* __restrict__ inv,
+    int32_t* __restrict__ perm, int* status, const __nv_bfloat16* __restrict__ x, int64_t H, uint8_t* aq,
+    float* __restrict__ ga, uint32_t* __restrict__ h_amax) {
+  __shared__ PermuteSmem sm;
+  permute_small_block(ids, n, k, E, blockIdx.x == 0, counts, offsets, padded, inv, perm, status, sm);
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  constexpr int kMaxSlots = 4;                  // 16-value blocks per lane: H <= 2048
+  const int lane = threadIdx.x;
+  const int64_t t = blockIdx.x;
+  const int nb = (int)(H / 16);
+  const int64_t kblocks = H / 256;
+  uint4 q[kMaxSlots][2];
+  float bm[kMaxSlots];
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxSlots; ++i) {
+    const int b = lane + 32 * i;
+    q[i][0] = q[i][1] = make_uint4(0u, 0u, 0u, 0u);
+    bm[i] = 0.0f;
+    if (b < nb) {
+      q[i][0] = *reinterpret_cast<const uint4*>(x + t * H + 16 * b);
+      q[i][1] = *reinterpret_cast<const uint4*>(x + t * H + 16 * b + 8);
+      bm[i] = absmax16_bf16(q[i][0], q[i][1]);
+      m = fmaxf(m, bm[i]);
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
+  const float g = __fdiv_rn(m, kGlobalDivisor);
+  const float six_g = __fmul_rn(6.0f, g);
+  uint2 cw[kMaxSlots];
+  uint32_t sfw[kMaxSlots];
+#pragma unroll
+  for (int i = 0; i < kMaxSlots; ++i) {
+    const int b = lane + 32 * i;
+    uint32_t sfb = 0;
+    cw[i] = make_uint2(0u, 0u);
+    if (b < nb) {
+      float h0[8], h1[8];
+      bf16x8_to_f32(q[i][0], h0);
+      bf16x8_to_f32(q[i][1], h1);
+      const BlockScale bs = block_scale(bm[i], g, six_g);
+      cw[i] = e2m1x16_rn(h0, h1, bs);
+      sfb = bs.sf;
+    }
+    const uint32_t s1 = __shfl_down_sync(kFullMask, sfb, 1);
+    const uint32_t s2 = __shfl_down_sync(kFullMask, sfb, 2);
+    const uint32_t s3 = __shfl_down_sync(kFullMask, sfb, 3);
+    sfw[i] = sfb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  }
+  for (int j = 0; j < k; ++j) {
+    const int32_t slot = sm.inv[t * k + j];
+    if (slot < 0) continue;                     // an id out of range: counted nowhere
+    const int64_t rr = slot & 127;
+    uint8_t* blk0 = aq + (int64_t)(slot >> 7) * kblocks * tiled_block_bytes(128);
+#pragma unroll
+    for (int i = 0; i < kMaxSlots; ++i) {
+      const int b = lane + 32 * i;
+      if (b >= nb) continue;
+      *reinterpret_cast<uint2*>(blk0 + (b >> 4) * tiled_block_bytes(128) + rr * 128 +
+                                ((((b >> 1) & 7) ^ (rr & 7)) << 4) + (b & 1) * 8) = cw[i];
+      const int wd = b >> 2;
+      if ((lane & 3) == 0)
+        *reinterpret_cast<uint32_t*>(blk0 + (wd >> 2) * tiled_block_bytes(128) + 128 * 128 + (wd & 3) * 512 +
+                                     (rr & 31) * 16 + (rr >> 5) * 4) = sfw[i];
+    }
+    if (lane == 0) {
+      ga[slot] = g;
+      h_amax[slot] = 0u;
+    }
+  }
+}
+
+cudaError_t launch_prologue_small(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
+                                  int32_t* padded, int32_t* inv, int32_t* perm, int* status, const void* x, int64_t H,
+                                  uint8_t* aq, float* ga, uint32_t* h_amax, cudaStream_t s) {
+  if (T * k > 1024 || E > 1024 || H % 256 != 0 || H > 2048) return cudaErrorInvalidValue;
+  if (T == 0) return cudaSuccess;
+  moe_prologue_small_kernel<<<(int)T, 1024, 0, s>>>(ids, (int)(T * k), k, E, counts, offsets, padded, inv, perm,
+                                                     status, static_cast<const __nv_bfloat16*>(x), H, aq, ga, h_amax);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
