@@ -64,14 +64,13 @@ constexpr int kAccCols = kBN;
 constexpr int kSFCol0 = kAccCols;
 constexpr int kSFStageCols = 16 + 32;       // A: 4 x 4 columns, B: 4 x 8 columns
 constexpr int kFirstEpiWarp = 3;
-constexpr int kScaleWarps = 4;              // one CTA per tile: one per TMEM lane quadrant
+constexpr int kScaleWarps = 4;              // one per TMEM lane quadrant
 // Epilogue warps: 8 for the plain store (two per TMEM lane quadrant, 128 columns each);
 // 16 for the SwiGLU epilogue, whose per-value arithmetic needs the latency hiding of four
 // warps per quadrant (each one 32-column gate slice and its up slice).
 __host__ __device__ constexpr int epi_warps(bool swiglu) { return swiglu ? 16 : 8; }
-// The CTA pair keeps the scale copies on tcgen05.cp (issued by CTA 0 for both SMs).
 __host__ __device__ constexpr int threads(bool swiglu, bool pair) {
-  return 32 * (kFirstEpiWarp + epi_warps(swiglu) + (pair ? 0 : kScaleWarps));
+  return 32 * (kFirstEpiWarp + epi_warps(swiglu) + kScaleWarps) + 0 * pair;
 }
 constexpr int kMaxE = 512;
 
@@ -95,8 +94,8 @@ struct Smem {
   uint8_t out[kOutBytes];
   uint64_t full[Layout<kPair>::kStages];
   uint64_t empty[Layout<kPair>::kStages];
-  uint64_t sfull[Layout<kPair>::kStages];     // one CTA per tile: the stage's scale bytes have landed
-  uint64_t sfready[Layout<kPair>::kStages];   // one CTA per tile: the stage's scales are in TMEM
+  uint64_t sfull[Layout<kPair>::kStages];     // the stage's scale bytes have landed
+  uint64_t sfready[Layout<kPair>::kStages];   // the stage's scales are in TMEM (pair: in both CTAs')
   uint64_t accf;
   uint64_t acce;
   uint64_t fin;               // the MMA issuer's last operations have completed
@@ -208,10 +207,11 @@ __device__ __forceinline__ TileJob tile_job_pair(const GemmArgs& g, const int32_
 
 // kMode: 0 plain store, 1 SwiGLU epilogue, 2 plain store with ragged K per expert.
 // kPair: a cluster of two CTAs on two SMs shares each M=256 x N=256 tile (cta_group::2):
-// CTA 0 issues the MMAs and the scale copies; each CTA loads its own A block, its half of
-// B's codes and all of B's scales into its own shared memory (no shared loads); CTA 1's
-// warp 2 tells CTA 0 when a stage of CTA 1 is full; CTA 0's commits free the stages and
-// fill the accumulators of both; both CTAs' epilogues release the accumulator to CTA 0.
+// CTA 0 issues the MMAs; each CTA loads its own A block, its half of B's codes and all of
+// B's scales into its own shared memory (no shared loads), and its scale warps write its
+// own TMEM; CTA 1's warp 2 tells CTA 0 when a stage of CTA 1 is full and its scales are in
+// CTA 1's TMEM; CTA 0's commits free the stages and fill the accumulators of both; both
+// CTAs' epilogues release the accumulator to CTA 0.
 template <int kMode, bool kPair>
 __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
     grouped_gemm_tiled_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B,
@@ -310,17 +310,26 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
             mbar_arrive_expect_tx(&sm.full[stage], codes);
             bulk_load(dst, src, codes, &sm.full[stage]);
           } else if (is_a) {
+            // pair: this CTA's A block (scales first, on the scale barrier), or nothing
+            // for the empty half of a group's last pair
             if (job.has_a) {
-              mbar_arrive_expect_tx(&sm.full[stage], kABlock);
-              bulk_load(st + L::kA, job.a + (int64_t)kb * kABlock, kABlock, &sm.full[stage]);
+              const uint8_t* src = job.a + (int64_t)kb * kABlock;
+              mbar_arrive_expect_tx(&sm.sfull[stage], kABlock - kACodes);
+              bulk_load(st + L::kSFA, src + kACodes, kABlock - kACodes, &sm.sfull[stage]);
+              mbar_arrive_expect_tx(&sm.full[stage], kACodes);
+              bulk_load(st + L::kA, src, kACodes, &sm.full[stage]);
             } else {
+              mbar_arrive(&sm.sfull[stage]);
               mbar_arrive(&sm.full[stage]);
             }
           } else {
+            // pair: all of B's scales (each SM's MMA reads them all), then this CTA's half
+            // of B's codes
             const uint8_t* src = job.b + (int64_t)kb * kBBlock;
-            mbar_arrive_expect_tx(&sm.full[stage], kBHalfCodes + kBScales);
+            mbar_arrive_expect_tx(&sm.sfull[stage], kBScales);
+            bulk_load(st + L::kSFB, src + kBCodes, kBScales, &sm.sfull[stage]);
+            mbar_arrive_expect_tx(&sm.full[stage], kBHalfCodes);
             bulk_load(st + L::kB, src + rank * kBHalfCodes, kBHalfCodes, &sm.full[stage]);
-            bulk_load(st + L::kSFB, src + kBCodes, kBScales, &sm.full[stage]);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -350,26 +359,13 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
                                 : kblocks;
         for (int kb = 0; kb < kbt; ++kb) {
           bool ok = wait(&sm.full[stage], phase);
-          if (!kPair) ok = ok && wait(&sm.sfready[stage], phase);
+          ok = ok && wait(&sm.sfready[stage], phase);
           if (!__all_sync(0xFFFFFFFFu, ok)) goto mma_done;
           tc_fence_after();
           const uint32_t sfa_t = tmem + kSFCol0 + stage * kSFStageCols;
           const uint32_t sfb_t = sfa_t + 16;
           const uint64_t adesc = adesc0 + stage * kStageDesc, bdesc = bdesc0 + stage * kStageDesc;
-          if (kPair && leader) {
-            const uint32_t st = st0 + stage * (uint32_t)L::kStageBytes;
-            const uint32_t ssfa = st + L::kSFA, ssfb = st + L::kSFB;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, smem_desc(ssfa + 512 * j, 0, 128, 0));
-              tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j, smem_desc(ssfb + 512 * j, 0, 128, 0));
-              tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4, smem_desc(ssfb + 2048 + 512 * j, 0, 128, 0));
-            }
-          }
           if (kb == 0) {
-            // (pair) the first stage's scale copies are issued before this wait: they do
-            // not touch the accumulator, so the tensor pipe runs them while the epilogue
-            // drains the previous tile (tcgen05 ops of one thread execute in issue order)
             if (!__all_sync(0xFFFFFFFFu, wait(&sm.acce, (it & 1) ^ 1u))) goto mma_done;
             tc_fence_after();
           }
@@ -417,12 +413,14 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
       }
       __syncwarp();
     } else if (kPair && lane == 0) {
-      // CTA 1: each of this CTA's full stages counts as one arrival on CTA 0's barrier
+      // CTA 1: each stage of this CTA that is full and whose scales are in its TMEM counts
+      // as one arrival on CTA 0's full barrier (one cluster-scope arrival per stage: as
+      // four, one per scale warp, they stretched a stage to ~1500 cycles)
       uint32_t stage = 0, phase = 0;
       const uint32_t full0 = cluster_addr(&sm.full[0], 0);
       for (int t = first; t < total; t += stride) {
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait(&sm.full[stage], phase)) goto relay_done;
+          if (!wait(&sm.full[stage], phase) || !wait(&sm.sfready[stage], phase)) goto relay_done;
           mbar_arrive_cluster(full0 + stage * (uint32_t)sizeof(uint64_t));
           if (++stage == kStages) {
             stage = 0;
@@ -432,7 +430,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
       }
     relay_done:;
     }
-  } else if (!kPair && warp >= kFirstEpiWarp + kEpiWarps) {
+  } else if (warp >= kFirstEpiWarp + kEpiWarps) {
     // scale warps: the stage's A scales (four 512-byte blocks, one per MMA) go to columns
     // [0, 16) of the stage's scale slot, B's (two blocks per MMA: rows 0-127, then
     // 128-255) to [16, 48), block j at 4j / 16 + 8j (+4), each as 32 lanes x 16 bytes in
@@ -463,7 +461,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.sfready[stage]);
+        if (lane == 0) mbar_arrive(&sm.sfready[stage]);   // (pair, CTA 1: relayed to CTA 0 by warp 2)
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
