@@ -255,8 +255,8 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
     }
     mbar_init(&sm.accf, 1);
     mbar_init(&sm.fin, 1);
-    // pair: one arrival per epilogue warp of either CTA (on CTA 0's barrier)
-    mbar_init(&sm.acce, kPair ? 2 * kEpiWarps : kEpiWarps * 32);
+    // one arrival per epilogue warp (pair: of either CTA, on CTA 0's barrier)
+    mbar_init(&sm.acce, kPair ? 2 * kEpiWarps : kEpiWarps);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -510,16 +510,15 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
       d_n = 0;
       d_mask = 0;
     };
-    // the accumulator is drained: every lane arrives on its CTA's barrier, or, in a pair,
-    // one lane per warp on CTA 0's
+    // the accumulator is drained: one lane per warp arrives (after the warp's loads have
+    // completed) on its CTA's barrier, or, in a pair, on CTA 0's
     const uint32_t acce0 = kPair ? cluster_addr(&sm.acce, 0) : 0u;
     auto release_acc = [&]() {
       tc_fence_before();
-      if (kPair) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acce0);
-      } else {
-        mbar_arrive(&sm.acce);
+      __syncwarp();
+      if (lane == 0) {
+        if (kPair) mbar_arrive_cluster(acce0);
+        else mbar_arrive(&sm.acce);
       }
     };
     bool aborted = false;
