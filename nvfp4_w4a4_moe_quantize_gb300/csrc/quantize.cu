@@ -600,6 +600,8 @@ __device__ __forceinline__ void requant_block(const uint4& q0, const uint4& q1, 
   c1 = c.y;
 }
 
+// Idx: the index type of the unit and byte arithmetic (32-bit when every index fits).
+template <typename Idx>
 __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16* __restrict__ h,
                                                             const uint32_t* __restrict__ amax_bits,
                                                             const int32_t* __restrict__ perm,
@@ -609,17 +611,17 @@ __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16*
   const int lane = threadIdx.x & 31;
   int64_t rows = *n_rows_dev;
   if (rows > max_rows) rows = max_rows;
-  const int64_t np = Ip / 32, np_data = I / 32, kblocks = Ip / 256;
-  const int64_t total = rows * np;   // np % 2 == 0: lane pairs hold blocks 4w .. 4w+3 of one row
+  const Idx np = (Idx)(Ip / 32), np_data = (Idx)(I / 32), kblocks = (Idx)(Ip / 256);
+  const int64_t total = rows * (int64_t)np;   // np % 2 == 0: lane pairs hold blocks 4w .. 4w+3 of one row
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += stride) {
-    const int64_t i = base + threadIdx.x;
-    const bool in = i < total;
-    const int64_t row = in ? i / np : 0, pr = in ? i - (i / np) * np : 0;
+    const Idx i = (Idx)(base + threadIdx.x);
+    const bool in = base + threadIdx.x < total;
+    const Idx row = in ? i / np : 0, pr = in ? i - row * np : 0;
     const bool data = in && pr < np_data;
     uint4 q[4] = {};
     if (data) {
-      const __nv_bfloat16* src = h + row * I + pr * 32;
+      const __nv_bfloat16* src = h + (int64_t)row * I + pr * 32;
 #pragma unroll
       for (int j = 0; j < 4; ++j) q[j] = ld_nc_v4(src + 8 * j);
     }
@@ -636,9 +638,17 @@ __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16*
     }
     const uint32_t s1 = __shfl_down_sync(kFull, sf2, 1);
     if (live) {
-      *reinterpret_cast<uint4*>(out + tiled_code_offset(row, pr * 16, kblocks, 128)) = cw;
-      if ((lane & 1) == 0)
-        *reinterpret_cast<uint32_t*>(out + tiled_sf_offset(row, 2 * pr, kblocks, 128)) = sf2 | (s1 << 16);
+      // the GEMM-tiled layout (128-row blocks) in Idx arithmetic: codes bytes 16 pr .. of the
+      // row, scale columns 2 pr, 2 pr + 1
+      const Idx blk = row >> 7, rr = row & 127, b = pr * 16, kb = b >> 7, bb = b & 127;
+      *reinterpret_cast<uint4*>(out + (size_t)((blk * kblocks + kb) * (Idx)(128 * 144) + rr * 128 +
+                                               (((bb >> 4) ^ (rr & 7)) << 4))) = cw;
+      if ((lane & 1) == 0) {
+        const Idx c = 2 * pr, kc = c >> 4, cc = c & 15;
+        *reinterpret_cast<uint32_t*>(out + (size_t)((blk * kblocks + kc) * (Idx)(128 * 144) + 128 * 128 +
+                                                    (cc >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (cc & 3))) =
+            sf2 | (s1 << 16);
+      }
     }
   }
 }
@@ -650,7 +660,13 @@ cudaError_t launch_requant_tiled(const __nv_bfloat16* h, const uint32_t* amax_bi
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
-  requant_tiled_kernel<<<(int)blocks, 256, 0, s>>>(h, amax_bits, perm, n_rows_dev, max_rows, I, Ip, out, g_out);
+  // 32-bit index arithmetic when the units and the output's bytes all fit
+  if (total < ((int64_t)1 << 31) && tiled_bytes(max_rows, Ip, 128) < ((int64_t)1 << 31))
+    requant_tiled_kernel<uint32_t><<<(int)blocks, 256, 0, s>>>(h, amax_bits, perm, n_rows_dev, max_rows, I, Ip, out,
+                                                               g_out);
+  else
+    requant_tiled_kernel<int64_t><<<(int)blocks, 256, 0, s>>>(h, amax_bits, perm, n_rows_dev, max_rows, I, Ip, out,
+                                                              g_out);
   return cudaGetLastError();
 }
 
