@@ -99,6 +99,65 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint8_t* __restri
   }
 }
 
+// BF16 output, one thread per 16-value block (8 code bytes, 1 scale byte).  The block's
+// 8 magnitudes v * s * g (v = 0, 0.5, 1, 1.5, 2, 3, 4, 6) take 8 BF16 values: P = BF16(s g)
+// and Q = BF16(1.5 s g) are rounded once each (dq_bf16_bits), and the others are P and Q
+// times a power of two -- exact while every one of them stays a normal BF16 value, since
+// scaling by a power of two commutes with the rounding there; otherwise each of the 7 is
+// rounded on its own.  The 8 values sit as a byte table (low bytes, high bytes), and four
+// codes at a time become four BF16 values by byte permutes indexed by their magnitude
+// bits, the sign bit ORed in (a zero keeps the code's sign, as the exact product does).
+template <typename Idx>
+__global__ void __launch_bounds__(256) dequantize_bf16_kernel(const uint8_t* __restrict__ codes,
+                                                              const uint8_t* __restrict__ sf,
+                                                              const float* __restrict__ g, int64_t rows,
+                                                              int64_t cols, int mode, int64_t group_rows,
+                                                              __nv_bfloat16* __restrict__ out, int64_t ldo) {
+  const Idx bpr = (Idx)(cols / 16);
+  const int64_t total = rows * (int64_t)bpr, sf_words = (cols / 16 + 3) / 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const Idx r = (Idx)i / bpr, b = (Idx)i - r * bpr;
+    const uint2 cw = __ldcs(reinterpret_cast<const uint2*>(codes + (int64_t)r * (cols / 2) + 8 * (int64_t)b));
+    const uint32_t sfb = sf[(((int64_t)r >> 7) * sf_words + b / 4) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3)];
+    const float gs = g[mode == kScopeTensor ? 0 : (mode == kScopeRow ? (int64_t)r : (int64_t)r / group_rows)];
+    const float s = e4m3_value(sfb);
+    const uint32_t P = dq_bf16_bits(s, gs), Q = dq_bf16_bits(__fmul_rn(1.5f, s), gs);
+    const uint32_t eP = (P >> 7) & 0xFFu, eQ = (Q >> 7) & 0xFFu;
+    uint32_t t[8];
+    t[0] = 0u;
+    if (eP - 2u <= 250u && eQ - 1u <= 251u) {   // P/2 .. 4P and Q .. 4Q all normal BF16 values
+      t[1] = P - 0x80u;
+      t[2] = P;
+      t[3] = Q;
+      t[4] = P + 0x80u;
+      t[5] = Q + 0x80u;
+      t[6] = P + 0x100u;
+      t[7] = Q + 0x100u;
+    } else {
+#pragma unroll
+      for (int m = 1; m < 8; ++m)
+        t[m] = dq_bf16_bits(__fmul_rn(__fmul_rn(e2m1_scaled((uint32_t)m), s), 0x1p126f), gs);
+    }
+    const uint32_t w0 = t[0] | (t[1] << 16), w1 = t[2] | (t[3] << 16), w2 = t[4] | (t[5] << 16),
+                   w3 = t[6] | (t[7] << 16);
+    const uint32_t lo0 = __byte_perm(w0, w1, 0x6420), lo1 = __byte_perm(w2, w3, 0x6420);   // low bytes of t[0..7]
+    const uint32_t hi0 = __byte_perm(w0, w1, 0x7531), hi1 = __byte_perm(w2, w3, 0x7531);   // high bytes
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t c4 = ((q < 2 ? cw.x : cw.y) >> (16 * (q & 1))) & 0xFFFFu;   // codes 4q .. 4q+3
+      const uint32_t sel = c4 & 0x7777u;                                         // their magnitudes
+      const uint32_t lo = __byte_perm(lo0, lo1, sel), hi = __byte_perm(hi0, hi1, sel);
+      o[2 * q] = __byte_perm(lo, hi, 0x5140) | ((c4 << 12) & 0x8000u) | ((c4 << 24) & 0x80000000u);
+      o[2 * q + 1] = __byte_perm(lo, hi, 0x7362) | ((c4 << 4) & 0x8000u) | ((c4 << 16) & 0x80000000u);
+    }
+    __nv_bfloat16* op = out + (int64_t)r * ldo + 16 * (int64_t)b;
+    __stcs(reinterpret_cast<uint4*>(op), make_uint4(o[0], o[1], o[2], o[3]));
+    __stcs(reinterpret_cast<uint4*>(op + 8), make_uint4(o[4], o[5], o[6], o[7]));
+  }
+}
+
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows, int64_t cols,
                               int mode, int64_t group_rows, void* out, bool out_f32, int64_t ldo, cudaStream_t s) {
   const int64_t total = rows * (cols / 8);
@@ -110,12 +169,16 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* sf, const flo
     dequantize_kernel<true, uint32_t><<<(int)blocks, 256, 0, s>>>(codes, sf, g, rows, cols, mode, group_rows, out, ldo);
   else if (out_f32)
     dequantize_kernel<true, int64_t><<<(int)blocks, 256, 0, s>>>(codes, sf, g, rows, cols, mode, group_rows, out, ldo);
-  else if (i32)
-    dequantize_kernel<false, uint32_t><<<(int)blocks, 256, 0, s>>>(codes, sf, g, rows, cols, mode, group_rows, out,
-                                                                   ldo);
-  else
-    dequantize_kernel<false, int64_t><<<(int)blocks, 256, 0, s>>>(codes, sf, g, rows, cols, mode, group_rows, out,
-                                                                  ldo);
+  else {
+    const int64_t nblk = rows * (cols / 16);
+    int64_t bb = (nblk + 255) / 256;
+    if (bb > 16 * (int64_t)num_sms()) bb = 16 * (int64_t)num_sms();
+    auto* o = static_cast<__nv_bfloat16*>(out);
+    if (nblk < ((int64_t)1 << 32) && rows < ((int64_t)1 << 31))
+      dequantize_bf16_kernel<uint32_t><<<(int)bb, 256, 0, s>>>(codes, sf, g, rows, cols, mode, group_rows, o, ldo);
+    else
+      dequantize_bf16_kernel<int64_t><<<(int)bb, 256, 0, s>>>(codes, sf, g, rows, cols, mode, group_rows, o, ldo);
+  }
   return cudaGetLastError();
 }
 

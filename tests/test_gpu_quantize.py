@@ -161,6 +161,26 @@ def test_dequantize_matches_oracle(cuda_lib, scope, shape):
     np.testing.assert_array_equal(got_f32.view(np.uint32), exact.astype(np.float32).view(np.uint32))
 
 
+def test_dequantize_every_scale_and_code(cuda_lib):
+    """DQ of every (E4M3 scale byte, E2M1 code) pair under per-row global scales from the
+    subnormal BF16 range to near the top of the float32 range: BF16 and float32 outputs
+    equal the oracle's exact dequantisation rounded once, bit for bit."""
+    sfb = np.arange(127, dtype=np.uint8)                     # every finite E4M3 scale byte
+    gs = np.array([1.0, 1.0 / 2688, 3.7e-5, 2.0 ** -126, 1e-38, 7.1e-42, 1e-30, 3e30, 2.0 ** 120, 0.0], np.float32)
+    rows = sfb.size * gs.size
+    codes = np.tile(np.arange(16, dtype=np.uint8), (rows, 1))
+    sf = np.tile(sfb, gs.size).reshape(rows, 1)
+    g_rows = np.repeat(gs, sfb.size)
+    exact = Q.dequantize(codes, sf, g_rows.astype(np.float64))
+    c = dev(F.pack_e2m1(codes))
+    s_ = dev(F.sf_swizzle(sf))
+    g = dev(g_rows)
+    got_bf16 = u16(cuda_lib.nvfp4_dequantize(c, s_, g, 16, cuda_lib.SCALE_PER_ROW, 0))
+    np.testing.assert_array_equal(got_bf16, F.bf16_round(exact))
+    got_f32 = npy(cuda_lib.nvfp4_dequantize(c, s_, g, 16, cuda_lib.SCALE_PER_ROW, 0, out_dtype=torch.float32))
+    np.testing.assert_array_equal(got_f32.view(np.uint32), exact.astype(np.float32).view(np.uint32))
+
+
 @pytest.mark.parametrize("scope", ["tensor", "row", "group"])
 @pytest.mark.parametrize("rounding", ["rne", "sr"])
 @pytest.mark.parametrize("shape", [(3, 48, 40), (1, 256, 2048), (2, 2048, 72)])
