@@ -130,11 +130,12 @@ __global__ void __launch_bounds__(256, 3) combine_backward_kernel(const __nv_bfl
           uint4* dyp = reinterpret_cast<uint4*>(dy + (int64_t)slot * H + 16 * b);
           dyp[0] = make_uint4(o[0], o[1], o[2], o[3]);
           dyp[1] = make_uint4(o[4], o[5], o[6], o[7]);
-          const BlockScale bs = block_scale(fmaxf(absmax8(lo8), absmax8(hi8)), g, six_g);
+          const uint4 ow0 = make_uint4(o[0], o[1], o[2], o[3]), ow1 = make_uint4(o[4], o[5], o[6], o[7]);
+          const BlockScale bs = block_scale(absmax16_bf16(ow0, ow1), g, six_g);
           const uint64_t jc = (uint64_t)(slot * H + 16 * b) / 8u;
-          cw.x = e2m1x8_sr(lo8, bs, philox4x32_10(make_uint4((uint32_t)jc, (uint32_t)(jc >> 32), 0u, 0u), k0, k1));
-          cw.y = e2m1x8_sr(hi8, bs, philox4x32_10(make_uint4((uint32_t)(jc + 1), (uint32_t)((jc + 1) >> 32), 0u, 0u),
-                                                  k0, k1));
+          cw.x = e2m1x8_sr(lo8, ow0, bs, philox4x32_10(make_uint4((uint32_t)jc, (uint32_t)(jc >> 32), 0u, 0u), k0, k1));
+          cw.y = e2m1x8_sr(hi8, ow1, bs,
+                           philox4x32_10(make_uint4((uint32_t)(jc + 1), (uint32_t)((jc + 1) >> 32), 0u, 0u), k0, k1));
           sfb = bs.sf;
         }
         const uint32_t s1 = __shfl_down_sync(kAll, sfb, 1);

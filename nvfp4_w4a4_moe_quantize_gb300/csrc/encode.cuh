@@ -19,6 +19,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace nvfp4 {
 
@@ -34,14 +35,18 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
   }
 }
 
-// max |x| of 16 BF16 values (two 16-byte chunks), as a float: sign-cleared BF16 bit
-// patterns order like the magnitudes (inputs are finite), two 16-bit maxima per
-// instruction.
+// max |x| of 16 BF16 values (two 16-byte chunks), as a float: a tree of packed BF16
+// maxima of magnitudes (max.xorsign.abs: the larger magnitude of each half, its sign the
+// XOR of the two signs, cleared at the end); inputs are finite, so the result is exact.
+__device__ __forceinline__ uint32_t maxabs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ float absmax16_bf16(const uint4& q0, const uint4& q1) {
-  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-  uint32_t m = w[0] & 0x7FFF7FFFu;
-#pragma unroll
-  for (int i = 1; i < 8; ++i) asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(w[i] & 0x7FFF7FFFu));
+  const uint32_t m = maxabs_bf16x2(maxabs_bf16x2(maxabs_bf16x2(q0.x, q0.y), maxabs_bf16x2(q0.z, q0.w)),
+                                   maxabs_bf16x2(maxabs_bf16x2(q1.x, q1.y), maxabs_bf16x2(q1.z, q1.w))) &
+                     0x7FFF7FFFu;
   return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
 }
 
@@ -52,10 +57,13 @@ __device__ __forceinline__ float absmax8(const float (&f)[8]) {
   return m;
 }
 
-// E4M3 byte -> float32 (exact; scales are non-negative so the sign bit is 0).
+// E4M3 byte -> float32 (exact; scales are non-negative so the sign bit is 0): the
+// hardware E4M3 -> FP16 conversion (every E4M3 value, subnormals included, is an FP16
+// value), then FP16 -> FP32.
 __device__ __forceinline__ float e4m3_decode(uint32_t b) {
-  const uint32_t e = (b >> 3) & 0xFu, m = b & 7u;
-  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
+  uint32_t h2;
+  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(h2) : "r"(b));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
 // float32 (>= 0) -> E4M3 byte, round to nearest even, saturating at 448.
@@ -77,8 +85,8 @@ struct BlockScale {
 };
 
 // Block scale of one 16-value block with max |x| = amax_b, given the scope's g and 6g.
-// The brackets come from the hardware reciprocal (rcp.approx.f32, at most one ulp from
-// 1/s): r * (1 -/+ 2^-18) leaves a margin of over 2^-19 on either side of 1/s, far more
+// The brackets come from the hardware reciprocal (rcp.approx.ftz.f32, at most one ulp from
+// 1/s; s >= 2^-60 is a normal number, so flushing subnormals changes nothing): r * (1 -/+ 2^-18) leaves a margin of over 2^-19 on either side of 1/s, far more
 // than the rounding of the reciprocal, of the bracket product and of |x| * r (2^-23 +
 // 2 * 2^-24).
 __device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float six_g) {
@@ -95,7 +103,7 @@ __device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float s
   bs.s = __fmul_rn(e4m3_decode(bs.sf), g);
   if (bs.s >= kTinyScale) {
     float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(bs.s));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(bs.s));
     bs.r = r;
     bs.r_lo = __fmul_rn(r, 0.99999618530273438f);   // 1 - 2^-18
     bs.r_hi = __fmul_rn(r, 1.0000038146972656f);    // 1 + 2^-18
@@ -236,6 +244,23 @@ __device__ __forceinline__ uint2 e2m1x16_rn(const float (&h0)[8], const float (&
   return make_uint2(canonical_zero((uint32_t)lo), canonical_zero((uint32_t)(lo >> 32)));
 }
 
+// The sign bits of 8 BF16 values (4 words, value 2i in the low half of word i) at bit
+// 4e + 3 of a packed code word: a byte permute with sign replication turns the sign of
+// each value into a 0x00 / 0xFF byte, two more interleave the even and odd values.
+__device__ __forceinline__ uint32_t sign_nibbles(const uint4& w) {
+  uint32_t lo, hi;
+  asm("prmt.b32 %0, %1, %2, 0xFDB9;" : "=r"(lo) : "r"(w.x), "r"(w.y));   // values 0..3
+  asm("prmt.b32 %0, %1, %2, 0xFDB9;" : "=r"(hi) : "r"(w.z), "r"(w.w));   // values 4..7
+  return (__byte_perm(lo, hi, 0x6420) & 0x08080808u) | (__byte_perm(lo, hi, 0x7531) & 0x80808080u);
+}
+
+// The words of 8 floats as BF16 pairs (value 2i in the low half of word i); only the
+// sign bits are used, so the floats need not be BF16 values.
+__device__ __forceinline__ uint4 bf16_words(const float (&f)[8]) {
+  const auto hi16 = [](float a, float b) { return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632); };
+  return make_uint4(hi16(f[0], f[1]), hi16(f[2], f[3]), hi16(f[4], f[5]), hi16(f[6], f[7]));
+}
+
 // Philox4x32-10 (Salmon et al., SC'11): 10 rounds of the Philox-4x32 bijection, key
 // bumped by the Weyl constants between rounds.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
@@ -285,9 +310,11 @@ __device__ __forceinline__ uint32_t e2m1_exact_sr(float x, float s, uint32_t r16
 // count is the exact quotient's unless X4 - 4 T_j is -1 or 0 for some j; those values --
 // about one in 10^5 -- take the exact count of thresholds below q (e2m1_exact_sr).  The
 // count from X4 is (X4 + 2^18 - 1 - 4 r16) / 2^18, saturated at 7.
-// Codes and signs are placed with integer multiply-adds (code * 16^e + out), which can
-// run on the FMA pipe next to the ALU work.
-__device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockScale& bs, uint4 rnd) {
+// Codes are placed with integer multiply-adds (code * 16^e + out), which can run on the
+// FMA pipe next to the ALU work; the eight signs come from the BF16 words w (value 2i in
+// the low half of word i) by byte permutes.
+__device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const uint4& words, const BlockScale& bs,
+                                              uint4 rnd) {
   const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
   if (!(bs.s > 0.0f)) return 0u;
   if (!bs.exact_only) {
@@ -303,9 +330,8 @@ __device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockSc
       const uint32_t a = x4 - 4u * r16 + (0x3FFFFu - 0x3F00000u);      // X4 + 2^18 - 1 - 4 r16
       near = min(near, ~a & 0x3FFFEu);                                  // 0: X4 - 4 T_j in {-1, 0}
       out += min(a >> 18, 7u) * (1u << (4 * e));
-      out += (__float_as_uint(f[e]) >> 31) * (8u << (4 * e));
     }
-    out = canonical_zero(out);
+    out = canonical_zero(out | sign_nibbles(words));
     if (near == 0u) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -326,6 +352,11 @@ __device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockSc
 #pragma unroll
   for (int e = 0; e < 8; ++e) out |= e2m1_exact_sr(f[e], bs.s, (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << (4 * e);
   return out;
+}
+
+// The same, for callers that hold only the floats.
+__device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const BlockScale& bs, uint4 rnd) {
+  return e2m1x8_sr(f, bf16_words(f), bs, rnd);
 }
 
 }  // namespace nvfp4

@@ -239,7 +239,7 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, int64_t row, co
       const uint64_t j = a.rng_offset + (uint64_t)(row * a.cols + col) / 8u;
       const uint4 rnd = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), (uint32_t)a.seed,
                                       (uint32_t)(a.seed >> 32));
-      word = e2m1x8_sr(f, bs, rnd);
+      word = e2m1x8_sr(f, q[i], bs, rnd);
     } else {
       word = e2m1x8_rn(f, bs);
     }
@@ -316,13 +316,13 @@ __device__ __forceinline__ void encode_regs(const QuantArgs& a, int64_t row, int
   float h0[8], h1[8];
   bf16x8_to_f32(q0, h0);
   bf16x8_to_f32(q1, h1);
-  const BlockScale bs = block_scale(amax_b >= 0.0f ? amax_b : fmaxf(absmax8(h0), absmax8(h1)), g, six_g);
+  const BlockScale bs = block_scale(amax_b >= 0.0f ? amax_b : absmax16_bf16(q0, q1), g, six_g);
   if (RND == kRoundSR) {
     const uint64_t j = a.rng_offset + (uint64_t)(row * a.cols + blk * 16) / 8u;
     const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
-    codes_out.x = e2m1x8_sr(h0, bs, philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), k0, k1));
-    codes_out.y = e2m1x8_sr(h1, bs, philox4x32_10(make_uint4((uint32_t)(j + 1), (uint32_t)((j + 1) >> 32), 0u, 0u),
-                                                  k0, k1));
+    codes_out.x = e2m1x8_sr(h0, q0, bs, philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), 0u, 0u), k0, k1));
+    codes_out.y = e2m1x8_sr(h1, q1, bs,
+                            philox4x32_10(make_uint4((uint32_t)(j + 1), (uint32_t)((j + 1) >> 32), 0u, 0u), k0, k1));
   } else {
     codes_out = e2m1x16_rn(h0, h1, bs);
   }
@@ -593,7 +593,7 @@ __device__ __forceinline__ void requant_block(const uint4& q0, const uint4& q1, 
   float v0[8], v1[8];
   bf16x8_to_f32(q0, v0);
   bf16x8_to_f32(q1, v1);
-  const BlockScale bs = block_scale(fmaxf(absmax8(v0), absmax8(v1)), g, __fmul_rn(6.0f, g));
+  const BlockScale bs = block_scale(absmax16_bf16(q0, q1), g, __fmul_rn(6.0f, g));
   sf = bs.sf;
   const uint2 c = e2m1x16_rn(v0, v1, bs);
   c0 = c.x;
