@@ -32,22 +32,50 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
   return v;
 }
 
+// BF16 (bits) of the exact product w * d, rounded once to nearest even, in float64: the
+// product of a float32 and a BF16 value has at most 32 significant bits, so it is exact
+// there; it is rounded at the spacing of its BF16 binade (2^-133 below 2^-126, where BF16
+// values are subnormal).  The slow path of bf16_of_product.
+__device__ __noinline__ uint32_t bf16_of_product_f64(float w, float d) {
+  const double x = (double)w * (double)d;
+  const double ax = fabs(x);
+  int ex;
+  frexp(ax, &ex);                                   // ax = m 2^ex, m in [0.5, 1)
+  const int e = max(ex - 1, -126);                  // exponent of the BF16 binade
+  const double r = rint(ldexp(ax, 7 - e));          // ax / spacing, to an integer, ties to even
+  const float rf = (float)ldexp(r, e - 7);          // a BF16 value (or +inf past the range)
+  return ((__float_as_uint(rf) >> 16) & 0x7FFFu) | (x < 0.0 ? 0x8000u : 0u);
+}
+
 // BF16 (bits) of the exact product w * d of a float32 and a BF16 value, rounded once to
-// nearest even.  p = fl32(w d) and the FMA residual e = w d - p (exact) give the exact
-// product p + e.  Rounding p to BF16 is the rounding of p + e unless p sits exactly on a
-// BF16 midpoint (low half 0x8000): no BF16 midpoint lies strictly between p + e and its
-// float32 rounding p, so only there can the side differ, and e's sign decides it.
+// nearest even.  p = fl32(w d) rounded to BF16 is the rounding of the exact product
+// unless p sits exactly on a BF16 midpoint (low half 0x8000): BF16 midpoints are float32
+// values, so none lies strictly between the exact product and its nearest float32 p.  On
+// a midpoint the exact product decides (bf16_of_product_f64; an FMA residual cannot: for
+// products below about 2^-118 it may itself round to zero).
 __device__ __forceinline__ uint32_t bf16_of_product(float w, float d) {
-  const float p = __fmul_rn(w, d);
-  const float e = __fmaf_rn(w, d, -p);
-  const uint32_t b = __float_as_uint(p);
-  if ((b & 0xFFFFu) == 0x8000u && e != 0.0f) {
-    // away from zero iff e has p's sign (|p + e| > |p|); the upper half is the truncation
-    const bool away = (__float_as_uint(e) >> 31) == (b >> 31);
-    return (b >> 16) + (away ? 1u : 0u);
-  }
+  const uint32_t b = __float_as_uint(__fmul_rn(w, d));
+  if ((b & 0xFFFFu) == 0x8000u) return bf16_of_product_f64(w, d);
   const uint32_t lsb = (b >> 16) & 1u;
   return (b + 0x7FFFu + lsb) >> 16;   // round to nearest even (finite inputs)
+}
+
+// The same for two values at once, packed (w d0 in the low half): both float32 products
+// by one paired multiply, both roundings to BF16 by one paired conversion (round to
+// nearest even, subnormals kept); only a product that sits exactly on a BF16 midpoint
+// -- where the float32 rounding may have decided the side -- goes through
+// bf16_of_product.
+__device__ __forceinline__ uint32_t bf16x2_of_products(float w, float d0, float d1) {
+  float p0, p1;
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %4};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(p0), "=f"(p1)
+      : "f"(d0), "f"(d1), "f"(w));
+  if ((__float_as_uint(p0) & 0xFFFFu) == 0x8000u || (__float_as_uint(p1) & 0xFFFFu) == 0x8000u)
+    return bf16_of_product(w, d0) | (bf16_of_product(w, d1) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));   // upper half from p1
+  return r;
 }
 }  // namespace
 
@@ -120,7 +148,7 @@ __global__ void __launch_bounds__(256, 3) combine_backward_kernel(const __nv_bfl
           for (int p = 0; p < 8; ++p) {
             const float d0 = __uint_as_float(dw8[p] << 16), d1 = __uint_as_float(dw8[p] & 0xFFFF0000u);
             const float y0f = __uint_as_float(yw8[p] << 16), y1f = __uint_as_float(yw8[p] & 0xFFFF0000u);
-            o[p] = bf16_of_product(wj, d0) | (bf16_of_product(wj, d1) << 16);
+            o[p] = bf16x2_of_products(wj, d0, d1);
             acc = __fmaf_rn(d0, y0f, acc);
             acc = __fmaf_rn(d1, y1f, acc);
             float* dst = p < 4 ? lo8 : hi8;

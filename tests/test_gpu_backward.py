@@ -35,7 +35,7 @@ def _views(buf, lay, i, n, dtype):
     return buf[lay[i]:lay[i] + nbytes].view(dtype)
 
 
-def _run(lib, shape, seed=0, bwd_seed=123, x_scale=1.0):
+def _run(lib, shape, seed=0, bwd_seed=123, x_scale=1.0, d_scale=1.0):
     x, logits, w13, w2 = S.moe_inputs(shape, seed=seed)
     if x_scale != 1.0:
         x = (x.float() * x_scale).bfloat16()
@@ -47,6 +47,8 @@ def _run(lib, shape, seed=0, bwd_seed=123, x_scale=1.0):
     xc = x.cuda()
     lib.moe_expert_forward(xc, dev(ids), dev(w), pw, workspace=fws)
     dout = S.randn_bf16((T, H), 1e-3, seed=seed + 77)
+    if d_scale != 1.0:
+        dout = (dout.float() * d_scale).bfloat16()
     bws = lib.moe_backward_workspace(T, k, pw, "cuda")
     dx, dw, dw13, dw2 = lib.moe_expert_backward(dout.cuda(), xc, dev(w), pw, pt, fws, seed=bwd_seed, workspace=bws)
     assert lib.nvfp4_status_check() == 0
@@ -54,7 +56,7 @@ def _run(lib, shape, seed=0, bwd_seed=123, x_scale=1.0):
                 dw13=dw13, dw2=dw2, seed=bwd_seed)
 
 
-def _check_backward(lib, shape, r, wgrad_values=True):
+def _check_backward(lib, shape, r, wgrad_values=True, upto_dy_quant=False):
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     Ip = (I + 255) // 256 * 256
     flay = lib.moe_forward_workspace_layout(T, k, E, H, I)
@@ -109,6 +111,8 @@ def _check_backward(lib, shape, r, wgrad_values=True):
     np.testing.assert_array_equal(dyq_c[live], q_dy["codes"][live])
     np.testing.assert_array_equal(dyq_sf[live], q_dy["sf"][live])
     np.testing.assert_array_equal(npy(_views(bws, blay, 2, mcap, torch.float32))[live], q_dy["g"][live])
+    if upto_dy_quant:
+        return
     dh_gpu = u16(_views(bws, blay, 3, mcap * Ip, torch.bfloat16).view(mcap, Ip))[:n]
     dh_ref = M.grouped_gemm(q_dy["codes"], q_dy["sf"], q_dy["g"], w2q_t["codes"], w2q_t["sf"], w2q_t["g"], padded,
                             counts)
@@ -192,6 +196,22 @@ def test_backward_tiny_activations(cuda_lib):
     shape = S.MoEShape("tiny-bwd", T=256, H=256, I=128, E=4, k=2, routing="normal")
     r = _run(cuda_lib, shape, x_scale=2.0 ** -120)
     _check_backward(cuda_lib, shape, r, wgrad_values=False)
+
+
+def test_backward_subnormal_gradients(cuda_lib):
+    """Output gradients scaled by 2^-118 (about 2^-128, float32 subnormals): every
+    product w dout and so every dy = BF16(w dout) is a subnormal, rounded once from the
+    exact product (where the float32 product sits on a BF16 midpoint, an FMA residual
+    would itself underflow); dy and dw, and dy's per-row quantisation (codes, scales and
+    the subnormal global scales), match the oracle bit for bit.  The GEMMs that follow are
+    not compared: the product of dy's global scale (about 2^-139) and the weights' is
+    below the float32 range of the GEMM epilogue's scale, while the float64 reference
+    keeps it (as in test_backward_tiny_activations)."""
+    shape = S.MoEShape("tiny-bwd", T=256, H=256, I=128, E=4, k=2, routing="normal")
+    r = _run(cuda_lib, shape, d_scale=2.0 ** -118)
+    d = S.bf16_bits(r["dout"])
+    assert np.any((d & 0x7F80) == 0) and np.any(d & 0x7FFF), "subnormal gradients"
+    _check_backward(cuda_lib, shape, r, upto_dy_quant=True)
 
 
 def test_backward_is_deterministic_and_seeded(cuda_lib):
