@@ -123,7 +123,10 @@ def _swiglu_hard_pairs(n_random=8_000_000, seed=11):
     (b) gate in [8, 48] with gate*up exactly a midpoint, where silu(gate)*up sits just
         below it by exp(-gate) (the float64 reference ties to even once 1 + exp(-gate)
         rounds to 1, above gate = 36.74);
-    (c) range edges: |gate| near and beyond 80, tiny and huge products."""
+    (c) range edges: |gate| near and beyond 80, tiny and huge products;
+    (d) family (b) with up scaled by 2^-118 .. 2^-132: products at the bottom of the
+        float32 normal range and below it (BF16 subnormals), where the residual of a
+        float32 product can itself underflow."""
     rng = np.random.default_rng(seed)
     bf = lambda v: F.bf16_to_f32(F.bf16_round(v)).astype(np.float64)  # noqa: E731
     g = bf(rng.standard_normal(n_random) * rng.choice([0.05, 0.3, 1, 4, 20], n_random))
@@ -145,7 +148,16 @@ def _swiglu_hard_pairs(n_random=8_000_000, seed=11):
                       16.5, -17, 24, -30, 1e-39, -3e-40, 2e-41, 1.2e-38, -5e-39, 3e-30]))
     uc = bf(np.array([1.5, -3, 1e30, 2e-30, 1e38, -1e37, 1e35, 7e38, 1e-30, 1e25, 5e-39, 1.0, 1e20, 1e-10, 3e33,
                       -2e-35, 3.0, -1e10, 7.0, 2e20, 1e30, -3e35, 1e38, 2e25, 7e33, 1e30]))
-    return np.concatenate([ga, gb, gc]), np.concatenate([ua, ub, uc]), (ga.size, gb.size)
+    gd, ud = [], []
+    for sc in (-118, -124, -128, -132):
+        U4 = bf(us * 2.0 ** sc)
+        G4, U4 = (a.ravel() for a in np.meshgrid(gs, U4))
+        p4 = (G4.astype(np.float32) * U4.astype(np.float32)).view(np.uint32)
+        idx = np.flatnonzero((p4 & 0xFFFF) == 0x8000)
+        idx = idx[rng.permutation(idx.size)[:5000]]
+        gd.append(G4[idx])
+        ud.append(U4[idx])
+    return (np.concatenate([ga, gb, gc] + gd), np.concatenate([ua, ub, uc] + ud), (ga.size, gb.size))
 
 
 def test_swiglu_hard_cases_bit_exact(cuda_lib):
