@@ -115,6 +115,21 @@ template <bool kPair>
 constexpr size_t smem_bytes() { return sizeof(Smem<kPair>) + 1024; }
 }  // namespace gt
 
+// BF16 pair (a s in the low half, b s in the high half) of two accumulator values scaled
+// by s: both IEEE products by one paired multiply, both roundings by one paired
+// conversion (round to nearest even) -- the same bits as two multiplies and a
+// __floats2bfloat162_rn.
+__device__ __forceinline__ uint32_t bf16x2_scaled(uint32_t a, uint32_t b, float s) {
+  float pa, pb;
+  asm("{\n .reg .b64 x, y, d;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %4};\n"
+      " mul.rn.f32x2 d, x, y;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(pa), "=f"(pb)
+      : "r"(a), "r"(b), "f"(s));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(pb), "f"(pa));
+  return r;
+}
+
 // One lane's 128-byte row of a warp's 32-row output box, written 128-byte swizzled (16-byte
 // chunk j at (j ^ (row % 8)) * 16, the TMA SWIZZLE_128B image), then one TMA store of the
 // box at column x, row y.  The buffer is reused only after the previous store read it.
@@ -638,8 +653,9 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
           if (hmax != 0u) atomicMax(g.h_amax + row, hmax << 16);
         }
       } else if (!g.out_f32) {
-        // BF16: each pair of 32-column chunks is packed as soon as it is loaded, so at most
-        // 64 accumulator values are live next to the 64 packed words
+        // BF16: each pair of 32-column chunks is packed as soon as it is loaded (one paired
+        // multiply and one paired conversion per column pair), so at most 64 accumulator
+        // values are live next to the 64 packed words
         uint32_t w[2][32];
 #pragma unroll
         for (int b2 = 0; b2 < 2; ++b2) {
@@ -650,11 +666,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
 #pragma unroll
-            for (int p = 0; p < 16; ++p) {
-              const __nv_bfloat162 pr = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][2 * p]), scale),
-                                                              __fmul_rn(__uint_as_float(v[c][2 * p + 1]), scale));
-              w[b2][16 * c + p] = *reinterpret_cast<const uint32_t*>(&pr);
-            }
+            for (int p = 0; p < 16; ++p) w[b2][16 * c + p] = bf16x2_scaled(v[c][2 * p], v[c][2 * p + 1], scale);
           }
         }
         release_acc();
