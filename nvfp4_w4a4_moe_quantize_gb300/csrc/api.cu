@@ -558,7 +558,9 @@ nvfp4_status moe_route_topk(const float* logits, int64_t T, int32_t E, int32_t k
   if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > 32 || k > E) return NVFP4_ERR_INVALID_ARG;
   if (T == 0) return NVFP4_OK;
   if (!logits || !ids || !weights) return NVFP4_ERR_INVALID_ARG;
-  return from_cuda(launch_route_topk(logits, T, E, k, renormalize, ids, weights, static_cast<cudaStream_t>(stream)));
+  // decode-size batches: a programmatic dependent launch (as the expert block's kernels)
+  return from_cuda(launch_route_topk(logits, T, E, k, renormalize, ids, weights, static_cast<cudaStream_t>(stream),
+                                     T * k <= 1024));
 }
 
 nvfp4_status moe_permute(const int32_t* ids, int64_t T, int32_t k, int32_t E, int32_t* counts, int32_t* offsets,
@@ -691,7 +693,10 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   float* gx = reinterpret_cast<float*>(xq + align256(tiled_bytes(T, H, 128)));
   uint32_t* h_amax = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(gx) + align256(sizeof(float) * T));
   cudaError_t e;
-  if (T * k <= 1024 && E <= 1024) {
+  // decode-size batches: one prologue launch, and every kernel of the chain a programmatic
+  // dependent launch (its launch overlaps the previous kernel's tail)
+  const bool small = T * k <= 1024 && E <= 1024;
+  if (small) {
     // 1-2. decode-size batches: grouping, per-token NVFP4 of x and its placement in every
     //      routed slot in one launch (one CTA per token)
     e = launch_prologue_small(ids, T, k, E, counts, offsets, padded, inv, perm, status, x, H, aq, ga, h_amax, s);
@@ -744,12 +749,12 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   if (!make_map(&mh, hbuf, mcap, I, I * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64) ||
       !make_map(&my, ybuf, mcap, H, H * 2, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2))
     return NVFP4_ERR_CUDA;
-  e = launch_grouped_gemm_tiled(aq, wt->w13, mh, g1, mcap / 128, true, s);
+  e = launch_grouped_gemm_tiled(aq, wt->w13, mh, g1, mcap / 128, true, s, small);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
   // 4. per-row NVFP4 of h (routed rows only), K zero-padded to Ip, GEMM-tiled, with the
   //    row maxima the epilogue gathered
-  e = launch_requant_tiled(hbuf, h_amax, perm, padded + E, mcap, I, Ip, hq, gh, s);
+  e = launch_requant_tiled(hbuf, h_amax, perm, padded + E, mcap, I, Ip, hq, gh, s, small);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
   // 5. down GEMM -> y (BF16)
@@ -766,11 +771,11 @@ nvfp4_status moe_expert_forward(const void* x, const int32_t* ids, const float* 
   g2.ldd = H;
   g2.out_f32 = 0;
   g2.status = status;
-  e = launch_grouped_gemm_tiled(hq, wt->w2, my, g2, mcap / 128, false, s);
+  e = launch_grouped_gemm_tiled(hq, wt->w2, my, g2, mcap / 128, false, s, small);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
   // 6. weighted un-permute
-  return from_cuda(launch_combine(ybuf, inv, w, T, k, H, out, s));
+  return from_cuda(launch_combine(ybuf, inv, w, T, k, H, out, s, small));
 }
 
 nvfp4_status moe_weights_t_sizes(int32_t E, int64_t H, int64_t I, size_t sizes_out[4]) {

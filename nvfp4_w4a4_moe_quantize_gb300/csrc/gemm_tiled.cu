@@ -43,6 +43,7 @@
 
 #include "group.cuh"
 #include "launch.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "swiglu.cuh"
 #include "tiled.cuh"
@@ -231,6 +232,7 @@ template <int kMode, bool kPair>
 __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
     grouped_gemm_tiled_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B,
                               const __grid_constant__ CUtensorMap tmd, const GemmArgs g) {
+  grid_dep_sync();
   using namespace gt;
   using L = Layout<kPair>;
   constexpr int kStages = L::kStages;
@@ -731,7 +733,7 @@ __global__ void __launch_bounds__(gt::threads(kMode == 1, kPair), 1)
 
 template <int kMode>
 static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
-                                int64_t tiles, cudaStream_t s) {
+                                int64_t tiles, cudaStream_t s, bool pdl = false) {
   if (kMode == 1 && g.silu_tab == nullptr) return cudaErrorInvalidValue;
   static std::atomic<bool> attr_set[64];   // the attribute is set once per device
   cudaError_t err = set_smem_attr_once(attr_set, (const void*)grouped_gemm_tiled_kernel<kMode, false>,
@@ -740,9 +742,8 @@ static cudaError_t launch_tiled(const uint8_t* A, const uint8_t* B, const CUtens
   if (tiles == 0) return cudaSuccess;
   int grid = num_sms();
   if (tiles < grid) grid = (int)tiles;
-  grouped_gemm_tiled_kernel<kMode, false>
-      <<<grid, gt::threads(kMode == 1, false), gt::smem_bytes<false>(), s>>>(A, B, tmd, g);
-  return cudaGetLastError();
+  return launch_pdl(pdl, grouped_gemm_tiled_kernel<kMode, false>, dim3((unsigned)grid), dim3(gt::threads(kMode == 1, false)),
+                    gt::smem_bytes<false>(), s, A, B, tmd, g);
 }
 
 // CTA-pair launch: clusters of two CTAs, as many clusters as fit on the device at once
@@ -791,11 +792,11 @@ static bool pair_enabled() {
 }
 
 cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
-                                      int64_t max_m_tiles, bool swiglu, cudaStream_t s) {
+                                      int64_t max_m_tiles, bool swiglu, cudaStream_t s, bool pdl) {
   const int64_t tiles = max_m_tiles * (g.N / gt::kBN);
   if (pair_enabled())
     return swiglu ? launch_pair<1>(A, B, tmd, g, tiles, s) : launch_pair<0>(A, B, tmd, g, tiles, s);
-  return swiglu ? launch_tiled<1>(A, B, tmd, g, tiles, s) : launch_tiled<0>(A, B, tmd, g, tiles, s);
+  return swiglu ? launch_tiled<1>(A, B, tmd, g, tiles, s, pdl) : launch_tiled<0>(A, B, tmd, g, tiles, s, pdl);
 }
 
 cudaError_t launch_grouped_gemm_ragged_k(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd,

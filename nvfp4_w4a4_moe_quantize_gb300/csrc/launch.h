@@ -118,7 +118,7 @@ cudaError_t launch_mx_dequantize(const uint8_t* codes, const uint8_t* sf, int64_
 // tmd: tensor map of the output, 32-row boxes: D with 128-byte boxes (128-byte swizzle),
 // or h [M_total, N/2] BF16 with 64-byte boxes (64-byte swizzle).
 cudaError_t launch_grouped_gemm_tiled(const uint8_t* A, const uint8_t* B, const CUtensorMap& tmd, const GemmArgs& g,
-                                      int64_t max_m_tiles, bool swiglu, cudaStream_t s);
+                                      int64_t max_m_tiles, bool swiglu, cudaStream_t s, bool pdl = false);
 int tiled_max_experts();
 // The same kernel over ragged K per expert (the weight-gradient GEMMs): g.offsets = the
 // K-block prefix sums kofs [E+1], g.m_rows rows of A and D per expert, g.ga / g.gb one
@@ -164,12 +164,14 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* sf, const flo
                               int mode, int64_t group_rows, void* out, bool out_f32, int64_t ldo, cudaStream_t s);
 cudaError_t launch_requant_tiled(const __nv_bfloat16* h, const uint32_t* amax_bits, const int32_t* perm,
                                  const int32_t* n_rows_dev, int64_t max_rows, int64_t I, int64_t Ip, uint8_t* out,
-                                 float* g_out, cudaStream_t s);
+                                 float* g_out, cudaStream_t s, bool pdl = false);
 cudaError_t launch_pack_tiled(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K, int R,
                               uint8_t* out, cudaStream_t s);
 
+// pdl (here and in the launchers below): a programmatic dependent launch (pdl.cuh), for
+// decode-size batches.
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renorm, int32_t* ids,
-                              float* w, cudaStream_t s);
+                              float* w, cudaStream_t s, bool pdl = false);
 // The forward's prologue for T*k <= 1024: the permutation (as launch_permute), each
 // token's row of x quantised per row (RNE) straight into its k slots of the GEMM-tiled aq
 // (128-row blocks, K = H), ga[slot] = the token's global scale, h_amax[slot] = 0.
@@ -181,7 +183,7 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t*
                            int32_t* padded, int32_t* inv, int32_t* perm, int32_t* hist, int64_t nchunks,
                            int* status, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int64_t T, int k, int64_t H,
-                           void* out, cudaStream_t s);
+                           void* out, cudaStream_t s, bool pdl = false);
 // SwiGLU backward: [dgate | dup] (BF16 [rows, 2I]) from [gate | up] (BF16 [rows, 2I]) and dh
 // (BF16 [rows, I]); I % 8 == 0.
 // gu_interleaved: gu holds gate/up in the 64-chunk interleave of the prepared W13;

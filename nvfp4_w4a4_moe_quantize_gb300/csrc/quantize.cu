@@ -17,6 +17,7 @@
 
 #include "encode.cuh"
 #include "launch.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "status.cuh"
 #include "tiled.cuh"
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(256) quantize_known_coalesced_kernel(QuantArgs
 
 template <int RND>
 __global__ void __launch_bounds__(kQWarps * 32, 3) quantize_rows_stream_kernel(QuantArgs a) {
+  grid_dep_sync();
   extern __shared__ __align__(128) uint8_t qsm[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t warp = (int64_t)blockIdx.x * kQWarps + wib;
@@ -608,6 +610,7 @@ __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16*
                                                             const int32_t* __restrict__ n_rows_dev, int64_t max_rows,
                                                             int64_t I, int64_t Ip, uint8_t* __restrict__ out,
                                                             float* __restrict__ g_out) {
+  grid_dep_sync();
   const int lane = threadIdx.x & 31;
   int64_t rows = *n_rows_dev;
   if (rows > max_rows) rows = max_rows;
@@ -655,19 +658,17 @@ __global__ void __launch_bounds__(256) requant_tiled_kernel(const __nv_bfloat16*
 
 cudaError_t launch_requant_tiled(const __nv_bfloat16* h, const uint32_t* amax_bits, const int32_t* perm,
                                  const int32_t* n_rows_dev, int64_t max_rows, int64_t I, int64_t Ip, uint8_t* out,
-                                 float* g_out, cudaStream_t s) {
+                                 float* g_out, cudaStream_t s, bool pdl) {
   const int64_t total = max_rows * (Ip / 32);
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
   // 32-bit index arithmetic when the units and the output's bytes all fit
   if (total < ((int64_t)1 << 31) && tiled_bytes(max_rows, Ip, 128) < ((int64_t)1 << 31))
-    requant_tiled_kernel<uint32_t><<<(int)blocks, 256, 0, s>>>(h, amax_bits, perm, n_rows_dev, max_rows, I, Ip, out,
-                                                               g_out);
-  else
-    requant_tiled_kernel<int64_t><<<(int)blocks, 256, 0, s>>>(h, amax_bits, perm, n_rows_dev, max_rows, I, Ip, out,
-                                                              g_out);
-  return cudaGetLastError();
+    return launch_pdl(pdl, requant_tiled_kernel<uint32_t>, dim3((unsigned)blocks), dim3(256), 0, s, h, amax_bits, perm,
+                      n_rows_dev, max_rows, I, Ip, out, g_out);
+  return launch_pdl(pdl, requant_tiled_kernel<int64_t>, dim3((unsigned)blocks), dim3(256), 0, s, h, amax_bits, perm,
+                    n_rows_dev, max_rows, I, Ip, out, g_out);
 }
 
 template <int RND>
@@ -690,8 +691,7 @@ static cudaError_t launch_stream(const QuantArgs& a, int grid, size_t smem, cuda
     const cudaError_t err = set_smem_attr_once(attr_set, (const void*)quantize_rows_stream_kernel<RND>, (int)kQSmemMax + 4096);
     if (err != cudaSuccess) return err;
   }
-  quantize_rows_stream_kernel<RND><<<grid, kQWarps * 32, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(false, quantize_rows_stream_kernel<RND>, dim3((unsigned)grid), dim3(kQWarps * 32), smem, s, a);
 }
 
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t group_rows,

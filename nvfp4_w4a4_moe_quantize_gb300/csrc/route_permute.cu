@@ -12,6 +12,7 @@
 
 #include "encode.cuh"
 #include "launch.h"
+#include "pdl.cuh"
 #include "status.cuh"
 #include "tiled.cuh"
 
@@ -38,6 +39,7 @@ template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
                                                          int renorm, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
+  grid_dep_sync();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t nwarp = (int64_t)gridDim.x * 8;
@@ -123,6 +125,7 @@ template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_sorted_kernel(const float* __restrict__ logits, int64_t T, int E,
                                                                 int k, int renorm, int32_t* __restrict__ ids,
                                                                 float* __restrict__ w) {
+  grid_dep_sync();
   static_assert(EPL == 1 || EPL == 2 || EPL == 4, "lists of 1, 2 or 4");
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -190,23 +193,25 @@ __global__ void __launch_bounds__(256) route_topk_sorted_kernel(const float* __r
 }
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renorm, int32_t* ids, float* w,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
   int64_t blocks = (T + 7) / 8;
   if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
   const int epl = (E + 31) / 32;
-#define NVFP4_ROUTE(N) route_topk_kernel<N><<<(int)blocks, 256, 0, s>>>(logits, T, E, k, renorm, ids, w)
+#define NVFP4_ROUTE(N) \
+  launch_pdl(pdl, route_topk_kernel<N>, dim3((unsigned)blocks), dim3(256), 0, s, logits, T, E, k, renorm, ids, w)
 #define NVFP4_ROUTE_SORTED(N) \
-  route_topk_sorted_kernel<N><<<(int)blocks, 256, 0, s>>>(logits, T, E, k, renorm, ids, w)
-  if (epl <= 1) NVFP4_ROUTE_SORTED(1);
-  else if (epl <= 2) NVFP4_ROUTE_SORTED(2);
-  else if (epl <= 4) NVFP4_ROUTE_SORTED(4);
-  else if (epl <= 8) NVFP4_ROUTE(8);
-  else if (epl <= 16) NVFP4_ROUTE(16);
-  else NVFP4_ROUTE(32);
+  launch_pdl(pdl, route_topk_sorted_kernel<N>, dim3((unsigned)blocks), dim3(256), 0, s, logits, T, E, k, renorm, ids, w)
+  cudaError_t err;
+  if (epl <= 1) err = NVFP4_ROUTE_SORTED(1);
+  else if (epl <= 2) err = NVFP4_ROUTE_SORTED(2);
+  else if (epl <= 4) err = NVFP4_ROUTE_SORTED(4);
+  else if (epl <= 8) err = NVFP4_ROUTE(8);
+  else if (epl <= 16) err = NVFP4_ROUTE(16);
+  else err = NVFP4_ROUTE(32);
 #undef NVFP4_ROUTE
 #undef NVFP4_ROUTE_SORTED
-  return cudaGetLastError();
+  return err;
 }
 
 // ------------------------------------------------------------------ expert grouping
@@ -220,6 +225,7 @@ constexpr int kPermuteSteps = kPermuteChunk / 32;
 __global__ void __launch_bounds__(256) permute_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int E,
                                                            int64_t nchunks, int32_t* __restrict__ hist,
                                                            int* status) {
+  grid_dep_sync();
   extern __shared__ int32_t sh[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   if (blockIdx.x == 0 && threadIdx.x == 0) hist[(int64_t)E * nchunks] = 0;
@@ -259,6 +265,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
                                                             int32_t* __restrict__ offsets,
                                                             int32_t* __restrict__ padded,
                                                             int32_t* __restrict__ perm) {
+  grid_dep_sync();
   __shared__ int32_t s_cnt[1024];
   __shared__ int32_t s_pad[1025];
   __shared__ int32_t s_wsum[2][32];
@@ -369,6 +376,7 @@ __global__ void __launch_bounds__(256) permute_rank_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ hist,
                                                            const int32_t* __restrict__ padded,
                                                            int32_t* __restrict__ inv, int32_t* __restrict__ perm) {
+  grid_dep_sync();
   extern __shared__ int32_t sh[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   int32_t* s_pad = sh;                 // E
@@ -503,6 +511,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
                                                              int32_t* __restrict__ padded,
                                                              int32_t* __restrict__ inv, int32_t* __restrict__ perm,
                                                              int* status) {
+  grid_dep_sync();
   __shared__ PermuteSmem sm;
   permute_small_block(ids, n, k, E, true, counts, offsets, padded, inv, perm, status, sm);
 }
@@ -520,6 +529,7 @@ __global__ void __launch_bounds__(1024) moe_prologue_small_kernel(
     int32_t* __restrict__ offsets, int32_t* __restrict__ padded, int32_t* __restrict__ inv,
     int32_t* __restrict__ perm, int* status, const __nv_bfloat16* __restrict__ x, int64_t H, uint8_t* aq,
     float* __restrict__ ga, uint32_t* __restrict__ h_amax) {
+  grid_dep_sync();
   __shared__ PermuteSmem sm;
   permute_small_block(ids, n, k, E, blockIdx.x == 0, counts, offsets, padded, inv, perm, status, sm);
   __syncthreads();
@@ -596,9 +606,8 @@ cudaError_t launch_prologue_small(const int32_t* ids, int64_t T, int k, int E, i
                                   uint8_t* aq, float* ga, uint32_t* h_amax, cudaStream_t s) {
   if (T * k > 1024 || E > 1024 || H % 256 != 0 || H > 2048) return cudaErrorInvalidValue;
   if (T == 0) return cudaSuccess;
-  moe_prologue_small_kernel<<<(int)T, 1024, 0, s>>>(ids, (int)(T * k), k, E, counts, offsets, padded, inv, perm,
-                                                     status, static_cast<const __nv_bfloat16*>(x), H, aq, ga, h_amax);
-  return cudaGetLastError();
+  return launch_pdl(true, moe_prologue_small_kernel, dim3((unsigned)T), dim3(1024), 0, s, ids, (int)(T * k), k, E, counts,
+                    offsets, padded, inv, perm, status, static_cast<const __nv_bfloat16*>(x), H, aq, ga, h_amax);
 }
 
 cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
@@ -606,24 +615,21 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t*
                            int* status, cudaStream_t s) {
   const int64_t n = T * k;
   if (n > 0 && n <= 1024 && E <= 1024) {
-    permute_small_kernel<<<1, 1024, 0, s>>>(ids, (int)n, k, E, counts, offsets, padded, inv, perm, status);
-    return cudaGetLastError();
+    return launch_pdl(false, permute_small_kernel, dim3(1), dim3(1024), 0, s, ids, (int)n, k, E, counts, offsets, padded, inv,
+                      perm, status);
   }
   const int blocks = (int)((nchunks + 7) / 8);
   if (nchunks > 0) {
-    permute_hist_kernel<<<blocks, 256, 8 * E * sizeof(int32_t), s>>>(ids, n, E, nchunks, hist, status);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(false, permute_hist_kernel, dim3(blocks), dim3(256), 8 * E * sizeof(int32_t), s, ids, n, E,
+                                 nchunks, hist, status);
     if (err != cudaSuccess) return err;
   }
-  if (nchunks == 0) {   // no entries: the scan still writes counts / offsets (one block)
-    permute_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, E, counts, offsets, padded, perm);
-  } else {
-    permute_scan_kernel<<<(E + 31) / 32, 1024, 0, s>>>(hist, nchunks, E, counts, offsets, padded, perm);
-  }
-  cudaError_t err = cudaGetLastError();
+  // no entries: the scan still writes counts / offsets (one block)
+  cudaError_t err = launch_pdl(false, permute_scan_kernel, dim3(nchunks == 0 ? 1u : (unsigned)((E + 31) / 32)), dim3(1024), 0,
+                               s, hist, nchunks, E, counts, offsets, padded, perm);
   if (err != cudaSuccess || nchunks == 0) return err;
-  permute_rank_kernel<<<blocks, 256, 9 * E * sizeof(int32_t), s>>>(ids, n, k, E, nchunks, hist, padded, inv, perm);
-  return cudaGetLastError();
+  return launch_pdl(false, permute_rank_kernel, dim3(blocks), dim3(256), 9 * E * sizeof(int32_t), s, ids, n, k, E, nchunks,
+                    hist, padded, inv, perm);
 }
 
 // ------------------------------------------------------------------ weighted un-permute
@@ -638,6 +644,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int64_t T, int k, int64_t H,
                                                       __nv_bfloat16* __restrict__ out) {
+  grid_dep_sync();
   // one warp per (token, 256-column chunk): small batches still spread over the GPU
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -701,15 +708,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int64_t T, int k, int64_t H, void* out,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
   int64_t blocks = (T * ((H + 255) / 256) + 7) / 8;
   if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
   const auto* yp = static_cast<const __nv_bfloat16*>(y);
   auto* op = static_cast<__nv_bfloat16*>(out);
-  if (k <= 8) combine_kernel<8><<<(int)blocks, 256, 0, s>>>(yp, inv, w, T, k, H, op);
-  else combine_kernel<0><<<(int)blocks, 256, 0, s>>>(yp, inv, w, T, k, H, op);
-  return cudaGetLastError();
+  return k <= 8 ? launch_pdl(pdl, combine_kernel<8>, dim3((unsigned)blocks), dim3(256), 0, s, yp, inv, w, T, k, H, op)
+                : launch_pdl(pdl, combine_kernel<0>, dim3((unsigned)blocks), dim3(256), 0, s, yp, inv, w, T, k, H, op);
 }
 
 }  // namespace nvfp4

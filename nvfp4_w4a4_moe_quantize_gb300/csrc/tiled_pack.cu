@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "tiled.cuh"
 
@@ -50,6 +51,7 @@ __global__ void __launch_bounds__(32) gather_tiled_kernel(const uint8_t* __restr
                                                           int64_t kblocks, uint8_t* __restrict__ dst,
                                                           float* __restrict__ dst_g,
                                                           uint32_t* __restrict__ amax_zero) {
+  grid_dep_sync();
   constexpr int R = 128;
   constexpr int64_t kChunk = R * 144;
   extern __shared__ __align__(128) uint8_t gsm[];
@@ -125,9 +127,8 @@ cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const in
   // one warp per block and one 18 KB chunk image per warp: 12 per SM fit in shared memory
   int64_t blocks = chunks;
   if (blocks > 12 * (int64_t)num_sms()) blocks = 12 * (int64_t)num_sms();
-  gather_tiled_kernel<<<(int)blocks, 32, kSmem, s>>>(src, src_g, perm, n_rows_dev, max_rows, K / 256, dst, dst_g,
-                                                     amax_zero);
-  return cudaGetLastError();
+  return launch_pdl(false, gather_tiled_kernel, dim3((unsigned)blocks), dim3(32), kSmem, s, src, src_g, perm, n_rows_dev,
+                    max_rows, K / 256, dst, dst_g, amax_zero);
 }
 
 // out[b*C + c, r] = x[b*R + r, c] for `batches` stacked [R, C] BF16 matrices (pitch ld):
