@@ -36,6 +36,7 @@
 //               partial tile is stored row by row, so rows outside the groups are never
 //               written.
 // Tiles are (128-row block) x (256 columns), row-block-major; no split-K, fixed K order.
+#include <cstddef>
 #include <cstdlib>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -92,7 +93,7 @@ struct Layout {
 template <bool kPair>
 struct Smem {
   uint8_t stage[Layout<kPair>::kStages][Layout<kPair>::kStageBytes];
-  uint8_t out[kOutBytes];
+  uint8_t out[kOutBytes];     // TMA store boxes: 1024-byte aligned (128-byte swizzle), as the stages
   uint64_t full[Layout<kPair>::kStages];
   uint64_t empty[Layout<kPair>::kStages];
   uint64_t sfull[Layout<kPair>::kStages];     // the stage's scale bytes have landed
@@ -112,6 +113,8 @@ static_assert(Layout<false>::kStageBytes % 1024 == 0 && Layout<true>::kStageByte
 static_assert(kSFCol0 + Layout<false>::kStages * kSFStageCols <= kTmemCols, "TMEM budget");
 static_assert(kSFCol0 + Layout<true>::kStages * kSFStageCols <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Smem<false>) + 1024 <= 232448 && sizeof(Smem<true>) + 1024 <= 232448, "shared memory budget");
+static_assert(offsetof(Smem<false>, out) % 1024 == 0 && offsetof(Smem<true>, out) % 1024 == 0,
+              "TMA store boxes 1024-byte aligned");
 template <bool kPair>
 constexpr size_t smem_bytes() { return sizeof(Smem<kPair>) + 1024; }
 }  // namespace gt
