@@ -217,10 +217,30 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float (&f)[8], const BlockSc
   return out;
 }
 
+// The exact path of a whole block (scales below 2^-60), out of line; the values are
+// rebuilt from their BF16 words.
+static __device__ __noinline__ uint2 e2m1x16_rn_exact_w(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t w4,
+                                                       uint32_t w5, uint32_t w6, uint32_t w7, float s) {
+  const uint32_t wv[8] = {w0, w1, w2, w3, w4, w5, w6, w7};
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float fe = __uint_as_float((e & 1) ? (wv[e >> 1] & 0xFFFF0000u) : (wv[e >> 1] << 16));
+    const uint32_t c = e2m1_exact_rn(fe, s);
+    if (e < 8) lo |= c << (4 * e); else hi |= c << (4 * (e - 8));
+  }
+  return make_uint2(lo, hi);
+}
+__device__ __forceinline__ uint2 e2m1x16_rn_exact(const float (&h0)[8], const float (&h1)[8], float s) {
+  const auto pk = [](float a, float b) { return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632); };
+  return e2m1x16_rn_exact_w(pk(h0[0], h0[1]), pk(h0[2], h0[3]), pk(h0[4], h0[5]), pk(h0[6], h0[7]), pk(h1[0], h1[1]),
+                            pk(h1[2], h1[3]), pk(h1[4], h1[5]), pk(h1[6], h1[7]), s);
+}
+
 // One whole 16-value block (h0: values 0..7, h1: values 8..15) -> its 16 codes (x: 0..7,
 // y: 8..15), as e2m1x8_rn on both halves but with one settling loop for the block.
 __device__ __forceinline__ uint2 e2m1x16_rn(const float (&h0)[8], const float (&h1)[8], const BlockScale& bs) {
-  if (bs.exact_only) return make_uint2(e2m1x8_rn(h0, bs), e2m1x8_rn(h1, bs));
+  if (bs.exact_only) return e2m1x16_rn_exact(h0, h1, bs.s);
   float vl[8], vh[8];
   scale8(h0, bs.r_lo, vl);
   scale8(h0, bs.r_hi, vh);
@@ -254,8 +274,8 @@ __device__ __forceinline__ uint32_t sign_nibbles(const uint4& w) {
   return (__byte_perm(lo, hi, 0x6420) & 0x08080808u) | (__byte_perm(lo, hi, 0x7531) & 0x80808080u);
 }
 
-// The words of 8 floats as BF16 pairs (value 2i in the low half of word i); only the
-// sign bits are used, so the floats need not be BF16 values.
+// The words of 8 floats that hold BF16 values, as BF16 pairs (value 2i in the low half of
+// word i).
 __device__ __forceinline__ uint4 bf16_words(const float (&f)[8]) {
   const auto hi16 = [](float a, float b) { return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632); };
   return make_uint4(hi16(f[0], f[1]), hi16(f[2], f[3]), hi16(f[4], f[5]), hi16(f[6], f[7]));
@@ -297,6 +317,42 @@ __device__ __forceinline__ uint32_t e2m1_exact_sr(float x, float s, uint32_t r16
   return c | ((__float_as_uint(x) >> 31) && c ? 8u : 0u);
 }
 
+// The rare paths of e2m1x8_sr, out of line (kept inline, they doubled the hot loop's code:
+// measured, instruction-cache misses were the second stall reason of the SR quantiser, and
+// out of line the row quantiser runs 52 instead of 61 us): the values are rebuilt from the
+// BF16 words.  _settle: the exact stochastic rounding of every value whose grid
+// coordinate sits within one unit of a threshold; _exact: every value (scales below 2^-60).
+static __device__ __noinline__ uint32_t e2m1x8_sr_settle(uint4 words, float r, float s, uint4 rnd, uint32_t out) {
+  const uint32_t wv[4] = {words.x, words.y, words.z, words.w};
+  const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float fe = __uint_as_float((e & 1) ? (wv[e >> 1] & 0xFFFF0000u) : (wv[e >> 1] << 16));
+    const uint32_t vb = __float_as_uint(__fmul_rn(fabsf(fe), r));
+    const uint32_t lin = __float_as_uint(__fmaf_rd(__uint_as_float(vb), 0x1p-124f, 0x1.ep-120f));
+    const uint32_t x4 = vb < 0x3F800000u ? lin : (vb >> 4);
+    const uint32_t r16 = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+    const uint32_t a = x4 - 4u * r16 + (0x3FFFFu - 0x3F00000u);
+    if ((~a & 0x3FFFEu) == 0u) {
+      const uint32_t c = e2m1_exact_sr(fe, s, r16);
+      out = (out & ~(0xFu << (4 * e))) | (c << (4 * e));
+    }
+  }
+  return out;
+}
+
+static __device__ __noinline__ uint32_t e2m1x8_sr_exact(uint4 words, float s, uint4 rnd) {
+  const uint32_t wv[4] = {words.x, words.y, words.z, words.w};
+  const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+  uint32_t out = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float fe = __uint_as_float((e & 1) ? (wv[e >> 1] & 0xFFFF0000u) : (wv[e >> 1] << 16));
+    out |= e2m1_exact_sr(fe, s, (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << (4 * e);
+  }
+  return out;
+}
+
 // 8 values of one chunk with their Philox block output -> packed codes of the
 // stochastically rounded exact quotients.  One product v = |x| r per value (|v/q - 1| <=
 // 2^-21 for the exact quotient q = |x|/s).  The rounding counts the thresholds
@@ -332,26 +388,10 @@ __device__ __forceinline__ uint32_t e2m1x8_sr(const float (&f)[8], const uint4& 
       out += min(a >> 18, 7u) * (1u << (4 * e));
     }
     out = canonical_zero(out | sign_nibbles(words));
-    if (near == 0u) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t vb = __float_as_uint(__fmul_rn(fabsf(f[e]), bs.r));
-        const uint32_t lin = __float_as_uint(__fmaf_rd(__uint_as_float(vb), 0x1p-124f, 0x1.ep-120f));
-        const uint32_t x4 = vb < 0x3F800000u ? lin : (vb >> 4);
-        const uint32_t r16 = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-        const uint32_t a = x4 - 4u * r16 + (0x3FFFFu - 0x3F00000u);
-        if ((~a & 0x3FFFEu) == 0u) {
-          const uint32_t c = e2m1_exact_sr(f[e], bs.s, r16);
-          out = (out & ~(0xFu << (4 * e))) | (c << (4 * e));
-        }
-      }
-    }
+    if (near == 0u) out = e2m1x8_sr_settle(words, bs.r, bs.s, rnd, out);
     return out;
   }
-  uint32_t out = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) out |= e2m1_exact_sr(f[e], bs.s, (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << (4 * e);
-  return out;
+  return e2m1x8_sr_exact(words, bs.s, rnd);
 }
 
 // The same, for callers that hold only the floats.
