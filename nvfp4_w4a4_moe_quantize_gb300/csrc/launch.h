@@ -146,12 +146,13 @@ cudaError_t launch_tquant(const void* src, int64_t ld, const int32_t* rowmap, co
                           const uint32_t* amax_bits, float* g_out, uint8_t* out, int rounding, uint64_t seed,
                           int stream_id, int64_t max_kblocks, cudaStream_t s);
 // Slot r (r < min(*n_rows_dev, max_rows), a multiple of 128) of the 128-row-block tiled
-// `dst` gets token perm[r]'s row of the 128-row-block tiled `src` and dst_g[r] = src_g[perm[r]];
-// slots with perm[r] < 0 are not written.  K % 256 == 0.
+// `dst` gets token perm[r]'s row of the row-major per-token operand -- codes `src` [T, K/2],
+// scales `src_sf` [T, K/16], both 16-byte aligned -- and dst_g[r] = src_g[perm[r]]; slots
+// with perm[r] < 0 get zero codes and scales (dst_g[r] is not written).  K % 256 == 0.
 // amax_zero (nullable): amax_zero[r] = 0 for every slot r < min(*n_rows_dev, max_rows).
-cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const int32_t* perm, const int32_t* n_rows_dev,
-                                int64_t max_rows, int64_t K, uint8_t* dst, float* dst_g, uint32_t* amax_zero,
-                                cudaStream_t s);
+cudaError_t launch_gather_tiled(const uint8_t* src, const uint8_t* src_sf, const float* src_g, const int32_t* perm,
+                                const int32_t* n_rows_dev, int64_t max_rows, int64_t K, uint8_t* dst, float* dst_g,
+                                uint32_t* amax_zero, cudaStream_t s);
 // Per-row NVFP4 of h [rows, I] (BF16) whose row maxima |h| are already known (amax_bits,
 // float bits): g[r] = amax / 2688, codes and scales into the GEMM-tiled layout with
 // 128-row blocks and K = Ip (columns I .. Ip-1 zero).  Rows r < min(*n_rows_dev, max_rows)

@@ -35,16 +35,19 @@ __global__ void __launch_bounds__(256) pack_tiled_kernel(const uint8_t* __restri
   }
 }
 
-// Gather of routed rows in the GEMM-tiled layout (128-row blocks): slot r of the
-// expert-grouped order receives token perm[r]'s row of the per-token operand `src` --
-// its codes and scales of every 256-K block -- and its global scale.  Slots with
-// perm[r] < 0 (group padding) get zero codes and scales.  One warp per (128-row block,
-// K block) chunk of the output, assembled in shared memory: asynchronous 16-byte copies
-// move each row's 128 code bytes (8 lanes per row, re-swizzled for the destination row)
-// and 4-byte copies the chunk's 512 scale words, then one bulk store writes the 18 KB
-// image as whole lines.  The per-token operand is small next to L2, so the k-fold reads
-// hit there, and with no register staging each lane keeps its 48 copies in flight.
+// Gather of routed rows into the GEMM-tiled layout (128-row blocks): slot r of the
+// expert-grouped order receives token perm[r]'s row of the per-token operand -- row-major
+// codes `src` [T, K/2] and row-major scales `src_sf` [T, K/16] -- for every 256-K block,
+// and its global scale.  Slots with perm[r] < 0 (group padding) get zero codes and
+// scales.  One warp per (128-row block, K block) chunk of the output, assembled in shared
+// memory: each lane first loads the 16 scale bytes of its four rows (lane + 32 i) into
+// registers, then asynchronous 16-byte copies move each row's 128 code bytes (8 lanes per
+// row, swizzled for the destination row), the scales go to the 128x4 image with four
+// 16-byte shared stores per lane, and one bulk store writes the 18 KB image as whole
+// lines.  The per-token operand is small next to L2, so the k-fold reads hit there; a
+// row's scales of a K block are one 16-byte read.
 __global__ void __launch_bounds__(32) gather_tiled_kernel(const uint8_t* __restrict__ src,
+                                                          const uint8_t* __restrict__ src_sf,
                                                           const float* __restrict__ src_g,
                                                           const int32_t* __restrict__ perm,
                                                           const int32_t* __restrict__ n_rows_dev, int64_t max_rows,
@@ -60,39 +63,47 @@ __global__ void __launch_bounds__(32) gather_tiled_kernel(const uint8_t* __restr
   int64_t rows = *n_rows_dev;
   if (rows > max_rows) rows = max_rows;
   const int64_t chunks = rows / R * kblocks;
+  const int64_t code_row = kblocks * 128, sf_row = kblocks * 16;
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
     const int64_t b = c / kblocks, kb = c - (c / kblocks) * kblocks;
     int32_t pr[4];   // tokens of rows lane + 32 i of this block
 #pragma unroll
     for (int i = 0; i < 4; ++i) pr[i] = perm[b * R + lane + 32 * i];
+    uint4 sv[4];     // scale words 0..3 of this K block for rows lane + 32 i
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      sv[i] = pr[i] >= 0 ? *reinterpret_cast<const uint4*>(src_sf + (int64_t)pr[i] * sf_row + kb * 16)
+                         : make_uint4(0u, 0u, 0u, 0u);
     if (lane == 0) bulk_wait_read<0>();   // the previous chunk's store has read the buffer
     __syncwarp();
-    // codes: row rr's 16-byte chunk j, re-swizzled for the destination row
+    // codes: row rr's 16-byte chunk j, swizzled for the destination row
 #pragma unroll
     for (int p = 0; p < 32; ++p) {
       const int rr = 4 * p + (lane >> 3), j = lane & 7;
       const int32_t t = __shfl_sync(0xFFFFFFFFu, pr[p >> 3], rr & 31);
       const uint32_t d = sb + rr * 128 + ((j ^ (rr & 7)) << 4);
       if (t >= 0) {
-        const int ts = t & (R - 1);
-        cp_async_16(d, src + ((int64_t)(t / R) * kblocks + kb) * kChunk + ts * 128 + ((j ^ (ts & 7)) << 4));
+        cp_async_16(d, src + (int64_t)t * code_row + kb * 128 + j * 16);
       } else {
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
       }
     }
-    // scales: the chunk's 512 words, each moved to the destination row's position
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-      const int wi = 32 * p + lane, rr = wi >> 2, q = wi & 3;
-      const int32_t t = __shfl_sync(0xFFFFFFFFu, pr[p >> 2], rr & 31);
-      const uint32_t d = sb + R * 128 + q * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
-      if (t >= 0) {
-        const int ts = t & (R - 1);
-        cp_async_4(d, src + ((int64_t)(t / R) * kblocks + kb) * kChunk + R * 128 + q * 512 + (ts & 31) * 16 +
-                          (ts >> 5) * 4);
-      } else {
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(d), "r"(0u) : "memory");
-      }
+    // scales: word q of row rr sits at q * 512 + (rr & 31) * 16 + (rr >> 5) * 4, so the
+    // four rows of a lane fill one 16-byte slot per word
+    {
+      const uint32_t d = sb + R * 128 + lane * 16;
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(sv[0].x), "r"(sv[1].x), "r"(sv[2].x),
+                   "r"(sv[3].x)
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + 512), "r"(sv[0].y), "r"(sv[1].y),
+                   "r"(sv[2].y), "r"(sv[3].y)
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + 1024), "r"(sv[0].z), "r"(sv[1].z),
+                   "r"(sv[2].z), "r"(sv[3].z)
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + 1536), "r"(sv[0].w), "r"(sv[1].w),
+                   "r"(sv[2].w), "r"(sv[3].w)
+                   : "memory");
     }
     cp_async_wait_all();
     fence_proxy_async_smem();
@@ -113,9 +124,9 @@ __global__ void __launch_bounds__(32) gather_tiled_kernel(const uint8_t* __restr
   __syncwarp();
 }
 
-cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const int32_t* perm, const int32_t* n_rows_dev,
-                                int64_t max_rows, int64_t K, uint8_t* dst, float* dst_g, uint32_t* amax_zero,
-                                cudaStream_t s) {
+cudaError_t launch_gather_tiled(const uint8_t* src, const uint8_t* src_sf, const float* src_g, const int32_t* perm,
+                                const int32_t* n_rows_dev, int64_t max_rows, int64_t K, uint8_t* dst, float* dst_g,
+                                uint32_t* amax_zero, cudaStream_t s) {
   constexpr int kSmem = 128 * 144;
   const int64_t chunks = max_rows / 128 * (K / 256);
   if (chunks == 0) return cudaSuccess;
@@ -127,8 +138,8 @@ cudaError_t launch_gather_tiled(const uint8_t* src, const float* src_g, const in
   // one warp per block and one 18 KB chunk image per warp: 12 per SM fit in shared memory
   int64_t blocks = chunks;
   if (blocks > 12 * (int64_t)num_sms()) blocks = 12 * (int64_t)num_sms();
-  return launch_pdl(false, gather_tiled_kernel, dim3((unsigned)blocks), dim3(32), kSmem, s, src, src_g, perm, n_rows_dev,
-                    max_rows, K / 256, dst, dst_g, amax_zero);
+  return launch_pdl(false, gather_tiled_kernel, dim3((unsigned)blocks), dim3(32), kSmem, s, src, src_sf, src_g, perm,
+                    n_rows_dev, max_rows, K / 256, dst, dst_g, amax_zero);
 }
 
 // out[b*C + c, r] = x[b*R + r, c] for `batches` stacked [R, C] BF16 matrices (pitch ld):
