@@ -348,7 +348,9 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   a.seed = seed;
   a.rng_offset = rng_offset;
   a.status = device_status_ptr();
-  return from_cuda(launch_quantize_rows(a, rounding, s));
+  // after an amax pass the encode is its programmatic dependent (its launch overlaps the
+  // pass's tail)
+  return from_cuda(launch_quantize_rows(a, rounding, s, amax != nullptr));
 }
 
 nvfp4_status nvfp4_quantize_transposed(const void* x, int64_t batches, int64_t R, int64_t C, int64_t ld,

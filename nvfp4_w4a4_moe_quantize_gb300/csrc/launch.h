@@ -83,7 +83,9 @@ inline cudaError_t set_smem_attr_once(std::atomic<bool>* flags, const void* func
 
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t group_rows,
                         uint32_t* amax_bits, int64_t n_scopes, cudaStream_t s);
-cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s);
+// pdl: launched as a programmatic dependent of the kernel before it on the stream (the
+// encode kernels wait for that grid's completion before reading anything it wrote).
+cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s, bool pdl = false);
 
 // Grouped GEMM: tensor maps are built by the caller (api.cu), all with 128-row boxes.
 // The 128 x 256 tile kernel serves N % 256 == 0 and E <= 512; the 128 x 128

@@ -107,11 +107,20 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // ------------------------------------------------------------------ amax of each scope
 
+// Zeroes the n scope words before an amax pass (a kernel rather than a memset, so that the
+// amax kernel can be launched as its programmatic dependent).
+__global__ void __launch_bounds__(256) zero_words_kernel(uint32_t* p, int64_t n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = 0u;
+}
+
 // Max |x| over the tensor (group_rows == 0) or over each group of group_rows rows.
 // Results are float bit patterns combined with atomicMax, which for non-negative floats
 // is the float maximum whatever the order: deterministic.
 __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols,
                                                    int64_t ld, int64_t group_rows, uint32_t* amax_bits) {
+  grid_dep_sync();   // the scope words have been zeroed
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t nwarp = (int64_t)gridDim.x * 8;
@@ -150,9 +159,13 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
 
 // Max |x| of a contiguous tensor seen as n16 16-byte chunks: eight independent loads in
 // flight per thread (up to 2048 threads per SM: ~256 KB in flight), one atomicMax per
-// block.
+// block.  Launched as a programmatic dependent of the kernel that zeroes the result word:
+// the loads and the block's reduction overlap that kernel, and only the atomic waits for
+// it; the encode kernel after it may be scheduled as soon as this grid is placed (every
+// block fits at once) and waits for its completion before reading the result.
 __global__ void __launch_bounds__(256) amax_flat_kernel(const uint4* __restrict__ x, int64_t n16,
                                                         uint32_t* amax_bits) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kU = 8;
   float m = 0.0f;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -181,6 +194,7 @@ __global__ void __launch_bounds__(256) amax_flat_kernel(const uint4* __restrict_
   if (threadIdx.x == 0) {
     float b = sm[0];
     for (int k = 1; k < 8; ++k) b = fmaxf(b, sm[k]);
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the result word has been zeroed
     if (b > 0.0f) atomicMax(&amax_bits[0], __float_as_uint(b));
   }
 }
@@ -275,6 +289,7 @@ __device__ __forceinline__ void zero_pad_rows(const QuantArgs& a, int64_t warp, 
 // registers.
 template <int RND, int MAXC>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(QuantArgs a) {
+  grid_dep_sync();   // (programmatic launch after the amax pass: its result is visible)
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t nwarp = (int64_t)gridDim.x * 8;
@@ -339,6 +354,7 @@ __device__ __forceinline__ void encode_regs(const QuantArgs& a, int64_t row, int
 // of rows .. rows_total-1.
 template <int RND>
 __global__ void __launch_bounds__(256) quantize_known_scale_kernel(QuantArgs a) {
+  grid_dep_sync();
   const int64_t words = a.sf_words, nb = a.cols / 16, nb_pad = a.cols_pad / 16;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t s_row = stride / words, s_w = stride - s_row * words;
@@ -392,6 +408,7 @@ __global__ void __launch_bounds__(256) quantize_known_scale_kernel(QuantArgs a) 
 // fits).
 template <int RND, typename Idx>
 __global__ void __launch_bounds__(256) quantize_known_coalesced_kernel(QuantArgs a) {
+  grid_dep_sync();
   constexpr int kSlabs = 2;
   const int lane = threadIdx.x & 31;
   const Idx bpr = (Idx)(a.cols / 16);
@@ -672,49 +689,52 @@ cudaError_t launch_requant_tiled(const __nv_bfloat16* h, const uint32_t* amax_bi
 }
 
 template <int RND>
-static cudaError_t launch_quant_rnd(const QuantArgs& a, int maxc, int grid, cudaStream_t s) {
+static cudaError_t launch_quant_rnd(const QuantArgs& a, int maxc, int grid, cudaStream_t s, bool pdl) {
+  const dim3 g((unsigned)grid), b(256);
   switch (maxc) {
-    case 1: quantize_rows_kernel<RND, 1><<<grid, 256, 0, s>>>(a); break;
-    case 2: quantize_rows_kernel<RND, 2><<<grid, 256, 0, s>>>(a); break;
-    case 4: quantize_rows_kernel<RND, 4><<<grid, 256, 0, s>>>(a); break;
-    case 8: quantize_rows_kernel<RND, 8><<<grid, 256, 0, s>>>(a); break;
-    case 16: quantize_rows_kernel<RND, 16><<<grid, 256, 0, s>>>(a); break;
-    default: quantize_rows_kernel<RND, 32><<<grid, 256, 0, s>>>(a); break;
+    case 1: return launch_pdl(pdl, quantize_rows_kernel<RND, 1>, g, b, 0, s, a);
+    case 2: return launch_pdl(pdl, quantize_rows_kernel<RND, 2>, g, b, 0, s, a);
+    case 4: return launch_pdl(pdl, quantize_rows_kernel<RND, 4>, g, b, 0, s, a);
+    case 8: return launch_pdl(pdl, quantize_rows_kernel<RND, 8>, g, b, 0, s, a);
+    case 16: return launch_pdl(pdl, quantize_rows_kernel<RND, 16>, g, b, 0, s, a);
+    default: return launch_pdl(pdl, quantize_rows_kernel<RND, 32>, g, b, 0, s, a);
   }
-  return cudaGetLastError();
 }
 
 template <int RND>
-static cudaError_t launch_stream(const QuantArgs& a, int grid, size_t smem, cudaStream_t s) {
+static cudaError_t launch_stream(const QuantArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
   static std::atomic<bool> attr_set[64];   // the attribute is set once per device
   {
     const cudaError_t err = set_smem_attr_once(attr_set, (const void*)quantize_rows_stream_kernel<RND>, (int)kQSmemMax + 4096);
     if (err != cudaSuccess) return err;
   }
-  return launch_pdl(false, quantize_rows_stream_kernel<RND>, dim3((unsigned)grid), dim3(kQWarps * 32), smem, s, a);
+  return launch_pdl(pdl, quantize_rows_stream_kernel<RND>, dim3((unsigned)grid), dim3(kQWarps * 32), smem, s, a);
 }
 
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t group_rows,
                         uint32_t* amax_bits, int64_t n_scopes, cudaStream_t s) {
-  cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t) * n_scopes, s);
-  if (err != cudaSuccess) return err;
+  if (n_scopes > 0) {
+    int64_t zb = (n_scopes + 255) / 256;
+    if (zb > 4 * (int64_t)num_sms()) zb = 4 * (int64_t)num_sms();
+    const cudaError_t err = launch_pdl(false, zero_words_kernel, dim3((unsigned)zb), dim3(256), 0, s, amax_bits, n_scopes);
+    if (err != cudaSuccess) return err;
+  }
   if (rows == 0) return cudaSuccess;
   const int sms = num_sms();
   if (group_rows == 0 && ld == cols) {   // one scope over contiguous rows: flat pass
     const int64_t n16 = rows * cols / 8;
     int64_t blocks = (n16 + 255) / 256;
     if (blocks > 8 * sms) blocks = 8 * sms;
-    amax_flat_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(x), n16, amax_bits);
-    return cudaGetLastError();
+    return launch_pdl(true, amax_flat_kernel, dim3((unsigned)blocks), dim3(256), 0, s, static_cast<const uint4*>(x), n16,
+                      amax_bits);
   }
   int64_t blocks = (rows + 7) / 8;
   if (blocks > 4 * sms) blocks = 4 * sms;
-  amax_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, group_rows,
-                                          amax_bits);
-  return cudaGetLastError();
+  return launch_pdl(true, amax_kernel, dim3((unsigned)blocks), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(x),
+                    rows, cols, ld, group_rows, amax_bits);
 }
 
-cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s) {
+cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t s, bool pdl) {
   if (a.rows_total == 0) return cudaSuccess;
   int maxc = 1;
   while (maxc * 256 < a.cols) maxc *= 2;
@@ -733,22 +753,19 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
       if (nb > 8 * (int64_t)sms) nb = 8 * (int64_t)sms;   // 8 CTAs of 8 warps per SM, several iterations each
       if (nb < 1) nb = 1;
       const bool i32 = units + 128 < ((int64_t)1 << 32);
-      if (rounding == kRoundSR) {
-        if (i32) quantize_known_coalesced_kernel<kRoundSR, uint32_t><<<(int)nb, 256, 0, s>>>(a);
-        else quantize_known_coalesced_kernel<kRoundSR, int64_t><<<(int)nb, 256, 0, s>>>(a);
-      } else {
-        if (i32) quantize_known_coalesced_kernel<kRoundRNE, uint32_t><<<(int)nb, 256, 0, s>>>(a);
-        else quantize_known_coalesced_kernel<kRoundRNE, int64_t><<<(int)nb, 256, 0, s>>>(a);
-      }
-      return cudaGetLastError();
+      const dim3 g((unsigned)nb), b(256);
+      if (rounding == kRoundSR)
+        return i32 ? launch_pdl(pdl, quantize_known_coalesced_kernel<kRoundSR, uint32_t>, g, b, 0, s, a)
+                   : launch_pdl(pdl, quantize_known_coalesced_kernel<kRoundSR, int64_t>, g, b, 0, s, a);
+      return i32 ? launch_pdl(pdl, quantize_known_coalesced_kernel<kRoundRNE, uint32_t>, g, b, 0, s, a)
+                 : launch_pdl(pdl, quantize_known_coalesced_kernel<kRoundRNE, int64_t>, g, b, 0, s, a);
     }
     const int64_t total = (a.rows > a.rows_total - a.rows ? a.rows : a.rows_total - a.rows) * a.sf_words;
     int64_t nb = (total + 255) / 256;
     if (nb > 8 * (int64_t)sms) nb = 8 * (int64_t)sms;
     if (nb < 1) nb = 1;
-    if (rounding == kRoundSR) quantize_known_scale_kernel<kRoundSR><<<(int)nb, 256, 0, s>>>(a);
-    else quantize_known_scale_kernel<kRoundRNE><<<(int)nb, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return rounding == kRoundSR ? launch_pdl(pdl, quantize_known_scale_kernel<kRoundSR>, dim3((unsigned)nb), dim3(256), 0, s, a)
+                                : launch_pdl(pdl, quantize_known_scale_kernel<kRoundRNE>, dim3((unsigned)nb), dim3(256), 0, s, a);
   }
   if (!stream_ok && (a.tiled_R != 0 || a.row_filter != nullptr || a.rows_dev != nullptr)) return cudaErrorInvalidValue;
   if (stream_ok) {
@@ -774,13 +791,13 @@ cudaError_t launch_quantize_rows(const QuantArgs& a, int rounding, cudaStream_t 
       blocks_per_sm = resident;
     int64_t nb = (a.rows_total + kQWarps - 1) / kQWarps;
     if (nb > (int64_t)blocks_per_sm * sms) nb = (int64_t)blocks_per_sm * sms;
-    return rounding == kRoundSR ? launch_stream<kRoundSR>(b, (int)nb, smem, s)
-                                : launch_stream<kRoundRNE>(b, (int)nb, smem, s);
+    return rounding == kRoundSR ? launch_stream<kRoundSR>(b, (int)nb, smem, s, pdl)
+                                : launch_stream<kRoundRNE>(b, (int)nb, smem, s, pdl);
   }
   const int64_t cap = (int64_t)(maxc <= 8 ? 8 : 4) * sms;
   if (blocks > cap) blocks = cap;
-  return rounding == kRoundSR ? launch_quant_rnd<kRoundSR>(a, maxc, (int)blocks, s)
-                              : launch_quant_rnd<kRoundRNE>(a, maxc, (int)blocks, s);
+  return rounding == kRoundSR ? launch_quant_rnd<kRoundSR>(a, maxc, (int)blocks, s, pdl)
+                              : launch_quant_rnd<kRoundRNE>(a, maxc, (int)blocks, s, pdl);
 }
 
 }  // namespace nvfp4
