@@ -157,6 +157,23 @@ def time_launches(fn, iters, flush, stream):
     return float(np.mean(ts)), float(np.median(ts))
 
 
+def capture_graph(fn):
+    """fn()'s launches captured once in a CUDA graph (after a warm-up call on a side
+    stream, as torch asks before a capture)."""
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def time_launches_median(fn, iters, flush, stream):
     """Median device time (ms) of fn() over iters launches, L2 flushed before each: the
     per-kernel figures (standalone quantisers, grouped GEMMs) are medians."""
@@ -476,6 +493,8 @@ def run_ours(args, rank, world, local_rank):
     decode = {"timing": f"median of {iters} launches, L2 flushed before each",
               "us_clean_l2": "the same launches after a flush whose 256 MB write is followed by a 256 MB read, "
                              "so that the flush's dirty lines are not written back inside the timed launch",
+              "us_graph": "the same launches captured once in a CUDA graph and replayed (the flush, a write, "
+                          "outside the graph before each replay)",
               "batches": []}
     w13_e = L.nvfp4_tiled_bytes(2 * I, H, 256) + 4
     w2_e = L.nvfp4_tiled_bytes(H, pw.Ip, 256) + 4
@@ -492,10 +511,14 @@ def run_ours(args, rank, world, local_rank):
             L.moe_expert_forward(dx_, dids, dwts, pw, out=dout_, workspace=dws)
         dtime = time_launches_median(dstep, iters, flush, stream)
         dtime_clean = time_launches_median(dstep, iters, flush_clean, stream)
+        dgraph = capture_graph(dstep)
+        dtime_graph = time_launches_median(dgraph.replay, iters, flush, stream)
+        del dgraph
         active = int(torch.unique(dids).numel())
         dbytes = active * (w13_e + w2_e) + dt * H * 2 * 2 + dt * E * 4
         decode["batches"].append({"tokens": dt, "active_experts": active, "us": round(dtime * 1e3, 2),
                                   "us_clean_l2": round(dtime_clean * 1e3, 2),
+                                  "us_graph": round(dtime_graph * 1e3, 2),
                                   "tokens_per_s": round(dt / (dtime * 1e-3), 1),
                                   "weight_bytes_read": active * (w13_e + w2_e),
                                   "gbs": round(dbytes / (dtime * 1e-3) / 1e9, 1),
