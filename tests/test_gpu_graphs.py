@@ -36,12 +36,13 @@ def moe_setup(cuda_lib):
     x_h, logits_h, w13_h, w2_h = S.moe_inputs(shape, seed=5)
     dev = torch.device("cuda", 0)
     pw = L.moe_prepare_weights(w13_h.to(dev), w2_h.to(dev))
-    return L, shape, x_h, logits_h, pw, dev
+    pt = L.moe_prepare_weights_backward(w13_h.to(dev), w2_h.to(dev))
+    return L, shape, x_h, logits_h, pw, pt, dev
 
 
 @pytest.mark.parametrize("T", [8, 2048])   # decode-size path (T*k <= 1024) and the large path
 def test_forward_replays_in_a_cuda_graph(moe_setup, T):
-    L, shape, x_h, logits_h, pw, dev = moe_setup
+    L, shape, x_h, logits_h, pw, _, dev = moe_setup
     k, H = shape.k, shape.H
     x = x_h[:T].contiguous().to(dev)
     logits = logits_h[:T].contiguous().to(dev)
@@ -75,6 +76,53 @@ def test_forward_replays_in_a_cuda_graph(moe_setup, T):
     assert torch.equal(got_ids, ids) and torch.equal(got_w, w)
     assert torch.equal(got_out.view(torch.int16), out.view(torch.int16))
     assert not torch.equal(got_out.view(torch.int16), ref_out.view(torch.int16))
+    assert L.nvfp4_status_check() == 0
+
+
+def test_learner_step_replays_in_a_cuda_graph(moe_setup):
+    """Routing, the forward and the W4A4 backward (stochastic rounding, fixed seed) of a
+    1024-token batch as one graph."""
+    L, shape, x_h, logits_h, pw, pt, dev = moe_setup
+    T, k, H = 1024, shape.k, shape.H
+    x = x_h[:T].contiguous().to(dev)
+    logits = logits_h[:T].contiguous().to(dev)
+    dout = S.randn_bf16((T, H), 1e-3, seed=9).to(dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    fws = L.moe_forward_workspace(T, k, pw, dev)
+    bws = L.moe_backward_workspace(T, k, pw, dev)
+    grads = (torch.empty(T, H, dtype=torch.bfloat16, device=dev), torch.empty(T, k, dtype=torch.float32, device=dev),
+             torch.empty(pw.E, 2 * pw.I, H, dtype=torch.float32, device=dev),
+             torch.empty(pw.E, H, pw.I, dtype=torch.float32, device=dev))
+
+    def step():
+        L.moe_route_topk(logits, k, True, out=(ids, w))
+        L.moe_expert_forward(x, ids, w, pw, out=out, workspace=fws)
+        L.moe_expert_backward(dout, x, w, pw, pt, fws, seed=21, out=grads, workspace=bws)
+
+    def bits(t):
+        return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+    step()
+    torch.cuda.synchronize()
+    ref = [bits(t).clone() for t in (out,) + grads]
+    g = _capture(step)
+    for t in grads:
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip([bits(t) for t in (out,) + grads], ref):
+        assert torch.equal(a, b)
+    dout.copy_(S.randn_bf16((T, H), 1e-3, seed=10).to(dev))
+    g.replay()
+    torch.cuda.synchronize()
+    got = [bits(t).clone() for t in (out,) + grads]
+    step()
+    torch.cuda.synchronize()
+    for a, b in zip(got, [bits(t) for t in (out,) + grads]):
+        assert torch.equal(a, b)
+    assert not torch.equal(got[1], ref[1])   # dx follows the new gradient
     assert L.nvfp4_status_check() == 0
 
 
